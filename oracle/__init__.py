@@ -1,0 +1,183 @@
+"""CPU oracle of the error-bounded embedding codec (ctypes wrapper).
+
+TEST INFRASTRUCTURE ONLY.  The test suite, ``__graft_entry__.smoke()`` and
+``bench.py``'s CPU-baseline leg are the only importers.  The product library
+never imports, links or executes anything here, and the oracle shares no code
+with it: ``ebc_oracle.c`` re-implements the container format from its
+specification.
+
+Method: "Accelerating Communication in Deep Learning Recommendation Model
+Training with Dual-Level Adaptive Lossy Compression" (arXiv 2407.04272),
+sections III-C (error-bound schedule), III-D (quantization encoder,
+vector-based LZ, Huffman) and III-E (single-buffer layout).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "ebc_oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_SO = os.path.join(_BUILD, "libebc_oracle.so")
+_LOCK = threading.Lock()
+_LIB = None
+
+OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT = 0, 1, 2, 3
+DECAY = {"none": 0, "linear": 1, "stepwise": 2, "drop": 3, "log": 4}
+LMAX = 24
+RADIUS = 128
+
+
+class Info(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in
+                ("n_literal", "n_match", "n_outlier", "n_chunks", "bitstream_bytes", "total_bytes")]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (no FMA contraction); returns the .so path."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+        tmp = _SO + f".{os.getpid()}.tmp"
+        subprocess.check_call(["gcc", "-O2", "-std=c99", "-ffp-contract=off", "-fPIC", "-shared",
+                               "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _SO)
+    return _SO
+
+
+def _lib():
+    global _LIB
+    with _LOCK:
+        if _LIB is None:
+            lib = ctypes.CDLL(build())
+            P, I64, U64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_uint64, ctypes.c_int
+            lib.ebo_quantize.argtypes = [P, I64, ctypes.c_float, P]
+            lib.ebo_quantize.restype = I64
+            lib.ebo_dequantize.argtypes = [I, ctypes.c_float]
+            lib.ebo_dequantize.restype = ctypes.c_float
+            lib.ebo_vector_hash.argtypes = [P, P, I]
+            lib.ebo_vector_hash.restype = ctypes.c_uint32
+            lib.ebo_huffman_lengths.argtypes = [P, I, P]
+            lib.ebo_huffman_lengths.restype = I
+            lib.ebo_canonical_codes.argtypes = [P, I, P]
+            lib.ebo_canonical_codes.restype = I
+            lib.ebo_decay_factor.argtypes = [I, I64, ctypes.c_double, I64, I]
+            lib.ebo_decay_factor.restype = ctypes.c_double
+            lib.ebo_compress_bound.argtypes = [I64, I, I]
+            lib.ebo_compress_bound.restype = U64
+            lib.ebo_compress.argtypes = [P, I64, I, I, P, P, U64, ctypes.POINTER(Info), P, P, P]
+            lib.ebo_compress.restype = I
+            lib.ebo_decompress.argtypes = [P, U64, I64, I, I, P, P]
+            lib.ebo_decompress.restype = I
+            _LIB = lib
+    return _LIB
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def quantize(x, eb: float) -> np.ndarray:
+    """Quantization codes (uint8; 0 = outlier) of a float32 array under bound eb."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    sym = np.empty(x.shape, dtype=np.uint8)
+    r = _lib().ebo_quantize(_ptr(x), x.size, float(eb), _ptr(sym))
+    if r < 0:
+        raise ValueError("invalid error bound")
+    return sym
+
+
+def dequantize(sym: int, eb: float) -> float:
+    return float(_lib().ebo_dequantize(int(sym), float(eb)))
+
+
+def vector_hash(sym_row, x_row) -> int:
+    s = np.ascontiguousarray(sym_row, dtype=np.uint8)
+    x = np.ascontiguousarray(x_row, dtype=np.float32)
+    return int(_lib().ebo_vector_hash(_ptr(s), _ptr(x), s.size))
+
+
+def huffman_lengths(freq, lmax: int = LMAX):
+    """(lengths uint8[256], halving rounds) of the two-queue Huffman code."""
+    f = np.zeros(256, dtype=np.uint64)
+    freq = np.asarray(freq, dtype=np.uint64)
+    f[: freq.size] = freq
+    ln = np.zeros(256, dtype=np.uint8)
+    rounds = _lib().ebo_huffman_lengths(_ptr(f), int(lmax), _ptr(ln))
+    if rounds < 0:
+        raise ValueError("bad arguments")
+    return ln, rounds
+
+
+def canonical_codes(lens, lmax: int = LMAX) -> np.ndarray:
+    ln = np.ascontiguousarray(lens, dtype=np.uint8)
+    code = np.zeros(256, dtype=np.uint32)
+    if _lib().ebo_canonical_codes(_ptr(ln), int(lmax), _ptr(code)) < 0:
+        raise ValueError("lengths violate the Kraft inequality")
+    return code
+
+
+def decay_factor(fn, iteration: int, m0: float, phase_len: int, n_steps: int = 1) -> float:
+    fn = DECAY[fn] if isinstance(fn, str) else int(fn)
+    return float(_lib().ebo_decay_factor(fn, int(iteration), float(m0), int(phase_len), int(n_steps)))
+
+
+def scheduled_bounds(eb_base, fn, iteration, m0, phase_len, n_steps=1) -> np.ndarray:
+    """eb_t(i) = fl32(base_t * factor(i)), factor in double."""
+    f = decay_factor(fn, iteration, m0, phase_len, n_steps)
+    base = np.asarray(eb_base, dtype=np.float32).astype(np.float64)
+    return (base * f).astype(np.float32)
+
+
+def compress_bound(B: int, T: int, D: int) -> int:
+    return int(_lib().ebo_compress_bound(int(B), int(T), int(D)))
+
+
+def compress(x, eb, *, want_internals: bool = False):
+    """Compress x [B,T,D] float32 with per-table bounds eb [T].
+
+    Returns (container uint8 array, info dict) and, with want_internals,
+    also (sym [T,B,D] uint8, ref [T,B] uint32, lens [T,256] uint8)."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    B, T, D = x.shape
+    eb = np.ascontiguousarray(eb, dtype=np.float32)
+    assert eb.shape == (T,)
+    cap = compress_bound(B, T, D)
+    if cap == 0 and B * T * D > 0:
+        raise ValueError("unsupported shape")
+    out = np.zeros(max(cap, 16), dtype=np.uint8)
+    info = Info()
+    sym = np.empty((T, B, D), dtype=np.uint8) if want_internals else None
+    ref = np.empty((T, B), dtype=np.uint32) if want_internals else None
+    lens = np.empty((T, 256), dtype=np.uint8) if want_internals else None
+    rc = _lib().ebo_compress(_ptr(x), B, T, D, _ptr(eb), _ptr(out), out.size, ctypes.byref(info),
+                             _ptr(sym) if sym is not None else None,
+                             _ptr(ref) if ref is not None else None,
+                             _ptr(lens) if lens is not None else None)
+    if rc != OK:
+        raise RuntimeError(f"oracle compress failed: {rc}")
+    d = {k: int(getattr(info, k)) for k, _ in Info._fields_}
+    buf = out[: d["total_bytes"]].copy()
+    if want_internals:
+        return buf, d, sym, ref, lens
+    return buf, d
+
+
+def decompress_rc(buf, B: int, T: int, D: int):
+    """(return code, xhat [B,T,D], sym [T,B,D]) without raising."""
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    xhat = np.zeros((B, T, D), dtype=np.float32)
+    sym = np.zeros((T, B, D), dtype=np.uint8)
+    rc = _lib().ebo_decompress(_ptr(buf), buf.size, int(B), int(T), int(D), _ptr(xhat), _ptr(sym))
+    return rc, xhat, sym
+
+
+def decompress(buf, B: int, T: int, D: int):
+    rc, xhat, sym = decompress_rc(buf, B, T, D)
+    if rc != OK:
+        raise RuntimeError(f"oracle decompress failed: {rc}")
+    return xhat, sym

@@ -1,0 +1,615 @@
+/*
+ * ebc_oracle.c -- plain, slow, single-threaded CPU oracle of the
+ * error-bounded embedding codec.
+ *
+ * TEST INFRASTRUCTURE ONLY: the test suite, the smoke check and the
+ * benchmark's CPU-baseline leg are its only users.  The product path (the CUDA
+ * library) never links or calls it, and the two share no source.
+ *
+ * Method source: "Accelerating Communication in Deep Learning Recommendation
+ * Model Training with Dual-Level Adaptive Lossy Compression" (arXiv
+ * 2407.04272v5), cited as [DLRM-EBLC].  The pages give the pipeline
+ * (quantization encoder -> vector-based LZ -> Huffman, §III-D), the table-wise
+ * and iteration-wise error bounds (§III-C, §IV-B) and the single-buffer
+ * layout (§III-E, Fig. 7), but no formulas or formats; every step the pages
+ * leave open is fixed here as a "reading" and written the same way in the
+ * library's header comments.
+ *
+ * Build: gcc -O2 -std=c99 -ffp-contract=off -fPIC -shared (no FMA
+ * contraction, so every float operation below rounds once, as written).
+ */
+#include "ebc_oracle.h"
+
+#include <float.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---- format constants (the container specification, version 1) ---- */
+#define O_RADIUS 128            /* bins q in (-R, R); sym = q + R          */
+#define O_LMAX 24               /* longest Huffman code                    */
+#define O_MAGIC 0x31434245u     /* bytes 'E' 'B' 'C' '1'                   */
+#define O_VERSION 1u
+#define O_HEADER 144u
+#define O_TABLE_REC 272u        /* eb, n_lit, n_match, n_out, 256 lengths  */
+#define O_SEG_REC 16u           /* word_off, chunk_base, match_base, out_base */
+#define O_MAX_T 1024
+
+static uint64_t pad16(uint64_t n) { return (n + 15u) & ~(uint64_t)15u; }
+static int dim_ok(int D) { return D >= 4 && D <= 512 && (D & (D - 1)) == 0; }
+/* Segment = run of consecutive batch rows of one table, padded to 128 bits in
+ * the stream; about 8192 codes, and a whole number of 32-row bitmap words. */
+static int64_t seg_rows(int D) { int64_t s = 8192 / D; return s < 32 ? 32 : s; }
+/* Chunk = run of literal vectors of one segment decoded by one thread:
+ * max(128, D) codes. */
+static int64_t chunk_rows(int D) { int64_t k = 128 / D; return k < 1 ? 1 : k; }
+
+static void wr16(uint8_t* p, uint32_t v) { p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); }
+static void wr32(uint8_t* p, uint32_t v) {
+  p[0] = (uint8_t)v; p[1] = (uint8_t)(v >> 8); p[2] = (uint8_t)(v >> 16); p[3] = (uint8_t)(v >> 24);
+}
+static void wr64(uint8_t* p, uint64_t v) { wr32(p, (uint32_t)v); wr32(p + 4, (uint32_t)(v >> 32)); }
+static uint32_t rd16(const uint8_t* p) { return (uint32_t)p[0] | ((uint32_t)p[1] << 8); }
+static uint32_t rd32(const uint8_t* p) {
+  return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+static uint64_t rd64(const uint8_t* p) { return (uint64_t)rd32(p) | ((uint64_t)rd32(p + 4) << 32); }
+static uint32_t f2u(float f) { uint32_t u; memcpy(&u, &f, 4); return u; }
+static float u2f(uint32_t u) { float f; memcpy(&f, &u, 4); return f; }
+
+/* An absolute bound is usable when eb and 2*eb are finite normal numbers and
+ * the reciprocal 1/(2*eb) is a normal number too. */
+static int eb_ok(float eb) {
+  if (!(eb >= FLT_MIN) || !(eb <= FLT_MAX)) return 0;
+  float ebx2 = 2.0f * eb;
+  if (!(ebx2 <= FLT_MAX)) return 0;
+  float inv = 1.0f / ebx2;
+  return inv >= FLT_MIN;
+}
+
+/* ------------------------------------------------------------------------
+ * Quantization encoder, [DLRM-EBLC] §III-D: each float becomes an integer bin
+ * under the absolute bound eb.  The pages reject prediction for embedding
+ * vectors (§III-B observation 1 and §III-D "Optimized Entropy Encoding", the
+ * Lorenzo "false prediction" of Fig. 4), so the prediction is zero:
+ *     q = round_half_even(x / (2 eb)),   xhat = q * 2 eb.
+ * Reading: the division is a multiplication by the fp32 reciprocal of 2 eb,
+ * and a bin is accepted only if |x - xhat| <= eb holds in fp32 and |q| < R;
+ * otherwise the element is an outlier (sym 0) and its raw bits are kept.
+ * ---------------------------------------------------------------------- */
+static int quantize_one(float x, float eb, float ebx2, float inv) {
+  float t = x * inv;
+  if (isnan(t) || fabsf(t) >= 1073741824.0f) return 0;
+  float qf = nearbyintf(t);                 /* default mode: ties to even */
+  int q = (int)qf;
+  if (q <= -O_RADIUS || q >= O_RADIUS) return 0;
+  float xhat = (float)q * ebx2;
+  float err = fabsf(x - xhat);
+  if (!(err <= eb)) return 0;
+  return q + O_RADIUS;
+}
+
+int64_t ebo_quantize(const float* x, int64_t n, float eb, uint8_t* sym) {
+  if (!eb_ok(eb) || n < 0) return -1;
+  float ebx2 = 2.0f * eb, inv = 1.0f / ebx2;
+  int64_t outl = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    sym[i] = (uint8_t)quantize_one(x[i], eb, ebx2, inv);
+    if (sym[i] == 0) ++outl;
+  }
+  return outl;
+}
+
+float ebo_dequantize(int sym, float eb) {
+  float ebx2 = 2.0f * eb;
+  return (float)(sym - O_RADIUS) * ebx2;
+}
+
+/* ------------------------------------------------------------------------
+ * Dedup key for the vector-based LZ encoder ([DLRM-EBLC] §III-D "Vector-based
+ * LZ Encoding", §III-E "fixed pattern length"): the pattern is one whole
+ * quantized embedding vector.  Reading: a 32-bit hash, the wrapping sum over
+ * 4-code words w_k of lowbias32(w_k + k*0x9E3779B9) plus, for each outlier at
+ * position d, lowbias32(raw_d ^ (d+1)*0x85EBCA6B).  lowbias32 is C. Wellons'
+ * published 32-bit integer mixer (xor-shift 16, multiply 0x7feb352d,
+ * xor-shift 15, multiply 0x846ca68b, xor-shift 16).
+ * ---------------------------------------------------------------------- */
+static uint32_t lowbias32(uint32_t v) {
+  v ^= v >> 16;
+  v *= 0x7feb352dU;
+  v ^= v >> 15;
+  v *= 0x846ca68bU;
+  v ^= v >> 16;
+  return v;
+}
+
+uint32_t ebo_vector_hash(const uint8_t* sym, const float* x_row, int D) {
+  uint32_t h = 0;
+  for (int k = 0; k < D / 4; ++k) {
+    uint32_t w = (uint32_t)sym[4 * k] | ((uint32_t)sym[4 * k + 1] << 8) |
+                 ((uint32_t)sym[4 * k + 2] << 16) | ((uint32_t)sym[4 * k + 3] << 24);
+    h += lowbias32(w + (uint32_t)k * 0x9E3779B9u);
+  }
+  for (int d = 0; d < D; ++d)
+    if (sym[d] == 0) h += lowbias32(f2u(x_row[d]) ^ ((uint32_t)(d + 1) * 0x85EBCA6Bu));
+  return h;
+}
+
+/* ------------------------------------------------------------------------
+ * Huffman code lengths, [DLRM-EBLC] §III-D "Optimized Entropy Encoding"
+ * (Huffman's minimum-redundancy code).  Reading, since the pages give no
+ * tie rule: symbols with f > 0 sorted by (f, sym) ascending form the leaf
+ * queue; merged nodes go to a FIFO queue; each pick takes the smaller front
+ * and a tie goes to the leaf.  A single used symbol gets length 1.  If the
+ * longest code exceeds lmax, every nonzero f becomes max(1, f >> 1) and the
+ * code is rebuilt.
+ * ---------------------------------------------------------------------- */
+static int two_queue_lengths(const uint64_t* f, uint8_t* len) {
+  int order[256], n = 0;
+  memset(len, 0, 256);
+  for (int s = 0; s < 256; ++s)
+    if (f[s] > 0) {
+      /* insertion keeps (f, sym) order: equal f stay in sym order */
+      int j = n++;
+      while (j > 0 && f[order[j - 1]] > f[s]) { order[j] = order[j - 1]; --j; }
+      order[j] = s;
+    }
+  if (n == 0) return 0;
+  if (n == 1) { len[order[0]] = 1; return 1; }
+  uint64_t node_w[255];
+  int leaf_parent[256], node_parent[255];
+  int li = 0, qi = 0, qn = 0;
+  for (int m = 0; m < n - 1; ++m) {
+    uint64_t w = 0;
+    for (int pick = 0; pick < 2; ++pick) {
+      int leaf = li < n && (qi >= qn || f[order[li]] <= node_w[qi]);
+      if (leaf) { leaf_parent[li] = m; w += f[order[li]]; ++li; }
+      else { node_parent[qi] = m; w += node_w[qi]; ++qi; }
+    }
+    node_w[qn++] = w;
+  }
+  int depth[255];
+  depth[n - 2] = 0;                       /* the last merge is the root */
+  for (int m = n - 3; m >= 0; --m) depth[m] = depth[node_parent[m]] + 1;
+  int maxlen = 0;
+  for (int i = 0; i < n; ++i) {
+    int l = depth[leaf_parent[i]] + 1;
+    len[order[i]] = (uint8_t)(l > 255 ? 255 : l);
+    if (l > maxlen) maxlen = l;
+  }
+  return maxlen;
+}
+
+int ebo_huffman_lengths(const uint64_t* freq, int lmax, uint8_t* len) {
+  if (lmax < 8 || lmax > 32) return -1;
+  uint64_t f[256];
+  memcpy(f, freq, sizeof f);
+  for (int round = 0; round < 70; ++round) {
+    if (two_queue_lengths(f, len) <= lmax) return round;
+    for (int s = 0; s < 256; ++s)
+      if (f[s] > 0) f[s] = (f[s] >> 1) > 0 ? (f[s] >> 1) : 1;
+  }
+  return -1;
+}
+
+/* Canonical codes: lengths ascending, then symbols ascending, consecutive
+ * values, the first code of each length being (previous first + count) << 1
+ * (the DEFLATE rule). */
+int ebo_canonical_codes(const uint8_t* len, int lmax, uint32_t* code) {
+  uint64_t count[33] = {0};
+  for (int s = 0; s < 256; ++s) {
+    if (len[s] > lmax) return -1;
+    count[len[s]]++;
+  }
+  count[0] = 0;
+  uint64_t kraft = 0;
+  for (int l = 1; l <= lmax; ++l) kraft += count[l] << (lmax - l);
+  if (kraft > ((uint64_t)1 << lmax)) return -1;
+  uint64_t next[33];
+  uint64_t c = 0;
+  next[0] = 0;
+  for (int l = 1; l <= lmax; ++l) { c = (c + count[l - 1]) << 1; next[l] = c; }
+  for (int s = 0; s < 256; ++s) code[s] = len[s] ? (uint32_t)next[len[s]]++ : 0u;
+  return 0;
+}
+
+/* ------------------------------------------------------------------------
+ * Iteration-wise error-bound decay, [DLRM-EBLC] §III-C "Iteration-wise
+ * Configuration" (decay phase then constant phase; logarithmic or stepwise
+ * decay, stepwise the default) and §IV-B Fig. 10 ("Decay_2x": 2x base down to
+ * base; "Drop_2x": 2x base until the end of the initial phase, then base).
+ * Reading: the factor multiplies the base bound and does not compound;
+ * m0 is the initial multiplier, phase_len P the decay phase, n_steps S the
+ * stairs of the stepwise form:
+ *   linear     m0 - (m0-1) * (i/P)                    (i < P)
+ *   stepwise   m0 - (m0-1) * floor(i*S/P) / S          (i < P)
+ *   drop       m0                                       (i < P)
+ *   log        m0^(1 - i/P)                             (i < P)
+ * and 1 for i >= P, for "none", or when P <= 0.
+ * ---------------------------------------------------------------------- */
+double ebo_decay_factor(int fn, int64_t iter, double m0, int64_t P, int S) {
+  if (fn == 0 || P <= 0 || iter >= P) return 1.0;
+  if (iter < 0) iter = 0;
+  double frac = (double)iter / (double)P;
+  switch (fn) {
+    case 1: return m0 - (m0 - 1.0) * frac;
+    case 2: {
+      if (S < 1) S = 1;
+      int64_t k = (iter * (int64_t)S) / P;
+      return m0 - (m0 - 1.0) * ((double)k / (double)S);
+    }
+    case 3: return m0;
+    case 4: return pow(m0, 1.0 - frac);
+    default: return 1.0;
+  }
+}
+
+/* ------------------------------------------------------------------------
+ * Container layout (all little-endian, sections 16-byte aligned):
+ *   header (144 B) | T table records (272 B) | T*nseg segment records (16 B)
+ *   | match bitmap T*ceil(B/32) u32 | chunk lengths u16 | refs u16/u32
+ *   | outlier raw bits u32 | bitstream u32 words
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  uint64_t off_seg, off_bitmap, off_chunks, off_refs, off_out, off_bits, total;
+} layout_t;
+
+static layout_t make_layout(int64_t B, int T, int D, uint64_t n_chunks, uint64_t n_match,
+                            uint64_t n_out, uint64_t words, int ref_bytes) {
+  layout_t L;
+  int64_t nseg = (B + seg_rows(D) - 1) / seg_rows(D);
+  int64_t nw = (B + 31) / 32;
+  L.off_seg = O_HEADER + (uint64_t)T * O_TABLE_REC;
+  L.off_bitmap = L.off_seg + (uint64_t)T * (uint64_t)nseg * O_SEG_REC;
+  L.off_chunks = L.off_bitmap + pad16((uint64_t)T * (uint64_t)nw * 4u);
+  L.off_refs = L.off_chunks + pad16(n_chunks * 2u);
+  L.off_out = L.off_refs + pad16(n_match * (uint64_t)ref_bytes);
+  L.off_bits = L.off_out + pad16(n_out * 4u);
+  L.total = L.off_bits + words * 4u;
+  return L;
+}
+
+static int shape_ok(int64_t B, int T, int D) {
+  if (B < 0 || T < 0 || T > O_MAX_T || !dim_ok(D)) return 0;
+  if (B > 16777215) return 0;
+  if ((uint64_t)B * (uint64_t)T * (uint64_t)D > 0xFFFFFFFFull) return 0;
+  return 1;
+}
+
+uint64_t ebo_compress_bound(int64_t B, int T, int D) {
+  if (!shape_ok(B, T, D)) return 0;
+  uint64_t N = (uint64_t)B * T * D;
+  int64_t nseg = (B + seg_rows(D) - 1) / seg_rows(D);
+  uint64_t vec = (uint64_t)B * T;
+  uint64_t words = (N * O_LMAX + 31) / 32 + 4u * (uint64_t)T * (uint64_t)nseg;
+  layout_t L = make_layout(B, T, D, vec, vec, N, words, B <= 65536 ? 2 : 4);
+  return L.total;
+}
+
+/* MSB-first bit writer over u32 words: bit i lives in word i/32 at bit 31-i%32. */
+static void put_bits(uint32_t* words, uint64_t* pos, uint32_t code, int len) {
+  for (int i = len - 1; i >= 0; --i) {
+    uint32_t bit = (code >> i) & 1u;
+    words[*pos >> 5] |= bit << (31 - (*pos & 31));
+    ++*pos;
+  }
+}
+
+typedef struct { uint32_t h; uint32_t b; } hb_t;
+static int cmp_hb(const void* a, const void* c) {
+  const hb_t* x = (const hb_t*)a; const hb_t* y = (const hb_t*)c;
+  if (x->h != y->h) return x->h < y->h ? -1 : 1;
+  return x->b < y->b ? -1 : (x->b > y->b);
+}
+
+int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8_t* out,
+                 uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
+                 uint8_t* lens_out) {
+  if (!shape_ok(B, T, D)) return EBO_ERR_INVALID_ARG;
+  for (int t = 0; t < T; ++t)
+    if (!eb_ok(eb[t])) return EBO_ERR_INVALID_ARG;
+  const int64_t SB = seg_rows(D), KC = chunk_rows(D);
+  const int64_t nseg = (B + SB - 1) / SB, nw = (B + 31) / 32;
+  const int ref_bytes = B <= 65536 ? 2 : 4;
+  const size_t nvec = (size_t)B * (size_t)T;
+  const size_t N = nvec * (size_t)D;
+
+  uint8_t* sym = (uint8_t*)malloc(N ? N : 1);            /* [T][B][D] */
+  uint32_t* hash = (uint32_t*)malloc((nvec ? nvec : 1) * 4);
+  uint32_t* ref = (uint32_t*)malloc((nvec ? nvec : 1) * 4);
+  uint8_t* lens = (uint8_t*)calloc((size_t)(T ? T : 1) * 256, 1);
+  uint32_t* codes = (uint32_t*)calloc((size_t)(T ? T : 1) * 256, 4);
+  hb_t* pairs = (hb_t*)malloc((size_t)(B ? B : 1) * sizeof(hb_t));
+  if (!sym || !hash || !ref || !lens || !codes || !pairs) {
+    free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
+    return EBO_ERR_INVALID_ARG;
+  }
+
+  /* 1. quantization codes, table-major */
+  for (int t = 0; t < T; ++t) {
+    float ebx2 = 2.0f * eb[t], inv = 1.0f / ebx2;
+    for (int64_t b = 0; b < B; ++b)
+      for (int d = 0; d < D; ++d)
+        sym[((size_t)t * B + b) * D + d] =
+            (uint8_t)quantize_one(x[((size_t)b * T + t) * D + d], eb[t], ebx2, inv);
+  }
+  /* 2. vector hashes */
+  for (int t = 0; t < T; ++t)
+    for (int64_t b = 0; b < B; ++b)
+      hash[(size_t)t * B + b] =
+          ebo_vector_hash(sym + ((size_t)t * B + b) * D, x + ((size_t)b * T + t) * D, D);
+  /* 3. vector dedup ([DLRM-EBLC] §III-D / §III-E, vector-based LZ).  Reading:
+   * the window is the whole batch of one table and the reference is the first
+   * occurrence, ref(b) = min{b' : hash(b') = hash(b)}; b is a match when
+   * ref(b) < b and both vectors have the same codes and the same raw bits at
+   * outliers, else a literal.  References therefore always name literals. */
+  for (int t = 0; t < T; ++t) {
+    for (int64_t b = 0; b < B; ++b) { pairs[b].h = hash[(size_t)t * B + b]; pairs[b].b = (uint32_t)b; }
+    qsort(pairs, (size_t)B, sizeof(hb_t), cmp_hb);
+    for (int64_t i = 0; i < B; ++i) {
+      int64_t g = i;
+      while (g > 0 && pairs[g - 1].h == pairs[i].h) --g;
+      uint32_t b = pairs[i].b, r = pairs[g].b;
+      int match = 0;
+      if (r < b) {
+        const uint8_t* sb = sym + ((size_t)t * B + b) * D;
+        const uint8_t* sr = sym + ((size_t)t * B + r) * D;
+        const float* xb = x + ((size_t)b * T + t) * D;
+        const float* xr = x + ((size_t)r * T + t) * D;
+        match = memcmp(sb, sr, (size_t)D) == 0;
+        for (int d = 0; match && d < D; ++d)
+          if (sb[d] == 0 && f2u(xb[d]) != f2u(xr[d])) match = 0;
+      }
+      ref[(size_t)t * B + b] = match ? r : b;
+    }
+  }
+  /* 4. per-table histogram of literal codes, Huffman lengths, canonical codes */
+  for (int t = 0; t < T; ++t) {
+    uint64_t f[256] = {0};
+    for (int64_t b = 0; b < B; ++b)
+      if (ref[(size_t)t * B + b] == (uint32_t)b)
+        for (int d = 0; d < D; ++d) f[sym[((size_t)t * B + b) * D + d]]++;
+    if (ebo_huffman_lengths(f, O_LMAX, lens + (size_t)t * 256) < 0 ||
+        ebo_canonical_codes(lens + (size_t)t * 256, O_LMAX, codes + (size_t)t * 256) < 0) {
+      free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
+      return EBO_ERR_INVALID_ARG;
+    }
+  }
+  /* 5. sizes */
+  uint64_t n_lit = 0, n_match = 0, n_out = 0, n_chunks = 0, words = 0;
+  for (int t = 0; t < T; ++t)
+    for (int64_t s = 0; s < nseg; ++s) {
+      uint64_t lits = 0, bits = 0;
+      for (int64_t b = s * SB; b < B && b < (s + 1) * SB; ++b) {
+        if (ref[(size_t)t * B + b] != (uint32_t)b) { ++n_match; continue; }
+        ++lits;
+        for (int d = 0; d < D; ++d) {
+          uint8_t c = sym[((size_t)t * B + b) * D + d];
+          bits += lens[(size_t)t * 256 + c];
+          if (c == 0) ++n_out;
+        }
+      }
+      n_lit += lits;
+      n_chunks += (lits + (uint64_t)KC - 1) / (uint64_t)KC;
+      words += ((bits + 127) / 128) * 4;
+    }
+  layout_t L = make_layout(B, T, D, n_chunks, n_match, n_out, words, ref_bytes);
+  if (info) {
+    info->n_literal = n_lit; info->n_match = n_match; info->n_outlier = n_out;
+    info->n_chunks = n_chunks; info->bitstream_bytes = words * 4; info->total_bytes = L.total;
+  }
+  if (sym_out) memcpy(sym_out, sym, N);
+  if (ref_out) memcpy(ref_out, ref, nvec * 4);
+  if (lens_out) memcpy(lens_out, lens, (size_t)T * 256);
+  if (L.total > cap) {
+    free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
+    return EBO_ERR_CAPACITY;
+  }
+
+  /* 6. write the container */
+  memset(out, 0, (size_t)L.total);
+  uint8_t* h = out;
+  wr32(h + 0, O_MAGIC); wr32(h + 4, O_VERSION); wr64(h + 8, (uint64_t)B);
+  wr32(h + 16, (uint32_t)T); wr32(h + 20, (uint32_t)D); wr32(h + 24, O_RADIUS);
+  wr32(h + 28, O_LMAX); wr32(h + 32, (uint32_t)SB); wr32(h + 36, (uint32_t)KC);
+  wr32(h + 40, (uint32_t)ref_bytes); wr32(h + 44, 0);
+  wr64(h + 48, n_lit); wr64(h + 56, n_match); wr64(h + 64, n_out); wr64(h + 72, n_chunks);
+  wr64(h + 80, words); wr64(h + 88, L.off_seg); wr64(h + 96, L.off_bitmap);
+  wr64(h + 104, L.off_chunks); wr64(h + 112, L.off_refs); wr64(h + 120, L.off_out);
+  wr64(h + 128, L.off_bits); wr64(h + 136, L.total);
+
+  uint32_t* stream = (uint32_t*)calloc((size_t)(words ? words : 1), 4);
+  uint64_t chunk_i = 0, match_i = 0, out_i = 0, word_i = 0;
+  for (int t = 0; t < T; ++t) {
+    uint8_t* rec = out + O_HEADER + (size_t)t * O_TABLE_REC;
+    uint32_t tl = 0, tm = 0, to = 0;
+    for (int64_t s = 0; s < nseg; ++s) {
+      uint8_t* srec = out + L.off_seg + ((size_t)t * nseg + s) * O_SEG_REC;
+      wr32(srec + 0, (uint32_t)word_i); wr32(srec + 4, (uint32_t)chunk_i);
+      wr32(srec + 8, (uint32_t)match_i); wr32(srec + 12, (uint32_t)out_i);
+      uint64_t pos = word_i * 32, lit_in_seg = 0, chunk_start = pos;
+      int64_t b_end = (s + 1) * SB < B ? (s + 1) * SB : B;
+      for (int64_t b = s * SB; b < b_end; ++b) {
+        uint32_t r = ref[(size_t)t * B + b];
+        if (r != (uint32_t)b) {
+          uint8_t* bm = out + L.off_bitmap + ((size_t)t * nw + (size_t)(b >> 5)) * 4;
+          wr32(bm, rd32(bm) | (1u << (b & 31)));
+          if (ref_bytes == 2) wr16(out + L.off_refs + match_i * 2, r);
+          else wr32(out + L.off_refs + match_i * 4, r);
+          ++match_i; ++tm;
+          continue;
+        }
+        const uint8_t* sv = sym + ((size_t)t * B + b) * D;
+        const float* xv = x + ((size_t)b * T + t) * D;
+        for (int d = 0; d < D; ++d) {
+          put_bits(stream, &pos, codes[(size_t)t * 256 + sv[d]], lens[(size_t)t * 256 + sv[d]]);
+          if (sv[d] == 0) { wr32(out + L.off_out + out_i * 4, f2u(xv[d])); ++out_i; ++to; }
+        }
+        ++lit_in_seg; ++tl;
+        if (lit_in_seg % (uint64_t)KC == 0) {        /* a chunk holds KC literals */
+          wr16(out + L.off_chunks + chunk_i * 2, (uint32_t)(pos - chunk_start));
+          ++chunk_i; chunk_start = pos;
+        }
+      }
+      if (lit_in_seg % (uint64_t)KC != 0) {          /* the segment's last, short chunk */
+        wr16(out + L.off_chunks + chunk_i * 2, (uint32_t)(pos - chunk_start));
+        ++chunk_i; chunk_start = pos;
+      }
+      word_i += ((pos - word_i * 32 + 127) / 128) * 4;
+    }
+    wr32(rec + 0, f2u(eb[t])); wr32(rec + 4, tl); wr32(rec + 8, tm); wr32(rec + 12, to);
+    memcpy(rec + 16, lens + (size_t)t * 256, 256);
+  }
+  for (uint64_t w = 0; w < words; ++w) wr32(out + L.off_bits + w * 4, stream[w]);
+  free(stream);
+  free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
+  return EBO_OK;
+}
+
+/* ------------------------------------------------------------------------
+ * Decoder: inverts the container; every read is bounds-checked and every
+ * inconsistency is EBO_ERR_CORRUPT.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  uint32_t first[O_LMAX + 2];   /* first canonical code of each length  */
+  uint32_t count[O_LMAX + 2];
+  uint32_t offset[O_LMAX + 2];  /* index of that first code in sorted[] */
+  uint8_t sorted[256];          /* symbols by (length, symbol)          */
+} dec_t;
+
+static int build_decoder(const uint8_t* len, dec_t* dc) {
+  uint32_t code[256];
+  if (ebo_canonical_codes(len, O_LMAX, code) < 0) return -1;
+  memset(dc, 0, sizeof *dc);
+  for (int s = 0; s < 256; ++s) dc->count[len[s]]++;
+  dc->count[0] = 0;
+  uint32_t k = 0;
+  for (int l = 1; l <= O_LMAX; ++l) {
+    dc->offset[l] = k;
+    for (int s = 0; s < 256; ++s)
+      if (len[s] == l) {
+        if (k == dc->offset[l]) dc->first[l] = code[s];
+        dc->sorted[k++] = (uint8_t)s;
+      }
+  }
+  return 0;
+}
+
+int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D, float* xhat,
+                   uint8_t* sym_out) {
+  if (!shape_ok(B, T, D)) return EBO_ERR_INVALID_ARG;
+  if (in_bytes < O_HEADER) return EBO_ERR_CORRUPT;
+  if (rd32(in) != O_MAGIC || rd32(in + 4) != O_VERSION) return EBO_ERR_CORRUPT;
+  if (rd64(in + 8) != (uint64_t)B || rd32(in + 16) != (uint32_t)T || rd32(in + 20) != (uint32_t)D)
+    return EBO_ERR_INVALID_ARG;
+  const int64_t SB = seg_rows(D), KC = chunk_rows(D);
+  const int64_t nseg = (B + SB - 1) / SB, nw = (B + 31) / 32;
+  const int ref_bytes = B <= 65536 ? 2 : 4;
+  if (rd32(in + 24) != O_RADIUS || rd32(in + 28) != O_LMAX || rd32(in + 32) != (uint32_t)SB ||
+      rd32(in + 36) != (uint32_t)KC || rd32(in + 40) != (uint32_t)ref_bytes || rd32(in + 44) != 0)
+    return EBO_ERR_CORRUPT;
+  uint64_t n_lit = rd64(in + 48), n_match = rd64(in + 56), n_out = rd64(in + 64);
+  uint64_t n_chunks = rd64(in + 72), words = rd64(in + 80);
+  uint64_t nvec = (uint64_t)B * (uint64_t)T;
+  if (n_lit + n_match != nvec || n_chunks > nvec || n_out > nvec * (uint64_t)D ||
+      words > ((uint64_t)1 << 34))
+    return EBO_ERR_CORRUPT;
+  layout_t L = make_layout(B, T, D, n_chunks, n_match, n_out, words, ref_bytes);
+  if (rd64(in + 88) != L.off_seg || rd64(in + 96) != L.off_bitmap || rd64(in + 104) != L.off_chunks ||
+      rd64(in + 112) != L.off_refs || rd64(in + 120) != L.off_out || rd64(in + 128) != L.off_bits ||
+      rd64(in + 136) != L.total || L.total > in_bytes)
+    return EBO_ERR_CORRUPT;
+
+  const size_t N = (size_t)nvec * (size_t)D;
+  uint8_t* sym = (uint8_t*)malloc(N ? N : 1);
+  if (!sym) return EBO_ERR_INVALID_ARG;
+  uint64_t chunk_i = 0, match_i = 0, out_i = 0, word_i = 0, lit_total = 0;
+  int err = EBO_OK;
+  for (int t = 0; t < T && err == EBO_OK; ++t) {
+    const uint8_t* rec = in + O_HEADER + (size_t)t * O_TABLE_REC;
+    float eb = u2f(rd32(rec));
+    if (!eb_ok(eb)) { err = EBO_ERR_CORRUPT; break; }
+    dec_t dc;
+    if (build_decoder(rec + 16, &dc) < 0) { err = EBO_ERR_CORRUPT; break; }
+    uint32_t tl = 0, tm = 0, to = 0;
+    for (int64_t s = 0; s < nseg && err == EBO_OK; ++s) {
+      const uint8_t* srec = in + L.off_seg + ((size_t)t * nseg + s) * O_SEG_REC;
+      if (rd32(srec) != word_i || rd32(srec + 4) != chunk_i || rd32(srec + 8) != match_i ||
+          rd32(srec + 12) != out_i) { err = EBO_ERR_CORRUPT; break; }
+      int64_t b_end = (s + 1) * SB < B ? (s + 1) * SB : B;
+      uint64_t seg_bit0 = word_i * 32, pos = seg_bit0, lit_in_seg = 0, chunk_start = pos;
+      uint64_t seg_lits = 0;
+      for (int64_t b = s * SB; b < b_end; ++b) {
+        const uint8_t* bm = in + L.off_bitmap + ((size_t)t * nw + (size_t)(b >> 5)) * 4;
+        if (!((rd32(bm) >> (b & 31)) & 1u)) ++seg_lits;
+      }
+      for (int64_t b = s * SB; b < b_end && err == EBO_OK; ++b) {
+        const uint8_t* bm = in + L.off_bitmap + ((size_t)t * nw + (size_t)(b >> 5)) * 4;
+        if ((rd32(bm) >> (b & 31)) & 1u) { ++match_i; ++tm; continue; }
+        if (chunk_i >= n_chunks) { err = EBO_ERR_CORRUPT; break; }
+        uint64_t chunk_end = chunk_start + rd16(in + L.off_chunks + chunk_i * 2);
+        uint8_t* sv = sym + ((size_t)t * B + b) * D;
+        for (int d = 0; d < D; ++d) {
+          uint32_t code = 0;
+          int l = 0, found = 0;
+          while (!found) {
+            if (l >= O_LMAX || pos >= chunk_end || pos >= words * 32) { err = EBO_ERR_CORRUPT; break; }
+            uint32_t word = rd32(in + L.off_bits + (pos >> 5) * 4);
+            code = (code << 1) | ((word >> (31 - (pos & 31))) & 1u);
+            ++pos; ++l;
+            if (dc.count[l] && code >= dc.first[l] && code - dc.first[l] < dc.count[l]) {
+              sv[d] = dc.sorted[dc.offset[l] + (code - dc.first[l])];
+              found = 1;
+            }
+          }
+          if (err) break;
+          float v;
+          if (sv[d] == 0) {
+            if (out_i >= n_out) { err = EBO_ERR_CORRUPT; break; }
+            v = u2f(rd32(in + L.off_out + out_i * 4));
+            ++out_i; ++to;
+          } else {
+            v = ebo_dequantize(sv[d], eb);
+          }
+          xhat[((size_t)b * T + t) * D + d] = v;
+        }
+        if (err) break;
+        ++lit_in_seg; ++tl; ++lit_total;
+        if (lit_in_seg % (uint64_t)KC == 0 || lit_in_seg == seg_lits) {
+          if (pos != chunk_end) { err = EBO_ERR_CORRUPT; break; }
+          ++chunk_i; chunk_start = pos;
+        }
+      }
+      if (err) break;
+      /* bitmap bits past B must be clear */
+      if (s == nseg - 1 && (B & 31)) {
+        const uint8_t* bm = in + L.off_bitmap + ((size_t)t * nw + (size_t)(nw - 1)) * 4;
+        if (rd32(bm) >> (B & 31)) { err = EBO_ERR_CORRUPT; break; }
+      }
+      word_i += ((pos - seg_bit0 + 127) / 128) * 4;
+      if (word_i > words) { err = EBO_ERR_CORRUPT; break; }
+    }
+    if (err) break;
+    if (rd32(rec + 4) != tl || rd32(rec + 8) != tm || rd32(rec + 12) != to) err = EBO_ERR_CORRUPT;
+    /* matches: copy the reference row (references always name literals) */
+    if (err == EBO_OK) {
+      uint64_t m = match_i - tm;
+      for (int64_t b = 0; b < B && err == EBO_OK; ++b) {
+        const uint8_t* bm = in + L.off_bitmap + ((size_t)t * nw + (size_t)(b >> 5)) * 4;
+        if (!((rd32(bm) >> (b & 31)) & 1u)) continue;
+        uint32_t r = ref_bytes == 2 ? rd16(in + L.off_refs + m * 2) : rd32(in + L.off_refs + m * 4);
+        ++m;
+        const uint8_t* bmr = in + L.off_bitmap + ((size_t)t * nw + (size_t)(r >> 5)) * 4;
+        if ((int64_t)r >= b || ((rd32(bmr) >> (r & 31)) & 1u)) { err = EBO_ERR_CORRUPT; break; }
+        memcpy(sym + ((size_t)t * B + b) * D, sym + ((size_t)t * B + r) * D, (size_t)D);
+        memcpy(xhat + ((size_t)b * T + t) * D, xhat + ((size_t)r * T + t) * D, (size_t)D * 4);
+      }
+    }
+  }
+  if (err == EBO_OK && (chunk_i != n_chunks || match_i != n_match || out_i != n_out ||
+                        word_i != words || lit_total != n_lit))
+    err = EBO_ERR_CORRUPT;
+  if (err == EBO_OK && sym_out) memcpy(sym_out, sym, N);
+  free(sym);
+  return err;
+}
