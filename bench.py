@@ -1,0 +1,362 @@
+#!/usr/bin/env python
+"""Throughput of the error-bounded embedding codec on GB300.
+
+One step = one compress + one decompress of the DLRM forward-lookup batch
+[8192, 26, 128] fp32 (26 tables, rows 10^3..10^6 log-uniform, Zipf(1.05)
+lookups, eb_t = 1e-2 * range of table t), the whole hot path.  The metric is
+GB/s of uncompressed fp32 through compress + decompress (4N bytes per step over
+the summed compress and decompress time), with the compression ratio and the
+roofline fraction of the dominant kernel alongside.
+
+  python bench.py [--steps K] [--warmup W] [--gpus N] [--impl ours|reference]
+
+Under torchrun each rank compresses its own batch (seed = rank): independent
+units, no collective on the data path ("scaling": "weak").  --impl reference
+times the plain single-threaded CPU oracle on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+WORKLOAD = "fwd"
+METRIC = "compress+decompress GB/s (uncompressed fp32)"
+KERNEL_SOURCES = ["ebc_compress.cu", "ebc_decompress.cu", "ebc_internal.cuh"]
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    return p.parse_args()
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peak_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    for s in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "error_bounded_lossy_gb300", "csrc", s), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(kernel: str):
+    """dram bytes per launch of `kernel` from the committed ncu summary, if it was
+    taken on the current kernel sources; else None."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_fwd_8192x26x128.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m = re.search(r"source_hash:\s*([0-9a-f]+)", text)
+    t = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", text)
+    if not m or not t or m.group(1) != source_hash():
+        return None
+    return int(t.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.2)
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            f = [v.strip() for v in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                rows.append((float(f[1]), float(f[2]), f[5], f[6], f[7], f[8]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        loaded = [r for r in rows if r[0] > 0.5 * r[1]] or rows
+        reasons = set()
+        for r in loaded:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[2:]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r[0] for r in loaded), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# algorithmic HBM bytes per launch (inputs read and outputs written that the
+# step cannot avoid; scratch meant to stay in L2 is not counted)
+def algorithmic_bytes(kernel: str, N: int, D: int, st: dict) -> int:
+    C = st["out_bytes"]
+    return {
+        "k_quantize": 4 * N,
+        "k_resolve": 0,
+        "k_codebook": 0,
+        "k_emit": C,
+        "k_dec_tables": 0,
+        "k_dec_segments": C + 4 * D * st["n_literal"],
+        "k_dec_matches": 4 * D * st["n_match"],
+    }.get(kernel, 0)
+
+
+def oracle_sample_rate(x_np, eb, seconds: float):
+    """Oracle compress+decompress GB/s on the host, looping over a bounded sample."""
+    import oracle
+    oracle.build()
+    done, t_total, reps = 0, 0.0, 0
+    B, T, D = x_np.shape
+    while t_total < seconds or reps == 0:
+        t0 = time.perf_counter()
+        buf, info = oracle.compress(x_np, eb)
+        oracle.decompress(buf, B, T, D)
+        t_total += time.perf_counter() - t0
+        done += x_np.nbytes
+        reps += 1
+    return done / t_total / 1e9, reps, info
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    wl = workloads.make(WORKLOAD, batch=512)
+    x_np, eb = wl.x.numpy(), wl.eb.numpy()
+    for _ in range(args.warmup):
+        oracle_sample_rate(x_np, eb, 0.0)
+    steps = max(1, min(args.steps, 60))
+    t0 = time.perf_counter()
+    rate, reps, info = oracle_sample_rate(x_np, eb, 0.0)
+    times = []
+    import oracle
+    for _ in range(steps):
+        s = time.perf_counter()
+        buf, _ = oracle.compress(x_np, eb)
+        oracle.decompress(buf, *x_np.shape)
+        times.append(time.perf_counter() - s)
+    total = sum(times)
+    value = steps * x_np.nbytes / total / 1e9
+    sample = f"first 512 of 8192 batch rows, all 26 tables, D=128 ({x_np.nbytes} B) per step"
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": "DLRM forward lookups [8192,26,128] fp32, Zipf(1.05), eb=1e-2*range (oracle sample)",
+                   "global_batch": 512, "tables": 26, "dim": 128, "l2": "n/a (host)"},
+        "compression_ratio": round(x_np.nbytes / info["total_bytes"], 3),
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    world, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+        return
+    import error_bounded_lossy_gb300 as ebc
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    wl = workloads.make(WORKLOAD, device=dev, seed=rank)
+    x = wl.x
+    eb = wl.eb.numpy()
+    B, T, D = x.shape
+    N = x.numel()
+    codec = ebc.Codec(local)
+    cap = codec.compress_bound(B, T, D)
+    out = torch.empty(cap, dtype=torch.uint8, device=dev)
+    nbytes = torch.zeros(1, dtype=torch.int64, device=dev)
+    xhat = torch.empty_like(x)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        codec.compress_into(x, eb, out, nbytes, stream)
+        codec.decompress_into(out, cap, xhat, stream)
+
+    # warm-up and correctness gate (outside the timed region)
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    codec.check()
+    st = codec.stats()
+    C = st["out_bytes"]
+    err = (x.double() - xhat.double()).abs().amax(dim=(0, 2)).cpu().numpy()
+    if not (err <= eb.astype(np.float64)).all():
+        raise SystemExit("error bound violated")
+
+    # ---- timed region: per-step CUDA events, L2 flushed before every step ----
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+            torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.perf_counter()
+    with ClockSampler(local) as clk:
+        for e0, e1, e2 in evs:
+            flush.zero_()
+            e0.record(stream)
+            codec.compress_into(x, eb, out, nbytes, stream)
+            e1.record(stream)
+            codec.decompress_into(out, cap, xhat, stream)
+            e2.record(stream)
+        torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    if pg:
+        pg.barrier()
+    codec.check()
+    t_c = sum(a.elapsed_time(b) for a, b, _ in evs) / 1e3
+    t_d = sum(b.elapsed_time(c) for _, b, c in evs) / 1e3
+    t_step = t_c + t_d
+    if pg:
+        tt = torch.tensor([t_step, t_c, t_d], dtype=torch.float64, device=dev)
+        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
+        t_step, t_c, t_d = tt.tolist()
+    value = world * K * 4 * N / t_step / 1e9
+
+    # ---- per-kernel durations (same steps, events around every launch) ----
+    codec.set_profiling(True)
+    codec.profile()
+    for _ in range(min(K, 1000)):
+        flush.zero_()
+        step()
+    prof = codec.profile()
+    codec.set_profiling(False)
+    total_ms = sum(v[1] for v in prof.values())
+    top = max(prof.items(), key=lambda kv: kv[1][1])
+    kname, (launches, kms) = top
+    avg_s = kms / launches / 1e3
+    peak, peak_kind = measured_peak_gbs()
+    alg = algorithmic_bytes(kname, N, D, st)
+    achieved = alg / avg_s / 1e9
+    roofline = {"bound": "hbm", "kernel": kname, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst)",
+                "traffic": committed_traffic(kname), "algorithmic_bytes": alg,
+                "avg_launch_us": round(avg_s * 1e6, 2)}
+    kernels = {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / v[0], 2), "share": round(v[1] / total_ms, 4),
+                   "algorithmic_gbs": round(algorithmic_bytes(k, N, D, st) / (v[1] / v[0] / 1e3) / 1e9, 1)}
+               for k, v in prof.items()}
+
+    # ---- end to end through the host-buffer C-ABI calls (pinned memory) ----
+    x_host = x.cpu().pin_memory()
+    cont_host = torch.empty(cap, dtype=torch.uint8).pin_memory()
+    xhat_host = torch.empty((B, T, D), dtype=torch.float32).pin_memory()
+    codec.compress_host(x_host, eb, cont_host)
+    e2e_t = []
+    for _ in range(args.e2e_steps):
+        s = time.perf_counter()
+        _, n = codec.compress_host(x_host, eb, cont_host)
+        codec.decompress_host(cont_host, n, B, T, D, xhat_host)
+        e2e_t.append(time.perf_counter() - s)
+    e2e_value = 4 * N / statistics.median(e2e_t) / 1e9
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        sample = workloads.make(WORKLOAD, batch=512)
+        rate, reps, _ = oracle_sample_rate(sample.x.numpy(), sample.eb.numpy(), args.cpu_seconds)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"first 512 of 8192 batch rows x 26 tables x 128 ({sample.nbytes} B), "
+                         f"compress+decompress repeated {reps}x"}
+
+    if rank == 0:
+        clocks = clk.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(1e3 * t_step / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "DLRM forward lookups [8192,26,128] fp32, 26 tables rows 1e3..1e6 log-uniform, "
+                                   "Zipf(1.05), eb_t=1e-2*range", "global_batch": B * world, "tables": T, "dim": D,
+                       "parallelism": f"replicas x{world}", "l2": "flushed before every step (2x L2 memset)"},
+            "compress_gbs": round(world * K * 4 * N / t_c / 1e9, 2),
+            "decompress_gbs": round(world * K * 4 * N / t_d / 1e9, 2),
+            "compression_ratio": round(4 * N / C, 3),
+            "stats": {k: st[k] for k in ("out_bytes", "n_literal", "n_match", "n_outlier", "bitstream_bytes")},
+            "hbm_frac_compress": round((4 * N + C) / (t_c / K) / 1e9 / peak, 4),
+            "hbm_frac_decompress": round((4 * N + C) / (t_d / K) / 1e9 / peak, 4),
+            "roofline": roofline,
+            "kernels": kernels,
+            "gpu_launches": 7 * K,
+            "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": 4 * N + C,
+                    "d2h_bytes_per_step": 8 + C + 4 * N},
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "wall_s": round(wall, 3),
+        }
+        print(json.dumps(line), flush=True)
+    codec.close()
+    if pg:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

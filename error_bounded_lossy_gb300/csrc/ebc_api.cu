@@ -1,0 +1,488 @@
+// ebc_api.cu -- host side of the C ABI declared in include/ebc.h: argument
+// checks, the error-bound schedule, device scratch, and the kernel launches.
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "ebc_internal.cuh"
+
+
+using namespace ebc;
+
+// Per-kernel timing: a pool of CUDA event pairs recorded around each launch
+// while profiling is on; read back (and cleared) by ebc_get_profile.
+struct ebc::Prof {
+  static constexpr int kPairs = 2048;
+  cudaEvent_t ev[2 * kPairs] = {};
+  const char* name[kPairs] = {};
+  int used = 0;
+  bool on = false;
+  bool created = false;
+};
+
+void ebc::prof_begin(Prof* p, const char* name, cudaStream_t st) {
+  if (!p || !p->on || p->used >= Prof::kPairs) return;
+  p->name[p->used] = name;
+  cudaEventRecord(p->ev[2 * p->used], st);
+}
+
+void ebc::prof_end(Prof* p, cudaStream_t st) {
+  if (!p || !p->on || p->used >= Prof::kPairs) return;
+  cudaEventRecord(p->ev[2 * p->used + 1], st);
+  ++p->used;
+}
+
+struct ebc_ctx {
+  int device = 0;
+  cudaStream_t last_stream = nullptr;
+  Glob* glob = nullptr;                // device
+  unsigned long long* h_pinned = nullptr;  // pinned scratch for the host-buffer calls
+  // compress scratch
+  void* cbuf = nullptr;
+  size_t cbuf_bytes = 0;
+  // decompress scratch
+  void* dbuf = nullptr;
+  size_t dbuf_bytes = 0;
+  // host-buffer staging
+  void* stage_in = nullptr;
+  size_t stage_in_bytes = 0;
+  void* stage_out = nullptr;
+  size_t stage_out_bytes = 0;
+  unsigned long long* d_nbytes = nullptr;
+  uint32_t cepoch = 0, depoch = 0;
+  // schedule
+  float* eb_base = nullptr;
+  float* eb_now = nullptr;
+  int sched_T = 0;
+  // last compress shape
+  int64_t lastB = 0;
+  int lastT = 0, lastD = 0;
+  Prof* prof = nullptr;
+};
+
+// ---------------------------------------------------------------------------
+// shapes and argument checks
+// ---------------------------------------------------------------------------
+static bool dim_ok(int D) { return D >= 4 && D <= 512 && (D & (D - 1)) == 0; }
+
+static bool shape_ok(int64_t B, int T, int D) {
+  if (B < 0 || B > kMaxB || T < 0 || T > kMaxT || !dim_ok(D)) return false;
+  return (uint64_t)B * (uint64_t)T * (uint64_t)D <= 0xFFFFFFFFull;
+}
+
+static Shape make_shape(int64_t B, int T, int D) {
+  Shape sh;
+  sh.B = B;
+  sh.T = T;
+  sh.D = D;
+  sh.SB = 8192 / D < 32 ? 32 : 8192 / D;
+  sh.KC = 128 / D < 1 ? 1 : 128 / D;
+  sh.nseg = (int)((B + sh.SB - 1) / sh.SB);
+  sh.nw = (int)((B + 31) / 32);
+  uint32_t S = 64;
+  while ((int64_t)S < 2 * B) S <<= 1;
+  sh.S = S;
+  sh.ref_bytes = B <= 65536 ? 2 : 4;
+  return sh;
+}
+
+static uint64_t pad16h(uint64_t n) { return (n + 15u) & ~(uint64_t)15u; }
+
+// Bytes of the container that do not depend on the data: header, table and
+// segment records, match bitmap.
+static uint64_t fixed_bytes(const Shape& sh) {
+  return kHeaderBytes + (uint64_t)sh.T * kTableRecBytes + (uint64_t)sh.T * sh.nseg * kSegRecBytes +
+         pad16h((uint64_t)sh.T * sh.nw * 4u);
+}
+
+static bool eb_ok(float eb) {
+  if (!(eb >= 1.17549435e-38f) || !(eb <= 3.40282347e+38f)) return false;
+  const volatile float ebx2 = 2.0f * eb;
+  if (!(ebx2 <= 3.40282347e+38f)) return false;
+  const volatile float inv = 1.0f / ebx2;
+  return inv >= 1.17549435e-38f;
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int cuda_err(cudaError_t e) { return e == cudaSuccess ? EBC_OK : EBC_ERR_CUDA; }
+
+// ---------------------------------------------------------------------------
+// scratch
+// ---------------------------------------------------------------------------
+namespace {
+struct Carver {
+  char* base;
+  size_t off = 0;
+  template <class P>
+  P* take(size_t bytes) {
+    P* p = reinterpret_cast<P*>(base ? base + off : nullptr);
+    off += (bytes + 255) & ~(size_t)255;
+    return p;
+  }
+};
+}  // namespace
+
+static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
+  Carver c{reinterpret_cast<char*>(buf)};
+  Work w{};
+  const size_t nvec = (size_t)sh.B * sh.T, nsegT = (size_t)sh.T * sh.nseg;
+  w.sym = c.take<uint8_t>(nvec * sh.D);
+  w.vhash = c.take<uint32_t>(4 * nvec);
+  w.vnout = c.take<uint32_t>(4 * nvec);
+  w.ref = c.take<uint32_t>(4 * nvec);
+  w.slots = c.take<unsigned long long>(8 * (size_t)sh.T * sh.S);
+  w.bitmap = c.take<uint32_t>(4 * (size_t)sh.T * sh.nw);
+  w.seg_hist = c.take<uint32_t>(1024 * nsegT);
+  w.seg_cnt = c.take<uint4>(16 * nsegT);
+  w.seg_off = c.take<uint4>(16 * nsegT);
+  w.seg_words = c.take<uint32_t>(4 * nsegT);
+  w.tabcode = c.take<uint32_t>(1024 * (size_t)sh.T);
+  w.tab_tot = c.take<uint4>(16 * (size_t)sh.T);
+  w.tab_lits = c.take<uint32_t>(4 * (size_t)sh.T);
+  w.tab_base = c.take<uint4>(16 * (size_t)sh.T);
+  w.glob = g;
+  *total = c.off;
+  return w;
+}
+
+static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total) {
+  Carver c{reinterpret_cast<char*>(buf)};
+  Work w{};
+  w.lut = c.take<uint16_t>(2u * (1u << kLutBits) * (size_t)sh.T);
+  w.dtab = c.take<DecTab>(sizeof(DecTab) * (size_t)sh.T);
+  w.glob = g;
+  *total = c.off;
+  return w;
+}
+
+static int grow(void** buf, size_t* have, size_t need) {
+  if (need <= *have && *buf) return EBC_OK;
+  if (*buf) {
+    if (cudaDeviceSynchronize() != cudaSuccess) return EBC_ERR_CUDA;
+    cudaFree(*buf);
+    *buf = nullptr;
+    *have = 0;
+  }
+  if (need == 0) need = 256;
+  if (cudaMalloc(buf, need) != cudaSuccess) {
+    *buf = nullptr;
+    return EBC_ERR_CUDA;
+  }
+  *have = need;
+  return EBC_OK;
+}
+
+// ---------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------
+extern "C" {
+
+int ebc_version(void) { return EBC_VERSION; }
+
+const char* ebc_strerror(int code) {
+  switch (code) {
+    case EBC_OK: return "ok";
+    case EBC_ERR_INVALID_ARG: return "invalid argument";
+    case EBC_ERR_CAPACITY: return "output buffer too small for the container";
+    case EBC_ERR_CORRUPT: return "corrupt container";
+    case EBC_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case EBC_ERR_CUDA: return "CUDA runtime error";
+    case EBC_ERR_NO_DEVICE: return "no usable sm_103 device";
+    case EBC_ERR_INTERNAL: return "internal invariant failed on the device";
+    default: return "unknown error";
+  }
+}
+
+int ebc_create(ebc_ctx** out, int device) {
+  if (!out) return EBC_ERR_INVALID_ARG;
+  *out = nullptr;
+  int n = 0;
+  if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) return EBC_ERR_NO_DEVICE;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return EBC_ERR_NO_DEVICE;
+  if (!(prop.major == 10 && prop.minor == 3)) return EBC_ERR_NO_DEVICE;
+  if (cudaSetDevice(device) != cudaSuccess) return EBC_ERR_CUDA;
+  ebc_ctx* c = new (std::nothrow) ebc_ctx();
+  if (!c) return EBC_ERR_INTERNAL;
+  c->device = device;
+  if (cudaMalloc(&c->glob, sizeof(Glob)) != cudaSuccess || cudaMemset(c->glob, 0, sizeof(Glob)) != cudaSuccess ||
+      cudaMalloc(&c->d_nbytes, 16) != cudaSuccess || cudaMallocHost(&c->h_pinned, 64) != cudaSuccess) {
+    ebc_destroy(c);
+    return EBC_ERR_CUDA;
+  }
+  if (set_kernel_attributes() != cudaSuccess) {
+    ebc_destroy(c);
+    return EBC_ERR_CUDA;
+  }
+  *out = c;
+  return EBC_OK;
+}
+
+void ebc_destroy(ebc_ctx* c) {
+  if (!c) return;
+  cudaSetDevice(c->device);
+  cudaDeviceSynchronize();
+  cudaFree(c->glob);
+  cudaFree(c->cbuf);
+  cudaFree(c->dbuf);
+  cudaFree(c->stage_in);
+  cudaFree(c->stage_out);
+  cudaFree(c->d_nbytes);
+  if (c->h_pinned) cudaFreeHost(c->h_pinned);
+  std::free(c->eb_base);
+  std::free(c->eb_now);
+  if (c->prof) {
+    if (c->prof->created)
+      for (cudaEvent_t e : c->prof->ev) cudaEventDestroy(e);
+    delete c->prof;
+  }
+  delete c;
+}
+
+// The decay factor and the scheduled bound are computed in double and rounded
+// once to float; the same expressions, in the same order, define the schedule
+// in the header.
+static double decay_factor(int fn, int64_t i, double m0, int64_t P, int S) {
+  if (fn == EBC_DECAY_NONE || P <= 0 || i >= P) return 1.0;
+  if (i < 0) i = 0;
+  const double frac = (double)i / (double)P;
+  switch (fn) {
+    case EBC_DECAY_LINEAR: return m0 - (m0 - 1.0) * frac;
+    case EBC_DECAY_STEPWISE: {
+      if (S < 1) S = 1;
+      const int64_t k = (i * (int64_t)S) / P;
+      return m0 - (m0 - 1.0) * ((double)k / (double)S);
+    }
+    case EBC_DECAY_DROP: return m0;
+    case EBC_DECAY_LOG: return std::pow(m0, 1.0 - frac);
+    default: return 1.0;
+  }
+}
+
+int ebc_set_error_bounds(ebc_ctx* c, const float* eb_base, int T, int64_t iteration, int decay_fn, double m0,
+                         int64_t phase_len, int n_steps) {
+  if (!c || !eb_base || T < 1 || T > kMaxT || decay_fn < EBC_DECAY_NONE || decay_fn > EBC_DECAY_LOG ||
+      iteration < 0 || !(m0 > 0.0) || !std::isfinite(m0) || (decay_fn == EBC_DECAY_STEPWISE && n_steps < 1))
+    return EBC_ERR_INVALID_ARG;
+  const double f = decay_factor(decay_fn, iteration, m0, phase_len, n_steps);
+  float* base = (float*)std::malloc(sizeof(float) * T);
+  float* now = (float*)std::malloc(sizeof(float) * T);
+  if (!base || !now) {
+    std::free(base);
+    std::free(now);
+    return EBC_ERR_INTERNAL;
+  }
+  for (int t = 0; t < T; ++t) {
+    base[t] = eb_base[t];
+    now[t] = (float)((double)eb_base[t] * f);
+    if (!eb_ok(base[t]) || !eb_ok(now[t])) {
+      std::free(base);
+      std::free(now);
+      return EBC_ERR_INVALID_ARG;
+    }
+  }
+  std::free(c->eb_base);
+  std::free(c->eb_now);
+  c->eb_base = base;
+  c->eb_now = now;
+  c->sched_T = T;
+  return EBC_OK;
+}
+
+int ebc_get_error_bounds(const ebc_ctx* c, float* eb_out, int T) {
+  if (!c || !eb_out || T != c->sched_T || !c->eb_now) return EBC_ERR_INVALID_ARG;
+  std::memcpy(eb_out, c->eb_now, sizeof(float) * T);
+  return EBC_OK;
+}
+
+uint64_t ebc_compress_bound(int64_t B, int T, int D) {
+  if (!shape_ok(B, T, D)) return 0;
+  const Shape sh = make_shape(B, T, D);
+  const uint64_t N = (uint64_t)B * T * D, nvec = (uint64_t)B * T;
+  const uint64_t words = (N * kLmax + 31) / 32 + 4ull * T * sh.nseg;
+  return fixed_bytes(sh) + pad16h(nvec * 2u) + pad16h(nvec * sh.ref_bytes) + pad16h(N * 4u) + words * 4u;
+}
+
+int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, void* d_out,
+                 uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
+  if (!c || !shape_ok(B, T, D) || !d_out || !d_out_bytes || !aligned16(d_out) ||
+      ((uintptr_t)d_out_bytes & 7u) != 0)
+    return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T * D;
+  if (N > 0 && (!d_x || !aligned16(d_x))) return EBC_ERR_INVALID_ARG;
+  const float* ebs = eb;
+  if (!ebs) {
+    if (!c->eb_now || c->sched_T != T) return EBC_ERR_INVALID_ARG;
+    ebs = c->eb_now;
+  }
+  EbParams ep;
+  std::memset(&ep, 0, sizeof ep);
+  for (int t = 0; t < T; ++t) {
+    if (!eb_ok(ebs[t])) return EBC_ERR_INVALID_ARG;
+    ep.eb[t] = ebs[t];
+  }
+  const Shape sh = make_shape(B, T, D);
+  if (out_capacity < fixed_bytes(sh)) return EBC_ERR_CAPACITY;
+  if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
+  size_t need = 0;
+  carve_compress(nullptr, sh, c->glob, &need);
+  int rc = grow(&c->cbuf, &c->cbuf_bytes, need);
+  if (rc) return rc;
+  const Work w = carve_compress(c->cbuf, sh, c->glob, &need);
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  c->cepoch = (c->cepoch + 1) & 0xFFFFFFu;
+  c->lastB = B;
+  c->lastT = T;
+  c->lastD = D;
+  if (T > 0 && sh.nseg > 0 &&
+      cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  return cuda_err(launch_compress(d_x, sh, ep, w, (uint8_t*)d_out, out_capacity,
+                                  (unsigned long long*)d_out_bytes, c->cepoch, st, c->prof));
+}
+
+int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
+                   void* stream) {
+  if (!c || !shape_ok(B, T, D) || !d_in || !aligned16(d_in)) return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T * D;
+  if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
+  const Shape sh = make_shape(B, T, D);
+  if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
+  size_t need = 0;
+  carve_decompress(nullptr, sh, c->glob, &need);
+  int rc = grow(&c->dbuf, &c->dbuf_bytes, need);
+  if (rc) return rc;
+  const Work w = carve_decompress(c->dbuf, sh, c->glob, &need);
+  cudaStream_t st = (cudaStream_t)stream;
+  c->last_stream = st;
+  c->depoch = (c->depoch + 1) & 0xFFFFFFu;
+  return cuda_err(launch_decompress((const uint8_t*)d_in, in_bytes, sh, w, d_xhat, c->depoch, st, c->prof));
+}
+
+int ebc_last_device_error(ebc_ctx* c) {
+  if (!c) return EBC_ERR_INVALID_ARG;
+  if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
+  if (cudaStreamSynchronize(c->last_stream) != cudaSuccess) return EBC_ERR_CUDA;
+  unsigned int code = 0;
+  if (cudaMemcpy(&code, &c->glob->sticky, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return EBC_ERR_CUDA;
+  if (code) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(&c->glob->sticky, &zero, 4, cudaMemcpyHostToDevice) != cudaSuccess) return EBC_ERR_CUDA;
+  }
+  return (int)code;
+}
+
+int ebc_get_stats(ebc_ctx* c, ebc_stats* out) {
+  if (!c || !out) return EBC_ERR_INVALID_ARG;
+  const int err = ebc_last_device_error(c);
+  if (err == EBC_ERR_CUDA) return err;
+  Glob g;
+  if (cudaMemcpy(&g, c->glob, sizeof g, cudaMemcpyDeviceToHost) != cudaSuccess) return EBC_ERR_CUDA;
+  std::memset(out, 0, sizeof *out);
+  out->n_vectors = (uint64_t)c->lastB * c->lastT;
+  out->in_bytes = out->n_vectors * c->lastD * 4u;
+  out->out_bytes = g.total;
+  out->n_literal = g.n_lit;
+  out->n_match = g.n_match;
+  out->n_outlier = g.n_out;
+  out->n_chunks = g.n_chunks;
+  out->bitstream_bytes = g.words * 4u;
+  return err;
+}
+
+int ebc_compress_host(ebc_ctx* c, const float* h_x, int64_t B, int T, int D, const float* eb, void* h_out,
+                      uint64_t out_capacity, uint64_t* out_bytes, void* stream) {
+  if (!c || !shape_ok(B, T, D) || !h_out || !out_bytes) return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T * D;
+  if (N > 0 && !h_x) return EBC_ERR_INVALID_ARG;
+  if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
+  const uint64_t bound = ebc_compress_bound(B, T, D);
+  int rc = grow(&c->stage_in, &c->stage_in_bytes, N * 4u);
+  if (!rc) rc = grow(&c->stage_out, &c->stage_out_bytes, bound);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (N > 0 && cudaMemcpyAsync(c->stage_in, h_x, N * 4u, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  rc = ebc_compress(c, (const float*)c->stage_in, B, T, D, eb, c->stage_out, bound, (uint64_t*)c->d_nbytes, stream);
+  if (rc) return rc;
+  if (cudaMemcpyAsync(c->h_pinned, c->d_nbytes, 8, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  const int err = ebc_last_device_error(c);
+  if (err) return err;
+  const uint64_t n = c->h_pinned[0];
+  *out_bytes = n;
+  if (n > out_capacity) return EBC_ERR_CAPACITY;
+  if (cudaMemcpyAsync(h_out, c->stage_out, n, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  return EBC_OK;
+}
+
+int ebc_decompress_host(ebc_ctx* c, const void* h_in, uint64_t in_bytes, float* h_xhat, int64_t B, int T, int D,
+                        void* stream) {
+  if (!c || !shape_ok(B, T, D) || !h_in) return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T * D;
+  if (N > 0 && !h_xhat) return EBC_ERR_INVALID_ARG;
+  if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
+  int rc = grow(&c->stage_out, &c->stage_out_bytes, in_bytes);
+  if (!rc) rc = grow(&c->stage_in, &c->stage_in_bytes, N * 4u);
+  if (rc) return rc;
+  cudaStream_t st = (cudaStream_t)stream;
+  if (in_bytes && cudaMemcpyAsync(c->stage_out, h_in, in_bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  rc = ebc_decompress(c, c->stage_out, in_bytes, (float*)c->stage_in, B, T, D, stream);
+  if (rc) return rc;
+  if (N > 0 && cudaMemcpyAsync(h_xhat, c->stage_in, N * 4u, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return EBC_ERR_CUDA;
+  return ebc_last_device_error(c);
+}
+
+int ebc_set_profiling(ebc_ctx* c, int enable) {
+  if (!c) return EBC_ERR_INVALID_ARG;
+  if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
+  if (!c->prof) {
+    c->prof = new (std::nothrow) Prof();
+    if (!c->prof) return EBC_ERR_INTERNAL;
+  }
+  if (enable && !c->prof->created) {
+    for (cudaEvent_t& e : c->prof->ev)
+      if (cudaEventCreate(&e) != cudaSuccess) return EBC_ERR_CUDA;
+    c->prof->created = true;
+  }
+  c->prof->on = enable != 0;
+  return EBC_OK;
+}
+
+int ebc_get_profile(ebc_ctx* c, ebc_kernel_time* out, int capacity, int* count) {
+  if (!c || !count || capacity < 0 || (capacity > 0 && !out)) return EBC_ERR_INVALID_ARG;
+  *count = 0;
+  if (!c->prof || !c->prof->created) return EBC_OK;
+  Prof* p = c->prof;
+  if (p->used > 0 && cudaEventSynchronize(p->ev[2 * p->used - 1]) != cudaSuccess) return EBC_ERR_CUDA;
+  int n = 0;
+  for (int i = 0; i < p->used; ++i) {
+    float ms = 0.f;
+    if (cudaEventElapsedTime(&ms, p->ev[2 * i], p->ev[2 * i + 1]) != cudaSuccess) return EBC_ERR_CUDA;
+    int k = 0;
+    while (k < n && std::strncmp(out[k].name, p->name[i], sizeof out[k].name) != 0) ++k;
+    if (k == n) {
+      if (n == capacity) continue;
+      std::memset(&out[k], 0, sizeof out[k]);
+      std::strncpy(out[k].name, p->name[i], sizeof out[k].name - 1);
+      ++n;
+    }
+    out[k].launches += 1;
+    out[k].total_ms += ms;
+  }
+  p->used = 0;
+  *count = n;
+  return EBC_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,140 @@
+// ebc_internal.cuh -- types, format constants and device helpers shared by the
+// codec's CUDA kernels (sm_103a).  See include/ebc.h for the container format.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/ebc.h"
+
+namespace ebc {
+
+// ---- container format, version 1 ----
+constexpr int kRadius = 128;               // codes q + 128 for |q| < 128; 0 = outlier
+constexpr int kLmax = 24;                  // longest Huffman code
+constexpr uint32_t kMagic = 0x31434245u;   // "EBC1"
+constexpr uint32_t kFormatVersion = 1;
+constexpr uint32_t kHeaderBytes = 144;
+constexpr uint32_t kTableRecBytes = 272;   // f32 eb, u32 n_lit, n_match, n_out, u8 len[256]
+constexpr uint32_t kSegRecBytes = 16;      // u32 word_off, chunk_base, match_base, out_base
+constexpr int kMaxT = 1024;
+constexpr int kMaxB = 16777215;
+
+// ---- decoder ----
+constexpr int kLutBits = 11;               // first-level decode table: 2^11 entries
+
+constexpr unsigned long long kEmptySlot = ~0ull;
+
+// Shape-derived constants of one call.
+struct Shape {
+  int64_t B;
+  int T;
+  int D;
+  int SB;         // rows per segment: max(32, 8192 / D)
+  int KC;         // literal rows per chunk: max(1, 128 / D)
+  int nseg;       // segments per table
+  int nw;         // bitmap words per table: ceil(B / 32)
+  uint32_t S;     // dedup slots per table (power of two >= 2B, >= 64)
+  int ref_bytes;  // 2 if B <= 65536 else 4
+};
+
+// Per-table absolute bounds of one compress call, passed by value.
+struct EbParams {
+  float eb[kMaxT];
+};
+
+// Device-resident state of a context.
+struct Glob {
+  unsigned int done;     // arrival counter of the last-block reductions
+  unsigned int cstat;    // (epoch << 8) | status of the last compress
+  unsigned int dstat;    // (epoch << 8) | status of the last decompress
+  unsigned int sticky;   // first device error since the last query (0 = none)
+  unsigned long long n_lit, n_match, n_out, n_chunks, words;
+  unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_out, off_bits, total;
+};
+
+// Decoder side tables of one table (canonical code).
+struct DecTab {
+  uint32_t first[kLmax + 1];   // first code of each length
+  uint32_t count[kLmax + 1];   // codes of each length
+  uint32_t offset[kLmax + 1];  // index of that first code in sorted[]
+  float ebx2;                  // 2 * eb
+  uint32_t pad[3];
+  uint8_t sorted[256];         // symbols by (length, symbol)
+};
+
+// Device scratch of a context.  Sizes follow Shape.
+struct Work {
+  uint8_t* sym;                // [T][B][D] quantization codes (table-major)
+  uint32_t* vhash;             // [T][B] dedup key
+  uint32_t* vnout;             // [T][B] outliers per vector
+  unsigned long long* slots;   // [T][S] (hash << 32 | first row)
+  uint32_t* bitmap;            // [T][nw] match bits
+  uint32_t* ref;               // [T][B] reference row (own row for literals)
+  uint32_t* seg_hist;          // [T*nseg][256] literal code histogram per segment
+  uint4* seg_cnt;              // [T*nseg] {literals, matches, outliers, chunks}
+  uint4* seg_off;              // [T*nseg] table-relative {words, chunks, matches, outliers}
+  uint32_t* seg_words;         // [T*nseg] bitstream words (multiple of 4)
+  uint32_t* tabcode;           // [T][256] code << 8 | length
+  uint4* tab_tot;              // [T] {words, chunks, matches, outliers}
+  uint32_t* tab_lits;          // [T]
+  uint4* tab_base;             // [T] absolute {words, chunks, matches, outliers}
+  uint16_t* lut;               // [T][1 << kLutBits] sym | len << 8 (len 0 = long code)
+  DecTab* dtab;                // [T]
+  Glob* glob;
+};
+
+// Error bits kept in Glob::sticky / status words.
+__host__ __device__ constexpr unsigned int status_word(uint32_t epoch, int code) {
+  return (epoch << 8) | (unsigned int)code;
+}
+
+// ---- small device helpers ----
+__device__ __forceinline__ uint32_t lowbias32(uint32_t v) {
+  // C. Wellons' 32-bit integer mixer "lowbias32" (hash-prospector).
+  v ^= v >> 16;
+  v *= 0x7feb352dU;
+  v ^= v >> 15;
+  v *= 0x846ca68bU;
+  v ^= v >> 16;
+  return v;
+}
+
+__device__ __forceinline__ void record_error(Glob* g, int code) {
+  atomicCAS(&g->sticky, 0u, (unsigned int)code);
+}
+
+__device__ __forceinline__ float4 ld_stream_f4(const float* p) {
+  // read-once input: evict-first streaming load
+  return __ldcs(reinterpret_cast<const float4*>(p));
+}
+
+template <int D>
+struct Geo {
+  static constexpr int kSB = (8192 / D) < 32 ? 32 : (8192 / D);   // rows per segment
+  static constexpr int kKC = (128 / D) < 1 ? 1 : (128 / D);       // rows per chunk
+  static constexpr int kLPR = D / 4 < 32 ? D / 4 : 32;            // lanes per row
+  static constexpr int kRPS = 32 / kLPR;                          // rows per 128-element slab
+  static constexpr int kSPR = D / 128 < 1 ? 1 : D / 128;          // slabs per row
+  static constexpr int kSlabs = kSB * D / 128;                    // slabs per segment
+  static constexpr int kSlabsPerWarp = kSlabs / 8;                // 8 warps per CTA
+  static constexpr int kRowsPerWarp = kSB / 8;
+  static constexpr int kBmWords = kSB / 32;                       // bitmap words per segment
+  static constexpr int kChunks = kSB / kKC;                       // max chunks per segment
+  static constexpr int kSegSyms = kSB * D;
+};
+
+// ---- optional per-kernel timing (host side, defined with the C ABI) ----
+struct Prof;
+void prof_begin(Prof* p, const char* name, cudaStream_t st);
+void prof_end(Prof* p, cudaStream_t st);
+
+// ---- launchers (one per direction; D is dispatched to the templated kernels) ----
+cudaError_t launch_compress(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
+                            unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch, cudaStream_t st,
+                            Prof* prof);
+cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const Shape& sh, const Work& w,
+                              float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof);
+cudaError_t set_kernel_attributes();
+
+}  // namespace ebc

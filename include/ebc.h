@@ -1,0 +1,189 @@
+/*
+ * ebc.h -- C ABI of the GB300 error-bounded embedding codec.
+ *
+ * The codec compresses the gathered embedding-lookup tensor (forward) or the
+ * embedding-gradient tensor (backward) x[B][T][D] (fp32, row-major, element
+ * (b,t,d) at ((b*T)+t)*D+d; T tables, batch B, embedding dim D) into one
+ * contiguous container, and decompresses it back, so that every element obeys
+ * the per-table absolute bound |x - xhat| <= eb[t].
+ *
+ * Method: "Accelerating Communication in Deep Learning Recommendation Model
+ * Training with Dual-Level Adaptive Lossy Compression" (arXiv 2407.04272):
+ *   - quantization encoder, no predictor ........ §III-D, §III-B observation 1
+ *   - vector-based LZ (whole-vector matches) ..... §III-D, §III-E "fixed pattern length"
+ *   - Huffman entropy encoder over the bins ...... §III-D "Optimized Entropy Encoding"
+ *   - table-wise and iteration-wise bounds ....... §III-C (Eq. 1, OnlineDecay), §IV-B Fig. 10
+ *   - one output buffer, metadata with sizes ..... §III-A stage 2, §III-E "Buffer Optimization"
+ *
+ * Pipeline (all on the GPU, on the caller's stream):
+ *   quantize:  q = round_half_even(x * fl32(1/(2 eb_t))), kept if |q| < 128 and
+ *              |x - fl32(q * 2 eb_t)| <= eb_t in fp32, else an outlier whose raw
+ *              32 bits are stored; code sym = q + 128 (1..255), 0 = outlier.
+ *   dedup:     within each table, a vector whose codes (and outlier bits) equal
+ *              those of an earlier vector of the batch is a match to the first
+ *              occurrence; the others are literals.
+ *   entropy:   per table, canonical Huffman code (longest code 24 bits) built on
+ *              the GPU from the literal codes' histogram; literal vectors are
+ *              written MSB-first into a bitstream with a chunk index.
+ *
+ * Container (little-endian, every section 16-byte aligned):
+ *   header 144 B | T table records (eb, counts, 256 code lengths; 272 B each)
+ *   | segment records (16 B each) | match bitmap (T x ceil(B/32) u32)
+ *   | chunk bit lengths (u16) | match references (u16 if B <= 65536, else u32)
+ *   | outlier raw bits (u32) | bitstream (u32 words)
+ * A segment is max(32, 8192/D) consecutive batch rows of one table; its bits
+ * start on a 128-bit boundary.  A chunk is max(1, 128/D) literal vectors of one
+ * segment, decoded by one GPU thread.
+ *
+ * Supported shapes: 0 <= B <= 16,777,215; 0 <= T <= 1024; D a power of two in
+ * [4, 512]; B*T*D < 2^32.  Device pointers must be 16-byte aligned.
+ *
+ * Ownership: the caller allocates and owns every input and output buffer.  A
+ * context owns its device scratch (grown on demand, which synchronises the
+ * device) and the error-bound schedule.  A context is not thread safe; use one
+ * per host thread.
+ *
+ * Errors: every call returns an EBC_* code.  The compress and decompress calls
+ * are asynchronous: argument errors are returned at once; errors found by the
+ * kernels (capacity too small, corrupt input) are recorded in the context and
+ * returned by the next ebc_last_device_error() or ebc_get_stats(), which
+ * synchronise the stream of the last call.
+ */
+#ifndef EBC_H
+#define EBC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define EBC_VERSION 1
+
+enum {
+  EBC_OK = 0,
+  EBC_ERR_INVALID_ARG = 1,    /* bad shape, pointer, bound or schedule        */
+  EBC_ERR_CAPACITY = 2,       /* output buffer smaller than the container     */
+  EBC_ERR_CORRUPT = 3,        /* container fails validation                   */
+  EBC_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out           */
+  EBC_ERR_CUDA = 5,           /* a CUDA runtime call failed                   */
+  EBC_ERR_NO_DEVICE = 6,      /* no usable sm_103 device                      */
+  EBC_ERR_INTERNAL = 7        /* an internal invariant failed on the device   */
+};
+
+/* Iteration-wise decay of the error bound, §III-C "Iteration-wise
+ * Configuration" and §IV-B Fig. 10.  factor(i) multiplies the base bound (it
+ * does not compound); P = phase_len, S = n_steps, m0 = initial multiplier:
+ *   LINEAR    m0 - (m0-1) * i/P
+ *   STEPWISE  m0 - (m0-1) * floor(i*S/P)/S     (the method's default)
+ *   DROP      m0                              (the "Drop_2x" experiment with m0 = 2)
+ *   LOG       m0^(1 - i/P)
+ * for 0 <= i < P, and 1 for i >= P, for NONE, or when P <= 0. */
+typedef enum {
+  EBC_DECAY_NONE = 0,
+  EBC_DECAY_LINEAR = 1,
+  EBC_DECAY_STEPWISE = 2,
+  EBC_DECAY_DROP = 3,
+  EBC_DECAY_LOG = 4
+} ebc_decay;
+
+typedef struct ebc_ctx ebc_ctx;
+
+/* Counts of the last completed compress call of a context. */
+typedef struct {
+  uint64_t in_bytes;        /* 4*B*T*D                                  */
+  uint64_t out_bytes;       /* container bytes                          */
+  uint64_t n_vectors;       /* B*T                                      */
+  uint64_t n_literal;       /* vectors entropy-coded                    */
+  uint64_t n_match;         /* vectors coded as a reference             */
+  uint64_t n_outlier;       /* raw values stored                        */
+  uint64_t n_chunks;        /* chunk-index entries                      */
+  uint64_t bitstream_bytes; /* bytes of the Huffman bitstream section   */
+} ebc_stats;
+
+/* Library version (EBC_VERSION). */
+int ebc_version(void);
+
+/* Human-readable text of an EBC_* code; never NULL. */
+const char* ebc_strerror(int code);
+
+/* Create a context on CUDA device `device` (must be sm_103).  *out receives
+ * the context; it is released with ebc_destroy.  Returns EBC_ERR_NO_DEVICE if
+ * the device is absent or not sm_103. */
+int ebc_create(ebc_ctx** out, int device);
+
+/* Release a context and its device scratch (synchronises the device).  NULL
+ * is accepted. */
+void ebc_destroy(ebc_ctx* ctx);
+
+/* Table-wise and iteration-wise bounds, §III-C: stores base bounds eb_base[T]
+ * (host array, absolute, each finite and > 0) and the schedule; the bound used
+ * by ebc_compress(eb = NULL) is fl32(eb_base[t] * factor(iteration)) with the
+ * factor computed in double.  Host-only; no device work. */
+int ebc_set_error_bounds(ebc_ctx* ctx, const float* eb_base, int T, int64_t iteration,
+                         int decay_fn, double m0, int64_t phase_len, int n_steps);
+
+/* Copy the current scheduled bounds (T of them) into eb_out (host). */
+int ebc_get_error_bounds(const ebc_ctx* ctx, float* eb_out, int T);
+
+/* Worst-case container bytes for a [B,T,D] input; 0 for an unsupported shape. */
+uint64_t ebc_compress_bound(int64_t B, int T, int D);
+
+/* Compress d_x[B][T][D] (device, fp32) with bounds eb[T] (host array; NULL =
+ * the context's schedule) into d_out (device, out_capacity bytes).  The
+ * container size is written to *d_out_bytes (device u64) by the kernels, also
+ * when it exceeds out_capacity (then nothing beyond the fixed-size head of the
+ * container is written and the context records EBC_ERR_CAPACITY).  `stream` is
+ * a cudaStream_t (NULL = legacy default stream).  Asynchronous: returns after
+ * the kernels are enqueued.  The input must not be modified until the stream
+ * reaches the end of the call. */
+int ebc_compress(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D, const float* eb,
+                 void* d_out, uint64_t out_capacity, uint64_t* d_out_bytes, void* stream);
+
+/* Decompress a container (device, in_bytes bytes) made for the same B, T, D
+ * into d_xhat[B][T][D] (device, fp32).  Asynchronous.  A container that fails
+ * validation makes the kernels stop without writing out of bounds and records
+ * EBC_ERR_CORRUPT (EBC_ERR_INVALID_ARG if its B, T, D differ from the
+ * arguments); d_xhat is then unspecified. */
+int ebc_decompress(ebc_ctx* ctx, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B,
+                   int T, int D, void* stream);
+
+/* Host-buffer variants (synchronous): the input is copied from host memory
+ * h_x (pinned memory is fastest) to context-owned device buffers, processed,
+ * and the result copied back.  ebc_compress_host writes the container to
+ * h_out (out_capacity bytes) and its size to *out_bytes; it returns
+ * EBC_ERR_CAPACITY (with *out_bytes = required size) when it does not fit.
+ * ebc_decompress_host reads in_bytes from h_in and writes h_xhat[B][T][D]. */
+int ebc_compress_host(ebc_ctx* ctx, const float* h_x, int64_t B, int T, int D, const float* eb,
+                      void* h_out, uint64_t out_capacity, uint64_t* out_bytes, void* stream);
+int ebc_decompress_host(ebc_ctx* ctx, const void* h_in, uint64_t in_bytes, float* h_xhat,
+                        int64_t B, int T, int D, void* stream);
+
+/* Counts of the last compress call (synchronises its stream).  Returns the
+ * recorded device error of the context, if any, as ebc_last_device_error. */
+int ebc_get_stats(ebc_ctx* ctx, ebc_stats* out);
+
+/* Synchronise the stream of the last call and return (and clear) the first
+ * error the kernels recorded since the previous query: EBC_OK,
+ * EBC_ERR_CAPACITY, EBC_ERR_CORRUPT, EBC_ERR_INVALID_ARG or EBC_ERR_INTERNAL. */
+int ebc_last_device_error(ebc_ctx* ctx);
+
+/* Per-kernel timing (tracing aid).  While enabled, every kernel launch of the
+ * context is bracketed by a pair of CUDA events on its stream (up to 2048
+ * launches between reads).  ebc_get_profile synchronises on the last event,
+ * writes one entry per kernel name (launch count and summed milliseconds) into
+ * out[capacity], sets *count, and clears the record. */
+typedef struct {
+  char name[32];
+  uint64_t launches;
+  double total_ms;
+} ebc_kernel_time;
+
+int ebc_set_profiling(ebc_ctx* ctx, int enable);
+int ebc_get_profile(ebc_ctx* ctx, ebc_kernel_time* out, int capacity, int* count);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* EBC_H */

@@ -1,0 +1,64 @@
+"""The C-ABI library builds for sm_103a, loads without a GPU and exports every
+entry point that include/ebc.h declares; host-only calls behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import error_bounded_lossy_gb300 as ebc
+import oracle
+from error_bounded_lossy_gb300 import build as ebc_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    ebc_build.build()
+    return ebc.lib()
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "ebc.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ebc_[a-z_]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("ebc_compress", "ebc_decompress", "ebc_set_error_bounds"):
+        assert required in names
+    assert set(names) == set(ebc.EXPORTED_SYMBOLS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {ebc.library_path()}").read()
+    exported = set(re.findall(r"\bT (ebc_[a-z_]+)\b", out))
+    assert set(declared_functions()) <= exported
+
+
+def test_host_only_calls(lib):
+    assert ebc.ebc_version() == 1
+    for code in range(8):
+        assert ebc.ebc_strerror(code)
+    assert ebc.ebc_strerror(99) == "unknown error"
+    # unsupported shapes
+    assert ebc.ebc_compress_bound(10, 2, 24) == 0
+    assert ebc.ebc_compress_bound(10, 2000, 16) == 0
+    assert ebc.ebc_compress_bound(1 << 24, 1, 16) == 0
+    # the worst-case bound agrees with the oracle's and covers real containers
+    for shape in [(0, 3, 16), (1, 1, 4), (512, 4, 16), (8192, 26, 128), (65536, 26, 256), (33, 2, 512)]:
+        assert ebc.ebc_compress_bound(*shape) == oracle.compress_bound(*shape)
+
+
+def test_create_without_device_reports_no_device(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    assert lib.ebc_create(ctypes.byref(h), 0) == ebc.EBC_ERR_NO_DEVICE
+    assert not h.value
+    assert lib.ebc_last_device_error(None) == ebc.EBC_ERR_INVALID_ARG
