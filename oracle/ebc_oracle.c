@@ -29,10 +29,10 @@
 #define O_RADIUS 128            /* bins q in (-R, R); sym = q + R          */
 #define O_LMAX 24               /* longest Huffman code                    */
 #define O_MAGIC 0x31434245u     /* bytes 'E' 'B' 'C' '1'                   */
-#define O_VERSION 1u
+#define O_VERSION 2u
 #define O_HEADER 144u
 #define O_TABLE_REC 272u        /* eb, n_lit, n_match, n_out, 256 lengths  */
-#define O_SEG_REC 16u           /* word_off, chunk_base, match_base, out_base */
+#define O_SEG_REC 16u           /* word_off, chunk_base, match_base, n_bits */
 #define O_MAX_T 1024
 
 static uint64_t pad16(uint64_t n) { return (n + 15u) & ~(uint64_t)15u; }
@@ -248,14 +248,16 @@ double ebo_decay_factor(int fn, int64_t iter, double m0, int64_t P, int S) {
  * Container layout (all little-endian, sections 16-byte aligned):
  *   header (144 B) | T table records (272 B) | T*nseg segment records (16 B)
  *   | match bitmap T*ceil(B/32) u32 | chunk lengths u16 | refs u16/u32
- *   | outlier raw bits u32 | bitstream u32 words
+ *   | bitstream u32 words
+ * An outlier is coded inline: the code of symbol 0, then the 32 raw bits of
+ * the value, MSB first.
  * ---------------------------------------------------------------------- */
 typedef struct {
-  uint64_t off_seg, off_bitmap, off_chunks, off_refs, off_out, off_bits, total;
+  uint64_t off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
 } layout_t;
 
 static layout_t make_layout(int64_t B, int T, int D, uint64_t n_chunks, uint64_t n_match,
-                            uint64_t n_out, uint64_t words, int ref_bytes) {
+                            uint64_t words, int ref_bytes) {
   layout_t L;
   int64_t nseg = (B + seg_rows(D) - 1) / seg_rows(D);
   int64_t nw = (B + 31) / 32;
@@ -263,8 +265,7 @@ static layout_t make_layout(int64_t B, int T, int D, uint64_t n_chunks, uint64_t
   L.off_bitmap = L.off_seg + (uint64_t)T * (uint64_t)nseg * O_SEG_REC;
   L.off_chunks = L.off_bitmap + pad16((uint64_t)T * (uint64_t)nw * 4u);
   L.off_refs = L.off_chunks + pad16(n_chunks * 2u);
-  L.off_out = L.off_refs + pad16(n_match * (uint64_t)ref_bytes);
-  L.off_bits = L.off_out + pad16(n_out * 4u);
+  L.off_bits = L.off_refs + pad16(n_match * (uint64_t)ref_bytes);
   L.total = L.off_bits + words * 4u;
   return L;
 }
@@ -281,8 +282,8 @@ uint64_t ebo_compress_bound(int64_t B, int T, int D) {
   uint64_t N = (uint64_t)B * T * D;
   int64_t nseg = (B + seg_rows(D) - 1) / seg_rows(D);
   uint64_t vec = (uint64_t)B * T;
-  uint64_t words = (N * O_LMAX + 31) / 32 + 4u * (uint64_t)T * (uint64_t)nseg;
-  layout_t L = make_layout(B, T, D, vec, vec, N, words, B <= 65536 ? 2 : 4);
+  uint64_t words = (N * (O_LMAX + 32) + 31) / 32 + 4u * (uint64_t)T * (uint64_t)nseg;
+  layout_t L = make_layout(B, T, D, vec, vec, words, B <= 65536 ? 2 : 4);
   return L.total;
 }
 
@@ -386,14 +387,14 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8
         for (int d = 0; d < D; ++d) {
           uint8_t c = sym[((size_t)t * B + b) * D + d];
           bits += lens[(size_t)t * 256 + c];
-          if (c == 0) ++n_out;
+          if (c == 0) { ++n_out; bits += 32; }
         }
       }
       n_lit += lits;
       n_chunks += (lits + (uint64_t)KC - 1) / (uint64_t)KC;
       words += ((bits + 127) / 128) * 4;
     }
-  layout_t L = make_layout(B, T, D, n_chunks, n_match, n_out, words, ref_bytes);
+  layout_t L = make_layout(B, T, D, n_chunks, n_match, words, ref_bytes);
   if (info) {
     info->n_literal = n_lit; info->n_match = n_match; info->n_outlier = n_out;
     info->n_chunks = n_chunks; info->bitstream_bytes = words * 4; info->total_bytes = L.total;
@@ -415,18 +416,18 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8
   wr32(h + 40, (uint32_t)ref_bytes); wr32(h + 44, 0);
   wr64(h + 48, n_lit); wr64(h + 56, n_match); wr64(h + 64, n_out); wr64(h + 72, n_chunks);
   wr64(h + 80, words); wr64(h + 88, L.off_seg); wr64(h + 96, L.off_bitmap);
-  wr64(h + 104, L.off_chunks); wr64(h + 112, L.off_refs); wr64(h + 120, L.off_out);
-  wr64(h + 128, L.off_bits); wr64(h + 136, L.total);
+  wr64(h + 104, L.off_chunks); wr64(h + 112, L.off_refs); wr64(h + 120, L.off_bits);
+  wr64(h + 128, L.total); wr64(h + 136, 0);
 
   uint32_t* stream = (uint32_t*)calloc((size_t)(words ? words : 1), 4);
-  uint64_t chunk_i = 0, match_i = 0, out_i = 0, word_i = 0;
+  uint64_t chunk_i = 0, match_i = 0, word_i = 0;
   for (int t = 0; t < T; ++t) {
     uint8_t* rec = out + O_HEADER + (size_t)t * O_TABLE_REC;
     uint32_t tl = 0, tm = 0, to = 0;
     for (int64_t s = 0; s < nseg; ++s) {
       uint8_t* srec = out + L.off_seg + ((size_t)t * nseg + s) * O_SEG_REC;
       wr32(srec + 0, (uint32_t)word_i); wr32(srec + 4, (uint32_t)chunk_i);
-      wr32(srec + 8, (uint32_t)match_i); wr32(srec + 12, (uint32_t)out_i);
+      wr32(srec + 8, (uint32_t)match_i);
       uint64_t pos = word_i * 32, lit_in_seg = 0, chunk_start = pos;
       int64_t b_end = (s + 1) * SB < B ? (s + 1) * SB : B;
       for (int64_t b = s * SB; b < b_end; ++b) {
@@ -443,7 +444,7 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8
         const float* xv = x + ((size_t)b * T + t) * D;
         for (int d = 0; d < D; ++d) {
           put_bits(stream, &pos, codes[(size_t)t * 256 + sv[d]], lens[(size_t)t * 256 + sv[d]]);
-          if (sv[d] == 0) { wr32(out + L.off_out + out_i * 4, f2u(xv[d])); ++out_i; ++to; }
+          if (sv[d] == 0) { put_bits(stream, &pos, f2u(xv[d]), 32); ++to; }
         }
         ++lit_in_seg; ++tl;
         if (lit_in_seg % (uint64_t)KC == 0) {        /* a chunk holds KC literals */
@@ -455,6 +456,7 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8
         wr16(out + L.off_chunks + chunk_i * 2, (uint32_t)(pos - chunk_start));
         ++chunk_i; chunk_start = pos;
       }
+      wr32(srec + 12, (uint32_t)(pos - word_i * 32));
       word_i += ((pos - word_i * 32 + 127) / 128) * 4;
     }
     wr32(rec + 0, f2u(eb[t])); wr32(rec + 4, tl); wr32(rec + 8, tm); wr32(rec + 12, to);
@@ -514,10 +516,10 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
   if (n_lit + n_match != nvec || n_chunks > nvec || n_out > nvec * (uint64_t)D ||
       words > ((uint64_t)1 << 34))
     return EBO_ERR_CORRUPT;
-  layout_t L = make_layout(B, T, D, n_chunks, n_match, n_out, words, ref_bytes);
+  layout_t L = make_layout(B, T, D, n_chunks, n_match, words, ref_bytes);
   if (rd64(in + 88) != L.off_seg || rd64(in + 96) != L.off_bitmap || rd64(in + 104) != L.off_chunks ||
-      rd64(in + 112) != L.off_refs || rd64(in + 120) != L.off_out || rd64(in + 128) != L.off_bits ||
-      rd64(in + 136) != L.total || L.total > in_bytes)
+      rd64(in + 112) != L.off_refs || rd64(in + 120) != L.off_bits || rd64(in + 128) != L.total ||
+      rd64(in + 136) != 0 || L.total > in_bytes)
     return EBO_ERR_CORRUPT;
 
   const size_t N = (size_t)nvec * (size_t)D;
@@ -534,8 +536,10 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
     uint32_t tl = 0, tm = 0, to = 0;
     for (int64_t s = 0; s < nseg && err == EBO_OK; ++s) {
       const uint8_t* srec = in + L.off_seg + ((size_t)t * nseg + s) * O_SEG_REC;
-      if (rd32(srec) != word_i || rd32(srec + 4) != chunk_i || rd32(srec + 8) != match_i ||
-          rd32(srec + 12) != out_i) { err = EBO_ERR_CORRUPT; break; }
+      if (rd32(srec) != word_i || rd32(srec + 4) != chunk_i || rd32(srec + 8) != match_i) {
+        err = EBO_ERR_CORRUPT;
+        break;
+      }
       int64_t b_end = (s + 1) * SB < B ? (s + 1) * SB : B;
       uint64_t seg_bit0 = word_i * 32, pos = seg_bit0, lit_in_seg = 0, chunk_start = pos;
       uint64_t seg_lits = 0;
@@ -565,8 +569,15 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
           if (err) break;
           float v;
           if (sv[d] == 0) {
-            if (out_i >= n_out) { err = EBO_ERR_CORRUPT; break; }
-            v = u2f(rd32(in + L.off_out + out_i * 4));
+            uint32_t raw = 0;
+            for (int k = 0; k < 32; ++k) {
+              if (pos >= chunk_end || pos >= words * 32) { err = EBO_ERR_CORRUPT; break; }
+              uint32_t word = rd32(in + L.off_bits + (pos >> 5) * 4);
+              raw = (raw << 1) | ((word >> (31 - (pos & 31))) & 1u);
+              ++pos;
+            }
+            if (err) break;
+            v = u2f(raw);
             ++out_i; ++to;
           } else {
             v = ebo_dequantize(sv[d], eb);
@@ -586,6 +597,7 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
         const uint8_t* bm = in + L.off_bitmap + ((size_t)t * nw + (size_t)(nw - 1)) * 4;
         if (rd32(bm) >> (B & 31)) { err = EBO_ERR_CORRUPT; break; }
       }
+      if (rd32(srec + 12) != (uint32_t)(pos - seg_bit0)) { err = EBO_ERR_CORRUPT; break; }
       word_i += ((pos - seg_bit0 + 127) / 128) * 4;
       if (word_i > words) { err = EBO_ERR_CORRUPT; break; }
     }

@@ -325,26 +325,44 @@ def test_container_worked_by_hand():
     # Stream: 0 11 10 0 -> bits 011100 -> word 0x70000000, padded to 128 bits.
     # Layout: header 144, table record 272 -> segments at 416 (1 x 16 B), bitmap at 432
     # (1 word, padded to 16), chunk lengths at 448 (1 x u16 = 6), refs at 464 (u16 0),
-    # outliers at 480 (none), bitstream at 480 (4 words), total 496.
+    # bitstream at 480 (4 words), total 496.
     x = np.array([[[0.0, 1.0, -1.0, 0.5]], [[0.0, 1.0, -1.0, 0.5]]], np.float32)
     buf, info = o.compress(x, np.array([0.5], np.float32))
     assert len(buf) == 496
     hdr = struct.unpack_from("<4sIQIIIIIIIIQQQQQQQQQQQQ", buf.tobytes(), 0)
-    assert hdr[0] == b"EBC1" and hdr[1] == 1 and hdr[2:5] == (2, 1, 4)
+    assert hdr[0] == b"EBC1" and hdr[1] == 2 and hdr[2:5] == (2, 1, 4)
     assert hdr[5:11] == (128, 24, 2048, 32, 2, 0)
     assert hdr[11:16] == (1, 1, 0, 1, 4)                 # lit, match, outliers, chunks, words
-    assert hdr[16:] == (416, 432, 448, 464, 480, 480, 496)
+    assert hdr[16:] == (416, 432, 448, 464, 480, 496, 0)
     b = buf.tobytes()
     assert struct.unpack_from("<fIII", b, 144) == (0.5, 1, 1, 0)
     lens = np.frombuffer(b, np.uint8, 256, 160)
     assert lens[127] == 2 and lens[128] == 1 and lens[129] == 2 and lens.sum() == 5
-    assert struct.unpack_from("<IIII", b, 416) == (0, 0, 0, 0)
+    assert struct.unpack_from("<IIII", b, 416) == (0, 0, 0, 6)   # word, chunk, match base; bits
     assert struct.unpack_from("<I", b, 432) == (0b10,)
     assert struct.unpack_from("<H", b, 448) == (6,)
     assert struct.unpack_from("<H", b, 464) == (0,)
     assert struct.unpack_from("<IIII", b, 480) == (0x70000000, 0, 0, 0)
     xh, sym = o.decompress(buf, 2, 1, 4)
     assert xh.tolist() == [[[0.0, 1.0, -1.0, 0.0]], [[0.0, 1.0, -1.0, 0.0]]]
+
+
+def test_outlier_inline_worked_by_hand():
+    # B=1, T=1, D=4, eb=0.5: codes 128, 0 (1000.0 is |q| >= 128), 129, 128.  Histogram
+    # {0:1, 128:2, 129:1}; leaves by (f, sym): 0, 129, 128 -> 0+129 merge, then leaf 128 ties
+    # the node and goes first: lengths 128:1, 0:2, 129:2; canonical 128='0', 0='10', 129='11'.
+    # Stream: '0' + '10' + 32 raw bits of 1000.0 (0x447A0000) + '11' + '0' = 38 bits.
+    x = np.array([[[0.0, 1000.0, 1.0, 0.0]]], np.float32)
+    buf, info = o.compress(x, np.array([0.5], np.float32))
+    # layout: header 144 + table 272 + segment 16 + bitmap 16 + chunks 16 + refs 0 -> bits at 464
+    assert info["n_outlier"] == 1 and len(buf) == 480
+    bits = "0" + "10" + format(0x447A0000, "032b") + "11" + "0"
+    bits = bits.ljust(128, "0")
+    words = [int(bits[i:i + 32], 2) for i in range(0, 128, 32)]
+    assert struct.unpack_from("<IIII", buf.tobytes(), 464) == tuple(words)
+    assert struct.unpack_from("<H", buf.tobytes(), 448) == (38,)
+    xh, _ = o.decompress(buf, 1, 1, 4)
+    assert xh.tolist() == [[[0.0, 1000.0, 1.0, 0.0]]]
 
 
 @pytest.mark.parametrize("B,T,D", [(1, 1, 4), (33, 2, 8), (100, 3, 16), (70, 2, 32), (64, 1, 64),
