@@ -51,7 +51,12 @@ struct ebc_ctx {
   void* stage_out = nullptr;
   size_t stage_out_bytes = 0;
   unsigned long long* d_nbytes = nullptr;
-  uint32_t cepoch = 0, depoch = 0;
+  uint32_t cepoch = 0, depoch = 0, sepoch = 0;
+  int nsm = 0;
+  // the compress layout whose dedup table and look-back flags are known clean
+  const void* clean_buf = nullptr;
+  int64_t cleanB = -1;
+  int cleanT = -1, cleanD = -1;
   // schedule
   float* eb_base = nullptr;
   float* eb_now = nullptr;
@@ -72,8 +77,9 @@ static bool shape_ok(int64_t B, int T, int D) {
   return (uint64_t)B * (uint64_t)T * (uint64_t)D <= 0xFFFFFFFFull;
 }
 
-static Shape make_shape(int64_t B, int T, int D) {
+static Shape make_shape(int64_t B, int T, int D, int nsm = 0) {
   Shape sh;
+  sh.nsm = nsm;
   sh.B = B;
   sh.T = T;
   sh.D = D;
@@ -129,20 +135,20 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   Carver c{reinterpret_cast<char*>(buf)};
   Work w{};
   const size_t nvec = (size_t)sh.B * sh.T, nsegT = (size_t)sh.T * sh.nseg;
+  w.slots = c.take<unsigned long long>(8 * (size_t)sh.T * sh.S);
+  w.seg_flag = c.take<uint32_t>(4 * nsegT);
   w.sym = c.take<uint8_t>(nvec * sh.D);
   w.vhash = c.take<uint32_t>(4 * nvec);
   w.vnout = c.take<uint32_t>(4 * nvec);
   w.ref = c.take<uint32_t>(4 * nvec);
-  w.slots = c.take<unsigned long long>(8 * (size_t)sh.T * sh.S);
   w.bitmap = c.take<uint32_t>(4 * (size_t)sh.T * sh.nw);
   w.seg_hist = c.take<uint32_t>(1024 * nsegT);
   w.seg_cnt = c.take<uint4>(16 * nsegT);
-  w.seg_off = c.take<uint4>(16 * nsegT);
-  w.seg_words = c.take<uint32_t>(4 * nsegT);
+  w.seg_agg = c.take<uint4>(16 * nsegT);
+  w.seg_incl = c.take<uint4>(16 * nsegT);
+  w.tab_hist = c.take<uint32_t>(1024 * (size_t)sh.T);
+  w.tab_cnt = c.take<uint4>(16 * (size_t)sh.T);
   w.tabcode = c.take<uint32_t>(1024 * (size_t)sh.T);
-  w.tab_tot = c.take<uint4>(16 * (size_t)sh.T);
-  w.tab_lits = c.take<uint32_t>(4 * (size_t)sh.T);
-  w.tab_base = c.take<uint4>(16 * (size_t)sh.T);
   w.glob = g;
   *total = c.off;
   return w;
@@ -151,8 +157,12 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
 static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   Carver c{reinterpret_cast<char*>(buf)};
   Work w{};
+  const size_t nsegT = (size_t)sh.T * sh.nseg;
+  const size_t max_chunks = nsegT * (size_t)(sh.SB / sh.KC);
   w.lut = c.take<uint16_t>(2u * (1u << kLutBits) * (size_t)sh.T);
   w.dtab = c.take<DecTab>(sizeof(DecTab) * (size_t)sh.T);
+  w.cdesc = c.take<uint4>(16 * max_chunks);
+  w.litrow = c.take<uint16_t>(2 * nsegT * (size_t)sh.SB);
   w.glob = g;
   *total = c.off;
   return w;
@@ -208,6 +218,7 @@ int ebc_create(ebc_ctx** out, int device) {
   ebc_ctx* c = new (std::nothrow) ebc_ctx();
   if (!c) return EBC_ERR_INTERNAL;
   c->device = device;
+  c->nsm = prop.multiProcessorCount;
   if (cudaMalloc(&c->glob, sizeof(Glob)) != cudaSuccess || cudaMemset(c->glob, 0, sizeof(Glob)) != cudaSuccess ||
       cudaMalloc(&c->d_nbytes, 16) != cudaSuccess || cudaMallocHost(&c->h_pinned, 64) != cudaSuccess) {
     ebc_destroy(c);
@@ -302,8 +313,8 @@ uint64_t ebc_compress_bound(int64_t B, int T, int D) {
   if (!shape_ok(B, T, D)) return 0;
   const Shape sh = make_shape(B, T, D);
   const uint64_t N = (uint64_t)B * T * D, nvec = (uint64_t)B * T;
-  const uint64_t words = (N * kLmax + 31) / 32 + 4ull * T * sh.nseg;
-  return fixed_bytes(sh) + pad16h(nvec * 2u) + pad16h(nvec * sh.ref_bytes) + pad16h(N * 4u) + words * 4u;
+  const uint64_t words = (N * (kLmax + 32) + 31) / 32 + 4ull * T * sh.nseg;
+  return fixed_bytes(sh) + pad16h(nvec * 2u) + pad16h(nvec * sh.ref_bytes) + words * 4u;
 }
 
 int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, void* d_out,
@@ -324,7 +335,7 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
     if (!eb_ok(ebs[t])) return EBC_ERR_INVALID_ARG;
     ep.eb[t] = ebs[t];
   }
-  const Shape sh = make_shape(B, T, D);
+  const Shape sh = make_shape(B, T, D, c->nsm);
   if (out_capacity < fixed_bytes(sh)) return EBC_ERR_CAPACITY;
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
@@ -335,14 +346,25 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
   c->cepoch = (c->cepoch + 1) & 0xFFFFFFu;
+  c->sepoch = c->sepoch + 1 >= (1u << 30) ? 1u : c->sepoch + 1;
   c->lastB = B;
   c->lastT = T;
   c->lastD = D;
-  if (T > 0 && sh.nseg > 0 &&
-      cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess)
-    return EBC_ERR_CUDA;
-  return cuda_err(launch_compress(d_x, sh, ep, w, (uint8_t*)d_out, out_capacity,
-                                  (unsigned long long*)d_out_bytes, c->cepoch, st, c->prof));
+  // Each call leaves its dedup table empty (k_codebook) and its look-back flags
+  // tagged with its own epoch.  A new layout on this buffer starts from a reset.
+  if (T > 0 && sh.nseg > 0 && (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D)) {
+    if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess ||
+        cudaMemsetAsync(w.seg_flag, 0, 4 * (size_t)T * sh.nseg, st) != cudaSuccess)
+      return EBC_ERR_CUDA;
+    c->clean_buf = c->cbuf;
+    c->cleanB = B;
+    c->cleanT = T;
+    c->cleanD = D;
+  }
+  const cudaError_t e = launch_compress(d_x, sh, ep, w, (uint8_t*)d_out, out_capacity,
+                                        (unsigned long long*)d_out_bytes, c->cepoch, c->sepoch, st, c->prof);
+  if (e != cudaSuccess) c->clean_buf = nullptr;   // the dedup table may be left dirty
+  return cuda_err(e);
 }
 
 int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
@@ -350,7 +372,7 @@ int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xha
   if (!c || !shape_ok(B, T, D) || !d_in || !aligned16(d_in)) return EBC_ERR_INVALID_ARG;
   const uint64_t N = (uint64_t)B * T * D;
   if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
-  const Shape sh = make_shape(B, T, D);
+  const Shape sh = make_shape(B, T, D, c->nsm);
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
   carve_decompress(nullptr, sh, c->glob, &need);

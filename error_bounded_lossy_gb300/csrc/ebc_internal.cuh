@@ -13,10 +13,10 @@ namespace ebc {
 constexpr int kRadius = 128;               // codes q + 128 for |q| < 128; 0 = outlier
 constexpr int kLmax = 24;                  // longest Huffman code
 constexpr uint32_t kMagic = 0x31434245u;   // "EBC1"
-constexpr uint32_t kFormatVersion = 1;
+constexpr uint32_t kFormatVersion = 2;
 constexpr uint32_t kHeaderBytes = 144;
 constexpr uint32_t kTableRecBytes = 272;   // f32 eb, u32 n_lit, n_match, n_out, u8 len[256]
-constexpr uint32_t kSegRecBytes = 16;      // u32 word_off, chunk_base, match_base, out_base
+constexpr uint32_t kSegRecBytes = 16;      // u32 word_off, chunk_base, match_base, n_bits
 constexpr int kMaxT = 1024;
 constexpr int kMaxB = 16777215;
 
@@ -36,6 +36,7 @@ struct Shape {
   int nw;         // bitmap words per table: ceil(B / 32)
   uint32_t S;     // dedup slots per table (power of two >= 2B, >= 64)
   int ref_bytes;  // 2 if B <= 65536 else 4
+  int nsm;        // SMs of the device (grid sizing)
 };
 
 // Per-table absolute bounds of one compress call, passed by value.
@@ -45,12 +46,14 @@ struct EbParams {
 
 // Device-resident state of a context.
 struct Glob {
-  unsigned int done;     // arrival counter of the last-block reductions
-  unsigned int cstat;    // (epoch << 8) | status of the last compress
-  unsigned int dstat;    // (epoch << 8) | status of the last decompress
-  unsigned int sticky;   // first device error since the last query (0 = none)
+  unsigned int done;      // arrival counter of the last-block reductions
+  unsigned int cstat;     // (epoch << 8) | status of the last compress
+  unsigned int dstat;     // (epoch << 8) | status of the last decompress
+  unsigned int sticky;    // first device error since the last query (0 = none)
+  unsigned int tile_ctr;  // next segment of k_emit (dynamic, in scheduling order)
+  unsigned int pad[3];
   unsigned long long n_lit, n_match, n_out, n_chunks, words;
-  unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_out, off_bits, total;
+  unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
 };
 
 // Decoder side tables of one table (canonical code).
@@ -65,22 +68,26 @@ struct DecTab {
 
 // Device scratch of a context.  Sizes follow Shape.
 struct Work {
+  // compress
   uint8_t* sym;                // [T][B][D] quantization codes (table-major)
   uint32_t* vhash;             // [T][B] dedup key
   uint32_t* vnout;             // [T][B] outliers per vector
-  unsigned long long* slots;   // [T][S] (hash << 32 | first row)
+  unsigned long long* slots;   // [T][S] (hash << 32 | first row); all ones = empty
   uint32_t* bitmap;            // [T][nw] match bits
-  uint32_t* ref;               // [T][B] reference row (own row for literals)
+  uint32_t* ref;               // [T][B] reference row of matched rows
   uint32_t* seg_hist;          // [T*nseg][256] literal code histogram per segment
   uint4* seg_cnt;              // [T*nseg] {literals, matches, outliers, chunks}
-  uint4* seg_off;              // [T*nseg] table-relative {words, chunks, matches, outliers}
-  uint32_t* seg_words;         // [T*nseg] bitstream words (multiple of 4)
+  uint32_t* seg_flag;          // [T*nseg] look-back state: (scan epoch << 2) | 1 aggregate / 2 inclusive
+  uint4* seg_agg;              // [T*nseg] {words, chunks, matches, 0}
+  uint4* seg_incl;             // [T*nseg] inclusive prefix of seg_agg in (table, segment) order
+  uint32_t* tab_hist;          // [T][256] literal code histogram per table
+  uint4* tab_cnt;              // [T] {literals, matches, outliers, chunks}
   uint32_t* tabcode;           // [T][256] code << 8 | length
-  uint4* tab_tot;              // [T] {words, chunks, matches, outliers}
-  uint32_t* tab_lits;          // [T]
-  uint4* tab_base;             // [T] absolute {words, chunks, matches, outliers}
+  // decompress
   uint16_t* lut;               // [T][1 << kLutBits] sym | len << 8 (len 0 = long code)
   DecTab* dtab;                // [T]
+  uint4* cdesc;                // [T*nseg*chunks] {start bit lo, start bit hi, segment, first literal | rows << 16}
+  uint16_t* litrow;            // [T*nseg][SB] literal rows of each segment, in row order
   Glob* glob;
 };
 
@@ -131,8 +138,8 @@ void prof_end(Prof* p, cudaStream_t st);
 
 // ---- launchers (one per direction; D is dispatched to the templated kernels) ----
 cudaError_t launch_compress(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
-                            unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch, cudaStream_t st,
-                            Prof* prof);
+                            unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
+                            uint32_t scan_epoch, cudaStream_t st, Prof* prof);
 cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const Shape& sh, const Work& w,
                               float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof);
 cudaError_t set_kernel_attributes();
