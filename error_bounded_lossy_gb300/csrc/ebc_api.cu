@@ -74,7 +74,7 @@ static bool dim_ok(int D) { return D >= 4 && D <= 512 && (D & (D - 1)) == 0; }
 
 static bool shape_ok(int64_t B, int T, int D) {
   if (B < 0 || B > kMaxB || T < 0 || T > kMaxT || !dim_ok(D)) return false;
-  return (uint64_t)B * (uint64_t)T * (uint64_t)D <= 0xFFFFFFFFull;
+  return (uint64_t)B * (uint64_t)T * (uint64_t)D <= (1ull << 31);
 }
 
 static Shape make_shape(int64_t B, int T, int D, int nsm = 0) {
@@ -136,7 +136,7 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   Work w{};
   const size_t nvec = (size_t)sh.B * sh.T, nsegT = (size_t)sh.T * sh.nseg;
   w.slots = c.take<unsigned long long>(8 * (size_t)sh.T * sh.S);
-  w.seg_flag = c.take<uint32_t>(4 * nsegT);
+  w.seg_desc = c.take<uint4>(16 * nsegT);
   w.sym = c.take<uint8_t>(nvec * sh.D);
   w.vhash = c.take<uint32_t>(4 * nvec);
   w.vnout = c.take<uint32_t>(4 * nvec);
@@ -144,8 +144,6 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   w.bitmap = c.take<uint32_t>(4 * (size_t)sh.T * sh.nw);
   w.seg_hist = c.take<uint32_t>(1024 * nsegT);
   w.seg_cnt = c.take<uint4>(16 * nsegT);
-  w.seg_agg = c.take<uint4>(16 * nsegT);
-  w.seg_incl = c.take<uint4>(16 * nsegT);
   w.tab_hist = c.take<uint32_t>(1024 * (size_t)sh.T);
   w.tab_cnt = c.take<uint4>(16 * (size_t)sh.T);
   w.tabcode = c.take<uint32_t>(1024 * (size_t)sh.T);
@@ -163,6 +161,7 @@ static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total)
   w.dtab = c.take<DecTab>(sizeof(DecTab) * (size_t)sh.T);
   w.cdesc = c.take<uint4>(16 * max_chunks);
   w.litrow = c.take<uint16_t>(2 * nsegT * (size_t)sh.SB);
+  w.mdesc = c.take<uint2>(8 * (size_t)sh.B * (size_t)sh.T);
   w.glob = g;
   *total = c.off;
   return w;
@@ -354,7 +353,7 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
   // tagged with its own epoch.  A new layout on this buffer starts from a reset.
   if (T > 0 && sh.nseg > 0 && (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D)) {
     if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess ||
-        cudaMemsetAsync(w.seg_flag, 0, 4 * (size_t)T * sh.nseg, st) != cudaSuccess)
+        cudaMemsetAsync(w.seg_desc, 0, 16 * (size_t)T * sh.nseg, st) != cudaSuccess)
       return EBC_ERR_CUDA;
     c->clean_buf = c->cbuf;
     c->cleanB = B;

@@ -550,75 +550,97 @@ __device__ __forceinline__ void put_bits(uint32_t* s, uint32_t p, uint32_t code,
   if (lo) atomicOr(&s[(p >> 5) + 1], lo);
 }
 
-// Decoupled look-back over segments in (table, segment) order, by one warp:
-// returns the sum of the aggregates of all earlier segments.  Each wait on a
-// flag is bounded; on time-out the segment counts as zero and the context
-// records EBC_ERR_DEVICE_TIMEOUT.
-__device__ uint4 lookback(const Work& w, int seg, uint32_t sepoch) {
-  const int lane = threadIdx.x & 31;
+// Look-back descriptors: {(scan epoch << 2) | state, words, chunks, matches},
+// state 1 = aggregate of the segment alone, 2 = inclusive prefix.  Each is
+// written and read with one 16-byte access, so status and values never tear
+// apart and no fence is needed between them.
+__device__ __forceinline__ void st_desc(uint4* p, uint4 v) {
+  asm volatile("st.volatile.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+               "r"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_desc(const uint4* p) {
+  uint4 v;
+  asm volatile("ld.volatile.global.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+// Decoupled look-back over segments in (table, segment) order, by the whole
+// CTA: thread k inspects segment seg-1-k of the current window of 256, so the
+// known-prefix frontier advances by up to 256 segments per round trip.  Returns
+// the sum {0, words, chunks, matches} of all earlier segments.  Each wait is
+// bounded; on time-out that segment counts as zero and the context records
+// EBC_ERR_DEVICE_TIMEOUT.
+__device__ uint4 lookback(const Work& w, int seg, uint32_t sepoch, uint4* s_warp, int* s_stop) {
+  const int tid = threadIdx.x;
   uint4 excl = make_uint4(0, 0, 0, 0);
-  int j = seg - 1;
-  while (j >= 0) {
-    const int k = j - lane;
+  for (int j = seg - 1; j >= 0; j -= 256) {
+    const int k = j - tid;
     uint32_t st = 2u;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (k >= 0) {
-      const volatile uint32_t* fp = w.seg_flag + k;
-      uint32_t f = *fp;
-      for (int spin = 0; (f >> 2) != sepoch && spin < kSpinLimit; ++spin) {
-        __nanosleep(32);
-        f = *fp;
+      v = ld_desc(w.seg_desc + k);
+      for (int spin = 0; (v.x >> 2) != sepoch && spin < kSpinLimit; ++spin) {
+        __nanosleep(64);
+        v = ld_desc(w.seg_desc + k);
       }
-      if ((f >> 2) != sepoch) {
+      if ((v.x >> 2) != sepoch) {
         record_error(w.glob, EBC_ERR_DEVICE_TIMEOUT);
+        v = make_uint4(0, 0, 0, 0);
       } else {
-        st = f & 3u;
-        __threadfence();
-        v = st == 2u ? __ldcg(w.seg_incl + k) : __ldcg(w.seg_agg + k);
+        st = v.x & 3u;
       }
+      v.x = 0;
     }
-    const unsigned incl = __ballot_sync(0xffffffffu, st == 2u);
-    const int stop = incl ? __ffs(incl) - 1 : 31;
-    if (lane > stop) v = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      v.x += __shfl_xor_sync(0xffffffffu, v.x, off);
-      v.y += __shfl_xor_sync(0xffffffffu, v.y, off);
-      v.z += __shfl_xor_sync(0xffffffffu, v.z, off);
-      v.w += __shfl_xor_sync(0xffffffffu, v.w, off);
-    }
-    excl = add4(excl, v);
-    if (incl) break;
-    j -= 32;
+    if (tid == 0) *s_stop = 256;
+    __syncthreads();
+    if (st == 2u) atomicMin(s_stop, tid);   // the nearest segment with a known inclusive prefix
+    __syncthreads();
+    const int stop = *s_stop;
+    if (tid > stop) v = make_uint4(0, 0, 0, 0);
+    uint4 tot;
+    block_excl_scan4(v, &tot, s_warp);
+    excl = add4(excl, tot);
+    if (stop < 256) break;
   }
   return excl;
+}
+
+// Rows of bitmap word wi of a segment that exist in the batch.
+__device__ __forceinline__ uint32_t valid_mask(int64_t B, int64_t row0, int wi) {
+  const int64_t nv = B - (row0 + (int64_t)wi * 32);
+  return nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
 }
 
 // ---------------------------------------------------------------------------
 // k_emit: one CTA per segment, taken in scheduling order.  The segment's bit
 // count comes from its histogram and the code lengths, so its aggregate
-// (words, chunks, matches) is published at once; the look-back then gives its
-// absolute offsets.  Codes (and the 32 raw bits after each outlier code) are
-// written MSB-first into a shared-memory copy of the segment's bitstream and
-// stored with 16-byte writes.
+// (words, chunks, matches) is published at once and the look-back gives its
+// absolute offsets before any encoding.  Only literal rows are visited.
+// Codes (and the 32 raw bits after each outlier code) are written MSB-first
+// into a shared-memory copy of the segment's bitstream and stored with 16-byte
+// writes; a segment larger than that copy (24 bits per code on average) is
+// written with atomic ORs straight into the zeroed output instead.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) k_emit(const float* __restrict__ x, Shape sh, Work w,
                                                uint8_t* __restrict__ out, unsigned long long cap,
                                                unsigned long long* out_bytes, uint32_t epoch, uint32_t sepoch) {
   using G = Geo<D>;
-  constexpr int kIters = G::kRowsPerWarp / G::kRPS;
+  constexpr uint32_t kSmemWords = (uint32_t)G::kSegSyms * 3u / 4u;
   extern __shared__ __align__(16) uint32_t s_bits[];
   __shared__ uint32_t s_code[256];
   __shared__ uint32_t s_bm[G::kBmWords];
-  __shared__ uint32_t s_rowoff[G::kSB];
-  __shared__ uint32_t s_aux[G::kSB];
+  __shared__ uint32_t s_wpre[G::kBmWords];
   __shared__ uint16_t s_litrow[G::kSB];
-  __shared__ uint4 s_warp[8];
+  __shared__ uint32_t s_rowoff[G::kSB + 1];
   __shared__ uint32_t s_red[8];
+  __shared__ uint4 s_warp[8];
   __shared__ uint4 s_base;
-  __shared__ uint32_t s_segbits;
-  __shared__ int s_seg;
+  __shared__ int s_seg, s_stop;
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) s_seg = (int)atomicAdd(&g->tile_ctr, 1u);
@@ -630,165 +652,182 @@ __global__ void __launch_bounds__(256) k_emit(const float* __restrict__ x, Shape
   const int T = sh.T;
   const int64_t row0 = (int64_t)s * G::kSB;
   const uint8_t* symt = w.sym + (size_t)t * B * D;
-  const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
 
   const uint32_t mycode = __ldcg(&w.tabcode[(size_t)t * 256 + tid]);
   s_code[tid] = mycode;
+  uint32_t litw = 0;
   if (tid < G::kBmWords) {
     const int64_t wi = (int64_t)s * G::kBmWords + tid;
-    s_bm[tid] = wi < sh.nw ? __ldcg(&w.bitmap[(size_t)t * sh.nw + wi]) : 0u;
+    uint32_t bm = 0;
+    if (wi < sh.nw) {
+      bm = __ldcg(&w.bitmap[(size_t)t * sh.nw + wi]);
+      const int64_t nv = B - (row0 + (int64_t)tid * 32);
+      litw = ~bm & (nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u));
+    }
+    s_bm[tid] = bm;
   }
   const uint4 cnt = __ldcg(&w.seg_cnt[seg]);
+  const uint32_t nlit = cnt.x;
   // segment bits: sum over codes of count * length, plus 32 raw bits per outlier
   const uint32_t hc = __ldcg(&w.seg_hist[(size_t)seg * 256 + tid]);
   const uint32_t bits = block_sum(hc * (mycode & 0xffu) + (tid == 0 ? 32u * hc : 0u), s_red);
   const uint32_t nwords = ((bits + 127u) >> 7) * 4u;
-  const uint4 agg = make_uint4(nwords, cnt.w, cnt.y, 0u);
-  if (tid == 0) {
-    w.seg_agg[seg] = agg;
-    __threadfence();
-    *reinterpret_cast<volatile uint32_t*>(w.seg_flag + seg) = (sepoch << 2) | 1u;
+  const uint4 agg = make_uint4(0u, nwords, cnt.w, cnt.y);   // {-, words, chunks, matches}
+
+  // publish the aggregate, look back, publish the inclusive prefix
+  if (tid == 0) st_desc(w.seg_desc + seg, make_uint4((sepoch << 2) | 1u, agg.y, agg.z, agg.w));
+  {
+    const uint4 ex = lookback(w, seg, sepoch, s_warp, &s_stop);
+    if (tid == 0) {
+      // base = {words, chunks, matches, -} of everything before this segment
+      s_base = make_uint4(ex.y, ex.z, ex.w, 0u);
+      st_desc(w.seg_desc + seg, make_uint4((sepoch << 2) | 2u, ex.y + agg.y, ex.z + agg.z, ex.w + agg.w));
+    }
   }
-  for (uint32_t i = tid; i < nwords; i += 256) s_bits[i] = 0u;
+  __syncthreads();
+  if (warp == 1) {   // literal rows in row order: per-word prefix of literal counts (<= 64 words)
+    uint32_t c0 = 0, c1 = 0;
+    if (lane * 2 < G::kBmWords) c0 = __popc(~s_bm[lane * 2] & valid_mask(B, row0, lane * 2));
+    if (lane * 2 + 1 < G::kBmWords) c1 = __popc(~s_bm[lane * 2 + 1] & valid_mask(B, row0, lane * 2 + 1));
+    uint32_t inc = c0 + c1;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t n = __shfl_up_sync(0xffffffffu, inc, off);
+      if (lane >= off) inc += n;
+    }
+    const uint32_t ex = inc - c0 - c1;
+    if (lane * 2 < G::kBmWords) s_wpre[lane * 2] = ex;
+    if (lane * 2 + 1 < G::kBmWords) s_wpre[lane * 2 + 1] = ex + c0;
+  }
+  __syncthreads();
+  if (tid < G::kBmWords) {
+    uint32_t k = s_wpre[tid];
+    for (uint32_t m = litw; m; m &= m - 1) s_litrow[k++] = (uint16_t)(tid * 32 + __ffs(m) - 1);
+  }
+  const uint4 base = s_base;
+  const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
+  const unsigned long long off_bits = __ldcg(&g->off_bits), off_chunks = __ldcg(&g->off_chunks);
+  const unsigned long long off_refs = __ldcg(&g->off_refs);
+  const unsigned long long off_seg = __ldcg(&g->off_seg), off_bitmap = __ldcg(&g->off_bitmap);
+  const bool bits_fit = writable && off_bits + 4ull * ((unsigned long long)base.x + nwords) <= cap;
+  const bool in_smem = nwords <= kSmemWords;
+  uint32_t* dstw = reinterpret_cast<uint32_t*>(out + off_bits) + base.x;
+  uint32_t* bitbuf = in_smem ? s_bits : dstw;
+  if (bits_fit)
+    for (uint32_t i = tid; i < nwords; i += 256) bitbuf[i] = 0u;
   __syncthreads();
 
-  // pass 1: bits per literal row; the codes stay in registers
-  uint32_t wv[kIters * G::kSPR];
-#pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
-    const int64_t b = row0 + r;
-    const bool lit = b < B && !((s_bm[r >> 5] >> (r & 31)) & 1u);
+  // pass 1: bits of each literal row (lane groups of kLPR lanes per row)
+  const uint32_t slots = (nlit + G::kRPS - 1) / G::kRPS;
+  for (uint32_t sl = warp; sl < slots; sl += 8) {
+    const uint32_t k = sl * G::kRPS + lane / G::kLPR;
+    const bool ok = k < nlit;
+    const int64_t b = row0 + (ok ? s_litrow[k] : 0);
     uint32_t nb = 0;
 #pragma unroll
     for (int j = 0; j < G::kSPR; ++j) {
       const int d = (lane % G::kLPR) * 4 + j * 128;
-      const uint32_t v = lit ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0x80808080u;
-      wv[it * G::kSPR + j] = v;
-      nb += (s_code[v & 0xffu] & 0xffu) + (s_code[(v >> 8) & 0xffu] & 0xffu) +
-            (s_code[(v >> 16) & 0xffu] & 0xffu) + (s_code[v >> 24] & 0xffu);
-      nb += 32u * (((v & 0xffu) == 0u) + (((v >> 8) & 0xffu) == 0u) + (((v >> 16) & 0xffu) == 0u) + ((v >> 24) == 0u));
-    }
-#pragma unroll
-    for (int off = G::kLPR / 2; off > 0; off >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, off);
-    if ((lane % G::kLPR) == 0) s_rowoff[r] = lit ? nb : 0u;
-  }
-  __syncthreads();
-
-  // row scan: bit offsets, literal ranks, match ranks
-  constexpr int kRPT = (G::kSB + 255) / 256;
-  {
-    uint4 loc[kRPT];
-    uint4 sum = make_uint4(0, 0, 0, 0);
-#pragma unroll
-    for (int k = 0; k < kRPT; ++k) {
-      const int r = tid * kRPT + k;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < G::kSB && row0 + r < B) {
-        const bool m = (s_bm[r >> 5] >> (r & 31)) & 1u;
-        v = make_uint4(s_rowoff[r], m ? 0u : 1u, m ? 1u : 0u, 0u);
-      }
-      loc[k] = sum;
-      sum = add4(sum, v);
-    }
-    uint4 tot;
-    const uint4 ex = block_excl_scan4(sum, &tot, s_warp);
-#pragma unroll
-    for (int k = 0; k < kRPT; ++k) {
-      const int r = tid * kRPT + k;
-      if (r < G::kSB) {
-        const uint4 p = add4(ex, loc[k]);
-        const bool m = (s_bm[r >> 5] >> (r & 31)) & 1u;
-        s_rowoff[r] = p.x;
-        if (row0 + r < B && !m) s_litrow[p.y] = (uint16_t)r;
-        s_aux[r] = p.z;
-      }
-    }
-    if (tid == 0) {
-      s_segbits = tot.x;
-      if (tot.x != bits) record_error(g, EBC_ERR_INTERNAL);
-    }
-  }
-  __syncthreads();
-
-  // pass 2: codes (and raw outlier bits) into the shared bitstream
-#pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
-    const int64_t b = row0 + r;
-    const bool lit = b < B && !((s_bm[r >> 5] >> (r & 31)) & 1u);
-    uint32_t p = s_rowoff[r];
-#pragma unroll
-    for (int j = 0; j < G::kSPR; ++j) {
-      const uint32_t v = wv[it * G::kSPR + j];
-      uint32_t nb = 0;
+      const uint32_t v = ok ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0x80808080u;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t c = (v >> (8 * q)) & 0xffu;
         nb += (s_code[c] & 0xffu) + (c == 0u ? 32u : 0u);
       }
-      if (!lit) nb = 0;
-      // exclusive prefix of nb within the row's lane group (stream order = d order)
-      uint32_t inc = nb;
-#pragma unroll
-      for (int off = 1; off < G::kLPR; off <<= 1) {
-        const uint32_t n = __shfl_up_sync(0xffffffffu, inc, off);
-        if ((lane % G::kLPR) >= off) inc += n;
-      }
-      const uint32_t slab_total = __shfl_sync(0xffffffffu, inc, (lane & ~(G::kLPR - 1)) + G::kLPR - 1);
-      if (lit) {
-        uint32_t qpos = p + inc - nb;
-        const int d = (lane % G::kLPR) * 4 + j * 128;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const uint32_t c = (v >> (8 * q)) & 0xffu;
-          const uint32_t e = s_code[c];
-          put_bits(s_bits, qpos, e >> 8, e & 0xffu);
-          qpos += e & 0xffu;
-          if (c == 0u) {
-            put_bits(s_bits, qpos, __float_as_uint(x[((size_t)b * T + t) * D + d + q]), 32u);
-            qpos += 32u;
-          }
-        }
-      }
-      p += slab_total;
     }
+#pragma unroll
+    for (int off = G::kLPR / 2; off > 0; off >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, off);
+    if (ok && (lane % G::kLPR) == 0) s_rowoff[k] = nb;
   }
-
-  // absolute offsets of this segment
-  if (warp == 0) {
-    const uint4 ex = lookback(w, seg, sepoch);
-    if (lane == 0) {
-      s_base = ex;
-      w.seg_incl[seg] = add4(ex, agg);
-      __threadfence();
-      *reinterpret_cast<volatile uint32_t*>(w.seg_flag + seg) = (sepoch << 2) | 2u;
+  __syncthreads();
+  // exclusive scan over the literal rows
+  {
+    constexpr int kRPT = (G::kSB + 255) / 256;
+    uint32_t loc[kRPT];
+    uint32_t sum = 0;
+#pragma unroll
+    for (int k = 0; k < kRPT; ++k) {
+      const uint32_t i = tid * kRPT + k;
+      loc[k] = sum;
+      sum += i < nlit ? s_rowoff[i] : 0u;
+    }
+    uint4 tot;
+    const uint32_t ex = block_excl_scan4(make_uint4(sum, 0, 0, 0), &tot, s_warp).x;
+#pragma unroll
+    for (int k = 0; k < kRPT; ++k) {
+      const uint32_t i = tid * kRPT + k;
+      if (i < nlit) s_rowoff[i] = ex + loc[k];
+    }
+    if (tid == 0) {
+      s_rowoff[nlit] = tot.x;
+      if (tot.x != bits) record_error(g, EBC_ERR_INTERNAL);
     }
   }
   __syncthreads();
-  const uint4 base = s_base;
-  const unsigned long long off_bits = __ldcg(&g->off_bits), off_chunks = __ldcg(&g->off_chunks);
-  const unsigned long long off_refs = __ldcg(&g->off_refs);
-  const unsigned long long off_seg = __ldcg(&g->off_seg), off_bitmap = __ldcg(&g->off_bitmap);
+
+  // pass 2: codes (and raw outlier bits) into the bitstream
+  if (bits_fit) {
+    for (uint32_t sl = warp; sl < slots; sl += 8) {
+      const uint32_t k = sl * G::kRPS + lane / G::kLPR;
+      const bool ok = k < nlit;
+      const int64_t b = row0 + (ok ? s_litrow[k] : 0);
+      uint32_t p = ok ? s_rowoff[k] : 0u;
+#pragma unroll
+      for (int j = 0; j < G::kSPR; ++j) {
+        const int d = (lane % G::kLPR) * 4 + j * 128;
+        const uint32_t v = ok ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0x80808080u;
+        uint32_t nb = 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const uint32_t c = (v >> (8 * q)) & 0xffu;
+          nb += (s_code[c] & 0xffu) + (c == 0u ? 32u : 0u);
+        }
+        if (!ok) nb = 0;
+        uint32_t inc = nb;
+#pragma unroll
+        for (int off = 1; off < G::kLPR; off <<= 1) {
+          const uint32_t n = __shfl_up_sync(0xffffffffu, inc, off);
+          if ((lane % G::kLPR) >= off) inc += n;
+        }
+        const uint32_t slab_total = __shfl_sync(0xffffffffu, inc, (lane & ~(G::kLPR - 1)) + G::kLPR - 1);
+        if (ok) {
+          uint32_t qpos = p + inc - nb;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint32_t c = (v >> (8 * q)) & 0xffu;
+            const uint32_t e = s_code[c];
+            put_bits(bitbuf, qpos, e >> 8, e & 0xffu);
+            qpos += e & 0xffu;
+            if (c == 0u) {
+              put_bits(bitbuf, qpos, __float_as_uint(x[((size_t)b * T + t) * D + d + q]), 32u);
+              qpos += 32u;
+            }
+          }
+        }
+        p += slab_total;
+      }
+    }
+  }
+  __syncthreads();
 
   if (writable) {
-    if (off_bits + 4ull * ((unsigned long long)base.x + nwords) <= cap) {
-      uint4* dst = reinterpret_cast<uint4*>(out + off_bits + 4ull * base.x);
+    if (bits_fit && in_smem) {
+      uint4* dst = reinterpret_cast<uint4*>(dstw);
       const uint4* src = reinterpret_cast<const uint4*>(s_bits);
       for (uint32_t i = tid; i < nwords / 4; i += 256) dst[i] = src[i];
     }
-    const uint32_t nlit = cnt.x;
     for (uint32_t k = tid * G::kKC; k < nlit; k += 256 * G::kKC) {
-      const uint32_t start = s_rowoff[s_litrow[k]];
-      const uint32_t end = k + G::kKC < nlit ? s_rowoff[s_litrow[k + G::kKC]] : s_segbits;
-      *reinterpret_cast<uint16_t*>(out + off_chunks + 2ull * (base.y + k / G::kKC)) = (uint16_t)(end - start);
+      const uint32_t end = k + G::kKC < nlit ? s_rowoff[k + G::kKC] : s_rowoff[nlit];
+      *reinterpret_cast<uint16_t*>(out + off_chunks + 2ull * (base.y + k / G::kKC)) = (uint16_t)(end - s_rowoff[k]);
     }
     for (int r = tid; r < G::kSB; r += 256) {
       const int64_t b = row0 + r;
       if (b >= B) break;
-      if ((s_bm[r >> 5] >> (r & 31)) & 1u) {
+      const uint32_t mw = s_bm[r >> 5];
+      if ((mw >> (r & 31)) & 1u) {
+        // matches before row r = rows before r - literals before r (all rows before r exist)
+        const uint32_t rank = (uint32_t)r - (s_wpre[r >> 5] + __popc(~mw & ((1u << (r & 31)) - 1u)));
         const uint32_t ref = __ldcg(&w.ref[(size_t)t * B + b]);
-        const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (base.z + s_aux[r]);
+        const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (base.z + rank);
         if (sh.ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)ref;
         else *reinterpret_cast<uint32_t*>(out + o) = ref;
       }
@@ -836,7 +875,7 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
   prof_end(prof, st);
   if (grid) {
     prof_begin(prof, "k_emit", st);
-    k_emit<D><<<grid, 256, Geo<D>::kSegSyms * 7, st>>>(x, sh, w, out, cap, out_bytes, epoch, sepoch);
+    k_emit<D><<<grid, 256, Geo<D>::kSegSyms * 3, st>>>(x, sh, w, out, cap, out_bytes, epoch, sepoch);
     prof_end(prof, st);
   }
 }
@@ -860,8 +899,8 @@ cudaError_t launch_compress(const float* x, const Shape& sh, const EbParams& ep,
 
 template <int D>
 static cudaError_t set_emit_smem() {
-  // worst-case bitstream of one segment: every code 24 bits, every value an outlier (+32)
-  return cudaFuncSetAttribute(k_emit<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 7);
+  // shared copy of a segment's bitstream: 24 bits per code on average (larger ones go to global memory)
+  return cudaFuncSetAttribute(k_emit<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3);
 }
 
 cudaError_t set_kernel_attributes() {

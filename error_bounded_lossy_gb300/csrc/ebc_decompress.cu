@@ -157,6 +157,16 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
       }
       DecTab* dt = w.dtab + t;
       dt->ebx2 = __fmul_rn(2.0f, eb);
+      // the table's chunk range (segment records are checked against each other by the segment warps)
+      const uint32_t* srec = reinterpret_cast<const uint32_t*>(in + L.off_seg);
+      uint32_t c0 = 0, c1 = 0;
+      if (sh.nseg > 0) {
+        c0 = srec[4ull * ((unsigned long long)t * sh.nseg) + 1];
+        c1 = t + 1 < T ? srec[4ull * ((unsigned long long)(t + 1) * sh.nseg) + 1] : (uint32_t)L.n_chunks;
+      }
+      if (c0 > c1 || c1 > L.n_chunks) s_bad = 1;
+      dt->chunk0 = c0;
+      dt->chunk1 = c1;
       for (int l = 0; l <= kLmax; ++l) {
         dt->first[l] = l ? s_next[l] : 0u;
         dt->count[l] = l ? s_count[l] : 0u;
@@ -259,192 +269,174 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     cstart = acc;
     ok = cstart == nbits;
   }
+  // matched rows: {destination, source} row pairs, in (table, row) order
+  if (__all_sync(0xffffffffu, ok)) {
+    const uint8_t* refs = in + L.off_refs;
+    uint32_t mbase = match_base;
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+      const int wi = half * 32 + lane;
+      uint32_t mw = 0;
+      if (wi < G::kBmWords) {
+        const int64_t gw = (int64_t)s * G::kBmWords + wi;
+        if (gw < sh.nw) mw = bmt[gw];
+      }
+      uint32_t tot;
+      uint32_t k = mbase + warp_excl(__popc(mw), &tot);
+      for (uint32_t m = mw; m; m &= m - 1) {
+        const int64_t b = row0 + wi * 32 + __ffs(m) - 1;
+        const uint32_t ref = sh.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[k]
+                                               : reinterpret_cast<const uint32_t*>(refs)[k];
+        if ((int64_t)ref >= b || ((bmt[ref >> 5] >> (ref & 31)) & 1u)) {
+          ok = false;
+          break;
+        }
+        w.mdesc[k] = make_uint2((uint32_t)(b * T + t), (uint32_t)((int64_t)ref * T + t));
+        ++k;
+      }
+      mbase += tot;
+    }
+  }
   if (!__all_sync(0xffffffffu, ok) || s_bad) {
     if (lane == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
   }
 }
 
 // ---------------------------------------------------------------------------
-// k_dec_chunks: one thread per chunk (grid-stride).  The thread decodes its
-// chunk's codes with the first-level table (long codes by the canonical
-// first-code search), reads the 32 raw bits after each outlier code, and
-// writes each literal row with 16-byte stores.
+// k_dec_chunks: one thread per chunk; CTA (t, k) takes the k-th run of 256
+// chunks of table t, with the table's decode tables in shared memory.  The
+// thread decodes its chunk's codes with the first-level table (long codes by
+// the canonical first-code search), reads the 32 raw bits after each outlier
+// code, and writes each literal row with 16-byte stores.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) k_dec_chunks(const uint8_t* __restrict__ in, Shape sh, Work w,
-                                                     float* __restrict__ xhat, uint32_t epoch) {
+                                                     float* __restrict__ xhat, uint32_t epoch, int cta_per_table) {
   using G = Geo<D>;
+  __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
+  __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
+  __shared__ uint8_t s_sorted[256];
   Glob* g = w.glob;
   if (dec_aborted(g, epoch)) return;
-  const unsigned long long n_chunks = __ldcg(&g->n_chunks), n_words = __ldcg(&g->words);
-  const unsigned long long off_bits = __ldcg(&g->off_bits);
+  const int t = blockIdx.x / cta_per_table;
+  const int blk = blockIdx.x - t * cta_per_table;
+  const DecTab* dt = w.dtab + t;
+  const uint32_t c0 = __ldcg(&dt->chunk0), c1 = __ldcg(&dt->chunk1);
+  const unsigned long long jbase = (unsigned long long)c0 + (unsigned long long)blk * 256ull;
+  if (jbase >= c1) return;
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(w.lut + (size_t)t * (1u << kLutBits));
+    uint4* dst = reinterpret_cast<uint4*>(s_lut);
+    for (int i = threadIdx.x; i < (1 << kLutBits) / 8; i += 256) dst[i] = __ldcg(src + i);
+    if (threadIdx.x <= kLmax) {
+      s_first[threadIdx.x] = __ldcg(&dt->first[threadIdx.x]);
+      s_count[threadIdx.x] = __ldcg(&dt->count[threadIdx.x]);
+      s_offset[threadIdx.x] = __ldcg(&dt->offset[threadIdx.x]);
+    }
+    s_sorted[threadIdx.x] = dt->sorted[threadIdx.x];
+  }
+  __syncthreads();
+  const unsigned long long j = jbase + threadIdx.x;
+  if (j >= c1) return;
+  const unsigned long long n_words = __ldcg(&g->words), off_bits = __ldcg(&g->off_bits);
   const uint32_t* words = reinterpret_cast<const uint32_t*>(in + off_bits);
   const int T = sh.T;
-  const int nsegT = T * sh.nseg;
-  for (unsigned long long j = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; j < n_chunks;
-       j += (unsigned long long)gridDim.x * blockDim.x) {
-    const uint4 dsc = __ldcg(&w.cdesc[j]);
-    const unsigned long long start = (unsigned long long)dsc.x | ((unsigned long long)(dsc.y & 0xffffu) << 32);
-    const uint32_t clen = dsc.y >> 16;
-    const int seg = (int)dsc.z;
-    const uint32_t first = dsc.w & 0xffffu, rows = dsc.w >> 16;
-    if (seg >= nsegT || rows == 0u || first + rows > (uint32_t)G::kSB || start + clen > n_words * 32ull) {
-      dec_fail(g, epoch, EBC_ERR_CORRUPT);
-      continue;
-    }
-    const int t = seg / sh.nseg;
-    const int s = seg - t * sh.nseg;
-    const uint16_t* lut = w.lut + (size_t)t * (1u << kLutBits);
-    const DecTab* dt = w.dtab + t;
-    const float ebx2 = __ldg(&dt->ebx2);
-    const unsigned long long wlim = (start + clen + 31ull) >> 5;
-    unsigned long long wp = start >> 5;
-    auto ldw = [&](unsigned long long i) -> unsigned long long {
-      return i < wlim ? (unsigned long long)__ldg(words + i) : 0ull;
-    };
-    unsigned long long buf = (ldw(wp) << 32) | ldw(wp + 1);
-    const uint32_t skip = (uint32_t)(start & 31ull);
-    buf <<= skip;
-    int nb = 64 - (int)skip;
-    wp += 2;
-    uint32_t used = 0;
-    bool bad = false;
-    const uint16_t* lrow = w.litrow + (size_t)seg * G::kSB + first;
-    for (uint32_t k = 0; k < rows && !bad; ++k) {
-      const int64_t b = (int64_t)s * G::kSB + lrow[k];
-      float4* dst = reinterpret_cast<float4*>(xhat + ((size_t)b * T + t) * D);
-      for (int q4 = 0; q4 < D / 4; ++q4) {
-        float o[4];
+  const uint4 dsc = __ldcg(&w.cdesc[j]);
+  const unsigned long long start = (unsigned long long)dsc.x | ((unsigned long long)(dsc.y & 0xffffu) << 32);
+  const uint32_t clen = dsc.y >> 16;
+  const int seg = (int)dsc.z;
+  const uint32_t first = dsc.w & 0xffffu, rows = dsc.w >> 16;
+  if (seg / sh.nseg != t || rows == 0u || first + rows > (uint32_t)G::kSB || start + clen > n_words * 32ull) {
+    dec_fail(g, epoch, EBC_ERR_CORRUPT);
+    return;
+  }
+  const int s = seg - t * sh.nseg;
+  const float ebx2 = __ldcg(&dt->ebx2);
+  const unsigned long long wlim = (start + clen + 31ull) >> 5;
+  auto ldw = [&](unsigned long long i) -> uint32_t { return i < wlim ? __ldg(words + i) : 0u; };
+  // bit window: the next stream bits are w0:w1 from bit `pos` of w0 (pos < 32)
+  unsigned long long wp = start >> 5;
+  uint32_t pos = (uint32_t)(start & 31ull);
+  uint32_t w0 = ldw(wp), w1 = ldw(wp + 1);
+  wp += 2;
+  uint32_t used = 0;
+  bool bad = false;
+  const uint16_t* lrow = w.litrow + (size_t)seg * G::kSB + first;
+  for (uint32_t k = 0; k < rows; ++k) {
+    const int64_t b = (int64_t)s * G::kSB + lrow[k];
+    float4* dst = reinterpret_cast<float4*>(xhat + ((size_t)b * T + t) * D);
+#pragma unroll 2
+    for (int q4 = 0; q4 < D / 4; ++q4) {
+      float o[4];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (nb < 32) {
-            buf |= ldw(wp++) << (32 - nb);
-            nb += 32;
+      for (int q = 0; q < 4; ++q) {
+        const uint32_t peek = __funnelshift_l(w1, w0, pos);   // the next 32 bits
+        const uint32_t e = s_lut[peek >> (32 - kLutBits)];
+        uint32_t len = e >> 8, sym = e & 0xffu;
+        if (len == 0u) {   // a code longer than the first-level table
+          for (int l = kLutBits + 1; l <= kLmax; ++l) {
+            const uint32_t code = peek >> (32 - l);
+            if (code - s_first[l] < s_count[l]) {
+              sym = s_sorted[s_offset[l] + code - s_first[l]];
+              len = (uint32_t)l;
+              break;
+            }
           }
-          const uint32_t e = __ldg(lut + (uint32_t)(buf >> (64 - kLutBits)));
-          uint32_t len = e >> 8, sym = e & 0xffu;
           if (len == 0u) {
-            for (int l = kLutBits + 1; l <= kLmax; ++l) {
-              const uint32_t code = (uint32_t)(buf >> (64 - l));
-              const uint32_t f = __ldg(&dt->first[l]);
-              if (code - f < __ldg(&dt->count[l])) {
-                sym = __ldg(&dt->sorted[__ldg(&dt->offset[l]) + code - f]);
-                len = (uint32_t)l;
-                break;
-              }
-            }
-            if (len == 0u) {
-              bad = true;
-              len = 1;
-            }
-          }
-          buf <<= len;
-          nb -= (int)len;
-          used += len;
-          if (sym == 0u) {
-            if (nb < 32) {
-              buf |= ldw(wp++) << (32 - nb);
-              nb += 32;
-            }
-            o[q] = __uint_as_float((uint32_t)(buf >> 32));
-            buf <<= 32;
-            nb -= 32;
-            used += 32;
-          } else {
-            o[q] = __fmul_rn((float)((int)sym - kRadius), ebx2);
+            bad = true;
+            len = 1;
           }
         }
-        dst[q4] = make_float4(o[0], o[1], o[2], o[3]);
+        used += len;
+        pos += len;
+        if (pos >= 32u) {
+          pos -= 32u;
+          w0 = w1;
+          w1 = ldw(wp++);
+        }
+        if (sym == 0u) {   // outlier: the next 32 bits are the raw value
+          o[q] = __uint_as_float(__funnelshift_l(w1, w0, pos));
+          used += 32u;
+          w0 = w1;
+          w1 = ldw(wp++);
+        } else {
+          o[q] = __fmul_rn((float)((int)sym - kRadius), ebx2);
+        }
       }
+      dst[q4] = make_float4(o[0], o[1], o[2], o[3]);
     }
-    if (bad || used != clen) dec_fail(g, epoch, EBC_ERR_CORRUPT);
   }
+  if (bad || used != clen) dec_fail(g, epoch, EBC_ERR_CORRUPT);
 }
 
 // ---------------------------------------------------------------------------
-// k_dec_matches: one CTA per (table, segment); each matched row copies its
-// reference row, which is always an earlier literal of the same table.
+// k_dec_matches: each matched row copies its reference row, which is always an
+// earlier literal of the same table (grid-stride over (matched row, 16-byte
+// column) pairs, four copies in flight per thread).
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) k_dec_matches(const uint8_t* __restrict__ in, Shape sh, Work w,
-                                                      float* __restrict__ xhat, uint32_t epoch) {
-  using G = Geo<D>;
-  __shared__ uint32_t s_bm[G::kBmWords];
-  __shared__ uint32_t s_pre[G::kBmWords + 1];
-  __shared__ uint16_t s_mrow[G::kSB];
-  __shared__ uint32_t s_mref[G::kSB];
-  __shared__ int s_bad;
+__global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __restrict__ xhat, uint32_t epoch) {
   Glob* g = w.glob;
   if (dec_aborted(g, epoch)) return;
-  const int tid = threadIdx.x;
-  const int seg = blockIdx.x;
-  const int t = seg / sh.nseg;
-  const int s = seg - t * sh.nseg;
-  const int64_t B = sh.B;
-  const int T = sh.T;
-  const int64_t row0 = (int64_t)s * G::kSB;
-  const unsigned long long off_seg = __ldcg(&g->off_seg), off_bitmap = __ldcg(&g->off_bitmap);
-  const unsigned long long off_refs = __ldcg(&g->off_refs), n_match = __ldcg(&g->n_match);
-  const uint32_t match_base = reinterpret_cast<const uint32_t*>(in + off_seg + (unsigned long long)seg * kSegRecBytes)[2];
-  const uint32_t* bmt = reinterpret_cast<const uint32_t*>(in + off_bitmap) + (size_t)t * sh.nw;
-  if (tid < G::kBmWords) {
-    const int64_t wi = (int64_t)s * G::kBmWords + tid;
-    s_bm[tid] = wi < sh.nw ? bmt[wi] : 0u;
-  }
-  if (tid == 0) s_bad = 0;
-  __syncthreads();
-  if (tid < 32) {   // prefix of match counts over the segment's bitmap words (<= 64)
-    const uint32_t a = tid * 2 < G::kBmWords ? __popc(s_bm[tid * 2]) : 0u;
-    const uint32_t c = tid * 2 + 1 < G::kBmWords ? __popc(s_bm[tid * 2 + 1]) : 0u;
-    uint32_t tot;
-    const uint32_t ex = warp_excl(a + c, &tot);
-    if (tid * 2 < G::kBmWords) s_pre[tid * 2] = ex;
-    if (tid * 2 + 1 < G::kBmWords) s_pre[tid * 2 + 1] = ex + a;
-    if (tid == 0) s_pre[G::kBmWords] = tot;
-  }
-  __syncthreads();
-  const uint32_t nm = s_pre[G::kBmWords];
-  if ((unsigned long long)match_base + nm > n_match) {
-    if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
-    return;
-  }
-  // references: one thread per matched row, loads in parallel
-  const uint8_t* refs = in + off_refs;
-  for (int r = tid; r < G::kSB; r += 256) {
-    const int64_t b = row0 + r;
-    if (b >= B || !((s_bm[r >> 5] >> (r & 31)) & 1u)) continue;
-    const uint32_t rank = s_pre[r >> 5] + __popc(s_bm[r >> 5] & ((1u << (r & 31)) - 1u));
-    const unsigned long long mi = (unsigned long long)match_base + rank;
-    const uint32_t ref = sh.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[mi]
-                                           : reinterpret_cast<const uint32_t*>(refs)[mi];
-    if ((int64_t)ref >= b || ((bmt[ref >> 5] >> (ref & 31)) & 1u)) s_bad = 1;
-    s_mrow[rank] = (uint16_t)r;
-    s_mref[rank] = ref;
-  }
-  __syncthreads();
-  if (s_bad) {
-    if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
-    return;
-  }
-  // copy: flat over (matched row, float4), four independent copies in flight per thread
   constexpr int kQ = D / 4;
-  const uint32_t n4 = nm * kQ;
-  for (uint32_t i0 = tid; i0 < n4; i0 += 4 * 256) {
+  const unsigned long long n4 = __ldcg(&g->n_match) * (unsigned long long)kQ;
+  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+  for (unsigned long long i0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n4; i0 += 4 * stride) {
     float4 v[4];
-    size_t dst[4];
+    unsigned long long dst[4];
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
-      const uint32_t i = i0 + k * 256;
+      const unsigned long long i = i0 + k * stride;
       if (i < n4) {
-        const uint32_t m = i / kQ, q = i % kQ;
-        const int64_t b = row0 + s_mrow[m];
-        v[k] = *reinterpret_cast<const float4*>(xhat + ((size_t)s_mref[m] * T + t) * D + 4 * q);
-        dst[k] = ((size_t)b * T + t) * D + 4 * q;
+        const uint2 m = __ldcg(&w.mdesc[i / kQ]);
+        const unsigned long long q = i % kQ;
+        v[k] = *reinterpret_cast<const float4*>(xhat + (size_t)m.y * D + 4 * q);
+        dst[k] = (size_t)m.x * D + 4 * q;
       }
     }
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      if (i0 + k * 256 < n4) __stcs(reinterpret_cast<float4*>(xhat + dst[k]), v[k]);
+      if (i0 + k * stride < n4) __stcs(reinterpret_cast<float4*>(xhat + dst[k]), v[k]);
   }
 }
 
@@ -459,15 +451,13 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
   k_dec_prep<D><<<(sh.T > 0 ? sh.T : 1) + (nsegT + 7) / 8, 256, 0, st>>>(in, in_bytes, sh, w, epoch);
   prof_end(prof, st);
   if (nsegT) {
-    const unsigned long long max_chunks = (unsigned long long)nsegT * Geo<D>::kChunks;
-    unsigned grid = (unsigned)((max_chunks + 255) / 256);
-    const unsigned cap = (unsigned)(sh.nsm > 0 ? sh.nsm : 152) * 8u;
-    if (grid > cap) grid = cap;
+    // CTAs per table: enough for the largest possible chunk count of a table
+    const int cpt = (int)(((unsigned long long)sh.nseg * Geo<D>::kChunks + 255) / 256);
     prof_begin(prof, "k_dec_chunks", st);
-    k_dec_chunks<D><<<grid, 256, 0, st>>>(in, sh, w, xhat, epoch);
+    k_dec_chunks<D><<<(unsigned)(sh.T * cpt), 256, 0, st>>>(in, sh, w, xhat, epoch, cpt);
     prof_end(prof, st);
     prof_begin(prof, "k_dec_matches", st);
-    k_dec_matches<D><<<nsegT, 256, 0, st>>>(in, sh, w, xhat, epoch);
+    k_dec_matches<D><<<(unsigned)((sh.nsm > 0 ? sh.nsm : 152) * 8), 256, 0, st>>>(sh, w, xhat, epoch);
     prof_end(prof, st);
   }
 }

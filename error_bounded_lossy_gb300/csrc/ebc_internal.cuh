@@ -62,7 +62,8 @@ struct DecTab {
   uint32_t count[kLmax + 1];   // codes of each length
   uint32_t offset[kLmax + 1];  // index of that first code in sorted[]
   float ebx2;                  // 2 * eb
-  uint32_t pad[3];
+  uint32_t chunk0, chunk1;     // the table's chunks: [chunk0, chunk1)
+  uint32_t pad;
   uint8_t sorted[256];         // symbols by (length, symbol)
 };
 
@@ -77,9 +78,8 @@ struct Work {
   uint32_t* ref;               // [T][B] reference row of matched rows
   uint32_t* seg_hist;          // [T*nseg][256] literal code histogram per segment
   uint4* seg_cnt;              // [T*nseg] {literals, matches, outliers, chunks}
-  uint32_t* seg_flag;          // [T*nseg] look-back state: (scan epoch << 2) | 1 aggregate / 2 inclusive
-  uint4* seg_agg;              // [T*nseg] {words, chunks, matches, 0}
-  uint4* seg_incl;             // [T*nseg] inclusive prefix of seg_agg in (table, segment) order
+  uint4* seg_desc;             // [T*nseg] look-back: {(scan epoch << 2) | 1 aggregate / 2 inclusive,
+                               //                      words, chunks, matches}
   uint32_t* tab_hist;          // [T][256] literal code histogram per table
   uint4* tab_cnt;              // [T] {literals, matches, outliers, chunks}
   uint32_t* tabcode;           // [T][256] code << 8 | length
@@ -88,6 +88,7 @@ struct Work {
   DecTab* dtab;                // [T]
   uint4* cdesc;                // [T*nseg*chunks] {start bit lo, start bit hi, segment, first literal | rows << 16}
   uint16_t* litrow;            // [T*nseg][SB] literal rows of each segment, in row order
+  uint2* mdesc;                // [n_match] {destination row, source row} as b * T + t
   Glob* glob;
 };
 

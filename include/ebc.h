@@ -36,7 +36,8 @@
  * segment, decoded by one GPU thread.
  *
  * Supported shapes: 0 <= B <= 16,777,215; 0 <= T <= 1024; D a power of two in
- * [4, 512]; B*T*D < 2^32.  Device pointers must be 16-byte aligned.
+ * [4, 512]; B*T*D <= 2^31 (every bitstream word offset then fits 32 bits).
+ * Device pointers must be 16-byte aligned.
  *
  * Ownership: the caller allocates and owns every input and output buffer.  A
  * context owns its device scratch (grown on demand, which synchronises the

@@ -273,7 +273,7 @@ static layout_t make_layout(int64_t B, int T, int D, uint64_t n_chunks, uint64_t
 static int shape_ok(int64_t B, int T, int D) {
   if (B < 0 || T < 0 || T > O_MAX_T || !dim_ok(D)) return 0;
   if (B > 16777215) return 0;
-  if ((uint64_t)B * (uint64_t)T * (uint64_t)D > 0xFFFFFFFFull) return 0;
+  if ((uint64_t)B * (uint64_t)T * (uint64_t)D > ((uint64_t)1 << 31)) return 0;
   return 1;
 }
 
