@@ -3,15 +3,16 @@
 // Method: "Accelerating Communication in Deep Learning Recommendation Model
 // Training with Dual-Level Adaptive Lossy Compression" (arXiv 2407.04272),
 // §III-D (quantization encoder, vector-based LZ, Huffman) and §III-E (one
-// output buffer, chunk offsets found on the device).  Four launches on the
+// output buffer, chunk offsets found on the device).  Five launches on the
 // caller's stream:
 //   k_quantize  x -> codes, per-vector dedup key, first-occurrence hash table
 //   k_resolve   literal / match decision; literal code histograms per segment
 //               and per table
 //   k_codebook  per-table Huffman code; empties the hash table; the last CTA
 //               lays out the container sections and writes the header
-//   k_emit      per segment: single-pass decoupled look-back for its offsets,
-//               then bitstream, chunk index, references, records
+//   k_layout    per segment bit counts and, by a decoupled look-back over
+//               CTAs, every segment's absolute offsets
+//   k_emit      per segment: bitstream, chunk index, references, records
 // All offsets come from prefix sums, never from atomic reservations, so the
 // container is byte-identical from run to run.
 #include <cstdint>
@@ -140,7 +141,7 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ x, S
       const uint32_t c2 = quantize_one(v[k].z, eb, ebx2, inv);
       const uint32_t c3 = quantize_one(v[k].w, eb, ebx2, inv);
       const uint32_t word = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
-      if (valid) st_keep_u32(reinterpret_cast<uint32_t*>(w.sym + ((size_t)t * B + b) * D + d), word, pol);
+      if (valid) st_keep_u32(reinterpret_cast<uint32_t*>(w.sym + (size_t)t * sh.symstride + (size_t)b * D + d), word, pol);
       acc += lowbias32(word + (uint32_t)(d >> 2) * 0x9E3779B9u);
       if ((c0 == 0u) | (c1 == 0u) | (c2 == 0u) | (c3 == 0u)) {
         if (c0 == 0u) { acc += lowbias32(__float_as_uint(v[k].x) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu); ++nout; }
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(256) k_resolve(const float* __restrict__ x, Sh
   const int T = sh.T;
   const int64_t row0 = (int64_t)s * G::kSB;
   const unsigned long long* slots = w.slots + (size_t)t * sh.S;
-  const uint8_t* symt = w.sym + (size_t)t * B * D;
+  const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
   // one thread per row: first occurrence of the row's key
   for (int r = tid; r < G::kSB; r += 256) {
     const int64_t b = row0 + r;
@@ -541,6 +542,18 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   }
 }
 
+// ORs the n (1..64) right-aligned bits of str MSB-first into a word array at bit
+// position p (up to three words).
+__device__ __forceinline__ void put_string(uint32_t* s, uint32_t p, unsigned long long str, uint32_t n) {
+  const unsigned long long v = str << (64u - n);   // left-aligned
+  const uint32_t sh = p & 31u;
+  uint32_t* w = s + (p >> 5);
+  const unsigned long long hi = v >> sh;
+  atomicOr(w, (uint32_t)(hi >> 32));
+  if (sh + n > 32u) atomicOr(w + 1, (uint32_t)hi);
+  if (sh + n > 64u) atomicOr(w + 2, (uint32_t)((v << (64u - sh)) >> 32));
+}
+
 // Writes `len` (1..32) bits of `code` MSB-first at bit position p of a word array.
 __device__ __forceinline__ void put_bits(uint32_t* s, uint32_t p, uint32_t code, uint32_t len) {
   const uint32_t sh = p & 31u;
@@ -616,118 +629,166 @@ __device__ __forceinline__ uint32_t valid_mask(int64_t B, int64_t row0, int wi) 
 }
 
 // ---------------------------------------------------------------------------
-// k_emit: one CTA per segment, taken in scheduling order.  The segment's bit
-// count comes from its histogram and the code lengths, so its aggregate
-// (words, chunks, matches) is published at once and the look-back gives its
-// absolute offsets before any encoding.  Only literal rows are visited.
-// Codes (and the 32 raw bits after each outlier code) are written MSB-first
-// into a shared-memory copy of the segment's bitstream and stored with 16-byte
-// writes; a segment larger than that copy (24 bits per code on average) is
-// written with atomic ORs straight into the zeroed output instead.
+// k_layout: absolute offsets of every segment.  One warp per segment computes
+// its bit count (sum over codes of count * length, plus 32 raw bits per
+// outlier) from its histogram; a CTA covers 8 consecutive segments and takes
+// its place in (table, segment) order by a decoupled look-back over CTAs.  The
+// CTA holding the last segment completes the header (bitstream words, total
+// size) and the capacity check.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __restrict__ out, unsigned long long cap,
+                                                 unsigned long long* out_bytes, uint32_t epoch, uint32_t sepoch) {
+  __shared__ uint4 s_warp[8];
+  __shared__ uint4 s_agg[8];
+  __shared__ uint4 s_base;
+  __shared__ int s_tile, s_stop;
+  Glob* g = w.glob;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) s_tile = (int)atomicAdd(&g->tile_ctr, 1u);
+  __syncthreads();
+  const int tile = s_tile;
+  const int nsegT = sh.T * sh.nseg;
+  const int seg = tile * 8 + warp;
+  uint4 a = make_uint4(0, 0, 0, 0);   // {-, words, chunks, matches}
+  uint32_t bits = 0;
+  if (seg < nsegT) {
+    const int t = seg / sh.nseg;
+    const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * 256) + lane * 2;
+    const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)t * 256) + lane * 2;
+    const uint4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1), c0 = __ldcg(cp), c1 = __ldcg(cp + 1);
+    const uint4 cnt = __ldcg(&w.seg_cnt[seg]);
+    bits = h0.x * (c0.x & 0xffu) + h0.y * (c0.y & 0xffu) + h0.z * (c0.z & 0xffu) + h0.w * (c0.w & 0xffu) +
+           h1.x * (c1.x & 0xffu) + h1.y * (c1.y & 0xffu) + h1.z * (c1.z & 0xffu) + h1.w * (c1.w & 0xffu);
+    if (lane == 0) bits += 32u * h0.x;   // symbol 0: the outliers' raw bits
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, off);
+    a = make_uint4(0u, ((bits + 127u) >> 7) * 4u, cnt.w, cnt.y);
+  }
+  if (lane == 0) s_agg[warp] = a;
+  __syncthreads();
+  uint4 tile_agg = make_uint4(0, 0, 0, 0), warp_excl = make_uint4(0, 0, 0, 0);
+  for (int i = 0; i < 8; ++i) {
+    if (i < warp) warp_excl = add4(warp_excl, s_agg[i]);
+    tile_agg = add4(tile_agg, s_agg[i]);
+  }
+  if (tid == 0) st_desc(w.seg_desc + tile, make_uint4((sepoch << 2) | 1u, tile_agg.y, tile_agg.z, tile_agg.w));
+  const uint4 ex = lookback(w, tile, sepoch, s_warp, &s_stop);
+  if (tid == 0) {
+    s_base = ex;
+    st_desc(w.seg_desc + tile, make_uint4((sepoch << 2) | 2u, ex.y + tile_agg.y, ex.z + tile_agg.z, ex.w + tile_agg.w));
+  }
+  __syncthreads();
+  const uint4 base = add4(s_base, warp_excl);
+  if (seg < nsegT && lane == 0) w.seg_base[seg] = make_uint4(base.y, base.z, base.w, bits);
+  if (seg == nsegT - 1 && lane == 0) {   // the last segment completes the header
+    const unsigned long long words = (unsigned long long)base.y + a.y;
+    const unsigned long long off_bits = __ldcg(&g->off_bits);
+    const unsigned long long total = off_bits + 4ull * words;
+    g->words = words;
+    g->total = total;
+    *out_bytes = total;
+    if (__ldcg(&g->cstat) == status_word(epoch, EBC_OK)) {
+      st_u64(out + 80, words);
+      st_u64(out + 128, total);
+    }
+    if (total > cap) {
+      record_error(g, EBC_ERR_CAPACITY);
+      g->cstat = status_word(epoch, EBC_ERR_CAPACITY);
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// k_emit: one CTA per (table, segment), offsets from k_layout.  Every global
+// read the CTA needs (codes of all its rows, bitmap, references, code table)
+// is issued first.  A warp takes whole rows (kLPR lanes per row, 4 codes per
+// lane) and skips matched ones; each lane joins its codes into one bit string
+// that is ORed into a shared-memory copy of the segment's bitstream at the
+// lane's offset (a prefix sum over the row).  Outlier codes are followed by the
+// 32 raw bits of the value.  The copy is stored with 16-byte writes; a segment
+// larger than the copy (24 bits per code on average) is ORed straight into the
+// zeroed output.
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) k_emit(const float* __restrict__ x, Shape sh, Work w,
-                                               uint8_t* __restrict__ out, unsigned long long cap,
-                                               unsigned long long* out_bytes, uint32_t epoch, uint32_t sepoch) {
+__global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Shape sh, Work w,
+                                               uint8_t* __restrict__ out, unsigned long long cap, uint32_t epoch) {
   using G = Geo<D>;
+  constexpr int kIters = G::kRowsPerWarp / G::kRPS;
+  constexpr int kRPT = (G::kSB + 255) / 256;   // rows per thread in the row scan
   constexpr uint32_t kSmemWords = (uint32_t)G::kSegSyms * 3u / 4u;
   extern __shared__ __align__(16) uint32_t s_bits[];
   __shared__ uint32_t s_code[256];
   __shared__ uint32_t s_bm[G::kBmWords];
-  __shared__ uint32_t s_wpre[G::kBmWords];
-  __shared__ uint16_t s_litrow[G::kSB];
   __shared__ uint32_t s_rowoff[G::kSB + 1];
-  __shared__ uint32_t s_red[8];
+  __shared__ uint32_t s_aux[G::kSB];
+  __shared__ uint16_t s_litrow[G::kSB];
   __shared__ uint4 s_warp[8];
-  __shared__ uint4 s_base;
-  __shared__ int s_seg, s_stop;
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) s_seg = (int)atomicAdd(&g->tile_ctr, 1u);
-  __syncthreads();
-  const int seg = s_seg;
+  const int seg = blockIdx.x;
   const int t = seg / sh.nseg;
   const int s = seg - t * sh.nseg;
   const int64_t B = sh.B;
   const int T = sh.T;
   const int64_t row0 = (int64_t)s * G::kSB;
-  const uint8_t* symt = w.sym + (size_t)t * B * D;
+  const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
 
+  // ---- every global read, issued together ----
+  const uint4 sb = __ldcg(&w.seg_base[seg]);   // {words, chunks, matches, bits}
   const uint32_t mycode = __ldcg(&w.tabcode[(size_t)t * 256 + tid]);
-  s_code[tid] = mycode;
-  uint32_t litw = 0;
+  uint32_t bmw = 0;
   if (tid < G::kBmWords) {
     const int64_t wi = (int64_t)s * G::kBmWords + tid;
-    uint32_t bm = 0;
-    if (wi < sh.nw) {
-      bm = __ldcg(&w.bitmap[(size_t)t * sh.nw + wi]);
-      const int64_t nv = B - (row0 + (int64_t)tid * 32);
-      litw = ~bm & (nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u));
-    }
-    s_bm[tid] = bm;
+    bmw = wi < sh.nw ? __ldcg(&w.bitmap[(size_t)t * sh.nw + wi]) : 0u;
   }
-  const uint4 cnt = __ldcg(&w.seg_cnt[seg]);
-  const uint32_t nlit = cnt.x;
-  // segment bits: sum over codes of count * length, plus 32 raw bits per outlier
-  const uint32_t hc = __ldcg(&w.seg_hist[(size_t)seg * 256 + tid]);
-  const uint32_t bits = block_sum(hc * (mycode & 0xffu) + (tid == 0 ? 32u * hc : 0u), s_red);
-  const uint32_t nwords = ((bits + 127u) >> 7) * 4u;
-  const uint4 agg = make_uint4(0u, nwords, cnt.w, cnt.y);   // {-, words, chunks, matches}
-
-  // publish the aggregate, look back, publish the inclusive prefix
-  if (tid == 0) st_desc(w.seg_desc + seg, make_uint4((sepoch << 2) | 1u, agg.y, agg.z, agg.w));
-  {
-    const uint4 ex = lookback(w, seg, sepoch, s_warp, &s_stop);
-    if (tid == 0) {
-      // base = {words, chunks, matches, -} of everything before this segment
-      s_base = make_uint4(ex.y, ex.z, ex.w, 0u);
-      st_desc(w.seg_desc + seg, make_uint4((sepoch << 2) | 2u, ex.y + agg.y, ex.z + agg.z, ex.w + agg.w));
-    }
-  }
-  __syncthreads();
-  if (warp == 1) {   // literal rows in row order: per-word prefix of literal counts (<= 64 words)
-    uint32_t c0 = 0, c1 = 0;
-    if (lane * 2 < G::kBmWords) c0 = __popc(~s_bm[lane * 2] & valid_mask(B, row0, lane * 2));
-    if (lane * 2 + 1 < G::kBmWords) c1 = __popc(~s_bm[lane * 2 + 1] & valid_mask(B, row0, lane * 2 + 1));
-    uint32_t inc = c0 + c1;
+  uint32_t wv[kIters][G::kSPR];
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const uint32_t n = __shfl_up_sync(0xffffffffu, inc, off);
-      if (lane >= off) inc += n;
+  for (int it = 0; it < kIters; ++it) {
+    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
+    const int64_t b = row0 + r;
+#pragma unroll
+    for (int j = 0; j < G::kSPR; ++j) {
+      const int d = (lane % G::kLPR) * 4 + j * 128;
+      wv[it][j] = b < B ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0x80808080u;
     }
-    const uint32_t ex = inc - c0 - c1;
-    if (lane * 2 < G::kBmWords) s_wpre[lane * 2] = ex;
-    if (lane * 2 + 1 < G::kBmWords) s_wpre[lane * 2 + 1] = ex + c0;
   }
-  __syncthreads();
-  if (tid < G::kBmWords) {
-    uint32_t k = s_wpre[tid];
-    for (uint32_t m = litw; m; m &= m - 1) s_litrow[k++] = (uint16_t)(tid * 32 + __ffs(m) - 1);
+  uint32_t refw[kRPT];
+#pragma unroll
+  for (int k = 0; k < kRPT; ++k) {
+    const int r = tid * kRPT + k;
+    refw[k] = (r < G::kSB && row0 + r < B) ? __ldcg(&w.ref[(size_t)t * B + row0 + r]) : 0u;
   }
-  const uint4 base = s_base;
   const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
   const unsigned long long off_bits = __ldcg(&g->off_bits), off_chunks = __ldcg(&g->off_chunks);
   const unsigned long long off_refs = __ldcg(&g->off_refs);
   const unsigned long long off_seg = __ldcg(&g->off_seg), off_bitmap = __ldcg(&g->off_bitmap);
-  const bool bits_fit = writable && off_bits + 4ull * ((unsigned long long)base.x + nwords) <= cap;
+
+  s_code[tid] = mycode;
+  if (tid < G::kBmWords) s_bm[tid] = bmw;
+  const uint32_t bits = sb.w;
+  const uint32_t nwords = ((bits + 127u) >> 7) * 4u;
+  const bool bits_fit = writable && off_bits + 4ull * ((unsigned long long)sb.x + nwords) <= cap;
   const bool in_smem = nwords <= kSmemWords;
-  uint32_t* dstw = reinterpret_cast<uint32_t*>(out + off_bits) + base.x;
-  uint32_t* bitbuf = in_smem ? s_bits : dstw;
-  if (bits_fit)
-    for (uint32_t i = tid; i < nwords; i += 256) bitbuf[i] = 0u;
+  uint32_t* dstw = reinterpret_cast<uint32_t*>(out + off_bits) + sb.x;
+  if (bits_fit) {
+    uint32_t* zb = in_smem ? s_bits : dstw;
+    for (uint32_t i = tid; i < nwords; i += 256) zb[i] = 0u;
+  }
   __syncthreads();
 
-  // pass 1: bits of each literal row (lane groups of kLPR lanes per row)
-  const uint32_t slots = (nlit + G::kRPS - 1) / G::kRPS;
-  for (uint32_t sl = warp; sl < slots; sl += 8) {
-    const uint32_t k = sl * G::kRPS + lane / G::kLPR;
-    const bool ok = k < nlit;
-    const int64_t b = row0 + (ok ? s_litrow[k] : 0);
+  // pass 1: bits of each literal row (0 for matched rows)
+#pragma unroll
+  for (int it = 0; it < kIters; ++it) {
+    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
+    const bool lit = row0 + r < B && !((s_bm[r >> 5] >> (r & 31)) & 1u);
+    if (!__any_sync(0xffffffffu, lit)) {   // all rows of this step are matches or past the batch
+      if ((lane % G::kLPR) == 0) s_rowoff[r] = 0u;
+      continue;
+    }
     uint32_t nb = 0;
 #pragma unroll
     for (int j = 0; j < G::kSPR; ++j) {
-      const int d = (lane % G::kLPR) * 4 + j * 128;
-      const uint32_t v = ok ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0x80808080u;
+      const uint32_t v = wv[it][j];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t c = (v >> (8 * q)) & 0xffu;
@@ -736,29 +797,42 @@ __global__ void __launch_bounds__(256) k_emit(const float* __restrict__ x, Shape
     }
 #pragma unroll
     for (int off = G::kLPR / 2; off > 0; off >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, off);
-    if (ok && (lane % G::kLPR) == 0) s_rowoff[k] = nb;
+    if ((lane % G::kLPR) == 0) s_rowoff[r] = lit ? nb : 0u;
   }
   __syncthreads();
-  // exclusive scan over the literal rows
+
+  // row scan: bit offsets, literal ranks, match ranks
+  uint32_t nlit;
   {
-    constexpr int kRPT = (G::kSB + 255) / 256;
-    uint32_t loc[kRPT];
-    uint32_t sum = 0;
+    uint4 loc[kRPT];
+    uint4 sum = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const uint32_t i = tid * kRPT + k;
+      const int r = tid * kRPT + k;
+      uint4 v = make_uint4(0, 0, 0, 0);
+      if (r < G::kSB && row0 + r < B) {
+        const bool m = (s_bm[r >> 5] >> (r & 31)) & 1u;
+        v = make_uint4(s_rowoff[r], m ? 0u : 1u, m ? 1u : 0u, 0u);
+      }
       loc[k] = sum;
-      sum += i < nlit ? s_rowoff[i] : 0u;
+      sum = add4(sum, v);
     }
     uint4 tot;
-    const uint32_t ex = block_excl_scan4(make_uint4(sum, 0, 0, 0), &tot, s_warp).x;
+    const uint4 ex = block_excl_scan4(sum, &tot, s_warp);
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const uint32_t i = tid * kRPT + k;
-      if (i < nlit) s_rowoff[i] = ex + loc[k];
+      const int r = tid * kRPT + k;
+      if (r < G::kSB) {
+        const uint4 p = add4(ex, loc[k]);
+        const bool m = (s_bm[r >> 5] >> (r & 31)) & 1u;
+        s_rowoff[r] = p.x;
+        if (row0 + r < B && !m) s_litrow[p.y] = (uint16_t)r;
+        s_aux[r] = p.z;
+      }
     }
+    nlit = tot.y;
     if (tid == 0) {
-      s_rowoff[nlit] = tot.x;
+      s_rowoff[G::kSB] = tot.x;
       if (tot.x != bits) record_error(g, EBC_ERR_INTERNAL);
     }
   }
@@ -766,22 +840,32 @@ __global__ void __launch_bounds__(256) k_emit(const float* __restrict__ x, Shape
 
   // pass 2: codes (and raw outlier bits) into the bitstream
   if (bits_fit) {
-    for (uint32_t sl = warp; sl < slots; sl += 8) {
-      const uint32_t k = sl * G::kRPS + lane / G::kLPR;
-      const bool ok = k < nlit;
-      const int64_t b = row0 + (ok ? s_litrow[k] : 0);
-      uint32_t p = ok ? s_rowoff[k] : 0u;
+    uint32_t* bitbuf = in_smem ? s_bits : dstw;
+#pragma unroll
+    for (int it = 0; it < kIters; ++it) {
+      const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
+      const int64_t b = row0 + r;
+      const bool lit = b < B && !((s_bm[r >> 5] >> (r & 31)) & 1u);
+      if (!__any_sync(0xffffffffu, lit)) continue;
+      uint32_t p = s_rowoff[r];
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        const int d = (lane % G::kLPR) * 4 + j * 128;
-        const uint32_t v = ok ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0x80808080u;
+        const uint32_t v = wv[it][j];
+        // the lane's 4 codes joined into one string (right-aligned), if short and outlier-free
         uint32_t nb = 0;
+        unsigned long long str = 0;
+        bool plain = true;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
           const uint32_t c = (v >> (8 * q)) & 0xffu;
-          nb += (s_code[c] & 0xffu) + (c == 0u ? 32u : 0u);
+          const uint32_t e = s_code[c];
+          const uint32_t len = e & 0xffu;
+          str = (str << len) | (e >> 8);
+          nb += len + (c == 0u ? 32u : 0u);
+          plain = plain && c != 0u;
         }
-        if (!ok) nb = 0;
+        plain = plain && nb <= 64u;
+        if (!lit) nb = 0;
         uint32_t inc = nb;
 #pragma unroll
         for (int off = 1; off < G::kLPR; off <<= 1) {
@@ -789,8 +873,11 @@ __global__ void __launch_bounds__(256) k_emit(const float* __restrict__ x, Shape
           if ((lane % G::kLPR) >= off) inc += n;
         }
         const uint32_t slab_total = __shfl_sync(0xffffffffu, inc, (lane & ~(G::kLPR - 1)) + G::kLPR - 1);
-        if (ok) {
+        if (lit && plain) {
+          put_string(bitbuf, p + inc - nb, str, nb);
+        } else if (lit) {
           uint32_t qpos = p + inc - nb;
+          const int d = (lane % G::kLPR) * 4 + j * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
             const uint32_t c = (v >> (8 * q)) & 0xffu;
@@ -816,41 +903,28 @@ __global__ void __launch_bounds__(256) k_emit(const float* __restrict__ x, Shape
       for (uint32_t i = tid; i < nwords / 4; i += 256) dst[i] = src[i];
     }
     for (uint32_t k = tid * G::kKC; k < nlit; k += 256 * G::kKC) {
-      const uint32_t end = k + G::kKC < nlit ? s_rowoff[k + G::kKC] : s_rowoff[nlit];
-      *reinterpret_cast<uint16_t*>(out + off_chunks + 2ull * (base.y + k / G::kKC)) = (uint16_t)(end - s_rowoff[k]);
+      const uint32_t start = s_rowoff[s_litrow[k]];
+      const uint32_t end = k + G::kKC < nlit ? s_rowoff[s_litrow[k + G::kKC]] : s_rowoff[G::kSB];
+      *reinterpret_cast<uint16_t*>(out + off_chunks + 2ull * (sb.y + k / G::kKC)) = (uint16_t)(end - start);
     }
-    for (int r = tid; r < G::kSB; r += 256) {
-      const int64_t b = row0 + r;
-      if (b >= B) break;
-      const uint32_t mw = s_bm[r >> 5];
-      if ((mw >> (r & 31)) & 1u) {
-        // matches before row r = rows before r - literals before r (all rows before r exist)
-        const uint32_t rank = (uint32_t)r - (s_wpre[r >> 5] + __popc(~mw & ((1u << (r & 31)) - 1u)));
-        const uint32_t ref = __ldcg(&w.ref[(size_t)t * B + b]);
-        const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (base.z + rank);
-        if (sh.ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)ref;
-        else *reinterpret_cast<uint32_t*>(out + o) = ref;
+#pragma unroll
+    for (int k = 0; k < kRPT; ++k) {
+      const int r = tid * kRPT + k;
+      if (r < G::kSB && row0 + r < B && ((s_bm[r >> 5] >> (r & 31)) & 1u)) {
+        const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (sb.z + s_aux[r]);
+        if (sh.ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)refw[k];
+        else *reinterpret_cast<uint32_t*>(out + o) = refw[k];
       }
     }
     if (tid == 0) {
       uint32_t* rec = reinterpret_cast<uint32_t*>(out + off_seg + (unsigned long long)seg * kSegRecBytes);
-      rec[0] = base.x; rec[1] = base.y; rec[2] = base.z; rec[3] = bits;
+      rec[0] = sb.x; rec[1] = sb.y; rec[2] = sb.z; rec[3] = bits;
     }
     if (tid < G::kBmWords) {
       const int64_t wi = (int64_t)s * G::kBmWords + tid;
       if (wi < sh.nw)
         *reinterpret_cast<uint32_t*>(out + off_bitmap + 4ull * ((size_t)t * sh.nw + wi)) = s_bm[tid];
     }
-  }
-  if (tid == 0 && seg == sh.T * sh.nseg - 1) {   // the last segment completes the header
-    const unsigned long long words = (unsigned long long)base.x + nwords;
-    const unsigned long long total = off_bits + 4ull * words;
-    g->words = words;
-    g->total = total;
-    *out_bytes = total;
-    st_u64(out + 80, words);
-    st_u64(out + 128, total);
-    if (total > cap) record_error(g, EBC_ERR_CAPACITY);
   }
 }
 
@@ -874,8 +948,11 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
   k_codebook<<<sh.T > 0 ? sh.T : 1, 256, 0, st>>>(sh, ep, w, out, cap, out_bytes, epoch);
   prof_end(prof, st);
   if (grid) {
+    prof_begin(prof, "k_layout", st);
+    k_layout<<<(grid + 7) / 8, 256, 0, st>>>(sh, w, out, cap, out_bytes, epoch, sepoch);
+    prof_end(prof, st);
     prof_begin(prof, "k_emit", st);
-    k_emit<D><<<grid, 256, Geo<D>::kSegSyms * 3, st>>>(x, sh, w, out, cap, out_bytes, epoch, sepoch);
+    k_emit<D><<<grid, 256, Geo<D>::kSegSyms * 3, st>>>(x, sh, w, out, cap, epoch);
     prof_end(prof, st);
   }
 }

@@ -37,6 +37,7 @@ struct Shape {
   uint32_t S;     // dedup slots per table (power of two >= 2B, >= 64)
   int ref_bytes;  // 2 if B <= 65536 else 4
   int nsm;        // SMs of the device (grid sizing)
+  uint64_t symstride;  // bytes per table in the code scratch: B*D rounded up to 16
 };
 
 // Per-table absolute bounds of one compress call, passed by value.
@@ -70,7 +71,7 @@ struct DecTab {
 // Device scratch of a context.  Sizes follow Shape.
 struct Work {
   // compress
-  uint8_t* sym;                // [T][B][D] quantization codes (table-major)
+  uint8_t* sym;                // [T][B][D] quantization codes, table t at t * symstride (16-byte aligned)
   uint32_t* vhash;             // [T][B] dedup key
   uint32_t* vnout;             // [T][B] outliers per vector
   unsigned long long* slots;   // [T][S] (hash << 32 | first row); all ones = empty
@@ -78,8 +79,9 @@ struct Work {
   uint32_t* ref;               // [T][B] reference row of matched rows
   uint32_t* seg_hist;          // [T*nseg][256] literal code histogram per segment
   uint4* seg_cnt;              // [T*nseg] {literals, matches, outliers, chunks}
-  uint4* seg_desc;             // [T*nseg] look-back: {(scan epoch << 2) | 1 aggregate / 2 inclusive,
-                               //                      words, chunks, matches}
+  uint4* seg_desc;             // [T*nseg] look-back over k_layout CTAs: {(scan epoch << 2) | 1 aggregate /
+                               //   2 inclusive, words, chunks, matches}
+  uint4* seg_base;             // [T*nseg] absolute {words, chunks, matches} of each segment, and its bits
   uint32_t* tab_hist;          // [T][256] literal code histogram per table
   uint4* tab_cnt;              // [T] {literals, matches, outliers, chunks}
   uint32_t* tabcode;           // [T][256] code << 8 | length
