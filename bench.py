@@ -163,6 +163,7 @@ def algorithmic_bytes(kernel: str, N: int, D: int, st: dict) -> int:
     C = st["out_bytes"]
     return {
         "k_quantize": 4 * N,                               # input read once
+        "k_insert": 0,
         "k_resolve": 0,
         "k_codebook": 0,
         "k_layout": 0,
@@ -354,7 +355,7 @@ def main():
             "hbm_frac_decompress": round((4 * N + C) / (t_d / K) / 1e9 / peak, 4),
             "roofline": roofline,
             "kernels": kernels,
-            "gpu_launches": 7 * K,
+            "gpu_launches": len(prof) * K,
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": 4 * N + C,
                     "d2h_bytes_per_step": 8 + C + 4 * N},
             "cpu_baseline": cpu,

@@ -51,7 +51,7 @@ struct ebc_ctx {
   void* stage_out = nullptr;
   size_t stage_out_bytes = 0;
   unsigned long long* d_nbytes = nullptr;
-  uint32_t cepoch = 0, depoch = 0, sepoch = 0;
+  uint32_t cepoch = 0, depoch = 0;
   int nsm = 0;
   // the compress layout whose dedup table and look-back flags are known clean
   const void* clean_buf = nullptr;
@@ -137,7 +137,8 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   Work w{};
   const size_t nvec = (size_t)sh.B * sh.T, nsegT = (size_t)sh.T * sh.nseg;
   w.slots = c.take<unsigned long long>(8 * (size_t)sh.T * sh.S);
-  w.seg_desc = c.take<uint4>(16 * nsegT);
+  w.seg_desc = c.take<uint4>(16 * ((nsegT + 7) / 8));
+  w.tile_base = c.take<uint4>(16 * ((nsegT + 7) / 8));
   w.seg_base = c.take<uint4>(16 * nsegT);
   w.sym = c.take<uint8_t>((size_t)sh.T * sh.symstride);
   w.vhash = c.take<uint32_t>(4 * nvec);
@@ -347,23 +348,20 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
   c->cepoch = (c->cepoch + 1) & 0xFFFFFFu;
-  c->sepoch = c->sepoch + 1 >= (1u << 30) ? 1u : c->sepoch + 1;
   c->lastB = B;
   c->lastT = T;
   c->lastD = D;
-  // Each call leaves its dedup table empty (k_codebook) and its look-back flags
-  // tagged with its own epoch.  A new layout on this buffer starts from a reset.
+  // Each call leaves its dedup table empty (k_codebook).  A new layout on this
+  // buffer starts from a reset.
   if (T > 0 && sh.nseg > 0 && (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D)) {
-    if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess ||
-        cudaMemsetAsync(w.seg_desc, 0, 16 * (size_t)T * sh.nseg, st) != cudaSuccess)
-      return EBC_ERR_CUDA;
+    if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess) return EBC_ERR_CUDA;
     c->clean_buf = c->cbuf;
     c->cleanB = B;
     c->cleanT = T;
     c->cleanD = D;
   }
   const cudaError_t e = launch_compress(d_x, sh, ep, w, (uint8_t*)d_out, out_capacity,
-                                        (unsigned long long*)d_out_bytes, c->cepoch, c->sepoch, st, c->prof);
+                                        (unsigned long long*)d_out_bytes, c->cepoch, st, c->prof);
   if (e != cudaSuccess) c->clean_buf = nullptr;   // the dedup table may be left dirty
   return cuda_err(e);
 }

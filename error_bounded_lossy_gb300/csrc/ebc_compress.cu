@@ -3,25 +3,27 @@
 // Method: "Accelerating Communication in Deep Learning Recommendation Model
 // Training with Dual-Level Adaptive Lossy Compression" (arXiv 2407.04272),
 // §III-D (quantization encoder, vector-based LZ, Huffman) and §III-E (one
-// output buffer, chunk offsets found on the device).  Five launches on the
+// output buffer, chunk offsets found on the device).  Six launches on the
 // caller's stream:
-//   k_quantize  x -> codes, per-vector dedup key, first-occurrence hash table
+//   k_quantize  x -> codes and per-vector dedup keys (TMA-staged input tiles)
+//   k_insert    keys -> per-table first-occurrence hash table
 //   k_resolve   literal / match decision; literal code histograms per segment
 //               and per table
 //   k_codebook  per-table Huffman code; empties the hash table; the last CTA
 //               lays out the container sections and writes the header
-//   k_layout    per segment bit counts and, by a decoupled look-back over
-//               CTAs, every segment's absolute offsets
+//   k_layout    per segment bit counts and every segment's absolute offsets
+//               (per-CTA totals scanned by the last CTA)
 //   k_emit      per segment: bitstream, chunk index, references, records
 // All offsets come from prefix sums, never from atomic reservations, so the
 // container is byte-identical from run to run.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <cstdint>
 
 #include "ebc_internal.cuh"
 
 namespace ebc {
-
-constexpr int kSpinLimit = 1 << 20;   // polls of one look-back flag before giving up
 
 // ---------------------------------------------------------------------------
 // Quantization encoder (§III-D), no predictor (§III-B observation 1): the code
@@ -90,64 +92,148 @@ __device__ __forceinline__ uint32_t dedup_lookup(const unsigned long long* slots
 }
 
 // ---------------------------------------------------------------------------
-// k_quantize: one CTA per (table, segment), 8 warps, each warp a run of
-// 128-element slabs (lane = 4 consecutive elements, one 16-byte load).
-// The dedup key of a vector is the wrapping sum over its 4-code words w_k of
-// lowbias32(w_k + k * 0x9E3779B9) plus lowbias32(raw ^ (d + 1) * 0x85EBCA6B)
-// for each outlier at position d.  Keys enter the hash table after the
-// segment is quantized, one thread per row.
+// Tensor-memory-accelerator (TMA) staging of input tiles.
 // ---------------------------------------------------------------------------
+constexpr int kWaitLimit = 1 << 22;   // polls of an mbarrier before giving up
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0u;
+}
+// Bounded wait for phase `parity` of an mbarrier; false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (int i = 0; i < kWaitLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
+          smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Box geometry of one segment's input tile x[row0 .. row0+SB)[t][0 .. D):
+// boxes of at most 256 rows x 256 elements; box (rb, db) lands at
+// ((rb * kNBoxD + db) * kBoxR) * kBoxD floats in the stage.
 template <int D>
-__global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ x, Shape sh, EbParams ep, Work w) {
-  using G = Geo<D>;
-  __shared__ uint32_t s_key[G::kSB];
-  const int seg = blockIdx.x;
+struct QGeo {
+  static constexpr int kBoxD = D < 256 ? D : 256;
+  static constexpr int kBoxR = Geo<D>::kSB < 256 ? Geo<D>::kSB : 256;
+  static constexpr int kNBoxD = D / kBoxD;
+  static constexpr int kNBoxR = Geo<D>::kSB / kBoxR;
+  static constexpr int kStageFloats = Geo<D>::kSegSyms;
+  static constexpr uint32_t kStageBytes = (uint32_t)kStageFloats * 4u;
+  __device__ static __forceinline__ int offset(int r, int d) {
+    return (((r / kBoxR) * kNBoxD + d / kBoxD) * kBoxR + r % kBoxR) * kBoxD + d % kBoxD;
+  }
+};
+
+template <int D>
+__device__ __forceinline__ void issue_segment_tile(float* stage, const CUtensorMap* map, uint64_t* bar, const Shape& sh,
+                                                   int seg) {
+  using Q = QGeo<D>;
   const int t = seg / sh.nseg;
   const int s = seg - t * sh.nseg;
+  mbar_expect_tx(bar, Q::kStageBytes);
+#pragma unroll
+  for (int rb = 0; rb < Q::kNBoxR; ++rb)
+#pragma unroll
+    for (int db = 0; db < Q::kNBoxD; ++db)
+      tma_load_3d(stage + ((rb * Q::kNBoxD + db) * Q::kBoxR) * Q::kBoxD, map, bar, db * Q::kBoxD, t,
+                  s * Geo<D>::kSB + rb * Q::kBoxR);
+}
+
+// ---------------------------------------------------------------------------
+// k_quantize: persistent CTAs, each taking segments blockIdx.x, +gridDim.x, ...
+// A segment's input tile (rows of one table) arrives in shared memory by TMA
+// into one of two stages, so the next tile streams in while the current one is
+// quantized.  8 warps, each a run of 128-element
+// slabs (lane = 4 consecutive elements).  The dedup key of a vector is the
+// wrapping sum over its 4-code words w_k of lowbias32(w_k + k * 0x9E3779B9)
+// plus lowbias32(raw ^ (d + 1) * 0x85EBCA6B) for each outlier at position d.
+// ---------------------------------------------------------------------------
+template <int D>
+__global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtensorMap tmap, Shape sh, EbParams ep,
+                                                   Work w) {
+  using G = Geo<D>;
+  using Q = QGeo<D>;
+  extern __shared__ __align__(128) float s_x[];   // 2 stages of kStageFloats
+  __shared__ __align__(8) uint64_t s_bar[2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (s == 0) {   // per-call table accumulators that k_resolve adds to
-    w.tab_hist[(size_t)t * 256 + tid] = 0u;
-    if (tid == 0) w.tab_cnt[t] = make_uint4(0, 0, 0, 0);
-  }
-  const float eb = ep.eb[t];
-  const float ebx2 = __fmul_rn(2.0f, eb);
-  const float inv = __fdiv_rn(1.0f, ebx2);
+  const int nsegT = sh.T * sh.nseg;
   const int64_t B = sh.B;
-  const int T = sh.T;
-  const int64_t row0 = (int64_t)s * G::kSB;
   const unsigned long long pol = l2_evict_last();
-  uint32_t acc = 0, nout = 0;
-  constexpr int kBatch = 8;
-#pragma unroll 1
-  for (int i0 = 0; i0 < G::kSlabsPerWarp; i0 += kBatch) {
-    float4 v[kBatch];
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int e = (warp * G::kSlabsPerWarp + i0 + k) * 128 + lane * 4;
-      const int64_t b = row0 + e / D;
-      const int d = e % D;
-      v[k] = b < B ? ld_stream_f4(x + ((size_t)(b * T + t) * D + d)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  if (tid == 0) {
+    mbar_init(&s_bar[0], 1);
+    mbar_init(&s_bar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    if ((int)blockIdx.x < nsegT) issue_segment_tile<D>(s_x, &tmap, &s_bar[0], sh, blockIdx.x);
+    if ((int)(blockIdx.x + gridDim.x) < nsegT)
+      issue_segment_tile<D>(s_x + Q::kStageFloats, &tmap, &s_bar[1], sh, blockIdx.x + gridDim.x);
+  }
+  __syncthreads();
+  uint32_t parity = 0;   // bit i: phase of stage i
+  int i = 0;
+  for (int seg = blockIdx.x; seg < nsegT; seg += gridDim.x, ++i) {
+    const int stg = i & 1;
+    const float* xs = s_x + stg * Q::kStageFloats;
+    const int t = seg / sh.nseg;
+    const int s = seg - t * sh.nseg;
+    const int64_t row0 = (int64_t)s * G::kSB;
+    if (s == 0) {   // per-call table accumulators that k_resolve adds to
+      w.tab_hist[(size_t)t * 256 + tid] = 0u;
+      if (tid == 0) w.tab_cnt[t] = make_uint4(0, 0, 0, 0);
     }
-#pragma unroll
-    for (int k = 0; k < kBatch; ++k) {
-      const int slab = warp * G::kSlabsPerWarp + i0 + k;
+    const float eb = ep.eb[t];
+    const float ebx2 = __fmul_rn(2.0f, eb);
+    const float inv = __fdiv_rn(1.0f, ebx2);
+    const bool arrived = mbar_wait(&s_bar[stg], (parity >> stg) & 1u);
+    if (__syncthreads_or(!arrived)) {   // the whole CTA stops together
+      if (tid == 0) record_error(w.glob, EBC_ERR_DEVICE_TIMEOUT);
+      // a copy may still be in flight: wait for it once more (bounded), then stop
+      if (!arrived) mbar_wait(&s_bar[stg], (parity >> stg) & 1u);
+      return;
+    }
+    parity ^= 1u << stg;
+    uint32_t acc = 0, nout = 0;
+#pragma unroll 4
+    for (int k = 0; k < G::kSlabsPerWarp; ++k) {
+      const int slab = warp * G::kSlabsPerWarp + k;
       const int e = slab * 128 + lane * 4;
       const int r = e / D;
       const int64_t b = row0 + r;
       const int d = e % D;
       const bool valid = b < B;
-      const uint32_t c0 = quantize_one(v[k].x, eb, ebx2, inv);
-      const uint32_t c1 = quantize_one(v[k].y, eb, ebx2, inv);
-      const uint32_t c2 = quantize_one(v[k].z, eb, ebx2, inv);
-      const uint32_t c3 = quantize_one(v[k].w, eb, ebx2, inv);
+      const float4 v = *reinterpret_cast<const float4*>(xs + Q::offset(r, d));
+      const uint32_t c0 = quantize_one(v.x, eb, ebx2, inv);
+      const uint32_t c1 = quantize_one(v.y, eb, ebx2, inv);
+      const uint32_t c2 = quantize_one(v.z, eb, ebx2, inv);
+      const uint32_t c3 = quantize_one(v.w, eb, ebx2, inv);
       const uint32_t word = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
-      if (valid) st_keep_u32(reinterpret_cast<uint32_t*>(w.sym + (size_t)t * sh.symstride + (size_t)b * D + d), word, pol);
+      if (valid)
+        st_keep_u32(reinterpret_cast<uint32_t*>(w.sym + (size_t)t * sh.symstride + (size_t)b * D + d), word, pol);
       acc += lowbias32(word + (uint32_t)(d >> 2) * 0x9E3779B9u);
       if ((c0 == 0u) | (c1 == 0u) | (c2 == 0u) | (c3 == 0u)) {
-        if (c0 == 0u) { acc += lowbias32(__float_as_uint(v[k].x) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu); ++nout; }
-        if (c1 == 0u) { acc += lowbias32(__float_as_uint(v[k].y) ^ (uint32_t)(d + 2) * 0x85EBCA6Bu); ++nout; }
-        if (c2 == 0u) { acc += lowbias32(__float_as_uint(v[k].z) ^ (uint32_t)(d + 3) * 0x85EBCA6Bu); ++nout; }
-        if (c3 == 0u) { acc += lowbias32(__float_as_uint(v[k].w) ^ (uint32_t)(d + 4) * 0x85EBCA6Bu); ++nout; }
+        if (c0 == 0u) { acc += lowbias32(__float_as_uint(v.x) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu); ++nout; }
+        if (c1 == 0u) { acc += lowbias32(__float_as_uint(v.y) ^ (uint32_t)(d + 2) * 0x85EBCA6Bu); ++nout; }
+        if (c2 == 0u) { acc += lowbias32(__float_as_uint(v.z) ^ (uint32_t)(d + 3) * 0x85EBCA6Bu); ++nout; }
+        if (c3 == 0u) { acc += lowbias32(__float_as_uint(v.w) ^ (uint32_t)(d + 4) * 0x85EBCA6Bu); ++nout; }
       }
       if ((slab + 1) % G::kSPR == 0) {            // the row ends with this slab
 #pragma unroll
@@ -156,7 +242,6 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ x, S
           nout += __shfl_xor_sync(0xffffffffu, nout, off);
         }
         if (valid && (lane % G::kLPR) == 0) {
-          s_key[r] = acc;
           w.vhash[(size_t)t * B + b] = acc;
           w.vnout[(size_t)t * B + b] = nout;
         }
@@ -164,13 +249,23 @@ __global__ void __launch_bounds__(256) k_quantize(const float* __restrict__ x, S
         nout = 0;
       }
     }
+    __syncthreads();   // the stage is consumed: refill it with the segment two steps ahead
+    if (tid == 0 && seg + 2 * (int)gridDim.x < nsegT)
+      issue_segment_tile<D>(s_x + stg * Q::kStageFloats, &tmap, &s_bar[stg], sh, seg + 2 * gridDim.x);
   }
-  __syncthreads();
-  unsigned long long* slots = w.slots + (size_t)t * sh.S;
-  for (int r = tid; r < G::kSB; r += 256) {
-    const int64_t b = row0 + r;
-    if (b < B) dedup_insert(slots, sh.S, s_key[r], (uint32_t)b, w.glob);
-  }
+}
+
+// ---------------------------------------------------------------------------
+// k_insert: one thread per (table, row) enters the row's key into the table's
+// first-occurrence hash table (all keys of the call, in one wave).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) k_insert(Shape sh, Work w) {
+  const unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const unsigned long long nvec = (unsigned long long)sh.B * sh.T;
+  if (i >= nvec) return;
+  const int t = (int)(i / (unsigned long long)sh.B);
+  const uint32_t b = (uint32_t)(i - (unsigned long long)t * sh.B);
+  dedup_insert(w.slots + (size_t)t * sh.S, sh.S, __ldcg(&w.vhash[i]), b, w.glob);
 }
 
 __device__ __forceinline__ bool has_zero_byte(uint32_t v) {
@@ -537,7 +632,6 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     }
     if (status != EBC_OK) record_error(g, status);
     g->cstat = status_word(epoch, status);
-    g->tile_ctr = 0u;
     g->done = 0u;
   }
 }
@@ -563,65 +657,6 @@ __device__ __forceinline__ void put_bits(uint32_t* s, uint32_t p, uint32_t code,
   if (lo) atomicOr(&s[(p >> 5) + 1], lo);
 }
 
-// Look-back descriptors: {(scan epoch << 2) | state, words, chunks, matches},
-// state 1 = aggregate of the segment alone, 2 = inclusive prefix.  Each is
-// written and read with one 16-byte access, so status and values never tear
-// apart and no fence is needed between them.
-__device__ __forceinline__ void st_desc(uint4* p, uint4 v) {
-  asm volatile("st.volatile.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
-               "r"(v.w)
-               : "memory");
-}
-__device__ __forceinline__ uint4 ld_desc(const uint4* p) {
-  uint4 v;
-  asm volatile("ld.volatile.global.v4.u32 {%0, %1, %2, %3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p)
-               : "memory");
-  return v;
-}
-
-// Decoupled look-back over segments in (table, segment) order, by the whole
-// CTA: thread k inspects segment seg-1-k of the current window of 256, so the
-// known-prefix frontier advances by up to 256 segments per round trip.  Returns
-// the sum {0, words, chunks, matches} of all earlier segments.  Each wait is
-// bounded; on time-out that segment counts as zero and the context records
-// EBC_ERR_DEVICE_TIMEOUT.
-__device__ uint4 lookback(const Work& w, int seg, uint32_t sepoch, uint4* s_warp, int* s_stop) {
-  const int tid = threadIdx.x;
-  uint4 excl = make_uint4(0, 0, 0, 0);
-  for (int j = seg - 1; j >= 0; j -= 256) {
-    const int k = j - tid;
-    uint32_t st = 2u;
-    uint4 v = make_uint4(0, 0, 0, 0);
-    if (k >= 0) {
-      v = ld_desc(w.seg_desc + k);
-      for (int spin = 0; (v.x >> 2) != sepoch && spin < kSpinLimit; ++spin) {
-        __nanosleep(64);
-        v = ld_desc(w.seg_desc + k);
-      }
-      if ((v.x >> 2) != sepoch) {
-        record_error(w.glob, EBC_ERR_DEVICE_TIMEOUT);
-        v = make_uint4(0, 0, 0, 0);
-      } else {
-        st = v.x & 3u;
-      }
-      v.x = 0;
-    }
-    if (tid == 0) *s_stop = 256;
-    __syncthreads();
-    if (st == 2u) atomicMin(s_stop, tid);   // the nearest segment with a known inclusive prefix
-    __syncthreads();
-    const int stop = *s_stop;
-    if (tid > stop) v = make_uint4(0, 0, 0, 0);
-    uint4 tot;
-    block_excl_scan4(v, &tot, s_warp);
-    excl = add4(excl, tot);
-    if (stop < 256) break;
-  }
-  return excl;
-}
-
 // Rows of bitmap word wi of a segment that exist in the batch.
 __device__ __forceinline__ uint32_t valid_mask(int64_t B, int64_t row0, int wi) {
   const int64_t nv = B - (row0 + (int64_t)wi * 32);
@@ -629,27 +664,26 @@ __device__ __forceinline__ uint32_t valid_mask(int64_t B, int64_t row0, int wi) 
 }
 
 // ---------------------------------------------------------------------------
-// k_layout: absolute offsets of every segment.  One warp per segment computes
-// its bit count (sum over codes of count * length, plus 32 raw bits per
-// outlier) from its histogram; a CTA covers 8 consecutive segments and takes
-// its place in (table, segment) order by a decoupled look-back over CTAs.  The
-// CTA holding the last segment completes the header (bitstream words, total
-// size) and the capacity check.
+// k_layout: per-segment aggregates.  One warp per segment computes its bit
+// count (sum over codes of count * length, plus 32 raw bits per outlier) from
+// its histogram; a CTA covers 8 consecutive segments and stores, per segment,
+// {words, chunks, matches, bits} relative to the CTA's first segment and, per
+// CTA, the totals.  The last CTA to finish turns the CTA totals into absolute
+// bases (an exclusive scan) and completes the header (bitstream words, total
+// size) and the capacity check.  No CTA waits on another.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __restrict__ out, unsigned long long cap,
-                                                 unsigned long long* out_bytes, uint32_t epoch, uint32_t sepoch) {
-  __shared__ uint4 s_warp[8];
+                                                 unsigned long long* out_bytes, uint32_t epoch) {
   __shared__ uint4 s_agg[8];
-  __shared__ uint4 s_base;
-  __shared__ int s_tile, s_stop;
+  __shared__ uint4 s_warp[8];
+  __shared__ int s_last;
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (tid == 0) s_tile = (int)atomicAdd(&g->tile_ctr, 1u);
-  __syncthreads();
-  const int tile = s_tile;
+  const int tile = blockIdx.x;
+  const int ntiles = gridDim.x;
   const int nsegT = sh.T * sh.nseg;
   const int seg = tile * 8 + warp;
-  uint4 a = make_uint4(0, 0, 0, 0);   // {-, words, chunks, matches}
+  uint4 a = make_uint4(0, 0, 0, 0);   // {words, chunks, matches, -}
   uint32_t bits = 0;
   if (seg < nsegT) {
     const int t = seg / sh.nseg;
@@ -662,26 +696,38 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
     if (lane == 0) bits += 32u * h0.x;   // symbol 0: the outliers' raw bits
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, off);
-    a = make_uint4(0u, ((bits + 127u) >> 7) * 4u, cnt.w, cnt.y);
+    a = make_uint4(((bits + 127u) >> 7) * 4u, cnt.w, cnt.y, 0u);
   }
   if (lane == 0) s_agg[warp] = a;
   __syncthreads();
-  uint4 tile_agg = make_uint4(0, 0, 0, 0), warp_excl = make_uint4(0, 0, 0, 0);
-  for (int i = 0; i < 8; ++i) {
-    if (i < warp) warp_excl = add4(warp_excl, s_agg[i]);
-    tile_agg = add4(tile_agg, s_agg[i]);
+  if (seg < nsegT && lane == 0) {
+    uint4 pre = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < warp; ++i) pre = add4(pre, s_agg[i]);
+    w.seg_base[seg] = make_uint4(pre.x, pre.y, pre.z, bits);   // relative to the tile; made absolute by k_emit
   }
-  if (tid == 0) st_desc(w.seg_desc + tile, make_uint4((sepoch << 2) | 1u, tile_agg.y, tile_agg.z, tile_agg.w));
-  const uint4 ex = lookback(w, tile, sepoch, s_warp, &s_stop);
   if (tid == 0) {
-    s_base = ex;
-    st_desc(w.seg_desc + tile, make_uint4((sepoch << 2) | 2u, ex.y + tile_agg.y, ex.z + tile_agg.z, ex.w + tile_agg.w));
+    uint4 tot = make_uint4(0, 0, 0, 0);
+    for (int i = 0; i < 8; ++i) tot = add4(tot, s_agg[i]);
+    w.seg_desc[tile] = tot;
   }
+  // ---- the last CTA: exclusive scan of the CTA totals, header completion ----
+  __threadfence();
   __syncthreads();
-  const uint4 base = add4(s_base, warp_excl);
-  if (seg < nsegT && lane == 0) w.seg_base[seg] = make_uint4(base.y, base.z, base.w, bits);
-  if (seg == nsegT - 1 && lane == 0) {   // the last segment completes the header
-    const unsigned long long words = (unsigned long long)base.y + a.y;
+  if (tid == 0) s_last = atomicAdd(&g->done, 1u) == gridDim.x - 1;
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  uint4 carry = make_uint4(0, 0, 0, 0);
+  for (int base = 0; base < ntiles; base += 256) {
+    const int i = base + tid;
+    const uint4 v = i < ntiles ? __ldcg(&w.seg_desc[i]) : make_uint4(0, 0, 0, 0);
+    uint4 tot;
+    const uint4 ex = block_excl_scan4(v, &tot, s_warp);
+    if (i < ntiles) w.tile_base[i] = add4(carry, ex);
+    carry = add4(carry, tot);
+  }
+  if (tid == 0) {
+    const unsigned long long words = carry.x;
     const unsigned long long off_bits = __ldcg(&g->off_bits);
     const unsigned long long total = off_bits + 4ull * words;
     g->words = words;
@@ -695,6 +741,7 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
       record_error(g, EBC_ERR_CAPACITY);
       g->cstat = status_word(epoch, EBC_ERR_CAPACITY);
     }
+    g->done = 0u;
   }
 }
 
@@ -734,7 +781,9 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
 
   // ---- every global read, issued together ----
-  const uint4 sb = __ldcg(&w.seg_base[seg]);   // {words, chunks, matches, bits}
+  const uint4 sbr = __ldcg(&w.seg_base[seg]);       // {words, chunks, matches} within its 8-segment tile, bits
+  const uint4 tb = __ldcg(&w.tile_base[seg >> 3]);  // absolute base of that tile
+  const uint4 sb = make_uint4(tb.x + sbr.x, tb.y + sbr.y, tb.z + sbr.z, sbr.w);
   const uint32_t mycode = __ldcg(&w.tabcode[(size_t)t * 256 + tid]);
   uint32_t bmw = 0;
   if (tid < G::kBmWords) {
@@ -934,11 +983,25 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
 template <int D>
 static void launch_compress_d(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
                               unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                              uint32_t sepoch, cudaStream_t st, Prof* prof) {
+                              cudaStream_t st, Prof* prof, const CUtensorMap* xmap) {
   const unsigned grid = (unsigned)(sh.T * sh.nseg);
   if (grid) {
+    // persistent quantize: as many CTAs as fit at once (two input stages each), at most one per segment
+    static int per_sm = -1;
+    const int smem = 2 * (int)QGeo<D>::kStageBytes;
+    if (per_sm < 0) {
+      cudaFuncSetAttribute(k_quantize<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize<D>, 256, smem) != cudaSuccess ||
+          per_sm < 1)
+        per_sm = 1;
+    }
+    unsigned qgrid = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm);
+    if (qgrid > grid) qgrid = grid;
     prof_begin(prof, "k_quantize", st);
-    k_quantize<D><<<grid, 256, 0, st>>>(x, sh, ep, w);
+    k_quantize<D><<<qgrid, 256, smem, st>>>(*xmap, sh, ep, w);
+    prof_end(prof, st);
+    prof_begin(prof, "k_insert", st);
+    k_insert<<<(unsigned)(((unsigned long long)sh.B * sh.T + 255) / 256), 256, 0, st>>>(sh, w);
     prof_end(prof, st);
     prof_begin(prof, "k_resolve", st);
     k_resolve<D><<<grid, 256, 0, st>>>(x, sh, w);
@@ -949,7 +1012,7 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
   prof_end(prof, st);
   if (grid) {
     prof_begin(prof, "k_layout", st);
-    k_layout<<<(grid + 7) / 8, 256, 0, st>>>(sh, w, out, cap, out_bytes, epoch, sepoch);
+    k_layout<<<(grid + 7) / 8, 256, 0, st>>>(sh, w, out, cap, out_bytes, epoch);
     prof_end(prof, st);
     prof_begin(prof, "k_emit", st);
     k_emit<D><<<grid, 256, Geo<D>::kSegSyms * 3, st>>>(x, sh, w, out, cap, epoch);
@@ -957,18 +1020,58 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
   }
 }
 
+// Tensor map of x viewed as [B][T][D] (dims innermost first: D, T, B), boxes of
+// min(D, 256) elements x 1 table x min(SB, 256) rows; rows past B read as zero.
+template <int D>
+static cudaError_t make_x_map(CUtensorMap* map, const float* x, const Shape& sh) {
+  static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  if (!encode) {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !fn)
+      return cudaErrorNotSupported;
+    encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)sh.T, (cuuint64_t)sh.B};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 4u, (cuuint64_t)sh.T * D * 4u};
+  const cuuint32_t box[3] = {(cuuint32_t)QGeo<D>::kBoxD, 1u, (cuuint32_t)QGeo<D>::kBoxR};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(x), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_compress(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
                             unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                            uint32_t sepoch, cudaStream_t st, Prof* prof) {
+                            cudaStream_t st, Prof* prof) {
+  CUtensorMap xmap;
+  if (sh.T > 0 && sh.nseg > 0) {
+    cudaError_t e = cudaSuccess;
+    switch (sh.D) {
+      case 4: e = make_x_map<4>(&xmap, x, sh); break;
+      case 8: e = make_x_map<8>(&xmap, x, sh); break;
+      case 16: e = make_x_map<16>(&xmap, x, sh); break;
+      case 32: e = make_x_map<32>(&xmap, x, sh); break;
+      case 64: e = make_x_map<64>(&xmap, x, sh); break;
+      case 128: e = make_x_map<128>(&xmap, x, sh); break;
+      case 256: e = make_x_map<256>(&xmap, x, sh); break;
+      case 512: e = make_x_map<512>(&xmap, x, sh); break;
+      default: return cudaErrorInvalidValue;
+    }
+    if (e != cudaSuccess) return e;
+  }
   switch (sh.D) {
-    case 4: launch_compress_d<4>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
-    case 8: launch_compress_d<8>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
-    case 16: launch_compress_d<16>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
-    case 32: launch_compress_d<32>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
-    case 64: launch_compress_d<64>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
-    case 128: launch_compress_d<128>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
-    case 256: launch_compress_d<256>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
-    case 512: launch_compress_d<512>(x, sh, ep, w, out, cap, out_bytes, epoch, sepoch, st, prof); break;
+    case 4: launch_compress_d<4>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 8: launch_compress_d<8>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 16: launch_compress_d<16>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 32: launch_compress_d<32>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 64: launch_compress_d<64>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 128: launch_compress_d<128>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 256: launch_compress_d<256>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 512: launch_compress_d<512>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

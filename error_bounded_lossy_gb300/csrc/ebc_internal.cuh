@@ -51,8 +51,7 @@ struct Glob {
   unsigned int cstat;     // (epoch << 8) | status of the last compress
   unsigned int dstat;     // (epoch << 8) | status of the last decompress
   unsigned int sticky;    // first device error since the last query (0 = none)
-  unsigned int tile_ctr;  // next segment of k_emit (dynamic, in scheduling order)
-  unsigned int pad[3];
+  unsigned int pad[4];
   unsigned long long n_lit, n_match, n_out, n_chunks, words;
   unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
 };
@@ -79,9 +78,9 @@ struct Work {
   uint32_t* ref;               // [T][B] reference row of matched rows
   uint32_t* seg_hist;          // [T*nseg][256] literal code histogram per segment
   uint4* seg_cnt;              // [T*nseg] {literals, matches, outliers, chunks}
-  uint4* seg_desc;             // [T*nseg] look-back over k_layout CTAs: {(scan epoch << 2) | 1 aggregate /
-                               //   2 inclusive, words, chunks, matches}
-  uint4* seg_base;             // [T*nseg] absolute {words, chunks, matches} of each segment, and its bits
+  uint4* seg_desc;             // [ceil(T*nseg/8)] totals {words, chunks, matches} of each 8-segment tile
+  uint4* tile_base;            // [ceil(T*nseg/8)] absolute base of each tile
+  uint4* seg_base;             // [T*nseg] {words, chunks, matches} relative to the tile, and the bit count
   uint32_t* tab_hist;          // [T][256] literal code histogram per table
   uint4* tab_cnt;              // [T] {literals, matches, outliers, chunks}
   uint32_t* tabcode;           // [T][256] code << 8 | length
@@ -142,7 +141,7 @@ void prof_end(Prof* p, cudaStream_t st);
 // ---- launchers (one per direction; D is dispatched to the templated kernels) ----
 cudaError_t launch_compress(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
                             unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                            uint32_t scan_epoch, cudaStream_t st, Prof* prof);
+                            cudaStream_t st, Prof* prof);
 cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const Shape& sh, const Work& w,
                               float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof);
 cudaError_t set_kernel_attributes();
