@@ -24,11 +24,12 @@ __all__ = [
     "ebc_version", "ebc_strerror", "ebc_create", "ebc_destroy", "ebc_set_error_bounds", "ebc_get_error_bounds",
     "ebc_compress_bound", "ebc_compress", "ebc_decompress", "ebc_compress_host", "ebc_decompress_host",
     "ebc_get_stats", "ebc_last_device_error", "ebc_set_profiling", "ebc_get_profile", "Codec",
-    "EXPORTED_SYMBOLS", "EbcKernelTime",
+    "EXPORTED_SYMBOLS", "EbcKernelTime", "EBC_ERR_SCRATCH_LIMIT", "ebc_decompress_noalloc",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
 EBC_ERR_DEVICE_TIMEOUT, EBC_ERR_CUDA, EBC_ERR_NO_DEVICE, EBC_ERR_INTERNAL = 4, 5, 6, 7
+EBC_ERR_SCRATCH_LIMIT = 8
 EBC_DECAY_NONE, EBC_DECAY_LINEAR, EBC_DECAY_STEPWISE, EBC_DECAY_DROP, EBC_DECAY_LOG = 0, 1, 2, 3, 4
 DECAY = {"none": 0, "linear": 1, "stepwise": 2, "drop": 3, "log": 4}
 
@@ -36,6 +37,7 @@ EXPORTED_SYMBOLS = (
     "ebc_version", "ebc_strerror", "ebc_create", "ebc_destroy", "ebc_set_error_bounds",
     "ebc_get_error_bounds", "ebc_compress_bound", "ebc_compress", "ebc_decompress", "ebc_compress_host",
     "ebc_decompress_host", "ebc_get_stats", "ebc_last_device_error", "ebc_set_profiling", "ebc_get_profile",
+    "ebc_decompress_noalloc",
 )
 
 
@@ -92,6 +94,7 @@ def lib():
                 "ebc_last_device_error": (I, [P]),
                 "ebc_set_profiling": (I, [P, I]),
                 "ebc_get_profile": (I, [P, ctypes.POINTER(EbcKernelTime), I, ctypes.POINTER(I)]),
+                "ebc_decompress_noalloc": (I, [P, U64, P, I64, I, I, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -142,6 +145,11 @@ def ebc_compress(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_bytes, st
 
 def ebc_decompress(ctx, d_in, in_bytes, d_xhat, B, T, D, stream) -> int:
     return lib().ebc_decompress(ctx, d_in, int(in_bytes), d_xhat, int(B), int(T), int(D), stream)
+
+
+def ebc_decompress_noalloc(d_in, in_bytes, d_xhat, B, T, D, stream) -> int:
+    """Allocation-free, synchronous decode (no context; static device scratch)."""
+    return lib().ebc_decompress_noalloc(d_in, int(in_bytes), d_xhat, int(B), int(T), int(D), stream)
 
 
 def ebc_compress_host(ctx, h_x, B, T, D, eb_ptr, h_out, out_capacity, out_bytes_ptr, stream) -> int:

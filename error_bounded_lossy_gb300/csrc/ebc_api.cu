@@ -4,6 +4,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "ebc_internal.cuh"
@@ -204,6 +205,7 @@ const char* ebc_strerror(int code) {
     case EBC_ERR_CUDA: return "CUDA runtime error";
     case EBC_ERR_NO_DEVICE: return "no usable sm_103 device";
     case EBC_ERR_INTERNAL: return "internal invariant failed on the device";
+    case EBC_ERR_SCRATCH_LIMIT: return "shape needs more than the 16 MiB static scratch of ebc_decompress_noalloc";
     default: return "unknown error";
   }
 }
@@ -504,6 +506,95 @@ int ebc_get_profile(ebc_ctx* c, ebc_kernel_time* out, int capacity, int* count) 
   p->used = 0;
   *count = n;
   return EBC_OK;
+}
+
+
+}  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free decompression
+//
+// Some callers cannot allocate device memory when they decode: a process whose
+// device memory has been handed to another allocator (a framework's caching
+// pool) gets an out-of-memory error or fragmentation from cudaMalloc, and in a
+// latency-bound loop cudaMalloc/cudaFree synchronise the device and stall the
+// other streams.  ebc_decompress_noalloc serves them: it runs the same decoder
+// kernels as ebc_decompress, but their scratch (status block, decode tables,
+// chunk descriptors, literal-row and match lists) is carved from the static
+// device array below instead of a context's buffer.
+// ---------------------------------------------------------------------------
+
+// The array is part of this library's device image: every GPU on which the
+// image is loaded holds these 16 MiB until the process exits.  Its first 256
+// bytes hold the status block (Glob); the decoder's tables follow.
+constexpr size_t kNoAllocScratchBytes = 16u << 20;
+constexpr size_t kNoAllocGlobBytes = 256;
+static_assert(sizeof(Glob) <= kNoAllocGlobBytes, "status block does not fit its slot");
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kNoAllocMaxDevices = 64;
+struct NoAllocDevice {
+  bool ready = false;
+  unsigned char* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+  int nsm = 0;
+};
+std::mutex g_noalloc_mu;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+
+// Once per device, with that device current: check it is an sm_103 part and
+// look up the device address of the scratch array.  (On the host the array's
+// name is only a stand-in symbol, never a pointer a kernel may be given.)
+int noalloc_setup(int dev, NoAllocDevice** out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  NoAllocDevice& d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, nsm = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return EBC_ERR_NO_DEVICE;
+    if (!(major == 10 && minor == 3)) return EBC_ERR_NO_DEVICE;
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return EBC_ERR_CUDA;
+    d.scratch = static_cast<unsigned char*>(p);
+    d.nsm = nsm;
+    d.ready = true;
+  }
+  *out = &d;
+  return EBC_OK;
+}
+}  // namespace
+
+extern "C" {
+
+int ebc_decompress_noalloc(const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
+                           void* stream) {
+  if (!shape_ok(B, T, D) || !d_in || !aligned16(d_in)) return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T * D;
+  if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kNoAllocMaxDevices) return EBC_ERR_NO_DEVICE;
+  NoAllocDevice* nd = nullptr;
+  int rc = noalloc_setup(dev, &nd);
+  if (rc) return rc;
+  const Shape sh = make_shape(B, T, D, nd->nsm);
+  size_t need = 0;
+  carve_decompress(nullptr, sh, nullptr, &need);
+  if (need > kNoAllocScratchBytes - kNoAllocGlobBytes) return EBC_ERR_SCRATCH_LIMIT;
+  Glob* g = reinterpret_cast<Glob*>(nd->scratch);
+  const Work w = carve_decompress(nd->scratch + kNoAllocGlobBytes, sh, g, &need);
+  cudaStream_t st = (cudaStream_t)stream;
+  // The array keeps whatever the previous call left; only the status block
+  // must start at zero (the tables are written before they are read).
+  if (cudaMemsetAsync(g, 0, sizeof(Glob), st) != cudaSuccess) return EBC_ERR_CUDA;
+  if (launch_decompress((const uint8_t*)d_in, in_bytes, sh, w, d_xhat, 1u, st, nullptr) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  unsigned int code = 0;
+  if (cudaMemcpyAsync(&code, &g->sticky, sizeof code, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return EBC_ERR_CUDA;
+  return (int)code;
 }
 
 }  // extern "C"

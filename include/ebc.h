@@ -70,7 +70,8 @@ enum {
   EBC_ERR_DEVICE_TIMEOUT = 4, /* a bounded device-side wait ran out           */
   EBC_ERR_CUDA = 5,           /* a CUDA runtime call failed                   */
   EBC_ERR_NO_DEVICE = 6,      /* no usable sm_103 device                      */
-  EBC_ERR_INTERNAL = 7        /* an internal invariant failed on the device   */
+  EBC_ERR_INTERNAL = 7,       /* an internal invariant failed on the device   */
+  EBC_ERR_SCRATCH_LIMIT = 8   /* shape too large for ebc_decompress_noalloc   */
 };
 
 /* Iteration-wise decay of the error bound, §III-C "Iteration-wise
@@ -160,6 +161,34 @@ int ebc_compress_host(ebc_ctx* ctx, const float* h_x, int64_t B, int T, int D, c
                       void* h_out, uint64_t out_capacity, uint64_t* out_bytes, void* stream);
 int ebc_decompress_host(ebc_ctx* ctx, const void* h_in, uint64_t in_bytes, float* h_xhat,
                         int64_t B, int T, int D, void* stream);
+
+/* Allocation-free decompression.  The paper has no counterpart: this entry
+ * point exists for callers that cannot allocate device memory while they
+ * decode -- a process that has handed its device memory to another allocator
+ * (where cudaMalloc fails or fragments that pool), or a latency-bound loop in
+ * which cudaMalloc/cudaFree would synchronise the device and stall other
+ * streams.  It needs no context and allocates nothing: it decodes with the
+ * same kernels and gives the same result as ebc_decompress, with their
+ * scratch in one static 16 MiB device array of this library (held by every GPU
+ * that loads the library until the process exits).
+ *
+ * Arguments as ebc_decompress; the caller owns d_in and d_xhat.  It works on
+ * the current device.  Its first call on a device sets up that device (checks
+ * for sm_103 and looks up the array's device address) and should come before
+ * any stream capture.  Synchronous: it enqueues the decode on `stream`, waits
+ * for the stream, and returns EBC_OK or the decoder's error (EBC_ERR_CORRUPT,
+ * EBC_ERR_INVALID_ARG for a container of another shape, EBC_ERR_INTERNAL).
+ * Host-side errors: EBC_ERR_INVALID_ARG (bad shape or pointer),
+ * EBC_ERR_NO_DEVICE (the current device is not sm_103), EBC_ERR_CUDA, and
+ * EBC_ERR_SCRATCH_LIMIT when the shape's scratch does not fit the 16 MiB,
+ * in which case nothing is launched.  The scratch is about
+ * 8*B*T + 16*T*ceil(B/SB)*(SB/KC) + 2*T*ceil(B/SB)*SB + 4668*T bytes
+ * (SB = max(32, 8192/D), KC = max(1, 128/D)); [8192, 26, 128] needs about 6 MB.
+ * Every call shares the one array per device, and each call clears its status
+ * block first: calls whose work overlaps on the GPU (from several host
+ * threads, or on several streams) race and must be serialised by the caller. */
+int ebc_decompress_noalloc(const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
+                           void* stream);
 
 /* Counts of the last compress call (synchronises its stream).  Returns the
  * recorded device error of the context, if any, as ebc_last_device_error. */
