@@ -166,6 +166,7 @@ static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total)
   w.cdesc = c.take<uint4>(16 * max_chunks);
   w.litrow = c.take<uint16_t>(2 * nsegT * (size_t)sh.SB);
   w.mdesc = c.take<uint2>(8 * (size_t)sh.B * (size_t)sh.T);
+  w.runmap = c.take<uint4>(16 * (size_t)dec_run_slots(sh));
   w.glob = g;
   *total = c.off;
   return w;

@@ -33,15 +33,22 @@ namespace ebc {
 // the low mantissa bits (valid for |t| < 2^22; larger |t| were rejected).
 // Every operation is an explicitly rounded intrinsic, so nothing is contracted.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t quantize_one(float x, float eb, float ebx2, float inv) {
-  const float t = __fmul_rn(x, inv);
-  if (!(fabsf(t) < 127.5f)) return 0u;             // NaN, +-inf, |q| >= 128
-  const float y = __fadd_rn(t, 12582912.0f);       // 1.5 * 2^23
-  const float qf = __fsub_rn(y, 12582912.0f);      // exact
-  const float xh = __fmul_rn(qf, ebx2);
-  const float err = fabsf(__fsub_rn(x, xh));
-  if (!(err <= eb)) return 0u;
-  return (uint32_t)(__float_as_int(y) - 0x4B400000 + kRadius);
+// Four codes packed into one word (code of element k in byte k), branch-free:
+// for an accepted q the low byte of y's bits is q mod 256, so code = byte ^ 0x80;
+// a rejected element takes the byte 0x80, which becomes code 0.
+__device__ __forceinline__ uint32_t quantize_four(float4 v, float eb, float ebx2, float inv, bool ok[4]) {
+  const float xs[4] = {v.x, v.y, v.z, v.w};
+  uint32_t u[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float t = __fmul_rn(xs[k], inv);
+    const float y = __fadd_rn(t, 12582912.0f);       // 1.5 * 2^23
+    const float qf = __fsub_rn(y, 12582912.0f);      // exact when |t| < 2^22
+    const float err = fabsf(__fsub_rn(xs[k], __fmul_rn(qf, ebx2)));
+    ok[k] = (fabsf(t) < 127.5f) & (err <= eb);        // false for NaN and +-inf too
+    u[k] = ok[k] ? __float_as_uint(y) : 0x80u;
+  }
+  return __byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u) ^ 0x80808080u;
 }
 
 __device__ __forceinline__ unsigned long long l2_evict_last() {
@@ -221,25 +228,31 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
       const int d = e % D;
       const bool valid = b < B;
       const float4 v = *reinterpret_cast<const float4*>(xs + Q::offset(r, d));
-      const uint32_t c0 = quantize_one(v.x, eb, ebx2, inv);
-      const uint32_t c1 = quantize_one(v.y, eb, ebx2, inv);
-      const uint32_t c2 = quantize_one(v.z, eb, ebx2, inv);
-      const uint32_t c3 = quantize_one(v.w, eb, ebx2, inv);
-      const uint32_t word = c0 | (c1 << 8) | (c2 << 16) | (c3 << 24);
+      bool ok[4];
+      const uint32_t word = quantize_four(v, eb, ebx2, inv, ok);
       if (valid)
         st_keep_u32(reinterpret_cast<uint32_t*>(w.sym + (size_t)t * sh.symstride + (size_t)b * D + d), word, pol);
       acc += lowbias32(word + (uint32_t)(d >> 2) * 0x9E3779B9u);
-      if ((c0 == 0u) | (c1 == 0u) | (c2 == 0u) | (c3 == 0u)) {
-        if (c0 == 0u) { acc += lowbias32(__float_as_uint(v.x) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu); ++nout; }
-        if (c1 == 0u) { acc += lowbias32(__float_as_uint(v.y) ^ (uint32_t)(d + 2) * 0x85EBCA6Bu); ++nout; }
-        if (c2 == 0u) { acc += lowbias32(__float_as_uint(v.z) ^ (uint32_t)(d + 3) * 0x85EBCA6Bu); ++nout; }
-        if (c3 == 0u) { acc += lowbias32(__float_as_uint(v.w) ^ (uint32_t)(d + 4) * 0x85EBCA6Bu); ++nout; }
+      if (!(ok[0] & ok[1] & ok[2] & ok[3])) {
+        if (!ok[0]) { acc += lowbias32(__float_as_uint(v.x) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu); ++nout; }
+        if (!ok[1]) { acc += lowbias32(__float_as_uint(v.y) ^ (uint32_t)(d + 2) * 0x85EBCA6Bu); ++nout; }
+        if (!ok[2]) { acc += lowbias32(__float_as_uint(v.z) ^ (uint32_t)(d + 3) * 0x85EBCA6Bu); ++nout; }
+        if (!ok[3]) { acc += lowbias32(__float_as_uint(v.w) ^ (uint32_t)(d + 4) * 0x85EBCA6Bu); ++nout; }
       }
       if ((slab + 1) % G::kSPR == 0) {            // the row ends with this slab
+        // sums over the row's kLPR lanes; outliers are rare, so their count is
+        // reduced only when the warp has one
+        const bool any_out = __any_sync(0xffffffffu, nout != 0u);
+        if constexpr (G::kLPR == 32) {
+          acc = __reduce_add_sync(0xffffffffu, acc);
+          if (any_out) nout = __reduce_add_sync(0xffffffffu, nout);
+        } else {
 #pragma unroll
-        for (int off = G::kLPR / 2; off > 0; off >>= 1) {
-          acc += __shfl_xor_sync(0xffffffffu, acc, off);
-          nout += __shfl_xor_sync(0xffffffffu, nout, off);
+          for (int off = G::kLPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+          if (any_out) {
+#pragma unroll
+            for (int off = G::kLPR / 2; off > 0; off >>= 1) nout += __shfl_xor_sync(0xffffffffu, nout, off);
+          }
         }
         if (valid && (lane % G::kLPR) == 0) {
           w.vhash[(size_t)t * B + b] = acc;
@@ -262,10 +275,18 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
 __global__ void __launch_bounds__(256) k_insert(Shape sh, Work w) {
   const unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
   const unsigned long long nvec = (unsigned long long)sh.B * sh.T;
-  if (i >= nvec) return;
+  const bool valid = i < nvec;
+  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+  if (!valid) return;
   const int t = (int)(i / (unsigned long long)sh.B);
   const uint32_t b = (uint32_t)(i - (unsigned long long)t * sh.B);
-  dedup_insert(w.slots + (size_t)t * sh.S, sh.S, __ldcg(&w.vhash[i]), b, w.glob);
+  const uint32_t h = __ldcg(&w.vhash[i]);
+  // lanes are consecutive rows: of the lanes holding the same (table, key),
+  // only the lowest (the smallest row) can set the slot, so only it inserts;
+  // this keeps hot keys from queueing atomics on one address
+  const unsigned same = __match_any_sync(vmask, ((unsigned long long)t << 32) | h);
+  if ((threadIdx.x & 31) != __ffs(same) - 1) return;
+  dedup_insert(w.slots + (size_t)t * sh.S, sh.S, h, b, w.glob);
 }
 
 __device__ __forceinline__ bool has_zero_byte(uint32_t v) {

@@ -9,8 +9,10 @@
 //                  first-level table + long codes); the others, one warp per
 //                  segment, check the segment records against each other and
 //                  write one descriptor per chunk (start bit, length, rows)
-//   k_dec_chunks   one thread per chunk: decodes its literal rows (codes,
-//                  inline outliers) and writes them straight to the output
+//   k_dec_chunks   one thread per chunk, one CTA per run of 64 chunks (listed
+//                  in a run map written by k_dec_prep): decodes its literal
+//                  rows (codes, inline outliers) from shared-memory copies of
+//                  the bitstream and writes them straight to the output
 //   k_dec_matches  copies each matched row from its (literal) reference
 // Every read of the container is bounds-checked; a failed check records
 // EBC_ERR_CORRUPT and stops the remaining work without out-of-bounds access.
@@ -107,6 +109,7 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
   __shared__ uint8_t s_len[256];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offset[kLmax + 2];
   __shared__ int s_bad;
+  __shared__ uint32_t s_c0, s_c1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = sh.T;
   Glob* g = w.glob;
@@ -164,9 +167,11 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
         c0 = srec[4ull * ((unsigned long long)t * sh.nseg) + 1];
         c1 = t + 1 < T ? srec[4ull * ((unsigned long long)(t + 1) * sh.nseg) + 1] : (uint32_t)L.n_chunks;
       }
-      if (c0 > c1 || c1 > L.n_chunks) s_bad = 1;
+      if (c0 > c1 || c1 > L.n_chunks || c1 > dec_max_chunks(sh)) s_bad = 1;
       dt->chunk0 = c0;
       dt->chunk1 = c1;
+      s_c0 = c0;
+      s_c1 = c1;
       for (int l = 0; l <= kLmax; ++l) {
         dt->first[l] = l ? s_next[l] : 0u;
         dt->count[l] = l ? s_count[l] : 0u;
@@ -177,6 +182,17 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     if (s_bad) {
       if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
       return;
+    }
+    {   // this table's run slots [c0 / kDecRun + t, c1 / kDecRun + t + 1): its runs, then one empty slot at most
+      const uint32_t c0 = s_c0, c1 = s_c1;
+      const uint32_t lo = c0 / kDecRun + (uint32_t)t, hi = c1 / kDecRun + (uint32_t)t + 1u;
+      const uint32_t nruns = (c1 - c0 + kDecRun - 1) / kDecRun;
+      for (uint32_t r = lo + tid; r < hi; r += 256) {
+        const uint32_t k = r - lo;
+        const uint32_t j0 = c0 + k * kDecRun;
+        w.runmap[r] = k < nruns ? make_uint4((uint32_t)t, j0, min(j0 + (uint32_t)kDecRun, c1), 0u)
+                                : make_uint4(~0u, 0u, 0u, 0u);
+      }
     }
     uint16_t* lut = w.lut + (size_t)t * (1u << kLutBits);
     for (int i = tid; i < (1 << kLutBits); i += 256) lut[i] = 0;
@@ -303,67 +319,37 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
 }
 
 // ---------------------------------------------------------------------------
-// k_dec_chunks: one thread per chunk; CTA (t, k) takes the k-th run of 256
-// chunks of table t, with the table's decode tables in shared memory.  The
-// thread decodes its chunk's codes with the first-level table (long codes by
-// the canonical first-code search), reads the 32 raw bits after each outlier
-// code, and writes each literal row with 16-byte stores.
+// k_dec_chunks: one thread per chunk, one CTA per run of kDecRun consecutive
+// chunks of one table (the run map lists the runs first, so every CTA with
+// work precedes the empty ones).  The run's chunks are consecutive in the
+// bitstream: the CTA copies their words into shared memory with coalesced
+// loads (when they fit), together with the table's decode tables and the 256
+// reconstruction values.  Each thread then decodes its chunk with the
+// first-level table (long codes by the canonical first-code search), reads the
+// 32 raw bits after each outlier code, and writes each literal row with
+// 16-byte stores.
 // ---------------------------------------------------------------------------
 template <int D>
-__global__ void __launch_bounds__(256) k_dec_chunks(const uint8_t* __restrict__ in, Shape sh, Work w,
-                                                     float* __restrict__ xhat, uint32_t epoch, int cta_per_table) {
-  using G = Geo<D>;
-  __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
-  __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
-  __shared__ uint8_t s_sorted[256];
-  Glob* g = w.glob;
-  if (dec_aborted(g, epoch)) return;
-  const int t = blockIdx.x / cta_per_table;
-  const int blk = blockIdx.x - t * cta_per_table;
-  const DecTab* dt = w.dtab + t;
-  const uint32_t c0 = __ldcg(&dt->chunk0), c1 = __ldcg(&dt->chunk1);
-  const unsigned long long jbase = (unsigned long long)c0 + (unsigned long long)blk * 256ull;
-  if (jbase >= c1) return;
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(w.lut + (size_t)t * (1u << kLutBits));
-    uint4* dst = reinterpret_cast<uint4*>(s_lut);
-    for (int i = threadIdx.x; i < (1 << kLutBits) / 8; i += 256) dst[i] = __ldcg(src + i);
-    if (threadIdx.x <= kLmax) {
-      s_first[threadIdx.x] = __ldcg(&dt->first[threadIdx.x]);
-      s_count[threadIdx.x] = __ldcg(&dt->count[threadIdx.x]);
-      s_offset[threadIdx.x] = __ldcg(&dt->offset[threadIdx.x]);
-    }
-    s_sorted[threadIdx.x] = dt->sorted[threadIdx.x];
-  }
-  __syncthreads();
-  const unsigned long long j = jbase + threadIdx.x;
-  if (j >= c1) return;
-  const unsigned long long n_words = __ldcg(&g->words), off_bits = __ldcg(&g->off_bits);
-  const uint32_t* words = reinterpret_cast<const uint32_t*>(in + off_bits);
-  const int T = sh.T;
-  const uint4 dsc = __ldcg(&w.cdesc[j]);
-  const unsigned long long start = (unsigned long long)dsc.x | ((unsigned long long)(dsc.y & 0xffffu) << 32);
-  const uint32_t clen = dsc.y >> 16;
-  const int seg = (int)dsc.z;
-  const uint32_t first = dsc.w & 0xffffu, rows = dsc.w >> 16;
-  if (seg / sh.nseg != t || rows == 0u || first + rows > (uint32_t)G::kSB || start + clen > n_words * 32ull) {
-    dec_fail(g, epoch, EBC_ERR_CORRUPT);
-    return;
-  }
-  const int s = seg - t * sh.nseg;
-  const float ebx2 = __ldcg(&dt->ebx2);
-  const unsigned long long wlim = (start + clen + 31ull) >> 5;
-  auto ldw = [&](unsigned long long i) -> uint32_t { return i < wlim ? __ldg(words + i) : 0u; };
-  // bit window: the next stream bits are w0:w1 from bit `pos` of w0 (pos < 32)
+struct DecStage {
+  static constexpr int kWords = D <= 128 ? 4096 : 8192;   // 16 / 32 KiB of bitstream per CTA
+};
+
+// Decodes one chunk (rows literal rows of D codes) starting at bit `start`;
+// ldw(i) returns word i of the bitstream.  Returns the number of bits read.
+template <int D, class LoadWord>
+__device__ __forceinline__ unsigned long long decode_chunk(LoadWord ldw, unsigned long long start,
+                                                           const uint16_t* s_lut, const float* s_val,
+                                                           const uint32_t* s_first, const uint32_t* s_count,
+                                                           const uint32_t* s_offset, const uint8_t* s_sorted,
+                                                           const uint16_t* lrow, uint32_t rows, int64_t row0, int T,
+                                                           int t, float* __restrict__ xhat, bool* bad) {
+  // bit window: the next stream bits are w0:w1 from bit `pos` of w0 (pos < 32); w0 is word wp - 2
   unsigned long long wp = start >> 5;
   uint32_t pos = (uint32_t)(start & 31ull);
   uint32_t w0 = ldw(wp), w1 = ldw(wp + 1);
   wp += 2;
-  uint32_t used = 0;
-  bool bad = false;
-  const uint16_t* lrow = w.litrow + (size_t)seg * G::kSB + first;
   for (uint32_t k = 0; k < rows; ++k) {
-    const int64_t b = (int64_t)s * G::kSB + lrow[k];
+    const int64_t b = row0 + lrow[k];
     float4* dst = reinterpret_cast<float4*>(xhat + ((size_t)b * T + t) * D);
 #pragma unroll 2
     for (int q4 = 0; q4 < D / 4; ++q4) {
@@ -383,28 +369,117 @@ __global__ void __launch_bounds__(256) k_dec_chunks(const uint8_t* __restrict__ 
             }
           }
           if (len == 0u) {
-            bad = true;
+            *bad = true;
             len = 1;
           }
         }
-        used += len;
         pos += len;
         if (pos >= 32u) {
           pos -= 32u;
           w0 = w1;
           w1 = ldw(wp++);
         }
+        o[q] = s_val[sym];
         if (sym == 0u) {   // outlier: the next 32 bits are the raw value
           o[q] = __uint_as_float(__funnelshift_l(w1, w0, pos));
-          used += 32u;
           w0 = w1;
           w1 = ldw(wp++);
-        } else {
-          o[q] = __fmul_rn((float)((int)sym - kRadius), ebx2);
         }
       }
       dst[q4] = make_float4(o[0], o[1], o[2], o[3]);
     }
+  }
+  return (wp - 2ull) * 32ull + pos - start;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restrict__ in, Shape sh, Work w,
+                                                         float* __restrict__ xhat, uint32_t epoch) {
+  using G = Geo<D>;
+  constexpr int kStage = DecStage<D>::kWords;
+  __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
+  __shared__ __align__(16) uint32_t s_words[kStage + 1];
+  __shared__ float s_val[256];
+  __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
+  __shared__ uint8_t s_sorted[256];
+  __shared__ unsigned long long s_lo, s_hi;
+  __shared__ int s_abort;
+  Glob* g = w.glob;
+  const int tid = threadIdx.x;
+  // the run, and whether the decode was aborted (then the run map may be
+  // stale): one decision for the whole CTA, taken before the run is used
+  if (tid == 0) s_abort = dec_aborted(g, epoch);
+  const unsigned long long nslots = __ldcg(&g->n_chunks) / kDecRun + (unsigned long long)sh.T;
+  uint4 run = make_uint4(~0u, 0u, 0u, 0u);
+  if (blockIdx.x < nslots) run = __ldcg(&w.runmap[blockIdx.x]);
+  __syncthreads();
+  if (s_abort || run.x == ~0u) return;
+  if (run.x >= (uint32_t)sh.T || run.y >= run.z || run.z > dec_max_chunks(sh)) {
+    if (tid == 0) dec_fail(g, epoch, EBC_ERR_INTERNAL);
+    return;
+  }
+  const int t = (int)run.x;
+  const unsigned long long j = (unsigned long long)run.y + tid;
+  const bool mine = j < run.z;
+  const DecTab* dt = w.dtab + t;
+  uint4 dsc = make_uint4(0, 0, 0, 0);
+  if (mine) dsc = __ldcg(&w.cdesc[j]);
+  {
+    const uint4* src = reinterpret_cast<const uint4*>(w.lut + (size_t)t * (1u << kLutBits));
+    uint4* dst = reinterpret_cast<uint4*>(s_lut);
+#pragma unroll
+    for (int i = tid; i < (1 << kLutBits) / 8; i += kDecRun) dst[i] = __ldcg(src + i);
+    if (tid <= kLmax) {
+      s_first[tid] = __ldcg(&dt->first[tid]);
+      s_count[tid] = __ldcg(&dt->count[tid]);
+      s_offset[tid] = __ldcg(&dt->offset[tid]);
+    }
+    const float ebx2 = __ldcg(&dt->ebx2);
+#pragma unroll
+    for (int i = tid; i < 256; i += kDecRun) {
+      s_sorted[i] = dt->sorted[i];
+      s_val[i] = __fmul_rn((float)(i - kRadius), ebx2);
+    }
+  }
+  const unsigned long long n_words = __ldcg(&g->words), off_bits = __ldcg(&g->off_bits);
+  const uint32_t* words = reinterpret_cast<const uint32_t*>(in + off_bits);
+  const unsigned long long start = (unsigned long long)dsc.x | ((unsigned long long)(dsc.y & 0xffffu) << 32);
+  const uint32_t clen = dsc.y >> 16;
+  const unsigned long long wlim = (start + clen + 31ull) >> 5;   // words the chunk may read: [start/32, wlim)
+  if (tid == 0) s_lo = start >> 5;
+  if (j + 1 == run.z) s_hi = wlim;
+  __syncthreads();
+  // the run's words, if they fit (chunk ranges are consecutive by construction;
+  // a thread whose range lies outside the staged one reads global memory)
+  const unsigned long long lo = s_lo, hi = s_hi;
+  const bool staged = hi >= lo && hi - lo <= (unsigned long long)kStage && hi <= n_words;
+  if (staged) {
+    for (unsigned long long i = lo + tid; i < hi; i += kDecRun) s_words[i - lo] = __ldg(words + i);
+    if (tid == 0) s_words[hi - lo] = 0u;   // read past the run's end: a zero word
+  }
+  __syncthreads();
+  if (!mine) return;
+  const int seg = (int)dsc.z;
+  const uint32_t first = dsc.w & 0xffffu, rows = dsc.w >> 16;
+  if (seg / sh.nseg != t || rows == 0u || first + rows > (uint32_t)G::kSB || start + clen > n_words * 32ull) {
+    dec_fail(g, epoch, EBC_ERR_CORRUPT);
+    return;
+  }
+  const int s = seg - t * sh.nseg;
+  const uint16_t* lrow = w.litrow + (size_t)seg * G::kSB + first;
+  const int64_t row0 = (int64_t)s * G::kSB;
+  bool bad = false;
+  unsigned long long used;
+  if (staged && (start >> 5) >= lo && wlim <= hi) {
+    // reads past the chunk's end see the following chunks' words, then zeros:
+    // they never change a code that lies inside the chunk
+    const uint32_t* sw = s_words - lo;
+    used = decode_chunk<D>([&](unsigned long long i) -> uint32_t { return sw[i < hi ? i : hi]; }, start, s_lut,
+                           s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T, t, xhat, &bad);
+  } else {
+    used = decode_chunk<D>([&](unsigned long long i) -> uint32_t { return i < wlim ? __ldg(words + i) : 0u; },
+                           start, s_lut, s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T, t,
+                           xhat, &bad);
   }
   if (bad || used != clen) dec_fail(g, epoch, EBC_ERR_CORRUPT);
 }
@@ -451,10 +526,9 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
   k_dec_prep<D><<<(sh.T > 0 ? sh.T : 1) + (nsegT + 7) / 8, 256, 0, st>>>(in, in_bytes, sh, w, epoch);
   prof_end(prof, st);
   if (nsegT) {
-    // CTAs per table: enough for the largest possible chunk count of a table
-    const int cpt = (int)(((unsigned long long)sh.nseg * Geo<D>::kChunks + 255) / 256);
+    // one CTA per run slot: enough for the largest possible chunk count
     prof_begin(prof, "k_dec_chunks", st);
-    k_dec_chunks<D><<<(unsigned)(sh.T * cpt), 256, 0, st>>>(in, sh, w, xhat, epoch, cpt);
+    k_dec_chunks<D><<<(unsigned)(dec_run_slots(sh) - 1), kDecRun, 0, st>>>(in, sh, w, xhat, epoch);
     prof_end(prof, st);
     prof_begin(prof, "k_dec_matches", st);
     k_dec_matches<D><<<(unsigned)((sh.nsm > 0 ? sh.nsm : 152) * 8), 256, 0, st>>>(sh, w, xhat, epoch);

@@ -22,6 +22,7 @@ constexpr int kMaxB = 16777215;
 
 // ---- decoder ----
 constexpr int kLutBits = 11;               // first-level decode table: 2^11 entries
+constexpr int kDecRun = 64;                // chunks per decoder CTA (one thread each)
 
 constexpr unsigned long long kEmptySlot = ~0ull;
 
@@ -39,6 +40,16 @@ struct Shape {
   int nsm;        // SMs of the device (grid sizing)
   uint64_t symstride;  // bytes per table in the code scratch: B*D rounded up to 16
 };
+
+// Decoder run slots: table t's runs of kDecRun chunks start at slot
+// floor(chunk0_t / kDecRun) + t, so the slots of all tables are disjoint and
+// ordered, and every slot below floor(n_chunks / kDecRun) + T is written.
+__host__ __device__ inline unsigned long long dec_max_chunks(const Shape& sh) {
+  return (unsigned long long)sh.T * (unsigned long long)sh.nseg * (unsigned long long)(sh.SB / sh.KC);
+}
+__host__ __device__ inline unsigned long long dec_run_slots(const Shape& sh) {
+  return dec_max_chunks(sh) / kDecRun + (unsigned long long)sh.T + 1ull;
+}
 
 // Per-table absolute bounds of one compress call, passed by value.
 struct EbParams {
@@ -90,6 +101,8 @@ struct Work {
   uint4* cdesc;                // [T*nseg*chunks] {start bit lo, start bit hi, segment, first literal | rows << 16}
   uint16_t* litrow;            // [T*nseg][SB] literal rows of each segment, in row order
   uint2* mdesc;                // [n_match] {destination row, source row} as b * T + t
+  uint4* runmap;               // [dec_run_slots] {table, first chunk, end chunk, 0} of each run of chunks;
+                               //   table ~0u = no run
   Glob* glob;
 };
 
