@@ -127,11 +127,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
-__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
+// The input is read once: its lines are the first the L2 gives up (policy from
+// createpolicy), so the code scratch written meanwhile stays resident for the
+// kernels that read it again.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2,
+                                            unsigned long long policy) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(
-          smem_u32(dst)),
-      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar))
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "l"(policy)
       : "memory");
 }
 
@@ -157,13 +161,15 @@ __device__ __forceinline__ void issue_segment_tile(float* stage, const CUtensorM
   using Q = QGeo<D>;
   const int t = seg / sh.nseg;
   const int s = seg - t * sh.nseg;
+  unsigned long long first;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(first));
   mbar_expect_tx(bar, Q::kStageBytes);
 #pragma unroll
   for (int rb = 0; rb < Q::kNBoxR; ++rb)
 #pragma unroll
     for (int db = 0; db < Q::kNBoxD; ++db)
       tma_load_3d(stage + ((rb * Q::kNBoxD + db) * Q::kBoxR) * Q::kBoxD, map, bar, db * Q::kBoxD, t,
-                  s * Geo<D>::kSB + rb * Q::kBoxR);
+                  s * Geo<D>::kSB + rb * Q::kBoxR, first);
 }
 
 // ---------------------------------------------------------------------------
@@ -300,18 +306,23 @@ __device__ __forceinline__ bool has_zero_byte(uint32_t v) {
 // and the same raw bits at outliers; otherwise a literal (a key collision is a
 // literal too).  Literal codes feed the segment and table histograms.
 // ---------------------------------------------------------------------------
+constexpr int kResolveThreads = 64;   // two warps per segment: many segments in flight per SM
+
 template <int D>
-__global__ void __launch_bounds__(256) k_resolve(const float* __restrict__ x, Shape sh, Work w) {
+__global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __restrict__ x, Shape sh, Work w) {
   using G = Geo<D>;
-  constexpr int kIters = G::kRowsPerWarp / G::kRPS;
-  __shared__ uint32_t s_hist[8][256];
+  constexpr int kNT = kResolveThreads, kNW = kNT / 32;
+  constexpr int kRPT = (G::kSB + kNT - 1) / kNT;          // rows per thread in the lookups
+  constexpr int kSteps = G::kSB / kNW / G::kRPS;         // warp steps (kRPS rows each) per warp
+  constexpr int kGroup = kSteps < 8 ? kSteps : 8;        // steps whose loads are issued together
+  __shared__ uint32_t s_hist[kNW][256];
   __shared__ uint32_t s_ref[G::kSB];
   __shared__ uint32_t s_nout[G::kSB];
   __shared__ uint32_t s_bm[G::kBmWords];
   __shared__ uint32_t s_cnt[3];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < 8 * 256; i += 256) (&s_hist[0][0])[i] = 0u;
-  if (tid < G::kBmWords) s_bm[tid] = 0u;
+  for (int i = tid; i < kNW * 256; i += kNT) (&s_hist[0][0])[i] = 0u;
+  for (int i = tid; i < G::kBmWords; i += kNT) s_bm[i] = 0u;
   if (tid < 3) s_cnt[tid] = 0u;
 
   const int seg = blockIdx.x;
@@ -323,13 +334,27 @@ __global__ void __launch_bounds__(256) k_resolve(const float* __restrict__ x, Sh
   const unsigned long long* slots = w.slots + (size_t)t * sh.S;
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
   // one thread per row: first occurrence of the row's key
-  for (int r = tid; r < G::kSB; r += 256) {
-    const int64_t b = row0 + r;
-    if (b < B) {
-      uint32_t ref = dedup_lookup(slots, sh.S, __ldcg(&w.vhash[(size_t)t * B + b]), w.glob);
-      if (ref > (uint32_t)b) ref = (uint32_t)b;   // only on an internal error
-      s_ref[r] = ref;
-      s_nout[r] = __ldcg(&w.vnout[(size_t)t * B + b]);
+  {
+    uint32_t h[kRPT], no[kRPT];
+#pragma unroll
+    for (int k = 0; k < kRPT; ++k) {
+      const int r = k * kNT + tid;
+      const int64_t b = row0 + r;
+      if (r < G::kSB && b < B) {
+        h[k] = __ldcg(&w.vhash[(size_t)t * B + b]);
+        no[k] = __ldcg(&w.vnout[(size_t)t * B + b]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kRPT; ++k) {
+      const int r = k * kNT + tid;
+      const int64_t b = row0 + r;
+      if (r < G::kSB && b < B) {
+        uint32_t ref = dedup_lookup(slots, sh.S, h[k], w.glob);
+        if (ref > (uint32_t)b) ref = (uint32_t)b;   // only on an internal error
+        s_ref[r] = ref;
+        s_nout[r] = no[k];
+      }
     }
   }
   __syncthreads();
@@ -338,87 +363,90 @@ __global__ void __launch_bounds__(256) k_resolve(const float* __restrict__ x, Sh
   const unsigned gshift = lane & ~(G::kLPR - 1);
   const unsigned gmask = (G::kLPR == 32 ? 0xffffffffu : ((1u << G::kLPR) - 1u)) << gshift;
   const bool leader = (lane % G::kLPR) == 0;
-  // all code loads of the warp's rows first
-  uint32_t wb[kIters][G::kSPR], wr[kIters][G::kSPR];
-#pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
-    const int64_t b = row0 + r;
-    const bool valid = b < B;
-    const uint32_t ref = valid ? s_ref[r] : 0u;
-#pragma unroll
-    for (int j = 0; j < G::kSPR; ++j) {
-      const int d = (lane % G::kLPR) * 4 + j * 128;
-      wb[it][j] = valid ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0u;
-      wr[it][j] = valid && ref != (uint32_t)b
-                      ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)ref * D + d))
-                      : wb[it][j];
-    }
-  }
   uint32_t n_lit = 0, n_match = 0, n_out = 0;
+#pragma unroll 1
+  for (int g0 = 0; g0 < kSteps; g0 += kGroup) {
+    // the codes of this group's rows and of their references, loaded together
+    uint32_t wb[kGroup][G::kSPR], wr[kGroup][G::kSPR];
 #pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
-    const int64_t b = row0 + r;
-    const bool valid = b < B;
-    const uint32_t ref = valid ? s_ref[r] : 0u;
-    bool eq = true;
-#pragma unroll
-    for (int j = 0; j < G::kSPR; ++j) {
-      bool e = wr[it][j] == wb[it][j];
-      if (valid && ref != (uint32_t)b && e && has_zero_byte(wb[it][j])) {
-        const int d = (lane % G::kLPR) * 4 + j * 128;
-        const float* xb = x + ((size_t)b * T + t) * D + d;
-        const float* xr = x + ((size_t)ref * T + t) * D + d;
-#pragma unroll
-        for (int q = 0; q < 4; ++q)
-          if (((wb[it][j] >> (8 * q)) & 0xffu) == 0u && __float_as_uint(xb[q]) != __float_as_uint(xr[q])) e = false;
-      }
-      eq = eq && e;
-    }
-    const unsigned bad = __ballot_sync(0xffffffffu, !eq);
-    const bool match = valid && ref != (uint32_t)b && (bad & gmask) == 0u;
-    if (valid && !match) {
+    for (int it = 0; it < kGroup; ++it) {
+      const int r = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
+      const int64_t b = row0 + r;
+      const bool valid = b < B;
+      const uint32_t ref = valid ? s_ref[r] : 0u;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        const uint32_t v = wb[it][j];
-        atomicAdd(&hist[v & 0xffu], 1u);
-        atomicAdd(&hist[(v >> 8) & 0xffu], 1u);
-        atomicAdd(&hist[(v >> 16) & 0xffu], 1u);
-        atomicAdd(&hist[v >> 24], 1u);
+        const int d = (lane % G::kLPR) * 4 + j * 128;
+        wb[it][j] = valid ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0u;
+        wr[it][j] = valid && ref != (uint32_t)b
+                        ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)ref * D + d))
+                        : wb[it][j];
       }
     }
-    if (valid && leader) {
-      if (match) {
-        w.ref[(size_t)t * B + b] = ref;
-        atomicOr(&s_bm[r >> 5], 1u << (r & 31));
-        ++n_match;
-      } else {
-        ++n_lit;
-        n_out += s_nout[r];
-      }
-    }
-  }
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    n_lit += __shfl_xor_sync(0xffffffffu, n_lit, off);
-    n_match += __shfl_xor_sync(0xffffffffu, n_match, off);
-    n_out += __shfl_xor_sync(0xffffffffu, n_out, off);
+    for (int it = 0; it < kGroup; ++it) {
+      const int r = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
+      const int64_t b = row0 + r;
+      const bool valid = b < B;
+      const uint32_t ref = valid ? s_ref[r] : 0u;
+      bool eq = true;
+#pragma unroll
+      for (int j = 0; j < G::kSPR; ++j) {
+        bool e = wr[it][j] == wb[it][j];
+        if (valid && ref != (uint32_t)b && e && has_zero_byte(wb[it][j])) {
+          const int d = (lane % G::kLPR) * 4 + j * 128;
+          const float* xb = x + ((size_t)b * T + t) * D + d;
+          const float* xr = x + ((size_t)ref * T + t) * D + d;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (((wb[it][j] >> (8 * q)) & 0xffu) == 0u && __float_as_uint(xb[q]) != __float_as_uint(xr[q])) e = false;
+        }
+        eq = eq && e;
+      }
+      const unsigned bad = __ballot_sync(0xffffffffu, !eq);
+      const bool match = valid && ref != (uint32_t)b && (bad & gmask) == 0u;
+      if (valid && !match) {
+#pragma unroll
+        for (int j = 0; j < G::kSPR; ++j) {
+          const uint32_t v = wb[it][j];
+          atomicAdd(&hist[v & 0xffu], 1u);
+          atomicAdd(&hist[(v >> 8) & 0xffu], 1u);
+          atomicAdd(&hist[(v >> 16) & 0xffu], 1u);
+          atomicAdd(&hist[v >> 24], 1u);
+        }
+      }
+      if (valid && leader) {
+        if (match) {
+          w.ref[(size_t)t * B + b] = ref;
+          atomicOr(&s_bm[r >> 5], 1u << (r & 31));
+          ++n_match;
+        } else {
+          ++n_lit;
+          n_out += s_nout[r];
+        }
+      }
+    }
   }
+  n_lit = __reduce_add_sync(0xffffffffu, n_lit);
+  n_match = __reduce_add_sync(0xffffffffu, n_match);
+  n_out = __reduce_add_sync(0xffffffffu, n_out);
   if (lane == 0) {
     atomicAdd(&s_cnt[0], n_lit);
     atomicAdd(&s_cnt[1], n_match);
     atomicAdd(&s_cnt[2], n_out);
   }
   __syncthreads();
-  uint32_t f = 0;
 #pragma unroll
-  for (int k = 0; k < 8; ++k) f += s_hist[k][tid];
-  w.seg_hist[(size_t)seg * 256 + tid] = f;
-  if (f) atomicAdd(&w.tab_hist[(size_t)t * 256 + tid], f);
-  if (tid < G::kBmWords) {
-    const int64_t wi = (int64_t)s * G::kBmWords + tid;
-    if (wi < sh.nw) w.bitmap[(size_t)t * sh.nw + wi] = s_bm[tid];
+  for (int i = tid; i < 256; i += kNT) {
+    uint32_t f = 0;
+#pragma unroll
+    for (int k = 0; k < kNW; ++k) f += s_hist[k][i];
+    w.seg_hist[(size_t)seg * 256 + i] = f;
+    if (f) atomicAdd(&w.tab_hist[(size_t)t * 256 + i], f);
+  }
+  for (int i = tid; i < G::kBmWords; i += kNT) {
+    const int64_t wi = (int64_t)s * G::kBmWords + i;
+    if (wi < sh.nw) w.bitmap[(size_t)t * sh.nw + wi] = s_bm[i];
   }
   if (tid == 0) {
     const uint32_t chunks = (s_cnt[0] + G::kKC - 1) / G::kKC;
@@ -526,23 +554,33 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       if (tid == 0) s_maxlen = 0;
       __syncthreads();
       if (tid == 0 && n >= 2) {
+        // the heads of both queues and the entries after them live in
+        // registers (kNone = exhausted), so a pick is a compare and a few moves
+        constexpr uint32_t kNone = 0xFFFFFFFFu;   // above any weight (the sum of all counts is < 2^32)
         int li = 0, qi = 0, qn = 0;
+        uint32_t a0 = s_lw[0], a1 = s_lw[1], q0 = kNone, q1 = kNone;
         for (int m = 0; m < n - 1; ++m) {
           uint32_t wsum = 0;
 #pragma unroll
           for (int pick = 0; pick < 2; ++pick) {
-            const bool leaf = li < n && (qi >= qn || s_lw[li] <= s_nodew[qi]);
-            if (leaf) {
+            if (a0 <= q0) {   // a leaf (ties go to the leaf)
               s_leafpar[li] = (uint8_t)m;
-              wsum += s_lw[li];
+              wsum += a0;
               ++li;
+              a0 = a1;
+              a1 = li + 1 < n ? s_lw[li + 1] : kNone;
             } else {
               s_nodepar[qi] = (uint8_t)m;
-              wsum += s_nodew[qi];
+              wsum += q0;
               ++qi;
+              q0 = q1;
+              q1 = qi + 1 < qn ? s_nodew[qi + 1] : kNone;
             }
           }
-          s_nodew[qn++] = wsum;
+          s_nodew[qn] = wsum;
+          if (qn == qi) q0 = wsum;
+          else if (qn == qi + 1) q1 = wsum;
+          ++qn;
         }
       }
       __syncthreads();
@@ -1025,7 +1063,7 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
     k_insert<<<(unsigned)(((unsigned long long)sh.B * sh.T + 255) / 256), 256, 0, st>>>(sh, w);
     prof_end(prof, st);
     prof_begin(prof, "k_resolve", st);
-    k_resolve<D><<<grid, 256, 0, st>>>(x, sh, w);
+    k_resolve<D><<<grid, kResolveThreads, 0, st>>>(x, sh, w);
     prof_end(prof, st);
   }
   prof_begin(prof, "k_codebook", st);
