@@ -184,6 +184,7 @@ __device__ __forceinline__ void issue_segment_tile(float* stage, const CUtensorM
 template <int D>
 __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtensorMap tmap, Shape sh, EbParams ep,
                                                    Work w) {
+  pdl_enter();
   using G = Geo<D>;
   using Q = QGeo<D>;
   extern __shared__ __align__(128) float s_x[];   // 2 stages of kStageFloats
@@ -279,6 +280,7 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
 // first-occurrence hash table (all keys of the call, in one wave).
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_insert(Shape sh, Work w) {
+  pdl_enter();
   const unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
   const unsigned long long nvec = (unsigned long long)sh.B * sh.T;
   const bool valid = i < nvec;
@@ -310,6 +312,7 @@ constexpr int kResolveThreads = 64;   // two warps per segment: many segments in
 
 template <int D>
 __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __restrict__ x, Shape sh, Work w) {
+  pdl_enter();
   using G = Geo<D>;
   constexpr int kNT = kResolveThreads, kNW = kNT / 32;
   constexpr int kRPT = (G::kSB + kNT - 1) / kNT;          // rows per thread in the lookups
@@ -519,6 +522,7 @@ __device__ __forceinline__ unsigned long long pad16(unsigned long long n) { retu
 __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w, uint8_t* __restrict__ out,
                                                    unsigned long long cap, unsigned long long* out_bytes,
                                                    uint32_t epoch) {
+  pdl_enter();
   __shared__ uint32_t s_f[256], s_lw[256], s_nodew[256];
   __shared__ uint16_t s_order[256];
   __shared__ uint8_t s_leafpar[256], s_nodepar[256], s_depth[256], s_len[256];
@@ -733,6 +737,7 @@ __device__ __forceinline__ uint32_t valid_mask(int64_t B, int64_t row0, int wi) 
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __restrict__ out, unsigned long long cap,
                                                  unsigned long long* out_bytes, uint32_t epoch) {
+  pdl_enter();
   __shared__ uint4 s_agg[8];
   __shared__ uint4 s_warp[8];
   __shared__ int s_last;
@@ -818,6 +823,7 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
 template <int D>
 __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Shape sh, Work w,
                                                uint8_t* __restrict__ out, unsigned long long cap, uint32_t epoch) {
+  pdl_enter();
   using G = Geo<D>;
   constexpr int kIters = G::kRowsPerWarp / G::kRPS;
   constexpr int kRPT = (G::kSB + 255) / 256;   // rows per thread in the row scan
@@ -1057,24 +1063,24 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
     unsigned qgrid = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm);
     if (qgrid > grid) qgrid = grid;
     prof_begin(prof, "k_quantize", st);
-    k_quantize<D><<<qgrid, 256, smem, st>>>(*xmap, sh, ep, w);
+    launch_k(k_quantize<D>, qgrid, 256, smem, st, *xmap, sh, ep, w);
     prof_end(prof, st);
     prof_begin(prof, "k_insert", st);
-    k_insert<<<(unsigned)(((unsigned long long)sh.B * sh.T + 255) / 256), 256, 0, st>>>(sh, w);
+    launch_k(k_insert, (unsigned)(((unsigned long long)sh.B * sh.T + 255) / 256), 256, 0, st, sh, w);
     prof_end(prof, st);
     prof_begin(prof, "k_resolve", st);
-    k_resolve<D><<<grid, kResolveThreads, 0, st>>>(x, sh, w);
+    launch_k(k_resolve<D>, grid, kResolveThreads, 0, st, x, sh, w);
     prof_end(prof, st);
   }
   prof_begin(prof, "k_codebook", st);
-  k_codebook<<<sh.T > 0 ? sh.T : 1, 256, 0, st>>>(sh, ep, w, out, cap, out_bytes, epoch);
+  launch_k(k_codebook, sh.T > 0 ? sh.T : 1, 256, 0, st, sh, ep, w, out, cap, out_bytes, epoch);
   prof_end(prof, st);
   if (grid) {
     prof_begin(prof, "k_layout", st);
-    k_layout<<<(grid + 7) / 8, 256, 0, st>>>(sh, w, out, cap, out_bytes, epoch);
+    launch_k(k_layout, (grid + 7) / 8, 256, 0, st, sh, w, out, cap, out_bytes, epoch);
     prof_end(prof, st);
     prof_begin(prof, "k_emit", st);
-    k_emit<D><<<grid, 256, Geo<D>::kSegSyms * 3, st>>>(x, sh, w, out, cap, epoch);
+    launch_k(k_emit<D>, grid, 256, Geo<D>::kSegSyms * 3, st, x, sh, w, out, cap, epoch);
     prof_end(prof, st);
   }
 }

@@ -102,6 +102,7 @@ __device__ __forceinline__ uint32_t warp_excl(uint32_t v, uint32_t* total) {
 template <int D>
 __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in, unsigned long long in_bytes,
                                                    Shape sh, Work w, uint32_t epoch) {
+  pdl_enter();
   using G = Geo<D>;
   __shared__ __align__(16) uint8_t s_hdr[kHeaderBytes];
   __shared__ Layout s_L;
@@ -395,6 +396,7 @@ __device__ __forceinline__ unsigned long long decode_chunk(LoadWord ldw, unsigne
 template <int D>
 __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restrict__ in, Shape sh, Work w,
                                                          float* __restrict__ xhat, uint32_t epoch) {
+  pdl_enter();
   using G = Geo<D>;
   constexpr int kStage = DecStage<D>::kWords;
   __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
@@ -491,6 +493,7 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __restrict__ xhat, uint32_t epoch) {
+  pdl_enter();
   Glob* g = w.glob;
   if (dec_aborted(g, epoch)) return;
   constexpr int kQ = D / 4;
@@ -523,15 +526,15 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
                                 float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof) {
   const unsigned nsegT = (unsigned)(sh.T * sh.nseg);
   prof_begin(prof, "k_dec_prep", st);
-  k_dec_prep<D><<<(sh.T > 0 ? sh.T : 1) + (nsegT + 7) / 8, 256, 0, st>>>(in, in_bytes, sh, w, epoch);
+  launch_k(k_dec_prep<D>, (sh.T > 0 ? sh.T : 1) + (nsegT + 7) / 8, 256, 0, st, in, in_bytes, sh, w, epoch);
   prof_end(prof, st);
   if (nsegT) {
     // one CTA per run slot: enough for the largest possible chunk count
     prof_begin(prof, "k_dec_chunks", st);
-    k_dec_chunks<D><<<(unsigned)(dec_run_slots(sh) - 1), kDecRun, 0, st>>>(in, sh, w, xhat, epoch);
+    launch_k(k_dec_chunks<D>, (unsigned)(dec_run_slots(sh) - 1), kDecRun, 0, st, in, sh, w, xhat, epoch);
     prof_end(prof, st);
     prof_begin(prof, "k_dec_matches", st);
-    k_dec_matches<D><<<(unsigned)((sh.nsm > 0 ? sh.nsm : 152) * 8), 256, 0, st>>>(sh, w, xhat, epoch);
+    launch_k(k_dec_matches<D>, (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * 8), 256, 0, st, sh, w, xhat, epoch);
     prof_end(prof, st);
   }
 }

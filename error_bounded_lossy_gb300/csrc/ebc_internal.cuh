@@ -146,6 +146,34 @@ struct Geo {
   static constexpr int kSegSyms = kSB * D;
 };
 
+// ---- programmatic dependent launch ----
+// Every kernel of a call is launched with programmatic stream serialization.
+// On entry it lets the next kernel of the stream launch (which happens once
+// all of its own CTAs have started, so the next grid fills the SMs its tail
+// frees), then waits until the kernels before it have completed and their
+// memory is visible, before it reads anything they wrote.  A kernel whose
+// predecessor is not a kernel waits for nothing.
+__device__ __forceinline__ void pdl_enter() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---- optional per-kernel timing (host side, defined with the C ABI) ----
 struct Prof;
 void prof_begin(Prof* p, const char* name, cudaStream_t st);
