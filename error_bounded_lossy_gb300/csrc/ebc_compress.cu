@@ -511,6 +511,33 @@ __device__ __forceinline__ void st_u64(uint8_t* p, unsigned long long v) {
 }
 __device__ __forceinline__ unsigned long long pad16(unsigned long long n) { return (n + 15ull) & ~15ull; }
 
+// Ascending bitonic sort of one 64-bit key per thread over a 256-thread CTA:
+// partners closer than a warp trade through shuffles, the others through
+// shared memory.  Returns the key of rank threadIdx.x.
+__device__ __forceinline__ unsigned long long bitonic_sort256(unsigned long long v, unsigned long long* s_key) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      unsigned long long p;
+      if (j >= 32) {
+        s_key[tid] = v;
+        __syncthreads();
+        p = s_key[tid ^ j];
+        __syncthreads();
+      } else {
+        p = __shfl_xor_sync(0xffffffffu, v, j);
+      }
+      const bool up = (tid & k) == 0;        // this run ascends
+      const bool low = (tid & j) == 0;       // lower element of the pair
+      const unsigned long long mn = v < p ? v : p, mx = v < p ? p : v;
+      v = (up == low) ? mn : mx;
+    }
+  }
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // k_codebook: one CTA per table.  Huffman code lengths (§III-D "Optimized
 // Entropy Encoding") by the two-queue construction over leaves sorted by
@@ -524,6 +551,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
                                                    uint32_t epoch) {
   pdl_enter();
   __shared__ uint32_t s_f[256], s_lw[256], s_nodew[256];
+  __shared__ unsigned long long s_key[256];
   __shared__ uint16_t s_order[256];
   __shared__ uint8_t s_leafpar[256], s_nodepar[256], s_depth[256], s_len[256];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2];
@@ -535,24 +563,19 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   Glob* g = w.glob;
 
   if (t < T) {
-    // the hash table of this table is not read again: empty it for the next call
-    unsigned long long* slots = w.slots + (size_t)t * sh.S;
-    for (uint32_t i = tid; i < sh.S; i += 256) slots[i] = kEmptySlot;
     // (with no segments, k_quantize did not run and the accumulators are stale)
     s_f[tid] = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)t * 256 + tid]) : 0u;
     __syncthreads();
     for (int round = 0; round < 40; ++round) {
       const uint32_t fi = s_f[tid];
-      int rank = 0;
-      if (fi > 0u)
-        for (int j = 0; j < 256; ++j) {
-          const uint32_t fj = s_f[j];
-          rank += (fj > 0u) && (fj < fi || (fj == fi && j < tid));
-        }
+      // leaves in (count, symbol) order: a bitonic sort of the keys count << 8 | symbol over the
+      // 256 threads (absent symbols sort last); thread i ends with the key of rank i
+      const unsigned long long key = fi > 0u ? ((unsigned long long)fi << 8) | (unsigned)tid : ~0ull;
+      const unsigned long long sk = bitonic_sort256(key, s_key);
       const int n = __syncthreads_count(fi > 0u);
-      if (fi > 0u) {
-        s_order[rank] = (uint16_t)tid;
-        s_lw[rank] = fi;
+      if (tid < n) {
+        s_order[tid] = (uint16_t)(sk & 0xffu);
+        s_lw[tid] = (uint32_t)(sk >> 8);
       }
       s_len[tid] = 0;
       if (tid == 0) s_maxlen = 0;
@@ -746,6 +769,13 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
   const int tile = blockIdx.x;
   const int ntiles = gridDim.x;
   const int nsegT = sh.T * sh.nseg;
+  {   // the dedup tables are not read again: empty them for the next call (a share per CTA)
+    const unsigned long long n2 = (unsigned long long)sh.T * sh.S / 2;   // slot pairs (S is even)
+    const unsigned long long per = (n2 + ntiles - 1) / ntiles;
+    const unsigned long long lo = per * tile, hi = lo + per < n2 ? lo + per : n2;
+    uint4* sl = reinterpret_cast<uint4*>(w.slots);
+    for (unsigned long long i = lo + tid; i < hi; i += 256) sl[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+  }
   const int seg = tile * 8 + warp;
   uint4 a = make_uint4(0, 0, 0, 0);   // {words, chunks, matches, -}
   uint32_t bits = 0;
