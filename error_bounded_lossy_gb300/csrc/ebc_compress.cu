@@ -841,29 +841,33 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
 
 // ---------------------------------------------------------------------------
 // k_emit: one CTA per (table, segment), offsets from k_layout.  Every global
-// read the CTA needs (codes of all its rows, bitmap, references, code table)
-// is issued first.  A warp takes whole rows (kLPR lanes per row, 4 codes per
-// lane) and skips matched ones; each lane joins its codes into one bit string
-// that is ORed into a shared-memory copy of the segment's bitstream at the
-// lane's offset (a prefix sum over the row).  Outlier codes are followed by the
-// 32 raw bits of the value.  The copy is stored with 16-byte writes; a segment
-// larger than the copy (24 bits per code on average) is ORed straight into the
-// zeroed output.
+// read the CTA needs (the segment's codes, into shared memory; bitmap,
+// references, code table) is issued first.  The literal rows are ranked from
+// the match bitmap and dealt to the warps in turn (kRPS rows per warp step,
+// kLPR lanes per row, 4 codes per lane), so matched rows cost nothing and the
+// warps get even shares.  Pass 1 adds up each literal row's code lengths; a
+// scan over the ranks gives each row's bit offset; in pass 2 each lane joins
+// its codes into one bit string that is ORed into a shared-memory copy of the
+// segment's bitstream at the lane's offset (a prefix sum over the row).
+// Outlier codes are followed by the 32 raw bits of the value.  The copy is
+// stored with 16-byte writes; a segment larger than the copy (24 bits per
+// code on average) is ORed straight into the zeroed output.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Shape sh, Work w,
                                                uint8_t* __restrict__ out, unsigned long long cap, uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
-  constexpr int kIters = G::kRowsPerWarp / G::kRPS;
-  constexpr int kRPT = (G::kSB + 255) / 256;   // rows per thread in the row scan
+  constexpr int kRPT = (G::kSB + 255) / 256;   // rows (and ranks) per thread
   constexpr uint32_t kSmemWords = (uint32_t)G::kSegSyms * 3u / 4u;
   extern __shared__ __align__(16) uint32_t s_bits[];
+  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4];   // the segment's codes, row-major
   __shared__ uint32_t s_code[256];
-  __shared__ uint32_t s_bm[G::kBmWords];
-  __shared__ uint32_t s_rowoff[G::kSB + 1];
-  __shared__ uint32_t s_aux[G::kSB];
-  __shared__ uint16_t s_litrow[G::kSB];
+  __shared__ uint32_t s_bm[G::kBmWords];      // match bits
+  __shared__ uint32_t s_lit[G::kBmWords];     // literal bits
+  __shared__ uint32_t s_pre[G::kBmWords];     // literal (low 16) and match (high 16) rows before each word
+  __shared__ uint32_t s_rowoff[G::kSB + 1];   // by literal rank: bits, then bit offset
+  __shared__ uint16_t s_litrow[G::kSB];       // by literal rank: row
   __shared__ uint4 s_warp[8];
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -885,21 +889,17 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
     const int64_t wi = (int64_t)s * G::kBmWords + tid;
     bmw = wi < sh.nw ? __ldcg(&w.bitmap[(size_t)t * sh.nw + wi]) : 0u;
   }
-  uint32_t wv[kIters][G::kSPR];
-#pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
-    const int64_t b = row0 + r;
-#pragma unroll
-    for (int j = 0; j < G::kSPR; ++j) {
-      const int d = (lane % G::kLPR) * 4 + j * 128;
-      wv[it][j] = b < B ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0x80808080u;
-    }
+  {   // rows row0 .. row0 + SB are contiguous; the table stride is padded to 16 bytes
+    const int64_t nrows = B - row0 < G::kSB ? B - row0 : G::kSB;
+    const int nq = (int)((nrows * D + 15) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D);
+    uint4* dst = reinterpret_cast<uint4*>(s_sym);
+    for (int i = tid; i < nq; i += 256) dst[i] = __ldcg(src + i);
   }
   uint32_t refw[kRPT];
 #pragma unroll
   for (int k = 0; k < kRPT; ++k) {
-    const int r = tid * kRPT + k;
+    const int r = k * 256 + tid;
     refw[k] = (r < G::kSB && row0 + r < B) ? __ldcg(&w.ref[(size_t)t * B + row0 + r]) : 0u;
   }
   const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
@@ -908,93 +908,101 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
   const unsigned long long off_seg = __ldcg(&g->off_seg), off_bitmap = __ldcg(&g->off_bitmap);
 
   s_code[tid] = mycode;
-  if (tid < G::kBmWords) s_bm[tid] = bmw;
+  if (tid < G::kBmWords) {
+    s_bm[tid] = bmw;
+    s_lit[tid] = ~bmw & valid_mask(B, row0, tid);
+  }
   const uint32_t bits = sb.w;
   const uint32_t nwords = ((bits + 127u) >> 7) * 4u;
   const bool bits_fit = writable && off_bits + 4ull * ((unsigned long long)sb.x + nwords) <= cap;
   const bool in_smem = nwords <= kSmemWords;
   uint32_t* dstw = reinterpret_cast<uint32_t*>(out + off_bits) + sb.x;
-  if (bits_fit) {
-    uint32_t* zb = in_smem ? s_bits : dstw;
-    for (uint32_t i = tid; i < nwords; i += 256) zb[i] = 0u;
-  }
+  uint32_t* bitbuf = in_smem ? s_bits : dstw;
+  if (bits_fit)
+    for (uint32_t i = tid; i < nwords; i += 256) bitbuf[i] = 0u;
   __syncthreads();
 
-  // pass 1: bits of each literal row (0 for matched rows)
+  // ---- literal ranks: rows counted before each bitmap word, then each literal row's rank ----
+  uint32_t nlit;
+  {
+    const uint32_t v = tid < G::kBmWords ? ((uint32_t)__popc(s_lit[tid]) | ((uint32_t)__popc(s_bm[tid]) << 16)) : 0u;
+    uint4 tot;
+    const uint4 ex = block_excl_scan4(make_uint4(v, 0, 0, 0), &tot, s_warp);
+    if (tid < G::kBmWords) s_pre[tid] = ex.x;
+    nlit = tot.x & 0xffffu;
+  }
+  __syncthreads();
 #pragma unroll
-  for (int it = 0; it < kIters; ++it) {
-    const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
-    const bool lit = row0 + r < B && !((s_bm[r >> 5] >> (r & 31)) & 1u);
-    if (!__any_sync(0xffffffffu, lit)) {   // all rows of this step are matches or past the batch
-      if ((lane % G::kLPR) == 0) s_rowoff[r] = 0u;
-      continue;
-    }
+  for (int k = 0; k < kRPT; ++k) {
+    const int r = k * 256 + tid;
+    if (r < G::kSB && ((s_lit[r >> 5] >> (r & 31)) & 1u))
+      s_litrow[(s_pre[r >> 5] & 0xffffu) + __popc(s_lit[r >> 5] & ((1u << (r & 31)) - 1u))] = (uint16_t)r;
+  }
+  __syncthreads();
+  const uint32_t nsteps = (nlit + G::kRPS - 1) / G::kRPS;
+
+  // ---- pass 1: bits of each literal row ----
+#pragma unroll 1
+  for (uint32_t i = warp; i < nsteps; i += 8) {
+    const uint32_t k = i * G::kRPS + lane / G::kLPR;   // literal rank of this lane's row
+    const bool act = k < nlit;
+    const int r = act ? s_litrow[k] : 0;
     uint32_t nb = 0;
 #pragma unroll
     for (int j = 0; j < G::kSPR; ++j) {
-      const uint32_t v = wv[it][j];
+      const uint32_t v = act ? s_sym[r * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t c = (v >> (8 * q)) & 0xffu;
         nb += (s_code[c] & 0xffu) + (c == 0u ? 32u : 0u);
       }
     }
+    if constexpr (G::kLPR == 32) {
+      nb = __reduce_add_sync(0xffffffffu, nb);
+    } else {
 #pragma unroll
-    for (int off = G::kLPR / 2; off > 0; off >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, off);
-    if ((lane % G::kLPR) == 0) s_rowoff[r] = lit ? nb : 0u;
+      for (int off = G::kLPR / 2; off > 0; off >>= 1) nb += __shfl_xor_sync(0xffffffffu, nb, off);
+    }
+    if (act && (lane % G::kLPR) == 0) s_rowoff[k] = nb;
   }
   __syncthreads();
 
-  // row scan: bit offsets, literal ranks, match ranks
-  uint32_t nlit;
+  // ---- bit offset of each literal row: scan over the ranks ----
   {
     uint4 loc[kRPT];
     uint4 sum = make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int r = tid * kRPT + k;
-      uint4 v = make_uint4(0, 0, 0, 0);
-      if (r < G::kSB && row0 + r < B) {
-        const bool m = (s_bm[r >> 5] >> (r & 31)) & 1u;
-        v = make_uint4(s_rowoff[r], m ? 0u : 1u, m ? 1u : 0u, 0u);
-      }
+      const uint32_t kk = (uint32_t)(tid * kRPT + k);
       loc[k] = sum;
-      sum = add4(sum, v);
+      if (kk < nlit) sum.x += s_rowoff[kk];
     }
     uint4 tot;
     const uint4 ex = block_excl_scan4(sum, &tot, s_warp);
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int r = tid * kRPT + k;
-      if (r < G::kSB) {
-        const uint4 p = add4(ex, loc[k]);
-        const bool m = (s_bm[r >> 5] >> (r & 31)) & 1u;
-        s_rowoff[r] = p.x;
-        if (row0 + r < B && !m) s_litrow[p.y] = (uint16_t)r;
-        s_aux[r] = p.z;
-      }
+      const uint32_t kk = (uint32_t)(tid * kRPT + k);
+      if (kk < nlit) s_rowoff[kk] = ex.x + loc[k].x;
     }
-    nlit = tot.y;
     if (tid == 0) {
-      s_rowoff[G::kSB] = tot.x;
+      s_rowoff[nlit] = tot.x;
       if (tot.x != bits) record_error(g, EBC_ERR_INTERNAL);
     }
   }
   __syncthreads();
 
-  // pass 2: codes (and raw outlier bits) into the bitstream
+  // ---- pass 2: codes (and raw outlier bits) into the bitstream ----
   if (bits_fit) {
-    uint32_t* bitbuf = in_smem ? s_bits : dstw;
-#pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-      const int r = warp * G::kRowsPerWarp + it * G::kRPS + lane / G::kLPR;
+#pragma unroll 1
+    for (uint32_t i = warp; i < nsteps; i += 8) {
+      const uint32_t k = i * G::kRPS + lane / G::kLPR;
+      const bool act = k < nlit;
+      const int r = act ? s_litrow[k] : 0;
       const int64_t b = row0 + r;
-      const bool lit = b < B && !((s_bm[r >> 5] >> (r & 31)) & 1u);
-      if (!__any_sync(0xffffffffu, lit)) continue;
-      uint32_t p = s_rowoff[r];
+      uint32_t p = act ? s_rowoff[k] : 0u;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        const uint32_t v = wv[it][j];
+        const uint32_t v = act ? s_sym[r * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
         // the lane's 4 codes joined into one string (right-aligned), if short and outlier-free
         uint32_t nb = 0;
         unsigned long long str = 0;
@@ -1009,7 +1017,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
           plain = plain && c != 0u;
         }
         plain = plain && nb <= 64u;
-        if (!lit) nb = 0;
+        if (!act) nb = 0;
         uint32_t inc = nb;
 #pragma unroll
         for (int off = 1; off < G::kLPR; off <<= 1) {
@@ -1017,9 +1025,9 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
           if ((lane % G::kLPR) >= off) inc += n;
         }
         const uint32_t slab_total = __shfl_sync(0xffffffffu, inc, (lane & ~(G::kLPR - 1)) + G::kLPR - 1);
-        if (lit && plain) {
+        if (act && plain) {
           put_string(bitbuf, p + inc - nb, str, nb);
-        } else if (lit) {
+        } else if (act) {
           uint32_t qpos = p + inc - nb;
           const int d = (lane % G::kLPR) * 4 + j * 128;
 #pragma unroll
@@ -1047,15 +1055,16 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
       for (uint32_t i = tid; i < nwords / 4; i += 256) dst[i] = src[i];
     }
     for (uint32_t k = tid * G::kKC; k < nlit; k += 256 * G::kKC) {
-      const uint32_t start = s_rowoff[s_litrow[k]];
-      const uint32_t end = k + G::kKC < nlit ? s_rowoff[s_litrow[k + G::kKC]] : s_rowoff[G::kSB];
-      *reinterpret_cast<uint16_t*>(out + off_chunks + 2ull * (sb.y + k / G::kKC)) = (uint16_t)(end - start);
+      const uint32_t end = k + G::kKC < nlit ? k + G::kKC : nlit;
+      *reinterpret_cast<uint16_t*>(out + off_chunks + 2ull * (sb.y + k / G::kKC)) =
+          (uint16_t)(s_rowoff[end] - s_rowoff[k]);
     }
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int r = tid * kRPT + k;
+      const int r = k * 256 + tid;
       if (r < G::kSB && row0 + r < B && ((s_bm[r >> 5] >> (r & 31)) & 1u)) {
-        const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (sb.z + s_aux[r]);
+        const uint32_t mrank = (s_pre[r >> 5] >> 16) + __popc(s_bm[r >> 5] & ((1u << (r & 31)) - 1u));
+        const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (sb.z + mrank);
         if (sh.ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)refw[k];
         else *reinterpret_cast<uint32_t*>(out + o) = refw[k];
       }
