@@ -106,6 +106,12 @@ constexpr int kWaitLimit = 1 << 22;   // polls of an mbarrier before giving up
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
+// 16-byte asynchronous global -> shared copies (completion by commit/wait groups)
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(smem)), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
@@ -319,6 +325,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
   constexpr int kSteps = G::kSB / kNW / G::kRPS;         // warp steps (kRPS rows each) per warp
   constexpr int kGroup = kSteps < 8 ? kSteps : 8;        // steps whose loads are issued together
   __shared__ uint32_t s_hist[kNW][256];
+  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4];   // the segment's own codes
   __shared__ uint32_t s_ref[G::kSB];
   __shared__ uint32_t s_nout[G::kSB];
   __shared__ uint32_t s_bm[G::kBmWords];
@@ -336,6 +343,13 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
   const int64_t row0 = (int64_t)s * G::kSB;
   const unsigned long long* slots = w.slots + (size_t)t * sh.S;
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
+  {   // the segment's codes (rows contiguous; the table stride is padded to 16 bytes), copied
+      // asynchronously while the keys are looked up
+    const int64_t nrows = B - row0 < G::kSB ? B - row0 : G::kSB;
+    const int nq = (int)((nrows * D + 15) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D);
+    for (int i = tid; i < nq; i += kNT) cp_async16(reinterpret_cast<uint4*>(s_sym) + i, src + i);
+  }
   // one thread per row: first occurrence of the row's key
   {
     uint32_t h[kRPT], no[kRPT];
@@ -360,6 +374,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
       }
     }
   }
+  cp_async_wait_all();
   __syncthreads();
 
   uint32_t* hist = s_hist[warp];
@@ -367,51 +382,51 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
   const unsigned gmask = (G::kLPR == 32 ? 0xffffffffu : ((1u << G::kLPR) - 1u)) << gshift;
   const bool leader = (lane % G::kLPR) == 0;
   uint32_t n_lit = 0, n_match = 0, n_out = 0;
-#pragma unroll 1
-  for (int g0 = 0; g0 < kSteps; g0 += kGroup) {
-    // the codes of this group's rows and of their references, loaded together
-    uint32_t wb[kGroup][G::kSPR], wr[kGroup][G::kSPR];
+  // the reference rows' codes of a group of steps (the next group's loads are in flight while
+  // this one is compared)
+  auto load_refs = [&](int g0, uint32_t (&wr)[kGroup][G::kSPR]) {
 #pragma unroll
     for (int it = 0; it < kGroup; ++it) {
       const int r = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
       const int64_t b = row0 + r;
-      const bool valid = b < B;
-      const uint32_t ref = valid ? s_ref[r] : 0u;
+      const uint32_t ref = b < B ? s_ref[r] : (uint32_t)b;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
         const int d = (lane % G::kLPR) * 4 + j * 128;
-        wb[it][j] = valid ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)b * D + d)) : 0u;
-        wr[it][j] = valid && ref != (uint32_t)b
-                        ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)ref * D + d))
-                        : wb[it][j];
+        wr[it][j] = ref != (uint32_t)b ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)ref * D + d)) : 0u;
       }
     }
+  };
+  auto process = [&](int g0, const uint32_t (&wr)[kGroup][G::kSPR]) {
 #pragma unroll
     for (int it = 0; it < kGroup; ++it) {
       const int r = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
       const int64_t b = row0 + r;
       const bool valid = b < B;
       const uint32_t ref = valid ? s_ref[r] : 0u;
+      const bool cand = valid && ref != (uint32_t)b;
+      uint32_t wb[G::kSPR];
       bool eq = true;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        bool e = wr[it][j] == wb[it][j];
-        if (valid && ref != (uint32_t)b && e && has_zero_byte(wb[it][j])) {
+        wb[j] = s_sym[r * (D / 4) + (lane % G::kLPR) + j * 32];
+        bool e = wr[it][j] == wb[j];
+        if (cand && e && has_zero_byte(wb[j])) {
           const int d = (lane % G::kLPR) * 4 + j * 128;
           const float* xb = x + ((size_t)b * T + t) * D + d;
           const float* xr = x + ((size_t)ref * T + t) * D + d;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (((wb[it][j] >> (8 * q)) & 0xffu) == 0u && __float_as_uint(xb[q]) != __float_as_uint(xr[q])) e = false;
+            if (((wb[j] >> (8 * q)) & 0xffu) == 0u && __float_as_uint(xb[q]) != __float_as_uint(xr[q])) e = false;
         }
         eq = eq && e;
       }
       const unsigned bad = __ballot_sync(0xffffffffu, !eq);
-      const bool match = valid && ref != (uint32_t)b && (bad & gmask) == 0u;
+      const bool match = cand && (bad & gmask) == 0u;
       if (valid && !match) {
 #pragma unroll
         for (int j = 0; j < G::kSPR; ++j) {
-          const uint32_t v = wb[it][j];
+          const uint32_t v = wb[j];
           atomicAdd(&hist[v & 0xffu], 1u);
           atomicAdd(&hist[(v >> 8) & 0xffu], 1u);
           atomicAdd(&hist[(v >> 16) & 0xffu], 1u);
@@ -428,6 +443,17 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
           n_out += s_nout[r];
         }
       }
+    }
+  };
+  uint32_t wr0[kGroup][G::kSPR], wr1[kGroup][G::kSPR];
+  load_refs(0, wr0);
+#pragma unroll 1
+  for (int g0 = 0; g0 < kSteps; g0 += 2 * kGroup) {
+    if (g0 + kGroup < kSteps) load_refs(g0 + kGroup, wr1);
+    process(g0, wr0);
+    if (g0 + kGroup < kSteps) {
+      if (g0 + 2 * kGroup < kSteps) load_refs(g0 + 2 * kGroup, wr0);
+      process(g0 + kGroup, wr1);
     }
   }
   n_lit = __reduce_add_sync(0xffffffffu, n_lit);
