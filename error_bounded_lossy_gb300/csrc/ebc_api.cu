@@ -93,6 +93,7 @@ static Shape make_shape(int64_t B, int T, int D, int nsm = 0) {
   sh.S = S;
   sh.ref_bytes = B <= 65536 ? 2 : 4;
   sh.symstride = ((uint64_t)B * (uint64_t)D + 15u) & ~(uint64_t)15u;
+  sh.fold = sh.nseg <= kFoldMaxSeg ? 1 : 0;
   return sh;
 }
 
@@ -138,8 +139,9 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   Work w{};
   const size_t nvec = (size_t)sh.B * sh.T, nsegT = (size_t)sh.T * sh.nseg;
   w.slots = c.take<unsigned long long>(8 * (size_t)sh.T * sh.S);
-  w.seg_desc = c.take<uint4>(16 * ((nsegT + 7) / 8));
-  w.tile_base = c.take<uint4>(16 * ((nsegT + 7) / 8));
+  const size_t groups = (nsegT + 7) / 8 > (size_t)sh.T ? (nsegT + 7) / 8 : (size_t)sh.T;
+  w.seg_desc = c.take<uint4>(16 * groups);
+  w.tile_base = c.take<uint4>(16 * groups);
   w.seg_base = c.take<uint4>(16 * nsegT);
   w.sym = c.take<uint8_t>((size_t)sh.T * sh.symstride);
   w.vhash = c.take<uint32_t>(4 * nvec);

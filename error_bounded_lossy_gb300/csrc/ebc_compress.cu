@@ -578,6 +578,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   pdl_enter();
   __shared__ uint32_t s_f[256], s_lw[256], s_nodew[256];
   __shared__ unsigned long long s_key[256];
+  __shared__ uint4 s_seg[kFoldMaxSeg];
   __shared__ uint16_t s_order[256];
   __shared__ uint8_t s_leafpar[256], s_nodepar[256], s_depth[256], s_len[256];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2];
@@ -690,6 +691,49 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       st_u32(rec + 8, tc.y);
       st_u32(rec + 12, tc.z);
     }
+    if (sh.fold && sh.nseg > 0) {
+      // this table's segments: bits = sum over codes of count * length (+32 raw bits per outlier),
+      // one warp per segment; then offsets relative to the table (a scan) and the table's totals
+      const int warp = tid >> 5, lane = tid & 31;
+      const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)t * 256) + lane * 2;
+      __syncthreads();   // tabcode of this table is written
+      const uint4 c0 = __ldcg(cp), c1 = __ldcg(cp + 1);
+      constexpr int kBatch = 4;   // segments whose histograms are loaded together
+      for (int i0 = warp; i0 < sh.nseg; i0 += 8 * kBatch) {
+        uint4 h0[kBatch], h1[kBatch], cnt[kBatch];
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          const int i = i0 + 8 * q;
+          if (i < sh.nseg) {
+            const int seg = t * sh.nseg + i;
+            const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * 256) + lane * 2;
+            h0[q] = __ldcg(hp);
+            h1[q] = __ldcg(hp + 1);
+            cnt[q] = lane == 0 ? __ldcg(&w.seg_cnt[seg]) : make_uint4(0, 0, 0, 0);
+          }
+        }
+#pragma unroll
+        for (int q = 0; q < kBatch; ++q) {
+          const int i = i0 + 8 * q;
+          if (i < sh.nseg) {
+            uint32_t bits = h0[q].x * (c0.x & 0xffu) + h0[q].y * (c0.y & 0xffu) + h0[q].z * (c0.z & 0xffu) +
+                            h0[q].w * (c0.w & 0xffu) + h1[q].x * (c1.x & 0xffu) + h1[q].y * (c1.y & 0xffu) +
+                            h1[q].z * (c1.z & 0xffu) + h1[q].w * (c1.w & 0xffu);
+            if (lane == 0) bits += 32u * h0[q].x;   // symbol 0: the outliers' raw bits
+            bits = __reduce_add_sync(0xffffffffu, bits);
+            if (lane == 0) s_seg[i] = make_uint4(((bits + 127u) >> 7) * 4u, cnt[q].w, cnt[q].y, bits);
+          }
+        }
+      }
+      __syncthreads();
+      uint4 v = tid < sh.nseg ? s_seg[tid] : make_uint4(0, 0, 0, 0);
+      const uint32_t segbits = v.w;
+      v.w = 0;
+      uint4 tot;
+      const uint4 ex = block_excl_scan4(v, &tot, s_warp);
+      if (tid < sh.nseg) w.seg_base[t * sh.nseg + tid] = make_uint4(ex.x, ex.y, ex.z, segbits);
+      if (tid == 0) w.seg_desc[t] = tot;
+    }
   }
 
   // ---- the last CTA: section layout and header ----
@@ -706,6 +750,17 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     uint4 tot;
     block_excl_scan4(v, &tot, s_warp);
     sum = add4(sum, tot);
+  }
+  uint4 fsum = make_uint4(0, 0, 0, 0);   // folded layout: table bases and the bitstream size
+  if (sh.fold && sh.nseg > 0) {
+    for (int base = 0; base < T; base += 256) {
+      const int i = base + tid;
+      const uint4 v = i < T ? __ldcg(&w.seg_desc[i]) : make_uint4(0, 0, 0, 0);
+      uint4 tot;
+      const uint4 ex = block_excl_scan4(v, &tot, s_warp);
+      if (i < T) w.tile_base[i] = add4(fsum, ex);
+      fsum = add4(fsum, tot);
+    }
   }
   if (tid == 0) {
     const unsigned long long lits = sum.x, matches = sum.y, outl = sum.z, chunks = sum.w;
@@ -741,6 +796,16 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       st_u64(out + 80, 0ull);
       st_u64(out + 128, off_bits);
       *out_bytes = off_bits;
+    } else if (sh.fold) {   // the bitstream size is known here (else k_layout completes it)
+      const unsigned long long words = fsum.x, total = off_bits + 4ull * words;
+      g->words = words;
+      g->total = total;
+      *out_bytes = total;
+      if (status == EBC_OK && total > cap) status = EBC_ERR_CAPACITY;
+      if (status == EBC_OK) {
+        st_u64(out + 80, words);
+        st_u64(out + 128, total);
+      }
     }
     if (status != EBC_OK) record_error(g, status);
     g->cstat = status_word(epoch, status);
@@ -795,13 +860,6 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
   const int tile = blockIdx.x;
   const int ntiles = gridDim.x;
   const int nsegT = sh.T * sh.nseg;
-  {   // the dedup tables are not read again: empty them for the next call (a share per CTA)
-    const unsigned long long n2 = (unsigned long long)sh.T * sh.S / 2;   // slot pairs (S is even)
-    const unsigned long long per = (n2 + ntiles - 1) / ntiles;
-    const unsigned long long lo = per * tile, hi = lo + per < n2 ? lo + per : n2;
-    uint4* sl = reinterpret_cast<uint4*>(w.slots);
-    for (unsigned long long i = lo + tid; i < hi; i += 256) sl[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
-  }
   const int seg = tile * 8 + warp;
   uint4 a = make_uint4(0, 0, 0, 0);   // {words, chunks, matches, -}
   uint32_t bits = 0;
@@ -906,8 +964,15 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
 
   // ---- every global read, issued together ----
-  const uint4 sbr = __ldcg(&w.seg_base[seg]);       // {words, chunks, matches} within its 8-segment tile, bits
-  const uint4 tb = __ldcg(&w.tile_base[seg >> 3]);  // absolute base of that tile
+  {   // the dedup tables are not read again: empty them for the next call (a share per CTA)
+    const unsigned long long n2 = (unsigned long long)sh.T * sh.S / 2;   // slot pairs (S is even)
+    const unsigned long long per = (n2 + gridDim.x - 1) / gridDim.x;
+    const unsigned long long lo = per * blockIdx.x, hi = lo + per < n2 ? lo + per : n2;
+    uint4* sl = reinterpret_cast<uint4*>(w.slots);
+    for (unsigned long long i = lo + tid; i < hi; i += 256) sl[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+  }
+  const uint4 sbr = __ldcg(&w.seg_base[seg]);       // {words, chunks, matches} within its group, bits
+  const uint4 tb = __ldcg(&w.tile_base[sh.fold ? t : seg >> 3]);   // absolute base of its group
   const uint4 sb = make_uint4(tb.x + sbr.x, tb.y + sbr.y, tb.z + sbr.z, sbr.w);
   const uint32_t mycode = __ldcg(&w.tabcode[(size_t)t * 256 + tid]);
   uint32_t bmw = 0;
@@ -1141,9 +1206,11 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
   launch_k(k_codebook, sh.T > 0 ? sh.T : 1, 256, 0, st, sh, ep, w, out, cap, out_bytes, epoch);
   prof_end(prof, st);
   if (grid) {
-    prof_begin(prof, "k_layout", st);
-    launch_k(k_layout, (grid + 7) / 8, 256, 0, st, sh, w, out, cap, out_bytes, epoch);
-    prof_end(prof, st);
+    if (!sh.fold) {
+      prof_begin(prof, "k_layout", st);
+      launch_k(k_layout, (grid + 7) / 8, 256, 0, st, sh, w, out, cap, out_bytes, epoch);
+      prof_end(prof, st);
+    }
     prof_begin(prof, "k_emit", st);
     launch_k(k_emit<D>, grid, 256, Geo<D>::kSegSyms * 3, st, x, sh, w, out, cap, epoch);
     prof_end(prof, st);

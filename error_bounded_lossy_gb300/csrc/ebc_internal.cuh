@@ -39,7 +39,11 @@ struct Shape {
   int ref_bytes;  // 2 if B <= 65536 else 4
   int nsm;        // SMs of the device (grid sizing)
   uint64_t symstride;  // bytes per table in the code scratch: B*D rounded up to 16
+  int fold;       // 1: segment offsets are built per table inside k_codebook (nseg <= kFoldMaxSeg);
+                  // 0: by k_layout, per 8-segment tile
 };
+
+constexpr int kFoldMaxSeg = 256;
 
 // Decoder run slots: table t's runs of kDecRun chunks start at slot
 // floor(chunk0_t / kDecRun) + t, so the slots of all tables are disjoint and
@@ -89,9 +93,10 @@ struct Work {
   uint32_t* ref;               // [T][B] reference row of matched rows
   uint32_t* seg_hist;          // [T*nseg][256] literal code histogram per segment
   uint4* seg_cnt;              // [T*nseg] {literals, matches, outliers, chunks}
-  uint4* seg_desc;             // [ceil(T*nseg/8)] totals {words, chunks, matches} of each 8-segment tile
-  uint4* tile_base;            // [ceil(T*nseg/8)] absolute base of each tile
-  uint4* seg_base;             // [T*nseg] {words, chunks, matches} relative to the tile, and the bit count
+  uint4* seg_desc;             // [groups] totals {words, chunks, matches} of each group of segments
+  uint4* tile_base;            // [groups] absolute base of each group
+  uint4* seg_base;             // [T*nseg] {words, chunks, matches} relative to its group, and the bit count
+                               // (a group: the table when Shape::fold, else 8 consecutive segments)
   uint32_t* tab_hist;          // [T][256] literal code histogram per table
   uint4* tab_cnt;              // [T] {literals, matches, outliers, chunks}
   uint32_t* tabcode;           // [T][256] code << 8 | length
