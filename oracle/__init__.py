@@ -73,6 +73,14 @@ def _lib():
             lib.ebo_compress.restype = I
             lib.ebo_decompress.argtypes = [P, U64, I64, I, I, P, P]
             lib.ebo_decompress.restype = I
+            lib.ebo_compress_modes.argtypes = [P, I64, I, I, P, P, P, U64, ctypes.POINTER(Info), P, P, P]
+            lib.ebo_compress_modes.restype = I
+            lib.ebo_homo_index.argtypes = [U64, U64]
+            lib.ebo_homo_index.restype = ctypes.c_double
+            lib.ebo_speedup.argtypes = [ctypes.c_double] * 4
+            lib.ebo_speedup.restype = ctypes.c_double
+            lib.ebo_select_modes.argtypes = [P, P, P, ctypes.c_double, I, I, P]
+            lib.ebo_select_modes.restype = I
             _LIB = lib
     return _LIB
 
@@ -137,8 +145,13 @@ def compress_bound(B: int, T: int, D: int) -> int:
     return int(_lib().ebo_compress_bound(int(B), int(T), int(D)))
 
 
-def compress(x, eb, *, want_internals: bool = False):
-    """Compress x [B,T,D] float32 with per-table bounds eb [T].
+MODE_DEDUP_HUFFMAN, MODE_HUFFMAN, MODE_DEDUP_RAW, MODE_RAW = 0, 1, 2, 3
+
+
+def compress(x, eb, *, want_internals: bool = False, modes=None):
+    """Compress x [B,T,D] float32 with per-table bounds eb [T] and, optionally,
+    per-table modes [T] (0 dedup + Huffman, 1 Huffman only, 2 dedup + raw
+    8-bit codes, 3 raw codes only).
 
     Returns (container uint8 array, info dict) and, with want_internals,
     also (sym [T,B,D] uint8, ref [T,B] uint32, lens [T,256] uint8)."""
@@ -154,10 +167,15 @@ def compress(x, eb, *, want_internals: bool = False):
     sym = np.empty((T, B, D), dtype=np.uint8) if want_internals else None
     ref = np.empty((T, B), dtype=np.uint32) if want_internals else None
     lens = np.empty((T, 256), dtype=np.uint8) if want_internals else None
-    rc = _lib().ebo_compress(_ptr(x), B, T, D, _ptr(eb), _ptr(out), out.size, ctypes.byref(info),
-                             _ptr(sym) if sym is not None else None,
-                             _ptr(ref) if ref is not None else None,
-                             _ptr(lens) if lens is not None else None)
+    md = None
+    if modes is not None:
+        md = np.ascontiguousarray(modes, dtype=np.uint8)
+        assert md.shape == (T,)
+    rc = _lib().ebo_compress_modes(_ptr(x), B, T, D, _ptr(eb), _ptr(md) if md is not None else None, _ptr(out),
+                                   out.size, ctypes.byref(info),
+                                   _ptr(sym) if sym is not None else None,
+                                   _ptr(ref) if ref is not None else None,
+                                   _ptr(lens) if lens is not None else None)
     if rc != OK:
         raise RuntimeError(f"oracle compress failed: {rc}")
     d = {k: int(getattr(info, k)) for k, _ in Info._fields_}
@@ -181,3 +199,26 @@ def decompress(buf, B: int, T: int, D: int):
     if rc != OK:
         raise RuntimeError(f"oracle decompress failed: {rc}")
     return xhat, sym
+
+
+def homo_index(n_original: int, n_compressed: int) -> float:
+    """Eq. (1) Homogenization Index of one table."""
+    return float(_lib().ebo_homo_index(int(n_original), int(n_compressed)))
+
+
+def speedup(cr: float, bw: float, tc: float, td: float) -> float:
+    """Eq. (2) theoretical speed-up."""
+    return float(_lib().ebo_speedup(float(cr), float(bw), float(tc), float(td)))
+
+
+def select_modes(cr, tc, td, bw: float):
+    """Per-table argmax of Eq. (2) over M candidates: cr [T, M], tc [M], td [M]."""
+    cr = np.ascontiguousarray(cr, dtype=np.float64)
+    T, M = cr.shape
+    tc = np.ascontiguousarray(tc, dtype=np.float64)
+    td = np.ascontiguousarray(td, dtype=np.float64)
+    out = np.zeros(T, dtype=np.uint8)
+    rc = _lib().ebo_select_modes(_ptr(cr), _ptr(tc), _ptr(td), float(bw), T, M, _ptr(out))
+    if rc != OK:
+        raise ValueError("bad selection arguments")
+    return out

@@ -306,9 +306,15 @@ static int cmp_hb(const void* a, const void* c) {
 int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8_t* out,
                  uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
                  uint8_t* lens_out) {
+  return ebo_compress_modes(x, B, T, D, eb, NULL, out, cap, info, sym_out, ref_out, lens_out);
+}
+
+int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes,
+                       uint8_t* out, uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
+                       uint8_t* lens_out) {
   if (!shape_ok(B, T, D)) return EBO_ERR_INVALID_ARG;
   for (int t = 0; t < T; ++t)
-    if (!eb_ok(eb[t])) return EBO_ERR_INVALID_ARG;
+    if (!eb_ok(eb[t]) || (modes && modes[t] > 3)) return EBO_ERR_INVALID_ARG;
   const int64_t SB = seg_rows(D), KC = chunk_rows(D);
   const int64_t nseg = (B + SB - 1) / SB, nw = (B + 31) / 32;
   const int ref_bytes = B <= 65536 ? 2 : 4;
@@ -345,6 +351,10 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8
    * ref(b) < b and both vectors have the same codes and the same raw bits at
    * outliers, else a literal.  References therefore always name literals. */
   for (int t = 0; t < T; ++t) {
+    if (modes && (modes[t] & EBO_MODE_NO_DEDUP)) {   /* the table's vectors are all literals */
+      for (int64_t b = 0; b < B; ++b) ref[(size_t)t * B + b] = (uint32_t)b;
+      continue;
+    }
     for (int64_t b = 0; b < B; ++b) { pairs[b].h = hash[(size_t)t * B + b]; pairs[b].b = (uint32_t)b; }
     qsort(pairs, (size_t)B, sizeof(hb_t), cmp_hb);
     for (int64_t i = 0; i < B; ++i) {
@@ -370,8 +380,14 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8
     for (int64_t b = 0; b < B; ++b)
       if (ref[(size_t)t * B + b] == (uint32_t)b)
         for (int d = 0; d < D; ++d) f[sym[((size_t)t * B + b) * D + d]]++;
-    if (ebo_huffman_lengths(f, O_LMAX, lens + (size_t)t * 256) < 0 ||
-        ebo_canonical_codes(lens + (size_t)t * 256, O_LMAX, codes + (size_t)t * 256) < 0) {
+    if (modes && (modes[t] & EBO_MODE_RAW_CODES)) {
+      /* raw codes: every symbol 8 bits (the canonical code of symbol s is s) */
+      memset(lens + (size_t)t * 256, 8, 256);
+    } else if (ebo_huffman_lengths(f, O_LMAX, lens + (size_t)t * 256) < 0) {
+      free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
+      return EBO_ERR_INVALID_ARG;
+    }
+    if (ebo_canonical_codes(lens + (size_t)t * 256, O_LMAX, codes + (size_t)t * 256) < 0) {
       free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
       return EBO_ERR_INVALID_ARG;
     }
@@ -624,4 +640,43 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
   if (err == EBO_OK && sym_out) memcpy(sym_out, sym, N);
   free(sym);
   return err;
+}
+
+/* Homogenization Index, [DLRM-EBLC] §III-C Eq. (1): the share of a table's
+ * distinct original vectors that quantization merges away,
+ * eta = (N_original - N_compressed) / N_original.  0 when every original
+ * pattern stays distinct, close to 1 when all collapse into one.  (Tables
+ * III and IV print N_compressed / N_original, i.e. 1 - eta.)  N_original = 0
+ * gives 0. */
+double ebo_homo_index(uint64_t n_original, uint64_t n_compressed) {
+  if (n_original == 0) return 0.0;
+  return ((double)n_original - (double)n_compressed) / (double)n_original;
+}
+
+/* Theoretical speed-up of compressing the traffic, [DLRM-EBLC] §III-D Eq. (2):
+ * 1 / (1/CR + B (1/Tc + 1/Td)) with CR the compression ratio, B the network
+ * bandwidth and Tc, Td the compression and decompression throughputs (B, Tc,
+ * Td in the same unit).  A non-positive CR, Tc or Td gives 0. */
+double ebo_speedup(double cr, double bw, double tc, double td) {
+  if (!(cr > 0.0) || !(tc > 0.0) || !(td > 0.0) || bw < 0.0) return 0.0;
+  return 1.0 / (1.0 / cr + bw * (1.0 / tc + 1.0 / td));
+}
+
+/* Offline compressor selection (§III-D "Selection Between Two Encoders"):
+ * for each table t, the candidate m (of M) with the largest Eq. (2) speed-up
+ * from its sampled ratio cr[t*M + m] and the candidates' throughputs tc[m],
+ * td[m]; ties go to the lower index.  Writes choice[t]. */
+int ebo_select_modes(const double* cr, const double* tc, const double* td, double bw, int T, int M,
+                     uint8_t* choice) {
+  if (T < 0 || M < 1 || M > 255 || (T > 0 && (!cr || !tc || !td || !choice))) return EBO_ERR_INVALID_ARG;
+  for (int t = 0; t < T; ++t) {
+    int best = 0;
+    double bs = ebo_speedup(cr[(size_t)t * M], bw, tc[0], td[0]);
+    for (int m = 1; m < M; ++m) {
+      const double s = ebo_speedup(cr[(size_t)t * M + m], bw, tc[m], td[m]);
+      if (s > bs) { bs = s; best = m; }
+    }
+    choice[t] = (uint8_t)best;
+  }
+  return EBO_OK;
 }

@@ -75,6 +75,32 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb,
                  uint8_t* out, uint64_t cap, ebo_info* info,
                  uint8_t* sym_out, uint32_t* ref_out, uint8_t* lens_out);
 
+/* Per-table coding modes (bit flags; mode 0 is the default pipeline):
+ *   EBO_MODE_NO_DEDUP   no vector dedup: every vector of the table is a literal
+ *   EBO_MODE_RAW_CODES  no Huffman: every code is stored in 8 bits (all code
+ *                       lengths 8, so the canonical code of symbol s is s)
+ * Together they give the four per-table choices of the hybrid selection
+ * ([DLRM-EBLC] §III-D "Selection Between Two Encoders", Eq. (2)); all of them
+ * use the same container. */
+#define EBO_MODE_NO_DEDUP 1
+#define EBO_MODE_RAW_CODES 2
+
+/* ebo_compress with a mode per table (modes[T] in 0..3, or NULL = all 0). */
+int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes,
+                       uint8_t* out, uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
+                       uint8_t* lens_out);
+
+/* Homogenization Index, [DLRM-EBLC] §III-C Eq. (1). */
+double ebo_homo_index(uint64_t n_original, uint64_t n_compressed);
+
+/* Eq. (2) speed-up, [DLRM-EBLC] §III-D. */
+double ebo_speedup(double cr, double bw, double tc, double td);
+
+/* Per-table argmax of the Eq. (2) speed-up over M candidates (cr [T][M],
+ * tc[M], td[M]); ties to the lower index. */
+int ebo_select_modes(const double* cr, const double* tc, const double* td, double bw, int T, int M,
+                     uint8_t* choice);
+
 /* Whole decompressor: writes xhat [B,T,D] and, if not NULL, the decoded
  * quantization codes sym_out [T][B][D] (matched vectors carry their
  * reference's codes). */
