@@ -25,11 +25,15 @@ __all__ = [
     "ebc_compress_bound", "ebc_compress", "ebc_decompress", "ebc_compress_host", "ebc_decompress_host",
     "ebc_get_stats", "ebc_last_device_error", "ebc_set_profiling", "ebc_get_profile", "Codec",
     "EXPORTED_SYMBOLS", "EbcKernelTime", "EBC_ERR_SCRATCH_LIMIT", "ebc_decompress_noalloc",
+    "EBC_MODE_DEDUP_HUFFMAN", "EBC_MODE_HUFFMAN", "EBC_MODE_DEDUP_RAW", "EBC_MODE_RAW", "EbcTableStats",
+    "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup", "ebc_select_modes",
+    "ebc_select_table_modes", "ebc_table_homo_index",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
 EBC_ERR_DEVICE_TIMEOUT, EBC_ERR_CUDA, EBC_ERR_NO_DEVICE, EBC_ERR_INTERNAL = 4, 5, 6, 7
 EBC_ERR_SCRATCH_LIMIT = 8
+EBC_MODE_DEDUP_HUFFMAN, EBC_MODE_HUFFMAN, EBC_MODE_DEDUP_RAW, EBC_MODE_RAW = 0, 1, 2, 3
 EBC_DECAY_NONE, EBC_DECAY_LINEAR, EBC_DECAY_STEPWISE, EBC_DECAY_DROP, EBC_DECAY_LOG = 0, 1, 2, 3, 4
 DECAY = {"none": 0, "linear": 1, "stepwise": 2, "drop": 3, "log": 4}
 
@@ -37,13 +41,21 @@ EXPORTED_SYMBOLS = (
     "ebc_version", "ebc_strerror", "ebc_create", "ebc_destroy", "ebc_set_error_bounds",
     "ebc_get_error_bounds", "ebc_compress_bound", "ebc_compress", "ebc_decompress", "ebc_compress_host",
     "ebc_decompress_host", "ebc_get_stats", "ebc_last_device_error", "ebc_set_profiling", "ebc_get_profile",
-    "ebc_decompress_noalloc",
+    "ebc_decompress_noalloc", "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup",
+    "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index",
 )
 
 
 class EbcStats(ctypes.Structure):
     _fields_ = [(n, ctypes.c_uint64) for n in ("in_bytes", "out_bytes", "n_vectors", "n_literal", "n_match",
                                                 "n_outlier", "n_chunks", "bitstream_bytes")]
+
+    def as_dict(self):
+        return {k: int(getattr(self, k)) for k, _ in self._fields_}
+
+
+class EbcTableStats(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_uint64) for n in ("n_literal", "n_match", "n_outlier", "n_chunks", "payload_bits")]
 
     def as_dict(self):
         return {k: int(getattr(self, k)) for k, _ in self._fields_}
@@ -95,6 +107,13 @@ def lib():
                 "ebc_set_profiling": (I, [P, I]),
                 "ebc_get_profile": (I, [P, ctypes.POINTER(EbcKernelTime), I, ctypes.POINTER(I)]),
                 "ebc_decompress_noalloc": (I, [P, U64, P, I64, I, I, P]),
+                "ebc_set_table_modes": (I, [P, P, I]),
+                "ebc_get_table_stats": (I, [P, ctypes.POINTER(EbcTableStats), I]),
+                "ebc_homo_index": (D, [U64, U64]),
+                "ebc_speedup": (D, [D, D, D, D]),
+                "ebc_select_modes": (I, [P, P, P, D, I, I, P]),
+                "ebc_select_table_modes": (I, [P, P, I64, I, I, P, D, P, P]),
+                "ebc_table_homo_index": (I, [P, P, I64, I, I, P, P, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -145,6 +164,37 @@ def ebc_compress(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_bytes, st
 
 def ebc_decompress(ctx, d_in, in_bytes, d_xhat, B, T, D, stream) -> int:
     return lib().ebc_decompress(ctx, d_in, int(in_bytes), d_xhat, int(B), int(T), int(D), stream)
+
+
+def ebc_set_table_modes(ctx, modes_ptr, T) -> int:
+    return lib().ebc_set_table_modes(ctx, modes_ptr, int(T))
+
+
+def ebc_get_table_stats(ctx, T):
+    """(return code, list of EbcTableStats)."""
+    arr = (EbcTableStats * max(int(T), 1))()
+    rc = lib().ebc_get_table_stats(ctx, arr, int(T))
+    return rc, list(arr)[: int(T)]
+
+
+def ebc_homo_index(n_original, n_compressed) -> float:
+    return float(lib().ebc_homo_index(int(n_original), int(n_compressed)))
+
+
+def ebc_speedup(cr, bw, tc, td) -> float:
+    return float(lib().ebc_speedup(float(cr), float(bw), float(tc), float(td)))
+
+
+def ebc_select_modes(cr_ptr, tc_ptr, td_ptr, bw, T, M, choice_ptr) -> int:
+    return lib().ebc_select_modes(cr_ptr, tc_ptr, td_ptr, float(bw), int(T), int(M), choice_ptr)
+
+
+def ebc_select_table_modes(ctx, d_x, B, T, D, eb_ptr, bw, modes_out_ptr, stream) -> int:
+    return lib().ebc_select_table_modes(ctx, d_x, int(B), int(T), int(D), eb_ptr, float(bw), modes_out_ptr, stream)
+
+
+def ebc_table_homo_index(ctx, d_x, B, T, D, eb_ptr, eta_out_ptr, stream) -> int:
+    return lib().ebc_table_homo_index(ctx, d_x, int(B), int(T), int(D), eb_ptr, eta_out_ptr, stream)
 
 
 def ebc_decompress_noalloc(d_in, in_bytes, d_xhat, B, T, D, stream) -> int:
@@ -304,6 +354,49 @@ class Codec:
         rc = self.last_error()
         if rc:
             raise EbcError(rc, "device")
+
+    def set_table_modes(self, modes) -> None:
+        """Per-table modes (0..3) for the following compress calls; None restores mode 0."""
+        import numpy as np
+        if modes is None:
+            rc = ebc_set_table_modes(self._ctx, None, 0)
+        else:
+            a = np.ascontiguousarray(modes, dtype=np.uint8).reshape(-1)
+            rc = ebc_set_table_modes(self._ctx, a.ctypes.data_as(ctypes.c_void_p), a.size)
+        if rc:
+            raise EbcError(rc, "ebc_set_table_modes")
+
+    def table_stats(self, T: int) -> list:
+        rc, st = ebc_get_table_stats(self._ctx, T)
+        if rc:
+            raise EbcError(rc, "ebc_get_table_stats")
+        return [s.as_dict() for s in st]
+
+    def select_table_modes(self, x, eb, bandwidth: float, stream=None):
+        """Eq. (2) per-table mode choice measured on the sample batch x (CUDA [B, T, D])."""
+        import numpy as np
+        B, T, D = x.shape
+        e = np.ascontiguousarray(eb, dtype=np.float32).reshape(-1)
+        out = np.zeros(T, dtype=np.uint8)
+        rc = ebc_select_table_modes(self._ctx, ctypes.c_void_p(x.data_ptr()), B, T, D,
+                                    e.ctypes.data_as(ctypes.c_void_p), bandwidth,
+                                    out.ctypes.data_as(ctypes.c_void_p), _stream_ptr(stream))
+        if rc:
+            raise EbcError(rc, "ebc_select_table_modes")
+        return out
+
+    def table_homo_index(self, x, eb, stream=None):
+        """Eq. (1) Homogenization Index of each table of the batch x (CUDA [B, T, D])."""
+        import numpy as np
+        B, T, D = x.shape
+        e = np.ascontiguousarray(eb, dtype=np.float32).reshape(-1)
+        out = np.zeros(T, dtype=np.float64)
+        rc = ebc_table_homo_index(self._ctx, ctypes.c_void_p(x.data_ptr()), B, T, D,
+                                  e.ctypes.data_as(ctypes.c_void_p), out.ctypes.data_as(ctypes.c_void_p),
+                                  _stream_ptr(stream))
+        if rc:
+            raise EbcError(rc, "ebc_table_homo_index")
+        return out
 
     def stats(self) -> dict:
         rc, st = ebc_get_stats(self._ctx)

@@ -62,6 +62,10 @@ struct ebc_ctx {
   float* eb_base = nullptr;
   float* eb_now = nullptr;
   int sched_T = 0;
+  // per-table coding modes (0 = dedup + Huffman for every table when modes_T == 0)
+  uint8_t* d_modes = nullptr;          // device [kMaxT]
+  uint8_t h_modes[kMaxT] = {};
+  int modes_T = 0;
   // last compress shape
   int64_t lastB = 0;
   int lastT = 0, lastD = 0;
@@ -152,6 +156,8 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   w.seg_cnt = c.take<uint4>(16 * nsegT);
   w.tab_hist = c.take<uint32_t>(1024 * (size_t)sh.T);
   w.tab_cnt = c.take<uint4>(16 * (size_t)sh.T);
+  w.tab_bits = c.take<unsigned long long>(8 * (size_t)sh.T);
+  w.modes = nullptr;
   w.tabcode = c.take<uint32_t>(1024 * (size_t)sh.T);
   w.glob = g;
   *total = c.off;
@@ -227,7 +233,8 @@ int ebc_create(ebc_ctx** out, int device) {
   c->device = device;
   c->nsm = prop.multiProcessorCount;
   if (cudaMalloc(&c->glob, sizeof(Glob)) != cudaSuccess || cudaMemset(c->glob, 0, sizeof(Glob)) != cudaSuccess ||
-      cudaMalloc(&c->d_nbytes, 16) != cudaSuccess || cudaMallocHost(&c->h_pinned, 64) != cudaSuccess) {
+      cudaMalloc(&c->d_nbytes, 16) != cudaSuccess || cudaMallocHost(&c->h_pinned, 64) != cudaSuccess ||
+      cudaMalloc(&c->d_modes, kMaxT) != cudaSuccess) {
     ebc_destroy(c);
     return EBC_ERR_CUDA;
   }
@@ -249,6 +256,7 @@ void ebc_destroy(ebc_ctx* c) {
   cudaFree(c->stage_in);
   cudaFree(c->stage_out);
   cudaFree(c->d_nbytes);
+  cudaFree(c->d_modes);
   if (c->h_pinned) cudaFreeHost(c->h_pinned);
   std::free(c->eb_base);
   std::free(c->eb_now);
@@ -331,6 +339,7 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
     return EBC_ERR_INVALID_ARG;
   const uint64_t N = (uint64_t)B * T * D;
   if (N > 0 && (!d_x || !aligned16(d_x))) return EBC_ERR_INVALID_ARG;
+  if (c->modes_T != 0 && c->modes_T != T) return EBC_ERR_INVALID_ARG;
   const float* ebs = eb;
   if (!ebs) {
     if (!c->eb_now || c->sched_T != T) return EBC_ERR_INVALID_ARG;
@@ -349,14 +358,15 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
   carve_compress(nullptr, sh, c->glob, &need);
   int rc = grow(&c->cbuf, &c->cbuf_bytes, need);
   if (rc) return rc;
-  const Work w = carve_compress(c->cbuf, sh, c->glob, &need);
+  Work w = carve_compress(c->cbuf, sh, c->glob, &need);
+  w.modes = c->modes_T ? c->d_modes : nullptr;
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
   c->cepoch = (c->cepoch + 1) & 0xFFFFFFu;
   c->lastB = B;
   c->lastT = T;
   c->lastD = D;
-  // Each call leaves its dedup table empty (k_codebook).  A new layout on this
+  // Each call leaves its dedup table empty (k_emit).  A new layout on this
   // buffer starts from a reset.
   if (T > 0 && sh.nseg > 0 && (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D)) {
     if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess) return EBC_ERR_CUDA;
@@ -387,6 +397,83 @@ int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xha
   c->last_stream = st;
   c->depoch = (c->depoch + 1) & 0xFFFFFFu;
   return cuda_err(launch_decompress((const uint8_t*)d_in, in_bytes, sh, w, d_xhat, c->depoch, st, c->prof));
+}
+
+int ebc_set_table_modes(ebc_ctx* c, const uint8_t* modes, int T) {
+  if (!c) return EBC_ERR_INVALID_ARG;
+  if (!modes || T == 0) {
+    c->modes_T = 0;
+    return EBC_OK;
+  }
+  if (T < 0 || T > kMaxT) return EBC_ERR_INVALID_ARG;
+  for (int t = 0; t < T; ++t)
+    if (modes[t] > (kModeNoDedup | kModeRawCodes)) return EBC_ERR_INVALID_ARG;
+  if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
+  // no call of this context may still be reading the previous modes
+  if (cudaDeviceSynchronize() != cudaSuccess) return EBC_ERR_CUDA;
+  if (cudaMemcpy(c->d_modes, modes, (size_t)T, cudaMemcpyHostToDevice) != cudaSuccess) return EBC_ERR_CUDA;
+  std::memcpy(c->h_modes, modes, (size_t)T);
+  c->modes_T = T;
+  return EBC_OK;
+}
+
+int ebc_get_table_stats(ebc_ctx* c, ebc_table_stats* out, int T) {
+  if (!c || !out || T <= 0 || T != c->lastT) return EBC_ERR_INVALID_ARG;
+  const int err = ebc_last_device_error(c);
+  if (err == EBC_ERR_CUDA) return err;
+  const Shape sh = make_shape(c->lastB, T, c->lastD, c->nsm);
+  std::memset(out, 0, sizeof(*out) * (size_t)T);
+  if (sh.nseg == 0 || !c->cbuf) return err;   // an empty batch: nothing was coded
+  size_t need = 0;
+  const Work w = carve_compress(c->cbuf, sh, c->glob, &need);   // the last compress's layout
+  uint4* cnt = new (std::nothrow) uint4[(size_t)T];
+  unsigned long long* bits = new (std::nothrow) unsigned long long[(size_t)T];
+  int rc = err;
+  if (!cnt || !bits) {
+    rc = EBC_ERR_INTERNAL;
+  } else if (cudaMemcpy(cnt, w.tab_cnt, 16 * (size_t)T, cudaMemcpyDeviceToHost) != cudaSuccess ||
+             cudaMemcpy(bits, w.tab_bits, 8 * (size_t)T, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    rc = EBC_ERR_CUDA;
+  } else {
+    for (int t = 0; t < T; ++t) {
+      out[t].n_literal = cnt[t].x;
+      out[t].n_match = cnt[t].y;
+      out[t].n_outlier = cnt[t].z;
+      out[t].n_chunks = cnt[t].w;
+      out[t].payload_bits = bits[t];
+    }
+  }
+  delete[] cnt;
+  delete[] bits;
+  return rc;
+}
+
+double ebc_homo_index(uint64_t n_original, uint64_t n_compressed) {
+  if (n_original == 0) return 0.0;
+  return ((double)n_original - (double)n_compressed) / (double)n_original;
+}
+
+double ebc_speedup(double cr, double bw, double tc, double td) {
+  if (!(cr > 0.0) || !(tc > 0.0) || !(td > 0.0) || bw < 0.0) return 0.0;
+  return 1.0 / (1.0 / cr + bw * (1.0 / tc + 1.0 / td));
+}
+
+int ebc_select_modes(const double* cr, const double* tc, const double* td, double bw, int T, int M,
+                     uint8_t* choice) {
+  if (T < 0 || M < 1 || M > 255 || (T > 0 && (!cr || !tc || !td || !choice))) return EBC_ERR_INVALID_ARG;
+  for (int t = 0; t < T; ++t) {
+    int best = 0;
+    double top = ebc_speedup(cr[(size_t)t * M], bw, tc[0], td[0]);
+    for (int m = 1; m < M; ++m) {
+      const double s = ebc_speedup(cr[(size_t)t * M + m], bw, tc[m], td[m]);
+      if (s > top) {
+        top = s;
+        best = m;
+      }
+    }
+    choice[t] = (uint8_t)best;
+  }
+  return EBC_OK;
 }
 
 int ebc_last_device_error(ebc_ctx* c) {
@@ -511,6 +598,114 @@ int ebc_get_profile(ebc_ctx* c, ebc_kernel_time* out, int capacity, int* count) 
   return EBC_OK;
 }
 
+
+// Compresses (and, with d_xhat, decompresses) one batch in the given mode for
+// every table; returns the per-table stats and the event-timed durations.
+static int run_mode(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, int mode,
+                    ebc_table_stats* stats, float* ms_c, float* ms_d, cudaStream_t st) {
+  uint8_t modes[kMaxT];
+  std::memset(modes, mode, (size_t)T);
+  int rc = ebc_set_table_modes(c, modes, T);
+  if (rc) return rc;
+  const uint64_t N = (uint64_t)B * T * D;
+  const uint64_t cap = ebc_compress_bound(B, T, D);
+  rc = grow(&c->stage_out, &c->stage_out_bytes, cap);
+  if (!rc) rc = grow(&c->stage_in, &c->stage_in_bytes, N * 4u);
+  if (rc) return rc;
+  cudaEvent_t ev[4];
+  for (cudaEvent_t& e : ev)
+    if (cudaEventCreate(&e) != cudaSuccess) return EBC_ERR_CUDA;
+  // a warm-up call, then a timed one of each direction
+  rc = ebc_compress(c, d_x, B, T, D, eb, c->stage_out, cap, (uint64_t*)c->d_nbytes, st);
+  if (!rc && cudaEventRecord(ev[0], st) != cudaSuccess) rc = EBC_ERR_CUDA;
+  if (!rc) rc = ebc_compress(c, d_x, B, T, D, eb, c->stage_out, cap, (uint64_t*)c->d_nbytes, st);
+  if (!rc && (cudaEventRecord(ev[1], st) != cudaSuccess ||
+              cudaMemcpyAsync(c->h_pinned, c->d_nbytes, 8, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+              cudaStreamSynchronize(st) != cudaSuccess))
+    rc = EBC_ERR_CUDA;
+  if (!rc) rc = ebc_get_table_stats(c, stats, T);
+  const uint64_t n = c->h_pinned[0];
+  if (!rc) rc = ebc_decompress(c, c->stage_out, n, (float*)c->stage_in, B, T, D, st);
+  if (!rc && cudaEventRecord(ev[2], st) != cudaSuccess) rc = EBC_ERR_CUDA;
+  if (!rc) rc = ebc_decompress(c, c->stage_out, n, (float*)c->stage_in, B, T, D, st);
+  if (!rc && (cudaEventRecord(ev[3], st) != cudaSuccess || cudaStreamSynchronize(st) != cudaSuccess)) rc = EBC_ERR_CUDA;
+  if (!rc) rc = ebc_last_device_error(c);
+  if (!rc && (cudaEventElapsedTime(ms_c, ev[0], ev[1]) != cudaSuccess ||
+              cudaEventElapsedTime(ms_d, ev[2], ev[3]) != cudaSuccess))
+    rc = EBC_ERR_CUDA;
+  for (cudaEvent_t& e : ev) cudaEventDestroy(e);
+  return rc;
+}
+
+// Restores the caller's modes after a sampling run.
+static int restore_modes(ebc_ctx* c, int saved_T, const uint8_t* saved) {
+  return ebc_set_table_modes(c, saved_T ? saved : nullptr, saved_T);
+}
+
+int ebc_select_table_modes(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, double bw,
+                           uint8_t* modes_out, void* stream) {
+  if (!c || !shape_ok(B, T, D) || T == 0 || B == 0 || !eb || !modes_out || !d_x || bw < 0.0)
+    return EBC_ERR_INVALID_ARG;
+  const int saved_T = c->modes_T;
+  uint8_t saved[kMaxT];
+  std::memcpy(saved, c->h_modes, (size_t)kMaxT);
+  const Shape sh = make_shape(B, T, D, c->nsm);
+  const double raw_bytes = 4.0 * (double)B * D;   // per table
+  const double fixed = (double)kTableRecBytes + (double)kSegRecBytes * sh.nseg + 4.0 * sh.nw;
+  double* cr = new (std::nothrow) double[(size_t)T * 4];
+  ebc_table_stats* st = new (std::nothrow) ebc_table_stats[(size_t)T];
+  double tc[4], td[4];
+  int rc = (!cr || !st) ? EBC_ERR_INTERNAL : EBC_OK;
+  for (int m = 0; m < 4 && !rc; ++m) {
+    float ms_c = 0.f, ms_d = 0.f;
+    rc = run_mode(c, d_x, B, T, D, eb, m, st, &ms_c, &ms_d, (cudaStream_t)stream);
+    if (rc) break;
+    tc[m] = raw_bytes * T / (ms_c * 1e-3);
+    td[m] = raw_bytes * T / (ms_d * 1e-3);
+    for (int t = 0; t < T; ++t) {
+      const double bytes = (double)st[t].payload_bits / 8.0 + 2.0 * st[t].n_chunks +
+                           (double)sh.ref_bytes * st[t].n_match + fixed;
+      cr[(size_t)t * 4 + m] = raw_bytes / bytes;
+    }
+  }
+  const int rr = restore_modes(c, saved_T, saved);
+  if (!rc) rc = rr;
+  if (!rc) rc = ebc_select_modes(cr, tc, td, bw, T, 4, modes_out);
+  delete[] cr;
+  delete[] st;
+  return rc;
+}
+
+int ebc_table_homo_index(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb,
+                         double* eta_out, void* stream) {
+  if (!c || !shape_ok(B, T, D) || T == 0 || !eb || !eta_out || (B > 0 && !d_x)) return EBC_ERR_INVALID_ARG;
+  const int saved_T = c->modes_T;
+  uint8_t saved[kMaxT];
+  std::memcpy(saved, c->h_modes, (size_t)kMaxT);
+  float* tiny = new (std::nothrow) float[(size_t)T];
+  ebc_table_stats* a = new (std::nothrow) ebc_table_stats[(size_t)T];
+  ebc_table_stats* b = new (std::nothrow) ebc_table_stats[(size_t)T];
+  int rc = (!tiny || !a || !b) ? EBC_ERR_INTERNAL : EBC_OK;
+  if (!rc) {
+    for (int t = 0; t < T; ++t) tiny[t] = 1.17549435e-38f;   // the smallest admissible bound
+    rc = ebc_set_table_modes(c, nullptr, 0);
+  }
+  const uint64_t cap = ebc_compress_bound(B, T, D);
+  if (!rc) rc = grow(&c->stage_out, &c->stage_out_bytes, cap);
+  cudaStream_t s = (cudaStream_t)stream;
+  if (!rc) rc = ebc_compress(c, d_x, B, T, D, eb, c->stage_out, cap, (uint64_t*)c->d_nbytes, s);
+  if (!rc) rc = ebc_get_table_stats(c, a, T);
+  if (!rc) rc = ebc_compress(c, d_x, B, T, D, tiny, c->stage_out, cap, (uint64_t*)c->d_nbytes, s);
+  if (!rc) rc = ebc_get_table_stats(c, b, T);
+  if (!rc)
+    for (int t = 0; t < T; ++t) eta_out[t] = ebc_homo_index(b[t].n_literal, a[t].n_literal);
+  const int rr = restore_modes(c, saved_T, saved);
+  if (!rc) rc = rr;
+  delete[] tiny;
+  delete[] a;
+  delete[] b;
+  return rc;
+}
 
 }  // extern "C"
 

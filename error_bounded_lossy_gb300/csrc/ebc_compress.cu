@@ -289,10 +289,11 @@ __global__ void __launch_bounds__(256) k_insert(Shape sh, Work w) {
   pdl_enter();
   const unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
   const unsigned long long nvec = (unsigned long long)sh.B * sh.T;
-  const bool valid = i < nvec;
+  const int t = i < nvec ? (int)(i / (unsigned long long)sh.B) : 0;
+  // (a table without dedup enters no keys)
+  const bool valid = i < nvec && !(w.modes && (w.modes[t] & kModeNoDedup));
   const unsigned vmask = __ballot_sync(0xffffffffu, valid);
   if (!valid) return;
-  const int t = (int)(i / (unsigned long long)sh.B);
   const uint32_t b = (uint32_t)(i - (unsigned long long)t * sh.B);
   const uint32_t h = __ldcg(&w.vhash[i]);
   // lanes are consecutive rows: of the lanes holding the same (table, key),
@@ -343,6 +344,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
   const int64_t row0 = (int64_t)s * G::kSB;
   const unsigned long long* slots = w.slots + (size_t)t * sh.S;
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
+  const bool nodedup = w.modes && (w.modes[t] & kModeNoDedup);   // every row its own reference
   {   // the segment's codes (rows contiguous; the table stride is padded to 16 bytes), copied
       // asynchronously while the keys are looked up
     const int64_t nrows = B - row0 < G::kSB ? B - row0 : G::kSB;
@@ -367,7 +369,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
       const int r = k * kNT + tid;
       const int64_t b = row0 + r;
       if (r < G::kSB && b < B) {
-        uint32_t ref = dedup_lookup(slots, sh.S, h[k], w.glob);
+        uint32_t ref = nodedup ? (uint32_t)b : dedup_lookup(slots, sh.S, h[k], w.glob);
         if (ref > (uint32_t)b) ref = (uint32_t)b;   // only on an internal error
         s_ref[r] = ref;
         s_nout[r] = no[k];
@@ -579,6 +581,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   __shared__ uint32_t s_f[256], s_lw[256], s_nodew[256];
   __shared__ unsigned long long s_key[256];
   __shared__ uint4 s_seg[kFoldMaxSeg];
+  __shared__ unsigned long long s_bits64[8];
   __shared__ uint16_t s_order[256];
   __shared__ uint8_t s_leafpar[256], s_nodepar[256], s_depth[256], s_len[256];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2];
@@ -591,9 +594,12 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
 
   if (t < T) {
     // (with no segments, k_quantize did not run and the accumulators are stale)
-    s_f[tid] = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)t * 256 + tid]) : 0u;
+    const uint32_t f0 = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)t * 256 + tid]) : 0u;
+    s_f[tid] = f0;
+    const bool raw = w.modes && (w.modes[t] & kModeRawCodes);   // every code 8 bits: no Huffman
+    if (raw) s_len[tid] = 8;
     __syncthreads();
-    for (int round = 0; round < 40; ++round) {
+    for (int round = 0; round < 40 && !raw; ++round) {
       const uint32_t fi = s_f[tid];
       // leaves in (count, symbol) order: a bitonic sort of the keys count << 8 | symbol over the
       // 256 threads (absent symbols sort last); thread i ends with the key of rank i
@@ -682,6 +688,18 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       for (int j = 0; j < tid; ++j) code += (s_len[j] == L);
     }
     w.tabcode[(size_t)t * 256 + tid] = (code << 8) | L;
+    {   // bits of the table's literal codes, plus the raw bits of its outliers (symbol 0)
+      unsigned long long sum = (unsigned long long)f0 * L + (tid == 0 ? 32ull * f0 : 0ull);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+      if ((tid & 31) == 0) s_bits64[tid >> 5] = sum;
+      __syncthreads();
+      if (tid == 0) {
+        unsigned long long tot = 0;
+        for (int k = 0; k < 8; ++k) tot += s_bits64[k];
+        w.tab_bits[t] = tot;
+      }
+    }
     uint8_t* rec = out + kHeaderBytes + (size_t)t * kTableRecBytes;
     rec[16 + tid] = (uint8_t)L;
     if (tid == 0) {

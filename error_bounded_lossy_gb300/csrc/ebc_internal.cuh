@@ -45,6 +45,10 @@ struct Shape {
 
 constexpr int kFoldMaxSeg = 256;
 
+// Per-table coding modes (bit flags; 0 = vector dedup + Huffman codes).
+constexpr uint32_t kModeNoDedup = 1;   // every vector of the table is a literal
+constexpr uint32_t kModeRawCodes = 2;  // every code 8 bits (lengths all 8: code of symbol s is s)
+
 // Decoder run slots: table t's runs of kDecRun chunks start at slot
 // floor(chunk0_t / kDecRun) + t, so the slots of all tables are disjoint and
 // ordered, and every slot below floor(n_chunks / kDecRun) + T is written.
@@ -84,6 +88,8 @@ struct DecTab {
 
 // Device scratch of a context.  Sizes follow Shape.
 struct Work {
+  const uint8_t* modes;        // [T] per-table modes, or null (all 0)
+  unsigned long long* tab_bits;   // [T] bits of the table's literal codes and outlier values
   // compress
   uint8_t* sym;                // [T][B][D] quantization codes, table t at t * symstride (16-byte aligned)
   uint32_t* vhash;             // [T][B] dedup key

@@ -162,6 +162,76 @@ int ebc_compress_host(ebc_ctx* ctx, const float* h_x, int64_t B, int T, int D, c
 int ebc_decompress_host(ebc_ctx* ctx, const void* h_in, uint64_t in_bytes, float* h_xhat,
                         int64_t B, int T, int D, void* stream);
 
+/* ---- Per-table hybrid coding (the pages' "Selection Between Two Encoders",
+ * §III-D, Eq. (2)) and the Homogenization Index (§III-C, Eq. (1)) ----
+ *
+ * Every table can be coded in one of four modes; all of them produce the same
+ * container, which ebc_decompress reads unchanged:
+ *   EBC_MODE_DEDUP_HUFFMAN  vector dedup + per-table canonical Huffman (default)
+ *   EBC_MODE_HUFFMAN        no dedup: every vector a literal, Huffman codes
+ *   EBC_MODE_DEDUP_RAW      vector dedup, each code stored in 8 bits
+ *   EBC_MODE_RAW            no dedup, 8-bit codes
+ * The quantization (and so the reconstruction) is the same in every mode. */
+typedef enum {
+  EBC_MODE_DEDUP_HUFFMAN = 0,
+  EBC_MODE_HUFFMAN = 1,
+  EBC_MODE_DEDUP_RAW = 2,
+  EBC_MODE_RAW = 3
+} ebc_mode;
+
+/* Sets the modes (host array modes[T], values 0..3) used by the following
+ * compress calls of the context, which must then have this T (else
+ * EBC_ERR_INVALID_ARG).  modes == NULL or T == 0 restores mode 0 for every
+ * table and any T.  Synchronises the device before it replaces the modes. */
+int ebc_set_table_modes(ebc_ctx* ctx, const uint8_t* modes, int T);
+
+/* Per-table counts of the last compress call (synchronises its stream). */
+typedef struct {
+  uint64_t n_literal;     /* distinct quantized vectors kept (N_compressed of Eq. (1)) */
+  uint64_t n_match;       /* vectors coded as references                               */
+  uint64_t n_outlier;     /* raw values stored                                         */
+  uint64_t n_chunks;      /* chunk-index entries                                       */
+  uint64_t payload_bits;  /* bits of the literal codes and outlier values              */
+} ebc_table_stats;
+
+/* Writes out[T] for the last compress call, whose T it must be.  Returns the
+ * device error recorded by the context, if any (as ebc_last_device_error). */
+int ebc_get_table_stats(ebc_ctx* ctx, ebc_table_stats* out, int T);
+
+/* Eq. (1): eta = (N_original - N_compressed) / N_original (0 when
+ * N_original = 0): 0 when quantization merges no distinct vectors, towards 1
+ * when they collapse into one.  (The pages' Tables III and IV print
+ * N_compressed / N_original = 1 - eta.) */
+double ebc_homo_index(uint64_t n_original, uint64_t n_compressed);
+
+/* Eq. (2): speed-up = 1 / (1/CR + bw * (1/Tc + 1/Td)), CR the compression
+ * ratio, bw the network bandwidth, Tc and Td the compression and
+ * decompression throughputs (bw, Tc, Td in one unit).  0 for CR, Tc or Td not
+ * positive or bw negative. */
+double ebc_speedup(double cr, double bw, double tc, double td);
+
+/* For each table t, the candidate m < M with the largest Eq. (2) speed-up from
+ * cr[t*M + m], tc[m], td[m] (ties to the lower m), written to choice[t]. */
+int ebc_select_modes(const double* cr, const double* tc, const double* td, double bw, int T, int M,
+                     uint8_t* choice);
+
+/* Offline selection on a sample batch (device x[B][T][D], host eb[T], both as
+ * for ebc_compress): compresses and decompresses it in each of the four modes
+ * (timed with CUDA events on `stream`), takes each table's compression ratio
+ * (4*B*D over its payload, chunk-index, reference and record bytes) and each
+ * mode's throughputs, and writes the Eq. (2) choice for bandwidth bw (bytes/s)
+ * to modes_out[T].  The context's own modes are kept.  Synchronous. */
+int ebc_select_table_modes(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D, const float* eb, double bw,
+                           uint8_t* modes_out, void* stream);
+
+/* Eq. (1) per table for a batch: N_compressed = distinct quantized vectors
+ * under eb[t] (mode 0), N_original = distinct vectors of the raw values
+ * (compressed at the smallest admissible bound, where every value of
+ * magnitude above about 3e-36 is an outlier kept bit-exactly).  Writes
+ * eta_out[T].  The context's own modes are kept.  Synchronous. */
+int ebc_table_homo_index(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D, const float* eb,
+                         double* eta_out, void* stream);
+
 /* Allocation-free decompression.  The paper has no counterpart: this entry
  * point exists for callers that cannot allocate device memory while they
  * decode -- a process that has handed its device memory to another allocator
