@@ -48,6 +48,9 @@ def parse():
     p.add_argument("--cpu-seconds", type=float, default=10.0, help="oracle CPU-baseline budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--link-gbs", type=float, default=12.5,
+                   help="network bandwidth (GB/s) for the Eq. (2) per-table mode choice (12.5 = 100 Gb/s)")
+    p.add_argument("--no-hybrid", action="store_true", help="skip the per-table mode measurements")
     return p.parse_args()
 
 
@@ -330,6 +333,55 @@ def main():
         e2e_t.append(time.perf_counter() - s)
     e2e_value = 4 * N / statistics.median(e2e_t) / 1e9
 
+    # ---- per-table hybrid modes (outside the timed region) ----
+    hybrid = None
+    if not args.no_hybrid:
+        hyb_steps = max(3, min(K, 50))
+
+        def timed(n):
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                   torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            step()
+            torch.cuda.synchronize()
+            for a, b, c_ in ev:
+                flush.zero_()
+                a.record(stream)
+                codec.compress_into(x, eb, out, nbytes, stream)
+                b.record(stream)
+                codec.decompress_into(out, cap, xhat, stream)
+                c_.record(stream)
+            torch.cuda.synchronize()
+            codec.check()
+            tc = sum(a.elapsed_time(b) for a, b, _ in ev) / 1e3 / n
+            td = sum(b.elapsed_time(c_) for _, b, c_ in ev) / 1e3 / n
+            return tc, td, codec.stats()["out_bytes"]
+
+        link = args.link_gbs * 1e9
+        names = {0: "dedup_huffman", 1: "huffman", 2: "dedup_raw", 3: "raw"}
+        modes_out = {}
+        for m in range(4):
+            codec.set_table_modes(np.full(T, m, np.uint8))
+            tc, td, sz = timed(hyb_steps)
+            modes_out[names[m]] = {"compress_gbs": round(4 * N / tc / 1e9, 1), "decompress_gbs": round(4 * N / td / 1e9, 1),
+                                   "compression_ratio": round(4 * N / sz, 3),
+                                   "speedup_eq2": round(ebc.ebc_speedup(4 * N / sz, link, 4 * N / tc, 4 * N / td), 3)}
+        codec.set_table_modes(None)
+        choice = codec.select_table_modes(x, eb, bandwidth=link)
+        codec.set_table_modes(choice)
+        tc, td, sz = timed(hyb_steps)
+        codec.set_table_modes(None)
+        eta = codec.table_homo_index(x, eb)
+        hybrid = {
+            "link_gbs": args.link_gbs, "steps": hyb_steps, "modes": modes_out,
+            "selected": {"per_table": choice.tolist(),
+                         "counts": {names[m]: int((choice == m).sum()) for m in range(4)},
+                         "compress_gbs": round(4 * N / tc / 1e9, 1), "decompress_gbs": round(4 * N / td / 1e9, 1),
+                         "compression_ratio": round(4 * N / sz, 3),
+                         "speedup_eq2": round(ebc.ebc_speedup(4 * N / sz, link, 4 * N / tc, 4 * N / td), 3)},
+            "homo_index": {"min": round(float(eta.min()), 4), "median": round(float(np.median(eta)), 4),
+                           "max": round(float(eta.max()), 4)},
+        }
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sample = workloads.make(WORKLOAD, batch=512)
@@ -359,6 +411,7 @@ def main():
             "e2e": {"value": round(e2e_value, 3), "unit": "GB/s", "h2d_bytes_per_step": 4 * N + C,
                     "d2h_bytes_per_step": 8 + C + 4 * N},
             "cpu_baseline": cpu,
+            "hybrid": hybrid,
             "clocks": clocks,
             "wall_s": round(wall, 3),
         }
