@@ -75,6 +75,8 @@ def _lib():
             lib.ebo_decompress.restype = I
             lib.ebo_compress_modes.argtypes = [P, I64, I, I, P, P, P, U64, ctypes.POINTER(Info), P, P, P]
             lib.ebo_compress_modes.restype = I
+            lib.ebo_compress_ex.argtypes = [P, I64, I, I, P, P, I, P, U64, ctypes.POINTER(Info), P, P, P]
+            lib.ebo_compress_ex.restype = I
             lib.ebo_homo_index.argtypes = [U64, U64]
             lib.ebo_homo_index.restype = ctypes.c_double
             lib.ebo_speedup.argtypes = [ctypes.c_double] * 4
@@ -148,10 +150,11 @@ def compress_bound(B: int, T: int, D: int) -> int:
 MODE_DEDUP_HUFFMAN, MODE_HUFFMAN, MODE_DEDUP_RAW, MODE_RAW = 0, 1, 2, 3
 
 
-def compress(x, eb, *, want_internals: bool = False, modes=None):
+def compress(x, eb, *, want_internals: bool = False, modes=None, window: int = 0):
     """Compress x [B,T,D] float32 with per-table bounds eb [T] and, optionally,
     per-table modes [T] (0 dedup + Huffman, 1 Huffman only, 2 dedup + raw
-    8-bit codes, 3 raw codes only).
+    8-bit codes, 3 raw codes only) and a dedup window (0 = whole batch, first
+    occurrence; 1..255 = nearest earlier vector within that many rows).
 
     Returns (container uint8 array, info dict) and, with want_internals,
     also (sym [T,B,D] uint8, ref [T,B] uint32, lens [T,256] uint8)."""
@@ -171,8 +174,8 @@ def compress(x, eb, *, want_internals: bool = False, modes=None):
     if modes is not None:
         md = np.ascontiguousarray(modes, dtype=np.uint8)
         assert md.shape == (T,)
-    rc = _lib().ebo_compress_modes(_ptr(x), B, T, D, _ptr(eb), _ptr(md) if md is not None else None, _ptr(out),
-                                   out.size, ctypes.byref(info),
+    rc = _lib().ebo_compress_ex(_ptr(x), B, T, D, _ptr(eb), _ptr(md) if md is not None else None, int(window),
+                                _ptr(out), out.size, ctypes.byref(info),
                                    _ptr(sym) if sym is not None else None,
                                    _ptr(ref) if ref is not None else None,
                                    _ptr(lens) if lens is not None else None)

@@ -312,12 +312,18 @@ int ebo_compress(const float* x, int64_t B, int T, int D, const float* eb, uint8
 int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes,
                        uint8_t* out, uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
                        uint8_t* lens_out) {
-  if (!shape_ok(B, T, D)) return EBO_ERR_INVALID_ARG;
+  return ebo_compress_ex(x, B, T, D, eb, modes, 0, out, cap, info, sym_out, ref_out, lens_out);
+}
+
+int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes, int window,
+                    uint8_t* out, uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
+                    uint8_t* lens_out) {
+  if (!shape_ok(B, T, D) || window < 0 || window > EBO_MAX_WINDOW) return EBO_ERR_INVALID_ARG;
   for (int t = 0; t < T; ++t)
     if (!eb_ok(eb[t]) || (modes && modes[t] > 3)) return EBO_ERR_INVALID_ARG;
   const int64_t SB = seg_rows(D), KC = chunk_rows(D);
   const int64_t nseg = (B + SB - 1) / SB, nw = (B + 31) / 32;
-  const int ref_bytes = B <= 65536 ? 2 : 4;
+  const int ref_bytes = window > 0 ? 1 : (B <= 65536 ? 2 : 4);
   const size_t nvec = (size_t)B * (size_t)T;
   const size_t N = nvec * (size_t)D;
 
@@ -353,6 +359,30 @@ int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb,
   for (int t = 0; t < T; ++t) {
     if (modes && (modes[t] & EBO_MODE_NO_DEDUP)) {   /* the table's vectors are all literals */
       for (int64_t b = 0; b < B; ++b) ref[(size_t)t * B + b] = (uint32_t)b;
+      continue;
+    }
+    if (window > 0) {
+      /* sliding window ([DLRM-EBLC] §III-E "extended window size", §IV-D Table VI): the
+       * reference is the nearest earlier row within `window` rows with the same hash; b is a
+       * match when it also has the same codes and raw outlier bits, else a literal.  A
+       * reference may itself be a match (chains end at a literal). */
+      for (int64_t b = 0; b < B; ++b) {
+        const uint32_t hb = hash[(size_t)t * B + b];
+        int64_t r = b;
+        for (int64_t c2 = b - 1; c2 >= 0 && c2 >= b - window; --c2)
+          if (hash[(size_t)t * B + c2] == hb) { r = c2; break; }
+        int match = 0;
+        if (r < b) {
+          const uint8_t* sb = sym + ((size_t)t * B + b) * D;
+          const uint8_t* sr = sym + ((size_t)t * B + r) * D;
+          const float* xb = x + ((size_t)b * T + t) * D;
+          const float* xr = x + ((size_t)r * T + t) * D;
+          match = memcmp(sb, sr, (size_t)D) == 0;
+          for (int d = 0; match && d < D; ++d)
+            if (sb[d] == 0 && f2u(xb[d]) != f2u(xr[d])) match = 0;
+        }
+        ref[(size_t)t * B + b] = match ? (uint32_t)r : (uint32_t)b;
+      }
       continue;
     }
     for (int64_t b = 0; b < B; ++b) { pairs[b].h = hash[(size_t)t * B + b]; pairs[b].b = (uint32_t)b; }
@@ -429,7 +459,7 @@ int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb,
   wr32(h + 0, O_MAGIC); wr32(h + 4, O_VERSION); wr64(h + 8, (uint64_t)B);
   wr32(h + 16, (uint32_t)T); wr32(h + 20, (uint32_t)D); wr32(h + 24, O_RADIUS);
   wr32(h + 28, O_LMAX); wr32(h + 32, (uint32_t)SB); wr32(h + 36, (uint32_t)KC);
-  wr32(h + 40, (uint32_t)ref_bytes); wr32(h + 44, 0);
+  wr32(h + 40, (uint32_t)ref_bytes); wr32(h + 44, (uint32_t)window);
   wr64(h + 48, n_lit); wr64(h + 56, n_match); wr64(h + 64, n_out); wr64(h + 72, n_chunks);
   wr64(h + 80, words); wr64(h + 88, L.off_seg); wr64(h + 96, L.off_bitmap);
   wr64(h + 104, L.off_chunks); wr64(h + 112, L.off_refs); wr64(h + 120, L.off_bits);
@@ -451,7 +481,8 @@ int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb,
         if (r != (uint32_t)b) {
           uint8_t* bm = out + L.off_bitmap + ((size_t)t * nw + (size_t)(b >> 5)) * 4;
           wr32(bm, rd32(bm) | (1u << (b & 31)));
-          if (ref_bytes == 2) wr16(out + L.off_refs + match_i * 2, r);
+          if (window > 0) out[L.off_refs + match_i] = (uint8_t)((uint32_t)b - r);   /* distance */
+          else if (ref_bytes == 2) wr16(out + L.off_refs + match_i * 2, r);
           else wr32(out + L.off_refs + match_i * 4, r);
           ++match_i; ++tm;
           continue;
@@ -522,9 +553,10 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
     return EBO_ERR_INVALID_ARG;
   const int64_t SB = seg_rows(D), KC = chunk_rows(D);
   const int64_t nseg = (B + SB - 1) / SB, nw = (B + 31) / 32;
-  const int ref_bytes = B <= 65536 ? 2 : 4;
+  const uint32_t window = rd32(in + 44);   /* 0: whole-batch references; else distances */
+  const int ref_bytes = window > 0 ? 1 : (B <= 65536 ? 2 : 4);
   if (rd32(in + 24) != O_RADIUS || rd32(in + 28) != O_LMAX || rd32(in + 32) != (uint32_t)SB ||
-      rd32(in + 36) != (uint32_t)KC || rd32(in + 40) != (uint32_t)ref_bytes || rd32(in + 44) != 0)
+      rd32(in + 36) != (uint32_t)KC || rd32(in + 40) != (uint32_t)ref_bytes || window > EBO_MAX_WINDOW)
     return EBO_ERR_CORRUPT;
   uint64_t n_lit = rd64(in + 48), n_match = rd64(in + 56), n_out = rd64(in + 64);
   uint64_t n_chunks = rd64(in + 72), words = rd64(in + 80);
@@ -619,16 +651,24 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
     }
     if (err) break;
     if (rd32(rec + 4) != tl || rd32(rec + 8) != tm || rd32(rec + 12) != to) err = EBO_ERR_CORRUPT;
-    /* matches: copy the reference row (references always name literals) */
+    /* matches, in row order: copy the reference row.  Whole-batch references name literals;
+     * window references are distances and may name an earlier match (already copied) */
     if (err == EBO_OK) {
       uint64_t m = match_i - tm;
       for (int64_t b = 0; b < B && err == EBO_OK; ++b) {
         const uint8_t* bm = in + L.off_bitmap + ((size_t)t * nw + (size_t)(b >> 5)) * 4;
         if (!((rd32(bm) >> (b & 31)) & 1u)) continue;
-        uint32_t r = ref_bytes == 2 ? rd16(in + L.off_refs + m * 2) : rd32(in + L.off_refs + m * 4);
+        uint32_t r;
+        if (window > 0) {
+          const uint32_t dist = in[L.off_refs + m];
+          if (dist == 0 || dist > window || (int64_t)dist > b) { err = EBO_ERR_CORRUPT; break; }
+          r = (uint32_t)(b - dist);
+        } else {
+          r = ref_bytes == 2 ? rd16(in + L.off_refs + m * 2) : rd32(in + L.off_refs + m * 4);
+        }
         ++m;
         const uint8_t* bmr = in + L.off_bitmap + ((size_t)t * nw + (size_t)(r >> 5)) * 4;
-        if ((int64_t)r >= b || ((rd32(bmr) >> (r & 31)) & 1u)) { err = EBO_ERR_CORRUPT; break; }
+        if ((int64_t)r >= b || (window == 0 && ((rd32(bmr) >> (r & 31)) & 1u))) { err = EBO_ERR_CORRUPT; break; }
         memcpy(sym + ((size_t)t * B + b) * D, sym + ((size_t)t * B + r) * D, (size_t)D);
         memcpy(xhat + ((size_t)b * T + t) * D, xhat + ((size_t)r * T + t) * D, (size_t)D * 4);
       }

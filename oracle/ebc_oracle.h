@@ -90,6 +90,16 @@ int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb,
                        uint8_t* out, uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
                        uint8_t* lens_out);
 
+/* Sliding-window vector LZ ([DLRM-EBLC] §III-E "extended window size",
+ * §IV-D Table VI): with window W in 1..EBO_MAX_WINDOW a vector's reference is
+ * the nearest earlier vector of its table within W rows with the same key
+ * (a match when codes and raw outlier bits are equal), stored as a one-byte
+ * distance; header field 44 holds W (0 = whole-batch first occurrence). */
+#define EBO_MAX_WINDOW 255
+int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes, int window,
+                    uint8_t* out, uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
+                    uint8_t* lens_out);
+
 /* Homogenization Index, [DLRM-EBLC] §III-C Eq. (1). */
 double ebo_homo_index(uint64_t n_original, uint64_t n_compressed);
 
