@@ -382,6 +382,23 @@ def main():
                            "max": round(float(eta.max()), 4)},
         }
 
+    # ---- sliding-window vector LZ (outside the timed region): ratio and throughput per window ----
+    window = None
+    if not args.no_hybrid:
+        rows = {}
+        base_cr = None
+        for wsz in (32, 64, 128, 255, 0):
+            codec.set_window(wsz)
+            tc, td, sz = timed(max(3, min(K, 20)))
+            cr = 4 * N / sz
+            if base_cr is None:
+                base_cr = cr
+            rows["batch" if wsz == 0 else str(wsz)] = {
+                "compression_ratio": round(cr, 3), "vs_window_32": round(cr / base_cr, 3),
+                "compress_gbs": round(4 * N / tc / 1e9, 1), "decompress_gbs": round(4 * N / td / 1e9, 1)}
+        codec.set_window(0)
+        window = rows
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sample = workloads.make(WORKLOAD, batch=512)
@@ -412,6 +429,7 @@ def main():
                     "d2h_bytes_per_step": 8 + C + 4 * N},
             "cpu_baseline": cpu,
             "hybrid": hybrid,
+            "window": window,
             "clocks": clocks,
             "wall_s": round(wall, 3),
         }

@@ -27,7 +27,7 @@ __all__ = [
     "EXPORTED_SYMBOLS", "EbcKernelTime", "EBC_ERR_SCRATCH_LIMIT", "ebc_decompress_noalloc",
     "EBC_MODE_DEDUP_HUFFMAN", "EBC_MODE_HUFFMAN", "EBC_MODE_DEDUP_RAW", "EBC_MODE_RAW", "EbcTableStats",
     "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup", "ebc_select_modes",
-    "ebc_select_table_modes", "ebc_table_homo_index",
+    "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
@@ -42,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "ebc_get_error_bounds", "ebc_compress_bound", "ebc_compress", "ebc_decompress", "ebc_compress_host",
     "ebc_decompress_host", "ebc_get_stats", "ebc_last_device_error", "ebc_set_profiling", "ebc_get_profile",
     "ebc_decompress_noalloc", "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup",
-    "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index",
+    "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window",
 )
 
 
@@ -108,6 +108,7 @@ def lib():
                 "ebc_get_profile": (I, [P, ctypes.POINTER(EbcKernelTime), I, ctypes.POINTER(I)]),
                 "ebc_decompress_noalloc": (I, [P, U64, P, I64, I, I, P]),
                 "ebc_set_table_modes": (I, [P, P, I]),
+                "ebc_set_window": (I, [P, I]),
                 "ebc_get_table_stats": (I, [P, ctypes.POINTER(EbcTableStats), I]),
                 "ebc_homo_index": (D, [U64, U64]),
                 "ebc_speedup": (D, [D, D, D, D]),
@@ -164,6 +165,10 @@ def ebc_compress(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_bytes, st
 
 def ebc_decompress(ctx, d_in, in_bytes, d_xhat, B, T, D, stream) -> int:
     return lib().ebc_decompress(ctx, d_in, int(in_bytes), d_xhat, int(B), int(T), int(D), stream)
+
+
+def ebc_set_window(ctx, window) -> int:
+    return lib().ebc_set_window(ctx, int(window))
 
 
 def ebc_set_table_modes(ctx, modes_ptr, T) -> int:
@@ -354,6 +359,12 @@ class Codec:
         rc = self.last_error()
         if rc:
             raise EbcError(rc, "device")
+
+    def set_window(self, window: int) -> None:
+        """Dedup window in rows for the following compress calls (0 = whole batch)."""
+        rc = ebc_set_window(self._ctx, window)
+        if rc:
+            raise EbcError(rc, "ebc_set_window")
 
     def set_table_modes(self, modes) -> None:
         """Per-table modes (0..3) for the following compress calls; None restores mode 0."""

@@ -63,6 +63,7 @@ struct ebc_ctx {
   float* eb_now = nullptr;
   int sched_T = 0;
   // per-table coding modes (0 = dedup + Huffman for every table when modes_T == 0)
+  int window = 0;                      // dedup window of the compress calls (0 = whole batch)
   uint8_t* d_modes = nullptr;          // device [kMaxT]
   uint8_t h_modes[kMaxT] = {};
   int modes_T = 0;
@@ -82,7 +83,7 @@ static bool shape_ok(int64_t B, int T, int D) {
   return (uint64_t)B * (uint64_t)T * (uint64_t)D <= (1ull << 31);
 }
 
-static Shape make_shape(int64_t B, int T, int D, int nsm = 0) {
+static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0) {
   Shape sh;
   sh.nsm = nsm;
   sh.B = B;
@@ -95,7 +96,8 @@ static Shape make_shape(int64_t B, int T, int D, int nsm = 0) {
   uint32_t S = 64;
   while ((int64_t)S < 2 * B) S <<= 1;
   sh.S = S;
-  sh.ref_bytes = B <= 65536 ? 2 : 4;
+  sh.window = window;
+  sh.ref_bytes = window > 0 ? 1 : (B <= 65536 ? 2 : 4);
   sh.symstride = ((uint64_t)B * (uint64_t)D + 15u) & ~(uint64_t)15u;
   sh.fold = sh.nseg <= kFoldMaxSeg ? 1 : 0;
   return sh;
@@ -175,6 +177,7 @@ static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total)
   w.litrow = c.take<uint16_t>(2 * nsegT * (size_t)sh.SB);
   w.mdesc = c.take<uint2>(8 * (size_t)sh.B * (size_t)sh.T);
   w.runmap = c.take<uint4>(16 * (size_t)dec_run_slots(sh));
+  w.srcrow = c.take<uint32_t>(4 * (size_t)sh.B * (size_t)sh.T);
   w.glob = g;
   *total = c.off;
   return w;
@@ -351,7 +354,7 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
     if (!eb_ok(ebs[t])) return EBC_ERR_INVALID_ARG;
     ep.eb[t] = ebs[t];
   }
-  const Shape sh = make_shape(B, T, D, c->nsm);
+  const Shape sh = make_shape(B, T, D, c->nsm, c->window);
   if (out_capacity < fixed_bytes(sh)) return EBC_ERR_CAPACITY;
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
@@ -397,6 +400,12 @@ int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xha
   c->last_stream = st;
   c->depoch = (c->depoch + 1) & 0xFFFFFFu;
   return cuda_err(launch_decompress((const uint8_t*)d_in, in_bytes, sh, w, d_xhat, c->depoch, st, c->prof));
+}
+
+int ebc_set_window(ebc_ctx* c, int window) {
+  if (!c || window < 0 || window > kMaxWindow) return EBC_ERR_INVALID_ARG;
+  c->window = window;
+  return EBC_OK;
 }
 
 int ebc_set_table_modes(ebc_ctx* c, const uint8_t* modes, int T) {
@@ -649,7 +658,7 @@ int ebc_select_table_modes(ebc_ctx* c, const float* d_x, int64_t B, int T, int D
   const int saved_T = c->modes_T;
   uint8_t saved[kMaxT];
   std::memcpy(saved, c->h_modes, (size_t)kMaxT);
-  const Shape sh = make_shape(B, T, D, c->nsm);
+  const Shape sh = make_shape(B, T, D, c->nsm, c->window);
   const double raw_bytes = 4.0 * (double)B * D;   // per table
   const double fixed = (double)kTableRecBytes + (double)kSegRecBytes * sh.nseg + 4.0 * sh.nw;
   double* cr = new (std::nothrow) double[(size_t)T * 4];

@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
   __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4];   // the segment's own codes
   __shared__ uint32_t s_ref[G::kSB];
   __shared__ uint32_t s_nout[G::kSB];
+  __shared__ uint32_t s_win[kMaxWindow + G::kSB];   // window mode: keys of rows row0 - window .. row0 + SB
   __shared__ uint32_t s_bm[G::kBmWords];
   __shared__ uint32_t s_cnt[3];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -352,6 +353,35 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
     const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D);
     for (int i = tid; i < nq; i += kNT) cp_async16(reinterpret_cast<uint4*>(s_sym) + i, src + i);
   }
+  if (sh.window > 0 && !nodedup) {
+    // window: the nearest earlier row within the window with the same key
+    // (the keys of the window and the segment, in shared memory)
+    const int64_t lo = row0 - sh.window > 0 ? row0 - sh.window : 0;
+    const int64_t hi = row0 + G::kSB < B ? row0 + G::kSB : B;
+    for (int64_t i = tid; i < hi - lo; i += kNT) s_win[i] = __ldcg(&w.vhash[(size_t)t * B + lo + i]);
+#pragma unroll
+    for (int k = 0; k < kRPT; ++k) {
+      const int r = k * kNT + tid;
+      if (r < G::kSB && row0 + r < B) s_nout[r] = __ldcg(&w.vnout[(size_t)t * B + row0 + r]);
+    }
+    __syncthreads();
+#pragma unroll 1
+    for (int k = 0; k < kRPT; ++k) {
+      const int r = k * kNT + tid;
+      const int64_t b = row0 + r;
+      if (r < G::kSB && b < B) {
+        const uint32_t h = s_win[b - lo];
+        const int64_t stop = b - sh.window > lo ? b - sh.window : lo;
+        uint32_t ref = (uint32_t)b;
+        for (int64_t c2 = b - 1; c2 >= stop; --c2)
+          if (s_win[c2 - lo] == h) {
+            ref = (uint32_t)c2;
+            break;
+          }
+        s_ref[r] = ref;
+      }
+    }
+  } else
   // one thread per row: first occurrence of the row's key
   {
     uint32_t h[kRPT], no[kRPT];
@@ -795,7 +825,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     st_u32(out + 0, kMagic); st_u32(out + 4, kFormatVersion); st_u64(out + 8, (unsigned long long)sh.B);
     st_u32(out + 16, (uint32_t)T); st_u32(out + 20, (uint32_t)sh.D); st_u32(out + 24, kRadius);
     st_u32(out + 28, kLmax); st_u32(out + 32, (uint32_t)sh.SB); st_u32(out + 36, (uint32_t)sh.KC);
-    st_u32(out + 40, (uint32_t)sh.ref_bytes); st_u32(out + 44, 0u);
+    st_u32(out + 40, (uint32_t)sh.ref_bytes); st_u32(out + 44, (uint32_t)sh.window);
     st_u64(out + 48, lits); st_u64(out + 56, matches); st_u64(out + 64, outl); st_u64(out + 72, chunks);
     st_u64(out + 88, off_seg); st_u64(out + 96, off_bitmap); st_u64(out + 104, off_chunks);
     st_u64(out + 112, off_refs); st_u64(out + 120, off_bits); st_u64(out + 136, 0ull);
@@ -1174,7 +1204,8 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
       if (r < G::kSB && row0 + r < B && ((s_bm[r >> 5] >> (r & 31)) & 1u)) {
         const uint32_t mrank = (s_pre[r >> 5] >> 16) + __popc(s_bm[r >> 5] & ((1u << (r & 31)) - 1u));
         const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (sb.z + mrank);
-        if (sh.ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)refw[k];
+        if (sh.window) out[o] = (uint8_t)((uint32_t)(row0 + r) - refw[k]);   // distance back, 1..window
+        else if (sh.ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)refw[k];
         else *reinterpret_cast<uint32_t*>(out + o) = refw[k];
       }
     }
@@ -1213,9 +1244,11 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
     prof_begin(prof, "k_quantize", st);
     launch_k(k_quantize<D>, qgrid, 256, smem, st, *xmap, sh, ep, w);
     prof_end(prof, st);
-    prof_begin(prof, "k_insert", st);
-    launch_k(k_insert, (unsigned)(((unsigned long long)sh.B * sh.T + 255) / 256), 256, 0, st, sh, w);
-    prof_end(prof, st);
+    if (sh.window == 0) {   // a window needs no hash table
+      prof_begin(prof, "k_insert", st);
+      launch_k(k_insert, (unsigned)(((unsigned long long)sh.B * sh.T + 255) / 256), 256, 0, st, sh, w);
+      prof_end(prof, st);
+    }
     prof_begin(prof, "k_resolve", st);
     launch_k(k_resolve<D>, grid, kResolveThreads, 0, st, x, sh, w);
     prof_end(prof, st);

@@ -48,6 +48,7 @@ __device__ __forceinline__ bool eb_usable(float eb) {
 struct Layout {
   unsigned long long n_lit, n_match, n_out, n_chunks, words;
   unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
+  unsigned int window, ref_bytes;   // dedup window (0 = whole batch) and bytes per reference
 };
 
 // Header checks (h: the 144 header bytes in shared memory).  Returns an EBC_*
@@ -60,8 +61,11 @@ __device__ int parse_header(const uint8_t* h, unsigned long long in_bytes, const
   if (ld64(h + 8) != (unsigned long long)sh.B || ld32(h + 16) != (uint32_t)T || ld32(h + 20) != (uint32_t)sh.D)
     return EBC_ERR_INVALID_ARG;
   if (ld32(h + 24) != (uint32_t)kRadius || ld32(h + 28) != (uint32_t)kLmax || ld32(h + 32) != (uint32_t)sh.SB ||
-      ld32(h + 36) != (uint32_t)sh.KC || ld32(h + 40) != (uint32_t)sh.ref_bytes || ld32(h + 44) != 0u)
+      ld32(h + 36) != (uint32_t)sh.KC || ld32(h + 44) > (uint32_t)kMaxWindow)
     return EBC_ERR_CORRUPT;
+  L->window = ld32(h + 44);
+  L->ref_bytes = L->window ? 1u : (uint32_t)sh.ref_bytes;   // windowed references are one-byte distances
+  if (ld32(h + 40) != L->ref_bytes) return EBC_ERR_CORRUPT;
   L->n_lit = ld64(h + 48);
   L->n_match = ld64(h + 56);
   L->n_out = ld64(h + 64);
@@ -74,7 +78,7 @@ __device__ int parse_header(const uint8_t* h, unsigned long long in_bytes, const
   L->off_bitmap = L->off_seg + (unsigned long long)T * sh.nseg * kSegRecBytes;
   L->off_chunks = L->off_bitmap + dpad16((unsigned long long)T * sh.nw * 4ull);
   L->off_refs = L->off_chunks + dpad16(L->n_chunks * 2ull);
-  L->off_bits = L->off_refs + dpad16(L->n_match * (unsigned long long)sh.ref_bytes);
+  L->off_bits = L->off_refs + dpad16(L->n_match * (unsigned long long)L->ref_bytes);
   L->total = L->off_bits + L->words * 4ull;
   if (ld64(h + 88) != L->off_seg || ld64(h + 96) != L->off_bitmap || ld64(h + 104) != L->off_chunks ||
       ld64(h + 112) != L->off_refs || ld64(h + 120) != L->off_bits || ld64(h + 128) != L->total ||
@@ -128,6 +132,7 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
         g->words = s_L.words; g->off_seg = s_L.off_seg; g->off_bitmap = s_L.off_bitmap;
         g->off_chunks = s_L.off_chunks; g->off_refs = s_L.off_refs; g->off_bits = s_L.off_bits;
         g->total = s_L.total;
+        g->window = s_L.window;
       }
     }
   }
@@ -206,6 +211,66 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
       if (len <= (uint32_t)kLutBits) {
         const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
         for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(tid | (len << 8));
+      }
+    }
+    if (L.window && sh.nseg > 0) {
+      // window references: every row's source (itself for a literal, b - distance for a match),
+      // from the table's bitmap and one-byte distances, then the chains resolved to their
+      // literal roots (pointer jumping, CTA barriers between rounds)
+      const int64_t B = sh.B;
+      const uint32_t* bmt = reinterpret_cast<const uint32_t*>(in + L.off_bitmap) + (size_t)t * sh.nw;
+      const uint8_t* dist = in + L.off_refs;
+      const uint32_t* srec = reinterpret_cast<const uint32_t*>(in + L.off_seg);
+      const unsigned long long mbase = srec[4ull * ((unsigned long long)t * sh.nseg) + 2];
+      uint32_t* src = w.srcrow + (size_t)t * B;
+      unsigned long long carry = 0;
+      for (int64_t base = 0; base < sh.nw; base += 256) {
+        const int64_t wi = base + tid;
+        const uint32_t bm = wi < sh.nw ? __ldcg(&bmt[wi]) : 0u;
+        // matches before this word: a CTA-wide exclusive scan of the words' counts
+        uint32_t wt;
+        const uint32_t in_warp = warp_excl((uint32_t)__popc(bm), &wt);
+        if (lane == 0) s_count[warp] = wt;
+        __syncthreads();
+        uint32_t before = 0, all = 0;
+        for (int k = 0; k < 8; ++k) {
+          if (k < warp) before += s_count[k];
+          all += s_count[k];
+        }
+        __syncthreads();
+        const unsigned long long rank0 = mbase + carry + before + in_warp;
+        if (wi < sh.nw) {
+          for (int j = 0; j < 32; ++j) {
+            const int64_t b = wi * 32 + j;
+            if (b >= B) break;
+            uint32_t from = (uint32_t)b;
+            if ((bm >> j) & 1u) {
+              const unsigned long long k = rank0 + __popc(bm & ((1u << j) - 1u));
+              const uint32_t d = k < L.n_match ? dist[k] : 0u;
+              if (d == 0u || d > L.window || (int64_t)d > b) s_bad = 1;
+              else from = (uint32_t)(b - d);
+            }
+            src[b] = from;
+          }
+        }
+        carry += all;
+      }
+      __syncthreads();
+      if (s_bad) {
+        if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
+        return;
+      }
+      int rounds = 1;
+      while ((1ll << rounds) < B) ++rounds;
+      for (int r = 0; r <= rounds; ++r) {
+        for (int64_t b = tid; b < B; b += 256) {
+          const uint32_t s = src[b];
+          if (s != (uint32_t)b) {
+            const uint32_t s2 = src[s];   // one step further (a literal points at itself)
+            if (s2 != s) src[b] = s2;
+          }
+        }
+        __syncthreads();
       }
     }
     return;
@@ -302,11 +367,21 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
       uint32_t k = mbase + warp_excl(__popc(mw), &tot);
       for (uint32_t m = mw; m; m &= m - 1) {
         const int64_t b = row0 + wi * 32 + __ffs(m) - 1;
-        const uint32_t ref = sh.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[k]
-                                               : reinterpret_cast<const uint32_t*>(refs)[k];
-        if ((int64_t)ref >= b || ((bmt[ref >> 5] >> (ref & 31)) & 1u)) {
-          ok = false;
-          break;
+        uint32_t ref;
+        if (L.window) {   // a distance back, within the window; the row there may itself be a match
+          const uint32_t dist = refs[k];
+          if (dist == 0u || dist > L.window || (int64_t)dist > b) {
+            ok = false;
+            break;
+          }
+          ref = (uint32_t)(b - dist);
+        } else {          // whole batch: the first occurrence, always a literal
+          ref = sh.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[k]
+                                  : reinterpret_cast<const uint32_t*>(refs)[k];
+          if ((int64_t)ref >= b || ((bmt[ref >> 5] >> (ref & 31)) & 1u)) {
+            ok = false;
+            break;
+          }
         }
         w.mdesc[k] = make_uint2((uint32_t)(b * T + t), (uint32_t)((int64_t)ref * T + t));
         ++k;
@@ -408,12 +483,13 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
   __shared__ int s_abort;
   Glob* g = w.glob;
   const int tid = threadIdx.x;
+  const unsigned int slot = blockIdx.x;   // run slot of this CTA
   // the run, and whether the decode was aborted (then the run map may be
   // stale): one decision for the whole CTA, taken before the run is used
   if (tid == 0) s_abort = dec_aborted(g, epoch);
   const unsigned long long nslots = __ldcg(&g->n_chunks) / kDecRun + (unsigned long long)sh.T;
   uint4 run = make_uint4(~0u, 0u, 0u, 0u);
-  if (blockIdx.x < nslots) run = __ldcg(&w.runmap[blockIdx.x]);
+  if (slot < nslots) run = __ldcg(&w.runmap[slot]);
   __syncthreads();
   if (s_abort || run.x == ~0u) return;
   if (run.x >= (uint32_t)sh.T || run.y >= run.z || run.z > dec_max_chunks(sh)) {
@@ -487,9 +563,10 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
 }
 
 // ---------------------------------------------------------------------------
-// k_dec_matches: each matched row copies its reference row, which is always an
-// earlier literal of the same table (grid-stride over (matched row, 16-byte
-// column) pairs, four copies in flight per thread).
+// k_dec_matches: each matched row copies its reference row: the literal the
+// reference names (whole batch), or the literal root of its chain (window;
+// resolved by k_dec_prep's table CTAs).  Grid-stride over (matched row,
+// 16-byte column) pairs, four copies in flight per thread.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __restrict__ xhat, uint32_t epoch) {
@@ -499,7 +576,20 @@ __global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __
   constexpr int kQ = D / 4;
   const unsigned long long n4 = __ldcg(&g->n_match) * (unsigned long long)kQ;
   const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-  for (unsigned long long i0 = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; i0 < n4; i0 += 4 * stride) {
+  const unsigned long long i_start = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (__ldcg(&g->window) != 0u) {   // source = the chain's literal root
+    const uint32_t T = (uint32_t)sh.T;
+    for (unsigned long long i = i_start; i < n4; i += stride) {
+      const uint2 m = __ldcg(&w.mdesc[i / kQ]);
+      const unsigned long long q = i % kQ;
+      const uint32_t b = m.x / T, t = m.x - b * T;
+      const uint32_t from = __ldcg(&w.srcrow[(size_t)t * sh.B + b]) * T + t;
+      __stcs(reinterpret_cast<float4*>(xhat + (size_t)m.x * D + 4 * q),
+             *reinterpret_cast<const float4*>(xhat + (size_t)from * D + 4 * q));
+    }
+    return;
+  }
+  for (unsigned long long i0 = i_start; i0 < n4; i0 += 4 * stride) {
     float4 v[4];
     unsigned long long dst[4];
 #pragma unroll

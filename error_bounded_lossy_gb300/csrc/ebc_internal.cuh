@@ -36,14 +36,16 @@ struct Shape {
   int nseg;       // segments per table
   int nw;         // bitmap words per table: ceil(B / 32)
   uint32_t S;     // dedup slots per table (power of two >= 2B, >= 64)
-  int ref_bytes;  // 2 if B <= 65536 else 4
+  int ref_bytes;  // 1 with a window (distances), else 2 if B <= 65536 else 4
   int nsm;        // SMs of the device (grid sizing)
   uint64_t symstride;  // bytes per table in the code scratch: B*D rounded up to 16
+  int window;     // dedup window in rows (0 = whole batch, first occurrence; else nearest earlier, 1..255)
   int fold;       // 1: segment offsets are built per table inside k_codebook (nseg <= kFoldMaxSeg);
                   // 0: by k_layout, per 8-segment tile
 };
 
 constexpr int kFoldMaxSeg = 256;
+constexpr int kMaxWindow = 255;
 
 // Per-table coding modes (bit flags; 0 = vector dedup + Huffman codes).
 constexpr uint32_t kModeNoDedup = 1;   // every vector of the table is a literal
@@ -70,7 +72,8 @@ struct Glob {
   unsigned int cstat;     // (epoch << 8) | status of the last compress
   unsigned int dstat;     // (epoch << 8) | status of the last decompress
   unsigned int sticky;    // first device error since the last query (0 = none)
-  unsigned int pad[4];
+  unsigned int window;    // the window of the container being decoded (0 = whole batch)
+  unsigned int pad[3];
   unsigned long long n_lit, n_match, n_out, n_chunks, words;
   unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
 };
@@ -112,6 +115,7 @@ struct Work {
   uint4* cdesc;                // [T*nseg*chunks] {start bit lo, start bit hi, segment, first literal | rows << 16}
   uint16_t* litrow;            // [T*nseg][SB] literal rows of each segment, in row order
   uint2* mdesc;                // [n_match] {destination row, source row} as b * T + t
+  uint32_t* srcrow;            // [T][B] windowed containers: each row's source row (itself for a literal)
   uint4* runmap;               // [dec_run_slots] {table, first chunk, end chunk, 0} of each run of chunks;
                                //   table ~0u = no run
   Glob* glob;

@@ -29,8 +29,9 @@
  * Container (little-endian, every section 16-byte aligned):
  *   header 144 B | T table records (eb, counts, 256 code lengths; 272 B each)
  *   | segment records (16 B each) | match bitmap (T x ceil(B/32) u32)
- *   | chunk bit lengths (u16) | match references (u16 if B <= 65536, else u32)
- *   | outlier raw bits (u32) | bitstream (u32 words)
+ *   | chunk bit lengths (u16) | match references (u16 row if B <= 65536, else
+ *   u32; one-byte distances when the header's window field, at byte 44, is not
+ *   0) | bitstream (u32 words; an outlier's code is followed by its 32 raw bits)
  * A segment is max(32, 8192/D) consecutive batch rows of one table; its bits
  * start on a 128-bit boundary.  A chunk is max(1, 128/D) literal vectors of one
  * segment, decoded by one GPU thread.
@@ -161,6 +162,16 @@ int ebc_compress_host(ebc_ctx* ctx, const float* h_x, int64_t B, int T, int D, c
                       void* h_out, uint64_t out_capacity, uint64_t* out_bytes, void* stream);
 int ebc_decompress_host(ebc_ctx* ctx, const void* h_in, uint64_t in_bytes, float* h_xhat,
                         int64_t B, int T, int D, void* stream);
+
+/* Sliding-window vector LZ (the pages' "extended window size" of §III-E,
+ * evaluated in §IV-D Table VI).  With window W in 1..255, the following
+ * compress calls of the context take as a vector's reference the nearest
+ * earlier vector of its table within W rows that has the same key (a match
+ * when its codes and raw outlier bits are equal, else a literal), stored as a
+ * one-byte distance; references may then chain, and ebc_decompress resolves
+ * the chains.  W = 0 (the default) is the whole-batch first occurrence.
+ * Returns EBC_ERR_INVALID_ARG for W outside 0..255. */
+int ebc_set_window(ebc_ctx* ctx, int window);
 
 /* ---- Per-table hybrid coding (the pages' "Selection Between Two Encoders",
  * §III-D, Eq. (2)) and the Homogenization Index (§III-C, Eq. (1)) ----
