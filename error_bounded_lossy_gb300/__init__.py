@@ -27,7 +27,7 @@ __all__ = [
     "EXPORTED_SYMBOLS", "EbcKernelTime", "EBC_ERR_SCRATCH_LIMIT", "ebc_decompress_noalloc",
     "EBC_MODE_DEDUP_HUFFMAN", "EBC_MODE_HUFFMAN", "EBC_MODE_DEDUP_RAW", "EBC_MODE_RAW", "EbcTableStats",
     "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup", "ebc_select_modes",
-    "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window",
+    "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
@@ -42,7 +42,7 @@ EXPORTED_SYMBOLS = (
     "ebc_get_error_bounds", "ebc_compress_bound", "ebc_compress", "ebc_decompress", "ebc_compress_host",
     "ebc_decompress_host", "ebc_get_stats", "ebc_last_device_error", "ebc_set_profiling", "ebc_get_profile",
     "ebc_decompress_noalloc", "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup",
-    "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window",
+    "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
 )
 
 
@@ -109,6 +109,7 @@ def lib():
                 "ebc_decompress_noalloc": (I, [P, U64, P, I64, I, I, P]),
                 "ebc_set_table_modes": (I, [P, P, I]),
                 "ebc_set_window": (I, [P, I]),
+                "ebc_compress_bf16": (I, [P, P, I64, I, I, P, P, U64, P, P]),
                 "ebc_get_table_stats": (I, [P, ctypes.POINTER(EbcTableStats), I]),
                 "ebc_homo_index": (D, [U64, U64]),
                 "ebc_speedup": (D, [D, D, D, D]),
@@ -165,6 +166,11 @@ def ebc_compress(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_bytes, st
 
 def ebc_decompress(ctx, d_in, in_bytes, d_xhat, B, T, D, stream) -> int:
     return lib().ebc_decompress(ctx, d_in, int(in_bytes), d_xhat, int(B), int(T), int(D), stream)
+
+
+def ebc_compress_bf16(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_bytes, stream) -> int:
+    return lib().ebc_compress_bf16(ctx, d_x, int(B), int(T), int(D), eb_ptr, d_out, int(out_capacity), d_out_bytes,
+                                   stream)
 
 
 def ebc_set_window(ctx, window) -> int:
@@ -311,18 +317,20 @@ class Codec:
 
     def compress_into(self, x, eb, out, nbytes, stream=None) -> None:
         """Asynchronous compress of CUDA tensor x [B,T,D] into preallocated out / nbytes."""
+        import torch
         B, T, D = x.shape
         ebh = None if eb is None else _f32_host(eb, T)
-        rc = ebc_compress(self._ctx, _ptr(x), B, T, D,
-                          ebh.ctypes.data_as(ctypes.c_void_p) if ebh is not None else None,
-                          _ptr(out), out.numel(), _ptr(nbytes), _stream_ptr(stream))
+        fn, name = (ebc_compress_bf16, "ebc_compress_bf16") if x.dtype == torch.bfloat16 else (ebc_compress,
+                                                                                               "ebc_compress")
+        rc = fn(self._ctx, _ptr(x), B, T, D, ebh.ctypes.data_as(ctypes.c_void_p) if ebh is not None else None,
+                _ptr(out), out.numel(), _ptr(nbytes), _stream_ptr(stream))
         if rc:
-            raise EbcError(rc, "ebc_compress")
+            raise EbcError(rc, name)
 
     def compress(self, x, eb=None, stream=None, out=None):
         import torch
-        if not (x.is_cuda and x.dtype == torch.float32 and x.is_contiguous() and x.dim() == 3):
-            raise ValueError("x must be a contiguous float32 CUDA tensor [B, T, D]")
+        if not (x.is_cuda and x.dtype in (torch.float32, torch.bfloat16) and x.is_contiguous() and x.dim() == 3):
+            raise ValueError("x must be a contiguous float32 or bfloat16 CUDA tensor [B, T, D]")
         B, T, D = x.shape
         cap = self.compress_bound(B, T, D)
         if out is None:

@@ -335,10 +335,11 @@ uint64_t ebc_compress_bound(int64_t B, int T, int D) {
   return fixed_bytes(sh) + pad16h(nvec * 2u) + pad16h(nvec * sh.ref_bytes) + words * 4u;
 }
 
-int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, void* d_out,
-                 uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
+// fp32 or bf16 input (bf16: its raw 16 bits; compressed as its exact fp32 value)
+static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T, int D, const float* eb, void* d_out,
+                        uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
   if (!c || !shape_ok(B, T, D) || !d_out || !d_out_bytes || !aligned16(d_out) ||
-      ((uintptr_t)d_out_bytes & 7u) != 0)
+      ((uintptr_t)d_out_bytes & 7u) != 0 || (bf16 && D < 8))
     return EBC_ERR_INVALID_ARG;
   const uint64_t N = (uint64_t)B * T * D;
   if (N > 0 && (!d_x || !aligned16(d_x))) return EBC_ERR_INVALID_ARG;
@@ -378,10 +379,20 @@ int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const fl
     c->cleanT = T;
     c->cleanD = D;
   }
-  const cudaError_t e = launch_compress(d_x, sh, ep, w, (uint8_t*)d_out, out_capacity,
+  const cudaError_t e = launch_compress(d_x, bf16, sh, ep, w, (uint8_t*)d_out, out_capacity,
                                         (unsigned long long*)d_out_bytes, c->cepoch, st, c->prof);
   if (e != cudaSuccess) c->clean_buf = nullptr;   // the dedup table may be left dirty
   return cuda_err(e);
+}
+
+int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, void* d_out,
+                 uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
+  return compress_any(c, d_x, false, B, T, D, eb, d_out, out_capacity, d_out_bytes, stream);
+}
+
+int ebc_compress_bf16(ebc_ctx* c, const uint16_t* d_x, int64_t B, int T, int D, const float* eb, void* d_out,
+                      uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
+  return compress_any(c, d_x, true, B, T, D, eb, d_out, out_capacity, d_out_bytes, stream);
 }
 
 int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,

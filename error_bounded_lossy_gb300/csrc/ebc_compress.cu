@@ -51,6 +51,17 @@ __device__ __forceinline__ uint32_t quantize_four(float4 v, float eb, float ebx2
   return __byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u) ^ 0x80808080u;
 }
 
+// Input element types: fp32, or bf16 carried as its 16 raw bits (its fp32
+// value is exact: the bf16 bits followed by 16 zero bits).
+__device__ __forceinline__ uint32_t raw32(float v) { return __float_as_uint(v); }
+__device__ __forceinline__ uint32_t raw32(uint16_t v) { return (uint32_t)v << 16; }
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const uint16_t* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  return make_float4(__uint_as_float(u.x << 16), __uint_as_float(u.x & 0xffff0000u), __uint_as_float(u.y << 16),
+                     __uint_as_float(u.y & 0xffff0000u));
+}
+
 __device__ __forceinline__ unsigned long long l2_evict_last() {
   unsigned long long pol;
   asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
@@ -148,23 +159,23 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, u
 // Box geometry of one segment's input tile x[row0 .. row0+SB)[t][0 .. D):
 // boxes of at most 256 rows x 256 elements; box (rb, db) lands at
 // ((rb * kNBoxD + db) * kBoxR) * kBoxD floats in the stage.
-template <int D>
+template <int D, typename In = float>
 struct QGeo {
   static constexpr int kBoxD = D < 256 ? D : 256;
   static constexpr int kBoxR = Geo<D>::kSB < 256 ? Geo<D>::kSB : 256;
   static constexpr int kNBoxD = D / kBoxD;
   static constexpr int kNBoxR = Geo<D>::kSB / kBoxR;
   static constexpr int kStageFloats = Geo<D>::kSegSyms;
-  static constexpr uint32_t kStageBytes = (uint32_t)kStageFloats * 4u;
+  static constexpr uint32_t kStageBytes = (uint32_t)kStageFloats * (uint32_t)sizeof(In);
   __device__ static __forceinline__ int offset(int r, int d) {
     return (((r / kBoxR) * kNBoxD + d / kBoxD) * kBoxR + r % kBoxR) * kBoxD + d % kBoxD;
   }
 };
 
-template <int D>
-__device__ __forceinline__ void issue_segment_tile(float* stage, const CUtensorMap* map, uint64_t* bar, const Shape& sh,
+template <int D, typename In>
+__device__ __forceinline__ void issue_segment_tile(In* stage, const CUtensorMap* map, uint64_t* bar, const Shape& sh,
                                                    int seg) {
-  using Q = QGeo<D>;
+  using Q = QGeo<D, In>;
   const int t = seg / sh.nseg;
   const int s = seg - t * sh.nseg;
   unsigned long long first;
@@ -187,13 +198,14 @@ __device__ __forceinline__ void issue_segment_tile(float* stage, const CUtensorM
 // wrapping sum over its 4-code words w_k of lowbias32(w_k + k * 0x9E3779B9)
 // plus lowbias32(raw ^ (d + 1) * 0x85EBCA6B) for each outlier at position d.
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, typename In>
 __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtensorMap tmap, Shape sh, EbParams ep,
                                                    Work w) {
   pdl_enter();
   using G = Geo<D>;
-  using Q = QGeo<D>;
-  extern __shared__ __align__(128) float s_x[];   // 2 stages of kStageFloats
+  using Q = QGeo<D, In>;
+  extern __shared__ __align__(128) unsigned char s_raw[];   // 2 stages of kStageFloats elements
+  In* s_x = reinterpret_cast<In*>(s_raw);
   __shared__ __align__(8) uint64_t s_bar[2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nsegT = sh.T * sh.nseg;
@@ -203,16 +215,16 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     mbar_init(&s_bar[0], 1);
     mbar_init(&s_bar[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    if ((int)blockIdx.x < nsegT) issue_segment_tile<D>(s_x, &tmap, &s_bar[0], sh, blockIdx.x);
+    if ((int)blockIdx.x < nsegT) issue_segment_tile<D, In>(s_x, &tmap, &s_bar[0], sh, blockIdx.x);
     if ((int)(blockIdx.x + gridDim.x) < nsegT)
-      issue_segment_tile<D>(s_x + Q::kStageFloats, &tmap, &s_bar[1], sh, blockIdx.x + gridDim.x);
+      issue_segment_tile<D, In>(s_x + Q::kStageFloats, &tmap, &s_bar[1], sh, blockIdx.x + gridDim.x);
   }
   __syncthreads();
   uint32_t parity = 0;   // bit i: phase of stage i
   int i = 0;
   for (int seg = blockIdx.x; seg < nsegT; seg += gridDim.x, ++i) {
     const int stg = i & 1;
-    const float* xs = s_x + stg * Q::kStageFloats;
+    const In* xs = s_x + stg * Q::kStageFloats;
     const int t = seg / sh.nseg;
     const int s = seg - t * sh.nseg;
     const int64_t row0 = (int64_t)s * G::kSB;
@@ -240,7 +252,7 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
       const int64_t b = row0 + r;
       const int d = e % D;
       const bool valid = b < B;
-      const float4 v = *reinterpret_cast<const float4*>(xs + Q::offset(r, d));
+      const float4 v = load4(xs + Q::offset(r, d));
       bool ok[4];
       const uint32_t word = quantize_four(v, eb, ebx2, inv, ok);
       if (valid)
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     }
     __syncthreads();   // the stage is consumed: refill it with the segment two steps ahead
     if (tid == 0 && seg + 2 * (int)gridDim.x < nsegT)
-      issue_segment_tile<D>(s_x + stg * Q::kStageFloats, &tmap, &s_bar[stg], sh, seg + 2 * gridDim.x);
+      issue_segment_tile<D, In>(s_x + stg * Q::kStageFloats, &tmap, &s_bar[stg], sh, seg + 2 * gridDim.x);
   }
 }
 
@@ -317,8 +329,8 @@ __device__ __forceinline__ bool has_zero_byte(uint32_t v) {
 // ---------------------------------------------------------------------------
 constexpr int kResolveThreads = 64;   // two warps per segment: many segments in flight per SM
 
-template <int D>
-__global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __restrict__ x, Shape sh, Work w) {
+template <int D, typename In>
+__global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restrict__ x, Shape sh, Work w) {
   pdl_enter();
   using G = Geo<D>;
   constexpr int kNT = kResolveThreads, kNW = kNT / 32;
@@ -445,11 +457,11 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const float* __rest
         bool e = wr[it][j] == wb[j];
         if (cand && e && has_zero_byte(wb[j])) {
           const int d = (lane % G::kLPR) * 4 + j * 128;
-          const float* xb = x + ((size_t)b * T + t) * D + d;
-          const float* xr = x + ((size_t)ref * T + t) * D + d;
+          const In* xb = x + ((size_t)b * T + t) * D + d;
+          const In* xr = x + ((size_t)ref * T + t) * D + d;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (((wb[j] >> (8 * q)) & 0xffu) == 0u && __float_as_uint(xb[q]) != __float_as_uint(xr[q])) e = false;
+            if (((wb[j] >> (8 * q)) & 0xffu) == 0u && raw32(xb[q]) != raw32(xr[q])) e = false;
         }
         eq = eq && e;
       }
@@ -985,8 +997,8 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
 // stored with 16-byte writes; a segment larger than the copy (24 bits per
 // code on average) is ORed straight into the zeroed output.
 // ---------------------------------------------------------------------------
-template <int D>
-__global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Shape sh, Work w,
+template <int D, typename In>
+__global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape sh, Work w,
                                                uint8_t* __restrict__ out, unsigned long long cap, uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
@@ -1176,7 +1188,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
             put_bits(bitbuf, qpos, e >> 8, e & 0xffu);
             qpos += e & 0xffu;
             if (c == 0u) {
-              put_bits(bitbuf, qpos, __float_as_uint(x[((size_t)b * T + t) * D + d + q]), 32u);
+              put_bits(bitbuf, qpos, raw32(x[((size_t)b * T + t) * D + d + q]), 32u);
               qpos += 32u;
             }
           }
@@ -1224,25 +1236,25 @@ __global__ void __launch_bounds__(256, 4) k_emit(const float* __restrict__ x, Sh
 // ---------------------------------------------------------------------------
 // launcher
 // ---------------------------------------------------------------------------
-template <int D>
-static void launch_compress_d(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
+template <int D, typename In>
+static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
                               unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
                               cudaStream_t st, Prof* prof, const CUtensorMap* xmap) {
   const unsigned grid = (unsigned)(sh.T * sh.nseg);
   if (grid) {
     // persistent quantize: as many CTAs as fit at once (two input stages each), at most one per segment
     static int per_sm = -1;
-    const int smem = 2 * (int)QGeo<D>::kStageBytes;
+    const int smem = 2 * (int)QGeo<D, In>::kStageBytes;
     if (per_sm < 0) {
-      cudaFuncSetAttribute(k_quantize<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize<D>, 256, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_quantize<D, In>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize<D, In>, 256, smem) != cudaSuccess ||
           per_sm < 1)
         per_sm = 1;
     }
     unsigned qgrid = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm);
     if (qgrid > grid) qgrid = grid;
     prof_begin(prof, "k_quantize", st);
-    launch_k(k_quantize<D>, qgrid, 256, smem, st, *xmap, sh, ep, w);
+    launch_k(k_quantize<D, In>, qgrid, 256, smem, st, *xmap, sh, ep, w);
     prof_end(prof, st);
     if (sh.window == 0) {   // a window needs no hash table
       prof_begin(prof, "k_insert", st);
@@ -1250,7 +1262,7 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
       prof_end(prof, st);
     }
     prof_begin(prof, "k_resolve", st);
-    launch_k(k_resolve<D>, grid, kResolveThreads, 0, st, x, sh, w);
+    launch_k(k_resolve<D, In>, grid, kResolveThreads, 0, st, x, sh, w);
     prof_end(prof, st);
   }
   prof_begin(prof, "k_codebook", st);
@@ -1263,15 +1275,15 @@ static void launch_compress_d(const float* x, const Shape& sh, const EbParams& e
       prof_end(prof, st);
     }
     prof_begin(prof, "k_emit", st);
-    launch_k(k_emit<D>, grid, 256, Geo<D>::kSegSyms * 3, st, x, sh, w, out, cap, epoch);
+    launch_k(k_emit<D, In>, grid, 256, Geo<D>::kSegSyms * 3, st, x, sh, w, out, cap, epoch);
     prof_end(prof, st);
   }
 }
 
 // Tensor map of x viewed as [B][T][D] (dims innermost first: D, T, B), boxes of
 // min(D, 256) elements x 1 table x min(SB, 256) rows; rows past B read as zero.
-template <int D>
-static cudaError_t make_x_map(CUtensorMap* map, const float* x, const Shape& sh) {
+template <int D, typename In>
+static cudaError_t make_x_map(CUtensorMap* map, const In* x, const Shape& sh) {
   static PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   if (!encode) {
     cudaDriverEntryPointQueryResult q;
@@ -1283,52 +1295,65 @@ static cudaError_t make_x_map(CUtensorMap* map, const float* x, const Shape& sh)
     encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
   }
   const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)sh.T, (cuuint64_t)sh.B};
-  const cuuint64_t strides[2] = {(cuuint64_t)D * 4u, (cuuint64_t)sh.T * D * 4u};
-  const cuuint32_t box[3] = {(cuuint32_t)QGeo<D>::kBoxD, 1u, (cuuint32_t)QGeo<D>::kBoxR};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * sizeof(In), (cuuint64_t)sh.T * D * sizeof(In)};
+  const cuuint32_t box[3] = {(cuuint32_t)QGeo<D, In>::kBoxD, 1u, (cuuint32_t)QGeo<D, In>::kBoxR};
   const cuuint32_t estr[3] = {1u, 1u, 1u};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<float*>(x), dims, strides, box, estr,
+  const CUtensorMapDataType dt = sizeof(In) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUresult r = encode(map, dt, 3, const_cast<In*>(x), dims, strides, box, estr,
                             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
                             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-cudaError_t launch_compress(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
-                            unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                            cudaStream_t st, Prof* prof) {
+template <typename In>
+static cudaError_t launch_compress_t(const In* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
+                                    unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
+                                    cudaStream_t st, Prof* prof) {
   CUtensorMap xmap;
   if (sh.T > 0 && sh.nseg > 0) {
     cudaError_t e = cudaSuccess;
     switch (sh.D) {
-      case 4: e = make_x_map<4>(&xmap, x, sh); break;
-      case 8: e = make_x_map<8>(&xmap, x, sh); break;
-      case 16: e = make_x_map<16>(&xmap, x, sh); break;
-      case 32: e = make_x_map<32>(&xmap, x, sh); break;
-      case 64: e = make_x_map<64>(&xmap, x, sh); break;
-      case 128: e = make_x_map<128>(&xmap, x, sh); break;
-      case 256: e = make_x_map<256>(&xmap, x, sh); break;
-      case 512: e = make_x_map<512>(&xmap, x, sh); break;
+      case 4: e = make_x_map<4, In>(&xmap, x, sh); break;
+      case 8: e = make_x_map<8, In>(&xmap, x, sh); break;
+      case 16: e = make_x_map<16, In>(&xmap, x, sh); break;
+      case 32: e = make_x_map<32, In>(&xmap, x, sh); break;
+      case 64: e = make_x_map<64, In>(&xmap, x, sh); break;
+      case 128: e = make_x_map<128, In>(&xmap, x, sh); break;
+      case 256: e = make_x_map<256, In>(&xmap, x, sh); break;
+      case 512: e = make_x_map<512, In>(&xmap, x, sh); break;
       default: return cudaErrorInvalidValue;
     }
     if (e != cudaSuccess) return e;
   }
   switch (sh.D) {
-    case 4: launch_compress_d<4>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 8: launch_compress_d<8>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 16: launch_compress_d<16>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 32: launch_compress_d<32>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 64: launch_compress_d<64>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 128: launch_compress_d<128>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 256: launch_compress_d<256>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 512: launch_compress_d<512>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 4: launch_compress_d<4, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 8: launch_compress_d<8, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 16: launch_compress_d<16, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 32: launch_compress_d<32, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 64: launch_compress_d<64, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 128: launch_compress_d<128, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 256: launch_compress_d<256, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 512: launch_compress_d<512, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
 
+cudaError_t launch_compress(const void* x, bool bf16, const Shape& sh, const EbParams& ep, const Work& w,
+                            uint8_t* out, unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
+                            cudaStream_t st, Prof* prof) {
+  return bf16 ? launch_compress_t(static_cast<const uint16_t*>(x), sh, ep, w, out, cap, out_bytes, epoch, st, prof)
+              : launch_compress_t(static_cast<const float*>(x), sh, ep, w, out, cap, out_bytes, epoch, st, prof);
+}
+
 template <int D>
 static cudaError_t set_emit_smem() {
   // shared copy of a segment's bitstream: 24 bits per code on average (larger ones go to global memory)
-  return cudaFuncSetAttribute(k_emit<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3);
+  const cudaError_t a = cudaFuncSetAttribute(k_emit<D, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Geo<D>::kSegSyms * 3);
+  const cudaError_t b = cudaFuncSetAttribute(k_emit<D, uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             Geo<D>::kSegSyms * 3);
+  return a != cudaSuccess ? a : b;
 }
 
 cudaError_t set_kernel_attributes() {

@@ -195,8 +195,8 @@ void prof_begin(Prof* p, const char* name, cudaStream_t st);
 void prof_end(Prof* p, cudaStream_t st);
 
 // ---- launchers (one per direction; D is dispatched to the templated kernels) ----
-cudaError_t launch_compress(const float* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
-                            unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
+cudaError_t launch_compress(const void* x, bool bf16, const Shape& sh, const EbParams& ep, const Work& w,
+                            uint8_t* out, unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
                             cudaStream_t st, Prof* prof);
 cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const Shape& sh, const Work& w,
                               float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof);

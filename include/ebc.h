@@ -144,6 +144,15 @@ uint64_t ebc_compress_bound(int64_t B, int T, int D);
 int ebc_compress(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D, const float* eb,
                  void* d_out, uint64_t out_capacity, uint64_t* d_out_bytes, void* stream);
 
+/* ebc_compress for bf16 input (the pages' "mixed precision" embeddings,
+ * §IV): d_x[B][T][D] holds bf16 values as their raw 16 bits.  Each value is
+ * coded as its exact fp32 value (an outlier keeps those 32 bits), so the
+ * container equals ebc_compress of the fp32-converted tensor, while the input
+ * read is half as large.  Requires D >= 8 (EBC_ERR_INVALID_ARG otherwise);
+ * ebc_decompress returns fp32. */
+int ebc_compress_bf16(ebc_ctx* ctx, const uint16_t* d_x, int64_t B, int T, int D, const float* eb,
+                      void* d_out, uint64_t out_capacity, uint64_t* d_out_bytes, void* stream);
+
 /* Decompress a container (device, in_bytes bytes) made for the same B, T, D
  * into d_xhat[B][T][D] (device, fp32).  Asynchronous.  A container that fails
  * validation makes the kernels stop without writing out of bounds and records

@@ -22,7 +22,7 @@ def lib():
 def declared_functions():
     text = open(os.path.join(ROOT, "include", "ebc.h")).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"\b(ebc_[a-z_]+)\s*\(", text)))
+    return sorted(set(re.findall(r"\b(ebc_[a-z0-9_]+)\s*\(", text)))
 
 
 def test_header_declares_the_boundary():
@@ -36,7 +36,7 @@ def test_library_exports_every_declared_symbol(lib):
     for name in declared_functions():
         assert hasattr(lib, name), name
     out = os.popen(f"nm -D --defined-only {ebc.library_path()}").read()
-    exported = set(re.findall(r"\bT (ebc_[a-z_]+)\b", out))
+    exported = set(re.findall(r"\bT (ebc_[a-z0-9_]+)\b", out))
     assert set(declared_functions()) <= exported
 
 
