@@ -166,7 +166,6 @@ def algorithmic_bytes(kernel: str, N: int, D: int, st: dict) -> int:
     C = st["out_bytes"]
     return {
         "k_quantize": 4 * N,                               # input read once
-        "k_insert": 0,
         "k_resolve": 0,
         "k_codebook": 0,
         "k_layout": 0,

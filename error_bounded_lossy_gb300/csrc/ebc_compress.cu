@@ -5,8 +5,8 @@
 // §III-D (quantization encoder, vector-based LZ, Huffman) and §III-E (one
 // output buffer, chunk offsets found on the device).  Six launches on the
 // caller's stream:
-//   k_quantize  x -> codes and per-vector dedup keys (TMA-staged input tiles)
-//   k_insert    keys -> per-table first-occurrence hash table
+//   k_quantize  x -> codes and per-vector dedup keys (TMA-staged input tiles);
+//               then the keys of its rows -> per-table first-occurrence hash table
 //   k_resolve   literal / match decision; literal code histograms per segment
 //               and per table
 //   k_codebook  per-table Huffman code; empties the hash table; the last CTA
@@ -193,7 +193,10 @@ __device__ __forceinline__ void issue_segment_tile(In* stage, const CUtensorMap*
 // k_quantize: persistent CTAs, each taking segments blockIdx.x, +gridDim.x, ...
 // A segment's input tile (rows of one table) arrives in shared memory by TMA
 // into one of two stages, so the next tile streams in while the current one is
-// quantized.  8 warps, each a run of 128-element
+// quantized.  After its last tile the CTA enters the keys of all its rows into
+// the first-occurrence tables (lanes holding the same key are merged with
+// match.any first, so hot keys queue fewer atomics); other CTAs are still
+// streaming meanwhile.  8 warps, each a run of 128-element
 // slabs (lane = 4 consecutive elements).  The dedup key of a vector is the
 // wrapping sum over its 4-code words w_k of lowbias32(w_k + k * 0x9E3779B9)
 // plus lowbias32(raw ^ (d + 1) * 0x85EBCA6B) for each outlier at position d.
@@ -291,29 +294,24 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     if (tid == 0 && seg + 2 * (int)gridDim.x < nsegT)
       issue_segment_tile<D, In>(s_x + stg * Q::kStageFloats, &tmap, &s_bar[stg], sh, seg + 2 * gridDim.x);
   }
-}
-
-// ---------------------------------------------------------------------------
-// k_insert: one thread per (table, row) enters the row's key into the table's
-// first-occurrence hash table (all keys of the call, in one wave).
-// ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_insert(Shape sh, Work w) {
-  pdl_enter();
-  const unsigned long long i = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
-  const unsigned long long nvec = (unsigned long long)sh.B * sh.T;
-  const int t = i < nvec ? (int)(i / (unsigned long long)sh.B) : 0;
-  // (a table without dedup enters no keys)
-  const bool valid = i < nvec && !(w.modes && (w.modes[t] & kModeNoDedup));
-  const unsigned vmask = __ballot_sync(0xffffffffu, valid);
-  if (!valid) return;
-  const uint32_t b = (uint32_t)(i - (unsigned long long)t * sh.B);
-  const uint32_t h = __ldcg(&w.vhash[i]);
-  // lanes are consecutive rows: of the lanes holding the same (table, key),
-  // only the lowest (the smallest row) can set the slot, so only it inserts;
-  // this keeps hot keys from queueing atomics on one address
-  const unsigned same = __match_any_sync(vmask, ((unsigned long long)t << 32) | h);
-  if ((threadIdx.x & 31) != __ffs(same) - 1) return;
-  dedup_insert(w.slots + (size_t)t * sh.S, sh.S, h, b, w.glob);
+  if (sh.window == 0 && (int)blockIdx.x < nsegT) {
+    // the keys of this CTA's rows into the first-occurrence tables, after its last tile
+    __syncthreads();
+    const int nmine = (nsegT - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int total = nmine * G::kSB;   // a multiple of 32: a warp's rows lie in one segment
+    for (int i = tid; i < total; i += 256) {
+      const int seg = (int)blockIdx.x + (i / G::kSB) * (int)gridDim.x;
+      const int t = seg / sh.nseg;
+      const int64_t b = (int64_t)(seg - t * sh.nseg) * G::kSB + i % G::kSB;
+      const bool valid = b < B && !(w.modes && (w.modes[t] & kModeNoDedup));
+      const unsigned vmask = __ballot_sync(0xffffffffu, valid);
+      if (valid) {
+        const uint32_t h = __ldcg(&w.vhash[(size_t)t * B + b]);
+        const unsigned same = __match_any_sync(vmask, h);
+        if (lane == __ffs(same) - 1) dedup_insert(w.slots + (size_t)t * sh.S, sh.S, h, (uint32_t)b, w.glob);
+      }
+    }
+  }
 }
 
 __device__ __forceinline__ bool has_zero_byte(uint32_t v) {
@@ -1256,11 +1254,7 @@ static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, 
     prof_begin(prof, "k_quantize", st);
     launch_k(k_quantize<D, In>, qgrid, 256, smem, st, *xmap, sh, ep, w);
     prof_end(prof, st);
-    if (sh.window == 0) {   // a window needs no hash table
-      prof_begin(prof, "k_insert", st);
-      launch_k(k_insert, (unsigned)(((unsigned long long)sh.B * sh.T + 255) / 256), 256, 0, st, sh, w);
-      prof_end(prof, st);
-    }
+
     prof_begin(prof, "k_resolve", st);
     launch_k(k_resolve<D, In>, grid, kResolveThreads, 0, st, x, sh, w);
     prof_end(prof, st);
