@@ -225,3 +225,44 @@ def select_modes(cr, tc, td, bw: float):
     if rc != OK:
         raise ValueError("bad selection arguments")
     return out
+
+
+def chunk_rows(B: int, n_chunks: int):
+    """Row ranges [b0, b1) of the n_chunks slices of a batch of B rows.
+
+    §III-E "Buffer Optimization" and §IV-E: the batch is split equally into
+    one slice per destination rank of the all-to-all.  Where B is not a
+    multiple of n_chunks, the first B % n_chunks slices take one row more
+    (slices past B are empty)."""
+    if n_chunks < 1:
+        raise ValueError("n_chunks must be >= 1")
+    q, rem = divmod(int(B), int(n_chunks))
+    starts = [r * q + min(r, rem) for r in range(n_chunks + 1)]
+    return [(starts[r], starts[r + 1]) for r in range(n_chunks)]
+
+
+def compress_chunked(x, eb, n_chunks: int, *, modes=None, window: int = 0):
+    """§III-E "Buffer Optimization", Fig. 7 (top): every slice of the batch is
+    compressed on its own, as a self-contained container, and the containers
+    lie back to back in one sending buffer.  Returns (buffer uint8, offsets
+    uint64 [n_chunks + 1]): container r spans [offsets[r], offsets[r+1])."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    B = x.shape[0]
+    parts, offs = [], [0]
+    for b0, b1 in chunk_rows(B, n_chunks):
+        buf, _ = compress(x[b0:b1], eb, modes=modes, window=window)
+        parts.append(buf)
+        offs.append(offs[-1] + buf.size)
+    return np.concatenate(parts), np.asarray(offs, dtype=np.uint64)
+
+
+def decompress_chunked(buf, offsets, B: int, T: int, D: int):
+    """Fig. 7 (bottom): container r of the buffer restores rows
+    chunk_rows(B, n)[r] of the batch, independently of the others."""
+    buf = np.ascontiguousarray(buf, dtype=np.uint8)
+    offsets = [int(v) for v in offsets]
+    xhat = np.zeros((B, T, D), dtype=np.float32)
+    for r, (b0, b1) in enumerate(chunk_rows(B, len(offsets) - 1)):
+        xh, _ = decompress(buf[offsets[r]:offsets[r + 1]], b1 - b0, T, D)
+        xhat[b0:b1] = xh
+    return xhat
