@@ -424,6 +424,77 @@ def main():
                 "compress_input_gbs": round(2 * N / tcb / 1e9, 1),
                 "decompress_gbs": round(4 * N / tdb / 1e9, 1)}
 
+    # ---- chunked sending buffer (outside the timed region): one pass over R slices, each its own
+    #      container, against R separate compress / decompress calls on the slices ----
+    chunked = None
+    if not args.no_hybrid:
+        chunked = {}
+        nrep = max(3, min(K, 20))
+        xref = torch.empty_like(x)   # the single container's reconstruction of this batch
+        codec.compress_into(x, eb, out, nbytes, stream)
+        codec.decompress_into(out, cap, xref, stream)
+        for R in (2, 4, 8, 16):
+            capc = codec.compress_chunked_bound(B, T, D, R)
+            outc = torch.empty(capc, dtype=torch.uint8, device=dev)
+            offs = torch.zeros(R + 1, dtype=torch.int64, device=dev)
+            xc = torch.empty_like(x)
+            codec.compress_chunked(x, R, eb, stream, out=outc, offsets=offs)
+            torch.cuda.synchronize()
+            o = offs.cpu().tolist()
+            codec.decompress_chunked(outc, o[-1], offs, B, T, D, stream, out=xc)
+            torch.cuda.synchronize()
+            codec.check()
+            if not torch.equal(xc, xref):   # dedup scope never changes a reconstructed value
+                raise SystemExit(f"chunked reconstruction differs from the single container (R={R})")
+            rows = [(b0, b1) for b0, b1 in
+                    ((r * (B // R) + min(r, B % R), (r + 1) * (B // R) + min(r + 1, B % R)) for r in range(R))]
+            slots = [codec.compress_bound(b1 - b0, T, D) for b0, b1 in rows]
+            base = np.concatenate([[0], np.cumsum([(s + 255) // 256 * 256 for s in slots])]).astype(np.int64)
+            outs = torch.empty(int(base[-1]), dtype=torch.uint8, device=dev)
+            nbs = torch.zeros(R, dtype=torch.int64, device=dev)
+            xs = [x[b0:b1] for b0, b1 in rows]
+
+            def seq_c():
+                for r in range(R):
+                    codec.compress_into(xs[r], eb, outs[base[r]:base[r + 1]], nbs[r:r + 1], stream)
+
+            def seq_d():
+                for r, (b0, b1) in enumerate(rows):
+                    codec.decompress_into(outc[o[r]:o[r + 1]], o[r + 1] - o[r], xc[b0:b1], stream)
+
+            def one_c():
+                codec.compress_chunked(x, R, eb, stream, out=outc, offsets=offs)
+
+            def one_d():
+                codec.decompress_chunked(outc, o[-1], offs, B, T, D, stream, out=xc)
+
+            times = {}
+            for name, fn in (("single_c", one_c), ("single_d", one_d), ("seq_c", seq_c), ("seq_d", seq_d)):
+                fn()
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                      for _ in range(nrep)]
+                for a, b_ in ev:
+                    flush.zero_()
+                    a.record(stream)
+                    fn()
+                    b_.record(stream)
+                torch.cuda.synchronize()
+                times[name] = sum(a.elapsed_time(b_) for a, b_ in ev) / 1e3 / nrep
+            codec.check()
+            if not torch.equal(xc, xref):
+                raise SystemExit(f"sequential decode of the chunked buffer differs (R={R})")
+            chunked[str(R)] = {
+                "compression_ratio": round(4 * N / o[-1], 3),
+                "single_pass_compress_gbs": round(4 * N / times["single_c"] / 1e9, 1),
+                "single_pass_decompress_gbs": round(4 * N / times["single_d"] / 1e9, 1),
+                "separate_calls_compress_gbs": round(4 * N / times["seq_c"] / 1e9, 1),
+                "separate_calls_decompress_gbs": round(4 * N / times["seq_d"] / 1e9, 1),
+                "compress_speedup": round(times["seq_c"] / times["single_c"], 3),
+                "decompress_speedup": round(times["seq_d"] / times["single_d"], 3),
+            }
+            del outc, outs, xc
+        del xref
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sample = workloads.make(WORKLOAD, batch=512)
@@ -456,6 +527,7 @@ def main():
             "hybrid": hybrid,
             "window": window,
             "bf16_input": bf16,
+            "chunked": chunked,
             "clocks": clocks,
             "wall_s": round(wall, 3),
         }

@@ -28,11 +28,14 @@ __all__ = [
     "EBC_MODE_DEDUP_HUFFMAN", "EBC_MODE_HUFFMAN", "EBC_MODE_DEDUP_RAW", "EBC_MODE_RAW", "EbcTableStats",
     "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup", "ebc_select_modes",
     "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
+    "EBC_MAX_CHUNKS", "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16",
+    "ebc_decompress_chunked",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
 EBC_ERR_DEVICE_TIMEOUT, EBC_ERR_CUDA, EBC_ERR_NO_DEVICE, EBC_ERR_INTERNAL = 4, 5, 6, 7
 EBC_ERR_SCRATCH_LIMIT = 8
+EBC_MAX_CHUNKS = 256
 EBC_MODE_DEDUP_HUFFMAN, EBC_MODE_HUFFMAN, EBC_MODE_DEDUP_RAW, EBC_MODE_RAW = 0, 1, 2, 3
 EBC_DECAY_NONE, EBC_DECAY_LINEAR, EBC_DECAY_STEPWISE, EBC_DECAY_DROP, EBC_DECAY_LOG = 0, 1, 2, 3, 4
 DECAY = {"none": 0, "linear": 1, "stepwise": 2, "drop": 3, "log": 4}
@@ -43,6 +46,7 @@ EXPORTED_SYMBOLS = (
     "ebc_decompress_host", "ebc_get_stats", "ebc_last_device_error", "ebc_set_profiling", "ebc_get_profile",
     "ebc_decompress_noalloc", "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup",
     "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
+    "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16", "ebc_decompress_chunked",
 )
 
 
@@ -116,6 +120,10 @@ def lib():
                 "ebc_select_modes": (I, [P, P, P, D, I, I, P]),
                 "ebc_select_table_modes": (I, [P, P, I64, I, I, P, D, P, P]),
                 "ebc_table_homo_index": (I, [P, P, I64, I, I, P, P, P]),
+                "ebc_compress_chunked_bound": (U64, [I64, I, I, I]),
+                "ebc_compress_chunked": (I, [P, P, I64, I, I, P, I, P, U64, P, P]),
+                "ebc_compress_chunked_bf16": (I, [P, P, I64, I, I, P, I, P, U64, P, P]),
+                "ebc_decompress_chunked": (I, [P, P, U64, P, I, P, I64, I, I, P]),
             }
             for name, (res, args) in sig.items():
                 f = getattr(L, name)
@@ -171,6 +179,25 @@ def ebc_decompress(ctx, d_in, in_bytes, d_xhat, B, T, D, stream) -> int:
 def ebc_compress_bf16(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_bytes, stream) -> int:
     return lib().ebc_compress_bf16(ctx, d_x, int(B), int(T), int(D), eb_ptr, d_out, int(out_capacity), d_out_bytes,
                                    stream)
+
+
+def ebc_compress_chunked_bound(B: int, T: int, D: int, n_chunks: int) -> int:
+    return int(lib().ebc_compress_chunked_bound(int(B), int(T), int(D), int(n_chunks)))
+
+
+def ebc_compress_chunked(ctx, d_x, B, T, D, eb_ptr, n_chunks, d_out, out_capacity, d_offsets, stream) -> int:
+    return lib().ebc_compress_chunked(ctx, d_x, int(B), int(T), int(D), eb_ptr, int(n_chunks), d_out,
+                                      int(out_capacity), d_offsets, stream)
+
+
+def ebc_compress_chunked_bf16(ctx, d_x, B, T, D, eb_ptr, n_chunks, d_out, out_capacity, d_offsets, stream) -> int:
+    return lib().ebc_compress_chunked_bf16(ctx, d_x, int(B), int(T), int(D), eb_ptr, int(n_chunks), d_out,
+                                           int(out_capacity), d_offsets, stream)
+
+
+def ebc_decompress_chunked(ctx, d_in, in_bytes, d_offsets, n_chunks, d_xhat, B, T, D, stream) -> int:
+    return lib().ebc_decompress_chunked(ctx, d_in, int(in_bytes), d_offsets, int(n_chunks), d_xhat, int(B), int(T),
+                                        int(D), stream)
 
 
 def ebc_set_window(ctx, window) -> int:
@@ -338,6 +365,43 @@ class Codec:
         nbytes = torch.zeros(1, dtype=torch.int64, device=x.device)
         self.compress_into(x, eb, out, nbytes, stream)
         return out, nbytes
+
+    @staticmethod
+    def compress_chunked_bound(B, T, D, n_chunks) -> int:
+        return ebc_compress_chunked_bound(B, T, D, n_chunks)
+
+    def compress_chunked(self, x, n_chunks: int, eb=None, stream=None, out=None, offsets=None):
+        """One container per slice of the batch (numpy array_split slices), back to
+        back in one buffer.  Returns (buffer uint8, offsets int64 [n_chunks + 1]),
+        both CUDA tensors; container r spans [offsets[r], offsets[r+1])."""
+        import torch
+        if not (x.is_cuda and x.dtype in (torch.float32, torch.bfloat16) and x.is_contiguous() and x.dim() == 3):
+            raise ValueError("x must be a contiguous float32 or bfloat16 CUDA tensor [B, T, D]")
+        B, T, D = x.shape
+        if out is None:
+            out = torch.empty(max(self.compress_chunked_bound(B, T, D, n_chunks), 16), dtype=torch.uint8,
+                              device=x.device)
+        if offsets is None:
+            offsets = torch.zeros(n_chunks + 1, dtype=torch.int64, device=x.device)
+        ebh = None if eb is None else _f32_host(eb, T)
+        fn, name = ((ebc_compress_chunked_bf16, "ebc_compress_chunked_bf16") if x.dtype == torch.bfloat16
+                    else (ebc_compress_chunked, "ebc_compress_chunked"))
+        rc = fn(self._ctx, _ptr(x), B, T, D, ebh.ctypes.data_as(ctypes.c_void_p) if ebh is not None else None,
+                n_chunks, _ptr(out), out.numel(), _ptr(offsets), _stream_ptr(stream))
+        if rc:
+            raise EbcError(rc, name)
+        return out, offsets
+
+    def decompress_chunked(self, buf, in_bytes: int, offsets, B: int, T: int, D: int, stream=None, out=None):
+        """Restores every slice of the batch from its container (offsets: CUDA int64 [n + 1])."""
+        import torch
+        if out is None:
+            out = torch.empty((B, T, D), dtype=torch.float32, device=buf.device)
+        rc = ebc_decompress_chunked(self._ctx, _ptr(buf), in_bytes, _ptr(offsets), offsets.numel() - 1, _ptr(out),
+                                    B, T, D, _stream_ptr(stream))
+        if rc:
+            raise EbcError(rc, "ebc_decompress_chunked")
+        return out
 
     def decompress_into(self, container, in_bytes: int, xhat, stream=None) -> None:
         B, T, D = xhat.shape

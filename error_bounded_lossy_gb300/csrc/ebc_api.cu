@@ -57,7 +57,7 @@ struct ebc_ctx {
   // the compress layout whose dedup table and look-back flags are known clean
   const void* clean_buf = nullptr;
   int64_t cleanB = -1;
-  int cleanT = -1, cleanD = -1;
+  int cleanT = -1, cleanD = -1, cleanR = -1;
   // schedule
   float* eb_base = nullptr;
   float* eb_now = nullptr;
@@ -69,7 +69,7 @@ struct ebc_ctx {
   int modes_T = 0;
   // last compress shape
   int64_t lastB = 0;
-  int lastT = 0, lastD = 0;
+  int lastT = 0, lastD = 0, lastR = 1;
   Prof* prof = nullptr;
 };
 
@@ -83,18 +83,25 @@ static bool shape_ok(int64_t B, int T, int D) {
   return (uint64_t)B * (uint64_t)T * (uint64_t)D <= (1ull << 31);
 }
 
-static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0) {
+// R: slices of the batch, each coded as a container of its own (1 = one container).
+static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0, int R = 1) {
   Shape sh;
   sh.nsm = nsm;
   sh.B = B;
   sh.T = T;
   sh.D = D;
+  sh.R = R;
+  sh.U = R * T;
+  sh.Bq = B / R;
+  sh.Brem = (int)(B % R);
+  sh.Bc = sh.Bq + (sh.Brem > 0 ? 1 : 0);
   sh.SB = 8192 / D < 32 ? 32 : 8192 / D;
   sh.KC = 128 / D < 1 ? 1 : 128 / D;
-  sh.nseg = (int)((B + sh.SB - 1) / sh.SB);
-  sh.nw = (int)((B + 31) / 32);
+  sh.qseg = (int)((B + sh.SB - 1) / sh.SB);
+  sh.nseg = (int)((sh.Bc + sh.SB - 1) / sh.SB);
+  sh.nw = (int)((sh.Bc + 31) / 32);
   uint32_t S = 64;
-  while ((int64_t)S < 2 * B) S <<= 1;
+  while ((int64_t)S < 2 * sh.Bc) S <<= 1;
   sh.S = S;
   sh.window = window;
   sh.ref_bytes = window > 0 ? 1 : (B <= 65536 ? 2 : 4);
@@ -143,9 +150,9 @@ struct Carver {
 static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   Carver c{reinterpret_cast<char*>(buf)};
   Work w{};
-  const size_t nvec = (size_t)sh.B * sh.T, nsegT = (size_t)sh.T * sh.nseg;
-  w.slots = c.take<unsigned long long>(8 * (size_t)sh.T * sh.S);
-  const size_t groups = (nsegT + 7) / 8 > (size_t)sh.T ? (nsegT + 7) / 8 : (size_t)sh.T;
+  const size_t nvec = (size_t)sh.B * sh.T, nsegT = (size_t)sh.U * sh.nseg, U = (size_t)sh.U;
+  w.slots = c.take<unsigned long long>(8 * U * sh.S);
+  const size_t groups = (nsegT + 7) / 8 > U ? (nsegT + 7) / 8 : U;
   w.seg_desc = c.take<uint4>(16 * groups);
   w.tile_base = c.take<uint4>(16 * groups);
   w.seg_base = c.take<uint4>(16 * nsegT);
@@ -153,14 +160,16 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   w.vhash = c.take<uint32_t>(4 * nvec);
   w.vnout = c.take<uint32_t>(4 * nvec);
   w.ref = c.take<uint32_t>(4 * nvec);
-  w.bitmap = c.take<uint32_t>(4 * (size_t)sh.T * sh.nw);
+  w.bitmap = c.take<uint32_t>(4 * U * sh.nw);
   w.seg_hist = c.take<uint32_t>(1024 * nsegT);
   w.seg_cnt = c.take<uint4>(16 * nsegT);
-  w.tab_hist = c.take<uint32_t>(1024 * (size_t)sh.T);
-  w.tab_cnt = c.take<uint4>(16 * (size_t)sh.T);
-  w.tab_bits = c.take<unsigned long long>(8 * (size_t)sh.T);
+  w.tab_hist = c.take<uint32_t>(1024 * U);
+  w.tab_cnt = c.take<uint4>(16 * U);
+  w.tab_rec = c.take<uint4>(16 * U);
+  w.tab_bits = c.take<unsigned long long>(8 * U);
   w.modes = nullptr;
-  w.tabcode = c.take<uint32_t>(1024 * (size_t)sh.T);
+  w.tabcode = c.take<uint32_t>(1024 * U);
+  w.cont = c.take<ContLay>(sizeof(ContLay) * (size_t)sh.R);
   w.glob = g;
   *total = c.off;
   return w;
@@ -169,10 +178,10 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
 static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   Carver c{reinterpret_cast<char*>(buf)};
   Work w{};
-  const size_t nsegT = (size_t)sh.T * sh.nseg;
+  const size_t nsegT = (size_t)sh.U * sh.nseg;
   const size_t max_chunks = nsegT * (size_t)(sh.SB / sh.KC);
-  w.lut = c.take<uint16_t>(2u * (1u << kLutBits) * (size_t)sh.T);
-  w.dtab = c.take<DecTab>(sizeof(DecTab) * (size_t)sh.T);
+  w.lut = c.take<uint16_t>(2u * (1u << kLutBits) * (size_t)sh.U);
+  w.dtab = c.take<DecTab>(sizeof(DecTab) * (size_t)sh.U);
   w.cdesc = c.take<uint4>(16 * max_chunks);
   w.litrow = c.take<uint16_t>(2 * nsegT * (size_t)sh.SB);
   w.mdesc = c.take<uint2>(8 * (size_t)sh.B * (size_t)sh.T);
@@ -335,10 +344,28 @@ uint64_t ebc_compress_bound(int64_t B, int T, int D) {
   return fixed_bytes(sh) + pad16h(nvec * 2u) + pad16h(nvec * sh.ref_bytes) + words * 4u;
 }
 
-// fp32 or bf16 input (bf16: its raw 16 bits; compressed as its exact fp32 value)
-static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T, int D, const float* eb, void* d_out,
-                        uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
-  if (!c || !shape_ok(B, T, D) || !d_out || !d_out_bytes || !aligned16(d_out) ||
+// Sum of the data-independent bytes of the containers of R slices.
+static uint64_t fixed_bytes_sliced(int64_t B, int T, int D, int R) {
+  const Shape all = make_shape(B, T, D, 0, 0, R);
+  uint64_t n = 0;
+  for (int r = 0; r < R; ++r) n += fixed_bytes(make_shape(slice_rows(all, r), T, D));
+  return n;
+}
+
+uint64_t ebc_compress_chunked_bound(int64_t B, int T, int D, int n_chunks) {
+  if (!shape_ok(B, T, D) || n_chunks < 1 || n_chunks > kMaxSlices) return 0;
+  const Shape all = make_shape(B, T, D, 0, 0, n_chunks);
+  uint64_t n = 0;
+  for (int r = 0; r < n_chunks; ++r) n += ebc_compress_bound(slice_rows(all, r), T, D);
+  return n;
+}
+
+// fp32 or bf16 input (bf16: its raw 16 bits; compressed as its exact fp32 value), in R slices
+// (d_offsets: null for one container, else [R + 1] container boundaries written on the device)
+static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T, int D, const float* eb, int R,
+                        void* d_out, uint64_t out_capacity, uint64_t* d_out_bytes, uint64_t* d_offsets,
+                        void* stream) {
+  if (!c || !shape_ok(B, T, D) || R < 1 || R > kMaxSlices || !d_out || !d_out_bytes || !aligned16(d_out) ||
       ((uintptr_t)d_out_bytes & 7u) != 0 || (bf16 && D < 8))
     return EBC_ERR_INVALID_ARG;
   const uint64_t N = (uint64_t)B * T * D;
@@ -355,8 +382,8 @@ static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T
     if (!eb_ok(ebs[t])) return EBC_ERR_INVALID_ARG;
     ep.eb[t] = ebs[t];
   }
-  const Shape sh = make_shape(B, T, D, c->nsm, c->window);
-  if (out_capacity < fixed_bytes(sh)) return EBC_ERR_CAPACITY;
+  const Shape sh = make_shape(B, T, D, c->nsm, c->window, R);
+  if (out_capacity < (R == 1 ? fixed_bytes(sh) : fixed_bytes_sliced(B, T, D, R))) return EBC_ERR_CAPACITY;
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
   carve_compress(nullptr, sh, c->glob, &need);
@@ -370,37 +397,52 @@ static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T
   c->lastB = B;
   c->lastT = T;
   c->lastD = D;
+  c->lastR = R;
   // Each call leaves its dedup table empty (k_emit).  A new layout on this
   // buffer starts from a reset.
-  if (T > 0 && sh.nseg > 0 && (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D)) {
-    if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)T * sh.S, st) != cudaSuccess) return EBC_ERR_CUDA;
+  if (T > 0 && sh.nseg > 0 &&
+      (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D || c->cleanR != R)) {
+    if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)sh.U * sh.S, st) != cudaSuccess) return EBC_ERR_CUDA;
     c->clean_buf = c->cbuf;
     c->cleanB = B;
     c->cleanT = T;
     c->cleanD = D;
+    c->cleanR = R;
   }
   const cudaError_t e = launch_compress(d_x, bf16, sh, ep, w, (uint8_t*)d_out, out_capacity,
-                                        (unsigned long long*)d_out_bytes, c->cepoch, st, c->prof);
+                                        (unsigned long long*)d_out_bytes, (unsigned long long*)d_offsets,
+                                        c->cepoch, st, c->prof);
   if (e != cudaSuccess) c->clean_buf = nullptr;   // the dedup table may be left dirty
   return cuda_err(e);
 }
 
 int ebc_compress(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, void* d_out,
                  uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
-  return compress_any(c, d_x, false, B, T, D, eb, d_out, out_capacity, d_out_bytes, stream);
+  return compress_any(c, d_x, false, B, T, D, eb, 1, d_out, out_capacity, d_out_bytes, nullptr, stream);
 }
 
 int ebc_compress_bf16(ebc_ctx* c, const uint16_t* d_x, int64_t B, int T, int D, const float* eb, void* d_out,
                       uint64_t out_capacity, uint64_t* d_out_bytes, void* stream) {
-  return compress_any(c, d_x, true, B, T, D, eb, d_out, out_capacity, d_out_bytes, stream);
+  return compress_any(c, d_x, true, B, T, D, eb, 1, d_out, out_capacity, d_out_bytes, nullptr, stream);
 }
 
-int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
-                   void* stream) {
-  if (!c || !shape_ok(B, T, D) || !d_in || !aligned16(d_in)) return EBC_ERR_INVALID_ARG;
-  const uint64_t N = (uint64_t)B * T * D;
-  if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
-  const Shape sh = make_shape(B, T, D, c->nsm);
+int ebc_compress_chunked(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const float* eb, int n_chunks,
+                         void* d_out, uint64_t out_capacity, uint64_t* d_offsets, void* stream) {
+  if (!d_offsets || n_chunks < 1 || n_chunks > kMaxSlices) return EBC_ERR_INVALID_ARG;
+  return compress_any(c, d_x, false, B, T, D, eb, n_chunks, d_out, out_capacity, d_offsets + n_chunks, d_offsets,
+                      stream);
+}
+
+int ebc_compress_chunked_bf16(ebc_ctx* c, const uint16_t* d_x, int64_t B, int T, int D, const float* eb,
+                              int n_chunks, void* d_out, uint64_t out_capacity, uint64_t* d_offsets, void* stream) {
+  if (!d_offsets || n_chunks < 1 || n_chunks > kMaxSlices) return EBC_ERR_INVALID_ARG;
+  return compress_any(c, d_x, true, B, T, D, eb, n_chunks, d_out, out_capacity, d_offsets + n_chunks, d_offsets,
+                      stream);
+}
+
+static int decompress_any(ebc_ctx* c, const void* d_in, uint64_t in_bytes, const uint64_t* d_offsets, int R,
+                          float* d_xhat, int64_t B, int T, int D, void* stream) {
+  const Shape sh = make_shape(B, T, D, c->nsm, 0, R);
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
   carve_decompress(nullptr, sh, c->glob, &need);
@@ -410,7 +452,26 @@ int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xha
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
   c->depoch = (c->depoch + 1) & 0xFFFFFFu;
-  return cuda_err(launch_decompress((const uint8_t*)d_in, in_bytes, sh, w, d_xhat, c->depoch, st, c->prof));
+  return cuda_err(launch_decompress((const uint8_t*)d_in, in_bytes, (const unsigned long long*)d_offsets, sh, w,
+                                    d_xhat, c->depoch, st, c->prof));
+}
+
+int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
+                   void* stream) {
+  if (!c || !shape_ok(B, T, D) || !d_in || !aligned16(d_in)) return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T * D;
+  if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
+  return decompress_any(c, d_in, in_bytes, nullptr, 1, d_xhat, B, T, D, stream);
+}
+
+int ebc_decompress_chunked(ebc_ctx* c, const void* d_in, uint64_t in_bytes, const uint64_t* d_offsets,
+                           int n_chunks, float* d_xhat, int64_t B, int T, int D, void* stream) {
+  if (!c || !shape_ok(B, T, D) || !d_in || !aligned16(d_in) || !d_offsets || ((uintptr_t)d_offsets & 7u) != 0 ||
+      n_chunks < 1 || n_chunks > kMaxSlices)
+    return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T * D;
+  if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
+  return decompress_any(c, d_in, in_bytes, d_offsets, n_chunks, d_xhat, B, T, D, stream);
 }
 
 int ebc_set_window(ebc_ctx* c, int window) {
@@ -441,26 +502,28 @@ int ebc_get_table_stats(ebc_ctx* c, ebc_table_stats* out, int T) {
   if (!c || !out || T <= 0 || T != c->lastT) return EBC_ERR_INVALID_ARG;
   const int err = ebc_last_device_error(c);
   if (err == EBC_ERR_CUDA) return err;
-  const Shape sh = make_shape(c->lastB, T, c->lastD, c->nsm);
+  const Shape sh = make_shape(c->lastB, T, c->lastD, c->nsm, c->window, c->lastR);
   std::memset(out, 0, sizeof(*out) * (size_t)T);
   if (sh.nseg == 0 || !c->cbuf) return err;   // an empty batch: nothing was coded
   size_t need = 0;
   const Work w = carve_compress(c->cbuf, sh, c->glob, &need);   // the last compress's layout
-  uint4* cnt = new (std::nothrow) uint4[(size_t)T];
-  unsigned long long* bits = new (std::nothrow) unsigned long long[(size_t)T];
+  const size_t U = (size_t)sh.U;
+  uint4* cnt = new (std::nothrow) uint4[U];
+  unsigned long long* bits = new (std::nothrow) unsigned long long[U];
   int rc = err;
   if (!cnt || !bits) {
     rc = EBC_ERR_INTERNAL;
-  } else if (cudaMemcpy(cnt, w.tab_cnt, 16 * (size_t)T, cudaMemcpyDeviceToHost) != cudaSuccess ||
-             cudaMemcpy(bits, w.tab_bits, 8 * (size_t)T, cudaMemcpyDeviceToHost) != cudaSuccess) {
+  } else if (cudaMemcpy(cnt, w.tab_cnt, 16 * U, cudaMemcpyDeviceToHost) != cudaSuccess ||
+             cudaMemcpy(bits, w.tab_bits, 8 * U, cudaMemcpyDeviceToHost) != cudaSuccess) {
     rc = EBC_ERR_CUDA;
   } else {
-    for (int t = 0; t < T; ++t) {
-      out[t].n_literal = cnt[t].x;
-      out[t].n_match = cnt[t].y;
-      out[t].n_outlier = cnt[t].z;
-      out[t].n_chunks = cnt[t].w;
-      out[t].payload_bits = bits[t];
+    for (size_t u = 0; u < U; ++u) {   // a table's counts over all slices
+      const int t = (int)(u % (size_t)T);
+      out[t].n_literal += cnt[u].x;
+      out[t].n_match += cnt[u].y;
+      out[t].n_outlier += cnt[u].z;
+      out[t].n_chunks += cnt[u].w;
+      out[t].payload_bits += bits[u];
     }
   }
   delete[] cnt;
@@ -806,7 +869,7 @@ int ebc_decompress_noalloc(const void* d_in, uint64_t in_bytes, float* d_xhat, i
   // The array keeps whatever the previous call left; only the status block
   // must start at zero (the tables are written before they are read).
   if (cudaMemsetAsync(g, 0, sizeof(Glob), st) != cudaSuccess) return EBC_ERR_CUDA;
-  if (launch_decompress((const uint8_t*)d_in, in_bytes, sh, w, d_xhat, 1u, st, nullptr) != cudaSuccess)
+  if (launch_decompress((const uint8_t*)d_in, in_bytes, nullptr, sh, w, d_xhat, 1u, st, nullptr) != cudaSuccess)
     return EBC_ERR_CUDA;
   unsigned int code = 0;
   if (cudaMemcpyAsync(&code, &g->sticky, sizeof code, cudaMemcpyDeviceToHost, st) != cudaSuccess ||

@@ -176,8 +176,8 @@ template <int D, typename In>
 __device__ __forceinline__ void issue_segment_tile(In* stage, const CUtensorMap* map, uint64_t* bar, const Shape& sh,
                                                    int seg) {
   using Q = QGeo<D, In>;
-  const int t = seg / sh.nseg;
-  const int s = seg - t * sh.nseg;
+  const int t = seg / sh.qseg;
+  const int s = seg - t * sh.qseg;
   unsigned long long first;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(first));
   mbar_expect_tx(bar, Q::kStageBytes);
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
   In* s_x = reinterpret_cast<In*>(s_raw);
   __shared__ __align__(8) uint64_t s_bar[2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int nsegT = sh.T * sh.nseg;
+  const int nsegT = sh.T * sh.qseg;
   const int64_t B = sh.B;
   const unsigned long long pol = l2_evict_last();
   if (tid == 0) {
@@ -228,12 +228,15 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
   for (int seg = blockIdx.x; seg < nsegT; seg += gridDim.x, ++i) {
     const int stg = i & 1;
     const In* xs = s_x + stg * Q::kStageFloats;
-    const int t = seg / sh.nseg;
-    const int s = seg - t * sh.nseg;
+    const int t = seg / sh.qseg;
+    const int s = seg - t * sh.qseg;
     const int64_t row0 = (int64_t)s * G::kSB;
-    if (s == 0) {   // per-call table accumulators that k_resolve adds to
-      w.tab_hist[(size_t)t * 256 + tid] = 0u;
-      if (tid == 0) w.tab_cnt[t] = make_uint4(0, 0, 0, 0);
+    if (s == 0) {   // per-call accumulators of the table's units, which k_resolve adds to
+      for (int r = 0; r < sh.R; ++r) {
+        const int u = r * sh.T + t;
+        w.tab_hist[(size_t)u * 256 + tid] = 0u;
+        if (tid == 0) w.tab_cnt[u] = make_uint4(0, 0, 0, 0);
+      }
     }
     const float eb = ep.eb[t];
     const float ebx2 = __fmul_rn(2.0f, eb);
@@ -301,14 +304,17 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     const int total = nmine * G::kSB;   // a multiple of 32: a warp's rows lie in one segment
     for (int i = tid; i < total; i += 256) {
       const int seg = (int)blockIdx.x + (i / G::kSB) * (int)gridDim.x;
-      const int t = seg / sh.nseg;
-      const int64_t b = (int64_t)(seg - t * sh.nseg) * G::kSB + i % G::kSB;
+      const int t = seg / sh.qseg;
+      const int64_t b = (int64_t)(seg - t * sh.qseg) * G::kSB + i % G::kSB;
       const bool valid = b < B && !(w.modes && (w.modes[t] & kModeNoDedup));
+      // each slice keeps its own table: a row never refers into another slice
+      const int u = valid ? slice_of_row(sh, b) * sh.T + t : 0;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);
       if (valid) {
         const uint32_t h = __ldcg(&w.vhash[(size_t)t * B + b]);
-        const unsigned same = __match_any_sync(vmask, h);
-        if (lane == __ffs(same) - 1) dedup_insert(w.slots + (size_t)t * sh.S, sh.S, h, (uint32_t)b, w.glob);
+        const unsigned same = sh.R == 1 ? __match_any_sync(vmask, h)
+                                        : __match_any_sync(vmask, ((unsigned long long)u << 32) | h);
+        if (lane == __ffs(same) - 1) dedup_insert(w.slots + (size_t)u * sh.S, sh.S, h, (uint32_t)b, w.glob);
       }
     }
   }
@@ -336,7 +342,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   constexpr int kSteps = G::kSB / kNW / G::kRPS;         // warp steps (kRPS rows each) per warp
   constexpr int kGroup = kSteps < 8 ? kSteps : 8;        // steps whose loads are issued together
   __shared__ uint32_t s_hist[kNW][256];
-  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4];   // the segment's own codes
+  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4 + 4];   // the segment's own codes
   __shared__ uint32_t s_ref[G::kSB];
   __shared__ uint32_t s_nout[G::kSB];
   __shared__ uint32_t s_win[kMaxWindow + G::kSB];   // window mode: keys of rows row0 - window .. row0 + SB
@@ -347,39 +353,46 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   for (int i = tid; i < G::kBmWords; i += kNT) s_bm[i] = 0u;
   if (tid < 3) s_cnt[tid] = 0u;
 
+  // segment s of unit u = (slice r, table t): rows b0 + s * SB .. of the batch
   const int seg = blockIdx.x;
-  const int t = seg / sh.nseg;
-  const int s = seg - t * sh.nseg;
+  const int u = seg / sh.nseg;
+  const int s = seg - u * sh.nseg;
+  const int r = u / sh.T;
+  const int t = u - r * sh.T;
   const int64_t B = sh.B;
   const int T = sh.T;
-  const int64_t row0 = (int64_t)s * G::kSB;
-  const unsigned long long* slots = w.slots + (size_t)t * sh.S;
+  const int64_t b0 = slice_row0(sh, r);
+  const int64_t bend = b0 + slice_rows(sh, r);              // rows of the slice: [b0, bend)
+  const int64_t row0 = b0 + (int64_t)s * G::kSB;
+  const unsigned long long* slots = w.slots + (size_t)u * sh.S;
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
   const bool nodedup = w.modes && (w.modes[t] & kModeNoDedup);   // every row its own reference
+  // the segment's codes start so words into s_sym (a slice may start off a 16-byte boundary when D < 16)
+  const int so = D >= 16 ? 0 : (int)(((size_t)row0 * D) & 15u) / 4;
   {   // the segment's codes (rows contiguous; the table stride is padded to 16 bytes), copied
       // asynchronously while the keys are looked up
-    const int64_t nrows = B - row0 < G::kSB ? B - row0 : G::kSB;
-    const int nq = (int)((nrows * D + 15) / 16);
-    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D);
+    const int64_t nrows = bend - row0 < G::kSB ? bend - row0 : G::kSB;
+    const int nq = nrows > 0 ? (int)((so * 4 + nrows * D + 15) / 16) : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D - so * 4);
     for (int i = tid; i < nq; i += kNT) cp_async16(reinterpret_cast<uint4*>(s_sym) + i, src + i);
   }
   if (sh.window > 0 && !nodedup) {
-    // window: the nearest earlier row within the window with the same key
+    // window: the nearest earlier row of the slice within the window with the same key
     // (the keys of the window and the segment, in shared memory)
-    const int64_t lo = row0 - sh.window > 0 ? row0 - sh.window : 0;
-    const int64_t hi = row0 + G::kSB < B ? row0 + G::kSB : B;
+    const int64_t lo = row0 - sh.window > b0 ? row0 - sh.window : b0;
+    const int64_t hi = row0 + G::kSB < bend ? row0 + G::kSB : bend;
     for (int64_t i = tid; i < hi - lo; i += kNT) s_win[i] = __ldcg(&w.vhash[(size_t)t * B + lo + i]);
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int r = k * kNT + tid;
-      if (r < G::kSB && row0 + r < B) s_nout[r] = __ldcg(&w.vnout[(size_t)t * B + row0 + r]);
+      const int rr = k * kNT + tid;
+      if (rr < G::kSB && row0 + rr < bend) s_nout[rr] = __ldcg(&w.vnout[(size_t)t * B + row0 + rr]);
     }
     __syncthreads();
 #pragma unroll 1
     for (int k = 0; k < kRPT; ++k) {
-      const int r = k * kNT + tid;
-      const int64_t b = row0 + r;
-      if (r < G::kSB && b < B) {
+      const int rr = k * kNT + tid;
+      const int64_t b = row0 + rr;
+      if (rr < G::kSB && b < bend) {
         const uint32_t h = s_win[b - lo];
         const int64_t stop = b - sh.window > lo ? b - sh.window : lo;
         uint32_t ref = (uint32_t)b;
@@ -388,31 +401,31 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
             ref = (uint32_t)c2;
             break;
           }
-        s_ref[r] = ref;
+        s_ref[rr] = ref;
       }
     }
   } else
-  // one thread per row: first occurrence of the row's key
+  // one thread per row: first occurrence of the row's key in the slice
   {
     uint32_t h[kRPT], no[kRPT];
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int r = k * kNT + tid;
-      const int64_t b = row0 + r;
-      if (r < G::kSB && b < B) {
+      const int rr = k * kNT + tid;
+      const int64_t b = row0 + rr;
+      if (rr < G::kSB && b < bend) {
         h[k] = __ldcg(&w.vhash[(size_t)t * B + b]);
         no[k] = __ldcg(&w.vnout[(size_t)t * B + b]);
       }
     }
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int r = k * kNT + tid;
-      const int64_t b = row0 + r;
-      if (r < G::kSB && b < B) {
+      const int rr = k * kNT + tid;
+      const int64_t b = row0 + rr;
+      if (rr < G::kSB && b < bend) {
         uint32_t ref = nodedup ? (uint32_t)b : dedup_lookup(slots, sh.S, h[k], w.glob);
-        if (ref > (uint32_t)b) ref = (uint32_t)b;   // only on an internal error
-        s_ref[r] = ref;
-        s_nout[r] = no[k];
+        if (ref > (uint32_t)b || (int64_t)ref < b0) ref = (uint32_t)b;   // only on an internal error
+        s_ref[rr] = ref;
+        s_nout[rr] = no[k];
       }
     }
   }
@@ -429,9 +442,9 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   auto load_refs = [&](int g0, uint32_t (&wr)[kGroup][G::kSPR]) {
 #pragma unroll
     for (int it = 0; it < kGroup; ++it) {
-      const int r = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
-      const int64_t b = row0 + r;
-      const uint32_t ref = b < B ? s_ref[r] : (uint32_t)b;
+      const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
+      const int64_t b = row0 + rr;
+      const uint32_t ref = b < bend ? s_ref[rr] : (uint32_t)b;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
         const int d = (lane % G::kLPR) * 4 + j * 128;
@@ -442,16 +455,16 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   auto process = [&](int g0, const uint32_t (&wr)[kGroup][G::kSPR]) {
 #pragma unroll
     for (int it = 0; it < kGroup; ++it) {
-      const int r = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
-      const int64_t b = row0 + r;
-      const bool valid = b < B;
-      const uint32_t ref = valid ? s_ref[r] : 0u;
+      const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
+      const int64_t b = row0 + rr;
+      const bool valid = b < bend;
+      const uint32_t ref = valid ? s_ref[rr] : 0u;
       const bool cand = valid && ref != (uint32_t)b;
       uint32_t wb[G::kSPR];
       bool eq = true;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        wb[j] = s_sym[r * (D / 4) + (lane % G::kLPR) + j * 32];
+        wb[j] = s_sym[so + rr * (D / 4) + (lane % G::kLPR) + j * 32];
         bool e = wr[it][j] == wb[j];
         if (cand && e && has_zero_byte(wb[j])) {
           const int d = (lane % G::kLPR) * 4 + j * 128;
@@ -478,11 +491,11 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
       if (valid && leader) {
         if (match) {
           w.ref[(size_t)t * B + b] = ref;
-          atomicOr(&s_bm[r >> 5], 1u << (r & 31));
+          atomicOr(&s_bm[rr >> 5], 1u << (rr & 31));
           ++n_match;
         } else {
           ++n_lit;
-          n_out += s_nout[r];
+          n_out += s_nout[rr];
         }
       }
     }
@@ -513,19 +526,19 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
 #pragma unroll
     for (int k = 0; k < kNW; ++k) f += s_hist[k][i];
     w.seg_hist[(size_t)seg * 256 + i] = f;
-    if (f) atomicAdd(&w.tab_hist[(size_t)t * 256 + i], f);
+    if (f) atomicAdd(&w.tab_hist[(size_t)u * 256 + i], f);
   }
-  for (int i = tid; i < G::kBmWords; i += kNT) {
+  for (int i = tid; i < G::kBmWords; i += kNT) {   // bit i of word k: row b0 + 32 k + i of the slice
     const int64_t wi = (int64_t)s * G::kBmWords + i;
-    if (wi < sh.nw) w.bitmap[(size_t)t * sh.nw + wi] = s_bm[i];
+    if (wi < sh.nw) w.bitmap[(size_t)u * sh.nw + wi] = s_bm[i];
   }
   if (tid == 0) {
     const uint32_t chunks = (s_cnt[0] + G::kKC - 1) / G::kKC;
     w.seg_cnt[seg] = make_uint4(s_cnt[0], s_cnt[1], s_cnt[2], chunks);
-    atomicAdd(&w.tab_cnt[t].x, s_cnt[0]);
-    atomicAdd(&w.tab_cnt[t].y, s_cnt[1]);
-    atomicAdd(&w.tab_cnt[t].z, s_cnt[2]);
-    atomicAdd(&w.tab_cnt[t].w, chunks);
+    atomicAdd(&w.tab_cnt[u].x, s_cnt[0]);
+    atomicAdd(&w.tab_cnt[u].y, s_cnt[1]);
+    atomicAdd(&w.tab_cnt[u].z, s_cnt[2]);
+    atomicAdd(&w.tab_cnt[u].w, chunks);
   }
 }
 
@@ -579,6 +592,103 @@ __device__ __forceinline__ void st_u64(uint8_t* p, unsigned long long v) {
 }
 __device__ __forceinline__ unsigned long long pad16(unsigned long long n) { return (n + 15ull) & ~15ull; }
 
+// Completes the containers, run by the whole CTA (the last one of k_codebook,
+// or of k_layout when the bitstream sizes come from there).  Thread r < R
+// brings container r's counts, bitstream words and first-unit bases in c; this
+// lays out its sections (a container is the single-call format for the rows
+// of its slice), places the containers back to back (a scan of their sizes),
+// writes the headers, zeroes the section padding and, for an empty batch, the
+// table records (k_emit writes them otherwise), and sets the status.
+__device__ void finish_containers(const Shape& sh, const EbParams& ep, const Work& w, ContLay c, uint8_t* out,
+                                  unsigned long long cap, unsigned long long* out_bytes,
+                                  unsigned long long* chunk_off, uint32_t epoch) {
+  __shared__ unsigned long long s_size[kMaxSlices];
+  __shared__ unsigned long long s_sum[5];   // literals, matches, outliers, chunks, words
+  __shared__ unsigned long long s_total;
+  const int tid = threadIdx.x;
+  const int T = sh.T;
+  Glob* g = w.glob;
+  if (tid < 5) s_sum[tid] = 0ull;
+  __syncthreads();
+  if (tid < sh.R) {
+    const int64_t n = slice_rows(sh, tid);
+    const unsigned long long nseg_r = (unsigned long long)div_up(n, sh.SB);
+    const unsigned long long nw_r = (unsigned long long)div_up(n, 32);
+    c.ref_bytes = (uint32_t)ref_bytes_of(n, sh.window);
+    c.off_seg = kHeaderBytes + (unsigned long long)T * kTableRecBytes;
+    c.off_bitmap = c.off_seg + (unsigned long long)T * nseg_r * kSegRecBytes;
+    c.off_chunks = c.off_bitmap + pad16((unsigned long long)T * nw_r * 4ull);
+    c.off_refs = c.off_chunks + pad16(c.n_chunks * 2ull);
+    c.off_bits = c.off_refs + pad16(c.n_match * c.ref_bytes);
+    c.total = c.off_bits + 4ull * c.words;
+    s_size[tid] = c.total;
+    atomicAdd(&s_sum[0], c.n_lit);
+    atomicAdd(&s_sum[1], c.n_match);
+    atomicAdd(&s_sum[2], c.n_out);
+    atomicAdd(&s_sum[3], c.n_chunks);
+    atomicAdd(&s_sum[4], c.words);
+  }
+  __syncthreads();
+  if (tid == 0) {   // container bases (every size is a multiple of 16 bytes)
+    unsigned long long acc = 0;
+    for (int r = 0; r < sh.R; ++r) {
+      const unsigned long long v = s_size[r];
+      s_size[r] = acc;
+      acc += v;
+    }
+    s_total = acc;
+  }
+  __syncthreads();
+  const unsigned long long total = s_total;
+  const int status = total > cap ? EBC_ERR_CAPACITY : EBC_OK;
+  if (tid < sh.R) {
+    c.base = s_size[tid];
+    w.cont[tid] = c;
+    if (chunk_off) chunk_off[tid] = c.base;
+    uint8_t* o = out + c.base;
+    const int64_t n = slice_rows(sh, tid);
+    if (c.base + kHeaderBytes <= cap) {
+      st_u32(o + 0, kMagic); st_u32(o + 4, kFormatVersion); st_u64(o + 8, (unsigned long long)n);
+      st_u32(o + 16, (uint32_t)T); st_u32(o + 20, (uint32_t)sh.D); st_u32(o + 24, kRadius);
+      st_u32(o + 28, kLmax); st_u32(o + 32, (uint32_t)sh.SB); st_u32(o + 36, (uint32_t)sh.KC);
+      st_u32(o + 40, c.ref_bytes); st_u32(o + 44, (uint32_t)sh.window);
+      st_u64(o + 48, c.n_lit); st_u64(o + 56, c.n_match); st_u64(o + 64, c.n_out); st_u64(o + 72, c.n_chunks);
+      st_u64(o + 88, c.off_seg); st_u64(o + 96, c.off_bitmap); st_u64(o + 104, c.off_chunks);
+      st_u64(o + 112, c.off_refs); st_u64(o + 120, c.off_bits); st_u64(o + 136, 0ull);
+      if (status == EBC_OK) {
+        st_u64(o + 80, c.words);
+        st_u64(o + 128, c.total);
+      }
+    }
+    if (status == EBC_OK) {   // the alignment padding after each variable-length section
+      const unsigned long long bm_end = c.off_bitmap + (unsigned long long)T * (unsigned long long)div_up(n, 32) * 4ull;
+      for (unsigned long long i = bm_end; i < c.off_chunks; ++i) o[i] = 0;
+      for (unsigned long long i = c.off_chunks + c.n_chunks * 2ull; i < c.off_refs; ++i) o[i] = 0;
+      for (unsigned long long i = c.off_refs + c.n_match * c.ref_bytes; i < c.off_bits; ++i) o[i] = 0;
+    }
+  }
+  if (sh.nseg == 0 && status == EBC_OK) {   // an empty batch: every table record is eb and zeros
+    const int per = (int)(kTableRecBytes / 4);
+    const long long nrec = (long long)sh.R * T * per;
+    for (long long i = tid; i < nrec; i += blockDim.x) {
+      const int r = (int)(i / ((long long)T * per));
+      const int t = (int)((i / per) % T);
+      const int k = (int)(i % per);
+      uint32_t* rec = reinterpret_cast<uint32_t*>(out + s_size[r] + kHeaderBytes + (size_t)t * kTableRecBytes);
+      rec[k] = k == 0 ? __float_as_uint(ep.eb[t]) : 0u;
+    }
+  }
+  if (tid == 0) {
+    g->n_lit = s_sum[0]; g->n_match = s_sum[1]; g->n_out = s_sum[2]; g->n_chunks = s_sum[3];
+    g->words = s_sum[4];
+    g->total = total;
+    *out_bytes = total;
+    if (status != EBC_OK) record_error(g, status);
+    g->cstat = status_word(epoch, status);
+    g->done = 0u;
+  }
+}
+
 // Ascending bitonic sort of one 64-bit key per thread over a 256-thread CTA:
 // partners closer than a warp trade through shuffles, the others through
 // shared memory.  Returns the key of rank threadIdx.x.
@@ -616,7 +726,7 @@ __device__ __forceinline__ unsigned long long bitonic_sort256(unsigned long long
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w, uint8_t* __restrict__ out,
                                                    unsigned long long cap, unsigned long long* out_bytes,
-                                                   uint32_t epoch) {
+                                                   unsigned long long* chunk_off, uint32_t epoch) {
   pdl_enter();
   __shared__ uint32_t s_f[256], s_lw[256], s_nodew[256];
   __shared__ unsigned long long s_key[256];
@@ -627,14 +737,17 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2];
   __shared__ int s_maxlen, s_last;
   __shared__ uint4 s_warp[8];
+  __shared__ uint4 s_cpre[kMaxSlices + 1], s_wpre[kMaxSlices + 1];   // unit prefixes at container starts
   const int tid = threadIdx.x;
-  const int t = blockIdx.x;
+  const int u = blockIdx.x;   // unit: slice u / T, table u % T
   const int T = sh.T;
+  const int U = sh.U;
   Glob* g = w.glob;
 
-  if (t < T) {
+  if (u < U) {
+    const int t = u % T;
     // (with no segments, k_quantize did not run and the accumulators are stale)
-    const uint32_t f0 = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)t * 256 + tid]) : 0u;
+    const uint32_t f0 = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)u * 256 + tid]) : 0u;
     s_f[tid] = f0;
     const bool raw = w.modes && (w.modes[t] & kModeRawCodes);   // every code 8 bits: no Huffman
     if (raw) s_len[tid] = 8;
@@ -727,7 +840,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       code = s_next[L];
       for (int j = 0; j < tid; ++j) code += (s_len[j] == L);
     }
-    w.tabcode[(size_t)t * 256 + tid] = (code << 8) | L;
+    w.tabcode[(size_t)u * 256 + tid] = (code << 8) | L;
     {   // bits of the table's literal codes, plus the raw bits of its outliers (symbol 0)
       unsigned long long sum = (unsigned long long)f0 * L + (tid == 0 ? 32ull * f0 : 0ull);
 #pragma unroll
@@ -737,23 +850,16 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       if (tid == 0) {
         unsigned long long tot = 0;
         for (int k = 0; k < 8; ++k) tot += s_bits64[k];
-        w.tab_bits[t] = tot;
+        w.tab_bits[u] = tot;
+        const uint4 tc = sh.nseg > 0 ? __ldcg(&w.tab_cnt[u]) : make_uint4(0, 0, 0, 0);
+        w.tab_rec[u] = make_uint4(__float_as_uint(ep.eb[t]), tc.x, tc.y, tc.z);   // head of the table record
       }
     }
-    uint8_t* rec = out + kHeaderBytes + (size_t)t * kTableRecBytes;
-    rec[16 + tid] = (uint8_t)L;
-    if (tid == 0) {
-      const uint4 tc = sh.nseg > 0 ? __ldcg(&w.tab_cnt[t]) : make_uint4(0, 0, 0, 0);
-      st_u32(rec + 0, __float_as_uint(ep.eb[t]));
-      st_u32(rec + 4, tc.x);
-      st_u32(rec + 8, tc.y);
-      st_u32(rec + 12, tc.z);
-    }
     if (sh.fold && sh.nseg > 0) {
-      // this table's segments: bits = sum over codes of count * length (+32 raw bits per outlier),
-      // one warp per segment; then offsets relative to the table (a scan) and the table's totals
+      // this unit's segments: bits = sum over codes of count * length (+32 raw bits per outlier),
+      // one warp per segment; then offsets relative to the unit (a scan) and the unit's totals
       const int warp = tid >> 5, lane = tid & 31;
-      const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)t * 256) + lane * 2;
+      const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * 256) + lane * 2;
       __syncthreads();   // tabcode of this table is written
       const uint4 c0 = __ldcg(cp), c1 = __ldcg(cp + 1);
       constexpr int kBatch = 4;   // segments whose histograms are loaded together
@@ -763,7 +869,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
         for (int q = 0; q < kBatch; ++q) {
           const int i = i0 + 8 * q;
           if (i < sh.nseg) {
-            const int seg = t * sh.nseg + i;
+            const int seg = u * sh.nseg + i;
             const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * 256) + lane * 2;
             h0[q] = __ldcg(hp);
             h1[q] = __ldcg(hp + 1);
@@ -789,85 +895,65 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       v.w = 0;
       uint4 tot;
       const uint4 ex = block_excl_scan4(v, &tot, s_warp);
-      if (tid < sh.nseg) w.seg_base[t * sh.nseg + tid] = make_uint4(ex.x, ex.y, ex.z, segbits);
-      if (tid == 0) w.seg_desc[t] = tot;
+      if (tid < sh.nseg) w.seg_base[u * sh.nseg + tid] = make_uint4(ex.x, ex.y, ex.z, segbits);
+      if (tid == 0) w.seg_desc[u] = tot;
     }
   }
 
-  // ---- the last CTA: section layout and header ----
+  // ---- the last CTA: container layouts and headers ----
   __threadfence();
   __syncthreads();
   if (tid == 0) s_last = atomicAdd(&g->done, 1u) == gridDim.x - 1;
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  uint4 sum = make_uint4(0, 0, 0, 0);
-  for (int base = 0; base < T; base += 256) {
+  // exclusive scans over the units of their counts (and, folded, of their bitstream sizes); the
+  // values at each container's first unit, and the totals, are kept
+  const bool have = sh.nseg > 0;
+  for (int i = tid; i <= sh.R; i += 256) s_cpre[i] = s_wpre[i] = make_uint4(0, 0, 0, 0);   // (T = 0: no units)
+  __syncthreads();
+  uint4 carry = make_uint4(0, 0, 0, 0), wcarry = make_uint4(0, 0, 0, 0);
+  for (int base = 0; base < U; base += 256) {
     const int i = base + tid;
-    const uint4 v = i < T && sh.nseg > 0 ? __ldcg(&w.tab_cnt[i]) : make_uint4(0, 0, 0, 0);
+    const uint4 v = i < U && have ? __ldcg(&w.tab_cnt[i]) : make_uint4(0, 0, 0, 0);
     uint4 tot;
-    block_excl_scan4(v, &tot, s_warp);
-    sum = add4(sum, tot);
-  }
-  uint4 fsum = make_uint4(0, 0, 0, 0);   // folded layout: table bases and the bitstream size
-  if (sh.fold && sh.nseg > 0) {
-    for (int base = 0; base < T; base += 256) {
-      const int i = base + tid;
-      const uint4 v = i < T ? __ldcg(&w.seg_desc[i]) : make_uint4(0, 0, 0, 0);
-      uint4 tot;
-      const uint4 ex = block_excl_scan4(v, &tot, s_warp);
-      if (i < T) w.tile_base[i] = add4(fsum, ex);
-      fsum = add4(fsum, tot);
+    const uint4 ex = add4(carry, block_excl_scan4(v, &tot, s_warp));
+    if (i < U && i % T == 0) s_cpre[i / T] = ex;
+    carry = add4(carry, tot);
+    if (sh.fold && have) {
+      const uint4 d = i < U ? __ldcg(&w.seg_desc[i]) : make_uint4(0, 0, 0, 0);
+      const uint4 wex = add4(wcarry, block_excl_scan4(d, &tot, s_warp));
+      if (i < U) w.tile_base[i] = wex;
+      if (i < U && i % T == 0) s_wpre[i / T] = wex;
+      wcarry = add4(wcarry, tot);
     }
   }
   if (tid == 0) {
-    const unsigned long long lits = sum.x, matches = sum.y, outl = sum.z, chunks = sum.w;
-    const unsigned long long nsegT = (unsigned long long)T * sh.nseg;
-    const unsigned long long off_seg = kHeaderBytes + (unsigned long long)T * kTableRecBytes;
-    const unsigned long long off_bitmap = off_seg + nsegT * kSegRecBytes;
-    const unsigned long long bm_bytes = (unsigned long long)T * sh.nw * 4ull;
-    const unsigned long long off_chunks = off_bitmap + pad16(bm_bytes);
-    const unsigned long long off_refs = off_chunks + pad16(chunks * 2ull);
-    const unsigned long long off_bits = off_refs + pad16(matches * (unsigned long long)sh.ref_bytes);
-    g->n_lit = lits; g->n_match = matches; g->n_out = outl; g->n_chunks = chunks;
-    g->off_seg = off_seg; g->off_bitmap = off_bitmap; g->off_chunks = off_chunks; g->off_refs = off_refs;
-    g->off_bits = off_bits;
-    st_u32(out + 0, kMagic); st_u32(out + 4, kFormatVersion); st_u64(out + 8, (unsigned long long)sh.B);
-    st_u32(out + 16, (uint32_t)T); st_u32(out + 20, (uint32_t)sh.D); st_u32(out + 24, kRadius);
-    st_u32(out + 28, kLmax); st_u32(out + 32, (uint32_t)sh.SB); st_u32(out + 36, (uint32_t)sh.KC);
-    st_u32(out + 40, (uint32_t)sh.ref_bytes); st_u32(out + 44, (uint32_t)sh.window);
-    st_u64(out + 48, lits); st_u64(out + 56, matches); st_u64(out + 64, outl); st_u64(out + 72, chunks);
-    st_u64(out + 88, off_seg); st_u64(out + 96, off_bitmap); st_u64(out + 104, off_chunks);
-    st_u64(out + 112, off_refs); st_u64(out + 120, off_bits); st_u64(out + 136, 0ull);
-    int status = EBC_OK;
-    if (off_bits > cap) {
-      status = EBC_ERR_CAPACITY;
-    } else {
-      // zero the alignment padding after each variable-length section
-      for (unsigned long long i = off_bitmap + bm_bytes; i < off_chunks; ++i) out[i] = 0;
-      for (unsigned long long i = off_chunks + chunks * 2ull; i < off_refs; ++i) out[i] = 0;
-      for (unsigned long long i = off_refs + matches * sh.ref_bytes; i < off_bits; ++i) out[i] = 0;
+    s_cpre[sh.R] = carry;
+    s_wpre[sh.R] = wcarry;
+  }
+  __syncthreads();
+  ContLay c{};
+  if (tid < sh.R) {
+    const uint4 a = s_cpre[tid], b = s_cpre[tid + 1];
+    c.n_lit = b.x - a.x;
+    c.n_match = b.y - a.y;
+    c.n_out = b.z - a.z;
+    c.n_chunks = b.w - a.w;
+    const uint4 wa = s_wpre[tid], wb = s_wpre[tid + 1];
+    c.words = wb.x - wa.x;   // folded (else completed by k_layout)
+    c.word0 = wa.x;
+    c.chunk0 = wa.y;
+    c.match0 = wa.z;
+  }
+  if (sh.fold || !have) {
+    finish_containers(sh, ep, w, c, out, cap, out_bytes, chunk_off, epoch);
+  } else {
+    if (tid < sh.R) w.cont[tid] = c;   // the counts; k_layout adds the bitstream sizes
+    if (tid == 0) {
+      g->cstat = status_word(epoch, EBC_OK);
+      g->done = 0u;
     }
-    if (nsegT == 0) {   // no segments: no bitstream, k_emit is not launched
-      g->words = 0;
-      g->total = off_bits;
-      st_u64(out + 80, 0ull);
-      st_u64(out + 128, off_bits);
-      *out_bytes = off_bits;
-    } else if (sh.fold) {   // the bitstream size is known here (else k_layout completes it)
-      const unsigned long long words = fsum.x, total = off_bits + 4ull * words;
-      g->words = words;
-      g->total = total;
-      *out_bytes = total;
-      if (status == EBC_OK && total > cap) status = EBC_ERR_CAPACITY;
-      if (status == EBC_OK) {
-        st_u64(out + 80, words);
-        st_u64(out + 128, total);
-      }
-    }
-    if (status != EBC_OK) record_error(g, status);
-    g->cstat = status_word(epoch, status);
-    g->done = 0u;
   }
 }
 
@@ -907,8 +993,9 @@ __device__ __forceinline__ uint32_t valid_mask(int64_t B, int64_t row0, int wi) 
 // bases (an exclusive scan) and completes the header (bitstream words, total
 // size) and the capacity check.  No CTA waits on another.
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __restrict__ out, unsigned long long cap,
-                                                 unsigned long long* out_bytes, uint32_t epoch) {
+__global__ void __launch_bounds__(256) k_layout(Shape sh, EbParams ep, Work w, uint8_t* __restrict__ out,
+                                                 unsigned long long cap, unsigned long long* out_bytes,
+                                                 unsigned long long* chunk_off, uint32_t epoch) {
   pdl_enter();
   __shared__ uint4 s_agg[8];
   __shared__ uint4 s_warp[8];
@@ -917,14 +1004,14 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int tile = blockIdx.x;
   const int ntiles = gridDim.x;
-  const int nsegT = sh.T * sh.nseg;
+  const int nsegT = sh.U * sh.nseg;
   const int seg = tile * 8 + warp;
   uint4 a = make_uint4(0, 0, 0, 0);   // {words, chunks, matches, -}
   uint32_t bits = 0;
   if (seg < nsegT) {
-    const int t = seg / sh.nseg;
+    const int u = seg / sh.nseg;
     const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * 256) + lane * 2;
-    const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)t * 256) + lane * 2;
+    const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * 256) + lane * 2;
     const uint4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1), c0 = __ldcg(cp), c1 = __ldcg(cp + 1);
     const uint4 cnt = __ldcg(&w.seg_cnt[seg]);
     bits = h0.x * (c0.x & 0xffu) + h0.y * (c0.y & 0xffu) + h0.z * (c0.z & 0xffu) + h0.w * (c0.w & 0xffu) +
@@ -962,23 +1049,28 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, Work w, uint8_t* __res
     if (i < ntiles) w.tile_base[i] = add4(carry, ex);
     carry = add4(carry, tot);
   }
-  if (tid == 0) {
-    const unsigned long long words = carry.x;
-    const unsigned long long off_bits = __ldcg(&g->off_bits);
-    const unsigned long long total = off_bits + 4ull * words;
-    g->words = words;
-    g->total = total;
-    *out_bytes = total;
-    if (__ldcg(&g->cstat) == status_word(epoch, EBC_OK)) {
-      st_u64(out + 80, words);
-      st_u64(out + 128, total);
+  __syncthreads();
+  // each container's bitstream: the absolute bases at its first segment and after its last
+  ContLay c{};
+  if (tid < sh.R) {
+    c = w.cont[tid];   // counts, from k_codebook
+    uint4 at[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const int i = (tid + e) * sh.T * sh.nseg;   // first segment of container tid + e
+      if (i >= nsegT) {
+        at[e] = carry;
+      } else {
+        const uint4 tb = __ldcg(&w.tile_base[i >> 3]), rel = __ldcg(&w.seg_base[i]);
+        at[e] = make_uint4(tb.x + rel.x, tb.y + rel.y, tb.z + rel.z, 0u);
+      }
     }
-    if (total > cap) {
-      record_error(g, EBC_ERR_CAPACITY);
-      g->cstat = status_word(epoch, EBC_ERR_CAPACITY);
-    }
-    g->done = 0u;
+    c.words = at[1].x - at[0].x;
+    c.word0 = at[0].x;
+    c.chunk0 = at[0].y;
+    c.match0 = at[0].z;
   }
+  finish_containers(sh, ep, w, c, out, cap, out_bytes, chunk_off, epoch);
 }
 
 // ---------------------------------------------------------------------------
@@ -1003,7 +1095,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   constexpr int kRPT = (G::kSB + 255) / 256;   // rows (and ranks) per thread
   constexpr uint32_t kSmemWords = (uint32_t)G::kSegSyms * 3u / 4u;
   extern __shared__ __align__(16) uint32_t s_bits[];
-  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4];   // the segment's codes, row-major
+  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4 + 4];   // the segment's codes, row-major
   __shared__ uint32_t s_code[256];
   __shared__ uint32_t s_bm[G::kBmWords];      // match bits
   __shared__ uint32_t s_lit[G::kBmWords];     // literal bits
@@ -1013,53 +1105,70 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   __shared__ uint4 s_warp[8];
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // segment s of unit u = (slice r, table t): rows lrow0 .. of the slice, b0 + lrow0 .. of the batch
   const int seg = blockIdx.x;
-  const int t = seg / sh.nseg;
-  const int s = seg - t * sh.nseg;
-  const int64_t B = sh.B;
+  const int u = seg / sh.nseg;
+  const int s = seg - u * sh.nseg;
+  const int r = u / sh.T;
+  const int t = u - r * sh.T;
   const int T = sh.T;
-  const int64_t row0 = (int64_t)s * G::kSB;
+  const int64_t b0 = slice_row0(sh, r);
+  const int64_t nr = slice_rows(sh, r);                     // rows of the slice
+  const int64_t lrow0 = (int64_t)s * G::kSB;
+  const int64_t row0 = b0 + lrow0;
+  const int nseg_r = div_up(nr, G::kSB), nw_r = div_up(nr, 32);
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
+  const int so = D >= 16 ? 0 : (int)(((size_t)row0 * D) & 15u) / 4;   // word offset of the codes in s_sym
 
   // ---- every global read, issued together ----
   {   // the dedup tables are not read again: empty them for the next call (a share per CTA)
-    const unsigned long long n2 = (unsigned long long)sh.T * sh.S / 2;   // slot pairs (S is even)
+    const unsigned long long n2 = (unsigned long long)sh.U * sh.S / 2;   // slot pairs (S is even)
     const unsigned long long per = (n2 + gridDim.x - 1) / gridDim.x;
     const unsigned long long lo = per * blockIdx.x, hi = lo + per < n2 ? lo + per : n2;
     uint4* sl = reinterpret_cast<uint4*>(w.slots);
     for (unsigned long long i = lo + tid; i < hi; i += 256) sl[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
   }
+  const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
+  const ContLay cl = w.cont[r];
+  const uint32_t mycode = __ldcg(&w.tabcode[(size_t)u * 256 + tid]);
+  if (s == 0 && writable) {   // the unit's table record: eb, counts, code lengths
+    uint8_t* rec = out + cl.base + kHeaderBytes + (size_t)t * kTableRecBytes;
+    rec[16 + tid] = (uint8_t)(mycode & 0xffu);
+    if (tid == 0) *reinterpret_cast<uint4*>(rec) = __ldcg(&w.tab_rec[u]);
+  }
+  if (s >= nseg_r) return;   // past the end of a shorter slice: no rows
   const uint4 sbr = __ldcg(&w.seg_base[seg]);       // {words, chunks, matches} within its group, bits
-  const uint4 tb = __ldcg(&w.tile_base[sh.fold ? t : seg >> 3]);   // absolute base of its group
-  const uint4 sb = make_uint4(tb.x + sbr.x, tb.y + sbr.y, tb.z + sbr.z, sbr.w);
-  const uint32_t mycode = __ldcg(&w.tabcode[(size_t)t * 256 + tid]);
+  const uint4 tb = __ldcg(&w.tile_base[sh.fold ? u : seg >> 3]);   // absolute base of its group
+  // the segment's bases within its container
+  const uint4 sb = make_uint4(tb.x + sbr.x - cl.word0, tb.y + sbr.y - cl.chunk0, tb.z + sbr.z - cl.match0, sbr.w);
   uint32_t bmw = 0;
   if (tid < G::kBmWords) {
     const int64_t wi = (int64_t)s * G::kBmWords + tid;
-    bmw = wi < sh.nw ? __ldcg(&w.bitmap[(size_t)t * sh.nw + wi]) : 0u;
+    bmw = wi < sh.nw ? __ldcg(&w.bitmap[(size_t)u * sh.nw + wi]) : 0u;
   }
   {   // rows row0 .. row0 + SB are contiguous; the table stride is padded to 16 bytes
-    const int64_t nrows = B - row0 < G::kSB ? B - row0 : G::kSB;
-    const int nq = (int)((nrows * D + 15) / 16);
-    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D);
+    const int64_t nrows = nr - lrow0 < G::kSB ? nr - lrow0 : G::kSB;
+    const int nq = (int)((so * 4 + nrows * D + 15) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D - so * 4);
     uint4* dst = reinterpret_cast<uint4*>(s_sym);
     for (int i = tid; i < nq; i += 256) dst[i] = __ldcg(src + i);
   }
   uint32_t refw[kRPT];
 #pragma unroll
   for (int k = 0; k < kRPT; ++k) {
-    const int r = k * 256 + tid;
-    refw[k] = (r < G::kSB && row0 + r < B) ? __ldcg(&w.ref[(size_t)t * B + row0 + r]) : 0u;
+    const int rr = k * 256 + tid;
+    refw[k] = (rr < G::kSB && lrow0 + rr < nr) ? __ldcg(&w.ref[(size_t)t * sh.B + row0 + rr]) : 0u;
   }
-  const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
-  const unsigned long long off_bits = __ldcg(&g->off_bits), off_chunks = __ldcg(&g->off_chunks);
-  const unsigned long long off_refs = __ldcg(&g->off_refs);
-  const unsigned long long off_seg = __ldcg(&g->off_seg), off_bitmap = __ldcg(&g->off_bitmap);
+  const unsigned long long cbase = cl.base;
+  const unsigned long long off_bits = cbase + cl.off_bits, off_chunks = cbase + cl.off_chunks;
+  const unsigned long long off_refs = cbase + cl.off_refs;
+  const unsigned long long off_seg = cbase + cl.off_seg, off_bitmap = cbase + cl.off_bitmap;
+  const int ref_bytes = (int)cl.ref_bytes;
 
   s_code[tid] = mycode;
   if (tid < G::kBmWords) {
     s_bm[tid] = bmw;
-    s_lit[tid] = ~bmw & valid_mask(B, row0, tid);
+    s_lit[tid] = ~bmw & valid_mask(nr, lrow0, tid);
   }
   const uint32_t bits = sb.w;
   const uint32_t nwords = ((bits + 127u) >> 7) * 4u;
@@ -1083,9 +1192,9 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < kRPT; ++k) {
-    const int r = k * 256 + tid;
-    if (r < G::kSB && ((s_lit[r >> 5] >> (r & 31)) & 1u))
-      s_litrow[(s_pre[r >> 5] & 0xffffu) + __popc(s_lit[r >> 5] & ((1u << (r & 31)) - 1u))] = (uint16_t)r;
+    const int rr = k * 256 + tid;
+    if (rr < G::kSB && ((s_lit[rr >> 5] >> (rr & 31)) & 1u))
+      s_litrow[(s_pre[rr >> 5] & 0xffffu) + __popc(s_lit[rr >> 5] & ((1u << (rr & 31)) - 1u))] = (uint16_t)rr;
   }
   __syncthreads();
   const uint32_t nsteps = (nlit + G::kRPS - 1) / G::kRPS;
@@ -1095,11 +1204,11 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   for (uint32_t i = warp; i < nsteps; i += 8) {
     const uint32_t k = i * G::kRPS + lane / G::kLPR;   // literal rank of this lane's row
     const bool act = k < nlit;
-    const int r = act ? s_litrow[k] : 0;
+    const int rr = act ? s_litrow[k] : 0;
     uint32_t nb = 0;
 #pragma unroll
     for (int j = 0; j < G::kSPR; ++j) {
-      const uint32_t v = act ? s_sym[r * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
+      const uint32_t v = act ? s_sym[so + rr * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const uint32_t c = (v >> (8 * q)) & 0xffu;
@@ -1146,12 +1255,12 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
     for (uint32_t i = warp; i < nsteps; i += 8) {
       const uint32_t k = i * G::kRPS + lane / G::kLPR;
       const bool act = k < nlit;
-      const int r = act ? s_litrow[k] : 0;
-      const int64_t b = row0 + r;
+      const int rr = act ? s_litrow[k] : 0;
+      const int64_t b = row0 + rr;
       uint32_t p = act ? s_rowoff[k] : 0u;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        const uint32_t v = act ? s_sym[r * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
+        const uint32_t v = act ? s_sym[so + rr * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
         // the lane's 4 codes joined into one string (right-aligned), if short and outlier-free
         uint32_t nb = 0;
         unsigned long long str = 0;
@@ -1210,23 +1319,24 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
     }
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int r = k * 256 + tid;
-      if (r < G::kSB && row0 + r < B && ((s_bm[r >> 5] >> (r & 31)) & 1u)) {
-        const uint32_t mrank = (s_pre[r >> 5] >> 16) + __popc(s_bm[r >> 5] & ((1u << (r & 31)) - 1u));
-        const unsigned long long o = off_refs + (unsigned long long)sh.ref_bytes * (sb.z + mrank);
-        if (sh.window) out[o] = (uint8_t)((uint32_t)(row0 + r) - refw[k]);   // distance back, 1..window
-        else if (sh.ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)refw[k];
-        else *reinterpret_cast<uint32_t*>(out + o) = refw[k];
+      const int rr = k * 256 + tid;
+      if (rr < G::kSB && lrow0 + rr < nr && ((s_bm[rr >> 5] >> (rr & 31)) & 1u)) {
+        const uint32_t mrank = (s_pre[rr >> 5] >> 16) + __popc(s_bm[rr >> 5] & ((1u << (rr & 31)) - 1u));
+        const unsigned long long o = off_refs + (unsigned long long)ref_bytes * (sb.z + mrank);
+        const uint32_t lref = refw[k] - (uint32_t)b0;   // the reference row within the slice
+        if (sh.window) out[o] = (uint8_t)((uint32_t)(row0 + rr) - refw[k]);   // distance back, 1..window
+        else if (ref_bytes == 2) *reinterpret_cast<uint16_t*>(out + o) = (uint16_t)lref;
+        else *reinterpret_cast<uint32_t*>(out + o) = lref;
       }
     }
-    if (tid == 0) {
-      uint32_t* rec = reinterpret_cast<uint32_t*>(out + off_seg + (unsigned long long)seg * kSegRecBytes);
+    if (tid == 0) {   // record t * nseg_r + s of the container
+      uint32_t* rec = reinterpret_cast<uint32_t*>(out + off_seg + ((unsigned long long)t * nseg_r + s) * kSegRecBytes);
       rec[0] = sb.x; rec[1] = sb.y; rec[2] = sb.z; rec[3] = bits;
     }
     if (tid < G::kBmWords) {
       const int64_t wi = (int64_t)s * G::kBmWords + tid;
-      if (wi < sh.nw)
-        *reinterpret_cast<uint32_t*>(out + off_bitmap + 4ull * ((size_t)t * sh.nw + wi)) = s_bm[tid];
+      if (wi < nw_r)
+        *reinterpret_cast<uint32_t*>(out + off_bitmap + 4ull * ((size_t)t * nw_r + wi)) = s_bm[tid];
     }
   }
 }
@@ -1236,9 +1346,10 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
 // ---------------------------------------------------------------------------
 template <int D, typename In>
 static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
-                              unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                              cudaStream_t st, Prof* prof, const CUtensorMap* xmap) {
-  const unsigned grid = (unsigned)(sh.T * sh.nseg);
+                              unsigned long long cap, unsigned long long* out_bytes, unsigned long long* chunk_off,
+                              uint32_t epoch, cudaStream_t st, Prof* prof, const CUtensorMap* xmap) {
+  const unsigned grid = (unsigned)(sh.U * sh.nseg);          // (unit, segment) pairs
+  const unsigned qsegs = (unsigned)(sh.T * sh.qseg);         // (table, segment) pairs of the whole batch
   if (grid) {
     // persistent quantize: as many CTAs as fit at once (two input stages each), at most one per segment
     static int per_sm = -1;
@@ -1250,7 +1361,7 @@ static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, 
         per_sm = 1;
     }
     unsigned qgrid = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm);
-    if (qgrid > grid) qgrid = grid;
+    if (qgrid > qsegs) qgrid = qsegs;
     prof_begin(prof, "k_quantize", st);
     launch_k(k_quantize<D, In>, qgrid, 256, smem, st, *xmap, sh, ep, w);
     prof_end(prof, st);
@@ -1260,12 +1371,12 @@ static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, 
     prof_end(prof, st);
   }
   prof_begin(prof, "k_codebook", st);
-  launch_k(k_codebook, sh.T > 0 ? sh.T : 1, 256, 0, st, sh, ep, w, out, cap, out_bytes, epoch);
+  launch_k(k_codebook, sh.U > 0 ? sh.U : 1, 256, 0, st, sh, ep, w, out, cap, out_bytes, chunk_off, epoch);
   prof_end(prof, st);
   if (grid) {
     if (!sh.fold) {
       prof_begin(prof, "k_layout", st);
-      launch_k(k_layout, (grid + 7) / 8, 256, 0, st, sh, w, out, cap, out_bytes, epoch);
+      launch_k(k_layout, (grid + 7) / 8, 256, 0, st, sh, ep, w, out, cap, out_bytes, chunk_off, epoch);
       prof_end(prof, st);
     }
     prof_begin(prof, "k_emit", st);
@@ -1301,10 +1412,10 @@ static cudaError_t make_x_map(CUtensorMap* map, const In* x, const Shape& sh) {
 
 template <typename In>
 static cudaError_t launch_compress_t(const In* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
-                                    unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                                    cudaStream_t st, Prof* prof) {
+                                    unsigned long long cap, unsigned long long* out_bytes,
+                                    unsigned long long* chunk_off, uint32_t epoch, cudaStream_t st, Prof* prof) {
   CUtensorMap xmap;
-  if (sh.T > 0 && sh.nseg > 0) {
+  if (sh.T > 0 && sh.qseg > 0) {
     cudaError_t e = cudaSuccess;
     switch (sh.D) {
       case 4: e = make_x_map<4, In>(&xmap, x, sh); break;
@@ -1320,24 +1431,26 @@ static cudaError_t launch_compress_t(const In* x, const Shape& sh, const EbParam
     if (e != cudaSuccess) return e;
   }
   switch (sh.D) {
-    case 4: launch_compress_d<4, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 8: launch_compress_d<8, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 16: launch_compress_d<16, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 32: launch_compress_d<32, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 64: launch_compress_d<64, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 128: launch_compress_d<128, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 256: launch_compress_d<256, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
-    case 512: launch_compress_d<512, In>(x, sh, ep, w, out, cap, out_bytes, epoch, st, prof, &xmap); break;
+    case 4: launch_compress_d<4, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 8: launch_compress_d<8, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 16: launch_compress_d<16, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 32: launch_compress_d<32, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 64: launch_compress_d<64, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 128: launch_compress_d<128, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 256: launch_compress_d<256, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 512: launch_compress_d<512, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_compress(const void* x, bool bf16, const Shape& sh, const EbParams& ep, const Work& w,
-                            uint8_t* out, unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                            cudaStream_t st, Prof* prof) {
-  return bf16 ? launch_compress_t(static_cast<const uint16_t*>(x), sh, ep, w, out, cap, out_bytes, epoch, st, prof)
-              : launch_compress_t(static_cast<const float*>(x), sh, ep, w, out, cap, out_bytes, epoch, st, prof);
+                            uint8_t* out, unsigned long long cap, unsigned long long* out_bytes,
+                            unsigned long long* chunk_off, uint32_t epoch, cudaStream_t st, Prof* prof) {
+  return bf16 ? launch_compress_t(static_cast<const uint16_t*>(x), sh, ep, w, out, cap, out_bytes, chunk_off, epoch,
+                                  st, prof)
+              : launch_compress_t(static_cast<const float*>(x), sh, ep, w, out, cap, out_bytes, chunk_off, epoch,
+                                  st, prof);
 }
 
 template <int D>

@@ -47,42 +47,52 @@ __device__ __forceinline__ bool eb_usable(float eb) {
 
 struct Layout {
   unsigned long long n_lit, n_match, n_out, n_chunks, words;
-  unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
+  unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;   // relative to base
+  unsigned long long base;          // the container's first byte in the input
+  unsigned long long row0, n;       // the batch rows it restores: [row0, row0 + n)
   unsigned int window, ref_bytes;   // dedup window (0 = whole batch) and bytes per reference
+  unsigned int nseg, nw;            // segments and bitmap words per table
+  unsigned int chunk0, match0;      // chunks and matches of the containers before it
 };
 
-// Header checks (h: the 144 header bytes in shared memory).  Returns an EBC_*
-// code; on success *L holds the section layout recomputed from the counts.
-__device__ int parse_header(const uint8_t* h, unsigned long long in_bytes, const Shape& sh, Layout* L) {
+// Header checks of a container of n rows and `bytes` bytes (h: its first
+// byte).  Returns an EBC_* code; on success *L holds the section layout
+// recomputed from the counts.
+__device__ int parse_header(const uint8_t* h, unsigned long long bytes, unsigned long long n, const Shape& sh,
+                            Layout* L) {
   const int T = sh.T;
-  const unsigned long long nvec = (unsigned long long)sh.B * (unsigned long long)T;
-  if (in_bytes < kHeaderBytes) return EBC_ERR_CORRUPT;
+  const unsigned long long nvec = n * (unsigned long long)T;
+  if (bytes < kHeaderBytes) return EBC_ERR_CORRUPT;
   if (ld32(h) != kMagic || ld32(h + 4) != kFormatVersion) return EBC_ERR_CORRUPT;
-  if (ld64(h + 8) != (unsigned long long)sh.B || ld32(h + 16) != (uint32_t)T || ld32(h + 20) != (uint32_t)sh.D)
+  if (ld64(h + 8) != n || ld32(h + 16) != (uint32_t)T || ld32(h + 20) != (uint32_t)sh.D)
     return EBC_ERR_INVALID_ARG;
   if (ld32(h + 24) != (uint32_t)kRadius || ld32(h + 28) != (uint32_t)kLmax || ld32(h + 32) != (uint32_t)sh.SB ||
       ld32(h + 36) != (uint32_t)sh.KC || ld32(h + 44) > (uint32_t)kMaxWindow)
     return EBC_ERR_CORRUPT;
+  L->n = n;
+  L->nseg = (unsigned int)div_up((int64_t)n, sh.SB);
+  L->nw = (unsigned int)div_up((int64_t)n, 32);
   L->window = ld32(h + 44);
-  L->ref_bytes = L->window ? 1u : (uint32_t)sh.ref_bytes;   // windowed references are one-byte distances
+  L->ref_bytes = (unsigned int)ref_bytes_of((int64_t)n, (int)L->window);   // windowed: one-byte distances
   if (ld32(h + 40) != L->ref_bytes) return EBC_ERR_CORRUPT;
   L->n_lit = ld64(h + 48);
   L->n_match = ld64(h + 56);
   L->n_out = ld64(h + 64);
   L->n_chunks = ld64(h + 72);
   L->words = ld64(h + 80);
-  if (L->n_lit + L->n_match != nvec || L->n_lit > nvec || L->n_chunks > nvec ||
+  if (L->n_lit + L->n_match != nvec || L->n_lit > nvec ||
+      L->n_chunks > (unsigned long long)T * L->nseg * (unsigned long long)(sh.SB / sh.KC) ||
       L->n_out > nvec * (unsigned long long)sh.D || L->words > (1ull << 34))
     return EBC_ERR_CORRUPT;
   L->off_seg = kHeaderBytes + (unsigned long long)T * kTableRecBytes;
-  L->off_bitmap = L->off_seg + (unsigned long long)T * sh.nseg * kSegRecBytes;
-  L->off_chunks = L->off_bitmap + dpad16((unsigned long long)T * sh.nw * 4ull);
+  L->off_bitmap = L->off_seg + (unsigned long long)T * L->nseg * kSegRecBytes;
+  L->off_chunks = L->off_bitmap + dpad16((unsigned long long)T * L->nw * 4ull);
   L->off_refs = L->off_chunks + dpad16(L->n_chunks * 2ull);
   L->off_bits = L->off_refs + dpad16(L->n_match * (unsigned long long)L->ref_bytes);
   L->total = L->off_bits + L->words * 4ull;
   if (ld64(h + 88) != L->off_seg || ld64(h + 96) != L->off_bitmap || ld64(h + 104) != L->off_chunks ||
       ld64(h + 112) != L->off_refs || ld64(h + 120) != L->off_bits || ld64(h + 128) != L->total ||
-      ld64(h + 136) != 0ull || L->total > in_bytes)
+      ld64(h + 136) != 0ull || L->total > bytes)
     return EBC_ERR_CORRUPT;
   return EBC_OK;
 }
@@ -101,15 +111,19 @@ __device__ __forceinline__ uint32_t warp_excl(uint32_t v, uint32_t* total) {
 }
 
 // ---------------------------------------------------------------------------
-// k_dec_prep: grid T + ceil(T * nseg / 8), 256 threads.
+// k_dec_prep: grid U + ceil(U * nseg / 8), 256 threads.  Every CTA checks all
+// R headers (thread r: container r) and takes the chunk and match bases of
+// each container from a scan of their counts; a failed check stops every CTA.
 // ---------------------------------------------------------------------------
 template <int D>
 __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in, unsigned long long in_bytes,
-                                                   Shape sh, Work w, uint32_t epoch) {
+                                                   const unsigned long long* __restrict__ offs, Shape sh, Work w,
+                                                   uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
-  __shared__ __align__(16) uint8_t s_hdr[kHeaderBytes];
-  __shared__ Layout s_L;
+  __shared__ Layout s_L[8];   // the containers of this CTA's units: r_lo .. r_lo + 7
+  __shared__ uint32_t s_nc[kMaxSlices + 1], s_nm[kMaxSlices + 1], s_win[kMaxSlices];
+  __shared__ unsigned long long s_tot[4];   // literals, outliers, words, bytes of all containers
   __shared__ int s_code;
   __shared__ uint8_t s_len[256];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offset[kLmax + 2];
@@ -117,33 +131,96 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
   __shared__ uint32_t s_c0, s_c1;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = sh.T;
+  const int U = sh.U;
+  const int nsegT = U * sh.nseg;
   Glob* g = w.glob;
-  if (in_bytes >= kHeaderBytes && tid < (int)(kHeaderBytes / 16))
-    reinterpret_cast<uint4*>(s_hdr)[tid] = reinterpret_cast<const uint4*>(in)[tid];
-  __syncthreads();
+  // the containers this CTA needs
+  int r_lo;
+  if ((int)blockIdx.x < U) {
+    r_lo = (int)blockIdx.x / T;
+  } else {
+    const int seg0 = ((int)blockIdx.x - U) * 8;
+    r_lo = seg0 < nsegT ? (seg0 / sh.nseg) / T : 0;
+  }
   if (tid == 0) {
-    s_code = parse_header(s_hdr, in_bytes, sh, &s_L);
+    s_code = EBC_OK;
     s_bad = 0;
-    if (blockIdx.x == 0) {
-      if (s_code != EBC_OK) {
-        dec_fail(g, epoch, s_code);
-      } else {
-        g->n_lit = s_L.n_lit; g->n_match = s_L.n_match; g->n_out = s_L.n_out; g->n_chunks = s_L.n_chunks;
-        g->words = s_L.words; g->off_seg = s_L.off_seg; g->off_bitmap = s_L.off_bitmap;
-        g->off_chunks = s_L.off_chunks; g->off_refs = s_L.off_refs; g->off_bits = s_L.off_bits;
-        g->total = s_L.total;
-        g->window = s_L.window;
+  }
+  if (tid < 4) s_tot[tid] = 0ull;
+  __syncthreads();
+  Layout L{};
+  int code = EBC_OK;
+  if (tid < sh.R) {
+    const unsigned long long lo = offs ? offs[tid] : 0ull, hi = offs ? offs[tid + 1] : in_bytes;
+    if ((lo & 15ull) != 0ull || lo > hi || hi > in_bytes) {
+      code = EBC_ERR_CORRUPT;
+    } else {
+      uint4 hdr[kHeaderBytes / 16];   // the header, by independent 16-byte loads
+      if (hi - lo >= kHeaderBytes) {
+#pragma unroll
+        for (int k = 0; k < (int)(kHeaderBytes / 16); ++k) hdr[k] = reinterpret_cast<const uint4*>(in + lo)[k];
       }
+      code = parse_header(reinterpret_cast<const uint8_t*>(hdr), hi - lo, (unsigned long long)slice_rows(sh, tid),
+                          sh, &L);
+      L.base = lo;
+      L.row0 = (unsigned long long)slice_row0(sh, tid);
+    }
+    // counts for the scan (zero for a container that failed: its check stops the decode)
+    s_nc[tid] = code == EBC_OK ? (uint32_t)L.n_chunks : 0u;
+    s_nm[tid] = code == EBC_OK ? (uint32_t)L.n_match : 0u;
+    s_win[tid] = code == EBC_OK ? L.window : 0u;
+    if (code != EBC_OK) {
+      atomicCAS(&s_code, EBC_OK, code);
+    } else if (blockIdx.x == 0) {
+      atomicAdd(&s_tot[0], L.n_lit);
+      atomicAdd(&s_tot[1], L.n_out);
+      atomicAdd(&s_tot[2], L.words);
+      atomicAdd(&s_tot[3], L.total);
     }
   }
   __syncthreads();
+  if (tid == 0) {   // chunk and match bases of the containers; one window for all of them
+    uint32_t c = 0, m = 0;
+    for (int r = 0; r < sh.R; ++r) {
+      const uint32_t a = s_nc[r], b = s_nm[r];
+      s_nc[r] = c;
+      s_nm[r] = m;
+      c += a;
+      m += b;
+      if (s_win[r] != s_win[0] && s_code == EBC_OK) s_code = EBC_ERR_CORRUPT;
+    }
+    s_nc[sh.R] = c;
+    s_nm[sh.R] = m;
+  }
+  __syncthreads();
+  if (tid < sh.R && code == EBC_OK) {
+    L.chunk0 = s_nc[tid];
+    L.match0 = s_nm[tid];
+    if (tid >= r_lo && tid < r_lo + 8) s_L[tid - r_lo] = L;
+  }
+  __syncthreads();
+  if (blockIdx.x == 0 && tid == 0) {
+    if (s_code != EBC_OK) {
+      dec_fail(g, epoch, s_code);
+    } else {
+      g->n_match = s_nm[sh.R];
+      g->n_chunks = s_nc[sh.R];
+      g->window = s_win[0];
+      g->n_lit = s_tot[0];
+      g->n_out = s_tot[1];
+      g->words = s_tot[2];
+      g->total = s_tot[3];
+    }
+  }
   if (s_code != EBC_OK) return;
-  const Layout L = s_L;
 
-  if ((int)blockIdx.x < T) {
-    // ---- decode tables of table t ----
-    const int t = blockIdx.x;
-    const uint8_t* rec = in + kHeaderBytes + (size_t)t * kTableRecBytes;
+  if ((int)blockIdx.x < U) {
+    // ---- decode tables of unit u = (slice r, table t) ----
+    const int u = blockIdx.x;
+    const int t = u % T;
+    const Layout& Lc = s_L[0];
+    const uint8_t* cin = in + Lc.base;
+    const uint8_t* rec = cin + kHeaderBytes + (size_t)t * kTableRecBytes;
     const uint32_t len = rec[16 + tid];
     s_len[tid] = (uint8_t)len;
     if (tid < kLmax + 2) s_count[tid] = 0;
@@ -164,18 +241,25 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
         s_offset[l] = off;
         off += s_count[l];
       }
-      DecTab* dt = w.dtab + t;
+      DecTab* dt = w.dtab + u;
       dt->ebx2 = __fmul_rn(2.0f, eb);
-      // the table's chunk range (segment records are checked against each other by the segment warps)
-      const uint32_t* srec = reinterpret_cast<const uint32_t*>(in + L.off_seg);
+      // the unit's chunk range (segment records are checked against each other by the segment warps)
+      const uint32_t* srec = reinterpret_cast<const uint32_t*>(cin + Lc.off_seg);
       uint32_t c0 = 0, c1 = 0;
-      if (sh.nseg > 0) {
-        c0 = srec[4ull * ((unsigned long long)t * sh.nseg) + 1];
-        c1 = t + 1 < T ? srec[4ull * ((unsigned long long)(t + 1) * sh.nseg) + 1] : (uint32_t)L.n_chunks;
+      if (Lc.nseg > 0) {
+        c0 = srec[4ull * ((unsigned long long)t * Lc.nseg) + 1];
+        c1 = t + 1 < T ? srec[4ull * ((unsigned long long)(t + 1) * Lc.nseg) + 1] : (uint32_t)Lc.n_chunks;
       }
-      if (c0 > c1 || c1 > L.n_chunks || c1 > dec_max_chunks(sh)) s_bad = 1;
+      if (c0 > c1 || c1 > Lc.n_chunks) s_bad = 1;
+      c0 += Lc.chunk0;   // over all containers
+      c1 += Lc.chunk0;
+      if (c1 > dec_max_chunks(sh)) s_bad = 1;
       dt->chunk0 = c0;
       dt->chunk1 = c1;
+      dt->t = (uint32_t)t;
+      dt->bits_off = Lc.base + Lc.off_bits;
+      dt->n_words = Lc.words;
+      dt->row0 = Lc.row0;
       s_c0 = c0;
       s_c1 = c1;
       for (int l = 0; l <= kLmax; ++l) {
@@ -189,44 +273,45 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
       if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
       return;
     }
-    {   // this table's run slots [c0 / kDecRun + t, c1 / kDecRun + t + 1): its runs, then one empty slot at most
+    {   // this unit's run slots [c0 / kDecRun + u, c1 / kDecRun + u + 1): its runs, then one empty slot at most
       const uint32_t c0 = s_c0, c1 = s_c1;
-      const uint32_t lo = c0 / kDecRun + (uint32_t)t, hi = c1 / kDecRun + (uint32_t)t + 1u;
+      const uint32_t lo = c0 / kDecRun + (uint32_t)u, hi = c1 / kDecRun + (uint32_t)u + 1u;
       const uint32_t nruns = (c1 - c0 + kDecRun - 1) / kDecRun;
       for (uint32_t r = lo + tid; r < hi; r += 256) {
         const uint32_t k = r - lo;
         const uint32_t j0 = c0 + k * kDecRun;
-        w.runmap[r] = k < nruns ? make_uint4((uint32_t)t, j0, min(j0 + (uint32_t)kDecRun, c1), 0u)
+        w.runmap[r] = k < nruns ? make_uint4((uint32_t)u, j0, min(j0 + (uint32_t)kDecRun, c1), 0u)
                                 : make_uint4(~0u, 0u, 0u, 0u);
       }
     }
-    uint16_t* lut = w.lut + (size_t)t * (1u << kLutBits);
+    uint16_t* lut = w.lut + (size_t)u * (1u << kLutBits);
     for (int i = tid; i < (1 << kLutBits); i += 256) lut[i] = 0;
     __syncthreads();
     if (len) {
       uint32_t rank = 0;
       for (int j = 0; j < tid; ++j) rank += (s_len[j] == len);
       const uint32_t code = s_next[len] + rank;
-      w.dtab[t].sorted[s_offset[len] + rank] = (uint8_t)tid;
+      w.dtab[u].sorted[s_offset[len] + rank] = (uint8_t)tid;
       if (len <= (uint32_t)kLutBits) {
         const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
         for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(tid | (len << 8));
       }
     }
-    if (L.window && sh.nseg > 0) {
+    if (Lc.window && Lc.nseg > 0) {
       // window references: every row's source (itself for a literal, b - distance for a match),
-      // from the table's bitmap and one-byte distances, then the chains resolved to their
+      // from the unit's bitmap and one-byte distances, then the chains resolved to their
       // literal roots (pointer jumping, CTA barriers between rounds)
-      const int64_t B = sh.B;
-      const uint32_t* bmt = reinterpret_cast<const uint32_t*>(in + L.off_bitmap) + (size_t)t * sh.nw;
-      const uint8_t* dist = in + L.off_refs;
-      const uint32_t* srec = reinterpret_cast<const uint32_t*>(in + L.off_seg);
-      const unsigned long long mbase = srec[4ull * ((unsigned long long)t * sh.nseg) + 2];
-      uint32_t* src = w.srcrow + (size_t)t * B;
+      const int64_t n = (int64_t)Lc.n, row0 = (int64_t)Lc.row0;
+      const int64_t nw = Lc.nw;
+      const uint32_t* bmt = reinterpret_cast<const uint32_t*>(cin + Lc.off_bitmap) + (size_t)t * nw;
+      const uint8_t* dist = cin + Lc.off_refs;
+      const uint32_t* srec = reinterpret_cast<const uint32_t*>(cin + Lc.off_seg);
+      const unsigned long long mbase = srec[4ull * ((unsigned long long)t * Lc.nseg) + 2];
+      uint32_t* src = w.srcrow + (size_t)t * sh.B + row0;
       unsigned long long carry = 0;
-      for (int64_t base = 0; base < sh.nw; base += 256) {
+      for (int64_t base = 0; base < nw; base += 256) {
         const int64_t wi = base + tid;
-        const uint32_t bm = wi < sh.nw ? __ldcg(&bmt[wi]) : 0u;
+        const uint32_t bm = wi < nw ? __ldcg(&bmt[wi]) : 0u;
         // matches before this word: a CTA-wide exclusive scan of the words' counts
         uint32_t wt;
         const uint32_t in_warp = warp_excl((uint32_t)__popc(bm), &wt);
@@ -239,16 +324,16 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
         }
         __syncthreads();
         const unsigned long long rank0 = mbase + carry + before + in_warp;
-        if (wi < sh.nw) {
+        if (wi < nw) {
           for (int j = 0; j < 32; ++j) {
-            const int64_t b = wi * 32 + j;
-            if (b >= B) break;
-            uint32_t from = (uint32_t)b;
+            const int64_t b = wi * 32 + j;   // row of the slice
+            if (b >= n) break;
+            uint32_t from = (uint32_t)(row0 + b);
             if ((bm >> j) & 1u) {
               const unsigned long long k = rank0 + __popc(bm & ((1u << j) - 1u));
-              const uint32_t d = k < L.n_match ? dist[k] : 0u;
-              if (d == 0u || d > L.window || (int64_t)d > b) s_bad = 1;
-              else from = (uint32_t)(b - d);
+              const uint32_t d = k < Lc.n_match ? dist[k] : 0u;
+              if (d == 0u || d > Lc.window || (int64_t)d > b) s_bad = 1;
+              else from = (uint32_t)(row0 + b - d);
             }
             src[b] = from;
           }
@@ -261,12 +346,12 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
         return;
       }
       int rounds = 1;
-      while ((1ll << rounds) < B) ++rounds;
-      for (int r = 0; r <= rounds; ++r) {
-        for (int64_t b = tid; b < B; b += 256) {
+      while ((1ll << rounds) < n) ++rounds;
+      for (int rd = 0; rd <= rounds; ++rd) {
+        for (int64_t b = tid; b < n; b += 256) {
           const uint32_t s = src[b];
-          if (s != (uint32_t)b) {
-            const uint32_t s2 = src[s];   // one step further (a literal points at itself)
+          if (s != (uint32_t)(row0 + b)) {
+            const uint32_t s2 = src[s - row0];   // one step further (a literal points at itself)
             if (s2 != s) src[b] = s2;
           }
         }
@@ -277,26 +362,32 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
   }
 
   // ---- one warp per segment: literal rows and chunk descriptors ----
-  const int nsegT = T * sh.nseg;
-  const int seg = ((int)blockIdx.x - T) * 8 + warp;
+  const int seg = ((int)blockIdx.x - U) * 8 + warp;
   if (seg >= nsegT) return;
-  const int t = seg / sh.nseg;
-  const int s = seg - t * sh.nseg;
-  const int64_t B = sh.B;
-  const int64_t row0 = (int64_t)s * G::kSB;
-  const uint32_t* rec = reinterpret_cast<const uint32_t*>(in + L.off_seg) + 4ull * seg;
+  const int u = seg / sh.nseg;
+  const int s = seg - u * sh.nseg;
+  const int r = u / T;
+  const int t = u - r * T;
+  const Layout& Lc = s_L[r - r_lo];
+  if (s >= (int)Lc.nseg) return;   // past the end of a shorter slice
+  const uint8_t* cin = in + Lc.base;
+  const int64_t B = (int64_t)Lc.n;                // rows of the slice
+  const int64_t row0 = (int64_t)s * G::kSB;      // within the slice
+  const int64_t nw = Lc.nw;
+  const unsigned long long ri = (unsigned long long)t * Lc.nseg + s;   // record of the segment
+  const uint32_t* rec = reinterpret_cast<const uint32_t*>(cin + Lc.off_seg) + 4ull * ri;
   const uint32_t word_off = rec[0], chunk_base = rec[1], match_base = rec[2], nbits = rec[3];
   unsigned long long nx_word, nx_chunk, nx_match;
-  if (seg + 1 < nsegT) {
+  if (ri + 1 < (unsigned long long)T * Lc.nseg) {
     nx_word = rec[4];
     nx_chunk = rec[5];
     nx_match = rec[6];
   } else {
-    nx_word = L.words;
-    nx_chunk = L.n_chunks;
-    nx_match = L.n_match;
+    nx_word = Lc.words;
+    nx_chunk = Lc.n_chunks;
+    nx_match = Lc.n_match;
   }
-  const uint32_t* bmt = reinterpret_cast<const uint32_t*>(in + L.off_bitmap) + (size_t)t * sh.nw;
+  const uint32_t* bmt = reinterpret_cast<const uint32_t*>(cin + Lc.off_bitmap) + (size_t)t * nw;
   // literal rows, in row order: words 0..31 on the lanes, then words 32..63
   uint32_t nlit = 0, nvalid_rows = 0;
   uint16_t* litrow = w.litrow + (size_t)seg * G::kSB;
@@ -306,11 +397,11 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     uint32_t litw = 0, valid = 0;
     if (wi < G::kBmWords) {
       const int64_t gw = (int64_t)s * G::kBmWords + wi;
-      if (gw < sh.nw) {
+      if (gw < nw) {
         const int64_t nv = B - (row0 + (int64_t)wi * 32);
         valid = nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u);
         const uint32_t bm = bmt[gw];
-        if (bm & ~valid) s_bad = 1;             // match bits past the batch
+        if (bm & ~valid) s_bad = 1;             // match bits past the slice
         litw = ~bm & valid;
       }
     }
@@ -325,14 +416,14 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
   const uint32_t nmatch = nvalid_rows - nlit;
   const uint32_t nchunks = (nlit + G::kKC - 1) / G::kKC;
   const unsigned long long seg_words = ((nbits + 127ull) >> 7) * 4ull;
-  bool ok = (unsigned long long)chunk_base + nchunks == nx_chunk && nx_chunk <= L.n_chunks &&
-            (unsigned long long)match_base + nmatch == nx_match && nx_match <= L.n_match &&
-            (unsigned long long)word_off + seg_words == nx_word && nx_word <= L.words &&
-            (seg != 0 || (word_off == 0 && chunk_base == 0 && match_base == 0));
+  bool ok = (unsigned long long)chunk_base + nchunks == nx_chunk && nx_chunk <= Lc.n_chunks &&
+            (unsigned long long)match_base + nmatch == nx_match && nx_match <= Lc.n_match &&
+            (unsigned long long)word_off + seg_words == nx_word && nx_word <= Lc.words &&
+            (ri != 0 || (word_off == 0 && chunk_base == 0 && match_base == 0));
   // chunk start bits
   uint32_t cstart = 0;
   if (ok) {
-    const uint16_t* cl = reinterpret_cast<const uint16_t*>(in + L.off_chunks) + chunk_base;
+    const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + Lc.off_chunks) + chunk_base;
     uint32_t acc = 0;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -343,17 +434,18 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
       if (c < nchunks) {
         const unsigned long long start = (unsigned long long)word_off * 32ull + st;
         const uint32_t rows = min((uint32_t)G::kKC, nlit - c * G::kKC);
-        w.cdesc[chunk_base + c] = make_uint4((uint32_t)start, (uint32_t)(start >> 32) | (len << 16), (uint32_t)seg,
-                                             (c * G::kKC) | (rows << 16));
+        w.cdesc[Lc.chunk0 + chunk_base + c] = make_uint4((uint32_t)start, (uint32_t)(start >> 32) | (len << 16),
+                                                         (uint32_t)seg, (c * G::kKC) | (rows << 16));
       }
       acc += tot;
     }
     cstart = acc;
     ok = cstart == nbits;
   }
-  // matched rows: {destination, source} row pairs, in (table, row) order
+  // matched rows: {destination, source} row pairs of the batch, in (unit, row) order
   if (__all_sync(0xffffffffu, ok)) {
-    const uint8_t* refs = in + L.off_refs;
+    const uint8_t* refs = cin + Lc.off_refs;
+    const int64_t brow0 = (int64_t)Lc.row0;
     uint32_t mbase = match_base;
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
@@ -361,29 +453,29 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
       uint32_t mw = 0;
       if (wi < G::kBmWords) {
         const int64_t gw = (int64_t)s * G::kBmWords + wi;
-        if (gw < sh.nw) mw = bmt[gw];
+        if (gw < nw) mw = bmt[gw];
       }
       uint32_t tot;
       uint32_t k = mbase + warp_excl(__popc(mw), &tot);
       for (uint32_t m = mw; m; m &= m - 1) {
-        const int64_t b = row0 + wi * 32 + __ffs(m) - 1;
+        const int64_t b = row0 + wi * 32 + __ffs(m) - 1;   // row of the slice
         uint32_t ref;
-        if (L.window) {   // a distance back, within the window; the row there may itself be a match
+        if (Lc.window) {   // a distance back, within the window; the row there may itself be a match
           const uint32_t dist = refs[k];
-          if (dist == 0u || dist > L.window || (int64_t)dist > b) {
+          if (dist == 0u || dist > Lc.window || (int64_t)dist > b) {
             ok = false;
             break;
           }
           ref = (uint32_t)(b - dist);
-        } else {          // whole batch: the first occurrence, always a literal
-          ref = sh.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[k]
+        } else {           // whole slice: the first occurrence, always a literal
+          ref = Lc.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[k]
                                   : reinterpret_cast<const uint32_t*>(refs)[k];
           if ((int64_t)ref >= b || ((bmt[ref >> 5] >> (ref & 31)) & 1u)) {
             ok = false;
             break;
           }
         }
-        w.mdesc[k] = make_uint2((uint32_t)(b * T + t), (uint32_t)((int64_t)ref * T + t));
+        w.mdesc[Lc.match0 + k] = make_uint2((uint32_t)((brow0 + b) * T + t), (uint32_t)((brow0 + ref) * T + t));
         ++k;
       }
       mbase += tot;
@@ -487,23 +579,23 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
   // the run, and whether the decode was aborted (then the run map may be
   // stale): one decision for the whole CTA, taken before the run is used
   if (tid == 0) s_abort = dec_aborted(g, epoch);
-  const unsigned long long nslots = __ldcg(&g->n_chunks) / kDecRun + (unsigned long long)sh.T;
+  const unsigned long long nslots = __ldcg(&g->n_chunks) / kDecRun + (unsigned long long)sh.U;
   uint4 run = make_uint4(~0u, 0u, 0u, 0u);
   if (slot < nslots) run = __ldcg(&w.runmap[slot]);
   __syncthreads();
   if (s_abort || run.x == ~0u) return;
-  if (run.x >= (uint32_t)sh.T || run.y >= run.z || run.z > dec_max_chunks(sh)) {
+  if (run.x >= (uint32_t)sh.U || run.y >= run.z || run.z > dec_max_chunks(sh)) {
     if (tid == 0) dec_fail(g, epoch, EBC_ERR_INTERNAL);
     return;
   }
-  const int t = (int)run.x;
+  const int u = (int)run.x;   // unit: slice u / T, table u % T
   const unsigned long long j = (unsigned long long)run.y + tid;
   const bool mine = j < run.z;
-  const DecTab* dt = w.dtab + t;
+  const DecTab* dt = w.dtab + u;
   uint4 dsc = make_uint4(0, 0, 0, 0);
   if (mine) dsc = __ldcg(&w.cdesc[j]);
   {
-    const uint4* src = reinterpret_cast<const uint4*>(w.lut + (size_t)t * (1u << kLutBits));
+    const uint4* src = reinterpret_cast<const uint4*>(w.lut + (size_t)u * (1u << kLutBits));
     uint4* dst = reinterpret_cast<uint4*>(s_lut);
 #pragma unroll
     for (int i = tid; i < (1 << kLutBits) / 8; i += kDecRun) dst[i] = __ldcg(src + i);
@@ -519,7 +611,10 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
       s_val[i] = __fmul_rn((float)(i - kRadius), ebx2);
     }
   }
-  const unsigned long long n_words = __ldcg(&g->words), off_bits = __ldcg(&g->off_bits);
+  // the bitstream of the unit's container
+  const unsigned long long n_words = __ldcg(&dt->n_words), off_bits = __ldcg(&dt->bits_off);
+  const int t = (int)__ldcg(&dt->t);
+  const int64_t slice0 = (int64_t)__ldcg(&dt->row0);
   const uint32_t* words = reinterpret_cast<const uint32_t*>(in + off_bits);
   const unsigned long long start = (unsigned long long)dsc.x | ((unsigned long long)(dsc.y & 0xffffu) << 32);
   const uint32_t clen = dsc.y >> 16;
@@ -539,13 +634,13 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
   if (!mine) return;
   const int seg = (int)dsc.z;
   const uint32_t first = dsc.w & 0xffffu, rows = dsc.w >> 16;
-  if (seg / sh.nseg != t || rows == 0u || first + rows > (uint32_t)G::kSB || start + clen > n_words * 32ull) {
+  if (seg / sh.nseg != u || rows == 0u || first + rows > (uint32_t)G::kSB || start + clen > n_words * 32ull) {
     dec_fail(g, epoch, EBC_ERR_CORRUPT);
     return;
   }
-  const int s = seg - t * sh.nseg;
+  const int s = seg - u * sh.nseg;
   const uint16_t* lrow = w.litrow + (size_t)seg * G::kSB + first;
-  const int64_t row0 = (int64_t)s * G::kSB;
+  const int64_t row0 = slice0 + (int64_t)s * G::kSB;   // batch row of the segment's first row
   bool bad = false;
   unsigned long long used;
   if (staged && (start >> 5) >= lo && wlim <= hi) {
@@ -612,11 +707,12 @@ __global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __
 // launcher
 // ---------------------------------------------------------------------------
 template <int D>
-static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, const Shape& sh, const Work& w,
-                                float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof) {
-  const unsigned nsegT = (unsigned)(sh.T * sh.nseg);
+static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, const unsigned long long* offs,
+                                const Shape& sh, const Work& w, float* xhat, uint32_t epoch, cudaStream_t st,
+                                Prof* prof) {
+  const unsigned nsegT = (unsigned)(sh.U * sh.nseg);
   prof_begin(prof, "k_dec_prep", st);
-  launch_k(k_dec_prep<D>, (sh.T > 0 ? sh.T : 1) + (nsegT + 7) / 8, 256, 0, st, in, in_bytes, sh, w, epoch);
+  launch_k(k_dec_prep<D>, (sh.U > 0 ? sh.U : 1) + (nsegT + 7) / 8, 256, 0, st, in, in_bytes, offs, sh, w, epoch);
   prof_end(prof, st);
   if (nsegT) {
     // one CTA per run slot: enough for the largest possible chunk count
@@ -629,17 +725,18 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
   }
 }
 
-cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const Shape& sh, const Work& w,
-                              float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof) {
+cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const unsigned long long* offs,
+                              const Shape& sh, const Work& w, float* xhat, uint32_t epoch, cudaStream_t st,
+                              Prof* prof) {
   switch (sh.D) {
-    case 4: launch_decompress_d<4>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
-    case 8: launch_decompress_d<8>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
-    case 16: launch_decompress_d<16>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
-    case 32: launch_decompress_d<32>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
-    case 64: launch_decompress_d<64>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
-    case 128: launch_decompress_d<128>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
-    case 256: launch_decompress_d<256>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
-    case 512: launch_decompress_d<512>(in, in_bytes, sh, w, xhat, epoch, st, prof); break;
+    case 4: launch_decompress_d<4>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 8: launch_decompress_d<8>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 16: launch_decompress_d<16>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 32: launch_decompress_d<32>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 64: launch_decompress_d<64>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 128: launch_decompress_d<128>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 256: launch_decompress_d<256>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 512: launch_decompress_d<512>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

@@ -27,38 +27,75 @@ constexpr int kDecRun = 64;                // chunks per decoder CTA (one thread
 constexpr unsigned long long kEmptySlot = ~0ull;
 
 // Shape-derived constants of one call.
+//
+// The batch may be split into R slices (the rows of one destination rank of an
+// all-to-all each), every slice coded as a container of its own.  The first
+// B % R slices hold B / R + 1 rows, the others B / R.  The coding unit is one
+// table of one slice: unit u = r * T + t, so the units of a container are
+// consecutive.  With R = 1 a unit is a table.
 struct Shape {
   int64_t B;
   int T;
   int D;
   int SB;         // rows per segment: max(32, 8192 / D)
   int KC;         // literal rows per chunk: max(1, 128 / D)
-  int nseg;       // segments per table
-  int nw;         // bitmap words per table: ceil(B / 32)
-  uint32_t S;     // dedup slots per table (power of two >= 2B, >= 64)
-  int ref_bytes;  // 1 with a window (distances), else 2 if B <= 65536 else 4
+  int nseg;       // segments per unit: ceil(Bc / SB)
+  int nw;         // bitmap words per unit: ceil(Bc / 32)
+  uint32_t S;     // dedup slots per unit (power of two >= 2 Bc, >= 64)
+  int ref_bytes;  // 1 with a window (distances), else 2 if B <= 65536 else 4 (of the R = 1 container)
   int nsm;        // SMs of the device (grid sizing)
   uint64_t symstride;  // bytes per table in the code scratch: B*D rounded up to 16
   int window;     // dedup window in rows (0 = whole batch, first occurrence; else nearest earlier, 1..255)
-  int fold;       // 1: segment offsets are built per table inside k_codebook (nseg <= kFoldMaxSeg);
+  int fold;       // 1: segment offsets are built per unit inside k_codebook (nseg <= kFoldMaxSeg);
                   // 0: by k_layout, per 8-segment tile
+  int R;          // slices of the batch (containers)
+  int U;          // units: R * T
+  int64_t Bq;     // B / R
+  int Brem;       // B % R
+  int64_t Bc;     // rows of the largest slice
+  int qseg;       // quantization segments per table: ceil(B / SB) (k_quantize works on whole tables)
 };
 
 constexpr int kFoldMaxSeg = 256;
 constexpr int kMaxWindow = 255;
+constexpr int kMaxSlices = EBC_MAX_CHUNKS;
+
+// Rows of slice r: [slice_row0, slice_row0 + slice_rows).
+__host__ __device__ inline int64_t slice_row0(const Shape& sh, int r) {
+  return (int64_t)r * sh.Bq + (r < sh.Brem ? r : sh.Brem);
+}
+__host__ __device__ inline int64_t slice_rows(const Shape& sh, int r) { return sh.Bq + (r < sh.Brem ? 1 : 0); }
+// The slice holding batch row b (0 <= b < B).
+__host__ __device__ inline int slice_of_row(const Shape& sh, int64_t b) {
+  if (sh.R == 1) return 0;
+  const int64_t big = (int64_t)sh.Brem * (sh.Bq + 1);   // rows of the longer slices
+  return b < big ? (int)(b / (sh.Bq + 1)) : sh.Brem + (int)((b - big) / sh.Bq);
+}
+// Bytes per reference of a container of n rows.
+__host__ __device__ inline int ref_bytes_of(int64_t n, int window) { return window > 0 ? 1 : (n <= 65536 ? 2 : 4); }
+__host__ __device__ inline int div_up(int64_t a, int b) { return (int)((a + b - 1) / b); }
+
+// Section layout of one container, relative to its first byte (base).
+struct ContLay {
+  unsigned long long n_lit, n_match, n_out, n_chunks, words;
+  unsigned long long base, off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
+  uint32_t word0, chunk0, match0;   // bitstream words, chunks and matches of the units before the container
+  uint32_t ref_bytes;
+};
 
 // Per-table coding modes (bit flags; 0 = vector dedup + Huffman codes).
 constexpr uint32_t kModeNoDedup = 1;   // every vector of the table is a literal
 constexpr uint32_t kModeRawCodes = 2;  // every code 8 bits (lengths all 8: code of symbol s is s)
 
-// Decoder run slots: table t's runs of kDecRun chunks start at slot
-// floor(chunk0_t / kDecRun) + t, so the slots of all tables are disjoint and
-// ordered, and every slot below floor(n_chunks / kDecRun) + T is written.
+// Decoder run slots: unit u's runs of kDecRun chunks start at slot
+// floor(chunk0_u / kDecRun) + u (chunk0_u counted over all containers), so the
+// slots of all units are disjoint and ordered, and every slot below
+// floor(n_chunks / kDecRun) + U is written.
 __host__ __device__ inline unsigned long long dec_max_chunks(const Shape& sh) {
-  return (unsigned long long)sh.T * (unsigned long long)sh.nseg * (unsigned long long)(sh.SB / sh.KC);
+  return (unsigned long long)sh.U * (unsigned long long)sh.nseg * (unsigned long long)(sh.SB / sh.KC);
 }
 __host__ __device__ inline unsigned long long dec_run_slots(const Shape& sh) {
-  return dec_max_chunks(sh) / kDecRun + (unsigned long long)sh.T + 1ull;
+  return dec_max_chunks(sh) / kDecRun + (unsigned long long)sh.U + 1ull;
 }
 
 // Per-table absolute bounds of one compress call, passed by value.
@@ -84,36 +121,41 @@ struct DecTab {
   uint32_t count[kLmax + 1];   // codes of each length
   uint32_t offset[kLmax + 1];  // index of that first code in sorted[]
   float ebx2;                  // 2 * eb
-  uint32_t chunk0, chunk1;     // the table's chunks: [chunk0, chunk1)
-  uint32_t pad;
+  uint32_t chunk0, chunk1;     // the unit's chunks: [chunk0, chunk1), over all containers
+  uint32_t t;                  // table of the unit
+  unsigned long long bits_off; // byte offset of the unit's container bitstream in the input
+  unsigned long long n_words;  // words of that bitstream
+  unsigned long long row0;     // first batch row of the unit's slice
   uint8_t sorted[256];         // symbols by (length, symbol)
 };
 
 // Device scratch of a context.  Sizes follow Shape.
 struct Work {
   const uint8_t* modes;        // [T] per-table modes, or null (all 0)
-  unsigned long long* tab_bits;   // [T] bits of the table's literal codes and outlier values
+  unsigned long long* tab_bits;   // [U] bits of the unit's literal codes and outlier values
   // compress
   uint8_t* sym;                // [T][B][D] quantization codes, table t at t * symstride (16-byte aligned)
   uint32_t* vhash;             // [T][B] dedup key
   uint32_t* vnout;             // [T][B] outliers per vector
-  unsigned long long* slots;   // [T][S] (hash << 32 | first row); all ones = empty
-  uint32_t* bitmap;            // [T][nw] match bits
-  uint32_t* ref;               // [T][B] reference row of matched rows
-  uint32_t* seg_hist;          // [T*nseg][256] literal code histogram per segment
-  uint4* seg_cnt;              // [T*nseg] {literals, matches, outliers, chunks}
+  unsigned long long* slots;   // [U][S] (hash << 32 | first row); all ones = empty
+  uint32_t* bitmap;            // [U][nw] match bits (rows of the unit's slice)
+  uint32_t* ref;               // [T][B] reference row (batch row) of matched rows
+  uint32_t* seg_hist;          // [U*nseg][256] literal code histogram per segment
+  uint4* seg_cnt;              // [U*nseg] {literals, matches, outliers, chunks}
   uint4* seg_desc;             // [groups] totals {words, chunks, matches} of each group of segments
   uint4* tile_base;            // [groups] absolute base of each group
-  uint4* seg_base;             // [T*nseg] {words, chunks, matches} relative to its group, and the bit count
-                               // (a group: the table when Shape::fold, else 8 consecutive segments)
-  uint32_t* tab_hist;          // [T][256] literal code histogram per table
-  uint4* tab_cnt;              // [T] {literals, matches, outliers, chunks}
-  uint32_t* tabcode;           // [T][256] code << 8 | length
+  uint4* seg_base;             // [U*nseg] {words, chunks, matches} relative to its group, and the bit count
+                               // (a group: the unit when Shape::fold, else 8 consecutive segments)
+  uint32_t* tab_hist;          // [U][256] literal code histogram per unit
+  uint4* tab_cnt;              // [U] {literals, matches, outliers, chunks}
+  uint4* tab_rec;              // [U] the first 16 bytes of the unit's table record: eb, literals, matches, outliers
+  uint32_t* tabcode;           // [U][256] code << 8 | length
+  ContLay* cont;               // [R] container layouts
   // decompress
-  uint16_t* lut;               // [T][1 << kLutBits] sym | len << 8 (len 0 = long code)
-  DecTab* dtab;                // [T]
-  uint4* cdesc;                // [T*nseg*chunks] {start bit lo, start bit hi, segment, first literal | rows << 16}
-  uint16_t* litrow;            // [T*nseg][SB] literal rows of each segment, in row order
+  uint16_t* lut;               // [U][1 << kLutBits] sym | len << 8 (len 0 = long code)
+  DecTab* dtab;                // [U]
+  uint4* cdesc;                // [U*nseg*chunks] {start bit lo, start bit hi | length << 16, segment, first literal | rows << 16}
+  uint16_t* litrow;            // [U*nseg][SB] literal rows of each segment, in row order
   uint2* mdesc;                // [n_match] {destination row, source row} as b * T + t
   uint32_t* srcrow;            // [T][B] windowed containers: each row's source row (itself for a literal)
   uint4* runmap;               // [dec_run_slots] {table, first chunk, end chunk, 0} of each run of chunks;
@@ -195,11 +237,14 @@ void prof_begin(Prof* p, const char* name, cudaStream_t st);
 void prof_end(Prof* p, cudaStream_t st);
 
 // ---- launchers (one per direction; D is dispatched to the templated kernels) ----
+// out_bytes: the total size; chunk_off: null, or [R] the first byte of each container.
 cudaError_t launch_compress(const void* x, bool bf16, const Shape& sh, const EbParams& ep, const Work& w,
-                            uint8_t* out, unsigned long long cap, unsigned long long* out_bytes, uint32_t epoch,
-                            cudaStream_t st, Prof* prof);
-cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const Shape& sh, const Work& w,
-                              float* xhat, uint32_t epoch, cudaStream_t st, Prof* prof);
+                            uint8_t* out, unsigned long long cap, unsigned long long* out_bytes,
+                            unsigned long long* chunk_off, uint32_t epoch, cudaStream_t st, Prof* prof);
+// offs: null (one container of in_bytes), or [R + 1] container boundaries in device memory.
+cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const unsigned long long* offs,
+                              const Shape& sh, const Work& w, float* xhat, uint32_t epoch, cudaStream_t st,
+                              Prof* prof);
 cudaError_t set_kernel_attributes();
 
 }  // namespace ebc

@@ -161,6 +161,51 @@ int ebc_compress_bf16(ebc_ctx* ctx, const uint16_t* d_x, int64_t B, int T, int D
 int ebc_decompress(ebc_ctx* ctx, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B,
                    int T, int D, void* stream);
 
+/* Chunked sending buffer (§III-E "Buffer Optimization", Fig. 7; §IV-E,
+ * Fig. 15): the batch is split into n_chunks slices, one per destination rank
+ * of the all-to-all, and every slice is coded as a container of its own, all
+ * of them in one pass of the kernels and back to back in one buffer.  Slice r
+ * holds rows [r*q + min(r, m), (r+1)*q + min(r+1, m)) of the batch, q = B /
+ * n_chunks, m = B % n_chunks (the first m slices have one row more; numpy's
+ * array_split); a slice may be empty when n_chunks > B.  Dedup, code tables
+ * and bitstreams are per slice: container r is exactly what ebc_compress
+ * makes of slice r alone, and ebc_decompress restores that slice from it.
+ * 1 <= n_chunks <= EBC_MAX_CHUNKS. */
+#define EBC_MAX_CHUNKS 256
+
+/* Worst-case bytes of the chunked buffer: the sum of ebc_compress_bound over
+ * the slices (0 for an unsupported shape or chunk count). */
+uint64_t ebc_compress_chunked_bound(int64_t B, int T, int D, int n_chunks);
+
+/* Compress d_x[B][T][D] (device, fp32) as n_chunks containers into d_out
+ * (device, 16-byte aligned, out_capacity bytes).  The kernels write the
+ * container boundaries to d_offsets[0 .. n_chunks] (device u64, caller-owned):
+ * container r spans [d_offsets[r], d_offsets[r+1]), every offset a multiple of
+ * 16, d_offsets[n_chunks] the total, written also when it exceeds
+ * out_capacity (then the containers are not written and the context records
+ * EBC_ERR_CAPACITY).  The sizes d_offsets[r+1] - d_offsets[r] are the send
+ * counts of an all-to-all, ready on the device without a host round trip.
+ * Other arguments and errors as for ebc_compress; the schedule, window and
+ * table modes of the context apply to every slice.  Asynchronous. */
+int ebc_compress_chunked(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D, const float* eb,
+                         int n_chunks, void* d_out, uint64_t out_capacity, uint64_t* d_offsets,
+                         void* stream);
+/* The same for bf16 input (see ebc_compress_bf16; D >= 8). */
+int ebc_compress_chunked_bf16(ebc_ctx* ctx, const uint16_t* d_x, int64_t B, int T, int D,
+                              const float* eb, int n_chunks, void* d_out, uint64_t out_capacity,
+                              uint64_t* d_offsets, void* stream);
+
+/* Decompress n_chunks containers from d_in (device, in_bytes bytes, 16-byte
+ * aligned) into the rows of their slices in d_xhat[B][T][D] (Fig. 7, bottom:
+ * all containers decoded in one pass of the kernels).  d_offsets[0 ..
+ * n_chunks] (device u64) are the container boundaries, as written by
+ * ebc_compress_chunked or gathered by an all-to-all: each must be a multiple
+ * of 16, non-decreasing, and at most in_bytes; container r must hold slice r
+ * of the same B, T, D and all containers the same window.  Errors as for
+ * ebc_decompress (a bad boundary is EBC_ERR_CORRUPT).  Asynchronous. */
+int ebc_decompress_chunked(ebc_ctx* ctx, const void* d_in, uint64_t in_bytes, const uint64_t* d_offsets,
+                           int n_chunks, float* d_xhat, int64_t B, int T, int D, void* stream);
+
 /* Host-buffer variants (synchronous): the input is copied from host memory
  * h_x (pinned memory is fastest) to context-owned device buffers, processed,
  * and the result copied back.  ebc_compress_host writes the container to
