@@ -3,17 +3,21 @@
 // Method: "Accelerating Communication in Deep Learning Recommendation Model
 // Training with Dual-Level Adaptive Lossy Compression" (arXiv 2407.04272),
 // §III-D (quantization encoder, vector-based LZ, Huffman) and §III-E (one
-// output buffer, chunk offsets found on the device).  Six launches on the
-// caller's stream:
+// output buffer, chunk offsets found on the device; with "Buffer
+// Optimization", one container per batch slice in the same pass).  The coding
+// unit is a table of one slice (a table when there is one slice).  Up to five
+// launches on the caller's stream:
 //   k_quantize  x -> codes and per-vector dedup keys (TMA-staged input tiles);
-//               then the keys of its rows -> per-table first-occurrence hash table
+//               then the keys of its rows -> per-unit first-occurrence hash tables
 //   k_resolve   literal / match decision; literal code histograms per segment
-//               and per table
-//   k_codebook  per-table Huffman code; empties the hash table; the last CTA
-//               lays out the container sections and writes the header
-//   k_layout    per segment bit counts and every segment's absolute offsets
-//               (per-CTA totals scanned by the last CTA)
-//   k_emit      per segment: bitstream, chunk index, references, records
+//               and per unit
+//   k_codebook  per-unit Huffman code (and, for units of at most 256 segments,
+//               their segment offsets); the last CTA lays out the containers
+//               and writes the headers
+//   k_layout    (units of more than 256 segments) per segment bit counts and
+//               offsets; its last CTA completes the containers
+//   k_emit      per segment: bitstream, chunk index, references, records;
+//               empties its share of the hash tables
 // All offsets come from prefix sums, never from atomic reservations, so the
 // container is byte-identical from run to run.
 #include <cuda.h>
@@ -717,12 +721,12 @@ __device__ __forceinline__ unsigned long long bitonic_sort256(unsigned long long
 }
 
 // ---------------------------------------------------------------------------
-// k_codebook: one CTA per table.  Huffman code lengths (§III-D "Optimized
+// k_codebook: one CTA per unit.  Huffman code lengths (§III-D "Optimized
 // Entropy Encoding") by the two-queue construction over leaves sorted by
 // (count, symbol), merged nodes in FIFO order, ties to the leaf; if the longest
 // code exceeds 24 bits every nonzero count becomes max(1, count >> 1) and the
 // code is rebuilt.  Canonical code values follow the DEFLATE rule.  The last
-// CTA to finish lays out the sections and writes the header.
+// CTA to finish lays out the containers and writes their headers.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w, uint8_t* __restrict__ out,
                                                    unsigned long long cap, unsigned long long* out_bytes,
@@ -1074,7 +1078,7 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, EbParams ep, Work w, u
 }
 
 // ---------------------------------------------------------------------------
-// k_emit: one CTA per (table, segment), offsets from k_layout.  Every global
+// k_emit: one CTA per (unit, segment), offsets from k_codebook or k_layout.  Every global
 // read the CTA needs (the segment's codes, into shared memory; bitmap,
 // references, code table) is issued first.  The literal rows are ranked from
 // the match bitmap and dealt to the warps in turn (kRPS rows per warp step,

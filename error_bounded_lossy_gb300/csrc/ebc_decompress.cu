@@ -3,9 +3,11 @@
 // Method: "Accelerating Communication in Deep Learning Recommendation Model
 // Training with Dual-Level Adaptive Lossy Compression" (arXiv 2407.04272),
 // §III-D (Huffman and vector-based LZ decoding, dequantization) and §III-E
-// ("parallel decompression" of chunks).  Three launches:
-//   k_dec_prep     every CTA checks the header and layout; the first T CTAs
-//                  build each table's canonical decode tables (2^11-entry
+// ("parallel decompression" of chunks; one or several containers, one per
+// batch slice, decoded in the same pass).  The unit is a table of one
+// container.  Three launches:
+//   k_dec_prep     every CTA checks every header and layout; the first U CTAs
+//                  build each unit's canonical decode tables (2^11-entry
 //                  first-level table + long codes); the others, one warp per
 //                  segment, check the segment records against each other and
 //                  write one descriptor per chunk (start bit, length, rows)
