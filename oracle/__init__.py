@@ -31,6 +31,7 @@ OK, ERR_INVALID_ARG, ERR_CAPACITY, ERR_CORRUPT = 0, 1, 2, 3
 DECAY = {"none": 0, "linear": 1, "stepwise": 2, "drop": 3, "log": 4}
 LMAX = 24
 RADIUS = 128
+RADIUS_WIDE = 512   # the wide alphabet: 1024 symbols, 16-bit codes
 
 
 class Info(ctypes.Structure):
@@ -83,6 +84,22 @@ def _lib():
             lib.ebo_speedup.restype = ctypes.c_double
             lib.ebo_select_modes.argtypes = [P, P, P, ctypes.c_double, I, I, P]
             lib.ebo_select_modes.restype = I
+            lib.ebo_quantize_r.argtypes = [P, I64, ctypes.c_float, I, P]
+            lib.ebo_quantize_r.restype = I64
+            lib.ebo_dequantize_r.argtypes = [I, ctypes.c_float, I]
+            lib.ebo_dequantize_r.restype = ctypes.c_float
+            lib.ebo_vector_hash_r.argtypes = [P, P, I, I]
+            lib.ebo_vector_hash_r.restype = ctypes.c_uint32
+            lib.ebo_huffman_lengths_n.argtypes = [P, I, I, P]
+            lib.ebo_huffman_lengths_n.restype = I
+            lib.ebo_canonical_codes_n.argtypes = [P, I, I, P]
+            lib.ebo_canonical_codes_n.restype = I
+            lib.ebo_compress_bound_r.argtypes = [I64, I, I, I]
+            lib.ebo_compress_bound_r.restype = U64
+            lib.ebo_compress_r.argtypes = [P, I64, I, I, P, P, I, I, P, U64, ctypes.POINTER(Info), P, P, P]
+            lib.ebo_compress_r.restype = I
+            lib.ebo_decompress_r.argtypes = [P, U64, I64, I, I, P, P]
+            lib.ebo_decompress_r.restype = I
             _LIB = lib
     return _LIB
 
@@ -101,23 +118,40 @@ def quantize(x, eb: float) -> np.ndarray:
     return sym
 
 
-def dequantize(sym: int, eb: float) -> float:
-    return float(_lib().ebo_dequantize(int(sym), float(eb)))
+def dequantize(sym: int, eb: float, radius: int = RADIUS) -> float:
+    return float(_lib().ebo_dequantize_r(int(sym), float(eb), int(radius)))
 
 
-def vector_hash(sym_row, x_row) -> int:
-    s = np.ascontiguousarray(sym_row, dtype=np.uint8)
+def quantize_r(x, eb: float, radius: int) -> np.ndarray:
+    """Quantization codes (uint16; 0 = outlier, else q + radius) with radius 128 or 512."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    sym = np.empty(x.shape, dtype=np.uint16)
+    r = _lib().ebo_quantize_r(_ptr(x), x.size, float(eb), int(radius), _ptr(sym))
+    if r < 0:
+        raise ValueError("invalid error bound or radius")
+    return sym
+
+
+def vector_hash(sym_row, x_row, radius: int = RADIUS) -> int:
     x = np.ascontiguousarray(x_row, dtype=np.float32)
-    return int(_lib().ebo_vector_hash(_ptr(s), _ptr(x), s.size))
+    if radius == RADIUS:
+        s = np.ascontiguousarray(sym_row, dtype=np.uint8)
+        return int(_lib().ebo_vector_hash(_ptr(s), _ptr(x), s.size))
+    s = np.ascontiguousarray(sym_row, dtype=np.uint16)
+    return int(_lib().ebo_vector_hash_r(_ptr(s), _ptr(x), s.size, int(radius)))
 
 
-def huffman_lengths(freq, lmax: int = LMAX):
-    """(lengths uint8[256], halving rounds) of the two-queue Huffman code."""
-    f = np.zeros(256, dtype=np.uint64)
+def huffman_lengths(freq, lmax: int = LMAX, symbols: int = 256):
+    """(lengths uint8[symbols], halving rounds) of the two-queue Huffman code
+    over an alphabet of 256 or 1024 symbols."""
+    f = np.zeros(symbols, dtype=np.uint64)
     freq = np.asarray(freq, dtype=np.uint64)
     f[: freq.size] = freq
-    ln = np.zeros(256, dtype=np.uint8)
-    rounds = _lib().ebo_huffman_lengths(_ptr(f), int(lmax), _ptr(ln))
+    ln = np.zeros(symbols, dtype=np.uint8)
+    if symbols == 256:
+        rounds = _lib().ebo_huffman_lengths(_ptr(f), int(lmax), _ptr(ln))
+    else:
+        rounds = _lib().ebo_huffman_lengths_n(_ptr(f), int(symbols), int(lmax), _ptr(ln))
     if rounds < 0:
         raise ValueError("bad arguments")
     return ln, rounds
@@ -125,8 +159,8 @@ def huffman_lengths(freq, lmax: int = LMAX):
 
 def canonical_codes(lens, lmax: int = LMAX) -> np.ndarray:
     ln = np.ascontiguousarray(lens, dtype=np.uint8)
-    code = np.zeros(256, dtype=np.uint32)
-    if _lib().ebo_canonical_codes(_ptr(ln), int(lmax), _ptr(code)) < 0:
+    code = np.zeros(ln.size, dtype=np.uint32)
+    if _lib().ebo_canonical_codes_n(_ptr(ln), ln.size, int(lmax), _ptr(code)) < 0:
         raise ValueError("lengths violate the Kraft inequality")
     return code
 
@@ -143,39 +177,41 @@ def scheduled_bounds(eb_base, fn, iteration, m0, phase_len, n_steps=1) -> np.nda
     return (base * f).astype(np.float32)
 
 
-def compress_bound(B: int, T: int, D: int) -> int:
-    return int(_lib().ebo_compress_bound(int(B), int(T), int(D)))
+def compress_bound(B: int, T: int, D: int, radius: int = RADIUS) -> int:
+    return int(_lib().ebo_compress_bound_r(int(B), int(T), int(D), int(radius)))
 
 
 MODE_DEDUP_HUFFMAN, MODE_HUFFMAN, MODE_DEDUP_RAW, MODE_RAW = 0, 1, 2, 3
 
 
-def compress(x, eb, *, want_internals: bool = False, modes=None, window: int = 0):
+def compress(x, eb, *, want_internals: bool = False, modes=None, window: int = 0, radius: int = RADIUS):
     """Compress x [B,T,D] float32 with per-table bounds eb [T] and, optionally,
     per-table modes [T] (0 dedup + Huffman, 1 Huffman only, 2 dedup + raw
-    8-bit codes, 3 raw codes only) and a dedup window (0 = whole batch, first
-    occurrence; 1..255 = nearest earlier vector within that many rows).
+    codes, 3 raw codes only), a dedup window (0 = whole batch, first
+    occurrence; 1..255 = nearest earlier vector within that many rows) and the
+    quantization radius (128, or 512 for the wide 1024-symbol alphabet).
 
     Returns (container uint8 array, info dict) and, with want_internals,
-    also (sym [T,B,D] uint8, ref [T,B] uint32, lens [T,256] uint8)."""
+    also (sym [T,B,D] uint8 (uint16 with radius 512), ref [T,B] uint32,
+    lens [T, 2 * radius] uint8)."""
     x = np.ascontiguousarray(x, dtype=np.float32)
     B, T, D = x.shape
     eb = np.ascontiguousarray(eb, dtype=np.float32)
     assert eb.shape == (T,)
-    cap = compress_bound(B, T, D)
+    cap = compress_bound(B, T, D, radius)
     if cap == 0 and B * T * D > 0:
         raise ValueError("unsupported shape")
     out = np.zeros(max(cap, 16), dtype=np.uint8)
     info = Info()
-    sym = np.empty((T, B, D), dtype=np.uint8) if want_internals else None
+    sym = np.empty((T, B, D), dtype=np.uint16) if want_internals else None
     ref = np.empty((T, B), dtype=np.uint32) if want_internals else None
-    lens = np.empty((T, 256), dtype=np.uint8) if want_internals else None
+    lens = np.empty((T, 2 * radius), dtype=np.uint8) if want_internals else None
     md = None
     if modes is not None:
         md = np.ascontiguousarray(modes, dtype=np.uint8)
         assert md.shape == (T,)
-    rc = _lib().ebo_compress_ex(_ptr(x), B, T, D, _ptr(eb), _ptr(md) if md is not None else None, int(window),
-                                _ptr(out), out.size, ctypes.byref(info),
+    rc = _lib().ebo_compress_r(_ptr(x), B, T, D, _ptr(eb), _ptr(md) if md is not None else None, int(window),
+                               int(radius), _ptr(out), out.size, ctypes.byref(info),
                                    _ptr(sym) if sym is not None else None,
                                    _ptr(ref) if ref is not None else None,
                                    _ptr(lens) if lens is not None else None)
@@ -184,17 +220,19 @@ def compress(x, eb, *, want_internals: bool = False, modes=None, window: int = 0
     d = {k: int(getattr(info, k)) for k, _ in Info._fields_}
     buf = out[: d["total_bytes"]].copy()
     if want_internals:
-        return buf, d, sym, ref, lens
+        return buf, d, (sym.astype(np.uint8) if radius == RADIUS else sym), ref, lens
     return buf, d
 
 
 def decompress_rc(buf, B: int, T: int, D: int):
-    """(return code, xhat [B,T,D], sym [T,B,D]) without raising."""
+    """(return code, xhat [B,T,D], sym [T,B,D]) without raising; sym is uint8,
+    or uint16 for a container of the wide alphabet (radius field 512)."""
     buf = np.ascontiguousarray(buf, dtype=np.uint8)
     xhat = np.zeros((B, T, D), dtype=np.float32)
-    sym = np.zeros((T, B, D), dtype=np.uint8)
-    rc = _lib().ebo_decompress(_ptr(buf), buf.size, int(B), int(T), int(D), _ptr(xhat), _ptr(sym))
-    return rc, xhat, sym
+    wide = buf.size >= 28 and int.from_bytes(bytes(buf[24:28]), "little") == RADIUS_WIDE
+    sym = np.zeros((T, B, D), dtype=np.uint16)
+    rc = _lib().ebo_decompress_r(_ptr(buf), buf.size, int(B), int(T), int(D), _ptr(xhat), _ptr(sym))
+    return rc, xhat, (sym if wide else sym.astype(np.uint8))
 
 
 def decompress(buf, B: int, T: int, D: int):
@@ -241,7 +279,7 @@ def chunk_rows(B: int, n_chunks: int):
     return [(starts[r], starts[r + 1]) for r in range(n_chunks)]
 
 
-def compress_chunked(x, eb, n_chunks: int, *, modes=None, window: int = 0):
+def compress_chunked(x, eb, n_chunks: int, *, modes=None, window: int = 0, radius: int = RADIUS):
     """§III-E "Buffer Optimization", Fig. 7 (top): every slice of the batch is
     compressed on its own, as a self-contained container, and the containers
     lie back to back in one sending buffer.  Returns (buffer uint8, offsets
@@ -250,7 +288,7 @@ def compress_chunked(x, eb, n_chunks: int, *, modes=None, window: int = 0):
     B = x.shape[0]
     parts, offs = [], [0]
     for b0, b1 in chunk_rows(B, n_chunks):
-        buf, _ = compress(x[b0:b1], eb, modes=modes, window=window)
+        buf, _ = compress(x[b0:b1], eb, modes=modes, window=window, radius=radius)
         parts.append(buf)
         offs.append(offs[-1] + buf.size)
     return np.concatenate(parts), np.asarray(offs, dtype=np.uint64)

@@ -27,11 +27,15 @@
 
 /* ---- format constants (the container specification, version 1) ---- */
 #define O_RADIUS 128            /* bins q in (-R, R); sym = q + R          */
+#define O_RADIUS_WIDE 512       /* the wide alphabet: 1024 symbols         */
+#define O_MAX_SYMS 1024
 #define O_LMAX 24               /* longest Huffman code                    */
 #define O_MAGIC 0x31434245u     /* bytes 'E' 'B' 'C' '1'                   */
 #define O_VERSION 2u
 #define O_HEADER 144u
 #define O_TABLE_REC 272u        /* eb, n_lit, n_match, n_out, 256 lengths  */
+/* Bytes of a table record with an alphabet of A = 2R symbols: eb, counts, A lengths. */
+static uint64_t table_rec(int R) { return 16u + 2u * (uint64_t)R; }
 #define O_SEG_REC 16u           /* word_off, chunk_base, match_base, n_bits */
 #define O_MAX_T 1024
 
@@ -77,16 +81,16 @@ static int eb_ok(float eb) {
  * and a bin is accepted only if |x - xhat| <= eb holds in fp32 and |q| < R;
  * otherwise the element is an outlier (sym 0) and its raw bits are kept.
  * ---------------------------------------------------------------------- */
-static int quantize_one(float x, float eb, float ebx2, float inv) {
+static int quantize_one(float x, float eb, float ebx2, float inv, int R) {
   float t = x * inv;
   if (isnan(t) || fabsf(t) >= 1073741824.0f) return 0;
   float qf = nearbyintf(t);                 /* default mode: ties to even */
   int q = (int)qf;
-  if (q <= -O_RADIUS || q >= O_RADIUS) return 0;
+  if (q <= -R || q >= R) return 0;
   float xhat = (float)q * ebx2;
   float err = fabsf(x - xhat);
   if (!(err <= eb)) return 0;
-  return q + O_RADIUS;
+  return q + R;
 }
 
 int64_t ebo_quantize(const float* x, int64_t n, float eb, uint8_t* sym) {
@@ -94,7 +98,18 @@ int64_t ebo_quantize(const float* x, int64_t n, float eb, uint8_t* sym) {
   float ebx2 = 2.0f * eb, inv = 1.0f / ebx2;
   int64_t outl = 0;
   for (int64_t i = 0; i < n; ++i) {
-    sym[i] = (uint8_t)quantize_one(x[i], eb, ebx2, inv);
+    sym[i] = (uint8_t)quantize_one(x[i], eb, ebx2, inv, O_RADIUS);
+    if (sym[i] == 0) ++outl;
+  }
+  return outl;
+}
+
+int64_t ebo_quantize_r(const float* x, int64_t n, float eb, int R, uint16_t* sym) {
+  if (!eb_ok(eb) || n < 0 || (R != O_RADIUS && R != O_RADIUS_WIDE)) return -1;
+  float ebx2 = 2.0f * eb, inv = 1.0f / ebx2;
+  int64_t outl = 0;
+  for (int64_t i = 0; i < n; ++i) {
+    sym[i] = (uint16_t)quantize_one(x[i], eb, ebx2, inv, R);
     if (sym[i] == 0) ++outl;
   }
   return outl;
@@ -105,12 +120,19 @@ float ebo_dequantize(int sym, float eb) {
   return (float)(sym - O_RADIUS) * ebx2;
 }
 
+float ebo_dequantize_r(int sym, float eb, int R) {
+  float ebx2 = 2.0f * eb;
+  return (float)(sym - R) * ebx2;
+}
+
 /* ------------------------------------------------------------------------
  * Dedup key for the vector-based LZ encoder ([DLRM-EBLC] §III-D "Vector-based
  * LZ Encoding", §III-E "fixed pattern length"): the pattern is one whole
  * quantized embedding vector.  Reading: a 32-bit hash, the wrapping sum over
  * 4-code words w_k of lowbias32(w_k + k*0x9E3779B9) plus, for each outlier at
- * position d, lowbias32(raw_d ^ (d+1)*0x85EBCA6B).  lowbias32 is C. Wellons'
+ * position d, lowbias32(raw_d ^ (d+1)*0x85EBCA6B).  A word packs its codes
+ * little-endian: four 8-bit codes, or with the wide alphabet (16-bit codes)
+ * two, so a vector has D/4 or D/2 words.  lowbias32 is C. Wellons'
  * published 32-bit integer mixer (xor-shift 16, multiply 0x7feb352d,
  * xor-shift 15, multiply 0x846ca68b, xor-shift 16).
  * ---------------------------------------------------------------------- */
@@ -135,6 +157,25 @@ uint32_t ebo_vector_hash(const uint8_t* sym, const float* x_row, int D) {
   return h;
 }
 
+uint32_t ebo_vector_hash_r(const uint16_t* sym, const float* x_row, int D, int R) {
+  uint32_t h = 0;
+  if (R == O_RADIUS) {
+    for (int k = 0; k < D / 4; ++k) {
+      uint32_t w = (uint32_t)sym[4 * k] | ((uint32_t)sym[4 * k + 1] << 8) |
+                   ((uint32_t)sym[4 * k + 2] << 16) | ((uint32_t)sym[4 * k + 3] << 24);
+      h += lowbias32(w + (uint32_t)k * 0x9E3779B9u);
+    }
+  } else {
+    for (int k = 0; k < D / 2; ++k) {
+      uint32_t w = (uint32_t)sym[2 * k] | ((uint32_t)sym[2 * k + 1] << 16);
+      h += lowbias32(w + (uint32_t)k * 0x9E3779B9u);
+    }
+  }
+  for (int d = 0; d < D; ++d)
+    if (sym[d] == 0) h += lowbias32(f2u(x_row[d]) ^ ((uint32_t)(d + 1) * 0x85EBCA6Bu));
+  return h;
+}
+
 /* ------------------------------------------------------------------------
  * Huffman code lengths, [DLRM-EBLC] §III-D "Optimized Entropy Encoding"
  * (Huffman's minimum-redundancy code).  Reading, since the pages give no
@@ -144,10 +185,10 @@ uint32_t ebo_vector_hash(const uint8_t* sym, const float* x_row, int D) {
  * longest code exceeds lmax, every nonzero f becomes max(1, f >> 1) and the
  * code is rebuilt.
  * ---------------------------------------------------------------------- */
-static int two_queue_lengths(const uint64_t* f, uint8_t* len) {
-  int order[256], n = 0;
-  memset(len, 0, 256);
-  for (int s = 0; s < 256; ++s)
+static int two_queue_lengths(const uint64_t* f, int A, uint8_t* len) {
+  int order[O_MAX_SYMS], n = 0;
+  memset(len, 0, (size_t)A);
+  for (int s = 0; s < A; ++s)
     if (f[s] > 0) {
       /* insertion keeps (f, sym) order: equal f stay in sym order */
       int j = n++;
@@ -156,8 +197,8 @@ static int two_queue_lengths(const uint64_t* f, uint8_t* len) {
     }
   if (n == 0) return 0;
   if (n == 1) { len[order[0]] = 1; return 1; }
-  uint64_t node_w[255];
-  int leaf_parent[256], node_parent[255];
+  uint64_t node_w[O_MAX_SYMS - 1];
+  int leaf_parent[O_MAX_SYMS], node_parent[O_MAX_SYMS - 1];
   int li = 0, qi = 0, qn = 0;
   for (int m = 0; m < n - 1; ++m) {
     uint64_t w = 0;
@@ -168,7 +209,7 @@ static int two_queue_lengths(const uint64_t* f, uint8_t* len) {
     }
     node_w[qn++] = w;
   }
-  int depth[255];
+  int depth[O_MAX_SYMS - 1];
   depth[n - 2] = 0;                       /* the last merge is the root */
   for (int m = n - 3; m >= 0; --m) depth[m] = depth[node_parent[m]] + 1;
   int maxlen = 0;
@@ -180,12 +221,24 @@ static int two_queue_lengths(const uint64_t* f, uint8_t* len) {
   return maxlen;
 }
 
+int ebo_huffman_lengths_n(const uint64_t* freq, int A, int lmax, uint8_t* len) {
+  if (lmax < 10 || lmax > 32 || A < 2 || A > O_MAX_SYMS) return -1;
+  uint64_t f[O_MAX_SYMS];
+  memcpy(f, freq, sizeof(uint64_t) * (size_t)A);
+  for (int round = 0; round < 70; ++round) {
+    if (two_queue_lengths(f, A, len) <= lmax) return round;
+    for (int s = 0; s < A; ++s)
+      if (f[s] > 0) f[s] = (f[s] >> 1) > 0 ? (f[s] >> 1) : 1;
+  }
+  return -1;
+}
+
 int ebo_huffman_lengths(const uint64_t* freq, int lmax, uint8_t* len) {
   if (lmax < 8 || lmax > 32) return -1;
   uint64_t f[256];
   memcpy(f, freq, sizeof f);
   for (int round = 0; round < 70; ++round) {
-    if (two_queue_lengths(f, len) <= lmax) return round;
+    if (two_queue_lengths(f, 256, len) <= lmax) return round;
     for (int s = 0; s < 256; ++s)
       if (f[s] > 0) f[s] = (f[s] >> 1) > 0 ? (f[s] >> 1) : 1;
   }
@@ -195,9 +248,10 @@ int ebo_huffman_lengths(const uint64_t* freq, int lmax, uint8_t* len) {
 /* Canonical codes: lengths ascending, then symbols ascending, consecutive
  * values, the first code of each length being (previous first + count) << 1
  * (the DEFLATE rule). */
-int ebo_canonical_codes(const uint8_t* len, int lmax, uint32_t* code) {
+int ebo_canonical_codes_n(const uint8_t* len, int A, int lmax, uint32_t* code) {
   uint64_t count[33] = {0};
-  for (int s = 0; s < 256; ++s) {
+  if (lmax < 1 || lmax > 32 || A < 1 || A > O_MAX_SYMS) return -1;
+  for (int s = 0; s < A; ++s) {
     if (len[s] > lmax) return -1;
     count[len[s]]++;
   }
@@ -209,8 +263,12 @@ int ebo_canonical_codes(const uint8_t* len, int lmax, uint32_t* code) {
   uint64_t c = 0;
   next[0] = 0;
   for (int l = 1; l <= lmax; ++l) { c = (c + count[l - 1]) << 1; next[l] = c; }
-  for (int s = 0; s < 256; ++s) code[s] = len[s] ? (uint32_t)next[len[s]]++ : 0u;
+  for (int s = 0; s < A; ++s) code[s] = len[s] ? (uint32_t)next[len[s]]++ : 0u;
   return 0;
+}
+
+int ebo_canonical_codes(const uint8_t* len, int lmax, uint32_t* code) {
+  return ebo_canonical_codes_n(len, 256, lmax, code);
 }
 
 /* ------------------------------------------------------------------------
@@ -257,11 +315,11 @@ typedef struct {
 } layout_t;
 
 static layout_t make_layout(int64_t B, int T, int D, uint64_t n_chunks, uint64_t n_match,
-                            uint64_t words, int ref_bytes) {
+                            uint64_t words, int ref_bytes, uint64_t rec_bytes) {
   layout_t L;
   int64_t nseg = (B + seg_rows(D) - 1) / seg_rows(D);
   int64_t nw = (B + 31) / 32;
-  L.off_seg = O_HEADER + (uint64_t)T * O_TABLE_REC;
+  L.off_seg = O_HEADER + (uint64_t)T * rec_bytes;
   L.off_bitmap = L.off_seg + (uint64_t)T * (uint64_t)nseg * O_SEG_REC;
   L.off_chunks = L.off_bitmap + pad16((uint64_t)T * (uint64_t)nw * 4u);
   L.off_refs = L.off_chunks + pad16(n_chunks * 2u);
@@ -277,15 +335,17 @@ static int shape_ok(int64_t B, int T, int D) {
   return 1;
 }
 
-uint64_t ebo_compress_bound(int64_t B, int T, int D) {
-  if (!shape_ok(B, T, D)) return 0;
+uint64_t ebo_compress_bound_r(int64_t B, int T, int D, int R) {
+  if (!shape_ok(B, T, D) || (R != O_RADIUS && R != O_RADIUS_WIDE)) return 0;
   uint64_t N = (uint64_t)B * T * D;
   int64_t nseg = (B + seg_rows(D) - 1) / seg_rows(D);
   uint64_t vec = (uint64_t)B * T;
   uint64_t words = (N * (O_LMAX + 32) + 31) / 32 + 4u * (uint64_t)T * (uint64_t)nseg;
-  layout_t L = make_layout(B, T, D, vec, vec, words, B <= 65536 ? 2 : 4);
+  layout_t L = make_layout(B, T, D, vec, vec, words, B <= 65536 ? 2 : 4, table_rec(R));
   return L.total;
 }
+
+uint64_t ebo_compress_bound(int64_t B, int T, int D) { return ebo_compress_bound_r(B, T, D, O_RADIUS); }
 
 /* MSB-first bit writer over u32 words: bit i lives in word i/32 at bit 31-i%32. */
 static void put_bits(uint32_t* words, uint64_t* pos, uint32_t code, int len) {
@@ -315,10 +375,41 @@ int ebo_compress_modes(const float* x, int64_t B, int T, int D, const float* eb,
   return ebo_compress_ex(x, B, T, D, eb, modes, 0, out, cap, info, sym_out, ref_out, lens_out);
 }
 
+static int compress_impl(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes,
+                         int window, int R, uint8_t* out, uint64_t cap, ebo_info* info, uint16_t* sym_out,
+                         uint32_t* ref_out, uint8_t* lens_out);
+
 int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes, int window,
                     uint8_t* out, uint64_t cap, ebo_info* info, uint8_t* sym_out, uint32_t* ref_out,
                     uint8_t* lens_out) {
-  if (!shape_ok(B, T, D) || window < 0 || window > EBO_MAX_WINDOW) return EBO_ERR_INVALID_ARG;
+  if (!shape_ok(B, T, D)) return EBO_ERR_INVALID_ARG;
+  const size_t N = (size_t)B * (size_t)T * (size_t)D;
+  uint16_t* s16 = sym_out ? (uint16_t*)malloc((N ? N : 1) * 2) : NULL;
+  if (sym_out && !s16) return EBO_ERR_INVALID_ARG;
+  const int rc = compress_impl(x, B, T, D, eb, modes, window, O_RADIUS, out, cap, info, s16, ref_out, lens_out);
+  if (s16) {
+    if (rc == EBO_OK || rc == EBO_ERR_CAPACITY)
+      for (size_t i = 0; i < N; ++i) sym_out[i] = (uint8_t)s16[i];
+    free(s16);
+  }
+  return rc;
+}
+
+int ebo_compress_r(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes, int window,
+                   int R, uint8_t* out, uint64_t cap, ebo_info* info, uint16_t* sym_out, uint32_t* ref_out,
+                   uint8_t* lens_out) {
+  return compress_impl(x, B, T, D, eb, modes, window, R, out, cap, info, sym_out, ref_out, lens_out);
+}
+
+/* The whole encoder with radius R: 128 (8-bit codes, the default) or 512 (the
+ * wide alphabet, 1024 symbols, 16-bit codes).  lens_out is [T][2R]. */
+static int compress_impl(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes,
+                         int window, int R, uint8_t* out, uint64_t cap, ebo_info* info, uint16_t* sym_out,
+                         uint32_t* ref_out, uint8_t* lens_out) {
+  if (!shape_ok(B, T, D) || window < 0 || window > EBO_MAX_WINDOW || (R != O_RADIUS && R != O_RADIUS_WIDE))
+    return EBO_ERR_INVALID_ARG;
+  const int A = 2 * R;                                      /* symbols: 0 (outlier) and q + R */
+  const uint64_t REC = table_rec(R);
   for (int t = 0; t < T; ++t)
     if (!eb_ok(eb[t]) || (modes && modes[t] > 3)) return EBO_ERR_INVALID_ARG;
   const int64_t SB = seg_rows(D), KC = chunk_rows(D);
@@ -327,11 +418,11 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
   const size_t nvec = (size_t)B * (size_t)T;
   const size_t N = nvec * (size_t)D;
 
-  uint8_t* sym = (uint8_t*)malloc(N ? N : 1);            /* [T][B][D] */
+  uint16_t* sym = (uint16_t*)malloc((N ? N : 1) * 2);    /* [T][B][D] */
   uint32_t* hash = (uint32_t*)malloc((nvec ? nvec : 1) * 4);
   uint32_t* ref = (uint32_t*)malloc((nvec ? nvec : 1) * 4);
-  uint8_t* lens = (uint8_t*)calloc((size_t)(T ? T : 1) * 256, 1);
-  uint32_t* codes = (uint32_t*)calloc((size_t)(T ? T : 1) * 256, 4);
+  uint8_t* lens = (uint8_t*)calloc((size_t)(T ? T : 1) * (size_t)A, 1);
+  uint32_t* codes = (uint32_t*)calloc((size_t)(T ? T : 1) * (size_t)A, 4);
   hb_t* pairs = (hb_t*)malloc((size_t)(B ? B : 1) * sizeof(hb_t));
   if (!sym || !hash || !ref || !lens || !codes || !pairs) {
     free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
@@ -344,13 +435,13 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
     for (int64_t b = 0; b < B; ++b)
       for (int d = 0; d < D; ++d)
         sym[((size_t)t * B + b) * D + d] =
-            (uint8_t)quantize_one(x[((size_t)b * T + t) * D + d], eb[t], ebx2, inv);
+            (uint16_t)quantize_one(x[((size_t)b * T + t) * D + d], eb[t], ebx2, inv, R);
   }
   /* 2. vector hashes */
   for (int t = 0; t < T; ++t)
     for (int64_t b = 0; b < B; ++b)
       hash[(size_t)t * B + b] =
-          ebo_vector_hash(sym + ((size_t)t * B + b) * D, x + ((size_t)b * T + t) * D, D);
+          ebo_vector_hash_r(sym + ((size_t)t * B + b) * D, x + ((size_t)b * T + t) * D, D, R);
   /* 3. vector dedup ([DLRM-EBLC] §III-D / §III-E, vector-based LZ).  Reading:
    * the window is the whole batch of one table and the reference is the first
    * occurrence, ref(b) = min{b' : hash(b') = hash(b)}; b is a match when
@@ -373,11 +464,11 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
           if (hash[(size_t)t * B + c2] == hb) { r = c2; break; }
         int match = 0;
         if (r < b) {
-          const uint8_t* sb = sym + ((size_t)t * B + b) * D;
-          const uint8_t* sr = sym + ((size_t)t * B + r) * D;
+          const uint16_t* sb = sym + ((size_t)t * B + b) * D;
+          const uint16_t* sr = sym + ((size_t)t * B + r) * D;
           const float* xb = x + ((size_t)b * T + t) * D;
           const float* xr = x + ((size_t)r * T + t) * D;
-          match = memcmp(sb, sr, (size_t)D) == 0;
+          match = memcmp(sb, sr, (size_t)D * 2) == 0;
           for (int d = 0; match && d < D; ++d)
             if (sb[d] == 0 && f2u(xb[d]) != f2u(xr[d])) match = 0;
         }
@@ -393,11 +484,11 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
       uint32_t b = pairs[i].b, r = pairs[g].b;
       int match = 0;
       if (r < b) {
-        const uint8_t* sb = sym + ((size_t)t * B + b) * D;
-        const uint8_t* sr = sym + ((size_t)t * B + r) * D;
+        const uint16_t* sb = sym + ((size_t)t * B + b) * D;
+        const uint16_t* sr = sym + ((size_t)t * B + r) * D;
         const float* xb = x + ((size_t)b * T + t) * D;
         const float* xr = x + ((size_t)r * T + t) * D;
-        match = memcmp(sb, sr, (size_t)D) == 0;
+        match = memcmp(sb, sr, (size_t)D * 2) == 0;
         for (int d = 0; match && d < D; ++d)
           if (sb[d] == 0 && f2u(xb[d]) != f2u(xr[d])) match = 0;
       }
@@ -406,18 +497,18 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
   }
   /* 4. per-table histogram of literal codes, Huffman lengths, canonical codes */
   for (int t = 0; t < T; ++t) {
-    uint64_t f[256] = {0};
+    uint64_t f[O_MAX_SYMS] = {0};
     for (int64_t b = 0; b < B; ++b)
       if (ref[(size_t)t * B + b] == (uint32_t)b)
         for (int d = 0; d < D; ++d) f[sym[((size_t)t * B + b) * D + d]]++;
     if (modes && (modes[t] & EBO_MODE_RAW_CODES)) {
-      /* raw codes: every symbol 8 bits (the canonical code of symbol s is s) */
-      memset(lens + (size_t)t * 256, 8, 256);
-    } else if (ebo_huffman_lengths(f, O_LMAX, lens + (size_t)t * 256) < 0) {
+      /* raw codes: every symbol log2(A) bits, 8 or 10 (the canonical code of symbol s is s) */
+      memset(lens + (size_t)t * A, A == 256 ? 8 : 10, (size_t)A);
+    } else if (ebo_huffman_lengths_n(f, A, O_LMAX, lens + (size_t)t * A) < 0) {
       free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
       return EBO_ERR_INVALID_ARG;
     }
-    if (ebo_canonical_codes(lens + (size_t)t * 256, O_LMAX, codes + (size_t)t * 256) < 0) {
+    if (ebo_canonical_codes_n(lens + (size_t)t * A, A, O_LMAX, codes + (size_t)t * A) < 0) {
       free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
       return EBO_ERR_INVALID_ARG;
     }
@@ -431,8 +522,8 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
         if (ref[(size_t)t * B + b] != (uint32_t)b) { ++n_match; continue; }
         ++lits;
         for (int d = 0; d < D; ++d) {
-          uint8_t c = sym[((size_t)t * B + b) * D + d];
-          bits += lens[(size_t)t * 256 + c];
+          uint16_t c = sym[((size_t)t * B + b) * D + d];
+          bits += lens[(size_t)t * A + c];
           if (c == 0) { ++n_out; bits += 32; }
         }
       }
@@ -440,14 +531,14 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
       n_chunks += (lits + (uint64_t)KC - 1) / (uint64_t)KC;
       words += ((bits + 127) / 128) * 4;
     }
-  layout_t L = make_layout(B, T, D, n_chunks, n_match, words, ref_bytes);
+  layout_t L = make_layout(B, T, D, n_chunks, n_match, words, ref_bytes, REC);
   if (info) {
     info->n_literal = n_lit; info->n_match = n_match; info->n_outlier = n_out;
     info->n_chunks = n_chunks; info->bitstream_bytes = words * 4; info->total_bytes = L.total;
   }
-  if (sym_out) memcpy(sym_out, sym, N);
+  if (sym_out) memcpy(sym_out, sym, N * 2);
   if (ref_out) memcpy(ref_out, ref, nvec * 4);
-  if (lens_out) memcpy(lens_out, lens, (size_t)T * 256);
+  if (lens_out) memcpy(lens_out, lens, (size_t)T * (size_t)A);
   if (L.total > cap) {
     free(sym); free(hash); free(ref); free(lens); free(codes); free(pairs);
     return EBO_ERR_CAPACITY;
@@ -457,7 +548,7 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
   memset(out, 0, (size_t)L.total);
   uint8_t* h = out;
   wr32(h + 0, O_MAGIC); wr32(h + 4, O_VERSION); wr64(h + 8, (uint64_t)B);
-  wr32(h + 16, (uint32_t)T); wr32(h + 20, (uint32_t)D); wr32(h + 24, O_RADIUS);
+  wr32(h + 16, (uint32_t)T); wr32(h + 20, (uint32_t)D); wr32(h + 24, (uint32_t)R);
   wr32(h + 28, O_LMAX); wr32(h + 32, (uint32_t)SB); wr32(h + 36, (uint32_t)KC);
   wr32(h + 40, (uint32_t)ref_bytes); wr32(h + 44, (uint32_t)window);
   wr64(h + 48, n_lit); wr64(h + 56, n_match); wr64(h + 64, n_out); wr64(h + 72, n_chunks);
@@ -468,7 +559,7 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
   uint32_t* stream = (uint32_t*)calloc((size_t)(words ? words : 1), 4);
   uint64_t chunk_i = 0, match_i = 0, word_i = 0;
   for (int t = 0; t < T; ++t) {
-    uint8_t* rec = out + O_HEADER + (size_t)t * O_TABLE_REC;
+    uint8_t* rec = out + O_HEADER + (size_t)t * REC;
     uint32_t tl = 0, tm = 0, to = 0;
     for (int64_t s = 0; s < nseg; ++s) {
       uint8_t* srec = out + L.off_seg + ((size_t)t * nseg + s) * O_SEG_REC;
@@ -487,10 +578,10 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
           ++match_i; ++tm;
           continue;
         }
-        const uint8_t* sv = sym + ((size_t)t * B + b) * D;
+        const uint16_t* sv = sym + ((size_t)t * B + b) * D;
         const float* xv = x + ((size_t)b * T + t) * D;
         for (int d = 0; d < D; ++d) {
-          put_bits(stream, &pos, codes[(size_t)t * 256 + sv[d]], lens[(size_t)t * 256 + sv[d]]);
+          put_bits(stream, &pos, codes[(size_t)t * A + sv[d]], lens[(size_t)t * A + sv[d]]);
           if (sv[d] == 0) { put_bits(stream, &pos, f2u(xv[d]), 32); ++to; }
         }
         ++lit_in_seg; ++tl;
@@ -507,7 +598,7 @@ int ebo_compress_ex(const float* x, int64_t B, int T, int D, const float* eb, co
       word_i += ((pos - word_i * 32 + 127) / 128) * 4;
     }
     wr32(rec + 0, f2u(eb[t])); wr32(rec + 4, tl); wr32(rec + 8, tm); wr32(rec + 12, to);
-    memcpy(rec + 16, lens + (size_t)t * 256, 256);
+    memcpy(rec + 16, lens + (size_t)t * A, (size_t)A);
   }
   for (uint64_t w = 0; w < words; ++w) wr32(out + L.off_bits + w * 4, stream[w]);
   free(stream);
@@ -523,29 +614,56 @@ typedef struct {
   uint32_t first[O_LMAX + 2];   /* first canonical code of each length  */
   uint32_t count[O_LMAX + 2];
   uint32_t offset[O_LMAX + 2];  /* index of that first code in sorted[] */
-  uint8_t sorted[256];          /* symbols by (length, symbol)          */
+  uint16_t sorted[O_MAX_SYMS];  /* symbols by (length, symbol)          */
 } dec_t;
 
-static int build_decoder(const uint8_t* len, dec_t* dc) {
-  uint32_t code[256];
-  if (ebo_canonical_codes(len, O_LMAX, code) < 0) return -1;
+static int build_decoder(const uint8_t* len, int A, dec_t* dc) {
+  uint32_t code[O_MAX_SYMS];
+  if (ebo_canonical_codes_n(len, A, O_LMAX, code) < 0) return -1;
   memset(dc, 0, sizeof *dc);
-  for (int s = 0; s < 256; ++s) dc->count[len[s]]++;
+  for (int s = 0; s < A; ++s) dc->count[len[s]]++;
   dc->count[0] = 0;
   uint32_t k = 0;
   for (int l = 1; l <= O_LMAX; ++l) {
     dc->offset[l] = k;
-    for (int s = 0; s < 256; ++s)
+    for (int s = 0; s < A; ++s)
       if (len[s] == l) {
         if (k == dc->offset[l]) dc->first[l] = code[s];
-        dc->sorted[k++] = (uint8_t)s;
+        dc->sorted[k++] = (uint16_t)s;
       }
   }
   return 0;
 }
 
+static int decompress_impl(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D, float* xhat,
+                           uint16_t* sym_out, int* radius_out);
+
 int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D, float* xhat,
                    uint8_t* sym_out) {
+  if (!shape_ok(B, T, D)) return EBO_ERR_INVALID_ARG;
+  const size_t N = (size_t)B * (size_t)T * (size_t)D;
+  uint16_t* s16 = sym_out ? (uint16_t*)malloc((N ? N : 1) * 2) : NULL;
+  if (sym_out && !s16) return EBO_ERR_INVALID_ARG;
+  int R = 0;
+  int rc = decompress_impl(in, in_bytes, B, T, D, xhat, s16, &R);
+  if (s16) {
+    if (rc == EBO_OK && R != O_RADIUS) rc = EBO_ERR_INVALID_ARG;   /* 16-bit codes: use ebo_decompress_r */
+    if (rc == EBO_OK)
+      for (size_t i = 0; i < N; ++i) sym_out[i] = (uint8_t)s16[i];
+    free(s16);
+  }
+  return rc;
+}
+
+int ebo_decompress_r(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D, float* xhat,
+                     uint16_t* sym_out) {
+  int R = 0;
+  return decompress_impl(in, in_bytes, B, T, D, xhat, sym_out, &R);
+}
+
+/* Decoder of containers with either radius (read from the header). */
+static int decompress_impl(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D, float* xhat,
+                           uint16_t* sym_out, int* radius_out) {
   if (!shape_ok(B, T, D)) return EBO_ERR_INVALID_ARG;
   if (in_bytes < O_HEADER) return EBO_ERR_CORRUPT;
   if (rd32(in) != O_MAGIC || rd32(in + 4) != O_VERSION) return EBO_ERR_CORRUPT;
@@ -555,7 +673,12 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
   const int64_t nseg = (B + SB - 1) / SB, nw = (B + 31) / 32;
   const uint32_t window = rd32(in + 44);   /* 0: whole-batch references; else distances */
   const int ref_bytes = window > 0 ? 1 : (B <= 65536 ? 2 : 4);
-  if (rd32(in + 24) != O_RADIUS || rd32(in + 28) != O_LMAX || rd32(in + 32) != (uint32_t)SB ||
+  const int R = (int)rd32(in + 24);
+  if (R != O_RADIUS && R != O_RADIUS_WIDE) return EBO_ERR_CORRUPT;
+  const int A = 2 * R;
+  const uint64_t REC = table_rec(R);
+  *radius_out = R;
+  if (rd32(in + 28) != O_LMAX || rd32(in + 32) != (uint32_t)SB ||
       rd32(in + 36) != (uint32_t)KC || rd32(in + 40) != (uint32_t)ref_bytes || window > EBO_MAX_WINDOW)
     return EBO_ERR_CORRUPT;
   uint64_t n_lit = rd64(in + 48), n_match = rd64(in + 56), n_out = rd64(in + 64);
@@ -564,23 +687,23 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
   if (n_lit + n_match != nvec || n_chunks > nvec || n_out > nvec * (uint64_t)D ||
       words > ((uint64_t)1 << 34))
     return EBO_ERR_CORRUPT;
-  layout_t L = make_layout(B, T, D, n_chunks, n_match, words, ref_bytes);
+  layout_t L = make_layout(B, T, D, n_chunks, n_match, words, ref_bytes, REC);
   if (rd64(in + 88) != L.off_seg || rd64(in + 96) != L.off_bitmap || rd64(in + 104) != L.off_chunks ||
       rd64(in + 112) != L.off_refs || rd64(in + 120) != L.off_bits || rd64(in + 128) != L.total ||
       rd64(in + 136) != 0 || L.total > in_bytes)
     return EBO_ERR_CORRUPT;
 
   const size_t N = (size_t)nvec * (size_t)D;
-  uint8_t* sym = (uint8_t*)malloc(N ? N : 1);
+  uint16_t* sym = (uint16_t*)malloc((N ? N : 1) * 2);
   if (!sym) return EBO_ERR_INVALID_ARG;
   uint64_t chunk_i = 0, match_i = 0, out_i = 0, word_i = 0, lit_total = 0;
   int err = EBO_OK;
   for (int t = 0; t < T && err == EBO_OK; ++t) {
-    const uint8_t* rec = in + O_HEADER + (size_t)t * O_TABLE_REC;
+    const uint8_t* rec = in + O_HEADER + (size_t)t * REC;
     float eb = u2f(rd32(rec));
     if (!eb_ok(eb)) { err = EBO_ERR_CORRUPT; break; }
     dec_t dc;
-    if (build_decoder(rec + 16, &dc) < 0) { err = EBO_ERR_CORRUPT; break; }
+    if (build_decoder(rec + 16, A, &dc) < 0) { err = EBO_ERR_CORRUPT; break; }
     uint32_t tl = 0, tm = 0, to = 0;
     for (int64_t s = 0; s < nseg && err == EBO_OK; ++s) {
       const uint8_t* srec = in + L.off_seg + ((size_t)t * nseg + s) * O_SEG_REC;
@@ -600,7 +723,7 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
         if ((rd32(bm) >> (b & 31)) & 1u) { ++match_i; ++tm; continue; }
         if (chunk_i >= n_chunks) { err = EBO_ERR_CORRUPT; break; }
         uint64_t chunk_end = chunk_start + rd16(in + L.off_chunks + chunk_i * 2);
-        uint8_t* sv = sym + ((size_t)t * B + b) * D;
+        uint16_t* sv = sym + ((size_t)t * B + b) * D;
         for (int d = 0; d < D; ++d) {
           uint32_t code = 0;
           int l = 0, found = 0;
@@ -628,7 +751,7 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
             v = u2f(raw);
             ++out_i; ++to;
           } else {
-            v = ebo_dequantize(sv[d], eb);
+            v = ebo_dequantize_r(sv[d], eb, R);
           }
           xhat[((size_t)b * T + t) * D + d] = v;
         }
@@ -669,7 +792,7 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
         ++m;
         const uint8_t* bmr = in + L.off_bitmap + ((size_t)t * nw + (size_t)(r >> 5)) * 4;
         if ((int64_t)r >= b || (window == 0 && ((rd32(bmr) >> (r & 31)) & 1u))) { err = EBO_ERR_CORRUPT; break; }
-        memcpy(sym + ((size_t)t * B + b) * D, sym + ((size_t)t * B + r) * D, (size_t)D);
+        memcpy(sym + ((size_t)t * B + b) * D, sym + ((size_t)t * B + r) * D, (size_t)D * 2);
         memcpy(xhat + ((size_t)b * T + t) * D, xhat + ((size_t)r * T + t) * D, (size_t)D * 4);
       }
     }
@@ -677,7 +800,7 @@ int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D
   if (err == EBO_OK && (chunk_i != n_chunks || match_i != n_match || out_i != n_out ||
                         word_i != words || lit_total != n_lit))
     err = EBO_ERR_CORRUPT;
-  if (err == EBO_OK && sym_out) memcpy(sym_out, sym, N);
+  if (err == EBO_OK && sym_out) memcpy(sym_out, sym, N * 2);
   free(sym);
   return err;
 }

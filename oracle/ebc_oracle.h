@@ -113,9 +113,34 @@ int ebo_select_modes(const double* cr, const double* tc, const double* td, doubl
 
 /* Whole decompressor: writes xhat [B,T,D] and, if not NULL, the decoded
  * quantization codes sym_out [T][B][D] (matched vectors carry their
- * reference's codes). */
+ * reference's codes; a wide-alphabet container then gives EBO_ERR_INVALID_ARG,
+ * its codes need ebo_decompress_r). */
 int ebo_decompress(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D,
                    float* xhat, uint8_t* sym_out);
+
+/* Wide alphabet (radius R = 512): bins q in (-512, 512), symbols q + 512 in
+ * 1..1023 and 0 for an outlier, kept as 16-bit codes; Huffman over 1024
+ * symbols with the same length limit; table records of 16 + 1024 bytes; the
+ * header's radius field (offset 24) says which alphabet a container uses.  The
+ * dedup key sums over 2-code words.  Raw-code mode stores 10-bit codes.  The
+ * pages fix no radius; R = 128 stays the default. */
+#define EBO_RADIUS 128
+#define EBO_RADIUS_WIDE 512
+int64_t ebo_quantize_r(const float* x, int64_t n, float eb, int R, uint16_t* sym);
+float ebo_dequantize_r(int sym, float eb, int R);
+uint32_t ebo_vector_hash_r(const uint16_t* sym, const float* x_row, int D, int R);
+/* Huffman lengths / canonical codes over an alphabet of A <= 1024 symbols. */
+int ebo_huffman_lengths_n(const uint64_t* freq, int A, int lmax, uint8_t* len);
+int ebo_canonical_codes_n(const uint8_t* len, int A, int lmax, uint32_t* code);
+uint64_t ebo_compress_bound_r(int64_t B, int T, int D, int R);
+/* ebo_compress_ex with radius R (128 or 512); sym_out is [T][B][D] 16-bit,
+ * lens_out [T][2R]. */
+int ebo_compress_r(const float* x, int64_t B, int T, int D, const float* eb, const uint8_t* modes, int window,
+                   int R, uint8_t* out, uint64_t cap, ebo_info* info, uint16_t* sym_out, uint32_t* ref_out,
+                   uint8_t* lens_out);
+/* ebo_decompress of either alphabet, with 16-bit codes out. */
+int ebo_decompress_r(const uint8_t* in, uint64_t in_bytes, int64_t B, int T, int D,
+                     float* xhat, uint16_t* sym_out);
 
 #ifdef __cplusplus
 }

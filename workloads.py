@@ -187,7 +187,9 @@ def make(name: str, *, device="cpu", iteration: int = 0, batch: int | None = Non
             it = torch.from_numpy(idx).to(dev)
             _, inv, cnt = torch.unique(it, return_inverse=True, return_counts=True)
             count = cnt[inv].to(torch.float32)[:, None]
-            x[:, t, :] = _normal_rows(seed, _S_NORMAL, t, it, D, 1e-4, dev) * count
+            # variant "s1e-2": sigma 1e-2, the robustness case with heavy tails past the 8-bit bins
+            sigma = 1e-2 if variant == "s1e-2" else 1e-4
+            x[:, t, :] = _normal_rows(seed, _S_NORMAL, t, it, D, sigma, dev) * count
         eb = torch.tensor([1e-3 * 30.0 ** (t / 25.0) for t in range(T)], dtype=torch.float32)
     elif name == "large":
         for t in range(T):
