@@ -29,13 +29,14 @@ __all__ = [
     "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup", "ebc_select_modes",
     "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
     "EBC_MAX_CHUNKS", "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16",
-    "ebc_decompress_chunked",
+    "ebc_decompress_chunked", "EBC_RADIUS", "EBC_RADIUS_WIDE", "ebc_set_radius", "ebc_compress_bound_radius",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
 EBC_ERR_DEVICE_TIMEOUT, EBC_ERR_CUDA, EBC_ERR_NO_DEVICE, EBC_ERR_INTERNAL = 4, 5, 6, 7
 EBC_ERR_SCRATCH_LIMIT = 8
 EBC_MAX_CHUNKS = 256
+EBC_RADIUS, EBC_RADIUS_WIDE = 128, 512
 EBC_MODE_DEDUP_HUFFMAN, EBC_MODE_HUFFMAN, EBC_MODE_DEDUP_RAW, EBC_MODE_RAW = 0, 1, 2, 3
 EBC_DECAY_NONE, EBC_DECAY_LINEAR, EBC_DECAY_STEPWISE, EBC_DECAY_DROP, EBC_DECAY_LOG = 0, 1, 2, 3, 4
 DECAY = {"none": 0, "linear": 1, "stepwise": 2, "drop": 3, "log": 4}
@@ -47,6 +48,7 @@ EXPORTED_SYMBOLS = (
     "ebc_decompress_noalloc", "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup",
     "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
     "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16", "ebc_decompress_chunked",
+    "ebc_set_radius", "ebc_compress_bound_radius",
 )
 
 
@@ -120,7 +122,9 @@ def lib():
                 "ebc_select_modes": (I, [P, P, P, D, I, I, P]),
                 "ebc_select_table_modes": (I, [P, P, I64, I, I, P, D, P, P]),
                 "ebc_table_homo_index": (I, [P, P, I64, I, I, P, P, P]),
-                "ebc_compress_chunked_bound": (U64, [I64, I, I, I]),
+                "ebc_compress_chunked_bound": (U64, [I64, I, I, I, I]),
+                "ebc_set_radius": (I, [P, I]),
+                "ebc_compress_bound_radius": (U64, [I64, I, I, I]),
                 "ebc_compress_chunked": (I, [P, P, I64, I, I, P, I, P, U64, P, P]),
                 "ebc_compress_chunked_bf16": (I, [P, P, I64, I, I, P, I, P, U64, P, P]),
                 "ebc_decompress_chunked": (I, [P, P, U64, P, I, P, I64, I, I, P]),
@@ -181,8 +185,16 @@ def ebc_compress_bf16(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_byte
                                    stream)
 
 
-def ebc_compress_chunked_bound(B: int, T: int, D: int, n_chunks: int) -> int:
-    return int(lib().ebc_compress_chunked_bound(int(B), int(T), int(D), int(n_chunks)))
+def ebc_compress_chunked_bound(B: int, T: int, D: int, n_chunks: int, radius: int = EBC_RADIUS) -> int:
+    return int(lib().ebc_compress_chunked_bound(int(B), int(T), int(D), int(n_chunks), int(radius)))
+
+
+def ebc_set_radius(ctx, radius) -> int:
+    return lib().ebc_set_radius(ctx, int(radius))
+
+
+def ebc_compress_bound_radius(B: int, T: int, D: int, radius: int) -> int:
+    return int(lib().ebc_compress_bound_radius(int(B), int(T), int(D), int(radius)))
 
 
 def ebc_compress_chunked(ctx, d_x, B, T, D, eb_ptr, n_chunks, d_out, out_capacity, d_offsets, stream) -> int:
@@ -304,6 +316,7 @@ class Codec:
         import torch
         self.device = torch.device("cuda", device)
         self._ctx = ebc_create(device)
+        self.radius = EBC_RADIUS
 
     def close(self):
         if self._ctx is not None:
@@ -338,9 +351,16 @@ class Codec:
             raise EbcError(rc, "ebc_get_error_bounds")
         return out
 
-    @staticmethod
-    def compress_bound(B, T, D) -> int:
-        return ebc_compress_bound(B, T, D)
+    def compress_bound(self, B, T, D) -> int:
+        """Worst-case container bytes with this context's alphabet."""
+        return ebc_compress_bound_radius(B, T, D, self.radius)
+
+    def set_radius(self, radius: int) -> None:
+        """Alphabet of later calls: 128 (8-bit codes) or 512 (the wide alphabet)."""
+        rc = ebc_set_radius(self._ctx, radius)
+        if rc:
+            raise EbcError(rc, "ebc_set_radius")
+        self.radius = int(radius)
 
     def compress_into(self, x, eb, out, nbytes, stream=None) -> None:
         """Asynchronous compress of CUDA tensor x [B,T,D] into preallocated out / nbytes."""
@@ -366,9 +386,8 @@ class Codec:
         self.compress_into(x, eb, out, nbytes, stream)
         return out, nbytes
 
-    @staticmethod
-    def compress_chunked_bound(B, T, D, n_chunks) -> int:
-        return ebc_compress_chunked_bound(B, T, D, n_chunks)
+    def compress_chunked_bound(self, B, T, D, n_chunks) -> int:
+        return ebc_compress_chunked_bound(B, T, D, n_chunks, self.radius)
 
     def compress_chunked(self, x, n_chunks: int, eb=None, stream=None, out=None, offsets=None):
         """One container per slice of the batch (numpy array_split slices), back to

@@ -57,19 +57,20 @@ struct ebc_ctx {
   // the compress layout whose dedup table and look-back flags are known clean
   const void* clean_buf = nullptr;
   int64_t cleanB = -1;
-  int cleanT = -1, cleanD = -1, cleanR = -1;
+  int cleanT = -1, cleanD = -1, cleanR = -1, cleanW = -1;
   // schedule
   float* eb_base = nullptr;
   float* eb_now = nullptr;
   int sched_T = 0;
   // per-table coding modes (0 = dedup + Huffman for every table when modes_T == 0)
   int window = 0;                      // dedup window of the compress calls (0 = whole batch)
+  int radius = kRadius;                // alphabet of the compress and decompress calls (128 or 512)
   uint8_t* d_modes = nullptr;          // device [kMaxT]
   uint8_t h_modes[kMaxT] = {};
   int modes_T = 0;
   // last compress shape
   int64_t lastB = 0;
-  int lastT = 0, lastD = 0, lastR = 1;
+  int lastT = 0, lastD = 0, lastR = 1, lastRadius = kRadius;
   Prof* prof = nullptr;
 };
 
@@ -84,8 +85,11 @@ static bool shape_ok(int64_t B, int T, int D) {
 }
 
 // R: slices of the batch, each coded as a container of its own (1 = one container).
-static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0, int R = 1) {
+// radius: 128 (8-bit codes) or 512 (the wide alphabet, 16-bit codes).
+static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0, int R = 1, int radius = kRadius) {
   Shape sh;
+  sh.W = radius == kRadiusWide ? 2 : 1;
+  sh.A = 2 * radius;
   sh.nsm = nsm;
   sh.B = B;
   sh.T = T;
@@ -105,7 +109,7 @@ static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0, in
   sh.S = S;
   sh.window = window;
   sh.ref_bytes = window > 0 ? 1 : (B <= 65536 ? 2 : 4);
-  sh.symstride = ((uint64_t)B * (uint64_t)D + 15u) & ~(uint64_t)15u;
+  sh.symstride = ((uint64_t)B * (uint64_t)D * (uint64_t)sh.W + 15u) & ~(uint64_t)15u;
   sh.fold = sh.nseg <= kFoldMaxSeg ? 1 : 0;
   return sh;
 }
@@ -115,7 +119,7 @@ static uint64_t pad16h(uint64_t n) { return (n + 15u) & ~(uint64_t)15u; }
 // Bytes of the container that do not depend on the data: header, table and
 // segment records, match bitmap.
 static uint64_t fixed_bytes(const Shape& sh) {
-  return kHeaderBytes + (uint64_t)sh.T * kTableRecBytes + (uint64_t)sh.T * sh.nseg * kSegRecBytes +
+  return kHeaderBytes + (uint64_t)sh.T * table_rec_bytes(sh.A) + (uint64_t)sh.T * sh.nseg * kSegRecBytes +
          pad16h((uint64_t)sh.T * sh.nw * 4u);
 }
 
@@ -161,14 +165,14 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   w.vnout = c.take<uint32_t>(4 * nvec);
   w.ref = c.take<uint32_t>(4 * nvec);
   w.bitmap = c.take<uint32_t>(4 * U * sh.nw);
-  w.seg_hist = c.take<uint32_t>(1024 * nsegT);
+  w.seg_hist = c.take<uint32_t>(4 * (size_t)sh.A * nsegT);
   w.seg_cnt = c.take<uint4>(16 * nsegT);
-  w.tab_hist = c.take<uint32_t>(1024 * U);
+  w.tab_hist = c.take<uint32_t>(4 * (size_t)sh.A * U);
   w.tab_cnt = c.take<uint4>(16 * U);
   w.tab_rec = c.take<uint4>(16 * U);
   w.tab_bits = c.take<unsigned long long>(8 * U);
   w.modes = nullptr;
-  w.tabcode = c.take<uint32_t>(1024 * U);
+  w.tabcode = c.take<uint32_t>(4 * (size_t)sh.A * U);
   w.cont = c.take<ContLay>(sizeof(ContLay) * (size_t)sh.R);
   w.glob = g;
   *total = c.off;
@@ -336,27 +340,31 @@ int ebc_get_error_bounds(const ebc_ctx* c, float* eb_out, int T) {
   return EBC_OK;
 }
 
-uint64_t ebc_compress_bound(int64_t B, int T, int D) {
-  if (!shape_ok(B, T, D)) return 0;
-  const Shape sh = make_shape(B, T, D);
+static bool radius_ok(int radius) { return radius == kRadius || radius == kRadiusWide; }
+
+uint64_t ebc_compress_bound(int64_t B, int T, int D) { return ebc_compress_bound_radius(B, T, D, kRadius); }
+
+uint64_t ebc_compress_bound_radius(int64_t B, int T, int D, int radius) {
+  if (!shape_ok(B, T, D) || !radius_ok(radius)) return 0;
+  const Shape sh = make_shape(B, T, D, 0, 0, 1, radius);
   const uint64_t N = (uint64_t)B * T * D, nvec = (uint64_t)B * T;
   const uint64_t words = (N * (kLmax + 32) + 31) / 32 + 4ull * T * sh.nseg;
   return fixed_bytes(sh) + pad16h(nvec * 2u) + pad16h(nvec * sh.ref_bytes) + words * 4u;
 }
 
 // Sum of the data-independent bytes of the containers of R slices.
-static uint64_t fixed_bytes_sliced(int64_t B, int T, int D, int R) {
+static uint64_t fixed_bytes_sliced(int64_t B, int T, int D, int R, int radius) {
   const Shape all = make_shape(B, T, D, 0, 0, R);
   uint64_t n = 0;
-  for (int r = 0; r < R; ++r) n += fixed_bytes(make_shape(slice_rows(all, r), T, D));
+  for (int r = 0; r < R; ++r) n += fixed_bytes(make_shape(slice_rows(all, r), T, D, 0, 0, 1, radius));
   return n;
 }
 
-uint64_t ebc_compress_chunked_bound(int64_t B, int T, int D, int n_chunks) {
-  if (!shape_ok(B, T, D) || n_chunks < 1 || n_chunks > kMaxSlices) return 0;
+uint64_t ebc_compress_chunked_bound(int64_t B, int T, int D, int n_chunks, int radius) {
+  if (!shape_ok(B, T, D) || n_chunks < 1 || n_chunks > kMaxSlices || !radius_ok(radius)) return 0;
   const Shape all = make_shape(B, T, D, 0, 0, n_chunks);
   uint64_t n = 0;
-  for (int r = 0; r < n_chunks; ++r) n += ebc_compress_bound(slice_rows(all, r), T, D);
+  for (int r = 0; r < n_chunks; ++r) n += ebc_compress_bound_radius(slice_rows(all, r), T, D, radius);
   return n;
 }
 
@@ -382,8 +390,8 @@ static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T
     if (!eb_ok(ebs[t])) return EBC_ERR_INVALID_ARG;
     ep.eb[t] = ebs[t];
   }
-  const Shape sh = make_shape(B, T, D, c->nsm, c->window, R);
-  if (out_capacity < (R == 1 ? fixed_bytes(sh) : fixed_bytes_sliced(B, T, D, R))) return EBC_ERR_CAPACITY;
+  const Shape sh = make_shape(B, T, D, c->nsm, c->window, R, c->radius);
+  if (out_capacity < (R == 1 ? fixed_bytes(sh) : fixed_bytes_sliced(B, T, D, R, c->radius))) return EBC_ERR_CAPACITY;
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
   carve_compress(nullptr, sh, c->glob, &need);
@@ -398,16 +406,19 @@ static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T
   c->lastT = T;
   c->lastD = D;
   c->lastR = R;
+  c->lastRadius = c->radius;
   // Each call leaves its dedup table empty (k_emit).  A new layout on this
   // buffer starts from a reset.
   if (T > 0 && sh.nseg > 0 &&
-      (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D || c->cleanR != R)) {
+      (c->clean_buf != c->cbuf || c->cleanB != B || c->cleanT != T || c->cleanD != D || c->cleanR != R ||
+       c->cleanW != sh.W)) {
     if (cudaMemsetAsync(w.slots, 0xFF, 8 * (size_t)sh.U * sh.S, st) != cudaSuccess) return EBC_ERR_CUDA;
     c->clean_buf = c->cbuf;
     c->cleanB = B;
     c->cleanT = T;
     c->cleanD = D;
     c->cleanR = R;
+    c->cleanW = sh.W;
   }
   const cudaError_t e = launch_compress(d_x, bf16, sh, ep, w, (uint8_t*)d_out, out_capacity,
                                         (unsigned long long*)d_out_bytes, (unsigned long long*)d_offsets,
@@ -442,7 +453,7 @@ int ebc_compress_chunked_bf16(ebc_ctx* c, const uint16_t* d_x, int64_t B, int T,
 
 static int decompress_any(ebc_ctx* c, const void* d_in, uint64_t in_bytes, const uint64_t* d_offsets, int R,
                           float* d_xhat, int64_t B, int T, int D, void* stream) {
-  const Shape sh = make_shape(B, T, D, c->nsm, 0, R);
+  const Shape sh = make_shape(B, T, D, c->nsm, 0, R, c->radius);
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
   carve_decompress(nullptr, sh, c->glob, &need);
@@ -474,6 +485,12 @@ int ebc_decompress_chunked(ebc_ctx* c, const void* d_in, uint64_t in_bytes, cons
   return decompress_any(c, d_in, in_bytes, d_offsets, n_chunks, d_xhat, B, T, D, stream);
 }
 
+int ebc_set_radius(ebc_ctx* c, int radius) {
+  if (!c || !radius_ok(radius)) return EBC_ERR_INVALID_ARG;
+  c->radius = radius;
+  return EBC_OK;
+}
+
 int ebc_set_window(ebc_ctx* c, int window) {
   if (!c || window < 0 || window > kMaxWindow) return EBC_ERR_INVALID_ARG;
   c->window = window;
@@ -502,7 +519,7 @@ int ebc_get_table_stats(ebc_ctx* c, ebc_table_stats* out, int T) {
   if (!c || !out || T <= 0 || T != c->lastT) return EBC_ERR_INVALID_ARG;
   const int err = ebc_last_device_error(c);
   if (err == EBC_ERR_CUDA) return err;
-  const Shape sh = make_shape(c->lastB, T, c->lastD, c->nsm, c->window, c->lastR);
+  const Shape sh = make_shape(c->lastB, T, c->lastD, c->nsm, c->window, c->lastR, c->lastRadius);
   std::memset(out, 0, sizeof(*out) * (size_t)T);
   if (sh.nseg == 0 || !c->cbuf) return err;   // an empty batch: nothing was coded
   size_t need = 0;
@@ -596,7 +613,7 @@ int ebc_compress_host(ebc_ctx* c, const float* h_x, int64_t B, int T, int D, con
   const uint64_t N = (uint64_t)B * T * D;
   if (N > 0 && !h_x) return EBC_ERR_INVALID_ARG;
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
-  const uint64_t bound = ebc_compress_bound(B, T, D);
+  const uint64_t bound = ebc_compress_bound_radius(B, T, D, c->radius);
   int rc = grow(&c->stage_in, &c->stage_in_bytes, N * 4u);
   if (!rc) rc = grow(&c->stage_out, &c->stage_out_bytes, bound);
   if (rc) return rc;
@@ -691,7 +708,7 @@ static int run_mode(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const
   int rc = ebc_set_table_modes(c, modes, T);
   if (rc) return rc;
   const uint64_t N = (uint64_t)B * T * D;
-  const uint64_t cap = ebc_compress_bound(B, T, D);
+  const uint64_t cap = ebc_compress_bound_radius(B, T, D, c->radius);
   rc = grow(&c->stage_out, &c->stage_out_bytes, cap);
   if (!rc) rc = grow(&c->stage_in, &c->stage_in_bytes, N * 4u);
   if (rc) return rc;
@@ -732,9 +749,9 @@ int ebc_select_table_modes(ebc_ctx* c, const float* d_x, int64_t B, int T, int D
   const int saved_T = c->modes_T;
   uint8_t saved[kMaxT];
   std::memcpy(saved, c->h_modes, (size_t)kMaxT);
-  const Shape sh = make_shape(B, T, D, c->nsm, c->window);
+  const Shape sh = make_shape(B, T, D, c->nsm, c->window, 1, c->radius);
   const double raw_bytes = 4.0 * (double)B * D;   // per table
-  const double fixed = (double)kTableRecBytes + (double)kSegRecBytes * sh.nseg + 4.0 * sh.nw;
+  const double fixed = (double)table_rec_bytes(sh.A) + (double)kSegRecBytes * sh.nseg + 4.0 * sh.nw;
   double* cr = new (std::nothrow) double[(size_t)T * 4];
   ebc_table_stats* st = new (std::nothrow) ebc_table_stats[(size_t)T];
   double tc[4], td[4];
@@ -773,7 +790,7 @@ int ebc_table_homo_index(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, 
     for (int t = 0; t < T; ++t) tiny[t] = 1.17549435e-38f;   // the smallest admissible bound
     rc = ebc_set_table_modes(c, nullptr, 0);
   }
-  const uint64_t cap = ebc_compress_bound(B, T, D);
+  const uint64_t cap = ebc_compress_bound_radius(B, T, D, c->radius);
   if (!rc) rc = grow(&c->stage_out, &c->stage_out_bytes, cap);
   cudaStream_t s = (cudaStream_t)stream;
   if (!rc) rc = ebc_compress(c, d_x, B, T, D, eb, c->stage_out, cap, (uint64_t*)c->d_nbytes, s);

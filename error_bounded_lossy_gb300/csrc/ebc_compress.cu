@@ -24,6 +24,7 @@
 #include <cudaTypedefs.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "ebc_internal.cuh"
 
@@ -55,6 +56,53 @@ __device__ __forceinline__ uint32_t quantize_four(float4 v, float eb, float ebx2
   return __byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u) ^ 0x80808080u;
 }
 
+// The wide alphabet (radius 512): four 16-bit codes q + 512 in two words.  The
+// low half-word of y's bits is q mod 2^16; a rejected element takes 0xFE00,
+// and a per-half-word add of 512 (no carry between the halves) gives the code.
+__device__ __forceinline__ uint2 quantize_four_wide(float4 v, float eb, float ebx2, float inv, bool ok[4]) {
+  const float xs[4] = {v.x, v.y, v.z, v.w};
+  uint32_t u[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float t = __fmul_rn(xs[k], inv);
+    const float y = __fadd_rn(t, 12582912.0f);       // 1.5 * 2^23
+    const float qf = __fsub_rn(y, 12582912.0f);      // exact when |t| < 2^22
+    const float err = fabsf(__fsub_rn(xs[k], __fmul_rn(qf, ebx2)));
+    ok[k] = (fabsf(t) < 511.5f) & (err <= eb);        // false for NaN and +-inf too
+    u[k] = ok[k] ? __float_as_uint(y) : 0xFE00u;
+  }
+  return make_uint2(__vadd2(__byte_perm(u[0], u[1], 0x5410u), 0x02000200u),
+                    __vadd2(__byte_perm(u[2], u[3], 0x5410u), 0x02000200u));
+}
+
+template <int W>
+__device__ __forceinline__ typename QuadOf<W>::T quantize_quad(float4 v, float eb, float ebx2, float inv, bool ok[4]) {
+  if constexpr (W == 1) return quantize_four(v, eb, ebx2, inv, ok);
+  else return quantize_four_wide(v, eb, ebx2, inv, ok);
+}
+
+// The dedup key's terms for four codes at element d of the row: one word of
+// four codes, or two words of two codes (word index k = d / 4 or d / 2).
+__device__ __forceinline__ uint32_t quad_key(uint32_t v, int d) {
+  return lowbias32(v + (uint32_t)(d >> 2) * 0x9E3779B9u);
+}
+__device__ __forceinline__ uint32_t quad_key(uint2 v, int d) {
+  return lowbias32(v.x + (uint32_t)(d >> 1) * 0x9E3779B9u) + lowbias32(v.y + (uint32_t)((d >> 1) + 1) * 0x9E3779B9u);
+}
+
+// Four codes from the code scratch (element index e of a table; W bytes each).
+__device__ __forceinline__ uint32_t ld_quad(const uint8_t* symt, size_t e, uint32_t*) {
+  return __ldcg(reinterpret_cast<const unsigned int*>(symt + e));
+}
+__device__ __forceinline__ uint2 ld_quad(const uint8_t* symt, size_t e, uint2*) {
+  return __ldcg(reinterpret_cast<const uint2*>(symt + 2 * e));
+}
+// ... and from a shared-memory copy, at 32-bit word index i (even for W = 2)
+__device__ __forceinline__ uint32_t sm_quad(const uint32_t* s, int i, uint32_t*) { return s[i]; }
+__device__ __forceinline__ uint2 sm_quad(const uint32_t* s, int i, uint2*) {
+  return *reinterpret_cast<const uint2*>(s + i);
+}
+
 // Input element types: fp32, or bf16 carried as its 16 raw bits (its fp32
 // value is exact: the bf16 bits followed by 16 zero bits).
 __device__ __forceinline__ uint32_t raw32(float v) { return __float_as_uint(v); }
@@ -76,6 +124,14 @@ __device__ __forceinline__ unsigned long long l2_evict_last() {
 // read-once input streams through.
 __device__ __forceinline__ void st_keep_u32(uint32_t* p, uint32_t v, unsigned long long pol) {
   asm volatile("st.global.L2::cache_hint.b32 [%0], %1, %2;" ::"l"(p), "r"(v), "l"(pol) : "memory");
+}
+// Four codes into the code scratch at element e of a table.
+__device__ __forceinline__ void st_keep_quad(uint8_t* symt, size_t e, uint32_t v, unsigned long long pol) {
+  st_keep_u32(reinterpret_cast<uint32_t*>(symt + e), v, pol);
+}
+__device__ __forceinline__ void st_keep_quad(uint8_t* symt, size_t e, uint2 v, unsigned long long pol) {
+  asm volatile("st.global.L2::cache_hint.v2.b32 [%0], {%1, %2}, %3;" ::"l"(symt + 2 * e), "r"(v.x), "r"(v.y), "l"(pol)
+               : "memory");
 }
 
 __device__ __forceinline__ void dedup_insert(unsigned long long* slots, uint32_t S, uint32_t h, uint32_t b,
@@ -205,12 +261,14 @@ __device__ __forceinline__ void issue_segment_tile(In* stage, const CUtensorMap*
 // wrapping sum over its 4-code words w_k of lowbias32(w_k + k * 0x9E3779B9)
 // plus lowbias32(raw ^ (d + 1) * 0x85EBCA6B) for each outlier at position d.
 // ---------------------------------------------------------------------------
-template <int D, typename In>
+template <int D, typename In, int W>
 __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtensorMap tmap, Shape sh, EbParams ep,
                                                    Work w) {
   pdl_enter();
   using G = Geo<D>;
   using Q = QGeo<D, In>;
+  using Quad = typename QuadOf<W>::T;
+  constexpr int kA = Alph<W>::kA;
   extern __shared__ __align__(128) unsigned char s_raw[];   // 2 stages of kStageFloats elements
   In* s_x = reinterpret_cast<In*>(s_raw);
   __shared__ __align__(8) uint64_t s_bar[2];
@@ -238,7 +296,7 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     if (s == 0) {   // per-call accumulators of the table's units, which k_resolve adds to
       for (int r = 0; r < sh.R; ++r) {
         const int u = r * sh.T + t;
-        w.tab_hist[(size_t)u * 256 + tid] = 0u;
+        for (int i = tid; i < kA; i += 256) w.tab_hist[(size_t)u * kA + i] = 0u;
         if (tid == 0) w.tab_cnt[u] = make_uint4(0, 0, 0, 0);
       }
     }
@@ -264,10 +322,9 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
       const bool valid = b < B;
       const float4 v = load4(xs + Q::offset(r, d));
       bool ok[4];
-      const uint32_t word = quantize_four(v, eb, ebx2, inv, ok);
-      if (valid)
-        st_keep_u32(reinterpret_cast<uint32_t*>(w.sym + (size_t)t * sh.symstride + (size_t)b * D + d), word, pol);
-      acc += lowbias32(word + (uint32_t)(d >> 2) * 0x9E3779B9u);
+      const Quad word = quantize_quad<W>(v, eb, ebx2, inv, ok);
+      if (valid) st_keep_quad(w.sym + (size_t)t * sh.symstride, (size_t)b * D + d, word, pol);
+      acc += quad_key(word, d);
       if (!(ok[0] & ok[1] & ok[2] & ok[3])) {
         if (!ok[0]) { acc += lowbias32(__float_as_uint(v.x) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu); ++nout; }
         if (!ok[1]) { acc += lowbias32(__float_as_uint(v.y) ^ (uint32_t)(d + 2) * 0x85EBCA6Bu); ++nout; }
@@ -324,9 +381,6 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
   }
 }
 
-__device__ __forceinline__ bool has_zero_byte(uint32_t v) {
-  return ((v - 0x01010101u) & ~v & 0x80808080u) != 0u;
-}
 
 // ---------------------------------------------------------------------------
 // k_resolve: vector-based LZ with the whole batch as window and the first
@@ -337,23 +391,27 @@ __device__ __forceinline__ bool has_zero_byte(uint32_t v) {
 // ---------------------------------------------------------------------------
 constexpr int kResolveThreads = 64;   // two warps per segment: many segments in flight per SM
 
-template <int D, typename In>
+template <int D, typename In, int W>
 __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restrict__ x, Shape sh, Work w) {
   pdl_enter();
   using G = Geo<D>;
+  using Quad = typename QuadOf<W>::T;
+  constexpr int kA = Alph<W>::kA;
   constexpr int kNT = kResolveThreads, kNW = kNT / 32;
   constexpr int kRPT = (G::kSB + kNT - 1) / kNT;          // rows per thread in the lookups
   constexpr int kSteps = G::kSB / kNW / G::kRPS;         // warp steps (kRPS rows each) per warp
   constexpr int kGroup = kSteps < 8 ? kSteps : 8;        // steps whose loads are issued together
-  __shared__ uint32_t s_hist[kNW][256];
-  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4 + 4];   // the segment's own codes
+  // window mode: keys of rows row0 - window .. row0 + SB during the lookups; then the literal
+  // code histograms, one per warp
+  constexpr int kHistWin = kNW * kA > kMaxWindow + G::kSB ? kNW * kA : kMaxWindow + G::kSB;
+  __shared__ uint32_t s_histwin[kHistWin];
+  uint32_t* s_win = s_histwin;
+  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms * W / 4 + 4];   // the segment's own codes
   __shared__ uint32_t s_ref[G::kSB];
   __shared__ uint32_t s_nout[G::kSB];
-  __shared__ uint32_t s_win[kMaxWindow + G::kSB];   // window mode: keys of rows row0 - window .. row0 + SB
   __shared__ uint32_t s_bm[G::kBmWords];
   __shared__ uint32_t s_cnt[3];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  for (int i = tid; i < kNW * 256; i += kNT) (&s_hist[0][0])[i] = 0u;
   for (int i = tid; i < G::kBmWords; i += kNT) s_bm[i] = 0u;
   if (tid < 3) s_cnt[tid] = 0u;
 
@@ -371,13 +429,14 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   const unsigned long long* slots = w.slots + (size_t)u * sh.S;
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
   const bool nodedup = w.modes && (w.modes[t] & kModeNoDedup);   // every row its own reference
-  // the segment's codes start so words into s_sym (a slice may start off a 16-byte boundary when D < 16)
-  const int so = D >= 16 ? 0 : (int)(((size_t)row0 * D) & 15u) / 4;
+  // the segment's codes start so words into s_sym (a slice may start off a 16-byte boundary when
+  // D * W < 16; so is even when W = 2)
+  const int so = D * W >= 16 ? 0 : (int)(((size_t)row0 * D * W) & 15u) / 4;
   {   // the segment's codes (rows contiguous; the table stride is padded to 16 bytes), copied
       // asynchronously while the keys are looked up
     const int64_t nrows = bend - row0 < G::kSB ? bend - row0 : G::kSB;
-    const int nq = nrows > 0 ? (int)((so * 4 + nrows * D + 15) / 16) : 0;
-    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D - so * 4);
+    const int nq = nrows > 0 ? (int)((so * 4 + nrows * D * W + 15) / 16) : 0;
+    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D * W - so * 4);
     for (int i = tid; i < nq; i += kNT) cp_async16(reinterpret_cast<uint4*>(s_sym) + i, src + i);
   }
   if (sh.window > 0 && !nodedup) {
@@ -435,15 +494,17 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   }
   cp_async_wait_all();
   __syncthreads();
+  for (int i = tid; i < kNW * kA; i += kNT) s_histwin[i] = 0u;   // the window keys are no longer needed
+  __syncthreads();
 
-  uint32_t* hist = s_hist[warp];
+  uint32_t* hist = s_histwin + warp * kA;
   const unsigned gshift = lane & ~(G::kLPR - 1);
   const unsigned gmask = (G::kLPR == 32 ? 0xffffffffu : ((1u << G::kLPR) - 1u)) << gshift;
   const bool leader = (lane % G::kLPR) == 0;
   uint32_t n_lit = 0, n_match = 0, n_out = 0;
   // the reference rows' codes of a group of steps (the next group's loads are in flight while
   // this one is compared)
-  auto load_refs = [&](int g0, uint32_t (&wr)[kGroup][G::kSPR]) {
+  auto load_refs = [&](int g0, Quad (&wr)[kGroup][G::kSPR]) {
 #pragma unroll
     for (int it = 0; it < kGroup; ++it) {
       const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
@@ -452,11 +513,11 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
         const int d = (lane % G::kLPR) * 4 + j * 128;
-        wr[it][j] = ref != (uint32_t)b ? __ldcg(reinterpret_cast<const unsigned int*>(symt + (size_t)ref * D + d)) : 0u;
+        wr[it][j] = ref != (uint32_t)b ? ld_quad(symt, (size_t)ref * D + d, (Quad*)nullptr) : Quad{};
       }
     }
   };
-  auto process = [&](int g0, const uint32_t (&wr)[kGroup][G::kSPR]) {
+  auto process = [&](int g0, const Quad (&wr)[kGroup][G::kSPR]) {
 #pragma unroll
     for (int it = 0; it < kGroup; ++it) {
       const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
@@ -464,19 +525,19 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
       const bool valid = b < bend;
       const uint32_t ref = valid ? s_ref[rr] : 0u;
       const bool cand = valid && ref != (uint32_t)b;
-      uint32_t wb[G::kSPR];
+      Quad wb[G::kSPR];
       bool eq = true;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        wb[j] = s_sym[so + rr * (D / 4) + (lane % G::kLPR) + j * 32];
-        bool e = wr[it][j] == wb[j];
-        if (cand && e && has_zero_byte(wb[j])) {
+        wb[j] = sm_quad(s_sym, so + (rr * (D / 4) + (lane % G::kLPR) + j * 32) * W, (Quad*)nullptr);
+        bool e = quad_eq(wr[it][j], wb[j]);
+        if (cand && e && quad_has_zero(wb[j])) {
           const int d = (lane % G::kLPR) * 4 + j * 128;
           const In* xb = x + ((size_t)b * T + t) * D + d;
           const In* xr = x + ((size_t)ref * T + t) * D + d;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (((wb[j] >> (8 * q)) & 0xffu) == 0u && raw32(xb[q]) != raw32(xr[q])) e = false;
+            if (quad_code(wb[j], q) == 0u && raw32(xb[q]) != raw32(xr[q])) e = false;
         }
         eq = eq && e;
       }
@@ -485,11 +546,8 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
       if (valid && !match) {
 #pragma unroll
         for (int j = 0; j < G::kSPR; ++j) {
-          const uint32_t v = wb[j];
-          atomicAdd(&hist[v & 0xffu], 1u);
-          atomicAdd(&hist[(v >> 8) & 0xffu], 1u);
-          atomicAdd(&hist[(v >> 16) & 0xffu], 1u);
-          atomicAdd(&hist[v >> 24], 1u);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) atomicAdd(&hist[quad_code(wb[j], q)], 1u);
         }
       }
       if (valid && leader) {
@@ -504,7 +562,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
       }
     }
   };
-  uint32_t wr0[kGroup][G::kSPR], wr1[kGroup][G::kSPR];
+  Quad wr0[kGroup][G::kSPR], wr1[kGroup][G::kSPR];
   load_refs(0, wr0);
 #pragma unroll 1
   for (int g0 = 0; g0 < kSteps; g0 += 2 * kGroup) {
@@ -525,12 +583,12 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   }
   __syncthreads();
 #pragma unroll
-  for (int i = tid; i < 256; i += kNT) {
+  for (int i = tid; i < kA; i += kNT) {
     uint32_t f = 0;
 #pragma unroll
-    for (int k = 0; k < kNW; ++k) f += s_hist[k][i];
-    w.seg_hist[(size_t)seg * 256 + i] = f;
-    if (f) atomicAdd(&w.tab_hist[(size_t)u * 256 + i], f);
+    for (int k = 0; k < kNW; ++k) f += s_histwin[k * kA + i];
+    w.seg_hist[(size_t)seg * kA + i] = f;
+    if (f) atomicAdd(&w.tab_hist[(size_t)u * kA + i], f);
   }
   for (int i = tid; i < G::kBmWords; i += kNT) {   // bit i of word k: row b0 + 32 k + i of the slice
     const int64_t wi = (int64_t)s * G::kBmWords + i;
@@ -619,7 +677,7 @@ __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Wor
     const unsigned long long nseg_r = (unsigned long long)div_up(n, sh.SB);
     const unsigned long long nw_r = (unsigned long long)div_up(n, 32);
     c.ref_bytes = (uint32_t)ref_bytes_of(n, sh.window);
-    c.off_seg = kHeaderBytes + (unsigned long long)T * kTableRecBytes;
+    c.off_seg = kHeaderBytes + (unsigned long long)T * table_rec_bytes(sh.A);
     c.off_bitmap = c.off_seg + (unsigned long long)T * nseg_r * kSegRecBytes;
     c.off_chunks = c.off_bitmap + pad16((unsigned long long)T * nw_r * 4ull);
     c.off_refs = c.off_chunks + pad16(c.n_chunks * 2ull);
@@ -653,7 +711,7 @@ __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Wor
     const int64_t n = slice_rows(sh, tid);
     if (c.base + kHeaderBytes <= cap) {
       st_u32(o + 0, kMagic); st_u32(o + 4, kFormatVersion); st_u64(o + 8, (unsigned long long)n);
-      st_u32(o + 16, (uint32_t)T); st_u32(o + 20, (uint32_t)sh.D); st_u32(o + 24, kRadius);
+      st_u32(o + 16, (uint32_t)T); st_u32(o + 20, (uint32_t)sh.D); st_u32(o + 24, (uint32_t)(sh.A / 2));
       st_u32(o + 28, kLmax); st_u32(o + 32, (uint32_t)sh.SB); st_u32(o + 36, (uint32_t)sh.KC);
       st_u32(o + 40, c.ref_bytes); st_u32(o + 44, (uint32_t)sh.window);
       st_u64(o + 48, c.n_lit); st_u64(o + 56, c.n_match); st_u64(o + 64, c.n_out); st_u64(o + 72, c.n_chunks);
@@ -672,13 +730,13 @@ __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Wor
     }
   }
   if (sh.nseg == 0 && status == EBC_OK) {   // an empty batch: every table record is eb and zeros
-    const int per = (int)(kTableRecBytes / 4);
+    const int per = (int)(table_rec_bytes(sh.A) / 4);
     const long long nrec = (long long)sh.R * T * per;
     for (long long i = tid; i < nrec; i += blockDim.x) {
       const int r = (int)(i / ((long long)T * per));
       const int t = (int)((i / per) % T);
       const int k = (int)(i % per);
-      uint32_t* rec = reinterpret_cast<uint32_t*>(out + s_size[r] + kHeaderBytes + (size_t)t * kTableRecBytes);
+      uint32_t* rec = reinterpret_cast<uint32_t*>(out + s_size[r] + kHeaderBytes + (size_t)t * (per * 4));
       rec[k] = k == 0 ? __float_as_uint(ep.eb[t]) : 0u;
     }
   }
@@ -720,6 +778,163 @@ __device__ __forceinline__ unsigned long long bitonic_sort256(unsigned long long
   return v;
 }
 
+// The code of one unit over the wide alphabet (1024 symbols, 4 per thread):
+// the same construction as for 256 symbols (two-queue Huffman over the leaves
+// sorted by (count, symbol), ties to the leaf, halving above 24 bits;
+// canonical values by the DEFLATE rule), with the leaf order and the canonical
+// ranks taken from shared-memory sorts.  Writes tabcode, tab_bits, tab_rec.
+__device__ void huffman_wide(const Shape& sh, const EbParams& ep, const Work& w, int u, int t, bool raw,
+                             uint32_t* s_f, uint32_t* s_lw, uint32_t* s_nodew, unsigned long long* s_key,
+                             uint16_t* s_order, uint16_t* s_leafpar, uint16_t* s_nodepar, uint16_t* s_depth,
+                             uint8_t* s_len, uint32_t* s_count, uint32_t* s_next, uint32_t* s_offl,
+                             unsigned long long* s_bits64, int* s_maxlen, int* s_n) {
+  constexpr int kA = Alph<2>::kA, kPer = kA / 256;
+  const int tid = threadIdx.x;
+  uint32_t f0[kPer];
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int sy = k * 256 + tid;
+    // (with no segments, k_quantize did not run and the accumulators are stale)
+    f0[k] = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)u * kA + sy]) : 0u;
+    s_f[sy] = f0[k];
+    s_len[sy] = raw ? (uint8_t)Alph<2>::kRawLen : 0;
+  }
+  __syncthreads();
+  for (int round = 0; round < 40 && !raw; ++round) {
+    if (tid == 0) {
+      *s_n = 0;
+      *s_maxlen = 0;
+    }
+    __syncthreads();
+    int mine = 0;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int sy = k * 256 + tid;
+      const uint32_t fi = s_f[sy];
+      s_key[sy] = fi > 0u ? ((unsigned long long)fi << 10) | (unsigned)sy : ~0ull;
+      s_len[sy] = 0;
+      mine += fi > 0u;
+    }
+    atomicAdd(s_n, mine);
+    __syncthreads();
+    bitonic_sort_smem(s_key, kA);   // leaves in (count, symbol) order, absent symbols last
+    const int n = *s_n;
+    for (int i = tid; i < n; i += 256) {
+      s_order[i] = (uint16_t)(s_key[i] & 1023u);
+      s_lw[i] = (uint32_t)(s_key[i] >> 10);
+    }
+    __syncthreads();
+    if (tid == 0 && n >= 2) {   // the two queues: leaves in order, merged nodes first in first out
+      constexpr uint32_t kNone = 0xFFFFFFFFu;
+      int li = 0, qi = 0, qn = 0;
+      uint32_t a0 = s_lw[0], a1 = s_lw[1], q0 = kNone, q1 = kNone;
+      for (int m = 0; m < n - 1; ++m) {
+        uint32_t wsum = 0;
+#pragma unroll
+        for (int pick = 0; pick < 2; ++pick) {
+          if (a0 <= q0) {   // a leaf (ties go to the leaf)
+            s_leafpar[li] = (uint16_t)m;
+            wsum += a0;
+            ++li;
+            a0 = a1;
+            a1 = li + 1 < n ? s_lw[li + 1] : kNone;
+          } else {
+            s_nodepar[qi] = (uint16_t)m;
+            wsum += q0;
+            ++qi;
+            q0 = q1;
+            q1 = qi + 1 < qn ? s_nodew[qi + 1] : kNone;
+          }
+        }
+        s_nodew[qn] = wsum;
+        if (qn == qi) q0 = wsum;
+        else if (qn == qi + 1) q1 = wsum;
+        ++qn;
+      }
+    }
+    __syncthreads();
+    for (int m = tid; m < n - 1; m += 256) {   // depth of each merged node: walk up to the root (node n-2)
+      int a = m, d = 0;
+      while (a != n - 2) {
+        a = s_nodepar[a];
+        ++d;
+      }
+      s_depth[m] = (uint16_t)d;
+    }
+    __syncthreads();
+    if (n == 1 && tid == 0) {
+      s_len[s_order[0]] = 1;
+      *s_maxlen = 1;
+    }
+    if (n >= 2)
+      for (int i = tid; i < n; i += 256) {
+        const int l = s_depth[s_leafpar[i]] + 1;
+        s_len[s_order[i]] = (uint8_t)(l < 255 ? l : 255);
+        atomicMax(s_maxlen, l);
+      }
+    __syncthreads();
+    if (*s_maxlen <= kLmax) break;
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      const int sy = k * 256 + tid;
+      const uint32_t fi = s_f[sy];
+      if (fi > 0u) s_f[sy] = (fi >> 1) > 0u ? (fi >> 1) : 1u;
+    }
+    __syncthreads();
+  }
+  // canonical codes: counts per length, first code and first rank of each length, then each
+  // symbol's rank among its length from a sort by (length, symbol)
+  if (tid < kLmax + 2) s_count[tid] = 0;
+  __syncthreads();
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int sy = k * 256 + tid;
+    const uint32_t L = s_len[sy];
+    if (L) atomicAdd(&s_count[L], 1u);
+    s_key[sy] = L ? ((unsigned long long)L << 10) | (unsigned)sy : ~0ull;
+    s_lw[sy] = 0u;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t c = 0, off = 0;
+    s_count[0] = 0;
+    for (int l = 1; l <= kLmax; ++l) {
+      c = (c + s_count[l - 1]) << 1;
+      s_next[l] = c;
+      s_offl[l] = off;
+      off += s_count[l];
+    }
+  }
+  bitonic_sort_smem(s_key, kA);
+  for (int p = tid; p < kA; p += 256) {
+    const unsigned long long key = s_key[p];
+    if (key != ~0ull) {
+      const uint32_t sy = (uint32_t)(key & 1023u), L = (uint32_t)(key >> 10);
+      s_lw[sy] = ((s_next[L] + ((uint32_t)p - s_offl[L])) << 8) | L;
+    }
+  }
+  __syncthreads();
+  unsigned long long sum = 0;   // bits of the unit's literal codes, plus the raw bits of its outliers
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const int sy = k * 256 + tid;
+    const uint32_t e = s_lw[sy];
+    w.tabcode[(size_t)u * kA + sy] = e;
+    sum += (unsigned long long)f0[k] * (e & 0xffu) + (sy == 0 ? 32ull * f0[k] : 0ull);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+  if ((tid & 31) == 0) s_bits64[tid >> 5] = sum;
+  __syncthreads();
+  if (tid == 0) {
+    unsigned long long tot = 0;
+    for (int k = 0; k < 8; ++k) tot += s_bits64[k];
+    w.tab_bits[u] = tot;
+    const uint4 tc = sh.nseg > 0 ? __ldcg(&w.tab_cnt[u]) : make_uint4(0, 0, 0, 0);
+    w.tab_rec[u] = make_uint4(__float_as_uint(ep.eb[t]), tc.x, tc.y, tc.z);   // head of the table record
+  }
+}
+
 // ---------------------------------------------------------------------------
 // k_codebook: one CTA per unit.  Huffman code lengths (§III-D "Optimized
 // Entropy Encoding") by the two-queue construction over leaves sorted by
@@ -728,18 +943,22 @@ __device__ __forceinline__ unsigned long long bitonic_sort256(unsigned long long
 // code is rebuilt.  Canonical code values follow the DEFLATE rule.  The last
 // CTA to finish lays out the containers and writes their headers.
 // ---------------------------------------------------------------------------
+template <int W>
 __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w, uint8_t* __restrict__ out,
                                                    unsigned long long cap, unsigned long long* out_bytes,
                                                    unsigned long long* chunk_off, uint32_t epoch) {
   pdl_enter();
-  __shared__ uint32_t s_f[256], s_lw[256], s_nodew[256];
-  __shared__ unsigned long long s_key[256];
+  constexpr int kA = Alph<W>::kA;
+  using Par = typename std::conditional<W == 1, uint8_t, uint16_t>::type;   // node indices and depths
+  __shared__ uint32_t s_f[kA], s_lw[kA], s_nodew[kA];
+  __shared__ unsigned long long s_key[kA];
   __shared__ uint4 s_seg[kFoldMaxSeg];
   __shared__ unsigned long long s_bits64[8];
-  __shared__ uint16_t s_order[256];
-  __shared__ uint8_t s_leafpar[256], s_nodepar[256], s_depth[256], s_len[256];
-  __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2];
-  __shared__ int s_maxlen, s_last;
+  __shared__ uint16_t s_order[kA];
+  __shared__ Par s_leafpar[kA], s_nodepar[kA], s_depth[kA];
+  __shared__ uint8_t s_len[kA];
+  __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offl[kLmax + 2];
+  __shared__ int s_maxlen, s_last, s_n;
   __shared__ uint4 s_warp[8];
   __shared__ uint4 s_cpre[kMaxSlices + 1], s_wpre[kMaxSlices + 1];   // unit prefixes at container starts
   const int tid = threadIdx.x;
@@ -750,10 +969,14 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
 
   if (u < U) {
     const int t = u % T;
+    const bool raw = w.modes && (w.modes[t] & kModeRawCodes);   // every code log2(A) bits: no Huffman
+    if constexpr (W == 2) {
+      huffman_wide(sh, ep, w, u, t, raw, s_f, s_lw, s_nodew, s_key, s_order, s_leafpar, s_nodepar, s_depth, s_len,
+                   s_count, s_next, s_offl, s_bits64, &s_maxlen, &s_n);
+    } else {
     // (with no segments, k_quantize did not run and the accumulators are stale)
     const uint32_t f0 = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)u * 256 + tid]) : 0u;
     s_f[tid] = f0;
-    const bool raw = w.modes && (w.modes[t] & kModeRawCodes);   // every code 8 bits: no Huffman
     if (raw) s_len[tid] = 8;
     __syncthreads();
     for (int round = 0; round < 40 && !raw; ++round) {
@@ -859,24 +1082,28 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
         w.tab_rec[u] = make_uint4(__float_as_uint(ep.eb[t]), tc.x, tc.y, tc.z);   // head of the table record
       }
     }
+    }   // W == 1
     if (sh.fold && sh.nseg > 0) {
       // this unit's segments: bits = sum over codes of count * length (+32 raw bits per outlier),
       // one warp per segment; then offsets relative to the unit (a scan) and the unit's totals
       const int warp = tid >> 5, lane = tid & 31;
-      const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * 256) + lane * 2;
-      __syncthreads();   // tabcode of this table is written
-      const uint4 c0 = __ldcg(cp), c1 = __ldcg(cp + 1);
-      constexpr int kBatch = 4;   // segments whose histograms are loaded together
+      constexpr int kV = kA / 128;                  // uint4 of histogram and codes per lane
+      constexpr int kBatch = W == 1 ? 4 : 1;        // segments whose histograms are loaded together
+      const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * kA) + lane * kV;
+      __syncthreads();   // tabcode of this unit is written
+      uint4 c[kV];
+#pragma unroll
+      for (int v = 0; v < kV; ++v) c[v] = __ldcg(cp + v);
       for (int i0 = warp; i0 < sh.nseg; i0 += 8 * kBatch) {
-        uint4 h0[kBatch], h1[kBatch], cnt[kBatch];
+        uint4 h[kBatch][kV], cnt[kBatch];
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
           const int i = i0 + 8 * q;
           if (i < sh.nseg) {
             const int seg = u * sh.nseg + i;
-            const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * 256) + lane * 2;
-            h0[q] = __ldcg(hp);
-            h1[q] = __ldcg(hp + 1);
+            const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * kA) + lane * kV;
+#pragma unroll
+            for (int v = 0; v < kV; ++v) h[q][v] = __ldcg(hp + v);
             cnt[q] = lane == 0 ? __ldcg(&w.seg_cnt[seg]) : make_uint4(0, 0, 0, 0);
           }
         }
@@ -884,10 +1111,12 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
         for (int q = 0; q < kBatch; ++q) {
           const int i = i0 + 8 * q;
           if (i < sh.nseg) {
-            uint32_t bits = h0[q].x * (c0.x & 0xffu) + h0[q].y * (c0.y & 0xffu) + h0[q].z * (c0.z & 0xffu) +
-                            h0[q].w * (c0.w & 0xffu) + h1[q].x * (c1.x & 0xffu) + h1[q].y * (c1.y & 0xffu) +
-                            h1[q].z * (c1.z & 0xffu) + h1[q].w * (c1.w & 0xffu);
-            if (lane == 0) bits += 32u * h0[q].x;   // symbol 0: the outliers' raw bits
+            uint32_t bits = 0;
+#pragma unroll
+            for (int v = 0; v < kV; ++v)
+              bits += h[q][v].x * (c[v].x & 0xffu) + h[q][v].y * (c[v].y & 0xffu) + h[q][v].z * (c[v].z & 0xffu) +
+                      h[q][v].w * (c[v].w & 0xffu);
+            if (lane == 0) bits += 32u * h[q][0].x;   // symbol 0: the outliers' raw bits
             bits = __reduce_add_sync(0xffffffffu, bits);
             if (lane == 0) s_seg[i] = make_uint4(((bits + 127u) >> 7) * 4u, cnt[q].w, cnt[q].y, bits);
           }
@@ -997,6 +1226,7 @@ __device__ __forceinline__ uint32_t valid_mask(int64_t B, int64_t row0, int wi) 
 // bases (an exclusive scan) and completes the header (bitstream words, total
 // size) and the capacity check.  No CTA waits on another.
 // ---------------------------------------------------------------------------
+template <int W>
 __global__ void __launch_bounds__(256) k_layout(Shape sh, EbParams ep, Work w, uint8_t* __restrict__ out,
                                                  unsigned long long cap, unsigned long long* out_bytes,
                                                  unsigned long long* chunk_off, uint32_t epoch) {
@@ -1013,14 +1243,19 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, EbParams ep, Work w, u
   uint4 a = make_uint4(0, 0, 0, 0);   // {words, chunks, matches, -}
   uint32_t bits = 0;
   if (seg < nsegT) {
+    constexpr int kA = Alph<W>::kA, kV = kA / 128;   // uint4 of histogram and codes per lane
     const int u = seg / sh.nseg;
-    const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * 256) + lane * 2;
-    const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * 256) + lane * 2;
-    const uint4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1), c0 = __ldcg(cp), c1 = __ldcg(cp + 1);
+    const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * kA) + lane * kV;
+    const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * kA) + lane * kV;
     const uint4 cnt = __ldcg(&w.seg_cnt[seg]);
-    bits = h0.x * (c0.x & 0xffu) + h0.y * (c0.y & 0xffu) + h0.z * (c0.z & 0xffu) + h0.w * (c0.w & 0xffu) +
-           h1.x * (c1.x & 0xffu) + h1.y * (c1.y & 0xffu) + h1.z * (c1.z & 0xffu) + h1.w * (c1.w & 0xffu);
-    if (lane == 0) bits += 32u * h0.x;   // symbol 0: the outliers' raw bits
+    uint32_t h0x = 0;
+#pragma unroll
+    for (int v = 0; v < kV; ++v) {
+      const uint4 h = __ldcg(hp + v), c = __ldcg(cp + v);
+      bits += h.x * (c.x & 0xffu) + h.y * (c.y & 0xffu) + h.z * (c.z & 0xffu) + h.w * (c.w & 0xffu);
+      if (v == 0) h0x = h.x;
+    }
+    if (lane == 0) bits += 32u * h0x;   // symbol 0: the outliers' raw bits
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) bits += __shfl_xor_sync(0xffffffffu, bits, off);
     a = make_uint4(((bits + 127u) >> 7) * 4u, cnt.w, cnt.y, 0u);
@@ -1091,16 +1326,18 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, EbParams ep, Work w, u
 // stored with 16-byte writes; a segment larger than the copy (24 bits per
 // code on average) is ORed straight into the zeroed output.
 // ---------------------------------------------------------------------------
-template <int D, typename In>
+template <int D, typename In, int W>
 __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape sh, Work w,
                                                uint8_t* __restrict__ out, unsigned long long cap, uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
+  using Quad = typename QuadOf<W>::T;
+  constexpr int kA = Alph<W>::kA;
   constexpr int kRPT = (G::kSB + 255) / 256;   // rows (and ranks) per thread
   constexpr uint32_t kSmemWords = (uint32_t)G::kSegSyms * 3u / 4u;
   extern __shared__ __align__(16) uint32_t s_bits[];
-  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms / 4 + 4];   // the segment's codes, row-major
-  __shared__ uint32_t s_code[256];
+  __shared__ __align__(16) uint32_t s_sym[G::kSegSyms * W / 4 + 4];   // the segment's codes, row-major
+  __shared__ uint32_t s_code[kA];
   __shared__ uint32_t s_bm[G::kBmWords];      // match bits
   __shared__ uint32_t s_lit[G::kBmWords];     // literal bits
   __shared__ uint32_t s_pre[G::kBmWords];     // literal (low 16) and match (high 16) rows before each word
@@ -1122,7 +1359,8 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   const int64_t row0 = b0 + lrow0;
   const int nseg_r = div_up(nr, G::kSB), nw_r = div_up(nr, 32);
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
-  const int so = D >= 16 ? 0 : (int)(((size_t)row0 * D) & 15u) / 4;   // word offset of the codes in s_sym
+  // word offset of the codes in s_sym (even when W = 2)
+  const int so = D * W >= 16 ? 0 : (int)(((size_t)row0 * D * W) & 15u) / 4;
 
   // ---- every global read, issued together ----
   {   // the dedup tables are not read again: empty them for the next call (a share per CTA)
@@ -1134,10 +1372,13 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   }
   const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
   const ContLay cl = w.cont[r];
-  const uint32_t mycode = __ldcg(&w.tabcode[(size_t)u * 256 + tid]);
+  uint32_t mycode[kA / 256];
+#pragma unroll
+  for (int k = 0; k < kA / 256; ++k) mycode[k] = __ldcg(&w.tabcode[(size_t)u * kA + k * 256 + tid]);
   if (s == 0 && writable) {   // the unit's table record: eb, counts, code lengths
-    uint8_t* rec = out + cl.base + kHeaderBytes + (size_t)t * kTableRecBytes;
-    rec[16 + tid] = (uint8_t)(mycode & 0xffu);
+    uint8_t* rec = out + cl.base + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
+#pragma unroll
+    for (int k = 0; k < kA / 256; ++k) rec[16 + k * 256 + tid] = (uint8_t)(mycode[k] & 0xffu);
     if (tid == 0) *reinterpret_cast<uint4*>(rec) = __ldcg(&w.tab_rec[u]);
   }
   if (s >= nseg_r) return;   // past the end of a shorter slice: no rows
@@ -1152,8 +1393,8 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   }
   {   // rows row0 .. row0 + SB are contiguous; the table stride is padded to 16 bytes
     const int64_t nrows = nr - lrow0 < G::kSB ? nr - lrow0 : G::kSB;
-    const int nq = (int)((so * 4 + nrows * D + 15) / 16);
-    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D - so * 4);
+    const int nq = (int)((so * 4 + nrows * D * W + 15) / 16);
+    const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D * W - so * 4);
     uint4* dst = reinterpret_cast<uint4*>(s_sym);
     for (int i = tid; i < nq; i += 256) dst[i] = __ldcg(src + i);
   }
@@ -1169,7 +1410,8 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   const unsigned long long off_seg = cbase + cl.off_seg, off_bitmap = cbase + cl.off_bitmap;
   const int ref_bytes = (int)cl.ref_bytes;
 
-  s_code[tid] = mycode;
+#pragma unroll
+  for (int k = 0; k < kA / 256; ++k) s_code[k * 256 + tid] = mycode[k];
   if (tid < G::kBmWords) {
     s_bm[tid] = bmw;
     s_lit[tid] = ~bmw & valid_mask(nr, lrow0, tid);
@@ -1212,11 +1454,11 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
     uint32_t nb = 0;
 #pragma unroll
     for (int j = 0; j < G::kSPR; ++j) {
-      const uint32_t v = act ? s_sym[so + rr * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
+      const Quad v = sm_quad(s_sym, so + (rr * (D / 4) + (lane % G::kLPR) + j * 32) * W, (Quad*)nullptr);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
-        const uint32_t c = (v >> (8 * q)) & 0xffu;
-        nb += (s_code[c] & 0xffu) + (c == 0u ? 32u : 0u);
+        const uint32_t c = quad_code(v, q);
+        nb += act ? (s_code[c] & 0xffu) + (c == 0u ? 32u : 0u) : 0u;
       }
     }
     if constexpr (G::kLPR == 32) {
@@ -1264,14 +1506,14 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
       uint32_t p = act ? s_rowoff[k] : 0u;
 #pragma unroll
       for (int j = 0; j < G::kSPR; ++j) {
-        const uint32_t v = act ? s_sym[so + rr * (D / 4) + (lane % G::kLPR) + j * 32] : 0x80808080u;
+        const Quad v = sm_quad(s_sym, so + (rr * (D / 4) + (lane % G::kLPR) + j * 32) * W, (Quad*)nullptr);
         // the lane's 4 codes joined into one string (right-aligned), if short and outlier-free
         uint32_t nb = 0;
         unsigned long long str = 0;
         bool plain = true;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-          const uint32_t c = (v >> (8 * q)) & 0xffu;
+          const uint32_t c = quad_code(v, q);
           const uint32_t e = s_code[c];
           const uint32_t len = e & 0xffu;
           str = (str << len) | (e >> 8);
@@ -1294,7 +1536,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
           const int d = (lane % G::kLPR) * 4 + j * 128;
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
-            const uint32_t c = (v >> (8 * q)) & 0xffu;
+            const uint32_t c = quad_code(v, q);
             const uint32_t e = s_code[c];
             put_bits(bitbuf, qpos, e >> 8, e & 0xffu);
             qpos += e & 0xffu;
@@ -1348,7 +1590,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
 // ---------------------------------------------------------------------------
 // launcher
 // ---------------------------------------------------------------------------
-template <int D, typename In>
+template <int D, typename In, int W>
 static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, const Work& w, uint8_t* out,
                               unsigned long long cap, unsigned long long* out_bytes, unsigned long long* chunk_off,
                               uint32_t epoch, cudaStream_t st, Prof* prof, const CUtensorMap* xmap) {
@@ -1359,32 +1601,32 @@ static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, 
     static int per_sm = -1;
     const int smem = 2 * (int)QGeo<D, In>::kStageBytes;
     if (per_sm < 0) {
-      cudaFuncSetAttribute(k_quantize<D, In>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize<D, In>, 256, smem) != cudaSuccess ||
+      cudaFuncSetAttribute(k_quantize<D, In, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize<D, In, W>, 256, smem) != cudaSuccess ||
           per_sm < 1)
         per_sm = 1;
     }
     unsigned qgrid = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm);
     if (qgrid > qsegs) qgrid = qsegs;
     prof_begin(prof, "k_quantize", st);
-    launch_k(k_quantize<D, In>, qgrid, 256, smem, st, *xmap, sh, ep, w);
+    launch_k(k_quantize<D, In, W>, qgrid, 256, smem, st, *xmap, sh, ep, w);
     prof_end(prof, st);
 
     prof_begin(prof, "k_resolve", st);
-    launch_k(k_resolve<D, In>, grid, kResolveThreads, 0, st, x, sh, w);
+    launch_k(k_resolve<D, In, W>, grid, kResolveThreads, 0, st, x, sh, w);
     prof_end(prof, st);
   }
   prof_begin(prof, "k_codebook", st);
-  launch_k(k_codebook, sh.U > 0 ? sh.U : 1, 256, 0, st, sh, ep, w, out, cap, out_bytes, chunk_off, epoch);
+  launch_k(k_codebook<W>, sh.U > 0 ? sh.U : 1, 256, 0, st, sh, ep, w, out, cap, out_bytes, chunk_off, epoch);
   prof_end(prof, st);
   if (grid) {
     if (!sh.fold) {
       prof_begin(prof, "k_layout", st);
-      launch_k(k_layout, (grid + 7) / 8, 256, 0, st, sh, ep, w, out, cap, out_bytes, chunk_off, epoch);
+      launch_k(k_layout<W>, (grid + 7) / 8, 256, 0, st, sh, ep, w, out, cap, out_bytes, chunk_off, epoch);
       prof_end(prof, st);
     }
     prof_begin(prof, "k_emit", st);
-    launch_k(k_emit<D, In>, grid, 256, Geo<D>::kSegSyms * 3, st, x, sh, w, out, cap, epoch);
+    launch_k(k_emit<D, In, W>, grid, 256, Geo<D>::kSegSyms * 3, st, x, sh, w, out, cap, epoch);
     prof_end(prof, st);
   }
 }
@@ -1434,15 +1676,29 @@ static cudaError_t launch_compress_t(const In* x, const Shape& sh, const EbParam
     }
     if (e != cudaSuccess) return e;
   }
+  if (sh.W == 2) {
+    switch (sh.D) {
+      case 4: launch_compress_d<4, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      case 8: launch_compress_d<8, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      case 16: launch_compress_d<16, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      case 32: launch_compress_d<32, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      case 64: launch_compress_d<64, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      case 128: launch_compress_d<128, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      case 256: launch_compress_d<256, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      case 512: launch_compress_d<512, In, 2>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+      default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
   switch (sh.D) {
-    case 4: launch_compress_d<4, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
-    case 8: launch_compress_d<8, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
-    case 16: launch_compress_d<16, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
-    case 32: launch_compress_d<32, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
-    case 64: launch_compress_d<64, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
-    case 128: launch_compress_d<128, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
-    case 256: launch_compress_d<256, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
-    case 512: launch_compress_d<512, In>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 4: launch_compress_d<4, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 8: launch_compress_d<8, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 16: launch_compress_d<16, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 32: launch_compress_d<32, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 64: launch_compress_d<64, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 128: launch_compress_d<128, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 256: launch_compress_d<256, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
+    case 512: launch_compress_d<512, In, 1>(x, sh, ep, w, out, cap, out_bytes, chunk_off, epoch, st, prof, &xmap); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();
@@ -1460,11 +1716,14 @@ cudaError_t launch_compress(const void* x, bool bf16, const Shape& sh, const EbP
 template <int D>
 static cudaError_t set_emit_smem() {
   // shared copy of a segment's bitstream: 24 bits per code on average (larger ones go to global memory)
-  const cudaError_t a = cudaFuncSetAttribute(k_emit<D, float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Geo<D>::kSegSyms * 3);
-  const cudaError_t b = cudaFuncSetAttribute(k_emit<D, uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             Geo<D>::kSegSyms * 3);
-  return a != cudaSuccess ? a : b;
+  const cudaError_t e[4] = {
+      cudaFuncSetAttribute(k_emit<D, float, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3),
+      cudaFuncSetAttribute(k_emit<D, uint16_t, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3),
+      cudaFuncSetAttribute(k_emit<D, float, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3),
+      cudaFuncSetAttribute(k_emit<D, uint16_t, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3)};
+  for (cudaError_t v : e)
+    if (v != cudaSuccess) return v;
+  return cudaSuccess;
 }
 
 cudaError_t set_kernel_attributes() {

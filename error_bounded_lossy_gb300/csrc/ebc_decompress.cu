@@ -68,7 +68,10 @@ __device__ int parse_header(const uint8_t* h, unsigned long long bytes, unsigned
   if (ld32(h) != kMagic || ld32(h + 4) != kFormatVersion) return EBC_ERR_CORRUPT;
   if (ld64(h + 8) != n || ld32(h + 16) != (uint32_t)T || ld32(h + 20) != (uint32_t)sh.D)
     return EBC_ERR_INVALID_ARG;
-  if (ld32(h + 24) != (uint32_t)kRadius || ld32(h + 28) != (uint32_t)kLmax || ld32(h + 32) != (uint32_t)sh.SB ||
+  const uint32_t radius = ld32(h + 24);   // the alphabet: both are valid, the call decodes one of them
+  if (radius != (uint32_t)kRadius && radius != (uint32_t)kRadiusWide) return EBC_ERR_CORRUPT;
+  if (radius != (uint32_t)(sh.A / 2)) return EBC_ERR_INVALID_ARG;
+  if (ld32(h + 28) != (uint32_t)kLmax || ld32(h + 32) != (uint32_t)sh.SB ||
       ld32(h + 36) != (uint32_t)sh.KC || ld32(h + 44) > (uint32_t)kMaxWindow)
     return EBC_ERR_CORRUPT;
   L->n = n;
@@ -86,7 +89,7 @@ __device__ int parse_header(const uint8_t* h, unsigned long long bytes, unsigned
       L->n_chunks > (unsigned long long)T * L->nseg * (unsigned long long)(sh.SB / sh.KC) ||
       L->n_out > nvec * (unsigned long long)sh.D || L->words > (1ull << 34))
     return EBC_ERR_CORRUPT;
-  L->off_seg = kHeaderBytes + (unsigned long long)T * kTableRecBytes;
+  L->off_seg = kHeaderBytes + (unsigned long long)T * table_rec_bytes(sh.A);
   L->off_bitmap = L->off_seg + (unsigned long long)T * L->nseg * kSegRecBytes;
   L->off_chunks = L->off_bitmap + dpad16((unsigned long long)T * L->nw * 4ull);
   L->off_refs = L->off_chunks + dpad16(L->n_chunks * 2ull);
@@ -117,17 +120,19 @@ __device__ __forceinline__ uint32_t warp_excl(uint32_t v, uint32_t* total) {
 // R headers (thread r: container r) and takes the chunk and match bases of
 // each container from a scan of their counts; a failed check stops every CTA.
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, int W>
 __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in, unsigned long long in_bytes,
                                                    const unsigned long long* __restrict__ offs, Shape sh, Work w,
                                                    uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
+  constexpr int kA = Alph<W>::kA, kPer = kA / 256;
   __shared__ Layout s_L[8];   // the containers of this CTA's units: r_lo .. r_lo + 7
   __shared__ uint32_t s_nc[kMaxSlices + 1], s_nm[kMaxSlices + 1], s_win[kMaxSlices];
   __shared__ unsigned long long s_tot[4];   // literals, outliers, words, bytes of all containers
   __shared__ int s_code;
-  __shared__ uint8_t s_len[256];
+  __shared__ uint8_t s_len[kA];
+  __shared__ unsigned long long s_key[W == 2 ? kA : 1];   // wide alphabet: (length, symbol) sort
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offset[kLmax + 2];
   __shared__ int s_bad;
   __shared__ uint32_t s_c0, s_c1;
@@ -222,13 +227,20 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     const int t = u % T;
     const Layout& Lc = s_L[0];
     const uint8_t* cin = in + Lc.base;
-    const uint8_t* rec = cin + kHeaderBytes + (size_t)t * kTableRecBytes;
-    const uint32_t len = rec[16 + tid];
-    s_len[tid] = (uint8_t)len;
+    const uint8_t* rec = cin + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
+    uint32_t lens[kPer];
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      lens[k] = rec[16 + k * 256 + tid];
+      s_len[k * 256 + tid] = (uint8_t)lens[k];
+    }
     if (tid < kLmax + 2) s_count[tid] = 0;
     __syncthreads();
-    if (len > (uint32_t)kLmax) s_bad = 1;
-    else if (len) atomicAdd(&s_count[len], 1u);
+#pragma unroll
+    for (int k = 0; k < kPer; ++k) {
+      if (lens[k] > (uint32_t)kLmax) s_bad = 1;
+      else if (lens[k]) atomicAdd(&s_count[lens[k]], 1u);
+    }
     __syncthreads();
     if (tid == 0) {
       const float eb = __uint_as_float(ld32(rec));
@@ -289,14 +301,38 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     uint16_t* lut = w.lut + (size_t)u * (1u << kLutBits);
     for (int i = tid; i < (1 << kLutBits); i += 256) lut[i] = 0;
     __syncthreads();
-    if (len) {
-      uint32_t rank = 0;
-      for (int j = 0; j < tid; ++j) rank += (s_len[j] == len);
-      const uint32_t code = s_next[len] + rank;
-      w.dtab[u].sorted[s_offset[len] + rank] = (uint8_t)tid;
-      if (len <= (uint32_t)kLutBits) {
-        const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
-        for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(tid | (len << 8));
+    if constexpr (W == 1) {
+      const uint32_t len = lens[0];
+      if (len) {
+        uint32_t rank = 0;
+        for (int j = 0; j < tid; ++j) rank += (s_len[j] == len);
+        const uint32_t code = s_next[len] + rank;
+        w.dtab[u].sorted[s_offset[len] + rank] = (uint16_t)tid;
+        if (len <= (uint32_t)kLutBits) {
+          const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
+          for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(tid | (len << Alph<W>::kLenShift));
+        }
+      }
+    } else {
+      // each symbol's rank among its length from a sort by (length, symbol): position p in the
+      // sorted order is the symbol's index in sorted[], its code is first[len] + p - offset[len]
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int sy = k * 256 + tid;
+        s_key[sy] = lens[k] ? ((unsigned long long)lens[k] << 10) | (unsigned)sy : ~0ull;
+      }
+      __syncthreads();
+      bitonic_sort_smem(s_key, kA);
+      for (int p = tid; p < kA; p += 256) {
+        const unsigned long long key = s_key[p];
+        if (key == ~0ull) continue;
+        const uint32_t sy = (uint32_t)(key & 1023u), len = (uint32_t)(key >> 10);
+        w.dtab[u].sorted[p] = (uint16_t)sy;
+        if (len <= (uint32_t)kLutBits) {
+          const uint32_t code = s_next[len] + ((uint32_t)p - s_offset[len]);
+          const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
+          for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(sy | (len << Alph<W>::kLenShift));
+        }
       }
     }
     if (Lc.window && Lc.nseg > 0) {
@@ -506,11 +542,11 @@ struct DecStage {
 
 // Decodes one chunk (rows literal rows of D codes) starting at bit `start`;
 // ldw(i) returns word i of the bitstream.  Returns the number of bits read.
-template <int D, class LoadWord>
+template <int D, int W, class LoadWord>
 __device__ __forceinline__ unsigned long long decode_chunk(LoadWord ldw, unsigned long long start,
                                                            const uint16_t* s_lut, const float* s_val,
                                                            const uint32_t* s_first, const uint32_t* s_count,
-                                                           const uint32_t* s_offset, const uint8_t* s_sorted,
+                                                           const uint32_t* s_offset, const uint16_t* s_sorted,
                                                            const uint16_t* lrow, uint32_t rows, int64_t row0, int T,
                                                            int t, float* __restrict__ xhat, bool* bad) {
   // bit window: the next stream bits are w0:w1 from bit `pos` of w0 (pos < 32); w0 is word wp - 2
@@ -528,7 +564,7 @@ __device__ __forceinline__ unsigned long long decode_chunk(LoadWord ldw, unsigne
       for (int q = 0; q < 4; ++q) {
         const uint32_t peek = __funnelshift_l(w1, w0, pos);   // the next 32 bits
         const uint32_t e = s_lut[peek >> (32 - kLutBits)];
-        uint32_t len = e >> 8, sym = e & 0xffu;
+        uint32_t len = e >> Alph<W>::kLenShift, sym = e & ((1u << Alph<W>::kLenShift) - 1u);
         if (len == 0u) {   // a code longer than the first-level table
           for (int l = kLutBits + 1; l <= kLmax; ++l) {
             const uint32_t code = peek >> (32 - l);
@@ -562,17 +598,18 @@ __device__ __forceinline__ unsigned long long decode_chunk(LoadWord ldw, unsigne
   return (wp - 2ull) * 32ull + pos - start;
 }
 
-template <int D>
+template <int D, int W>
 __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restrict__ in, Shape sh, Work w,
                                                          float* __restrict__ xhat, uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
+  constexpr int kA = Alph<W>::kA;
   constexpr int kStage = DecStage<D>::kWords;
   __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
   __shared__ __align__(16) uint32_t s_words[kStage + 1];
-  __shared__ float s_val[256];
+  __shared__ float s_val[kA];
   __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
-  __shared__ uint8_t s_sorted[256];
+  __shared__ uint16_t s_sorted[kA];
   __shared__ unsigned long long s_lo, s_hi;
   __shared__ int s_abort;
   Glob* g = w.glob;
@@ -608,9 +645,9 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
     }
     const float ebx2 = __ldcg(&dt->ebx2);
 #pragma unroll
-    for (int i = tid; i < 256; i += kDecRun) {
+    for (int i = tid; i < kA; i += kDecRun) {
       s_sorted[i] = dt->sorted[i];
-      s_val[i] = __fmul_rn((float)(i - kRadius), ebx2);
+      s_val[i] = __fmul_rn((float)(i - Alph<W>::kR), ebx2);
     }
   }
   // the bitstream of the unit's container
@@ -649,10 +686,10 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
     // reads past the chunk's end see the following chunks' words, then zeros:
     // they never change a code that lies inside the chunk
     const uint32_t* sw = s_words - lo;
-    used = decode_chunk<D>([&](unsigned long long i) -> uint32_t { return sw[i < hi ? i : hi]; }, start, s_lut,
+    used = decode_chunk<D, W>([&](unsigned long long i) -> uint32_t { return sw[i < hi ? i : hi]; }, start, s_lut,
                            s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T, t, xhat, &bad);
   } else {
-    used = decode_chunk<D>([&](unsigned long long i) -> uint32_t { return i < wlim ? __ldg(words + i) : 0u; },
+    used = decode_chunk<D, W>([&](unsigned long long i) -> uint32_t { return i < wlim ? __ldg(words + i) : 0u; },
                            start, s_lut, s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T, t,
                            xhat, &bad);
   }
@@ -708,18 +745,19 @@ __global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __
 // ---------------------------------------------------------------------------
 // launcher
 // ---------------------------------------------------------------------------
-template <int D>
+template <int D, int W>
 static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, const unsigned long long* offs,
                                 const Shape& sh, const Work& w, float* xhat, uint32_t epoch, cudaStream_t st,
                                 Prof* prof) {
   const unsigned nsegT = (unsigned)(sh.U * sh.nseg);
   prof_begin(prof, "k_dec_prep", st);
-  launch_k(k_dec_prep<D>, (sh.U > 0 ? sh.U : 1) + (nsegT + 7) / 8, 256, 0, st, in, in_bytes, offs, sh, w, epoch);
+  launch_k(k_dec_prep<D, W>, (sh.U > 0 ? sh.U : 1) + (nsegT + 7) / 8, 256, 0, st, in, in_bytes, offs, sh, w,
+           epoch);
   prof_end(prof, st);
   if (nsegT) {
     // one CTA per run slot: enough for the largest possible chunk count
     prof_begin(prof, "k_dec_chunks", st);
-    launch_k(k_dec_chunks<D>, (unsigned)(dec_run_slots(sh) - 1), kDecRun, 0, st, in, sh, w, xhat, epoch);
+    launch_k(k_dec_chunks<D, W>, (unsigned)(dec_run_slots(sh) - 1), kDecRun, 0, st, in, sh, w, xhat, epoch);
     prof_end(prof, st);
     prof_begin(prof, "k_dec_matches", st);
     launch_k(k_dec_matches<D>, (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * 8), 256, 0, st, sh, w, xhat, epoch);
@@ -730,15 +768,29 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
 cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, const unsigned long long* offs,
                               const Shape& sh, const Work& w, float* xhat, uint32_t epoch, cudaStream_t st,
                               Prof* prof) {
+  if (sh.W == 2) {
+    switch (sh.D) {
+      case 4: launch_decompress_d<4, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      case 8: launch_decompress_d<8, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      case 16: launch_decompress_d<16, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      case 32: launch_decompress_d<32, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      case 64: launch_decompress_d<64, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      case 128: launch_decompress_d<128, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      case 256: launch_decompress_d<256, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      case 512: launch_decompress_d<512, 2>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+      default: return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+  }
   switch (sh.D) {
-    case 4: launch_decompress_d<4>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
-    case 8: launch_decompress_d<8>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
-    case 16: launch_decompress_d<16>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
-    case 32: launch_decompress_d<32>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
-    case 64: launch_decompress_d<64>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
-    case 128: launch_decompress_d<128>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
-    case 256: launch_decompress_d<256>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
-    case 512: launch_decompress_d<512>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 4: launch_decompress_d<4, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 8: launch_decompress_d<8, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 16: launch_decompress_d<16, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 32: launch_decompress_d<32, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 64: launch_decompress_d<64, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 128: launch_decompress_d<128, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 256: launch_decompress_d<256, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
+    case 512: launch_decompress_d<512, 1>(in, in_bytes, offs, sh, w, xhat, epoch, st, prof); break;
     default: return cudaErrorInvalidValue;
   }
   return cudaGetLastError();

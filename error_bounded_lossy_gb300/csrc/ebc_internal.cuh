@@ -9,13 +9,16 @@
 
 namespace ebc {
 
-// ---- container format, version 1 ----
+// ---- container format, version 2 ----
 constexpr int kRadius = 128;               // codes q + 128 for |q| < 128; 0 = outlier
+constexpr int kRadiusWide = 512;           // the wide alphabet: codes q + 512 for |q| < 512, 16-bit
+constexpr int kMaxSyms = 1024;
 constexpr int kLmax = 24;                  // longest Huffman code
 constexpr uint32_t kMagic = 0x31434245u;   // "EBC1"
 constexpr uint32_t kFormatVersion = 2;
 constexpr uint32_t kHeaderBytes = 144;
 constexpr uint32_t kTableRecBytes = 272;   // f32 eb, u32 n_lit, n_match, n_out, u8 len[256]
+                                           // (16 + 1024 bytes with the wide alphabet)
 constexpr uint32_t kSegRecBytes = 16;      // u32 word_off, chunk_base, match_base, n_bits
 constexpr int kMaxT = 1024;
 constexpr int kMaxB = 16777215;
@@ -54,7 +57,45 @@ struct Shape {
   int Brem;       // B % R
   int64_t Bc;     // rows of the largest slice
   int qseg;       // quantization segments per table: ceil(B / SB) (k_quantize works on whole tables)
+  int W;          // bytes per code in the scratch: 1 (radius 128) or 2 (radius 512)
+  int A;          // symbols of the alphabet: 256 or 1024
 };
+
+// The two alphabets, by code width W in bytes.
+template <int W>
+struct Alph {
+  static constexpr int kR = W == 1 ? kRadius : kRadiusWide;   // radius: codes q + R for |q| < R
+  static constexpr int kA = 2 * kR;                             // symbols (0 = outlier)
+  static constexpr int kRawLen = W == 1 ? 8 : 10;               // bits of a raw code (log2 kA)
+  static constexpr int kLenShift = W == 1 ? 8 : 10;             // decode-table entry: sym | len << shift
+  static constexpr uint32_t kRecBytes = 16u + (uint32_t)kA;     // table record
+};
+__host__ __device__ inline uint32_t table_rec_bytes(int A) { return 16u + (uint32_t)A; }
+
+// Codes of four consecutive elements (one lane's share): one word of four
+// 8-bit codes, or two words of two 16-bit codes (code of element k in byte /
+// half-word k, little-endian).
+template <int W>
+struct QuadOf;
+template <>
+struct QuadOf<1> {
+  using T = uint32_t;
+};
+template <>
+struct QuadOf<2> {
+  using T = uint2;
+};
+__device__ __forceinline__ uint32_t quad_code(uint32_t v, int q) { return (v >> (8 * q)) & 0xffu; }
+__device__ __forceinline__ uint32_t quad_code(uint2 v, int q) {
+  return ((q < 2 ? v.x : v.y) >> (16 * (q & 1))) & 0xffffu;
+}
+__device__ __forceinline__ bool quad_eq(uint32_t a, uint32_t b) { return a == b; }
+__device__ __forceinline__ bool quad_eq(uint2 a, uint2 b) { return a.x == b.x && a.y == b.y; }
+// a zero code (an outlier) among the four
+__device__ __forceinline__ bool quad_has_zero(uint32_t v) { return ((v - 0x01010101u) & ~v & 0x80808080u) != 0u; }
+__device__ __forceinline__ bool quad_has_zero(uint2 v) {
+  return (((v.x - 0x00010001u) & ~v.x & 0x80008000u) | ((v.y - 0x00010001u) & ~v.y & 0x80008000u)) != 0u;
+}
 
 constexpr int kFoldMaxSeg = 256;
 constexpr int kMaxWindow = 255;
@@ -126,7 +167,7 @@ struct DecTab {
   unsigned long long bits_off; // byte offset of the unit's container bitstream in the input
   unsigned long long n_words;  // words of that bitstream
   unsigned long long row0;     // first batch row of the unit's slice
-  uint8_t sorted[256];         // symbols by (length, symbol)
+  uint16_t sorted[kMaxSyms];   // symbols by (length, symbol)
 };
 
 // Device scratch of a context.  Sizes follow Shape.
@@ -134,25 +175,26 @@ struct Work {
   const uint8_t* modes;        // [T] per-table modes, or null (all 0)
   unsigned long long* tab_bits;   // [U] bits of the unit's literal codes and outlier values
   // compress
-  uint8_t* sym;                // [T][B][D] quantization codes, table t at t * symstride (16-byte aligned)
+  uint8_t* sym;                // [T][B][D] quantization codes (W bytes each), table t at t * symstride
+                               //   (16-byte aligned)
   uint32_t* vhash;             // [T][B] dedup key
   uint32_t* vnout;             // [T][B] outliers per vector
   unsigned long long* slots;   // [U][S] (hash << 32 | first row); all ones = empty
   uint32_t* bitmap;            // [U][nw] match bits (rows of the unit's slice)
   uint32_t* ref;               // [T][B] reference row (batch row) of matched rows
-  uint32_t* seg_hist;          // [U*nseg][256] literal code histogram per segment
+  uint32_t* seg_hist;          // [U*nseg][A] literal code histogram per segment
   uint4* seg_cnt;              // [U*nseg] {literals, matches, outliers, chunks}
   uint4* seg_desc;             // [groups] totals {words, chunks, matches} of each group of segments
   uint4* tile_base;            // [groups] absolute base of each group
   uint4* seg_base;             // [U*nseg] {words, chunks, matches} relative to its group, and the bit count
                                // (a group: the unit when Shape::fold, else 8 consecutive segments)
-  uint32_t* tab_hist;          // [U][256] literal code histogram per unit
+  uint32_t* tab_hist;          // [U][A] literal code histogram per unit
   uint4* tab_cnt;              // [U] {literals, matches, outliers, chunks}
   uint4* tab_rec;              // [U] the first 16 bytes of the unit's table record: eb, literals, matches, outliers
-  uint32_t* tabcode;           // [U][256] code << 8 | length
+  uint32_t* tabcode;           // [U][A] code << 8 | length
   ContLay* cont;               // [R] container layouts
   // decompress
-  uint16_t* lut;               // [U][1 << kLutBits] sym | len << 8 (len 0 = long code)
+  uint16_t* lut;               // [U][1 << kLutBits] sym | len << kLenShift (len 0 = long code)
   DecTab* dtab;                // [U]
   uint4* cdesc;                // [U*nseg*chunks] {start bit lo, start bit hi | length << 16, segment, first literal | rows << 16}
   uint16_t* litrow;            // [U*nseg][SB] literal rows of each segment, in row order
@@ -202,6 +244,25 @@ struct Geo {
   static constexpr int kChunks = kSB / kKC;                       // max chunks per segment
   static constexpr int kSegSyms = kSB * D;
 };
+
+// Ascending bitonic sort of n (a power of two) keys in shared memory by the
+// whole CTA; every thread takes its share of the pairs of each stage.
+__device__ inline void bitonic_sort_smem(unsigned long long* key, int n) {
+  for (int k = 2; k <= n; k <<= 1)
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        const int l = i ^ j;
+        if (l > i) {
+          const unsigned long long a = key[i], b = key[l];
+          if ((a > b) == ((i & k) == 0)) {
+            key[i] = b;
+            key[l] = a;
+          }
+        }
+      }
+      __syncthreads();
+    }
+}
 
 // ---- programmatic dependent launch ----
 // Every kernel of a call is launched with programmatic stream serialization.

@@ -130,8 +130,30 @@ int ebc_set_error_bounds(ebc_ctx* ctx, const float* eb_base, int T, int64_t iter
 /* Copy the current scheduled bounds (T of them) into eb_out (host). */
 int ebc_get_error_bounds(const ebc_ctx* ctx, float* eb_out, int T);
 
-/* Worst-case container bytes for a [B,T,D] input; 0 for an unsupported shape. */
+/* Worst-case container bytes for a [B,T,D] input with the default alphabet
+ * (radius 128); 0 for an unsupported shape. */
 uint64_t ebc_compress_bound(int64_t B, int T, int D);
+
+/* Alphabet of the quantization codes.  Radius 128 (the default): bins q in
+ * (-128, 128), 8-bit codes q + 128, 256 symbols.  Radius 512, the wide
+ * alphabet: bins q in (-512, 512), codes q + 512 kept as 16 bits in the code
+ * scratch, Huffman over 1024 symbols (same 24-bit length limit), table records
+ * of 16 + 1024 bytes, 10-bit codes in raw-code mode; values up to 4x farther
+ * from zero stop being outliers (32 raw bits each), at twice the scratch and
+ * larger tables.  The pages (§III-D) fix no radius.  The container's
+ * radius field (header offset 24) records it. */
+#define EBC_RADIUS 128
+#define EBC_RADIUS_WIDE 512
+
+/* The radius of this context's later compress and decompress calls (chunked
+ * ones too): EBC_RADIUS or EBC_RADIUS_WIDE, else EBC_ERR_INVALID_ARG.  A
+ * container of the other alphabet is rejected by the decoder with
+ * EBC_ERR_INVALID_ARG (like a container of another shape).
+ * ebc_decompress_noalloc decodes radius-128 containers only. */
+int ebc_set_radius(ebc_ctx* ctx, int radius);
+
+/* ebc_compress_bound for either radius (0 for another value). */
+uint64_t ebc_compress_bound_radius(int64_t B, int T, int D, int radius);
 
 /* Compress d_x[B][T][D] (device, fp32) with bounds eb[T] (host array; NULL =
  * the context's schedule) into d_out (device, out_capacity bytes).  The
@@ -173,9 +195,9 @@ int ebc_decompress(ebc_ctx* ctx, const void* d_in, uint64_t in_bytes, float* d_x
  * 1 <= n_chunks <= EBC_MAX_CHUNKS. */
 #define EBC_MAX_CHUNKS 256
 
-/* Worst-case bytes of the chunked buffer: the sum of ebc_compress_bound over
- * the slices (0 for an unsupported shape or chunk count). */
-uint64_t ebc_compress_chunked_bound(int64_t B, int T, int D, int n_chunks);
+/* Worst-case bytes of the chunked buffer: the sum of ebc_compress_bound_radius
+ * over the slices (0 for an unsupported shape, chunk count or radius). */
+uint64_t ebc_compress_chunked_bound(int64_t B, int T, int D, int n_chunks, int radius);
 
 /* Compress d_x[B][T][D] (device, fp32) as n_chunks containers into d_out
  * (device, 16-byte aligned, out_capacity bytes).  The kernels write the
