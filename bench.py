@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--link-gbs", type=float, default=12.5,
                    help="network bandwidth (GB/s) for the Eq. (2) per-table mode choice (12.5 = 100 Gb/s)")
     p.add_argument("--no-hybrid", action="store_true", help="skip the per-table mode measurements")
+    p.add_argument("--radius", type=int, default=128, choices=[128, 512],
+                   help="quantization radius of the timed steps (512: the wide alphabet)")
     return p.parse_args()
 
 
@@ -247,6 +249,7 @@ def main():
     B, T, D = x.shape
     N = x.numel()
     codec = ebc.Codec(local)
+    codec.set_radius(args.radius)
     cap = codec.compress_bound(B, T, D)
     out = torch.empty(cap, dtype=torch.uint8, device=dev)
     nbytes = torch.zeros(1, dtype=torch.int64, device=dev)
@@ -495,6 +498,51 @@ def main():
             del outc, outs, xc
         del xref
 
+    # ---- wide alphabet (outside the timed region): radius 128 against 512 on the forward batch and on
+    #      the gradient batch with sigma 1e-2 (heavy tails past the 8-bit bins) ----
+    wide = None
+    if not args.no_hybrid:
+        wide = {}
+        nrep = max(3, min(K, 20))
+        for wname, wkw in (("fwd", {}), ("bwd_sigma_1e-2", {"variant": "s1e-2"})):
+            wl2 = wl if wname == "fwd" else workloads.make("bwd", device=dev, seed=rank, **wkw)
+            x2, eb2 = wl2.x, wl2.eb.numpy()
+            row = {}
+            for radius in (128, 512):
+                codec.set_radius(radius)
+                cap2 = codec.compress_bound(B, T, D)
+                out2 = torch.empty(cap2, dtype=torch.uint8, device=dev)
+                nb2 = torch.zeros(1, dtype=torch.int64, device=dev)
+                xh2 = torch.empty_like(x2)
+                codec.compress_into(x2, eb2, out2, nb2, stream)
+                codec.decompress_into(out2, cap2, xh2, stream)
+                torch.cuda.synchronize()
+                codec.check()
+                st2 = codec.stats()
+                err2 = (x2.double() - xh2.double()).abs().amax(dim=(0, 2)).cpu().numpy()
+                if not (err2 <= eb2.astype(np.float64)).all():
+                    raise SystemExit(f"error bound violated (radius {radius})")
+                ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                       torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+                for a, b_, c_ in ev:
+                    flush.zero_()
+                    a.record(stream)
+                    codec.compress_into(x2, eb2, out2, nb2, stream)
+                    b_.record(stream)
+                    codec.decompress_into(out2, cap2, xh2, stream)
+                    c_.record(stream)
+                torch.cuda.synchronize()
+                codec.check()
+                tc2 = sum(a.elapsed_time(b_) for a, b_, _ in ev) / 1e3 / nrep
+                td2 = sum(b_.elapsed_time(c_) for _, b_, c_ in ev) / 1e3 / nrep
+                row[str(radius)] = {"compression_ratio": round(4 * N / st2["out_bytes"], 3),
+                                    "n_outlier": st2["n_outlier"],
+                                    "compress_gbs": round(4 * N / tc2 / 1e9, 1),
+                                    "decompress_gbs": round(4 * N / td2 / 1e9, 1)}
+                del out2, xh2
+            codec.set_radius(args.radius)
+            wide[wname] = row
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         sample = workloads.make(WORKLOAD, batch=512)
@@ -511,7 +559,8 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": {"workload": "DLRM forward lookups [8192,26,128] fp32, 26 tables rows 1e3..1e6 log-uniform, "
                                    "Zipf(1.05), eb_t=1e-2*range", "global_batch": B * world, "tables": T, "dim": D,
-                       "parallelism": f"replicas x{world}", "l2": "flushed before every step (2x L2 memset)"},
+                       "parallelism": f"replicas x{world}", "l2": "flushed before every step (2x L2 memset)",
+                       "radius": args.radius},
             "compress_gbs": round(job_throughput_gbs(world, K, N, t_c), 2),
             "decompress_gbs": round(job_throughput_gbs(world, K, N, t_d), 2),
             "compression_ratio": round(4 * N / C, 3),
@@ -528,6 +577,7 @@ def main():
             "window": window,
             "bf16_input": bf16,
             "chunked": chunked,
+            "wide_alphabet": wide,
             "clocks": clocks,
             "wall_s": round(wall, 3),
         }

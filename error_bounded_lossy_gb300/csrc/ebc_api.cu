@@ -110,7 +110,9 @@ static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0, in
   sh.window = window;
   sh.ref_bytes = window > 0 ? 1 : (B <= 65536 ? 2 : 4);
   sh.symstride = ((uint64_t)B * (uint64_t)D * (uint64_t)sh.W + 15u) & ~(uint64_t)15u;
-  sh.fold = sh.nseg <= kFoldMaxSeg ? 1 : 0;
+  // per-unit segment offsets inside k_codebook for short units of the 8-bit alphabet; otherwise (long
+  // units, or 1024-bin histograms) k_layout spreads that work over all SMs
+  sh.fold = sh.nseg <= kFoldMaxSeg && sh.W == 1 ? 1 : 0;
   return sh;
 }
 

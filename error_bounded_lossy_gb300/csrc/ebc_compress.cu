@@ -404,7 +404,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   // window mode: keys of rows row0 - window .. row0 + SB during the lookups; then the literal
   // code histograms, one per warp
   constexpr int kHistWin = kNW * kA > kMaxWindow + G::kSB ? kNW * kA : kMaxWindow + G::kSB;
-  __shared__ uint32_t s_histwin[kHistWin];
+  __shared__ __align__(16) uint32_t s_histwin[kHistWin];
   uint32_t* s_win = s_histwin;
   __shared__ __align__(16) uint32_t s_sym[G::kSegSyms * W / 4 + 4];   // the segment's own codes
   __shared__ uint32_t s_ref[G::kSB];
@@ -494,7 +494,8 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   }
   cp_async_wait_all();
   __syncthreads();
-  for (int i = tid; i < kNW * kA; i += kNT) s_histwin[i] = 0u;   // the window keys are no longer needed
+  for (int i = tid; i < kNW * kA / 4; i += kNT)   // the window keys are no longer needed
+    reinterpret_cast<uint4*>(s_histwin)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
 
   uint32_t* hist = s_histwin + warp * kA;
@@ -583,12 +584,16 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   }
   __syncthreads();
 #pragma unroll
-  for (int i = tid; i < kA; i += kNT) {
-    uint32_t f = 0;
+  for (int i = tid; i < kA / 4; i += kNT) {   // four bins per thread and step
+    uint4 f = make_uint4(0, 0, 0, 0);
 #pragma unroll
-    for (int k = 0; k < kNW; ++k) f += s_histwin[k * kA + i];
-    w.seg_hist[(size_t)seg * kA + i] = f;
-    if (f) atomicAdd(&w.tab_hist[(size_t)u * kA + i], f);
+    for (int k = 0; k < kNW; ++k) f = add4(f, reinterpret_cast<const uint4*>(s_histwin + k * kA)[i]);
+    reinterpret_cast<uint4*>(w.seg_hist + (size_t)seg * kA)[i] = f;
+    uint32_t* th = w.tab_hist + (size_t)u * kA + 4 * i;
+    if (f.x) atomicAdd(th + 0, f.x);
+    if (f.y) atomicAdd(th + 1, f.y);
+    if (f.z) atomicAdd(th + 2, f.z);
+    if (f.w) atomicAdd(th + 3, f.w);
   }
   for (int i = tid; i < G::kBmWords; i += kNT) {   // bit i of word k: row b0 + 32 k + i of the slice
     const int64_t wi = (int64_t)s * G::kBmWords + i;
@@ -607,35 +612,6 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
 // ---------------------------------------------------------------------------
 // Block-wide helpers over 256 threads.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint4 add4(uint4 a, uint4 b) {
-  return make_uint4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-}
-
-__device__ uint4 block_excl_scan4(uint4 v, uint4* total, uint4* s_warp) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  uint4 inc = v;
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    uint4 n;
-    n.x = __shfl_up_sync(0xffffffffu, inc.x, off);
-    n.y = __shfl_up_sync(0xffffffffu, inc.y, off);
-    n.z = __shfl_up_sync(0xffffffffu, inc.z, off);
-    n.w = __shfl_up_sync(0xffffffffu, inc.w, off);
-    if (lane >= off) inc = add4(inc, n);
-  }
-  if (lane == 31) s_warp[warp] = inc;
-  __syncthreads();
-  uint4 pre = make_uint4(0, 0, 0, 0), tot = make_uint4(0, 0, 0, 0);
-  const int nwarps = blockDim.x >> 5;
-  for (int i = 0; i < nwarps; ++i) {
-    if (i < warp) pre = add4(pre, s_warp[i]);
-    tot = add4(tot, s_warp[i]);
-  }
-  __syncthreads();
-  *total = tot;
-  return make_uint4(pre.x + inc.x - v.x, pre.y + inc.y - v.y, pre.z + inc.z - v.z, pre.w + inc.w - v.w);
-}
-
 __device__ __forceinline__ uint32_t block_sum(uint32_t v, uint32_t* s_red) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
@@ -751,33 +727,6 @@ __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Wor
   }
 }
 
-// Ascending bitonic sort of one 64-bit key per thread over a 256-thread CTA:
-// partners closer than a warp trade through shuffles, the others through
-// shared memory.  Returns the key of rank threadIdx.x.
-__device__ __forceinline__ unsigned long long bitonic_sort256(unsigned long long v, unsigned long long* s_key) {
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int k = 2; k <= 256; k <<= 1) {
-#pragma unroll
-    for (int j = k >> 1; j > 0; j >>= 1) {
-      unsigned long long p;
-      if (j >= 32) {
-        s_key[tid] = v;
-        __syncthreads();
-        p = s_key[tid ^ j];
-        __syncthreads();
-      } else {
-        p = __shfl_xor_sync(0xffffffffu, v, j);
-      }
-      const bool up = (tid & k) == 0;        // this run ascends
-      const bool low = (tid & j) == 0;       // lower element of the pair
-      const unsigned long long mn = v < p ? v : p, mx = v < p ? p : v;
-      v = (up == low) ? mn : mx;
-    }
-  }
-  return v;
-}
-
 // The code of one unit over the wide alphabet (1024 symbols, 4 per thread):
 // the same construction as for 256 symbols (two-queue Huffman over the leaves
 // sorted by (count, symbol), ties to the leaf, halving above 24 bits;
@@ -787,7 +736,7 @@ __device__ void huffman_wide(const Shape& sh, const EbParams& ep, const Work& w,
                              uint32_t* s_f, uint32_t* s_lw, uint32_t* s_nodew, unsigned long long* s_key,
                              uint16_t* s_order, uint16_t* s_leafpar, uint16_t* s_nodepar, uint16_t* s_depth,
                              uint8_t* s_len, uint32_t* s_count, uint32_t* s_next, uint32_t* s_offl,
-                             unsigned long long* s_bits64, int* s_maxlen, int* s_n) {
+                             unsigned long long* s_bits64, int* s_maxlen, uint4* s_warp) {
   constexpr int kA = Alph<2>::kA, kPer = kA / 256;
   const int tid = threadIdx.x;
   uint32_t f0[kPer];
@@ -801,24 +750,16 @@ __device__ void huffman_wide(const Shape& sh, const EbParams& ep, const Work& w,
   }
   __syncthreads();
   for (int round = 0; round < 40 && !raw; ++round) {
-    if (tid == 0) {
-      *s_n = 0;
-      *s_maxlen = 0;
-    }
-    __syncthreads();
-    int mine = 0;
+    if (tid == 0) *s_maxlen = 0;
+    unsigned long long key[kPer];
 #pragma unroll
     for (int k = 0; k < kPer; ++k) {
       const int sy = k * 256 + tid;
       const uint32_t fi = s_f[sy];
-      s_key[sy] = fi > 0u ? ((unsigned long long)fi << 10) | (unsigned)sy : ~0ull;
+      key[k] = fi > 0u ? ((unsigned long long)fi << 10) | (unsigned)sy : ~0ull;
       s_len[sy] = 0;
-      mine += fi > 0u;
     }
-    atomicAdd(s_n, mine);
-    __syncthreads();
-    bitonic_sort_smem(s_key, kA);   // leaves in (count, symbol) order, absent symbols last
-    const int n = *s_n;
+    const int n = sort_used_keys<kPer>(key, s_key, s_warp);   // leaves in (count, symbol) order
     for (int i = tid; i < n; i += 256) {
       s_order[i] = (uint16_t)(s_key[i] & 1023u);
       s_lw[i] = (uint32_t)(s_key[i] >> 10);
@@ -886,12 +827,13 @@ __device__ void huffman_wide(const Shape& sh, const EbParams& ep, const Work& w,
   // symbol's rank among its length from a sort by (length, symbol)
   if (tid < kLmax + 2) s_count[tid] = 0;
   __syncthreads();
+  unsigned long long key[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
     const int sy = k * 256 + tid;
     const uint32_t L = s_len[sy];
     if (L) atomicAdd(&s_count[L], 1u);
-    s_key[sy] = L ? ((unsigned long long)L << 10) | (unsigned)sy : ~0ull;
+    key[k] = L ? ((unsigned long long)L << 10) | (unsigned)sy : ~0ull;
     s_lw[sy] = 0u;
   }
   __syncthreads();
@@ -905,13 +847,11 @@ __device__ void huffman_wide(const Shape& sh, const EbParams& ep, const Work& w,
       off += s_count[l];
     }
   }
-  bitonic_sort_smem(s_key, kA);
-  for (int p = tid; p < kA; p += 256) {
-    const unsigned long long key = s_key[p];
-    if (key != ~0ull) {
-      const uint32_t sy = (uint32_t)(key & 1023u), L = (uint32_t)(key >> 10);
-      s_lw[sy] = ((s_next[L] + ((uint32_t)p - s_offl[L])) << 8) | L;
-    }
+  const int nused = sort_used_keys<kPer>(key, s_key, s_warp);
+  for (int p = tid; p < nused; p += 256) {
+    const unsigned long long k2 = s_key[p];
+    const uint32_t sy = (uint32_t)(k2 & 1023u), L = (uint32_t)(k2 >> 10);
+    s_lw[sy] = ((s_next[L] + ((uint32_t)p - s_offl[L])) << 8) | L;
   }
   __syncthreads();
   unsigned long long sum = 0;   // bits of the unit's literal codes, plus the raw bits of its outliers
@@ -958,7 +898,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   __shared__ Par s_leafpar[kA], s_nodepar[kA], s_depth[kA];
   __shared__ uint8_t s_len[kA];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offl[kLmax + 2];
-  __shared__ int s_maxlen, s_last, s_n;
+  __shared__ int s_maxlen, s_last;
   __shared__ uint4 s_warp[8];
   __shared__ uint4 s_cpre[kMaxSlices + 1], s_wpre[kMaxSlices + 1];   // unit prefixes at container starts
   const int tid = threadIdx.x;
@@ -972,7 +912,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     const bool raw = w.modes && (w.modes[t] & kModeRawCodes);   // every code log2(A) bits: no Huffman
     if constexpr (W == 2) {
       huffman_wide(sh, ep, w, u, t, raw, s_f, s_lw, s_nodew, s_key, s_order, s_leafpar, s_nodepar, s_depth, s_len,
-                   s_count, s_next, s_offl, s_bits64, &s_maxlen, &s_n);
+                   s_count, s_next, s_offl, s_bits64, &s_maxlen, s_warp);
     } else {
     // (with no segments, k_quantize did not run and the accumulators are stale)
     const uint32_t f0 = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)u * 256 + tid]) : 0u;
@@ -1088,7 +1028,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       // one warp per segment; then offsets relative to the unit (a scan) and the unit's totals
       const int warp = tid >> 5, lane = tid & 31;
       constexpr int kV = kA / 128;                  // uint4 of histogram and codes per lane
-      constexpr int kBatch = W == 1 ? 4 : 1;        // segments whose histograms are loaded together
+      constexpr int kBatch = W == 1 ? 4 : 2;        // segments whose histograms are loaded together
       const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * kA) + lane * kV;
       __syncthreads();   // tabcode of this unit is written
       uint4 c[kV];

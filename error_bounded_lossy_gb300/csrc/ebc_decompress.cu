@@ -133,6 +133,7 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
   __shared__ int s_code;
   __shared__ uint8_t s_len[kA];
   __shared__ unsigned long long s_key[W == 2 ? kA : 1];   // wide alphabet: (length, symbol) sort
+  __shared__ uint4 s_warp4[8];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offset[kLmax + 2];
   __shared__ int s_bad;
   __shared__ uint32_t s_c0, s_c1;
@@ -316,16 +317,15 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     } else {
       // each symbol's rank among its length from a sort by (length, symbol): position p in the
       // sorted order is the symbol's index in sorted[], its code is first[len] + p - offset[len]
+      unsigned long long keys[kPer];
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
         const int sy = k * 256 + tid;
-        s_key[sy] = lens[k] ? ((unsigned long long)lens[k] << 10) | (unsigned)sy : ~0ull;
+        keys[k] = lens[k] ? ((unsigned long long)lens[k] << 10) | (unsigned)sy : ~0ull;
       }
-      __syncthreads();
-      bitonic_sort_smem(s_key, kA);
-      for (int p = tid; p < kA; p += 256) {
+      const int nused = sort_used_keys<kPer>(keys, s_key, s_warp4);
+      for (int p = tid; p < nused; p += 256) {
         const unsigned long long key = s_key[p];
-        if (key == ~0ull) continue;
         const uint32_t sy = (uint32_t)(key & 1023u), len = (uint32_t)(key >> 10);
         w.dtab[u].sorted[p] = (uint16_t)sy;
         if (len <= (uint32_t)kLutBits) {

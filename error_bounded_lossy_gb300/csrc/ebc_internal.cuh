@@ -264,6 +264,96 @@ __device__ inline void bitonic_sort_smem(unsigned long long* key, int n) {
     }
 }
 
+// Exclusive scan of one uint4 per thread over the CTA (s_warp: 8 slots).
+__device__ __forceinline__ uint4 add4(uint4 a, uint4 b) {
+  return make_uint4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+}
+
+__device__ inline uint4 block_excl_scan4(uint4 v, uint4* total, uint4* s_warp) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint4 inc = v;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    uint4 n;
+    n.x = __shfl_up_sync(0xffffffffu, inc.x, off);
+    n.y = __shfl_up_sync(0xffffffffu, inc.y, off);
+    n.z = __shfl_up_sync(0xffffffffu, inc.z, off);
+    n.w = __shfl_up_sync(0xffffffffu, inc.w, off);
+    if (lane >= off) inc = add4(inc, n);
+  }
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  uint4 pre = make_uint4(0, 0, 0, 0), tot = make_uint4(0, 0, 0, 0);
+  const int nwarps = blockDim.x >> 5;
+  for (int i = 0; i < nwarps; ++i) {
+    if (i < warp) pre = add4(pre, s_warp[i]);
+    tot = add4(tot, s_warp[i]);
+  }
+  __syncthreads();
+  *total = tot;
+  return make_uint4(pre.x + inc.x - v.x, pre.y + inc.y - v.y, pre.z + inc.z - v.z, pre.w + inc.w - v.w);
+}
+
+// Ascending bitonic sort of one 64-bit key per thread over a 256-thread CTA:
+// partners closer than a warp trade through shuffles, the others through
+// shared memory.  Returns the key of rank threadIdx.x.
+__device__ __forceinline__ unsigned long long bitonic_sort256(unsigned long long v, unsigned long long* s_key) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int k = 2; k <= 256; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      unsigned long long p;
+      if (j >= 32) {
+        s_key[tid] = v;
+        __syncthreads();
+        p = s_key[tid ^ j];
+        __syncthreads();
+      } else {
+        p = __shfl_xor_sync(0xffffffffu, v, j);
+      }
+      const bool up = (tid & k) == 0;        // this run ascends
+      const bool low = (tid & j) == 0;       // lower element of the pair
+      const unsigned long long mn = v < p ? v : p, mx = v < p ? p : v;
+      v = (up == low) ? mn : mx;
+    }
+  }
+  return v;
+}
+
+// Sorts the keys of the symbols in use, ascending, into s_key[0 .. n): each
+// thread passes its kPer keys (~0 = not in use).  The used keys are compacted
+// by a CTA scan; up to 256 of them are sorted in registers and shuffles, more
+// by a shared-memory sort of all of them.  Returns n.
+template <int kPer>
+__device__ int sort_used_keys(const unsigned long long (&key)[kPer], unsigned long long* s_key, uint4* s_warp) {
+  const int tid = threadIdx.x;
+  uint32_t mine = 0;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) mine += key[k] != ~0ull;
+  uint4 tot;
+  const uint32_t at = block_excl_scan4(make_uint4(mine, 0, 0, 0), &tot, s_warp).x;
+  const int n = (int)tot.x;
+  uint32_t p = at;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k)
+    if (key[k] != ~0ull) s_key[p++] = key[k];
+  if (n > 256)
+    for (int i = n + tid; i < kPer * 256; i += 256) s_key[i] = ~0ull;
+  __syncthreads();
+  if (n <= 256) {
+    const unsigned long long v = tid < n ? s_key[tid] : ~0ull;
+    __syncthreads();   // s_key becomes the sort's scratch
+    const unsigned long long sk = bitonic_sort256(v, s_key);
+    __syncthreads();
+    s_key[tid] = sk;
+    __syncthreads();
+  } else {
+    bitonic_sort_smem(s_key, kPer * 256);
+  }
+  return n;
+}
+
 // ---- programmatic dependent launch ----
 // Every kernel of a call is launched with programmatic stream serialization.
 // On entry it lets the next kernel of the stream launch (which happens once
