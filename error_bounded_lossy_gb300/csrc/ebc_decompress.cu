@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     // ---- decode tables of unit u = (slice r, table t) ----
     const int u = blockIdx.x;
     const int t = u % T;
-    const Layout& Lc = s_L[0];
+    const Layout Lc = s_L[0];
     const uint8_t* cin = in + Lc.base;
     const uint8_t* rec = cin + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
     uint32_t lens[kPer];
@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
   const int s = seg - u * sh.nseg;
   const int r = u / T;
   const int t = u - r * T;
-  const Layout& Lc = s_L[r - r_lo];
+  const Layout Lc = s_L[r - r_lo];
   if (s >= (int)Lc.nseg) return;   // past the end of a shorter slice
   const uint8_t* cin = in + Lc.base;
   const int64_t B = (int64_t)Lc.n;                // rows of the slice
@@ -760,7 +760,11 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
     launch_k(k_dec_chunks<D, W>, (unsigned)(dec_run_slots(sh) - 1), kDecRun, 0, st, in, sh, w, xhat, epoch);
     prof_end(prof, st);
     prof_begin(prof, "k_dec_matches", st);
-    launch_k(k_dec_matches<D>, (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * 8), 256, 0, st, sh, w, xhat, epoch);
+    static int per_sm = -1;   // resident CTAs per SM: the grid-stride loop runs in one wave
+    if (per_sm < 0 &&
+        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dec_matches<D>, 256, 0) != cudaSuccess || per_sm < 1))
+      per_sm = 4;
+    launch_k(k_dec_matches<D>, (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm), 256, 0, st, sh, w, xhat, epoch);
     prof_end(prof, st);
   }
 }
