@@ -899,6 +899,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   __shared__ uint8_t s_len[kA];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offl[kLmax + 2];
   __shared__ int s_maxlen, s_last;
+  __shared__ uint32_t s_wcnt[8][kLmax + 1];   // symbols of each length per warp
   __shared__ uint4 s_warp[8];
   __shared__ uint4 s_cpre[kMaxSlices + 1], s_wpre[kMaxSlices + 1];   // unit prefixes at container starts
   const int tid = threadIdx.x;
@@ -987,11 +988,16 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       if (fi > 0u) s_f[tid] = (fi >> 1) > 0u ? (fi >> 1) : 1u;
       __syncthreads();
     }
-    // canonical codes
+    // canonical codes: counts per length, and each symbol's rank among the symbols of its length
+    // below it (in its warp by a match mask, in the warps before by their counts)
+    const int lane = tid & 31, wp = tid >> 5;
     if (tid < kLmax + 2) s_count[tid] = 0;
+    for (int i = tid; i < 8 * (kLmax + 1); i += 256) (&s_wcnt[0][0])[i] = 0u;
     __syncthreads();
     const uint32_t L = s_len[tid];
     if (L) atomicAdd(&s_count[L], 1u);
+    const unsigned same = __match_any_sync(0xffffffffu, L);
+    if (lane == __ffs(same) - 1) s_wcnt[wp][L] = (uint32_t)__popc(same);
     __syncthreads();
     if (tid == 0) {
       uint32_t c = 0;
@@ -1004,8 +1010,8 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     __syncthreads();
     uint32_t code = 0;
     if (L) {
-      code = s_next[L];
-      for (int j = 0; j < tid; ++j) code += (s_len[j] == L);
+      code = s_next[L] + (uint32_t)__popc(same & ((1u << lane) - 1u));
+      for (int k = 0; k < wp; ++k) code += s_wcnt[k][L];
     }
     w.tabcode[(size_t)u * 256 + tid] = (code << 8) | L;
     {   // bits of the table's literal codes, plus the raw bits of its outliers (symbol 0)
@@ -1028,7 +1034,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
       // one warp per segment; then offsets relative to the unit (a scan) and the unit's totals
       const int warp = tid >> 5, lane = tid & 31;
       constexpr int kV = kA / 128;                  // uint4 of histogram and codes per lane
-      constexpr int kBatch = W == 1 ? 4 : 2;        // segments whose histograms are loaded together
+      constexpr int kBatch = W == 1 ? 8 : 2;        // segments whose histograms are loaded together
       const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * kA) + lane * kV;
       __syncthreads();   // tabcode of this unit is written
       uint4 c[kV];
