@@ -731,12 +731,12 @@ __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Wor
 // the same construction as for 256 symbols (two-queue Huffman over the leaves
 // sorted by (count, symbol), ties to the leaf, halving above 24 bits;
 // canonical values by the DEFLATE rule), with the leaf order and the canonical
-// ranks taken from shared-memory sorts.  Writes tabcode, tab_bits, tab_rec.
+// ranks counted per length (canonical_ranks).  Writes tabcode, tab_bits, tab_rec.
 __device__ void huffman_wide(const Shape& sh, const EbParams& ep, const Work& w, int u, int t, bool raw,
                              uint32_t* s_f, uint32_t* s_lw, uint32_t* s_nodew, unsigned long long* s_key,
                              uint16_t* s_order, uint16_t* s_leafpar, uint16_t* s_nodepar, uint16_t* s_depth,
-                             uint8_t* s_len, uint32_t* s_count, uint32_t* s_next, uint32_t* s_offl,
-                             unsigned long long* s_bits64, int* s_maxlen, uint4* s_warp) {
+                             uint8_t* s_len, uint32_t* s_count, uint32_t* s_next, uint32_t* s_wcnt,
+                             uint32_t* s_run, unsigned long long* s_bits64, int* s_maxlen, uint4* s_warp) {
   constexpr int kA = Alph<2>::kA, kPer = kA / 256;
   const int tid = threadIdx.x;
   uint32_t f0[kPer];
@@ -827,32 +827,25 @@ __device__ void huffman_wide(const Shape& sh, const EbParams& ep, const Work& w,
   // symbol's rank among its length from a sort by (length, symbol)
   if (tid < kLmax + 2) s_count[tid] = 0;
   __syncthreads();
-  unsigned long long key[kPer];
+  uint32_t lens[kPer], rk[kPer];
 #pragma unroll
   for (int k = 0; k < kPer; ++k) {
-    const int sy = k * 256 + tid;
-    const uint32_t L = s_len[sy];
-    if (L) atomicAdd(&s_count[L], 1u);
-    key[k] = L ? ((unsigned long long)L << 10) | (unsigned)sy : ~0ull;
-    s_lw[sy] = 0u;
+    lens[k] = s_len[k * 256 + tid];
+    if (lens[k]) atomicAdd(&s_count[lens[k]], 1u);
   }
   __syncthreads();
   if (tid == 0) {
-    uint32_t c = 0, off = 0;
+    uint32_t c = 0;
     s_count[0] = 0;
     for (int l = 1; l <= kLmax; ++l) {
       c = (c + s_count[l - 1]) << 1;
       s_next[l] = c;
-      s_offl[l] = off;
-      off += s_count[l];
     }
   }
-  const int nused = sort_used_keys<kPer>(key, s_key, s_warp);
-  for (int p = tid; p < nused; p += 256) {
-    const unsigned long long k2 = s_key[p];
-    const uint32_t sy = (uint32_t)(k2 & 1023u), L = (uint32_t)(k2 >> 10);
-    s_lw[sy] = ((s_next[L] + ((uint32_t)p - s_offl[L])) << 8) | L;
-  }
+  canonical_ranks<kPer>(lens, rk, s_wcnt, s_run);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k)
+    s_lw[k * 256 + tid] = lens[k] ? ((s_next[lens[k]] + rk[k]) << 8) | lens[k] : 0u;
   __syncthreads();
   unsigned long long sum = 0;   // bits of the unit's literal codes, plus the raw bits of its outliers
 #pragma unroll
@@ -897,7 +890,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   __shared__ uint16_t s_order[kA];
   __shared__ Par s_leafpar[kA], s_nodepar[kA], s_depth[kA];
   __shared__ uint8_t s_len[kA];
-  __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offl[kLmax + 2];
+  __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_run[kLmax + 2];
   __shared__ int s_maxlen, s_last;
   __shared__ uint32_t s_wcnt[8][kLmax + 1];   // symbols of each length per warp
   __shared__ uint4 s_warp[8];
@@ -913,7 +906,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     const bool raw = w.modes && (w.modes[t] & kModeRawCodes);   // every code log2(A) bits: no Huffman
     if constexpr (W == 2) {
       huffman_wide(sh, ep, w, u, t, raw, s_f, s_lw, s_nodew, s_key, s_order, s_leafpar, s_nodepar, s_depth, s_len,
-                   s_count, s_next, s_offl, s_bits64, &s_maxlen, s_warp);
+                   s_count, s_next, &s_wcnt[0][0], s_run, s_bits64, &s_maxlen, s_warp);
     } else {
     // (with no segments, k_quantize did not run and the accumulators are stale)
     const uint32_t f0 = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)u * 256 + tid]) : 0u;

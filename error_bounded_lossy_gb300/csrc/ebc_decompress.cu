@@ -132,8 +132,7 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
   __shared__ unsigned long long s_tot[4];   // literals, outliers, words, bytes of all containers
   __shared__ int s_code;
   __shared__ uint8_t s_len[kA];
-  __shared__ unsigned long long s_key[W == 2 ? kA : 1];   // wide alphabet: (length, symbol) sort
-  __shared__ uint4 s_warp4[8];
+  __shared__ uint32_t s_wcnt[8 * (kLmax + 1)], s_run[kLmax + 1];   // canonical ranks
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offset[kLmax + 2];
   __shared__ int s_bad;
   __shared__ uint32_t s_c0, s_c1;
@@ -302,34 +301,18 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
     uint16_t* lut = w.lut + (size_t)u * (1u << kLutBits);
     for (int i = tid; i < (1 << kLutBits); i += 256) lut[i] = 0;
     __syncthreads();
-    if constexpr (W == 1) {
-      const uint32_t len = lens[0];
-      if (len) {
-        uint32_t rank = 0;
-        for (int j = 0; j < tid; ++j) rank += (s_len[j] == len);
-        const uint32_t code = s_next[len] + rank;
-        w.dtab[u].sorted[s_offset[len] + rank] = (uint16_t)tid;
-        if (len <= (uint32_t)kLutBits) {
-          const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
-          for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(tid | (len << Alph<W>::kLenShift));
-        }
-      }
-    } else {
-      // each symbol's rank among its length from a sort by (length, symbol): position p in the
-      // sorted order is the symbol's index in sorted[], its code is first[len] + p - offset[len]
-      unsigned long long keys[kPer];
+    {
+      // each symbol's rank among the symbols of its length below it: its index in sorted[] is
+      // offset[len] + rank, its code first[len] + rank
+      uint32_t rk[kPer];
+      canonical_ranks<kPer>(lens, rk, s_wcnt, s_run);
 #pragma unroll
       for (int k = 0; k < kPer; ++k) {
-        const int sy = k * 256 + tid;
-        keys[k] = lens[k] ? ((unsigned long long)lens[k] << 10) | (unsigned)sy : ~0ull;
-      }
-      const int nused = sort_used_keys<kPer>(keys, s_key, s_warp4);
-      for (int p = tid; p < nused; p += 256) {
-        const unsigned long long key = s_key[p];
-        const uint32_t sy = (uint32_t)(key & 1023u), len = (uint32_t)(key >> 10);
-        w.dtab[u].sorted[p] = (uint16_t)sy;
+        const uint32_t len = lens[k], sy = (uint32_t)(k * 256 + tid);
+        if (!len) continue;
+        const uint32_t code = s_next[len] + rk[k];
+        w.dtab[u].sorted[s_offset[len] + rk[k]] = (uint16_t)sy;
         if (len <= (uint32_t)kLutBits) {
-          const uint32_t code = s_next[len] + ((uint32_t)p - s_offset[len]);
           const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
           for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(sy | (len << Alph<W>::kLenShift));
         }

@@ -354,6 +354,37 @@ __device__ int sort_used_keys(const unsigned long long (&key)[kPer], unsigned lo
   return n;
 }
 
+// Canonical ranks over a 256-thread CTA: thread tid holds the code lengths of
+// symbols k * 256 + tid (k < kPer); rank[k] is the number of symbols of the
+// same length with a smaller index (in its warp from a match mask, in the
+// warps and rounds before from counts).  s_wcnt: 8 x (kLmax + 1) words,
+// s_run: kLmax + 1 words of shared scratch.
+template <int kPer>
+__device__ void canonical_ranks(const uint32_t (&len)[kPer], uint32_t (&rank)[kPer], uint32_t* s_wcnt,
+                                uint32_t* s_run) {
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  constexpr int kL = kLmax + 1;
+  if (tid < kL) s_run[tid] = 0u;
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    for (int i = tid; i < 8 * kL; i += 256) s_wcnt[i] = 0u;
+    __syncthreads();
+    const unsigned same = __match_any_sync(0xffffffffu, len[k]);
+    if (lane == __ffs(same) - 1) s_wcnt[wp * kL + len[k]] = (uint32_t)__popc(same);
+    __syncthreads();
+    uint32_t r = s_run[len[k]] + (uint32_t)__popc(same & ((1u << lane) - 1u));
+    for (int j = 0; j < wp; ++j) r += s_wcnt[j * kL + len[k]];
+    rank[k] = r;
+    __syncthreads();
+    if (tid < kL) {
+      uint32_t add = 0;
+      for (int j = 0; j < 8; ++j) add += s_wcnt[j * kL + tid];
+      s_run[tid] += add;
+    }
+    __syncthreads();   // the counts are read before the next round clears them
+  }
+}
+
 // ---- programmatic dependent launch ----
 // Every kernel of a call is launched with programmatic stream serialization.
 // On entry it lets the next kernel of the stream launch (which happens once
