@@ -62,3 +62,29 @@ def test_create_without_device_reports_no_device(lib):
     assert lib.ebc_create(ctypes.byref(h), 0) == ebc.EBC_ERR_NO_DEVICE
     assert not h.value
     assert lib.ebc_last_device_error(None) == ebc.EBC_ERR_INVALID_ARG
+
+
+def test_bounds_of_the_wide_alphabet_and_of_chunked_buffers(lib):
+    # the wide alphabet's bound agrees with the oracle's (1040-byte table records)
+    for shape in [(0, 3, 16), (1, 1, 4), (512, 4, 16), (8192, 26, 128), (33, 2, 512)]:
+        assert ebc.ebc_compress_bound_radius(*shape, 512) == oracle.compress_bound(*shape, radius=512)
+        assert ebc.ebc_compress_bound_radius(*shape, 128) == ebc.ebc_compress_bound(*shape)
+    assert ebc.ebc_compress_bound_radius(512, 4, 16, 256) == 0
+    # a chunked buffer's bound is the sum of its slices' bounds (numpy array_split slices)
+    for B, T, D, n in [(8192, 26, 128, 8), (1001, 3, 8, 7), (3, 2, 16, 5), (0, 4, 16, 4), (65537, 1, 4, 2)]:
+        for radius in (128, 512):
+            want = sum(oracle.compress_bound(b1 - b0, T, D, radius) for b0, b1 in oracle.chunk_rows(B, n))
+            assert ebc.ebc_compress_chunked_bound(B, T, D, n, radius) == want
+    assert ebc.ebc_compress_chunked_bound(100, 2, 16, 0, 128) == 0
+    assert ebc.ebc_compress_chunked_bound(100, 2, 16, ebc.EBC_MAX_CHUNKS + 1, 128) == 0
+    assert ebc.ebc_compress_chunked_bound(100, 2, 24, 2, 128) == 0
+    assert ebc.ebc_compress_chunked_bound(100, 2, 16, 2, 300) == 0
+
+
+def test_chunked_and_radius_calls_reject_bad_arguments_before_any_device_work(lib):
+    # a null context is refused by every new entry point
+    assert ebc.ebc_set_radius(None, 512) == ebc.EBC_ERR_INVALID_ARG
+    assert ebc.ebc_compress_chunked(None, None, 8, 2, 16, None, 2, None, 0, None, None) == ebc.EBC_ERR_INVALID_ARG
+    assert ebc.ebc_compress_chunked_bf16(None, None, 8, 2, 16, None, 2, None, 0, None, None) == \
+        ebc.EBC_ERR_INVALID_ARG
+    assert ebc.ebc_decompress_chunked(None, None, 0, None, 2, None, 8, 2, 16, None) == ebc.EBC_ERR_INVALID_ARG
