@@ -16,9 +16,10 @@
  *   - one output buffer, metadata with sizes ..... §III-A stage 2, §III-E "Buffer Optimization"
  *
  * Pipeline (all on the GPU, on the caller's stream):
- *   quantize:  q = round_half_even(x * fl32(1/(2 eb_t))), kept if |q| < 128 and
+ *   quantize:  q = round_half_even(x * fl32(1/(2 eb_t))), kept if |q| < R and
  *              |x - fl32(q * 2 eb_t)| <= eb_t in fp32, else an outlier whose raw
- *              32 bits are stored; code sym = q + 128 (1..255), 0 = outlier.
+ *              32 bits are stored; code sym = q + R (1..2R-1), 0 = outlier.  The
+ *              radius R is 128 (8-bit codes) unless ebc_set_radius selects 512.
  *   dedup:     within each table, a vector whose codes (and outlier bits) equal
  *              those of an earlier vector of the batch is a match to the first
  *              occurrence; the others are literals.
@@ -27,14 +28,16 @@
  *              written MSB-first into a bitstream with a chunk index.
  *
  * Container (little-endian, every section 16-byte aligned):
- *   header 144 B | T table records (eb, counts, 256 code lengths; 272 B each)
+ *   header 144 B | T table records (eb, counts, 2R code lengths; 272 B each, 1040 B
+ *   with radius 512)
  *   | segment records (16 B each) | match bitmap (T x ceil(B/32) u32)
  *   | chunk bit lengths (u16) | match references (u16 row if B <= 65536, else
  *   u32; one-byte distances when the header's window field, at byte 44, is not
  *   0) | bitstream (u32 words; an outlier's code is followed by its 32 raw bits)
  * A segment is max(32, 8192/D) consecutive batch rows of one table; its bits
  * start on a 128-bit boundary.  A chunk is max(1, 128/D) literal vectors of one
- * segment, decoded by one GPU thread.
+ * segment, decoded by one GPU thread.  ebc_compress_chunked writes one such
+ * container per slice of the batch, back to back in one buffer.
  *
  * Supported shapes: 0 <= B <= 16,777,215; 0 <= T <= 1024; D a power of two in
  * [4, 512]; B*T*D <= 2^31 (every bitstream word offset then fits 32 bits).
