@@ -1262,18 +1262,24 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, EbParams ep, Work w, u
 // its codes into one bit string that is ORed into a shared-memory copy of the
 // segment's bitstream at the lane's offset (a prefix sum over the row).
 // Outlier codes are followed by the 32 raw bits of the value.  The copy is
-// stored with 16-byte writes; a segment larger than the copy (24 bits per
-// code on average) is ORed straight into the zeroed output.
+// stored with 16-byte writes; a segment larger than the copy (16 bits per
+// code of the segment on average, reached only by outlier-heavy rows) is ORed
+// straight into the zeroed output.  128 threads: a segment holds few literal
+// rows (most rows are matches), so the per-segment work (code table, bitmap,
+// ranks, scans) dominates and is cheaper on a smaller CTA.
 // ---------------------------------------------------------------------------
+constexpr int kET = 128, kEW = kET / 32;
+template <int D>
+constexpr int emit_stage_bytes() { return Geo<D>::kSegSyms * 2; }
 template <int D, typename In, int W>
-__global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape sh, Work w,
+__global__ void __launch_bounds__(kET, 8) k_emit(const In* __restrict__ x, Shape sh, Work w,
                                                uint8_t* __restrict__ out, unsigned long long cap, uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
   using Quad = typename QuadOf<W>::T;
   constexpr int kA = Alph<W>::kA;
-  constexpr int kRPT = (G::kSB + 255) / 256;   // rows (and ranks) per thread
-  constexpr uint32_t kSmemWords = (uint32_t)G::kSegSyms * 3u / 4u;
+  constexpr int kRPT = (G::kSB + kET - 1) / kET;   // rows (and ranks) per thread
+  constexpr uint32_t kSmemWords = (uint32_t)emit_stage_bytes<D>() / 4u;
   extern __shared__ __align__(16) uint32_t s_bits[];
   __shared__ __align__(16) uint32_t s_sym[G::kSegSyms * W / 4 + 4];   // the segment's codes, row-major
   __shared__ uint32_t s_code[kA];
@@ -1307,17 +1313,17 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
     const unsigned long long per = (n2 + gridDim.x - 1) / gridDim.x;
     const unsigned long long lo = per * blockIdx.x, hi = lo + per < n2 ? lo + per : n2;
     uint4* sl = reinterpret_cast<uint4*>(w.slots);
-    for (unsigned long long i = lo + tid; i < hi; i += 256) sl[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
+    for (unsigned long long i = lo + tid; i < hi; i += kET) sl[i] = make_uint4(~0u, ~0u, ~0u, ~0u);
   }
   const bool writable = __ldcg(&g->cstat) == status_word(epoch, EBC_OK);
   const ContLay cl = w.cont[r];
-  uint32_t mycode[kA / 256];
+  uint32_t mycode[kA / kET];
 #pragma unroll
-  for (int k = 0; k < kA / 256; ++k) mycode[k] = __ldcg(&w.tabcode[(size_t)u * kA + k * 256 + tid]);
+  for (int k = 0; k < kA / kET; ++k) mycode[k] = __ldcg(&w.tabcode[(size_t)u * kA + k * kET + tid]);
   if (s == 0 && writable) {   // the unit's table record: eb, counts, code lengths
     uint8_t* rec = out + cl.base + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
 #pragma unroll
-    for (int k = 0; k < kA / 256; ++k) rec[16 + k * 256 + tid] = (uint8_t)(mycode[k] & 0xffu);
+    for (int k = 0; k < kA / kET; ++k) rec[16 + k * kET + tid] = (uint8_t)(mycode[k] & 0xffu);
     if (tid == 0) *reinterpret_cast<uint4*>(rec) = __ldcg(&w.tab_rec[u]);
   }
   if (s >= nseg_r) return;   // past the end of a shorter slice: no rows
@@ -1335,12 +1341,12 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
     const int nq = (int)((so * 4 + nrows * D * W + 15) / 16);
     const uint4* src = reinterpret_cast<const uint4*>(symt + (size_t)row0 * D * W - so * 4);
     uint4* dst = reinterpret_cast<uint4*>(s_sym);
-    for (int i = tid; i < nq; i += 256) dst[i] = __ldcg(src + i);
+    for (int i = tid; i < nq; i += kET) dst[i] = __ldcg(src + i);
   }
   uint32_t refw[kRPT];
 #pragma unroll
   for (int k = 0; k < kRPT; ++k) {
-    const int rr = k * 256 + tid;
+    const int rr = k * kET + tid;
     refw[k] = (rr < G::kSB && lrow0 + rr < nr) ? __ldcg(&w.ref[(size_t)t * sh.B + row0 + rr]) : 0u;
   }
   const unsigned long long cbase = cl.base;
@@ -1350,7 +1356,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   const int ref_bytes = (int)cl.ref_bytes;
 
 #pragma unroll
-  for (int k = 0; k < kA / 256; ++k) s_code[k * 256 + tid] = mycode[k];
+  for (int k = 0; k < kA / kET; ++k) s_code[k * kET + tid] = mycode[k];
   if (tid < G::kBmWords) {
     s_bm[tid] = bmw;
     s_lit[tid] = ~bmw & valid_mask(nr, lrow0, tid);
@@ -1362,7 +1368,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   uint32_t* dstw = reinterpret_cast<uint32_t*>(out + off_bits) + sb.x;
   uint32_t* bitbuf = in_smem ? s_bits : dstw;
   if (bits_fit)
-    for (uint32_t i = tid; i < nwords; i += 256) bitbuf[i] = 0u;
+    for (uint32_t i = tid; i < nwords; i += kET) bitbuf[i] = 0u;
   __syncthreads();
 
   // ---- literal ranks: rows counted before each bitmap word, then each literal row's rank ----
@@ -1377,7 +1383,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   __syncthreads();
 #pragma unroll
   for (int k = 0; k < kRPT; ++k) {
-    const int rr = k * 256 + tid;
+    const int rr = k * kET + tid;
     if (rr < G::kSB && ((s_lit[rr >> 5] >> (rr & 31)) & 1u))
       s_litrow[(s_pre[rr >> 5] & 0xffffu) + __popc(s_lit[rr >> 5] & ((1u << (rr & 31)) - 1u))] = (uint16_t)rr;
   }
@@ -1386,7 +1392,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
 
   // ---- pass 1: bits of each literal row ----
 #pragma unroll 1
-  for (uint32_t i = warp; i < nsteps; i += 8) {
+  for (uint32_t i = warp; i < nsteps; i += kEW) {
     const uint32_t k = i * G::kRPS + lane / G::kLPR;   // literal rank of this lane's row
     const bool act = k < nlit;
     const int rr = act ? s_litrow[k] : 0;
@@ -1437,7 +1443,7 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
   // ---- pass 2: codes (and raw outlier bits) into the bitstream ----
   if (bits_fit) {
 #pragma unroll 1
-    for (uint32_t i = warp; i < nsteps; i += 8) {
+    for (uint32_t i = warp; i < nsteps; i += kEW) {
       const uint32_t k = i * G::kRPS + lane / G::kLPR;
       const bool act = k < nlit;
       const int rr = act ? s_litrow[k] : 0;
@@ -1495,16 +1501,16 @@ __global__ void __launch_bounds__(256, 4) k_emit(const In* __restrict__ x, Shape
     if (bits_fit && in_smem) {
       uint4* dst = reinterpret_cast<uint4*>(dstw);
       const uint4* src = reinterpret_cast<const uint4*>(s_bits);
-      for (uint32_t i = tid; i < nwords / 4; i += 256) dst[i] = src[i];
+      for (uint32_t i = tid; i < nwords / 4; i += kET) dst[i] = src[i];
     }
-    for (uint32_t k = tid * G::kKC; k < nlit; k += 256 * G::kKC) {
+    for (uint32_t k = tid * G::kKC; k < nlit; k += kET * G::kKC) {
       const uint32_t end = k + G::kKC < nlit ? k + G::kKC : nlit;
       *reinterpret_cast<uint16_t*>(out + off_chunks + 2ull * (sb.y + k / G::kKC)) =
           (uint16_t)(s_rowoff[end] - s_rowoff[k]);
     }
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
-      const int rr = k * 256 + tid;
+      const int rr = k * kET + tid;
       if (rr < G::kSB && lrow0 + rr < nr && ((s_bm[rr >> 5] >> (rr & 31)) & 1u)) {
         const uint32_t mrank = (s_pre[rr >> 5] >> 16) + __popc(s_bm[rr >> 5] & ((1u << (rr & 31)) - 1u));
         const unsigned long long o = off_refs + (unsigned long long)ref_bytes * (sb.z + mrank);
@@ -1565,7 +1571,7 @@ static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, 
       prof_end(prof, st);
     }
     prof_begin(prof, "k_emit", st);
-    launch_k(k_emit<D, In, W>, grid, 256, Geo<D>::kSegSyms * 3, st, x, sh, w, out, cap, epoch);
+    launch_k(k_emit<D, In, W>, grid, kET, emit_stage_bytes<D>(), st, x, sh, w, out, cap, epoch);
     prof_end(prof, st);
   }
 }
@@ -1654,12 +1660,12 @@ cudaError_t launch_compress(const void* x, bool bf16, const Shape& sh, const EbP
 
 template <int D>
 static cudaError_t set_emit_smem() {
-  // shared copy of a segment's bitstream: 24 bits per code on average (larger ones go to global memory)
+  // shared copy of a segment's bitstream: 16 bits per code on average (larger ones go to global memory)
   const cudaError_t e[4] = {
-      cudaFuncSetAttribute(k_emit<D, float, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3),
-      cudaFuncSetAttribute(k_emit<D, uint16_t, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3),
-      cudaFuncSetAttribute(k_emit<D, float, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3),
-      cudaFuncSetAttribute(k_emit<D, uint16_t, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, Geo<D>::kSegSyms * 3)};
+      cudaFuncSetAttribute(k_emit<D, float, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, emit_stage_bytes<D>()),
+      cudaFuncSetAttribute(k_emit<D, uint16_t, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, emit_stage_bytes<D>()),
+      cudaFuncSetAttribute(k_emit<D, float, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, emit_stage_bytes<D>()),
+      cudaFuncSetAttribute(k_emit<D, uint16_t, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, emit_stage_bytes<D>())};
   for (cudaError_t v : e)
     if (v != cudaSuccess) return v;
   return cudaSuccess;
