@@ -143,7 +143,7 @@ uint64_t ebc_compress_bound(int64_t B, int T, int D);
  * scratch, Huffman over 1024 symbols (same 24-bit length limit), table records
  * of 16 + 1024 bytes, 10-bit codes in raw-code mode; values up to 4x farther
  * from zero stop being outliers (32 raw bits each), at twice the scratch and
- * larger tables.  The pages (§III-D) fix no radius.  The container's
+ * larger tables.  The paper (§III-D) fixes no radius.  The container's
  * radius field (header offset 24) records it. */
 #define EBC_RADIUS 128
 #define EBC_RADIUS_WIDE 512

@@ -2,7 +2,7 @@
 code scratch) against the oracle with the same radius ("Accelerating
 Communication in Deep Learning Recommendation Model Training with Dual-Level
 Adaptive Lossy Compression", §III-D quantization and Huffman encoders; the
-pages fix no radius).
+paper fixes no radius).
 
 Bar: containers byte-identical to the oracle's, reconstructions 0 ulp, on the
 workloads (including the sigma = 1e-2 gradient case the alphabet is for),

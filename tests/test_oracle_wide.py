@@ -1,7 +1,7 @@
 """Pins of the oracle's wide alphabet (radius 512: bins q in (-512, 512),
-1024 symbols, 16-bit codes).  The pages ("Accelerating Communication in Deep
+1024 symbols, 16-bit codes).  The paper ("Accelerating Communication in Deep
 Learning Recommendation Model Training with Dual-Level Adaptive Lossy
-Compression", §III-D quantization encoder and Huffman encoder) fix no radius;
+Compression", §III-D quantization encoder and Huffman encoder) fixes no radius;
 this option widens the bins so that heavy-tailed values stop being outliers.
 Pinned against hand-computed codes, the 8-bit alphabet where both apply, a
 textbook heap Huffman and the Kraft equality over 1024 symbols, brute-force
