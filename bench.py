@@ -578,7 +578,7 @@ def main():
             "config": {"workload": "DLRM forward lookups [8192,26,128] fp32, 26 tables rows 1e3..1e6 log-uniform, "
                                    "Zipf(1.05), eb_t=1e-2*range", "global_batch": B * world, "tables": T, "dim": D,
                        "parallelism": f"replicas x{world}", "l2": "flushed before every step (2x L2 memset)",
-                       "radius": args.radius, "chunks": R},
+                       "radius": args.radius, "chunks": args.chunks},
             "compress_gbs": round(job_throughput_gbs(world, K, N, t_c), 2),
             "decompress_gbs": round(job_throughput_gbs(world, K, N, t_d), 2),
             "compression_ratio": round(4 * N / C, 3),
