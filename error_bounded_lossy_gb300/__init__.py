@@ -30,6 +30,7 @@ __all__ = [
     "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
     "EBC_MAX_CHUNKS", "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16",
     "ebc_decompress_chunked", "EBC_RADIUS", "EBC_RADIUS_WIDE", "ebc_set_radius", "ebc_compress_bound_radius",
+    "ebc_decompress_columns",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
@@ -48,7 +49,7 @@ EXPORTED_SYMBOLS = (
     "ebc_decompress_noalloc", "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup",
     "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
     "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16", "ebc_decompress_chunked",
-    "ebc_set_radius", "ebc_compress_bound_radius",
+    "ebc_set_radius", "ebc_compress_bound_radius", "ebc_decompress_columns",
 )
 
 
@@ -125,6 +126,7 @@ def lib():
                 "ebc_compress_chunked_bound": (U64, [I64, I, I, I, I]),
                 "ebc_set_radius": (I, [P, I]),
                 "ebc_compress_bound_radius": (U64, [I64, I, I, I]),
+                "ebc_decompress_columns": (I, [P, P, U64, P, I64, I, I, I, I, P]),
                 "ebc_compress_chunked": (I, [P, P, I64, I, I, P, I, P, U64, P, P]),
                 "ebc_compress_chunked_bf16": (I, [P, P, I64, I, I, P, I, P, U64, P, P]),
                 "ebc_decompress_chunked": (I, [P, P, U64, P, I, P, I64, I, I, P]),
@@ -191,6 +193,11 @@ def ebc_compress_chunked_bound(B: int, T: int, D: int, n_chunks: int, radius: in
 
 def ebc_set_radius(ctx, radius) -> int:
     return lib().ebc_set_radius(ctx, int(radius))
+
+
+def ebc_decompress_columns(ctx, d_in, in_bytes, d_xhat, B, T, D, T_out, t_off, stream) -> int:
+    return lib().ebc_decompress_columns(ctx, d_in, int(in_bytes), d_xhat, int(B), int(T), int(D), int(T_out),
+                                        int(t_off), stream)
 
 
 def ebc_compress_bound_radius(B: int, T: int, D: int, radius: int) -> int:
@@ -420,6 +427,16 @@ class Codec:
                                     B, T, D, _stream_ptr(stream))
         if rc:
             raise EbcError(rc, "ebc_decompress_chunked")
+        return out
+
+    def decompress_columns(self, container, in_bytes: int, T: int, out, t_off: int, stream=None):
+        """Restores a container of T tables into columns [t_off, t_off + T) of out
+        (CUDA float32 [B, T_out, D]); the other columns are not touched."""
+        B, T_out, D = out.shape
+        rc = ebc_decompress_columns(self._ctx, _ptr(container), in_bytes, _ptr(out), B, T, D, T_out, t_off,
+                                    _stream_ptr(stream))
+        if rc:
+            raise EbcError(rc, "ebc_decompress_columns")
         return out
 
     def decompress_into(self, container, in_bytes: int, xhat, stream=None) -> None:

@@ -90,6 +90,8 @@ static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0, in
   Shape sh;
   sh.W = radius == kRadiusWide ? 2 : 1;
   sh.A = 2 * radius;
+  sh.T_out = T;
+  sh.t_off = 0;
   sh.nsm = nsm;
   sh.B = B;
   sh.T = T;
@@ -453,9 +455,15 @@ int ebc_compress_chunked_bf16(ebc_ctx* c, const uint16_t* d_x, int64_t B, int T,
                       stream);
 }
 
+// T_out, t_off: the output rows hold T_out tables and the container's tables go to columns
+// [t_off, t_off + T) (T_out = T, t_off = 0 for a whole batch)
 static int decompress_any(ebc_ctx* c, const void* d_in, uint64_t in_bytes, const uint64_t* d_offsets, int R,
-                          float* d_xhat, int64_t B, int T, int D, void* stream) {
-  const Shape sh = make_shape(B, T, D, c->nsm, 0, R, c->radius);
+                          float* d_xhat, int64_t B, int T, int D, void* stream, int T_out = -1, int t_off = 0) {
+  Shape sh = make_shape(B, T, D, c->nsm, 0, R, c->radius);
+  if (T_out >= 0) {
+    sh.T_out = T_out;
+    sh.t_off = t_off;
+  }
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
   carve_decompress(nullptr, sh, c->glob, &need);
@@ -475,6 +483,16 @@ int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xha
   const uint64_t N = (uint64_t)B * T * D;
   if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
   return decompress_any(c, d_in, in_bytes, nullptr, 1, d_xhat, B, T, D, stream);
+}
+
+int ebc_decompress_columns(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
+                           int T_out, int t_off, void* stream) {
+  if (!c || !shape_ok(B, T, D) || !shape_ok(B, T_out, D) || t_off < 0 || (int64_t)t_off + T > T_out || !d_in ||
+      !aligned16(d_in))
+    return EBC_ERR_INVALID_ARG;
+  const uint64_t N = (uint64_t)B * T_out * D;
+  if (N > 0 && (!d_xhat || !aligned16(d_xhat))) return EBC_ERR_INVALID_ARG;
+  return decompress_any(c, d_in, in_bytes, nullptr, 1, d_xhat, B, T, D, stream, T_out, t_off);
 }
 
 int ebc_decompress_chunked(ebc_ctx* c, const void* d_in, uint64_t in_bytes, const uint64_t* d_offsets,

@@ -496,7 +496,8 @@ __global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in
             break;
           }
         }
-        w.mdesc[Lc.match0 + k] = make_uint2((uint32_t)((brow0 + b) * T + t), (uint32_t)((brow0 + ref) * T + t));
+        w.mdesc[Lc.match0 + k] = make_uint2((uint32_t)((brow0 + b) * sh.T_out + sh.t_off + t),
+                                            (uint32_t)((brow0 + ref) * sh.T_out + sh.t_off + t));
         ++k;
       }
       mbase += tot;
@@ -670,11 +671,12 @@ __global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restric
     // they never change a code that lies inside the chunk
     const uint32_t* sw = s_words - lo;
     used = decode_chunk<D, W>([&](unsigned long long i) -> uint32_t { return sw[i < hi ? i : hi]; }, start, s_lut,
-                           s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T, t, xhat, &bad);
+                           s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T_out, sh.t_off + t,
+                           xhat, &bad);
   } else {
     used = decode_chunk<D, W>([&](unsigned long long i) -> uint32_t { return i < wlim ? __ldg(words + i) : 0u; },
-                           start, s_lut, s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T, t,
-                           xhat, &bad);
+                           start, s_lut, s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T_out,
+                           sh.t_off + t, xhat, &bad);
   }
   if (bad || used != clen) dec_fail(g, epoch, EBC_ERR_CORRUPT);
 }
@@ -695,12 +697,12 @@ __global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __
   const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
   const unsigned long long i_start = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
   if (__ldcg(&g->window) != 0u) {   // source = the chain's literal root
-    const uint32_t T = (uint32_t)sh.T;
+    const uint32_t To = (uint32_t)sh.T_out;   // output rows hold T_out tables; ours start at column t_off
     for (unsigned long long i = i_start; i < n4; i += stride) {
       const uint2 m = __ldcg(&w.mdesc[i / kQ]);
       const unsigned long long q = i % kQ;
-      const uint32_t b = m.x / T, t = m.x - b * T;
-      const uint32_t from = __ldcg(&w.srcrow[(size_t)t * sh.B + b]) * T + t;
+      const uint32_t b = m.x / To, col = m.x - b * To;
+      const uint32_t from = __ldcg(&w.srcrow[(size_t)(col - (uint32_t)sh.t_off) * sh.B + b]) * To + col;
       __stcs(reinterpret_cast<float4*>(xhat + (size_t)m.x * D + 4 * q),
              *reinterpret_cast<const float4*>(xhat + (size_t)from * D + 4 * q));
     }

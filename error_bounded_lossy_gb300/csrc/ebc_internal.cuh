@@ -59,6 +59,8 @@ struct Shape {
   int qseg;       // quantization segments per table: ceil(B / SB) (k_quantize works on whole tables)
   int W;          // bytes per code in the scratch: 1 (radius 128) or 2 (radius 512)
   int A;          // symbols of the alphabet: 256 or 1024
+  int T_out;      // decode: tables of the output rows (T, or more when decoding into columns)
+  int t_off;      // decode: output column of the container's first table
 };
 
 // The two alphabets, by code width W in bytes.
@@ -198,7 +200,7 @@ struct Work {
   DecTab* dtab;                // [U]
   uint4* cdesc;                // [U*nseg*chunks] {start bit lo, start bit hi | length << 16, segment, first literal | rows << 16}
   uint16_t* litrow;            // [U*nseg][SB] literal rows of each segment, in row order
-  uint2* mdesc;                // [n_match] {destination row, source row} as b * T + t
+  uint2* mdesc;                // [n_match] {destination row, source row} as b * T_out + t_off + t
   uint32_t* srcrow;            // [T][B] windowed containers: each row's source row (itself for a literal)
   uint4* runmap;               // [dec_run_slots] {table, first chunk, end chunk, 0} of each run of chunks;
                                //   table ~0u = no run

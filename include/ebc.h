@@ -231,6 +231,16 @@ int ebc_compress_chunked_bf16(ebc_ctx* ctx, const uint16_t* d_x, int64_t B, int 
 int ebc_decompress_chunked(ebc_ctx* ctx, const void* d_in, uint64_t in_bytes, const uint64_t* d_offsets,
                            int n_chunks, float* d_xhat, int64_t B, int T, int D, void* stream);
 
+/* The receiving side of the all-to-all (Fig. 7, bottom): a container of T
+ * tables (from one sender) restores columns [t_off, t_off + T) of d_xhat[B]
+ * [T_out][D] (device, fp32, 16-byte aligned); the other columns are not
+ * touched.  One call per sender, each on its own stream (with its own context)
+ * to decode them in parallel.  0 <= t_off, t_off + T <= T_out, and [B, T_out, D]
+ * must be a supported shape, else EBC_ERR_INVALID_ARG.  Otherwise as
+ * ebc_decompress. */
+int ebc_decompress_columns(ebc_ctx* ctx, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T,
+                           int D, int T_out, int t_off, void* stream);
+
 /* Host-buffer variants (synchronous): the input is copied from host memory
  * h_x (pinned memory is fastest) to context-owned device buffers, processed,
  * and the result copied back.  ebc_compress_host writes the container to

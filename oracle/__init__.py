@@ -304,3 +304,16 @@ def decompress_chunked(buf, offsets, B: int, T: int, D: int):
         xh, _ = decompress(buf[offsets[r]:offsets[r + 1]], b1 - b0, T, D)
         xhat[b0:b1] = xh
     return xhat
+
+
+def decompress_columns(buf, B: int, T: int, D: int, T_out: int, t_off: int, out=None):
+    """The receiving side of the all-to-all (§III-E, Fig. 7 bottom): a container
+    of T tables restores columns [t_off, t_off + T) of an output [B, T_out, D];
+    the other columns are left as they are."""
+    if not (0 <= t_off and t_off + T <= T_out):
+        raise ValueError("columns out of range")
+    if out is None:
+        out = np.zeros((B, T_out, D), dtype=np.float32)
+    xh, _ = decompress(buf, B, T, D)
+    out[:, t_off:t_off + T] = xh
+    return out

@@ -236,3 +236,44 @@ def test_capacity(codec):
     assert rc == 0
     assert codec.last_error() == ebc.EBC_ERR_CAPACITY
     assert int(o2[-1].item()) == need
+
+
+def test_receiving_side_columns_on_parallel_streams():
+    # three senders (2, 3 and 4 tables; one with a window, one with the wide alphabet), each
+    # container decoded into its columns of one [B, 9, D] output, each on its own stream
+    B, D, T_out = 1500, 32, 9
+    senders = [(2, 0, 128), (3, 16, 128), (4, 0, 512)]   # tables, window, radius
+    out = torch.full((B, T_out, D), 7.0, dtype=torch.float32, device="cuda")
+    ref = np.full((B, T_out, D), np.float32(7.0))
+    keep = []
+    col = 0
+    for k, (Ts, win, rad) in enumerate(senders):
+        x, eb = _dup_rows(B, Ts, D, seed=40 + k, pool=300)
+        enc = ebc.Codec(0)
+        enc.set_radius(rad)
+        enc.set_window(win)
+        buf, nb = enc.compress(torch.from_numpy(x).cuda(), eb)
+        torch.cuda.synchronize()
+        assert enc.last_error() == 0
+        n = int(nb.item())
+        enc.close()
+        dec = ebc.Codec(0)
+        dec.set_radius(rad)
+        st = torch.cuda.Stream()
+        dec.decompress_columns(buf, n, Ts, out, col, stream=st)
+        keep.append((dec, st, buf))
+        oracle.decompress_columns(buf[:n].cpu().numpy(), B, Ts, D, T_out, col, out=ref)
+        col += Ts
+    torch.cuda.synchronize()
+    for dec, _, _ in keep:
+        assert dec.last_error() == 0
+    assert np.array_equal(out.cpu().numpy().view(np.uint32), ref.view(np.uint32))
+    # columns outside the output are refused before any device work
+    dec = keep[0][0]
+    buf = keep[0][2]
+    for Ts, t_off in ((2, 8), (2, -1)):
+        rc = ebc.ebc_decompress_columns(dec.handle, ctypes.c_void_p(buf.data_ptr()), buf.numel(),
+                                        ctypes.c_void_p(out.data_ptr()), B, Ts, D, T_out, t_off, None)
+        assert rc == ebc.EBC_ERR_INVALID_ARG
+    for dec, _, _ in keep:
+        dec.close()

@@ -105,3 +105,21 @@ def test_empty_slices():
         assert _u64(buf[int(offs[r]):int(offs[r + 1])], 8) == b1 - b0
     xh = o.decompress_chunked(buf, offs, 2, 1, 4)
     assert np.array_equal(xh, o.decompress(o.compress(x, eb)[0], 2, 1, 4)[0])
+
+
+def test_columns_of_a_wider_output():
+    # three senders with 2, 3 and 1 tables fill the columns of one [B, 6, D] output
+    wl = workloads.make("tiny", batch=100)
+    x, eb = wl.x.numpy(), wl.eb.numpy()          # [100, 4, 16]
+    parts = [x[:, 0:2], x[:, 1:4], x[:, 3:4]]
+    out = np.full((100, 6, 16), np.float32(7.0))
+    col = 0
+    for p, e in zip(parts, (eb[0:2], eb[1:4], eb[3:4])):
+        p = np.ascontiguousarray(p)
+        buf, _ = o.compress(p, e)
+        o.decompress_columns(buf, 100, p.shape[1], 16, 6, col, out=out)
+        assert np.array_equal(out[:, col:col + p.shape[1]], o.decompress(buf, *p.shape)[0])
+        col += p.shape[1]
+    assert col == 6
+    with pytest.raises(ValueError):
+        o.decompress_columns(buf, 100, 1, 16, 6, 6)
