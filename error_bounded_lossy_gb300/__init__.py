@@ -317,6 +317,10 @@ class Codec:
 
     compress(x, eb) -> (container uint8 CUDA tensor [capacity], nbytes int64 CUDA tensor [1])
     decompress(container, nbytes_or_len, B, T, D) -> xhat float32 CUDA tensor [B, T, D]
+    compress_chunked(x, n, eb) -> (buffer, offsets [n + 1]): one container per batch slice
+    decompress_chunked(buffer, nbytes, offsets, B, T, D) -> xhat
+    decompress_columns(container, nbytes, T, out, t_off): a sender's tables into columns of out
+    set_window(w), set_table_modes(modes), set_radius(128 | 512): options of later calls
     """
 
     def __init__(self, device: int = 0):
