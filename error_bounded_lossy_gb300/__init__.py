@@ -30,7 +30,7 @@ __all__ = [
     "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
     "EBC_MAX_CHUNKS", "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16",
     "ebc_decompress_chunked", "EBC_RADIUS", "EBC_RADIUS_WIDE", "ebc_set_radius", "ebc_compress_bound_radius",
-    "ebc_decompress_columns",
+    "ebc_decompress_columns", "EbcConfig", "ebc_set_first_wait_polls",
 ]
 
 EBC_OK, EBC_ERR_INVALID_ARG, EBC_ERR_CAPACITY, EBC_ERR_CORRUPT = 0, 1, 2, 3
@@ -49,8 +49,16 @@ EXPORTED_SYMBOLS = (
     "ebc_decompress_noalloc", "ebc_set_table_modes", "ebc_get_table_stats", "ebc_homo_index", "ebc_speedup",
     "ebc_select_modes", "ebc_select_table_modes", "ebc_table_homo_index", "ebc_set_window", "ebc_compress_bf16",
     "ebc_compress_chunked_bound", "ebc_compress_chunked", "ebc_compress_chunked_bf16", "ebc_decompress_chunked",
-    "ebc_set_radius", "ebc_compress_bound_radius", "ebc_decompress_columns",
+    "ebc_set_radius", "ebc_compress_bound_radius", "ebc_decompress_columns", "ebc_set_first_wait_polls",
 )
+
+
+class EbcConfig(ctypes.Structure):
+    """ebc_config: options of a context (EbcConfig() is EBC_CONFIG_DEFAULT)."""
+    _fields_ = [(n, ctypes.c_int) for n in ("radius", "chunk_vectors", "max_code_len", "dedup", "window")]
+
+    def __init__(self, radius=128, chunk_vectors=0, max_code_len=24, dedup=1, window=0):
+        super().__init__(int(radius), int(chunk_vectors), int(max_code_len), int(dedup), int(window))
 
 
 class EbcStats(ctypes.Structure):
@@ -100,22 +108,23 @@ def lib():
             sig = {
                 "ebc_version": (I, []),
                 "ebc_strerror": (ctypes.c_char_p, [I]),
-                "ebc_create": (I, [ctypes.POINTER(P), I]),
+                "ebc_create": (I, [ctypes.POINTER(P), ctypes.POINTER(EbcConfig), I]),
                 "ebc_destroy": (None, [P]),
                 "ebc_set_error_bounds": (I, [P, P, I, I64, I, D, I64, I]),
                 "ebc_get_error_bounds": (I, [P, P, I]),
-                "ebc_compress_bound": (U64, [I64, I, I]),
+                "ebc_compress_bound": (U64, [I64, I, I, ctypes.POINTER(EbcConfig)]),
                 "ebc_compress": (I, [P, P, I64, I, I, P, P, U64, P, P]),
                 "ebc_decompress": (I, [P, P, U64, P, I64, I, I, P]),
                 "ebc_compress_host": (I, [P, P, I64, I, I, P, P, U64, P, P]),
                 "ebc_decompress_host": (I, [P, P, U64, P, I64, I, I, P]),
-                "ebc_get_stats": (I, [P, ctypes.POINTER(EbcStats)]),
+                "ebc_get_stats": (I, [P, ctypes.POINTER(EbcStats), P]),
                 "ebc_last_device_error": (I, [P]),
                 "ebc_set_profiling": (I, [P, I]),
                 "ebc_get_profile": (I, [P, ctypes.POINTER(EbcKernelTime), I, ctypes.POINTER(I)]),
                 "ebc_decompress_noalloc": (I, [P, U64, P, I64, I, I, P]),
                 "ebc_set_table_modes": (I, [P, P, I]),
                 "ebc_set_window": (I, [P, I]),
+                "ebc_set_first_wait_polls": (I, [P, I]),
                 "ebc_compress_bf16": (I, [P, P, I64, I, I, P, P, U64, P, P]),
                 "ebc_get_table_stats": (I, [P, ctypes.POINTER(EbcTableStats), I]),
                 "ebc_homo_index": (D, [U64, U64]),
@@ -148,9 +157,10 @@ def ebc_strerror(code: int) -> str:
     return lib().ebc_strerror(int(code)).decode()
 
 
-def ebc_create(device: int = 0):
+def ebc_create(device: int = 0, config: "EbcConfig | None" = None):
+    """A context on `device` with options `config` (None = the defaults)."""
     h = ctypes.c_void_p()
-    rc = lib().ebc_create(ctypes.byref(h), int(device))
+    rc = lib().ebc_create(ctypes.byref(h), ctypes.byref(config) if config is not None else None, int(device))
     if rc:
         raise EbcError(rc, "ebc_create")
     return h
@@ -169,8 +179,9 @@ def ebc_get_error_bounds(ctx, eb_out_ptr, T) -> int:
     return lib().ebc_get_error_bounds(ctx, eb_out_ptr, int(T))
 
 
-def ebc_compress_bound(B: int, T: int, D: int) -> int:
-    return int(lib().ebc_compress_bound(int(B), int(T), int(D)))
+def ebc_compress_bound(B: int, T: int, D: int, config: "EbcConfig | None" = None) -> int:
+    return int(lib().ebc_compress_bound(int(B), int(T), int(D),
+                                        ctypes.byref(config) if config is not None else None))
 
 
 def ebc_compress(ctx, d_x, B, T, D, eb_ptr, d_out, out_capacity, d_out_bytes, stream) -> int:
@@ -223,6 +234,11 @@ def ebc_set_window(ctx, window) -> int:
     return lib().ebc_set_window(ctx, int(window))
 
 
+def ebc_set_first_wait_polls(ctx, polls) -> int:
+    """Test aid: polls of the quantize kernel's first tile wait (negative = the full limit)."""
+    return lib().ebc_set_first_wait_polls(ctx, int(polls))
+
+
 def ebc_set_table_modes(ctx, modes_ptr, T) -> int:
     return lib().ebc_set_table_modes(ctx, modes_ptr, int(T))
 
@@ -268,9 +284,10 @@ def ebc_decompress_host(ctx, h_in, in_bytes, h_xhat, B, T, D, stream) -> int:
     return lib().ebc_decompress_host(ctx, h_in, int(in_bytes), h_xhat, int(B), int(T), int(D), stream)
 
 
-def ebc_get_stats(ctx):
+def ebc_get_stats(ctx, stream=None):
+    """(return code, EbcStats); stream: a cudaStream_t pointer or None (the last call's)."""
     st = EbcStats()
-    rc = lib().ebc_get_stats(ctx, ctypes.byref(st))
+    rc = lib().ebc_get_stats(ctx, ctypes.byref(st), stream)
     return rc, st
 
 
@@ -323,11 +340,11 @@ class Codec:
     set_window(w), set_table_modes(modes), set_radius(128 | 512): options of later calls
     """
 
-    def __init__(self, device: int = 0):
+    def __init__(self, device: int = 0, config: "EbcConfig | None" = None):
         import torch
         self.device = torch.device("cuda", device)
-        self._ctx = ebc_create(device)
-        self.radius = EBC_RADIUS
+        self._ctx = ebc_create(device, config)
+        self.radius = config.radius if config is not None and config.radius else EBC_RADIUS
 
     def close(self):
         if self._ctx is not None:

@@ -65,6 +65,8 @@ struct ebc_ctx {
   // per-table coding modes (0 = dedup + Huffman for every table when modes_T == 0)
   int window = 0;                      // dedup window of the compress calls (0 = whole batch)
   int radius = kRadius;                // alphabet of the compress and decompress calls (128 or 512)
+  uint32_t mode_or = 0;                // modes added to every table's (kModeNoDedup: dedup off by config)
+  int first_wait = kWaitLimit;         // polls of the quantize kernel's first tile wait (test aid)
   uint8_t* d_modes = nullptr;          // device [kMaxT]
   uint8_t h_modes[kMaxT] = {};
   int modes_T = 0;
@@ -92,6 +94,7 @@ static Shape make_shape(int64_t B, int T, int D, int nsm = 0, int window = 0, in
   sh.A = 2 * radius;
   sh.T_out = T;
   sh.t_off = 0;
+  sh.first_wait = kWaitLimit;
   sh.nsm = nsm;
   sh.B = B;
   sh.T = T;
@@ -239,9 +242,22 @@ const char* ebc_strerror(int code) {
   }
 }
 
-int ebc_create(ebc_ctx** out, int device) {
+// A config the format can honour: the radius is 128 or 512, the chunk size and
+// the longest code are the format's own (0 selects them), dedup is on or off,
+// the window is 0..255.
+static bool config_ok(const ebc_config* cfg) {
+  if (!cfg) return true;
+  const bool radius = cfg->radius == 0 || cfg->radius == kRadius || cfg->radius == kRadiusWide;
+  return radius && cfg->chunk_vectors == 0 && (cfg->max_code_len == 0 || cfg->max_code_len == kLmax) &&
+         (cfg->dedup == 0 || cfg->dedup == 1) && cfg->window >= 0 && cfg->window <= kMaxWindow;
+}
+
+static int config_radius(const ebc_config* cfg) { return cfg && cfg->radius ? cfg->radius : kRadius; }
+
+int ebc_create(ebc_ctx** out, const ebc_config* cfg, int device) {
   if (!out) return EBC_ERR_INVALID_ARG;
   *out = nullptr;
+  if (!config_ok(cfg)) return EBC_ERR_INVALID_ARG;
   int n = 0;
   if (cudaGetDeviceCount(&n) != cudaSuccess || device < 0 || device >= n) return EBC_ERR_NO_DEVICE;
   cudaDeviceProp prop;
@@ -252,6 +268,9 @@ int ebc_create(ebc_ctx** out, int device) {
   if (!c) return EBC_ERR_INTERNAL;
   c->device = device;
   c->nsm = prop.multiProcessorCount;
+  c->radius = config_radius(cfg);
+  c->window = cfg ? cfg->window : 0;
+  c->mode_or = cfg && cfg->dedup == 0 ? kModeNoDedup : 0u;
   if (cudaMalloc(&c->glob, sizeof(Glob)) != cudaSuccess || cudaMemset(c->glob, 0, sizeof(Glob)) != cudaSuccess ||
       cudaMalloc(&c->d_nbytes, 16) != cudaSuccess || cudaMallocHost(&c->h_pinned, 64) != cudaSuccess ||
       cudaMalloc(&c->d_modes, kMaxT) != cudaSuccess) {
@@ -346,7 +365,10 @@ int ebc_get_error_bounds(const ebc_ctx* c, float* eb_out, int T) {
 
 static bool radius_ok(int radius) { return radius == kRadius || radius == kRadiusWide; }
 
-uint64_t ebc_compress_bound(int64_t B, int T, int D) { return ebc_compress_bound_radius(B, T, D, kRadius); }
+uint64_t ebc_compress_bound(int64_t B, int T, int D, const ebc_config* cfg) {
+  if (!config_ok(cfg)) return 0;
+  return ebc_compress_bound_radius(B, T, D, config_radius(cfg));
+}
 
 uint64_t ebc_compress_bound_radius(int64_t B, int T, int D, int radius) {
   if (!shape_ok(B, T, D) || !radius_ok(radius)) return 0;
@@ -394,7 +416,8 @@ static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T
     if (!eb_ok(ebs[t])) return EBC_ERR_INVALID_ARG;
     ep.eb[t] = ebs[t];
   }
-  const Shape sh = make_shape(B, T, D, c->nsm, c->window, R, c->radius);
+  Shape sh = make_shape(B, T, D, c->nsm, c->window, R, c->radius);
+  sh.first_wait = c->first_wait;
   if (out_capacity < (R == 1 ? fixed_bytes(sh) : fixed_bytes_sliced(B, T, D, R, c->radius))) return EBC_ERR_CAPACITY;
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
   size_t need = 0;
@@ -403,6 +426,7 @@ static int compress_any(ebc_ctx* c, const void* d_x, bool bf16, int64_t B, int T
   if (rc) return rc;
   Work w = carve_compress(c->cbuf, sh, c->glob, &need);
   w.modes = c->modes_T ? c->d_modes : nullptr;
+  w.mode_or = c->mode_or;
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
   c->cepoch = (c->cepoch + 1) & 0xFFFFFFu;
@@ -511,6 +535,12 @@ int ebc_set_radius(ebc_ctx* c, int radius) {
   return EBC_OK;
 }
 
+int ebc_set_first_wait_polls(ebc_ctx* c, int polls) {
+  if (!c || polls > kWaitLimit) return EBC_ERR_INVALID_ARG;
+  c->first_wait = polls < 0 ? kWaitLimit : polls;
+  return EBC_OK;
+}
+
 int ebc_set_window(ebc_ctx* c, int window) {
   if (!c || window < 0 || window > kMaxWindow) return EBC_ERR_INVALID_ARG;
   c->window = window;
@@ -609,12 +639,15 @@ int ebc_last_device_error(ebc_ctx* c) {
   return (int)code;
 }
 
-int ebc_get_stats(ebc_ctx* c, ebc_stats* out) {
+int ebc_get_stats(ebc_ctx* c, ebc_stats* out, void* stream) {
   if (!c || !out) return EBC_ERR_INVALID_ARG;
-  const int err = ebc_last_device_error(c);
+  const int err = ebc_last_device_error(c);   // the last call has completed
   if (err == EBC_ERR_CUDA) return err;
+  cudaStream_t st = stream ? (cudaStream_t)stream : c->last_stream;
   Glob g;
-  if (cudaMemcpy(&g, c->glob, sizeof g, cudaMemcpyDeviceToHost) != cudaSuccess) return EBC_ERR_CUDA;
+  if (cudaMemcpyAsync(&g, c->glob, sizeof g, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess)
+    return EBC_ERR_CUDA;
   std::memset(out, 0, sizeof *out);
   out->n_vectors = (uint64_t)c->lastB * c->lastT;
   out->in_bytes = out->n_vectors * c->lastD * 4u;
@@ -757,8 +790,10 @@ static int run_mode(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, const
   return rc;
 }
 
-// Restores the caller's modes after a sampling run.
-static int restore_modes(ebc_ctx* c, int saved_T, const uint8_t* saved) {
+// Restores the caller's modes (and the context's dedup switch, which the
+// sampling runs turn back on) after a sampling run.
+static int restore_modes(ebc_ctx* c, int saved_T, const uint8_t* saved, uint32_t saved_or) {
+  c->mode_or = saved_or;
   return ebc_set_table_modes(c, saved_T ? saved : nullptr, saved_T);
 }
 
@@ -769,6 +804,8 @@ int ebc_select_table_modes(ebc_ctx* c, const float* d_x, int64_t B, int T, int D
   const int saved_T = c->modes_T;
   uint8_t saved[kMaxT];
   std::memcpy(saved, c->h_modes, (size_t)kMaxT);
+  const uint32_t saved_or = c->mode_or;
+  c->mode_or = 0;   // every candidate mode as such
   const Shape sh = make_shape(B, T, D, c->nsm, c->window, 1, c->radius);
   const double raw_bytes = 4.0 * (double)B * D;   // per table
   const double fixed = (double)table_rec_bytes(sh.A) + (double)kSegRecBytes * sh.nseg + 4.0 * sh.nw;
@@ -788,7 +825,7 @@ int ebc_select_table_modes(ebc_ctx* c, const float* d_x, int64_t B, int T, int D
       cr[(size_t)t * 4 + m] = raw_bytes / bytes;
     }
   }
-  const int rr = restore_modes(c, saved_T, saved);
+  const int rr = restore_modes(c, saved_T, saved, saved_or);
   if (!rc) rc = rr;
   if (!rc) rc = ebc_select_modes(cr, tc, td, bw, T, 4, modes_out);
   delete[] cr;
@@ -802,6 +839,8 @@ int ebc_table_homo_index(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, 
   const int saved_T = c->modes_T;
   uint8_t saved[kMaxT];
   std::memcpy(saved, c->h_modes, (size_t)kMaxT);
+  const uint32_t saved_or = c->mode_or;
+  c->mode_or = 0;   // N_compressed counts distinct quantized vectors: dedup on
   float* tiny = new (std::nothrow) float[(size_t)T];
   ebc_table_stats* a = new (std::nothrow) ebc_table_stats[(size_t)T];
   ebc_table_stats* b = new (std::nothrow) ebc_table_stats[(size_t)T];
@@ -819,7 +858,7 @@ int ebc_table_homo_index(ebc_ctx* c, const float* d_x, int64_t B, int T, int D, 
   if (!rc) rc = ebc_get_table_stats(c, b, T);
   if (!rc)
     for (int t = 0; t < T; ++t) eta_out[t] = ebc_homo_index(b[t].n_literal, a[t].n_literal);
-  const int rr = restore_modes(c, saved_T, saved);
+  const int rr = restore_modes(c, saved_T, saved, saved_or);
   if (!rc) rc = rr;
   delete[] tiny;
   delete[] a;

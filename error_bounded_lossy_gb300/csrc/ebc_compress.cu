@@ -172,7 +172,6 @@ __device__ __forceinline__ uint32_t dedup_lookup(const unsigned long long* slots
 // ---------------------------------------------------------------------------
 // Tensor-memory-accelerator (TMA) staging of input tiles.
 // ---------------------------------------------------------------------------
-constexpr int kWaitLimit = 1 << 22;   // polls of an mbarrier before giving up
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -198,9 +197,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0u;
 }
-// Bounded wait for phase `parity` of an mbarrier; false on time-out.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (int i = 0; i < kWaitLimit; ++i)
+// Bounded wait for phase `parity` of an mbarrier (at most `limit` polls); false on time-out.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int limit = kWaitLimit) {
+  for (int i = 0; i < limit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
   return false;
 }
@@ -263,7 +262,7 @@ __device__ __forceinline__ void issue_segment_tile(In* stage, const CUtensorMap*
 // ---------------------------------------------------------------------------
 template <int D, typename In, int W>
 __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtensorMap tmap, Shape sh, EbParams ep,
-                                                   Work w) {
+                                                   Work w, uint32_t epoch) {
   pdl_enter();
   using G = Geo<D>;
   using Q = QGeo<D, In>;
@@ -303,11 +302,18 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     const float eb = ep.eb[t];
     const float ebx2 = __fmul_rn(2.0f, eb);
     const float inv = __fdiv_rn(1.0f, ebx2);
-    const bool arrived = mbar_wait(&s_bar[stg], (parity >> stg) & 1u);
+    const bool arrived = mbar_wait(&s_bar[stg], (parity >> stg) & 1u, i == 0 ? sh.first_wait : kWaitLimit);
     if (__syncthreads_or(!arrived)) {   // the whole CTA stops together
-      if (tid == 0) record_error(w.glob, EBC_ERR_DEVICE_TIMEOUT);
-      // a copy may still be in flight: wait for it once more (bounded), then stop
-      if (!arrived) mbar_wait(&s_bar[stg], (parity >> stg) & 1u);
+      if (tid == 0) {
+        record_error(w.glob, EBC_ERR_DEVICE_TIMEOUT);
+        // the call is given up: the kernels after this one write nothing to the output
+        atomicExch(&w.glob->cabort, status_word(epoch, EBC_ERR_DEVICE_TIMEOUT));
+        // no copy may still be writing into this CTA's shared memory when it exits: wait (with
+        // the full limit) for this stage's tile and for the next one, if it was issued
+        if (!arrived) mbar_wait(&s_bar[stg], (parity >> stg) & 1u);
+        if (seg + (int)gridDim.x < nsegT) mbar_wait(&s_bar[stg ^ 1], (parity >> (stg ^ 1)) & 1u);
+      }
+      __syncthreads();
       return;
     }
     parity ^= 1u << stg;
@@ -367,7 +373,7 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
       const int seg = (int)blockIdx.x + (i / G::kSB) * (int)gridDim.x;
       const int t = seg / sh.qseg;
       const int64_t b = (int64_t)(seg - t * sh.qseg) * G::kSB + i % G::kSB;
-      const bool valid = b < B && !(w.modes && (w.modes[t] & kModeNoDedup));
+      const bool valid = b < B && !(table_mode(w, t) & kModeNoDedup);
       // each slice keeps its own table: a row never refers into another slice
       const int u = valid ? slice_of_row(sh, b) * sh.T + t : 0;
       const unsigned vmask = __ballot_sync(0xffffffffu, valid);
@@ -428,7 +434,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   const int64_t row0 = b0 + (int64_t)s * G::kSB;
   const unsigned long long* slots = w.slots + (size_t)u * sh.S;
   const uint8_t* symt = w.sym + (size_t)t * sh.symstride;
-  const bool nodedup = w.modes && (w.modes[t] & kModeNoDedup);   // every row its own reference
+  const bool nodedup = (table_mode(w, t) & kModeNoDedup) != 0;   // every row its own reference
   // the segment's codes start so words into s_sym (a slice may start off a 16-byte boundary when
   // D * W < 16; so is even when W = 2)
   const int so = D * W >= 16 ? 0 : (int)(((size_t)row0 * D * W) & 15u) / 4;
@@ -678,7 +684,8 @@ __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Wor
   }
   __syncthreads();
   const unsigned long long total = s_total;
-  const int status = total > cap ? EBC_ERR_CAPACITY : EBC_OK;
+  int status = total > cap ? EBC_ERR_CAPACITY : EBC_OK;
+  if (__ldcg(&g->cabort) == status_word(epoch, EBC_ERR_DEVICE_TIMEOUT)) status = EBC_ERR_DEVICE_TIMEOUT;
   if (tid < sh.R) {
     c.base = s_size[tid];
     w.cont[tid] = c;
@@ -903,7 +910,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
 
   if (u < U) {
     const int t = u % T;
-    const bool raw = w.modes && (w.modes[t] & kModeRawCodes);   // every code log2(A) bits: no Huffman
+    const bool raw = (table_mode(w, t) & kModeRawCodes) != 0;   // every code log2(A) bits: no Huffman
     if constexpr (W == 2) {
       huffman_wide(sh, ep, w, u, t, raw, s_f, s_lw, s_nodew, s_key, s_order, s_leafpar, s_nodepar, s_depth, s_len,
                    s_count, s_next, &s_wcnt[0][0], s_run, s_bits64, &s_maxlen, s_warp);
@@ -1554,7 +1561,7 @@ static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, 
     unsigned qgrid = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm);
     if (qgrid > qsegs) qgrid = qsegs;
     prof_begin(prof, "k_quantize", st);
-    launch_k(k_quantize<D, In, W>, qgrid, 256, smem, st, *xmap, sh, ep, w);
+    launch_k(k_quantize<D, In, W>, qgrid, 256, smem, st, *xmap, sh, ep, w, epoch);
     prof_end(prof, st);
 
     prof_begin(prof, "k_resolve", st);

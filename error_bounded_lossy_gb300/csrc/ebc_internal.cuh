@@ -29,6 +29,8 @@ constexpr int kDecRun = 64;                // chunks per decoder CTA (one thread
 
 constexpr unsigned long long kEmptySlot = ~0ull;
 
+constexpr int kWaitLimit = 1 << 22;        // polls of an mbarrier before a wait gives up
+
 // Shape-derived constants of one call.
 //
 // The batch may be split into R slices (the rows of one destination rank of an
@@ -59,6 +61,7 @@ struct Shape {
   int qseg;       // quantization segments per table: ceil(B / SB) (k_quantize works on whole tables)
   int W;          // bytes per code in the scratch: 1 (radius 128) or 2 (radius 512)
   int A;          // symbols of the alphabet: 256 or 1024
+  int first_wait; // polls of each quantize CTA's first input-tile wait (a test aid; normally the full limit)
   int T_out;      // decode: tables of the output rows (T, or more when decoding into columns)
   int t_off;      // decode: output column of the container's first table
 };
@@ -153,7 +156,8 @@ struct Glob {
   unsigned int dstat;     // (epoch << 8) | status of the last decompress
   unsigned int sticky;    // first device error since the last query (0 = none)
   unsigned int window;    // the window of the container being decoded (0 = whole batch)
-  unsigned int pad[3];
+  unsigned int cabort;    // (epoch << 8) | status: a compress call given up by its quantize kernel
+  unsigned int pad[2];
   unsigned long long n_lit, n_match, n_out, n_chunks, words;
   unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
 };
@@ -175,6 +179,7 @@ struct DecTab {
 // Device scratch of a context.  Sizes follow Shape.
 struct Work {
   const uint8_t* modes;        // [T] per-table modes, or null (all 0)
+  uint32_t mode_or;            // modes added to every table's (dedup switched off for the context)
   unsigned long long* tab_bits;   // [U] bits of the unit's literal codes and outlier values
   // compress
   uint8_t* sym;                // [T][B][D] quantization codes (W bytes each), table t at t * symstride
@@ -206,6 +211,11 @@ struct Work {
                                //   table ~0u = no run
   Glob* glob;
 };
+
+// The modes of table t in a compress call.
+__device__ __forceinline__ uint32_t table_mode(const Work& w, int t) {
+  return (w.modes ? (uint32_t)w.modes[t] : 0u) | w.mode_or;
+}
 
 // Error bits kept in Glob::sticky / status words.
 __host__ __device__ constexpr unsigned int status_word(uint32_t epoch, int code) {

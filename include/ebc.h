@@ -114,10 +114,40 @@ int ebc_version(void);
 /* Human-readable text of an EBC_* code; never NULL. */
 const char* ebc_strerror(int code);
 
-/* Create a context on CUDA device `device` (must be sm_103).  *out receives
- * the context; it is released with ebc_destroy.  Returns EBC_ERR_NO_DEVICE if
- * the device is absent or not sm_103. */
-int ebc_create(ebc_ctx** out, int device);
+/* Options of a context, fixed when it is created (NULL = the defaults,
+ * EBC_CONFIG_DEFAULT).  The paper ("Accelerating Communication in Deep
+ * Learning Recommendation Model Training with Dual-Level Adaptive Lossy
+ * Compression", §III-D) names the quantization encoder, the vector-based LZ
+ * and the Huffman encoder but fixes none of their numbers; this container
+ * format fixes two of them (the header records both), and a config that asks
+ * for other values is refused with EBC_ERR_INVALID_ARG:
+ *   radius         quantization radius: EBC_RADIUS (128; 0 selects it) or
+ *                  EBC_RADIUS_WIDE (512), as ebc_set_radius
+ *   chunk_vectors  literal vectors per chunk (the decoder's unit of
+ *                  parallelism): 0 = the format's max(1, 128/D); nothing else
+ *   max_code_len   longest Huffman code: 0 or 24 (the format's); nothing else
+ *   dedup          1: vector-based LZ (the default); 0: every vector a literal,
+ *                  as EBC_MODE_HUFFMAN for every table (per-table modes set
+ *                  later still apply on top)
+ *   window         dedup window in rows: 0 = the whole batch, first occurrence
+ *                  (the default), 1..255 = nearest earlier vector (ebc_set_window)
+ * The radius and window can be changed later with ebc_set_radius and
+ * ebc_set_window. */
+typedef struct {
+  int radius;
+  int chunk_vectors;
+  int max_code_len;
+  int dedup;
+  int window;
+} ebc_config;
+#define EBC_CONFIG_DEFAULT {128, 0, 24, 1, 0}
+
+/* Create a context on CUDA device `device` (must be sm_103) with options cfg
+ * (host struct, read during the call; NULL = EBC_CONFIG_DEFAULT).  *out
+ * receives the context; it is released with ebc_destroy.  Returns
+ * EBC_ERR_INVALID_ARG for a bad cfg (checked first, without touching a
+ * device), EBC_ERR_NO_DEVICE if the device is absent or not sm_103. */
+int ebc_create(ebc_ctx** out, const ebc_config* cfg, int device);
 
 /* Release a context and its device scratch (synchronises the device).  NULL
  * is accepted. */
@@ -133,9 +163,10 @@ int ebc_set_error_bounds(ebc_ctx* ctx, const float* eb_base, int T, int64_t iter
 /* Copy the current scheduled bounds (T of them) into eb_out (host). */
 int ebc_get_error_bounds(const ebc_ctx* ctx, float* eb_out, int T);
 
-/* Worst-case container bytes for a [B,T,D] input with the default alphabet
- * (radius 128); 0 for an unsupported shape. */
-uint64_t ebc_compress_bound(int64_t B, int T, int D);
+/* Worst-case container bytes for a [B,T,D] input coded with options cfg
+ * (NULL = EBC_CONFIG_DEFAULT; only its radius changes the bound); 0 for an
+ * unsupported shape or a bad cfg.  Host-only. */
+uint64_t ebc_compress_bound(int64_t B, int T, int D, const ebc_config* cfg);
 
 /* Alphabet of the quantization codes.  Radius 128 (the default): bins q in
  * (-128, 128), 8-bit codes q + 128, 256 symbols.  Radius 512, the wide
@@ -360,14 +391,29 @@ int ebc_table_homo_index(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D
 int ebc_decompress_noalloc(const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
                            void* stream);
 
-/* Counts of the last compress call (synchronises its stream).  Returns the
- * recorded device error of the context, if any, as ebc_last_device_error. */
-int ebc_get_stats(ebc_ctx* ctx, ebc_stats* out);
+/* Counts of the last compress call of the context, read on `stream` (a
+ * cudaStream_t; NULL = the stream of the context's last call) after that call
+ * has completed; synchronises both streams.  Returns the recorded device error
+ * of the context, if any, as ebc_last_device_error. */
+int ebc_get_stats(ebc_ctx* ctx, ebc_stats* out, void* stream);
 
 /* Synchronise the stream of the last call and return (and clear) the first
  * error the kernels recorded since the previous query: EBC_OK,
  * EBC_ERR_CAPACITY, EBC_ERR_CORRUPT, EBC_ERR_INVALID_ARG or EBC_ERR_INTERNAL. */
 int ebc_last_device_error(ebc_ctx* ctx);
+
+/* Failure-detection test aid.  Every device-side wait of the codec is bounded:
+ * the quantize kernel polls the barrier of each input tile at most 2^22 times,
+ * and a wait that runs out records EBC_ERR_DEVICE_TIMEOUT, drains the tile
+ * copies still in flight (waiting for them with the full limit), and stops its
+ * block; the kernels after it then write nothing to the output, and the next
+ * ebc_last_device_error() returns the code.  This sets the number of polls of
+ * the FIRST tile wait of each quantize block of the following compress calls
+ * (0 <= polls <= 2^22; a negative value restores the full limit, which is the
+ * default).  With 0 the first wait gives up before looking, so a test can run
+ * the time-out path without hanging anything; later waits keep the full
+ * limit.  Host-only; EBC_ERR_INVALID_ARG for a null context or polls > 2^22. */
+int ebc_set_first_wait_polls(ebc_ctx* ctx, int polls);
 
 /* Per-kernel timing (tracing aid).  While enabled, every kernel launch of the
  * context is bracketed by a pair of CUDA events on its stream (up to 2048

@@ -59,7 +59,7 @@ def test_create_without_device_reports_no_device(lib):
     if torch.cuda.is_available():
         pytest.skip("a GPU is present")
     h = ctypes.c_void_p()
-    assert lib.ebc_create(ctypes.byref(h), 0) == ebc.EBC_ERR_NO_DEVICE
+    assert lib.ebc_create(ctypes.byref(h), None, 0) == ebc.EBC_ERR_NO_DEVICE
     assert not h.value
     assert lib.ebc_last_device_error(None) == ebc.EBC_ERR_INVALID_ARG
 
@@ -88,3 +88,32 @@ def test_chunked_and_radius_calls_reject_bad_arguments_before_any_device_work(li
     assert ebc.ebc_compress_chunked_bf16(None, None, 8, 2, 16, None, 2, None, 0, None, None) == \
         ebc.EBC_ERR_INVALID_ARG
     assert ebc.ebc_decompress_chunked(None, None, 0, None, 2, None, 8, 2, 16, None) == ebc.EBC_ERR_INVALID_ARG
+
+
+def test_config_path_through_ctypes(lib):
+    """ebc_config: NULL and EBC_CONFIG_DEFAULT agree; the radius changes the
+    bound as the oracle's does; values the container format does not allow are
+    refused before any device is touched."""
+    default = ebc.EbcConfig()
+    assert (default.radius, default.chunk_vectors, default.max_code_len, default.dedup, default.window) == \
+        (128, 0, 24, 1, 0)
+    for shape in [(0, 3, 16), (512, 4, 16), (8192, 26, 128), (33, 2, 512)]:
+        assert ebc.ebc_compress_bound(*shape, default) == ebc.ebc_compress_bound(*shape) == oracle.compress_bound(*shape)
+        assert ebc.ebc_compress_bound(*shape, ebc.EbcConfig(radius=512)) == oracle.compress_bound(*shape, radius=512)
+        assert ebc.ebc_compress_bound(*shape, ebc.EbcConfig(radius=0)) == oracle.compress_bound(*shape)
+        # dedup and window do not change the worst case
+        assert ebc.ebc_compress_bound(*shape, ebc.EbcConfig(dedup=0, window=64)) == oracle.compress_bound(*shape)
+    bad = [ebc.EbcConfig(radius=256), ebc.EbcConfig(chunk_vectors=4), ebc.EbcConfig(max_code_len=16),
+           ebc.EbcConfig(dedup=2), ebc.EbcConfig(window=256), ebc.EbcConfig(window=-1)]
+    for cfg in bad:
+        assert ebc.ebc_compress_bound(512, 4, 16, cfg) == 0
+        h = ctypes.c_void_p()
+        assert lib.ebc_create(ctypes.byref(h), ctypes.byref(cfg), 0) == ebc.EBC_ERR_INVALID_ARG
+        assert not h.value
+    # a good config reaches the device check (no GPU here: NO_DEVICE; with one: a context)
+    import torch
+    if not torch.cuda.is_available():
+        h = ctypes.c_void_p()
+        assert lib.ebc_create(ctypes.byref(h), ctypes.byref(ebc.EbcConfig(radius=512)), 0) == ebc.EBC_ERR_NO_DEVICE
+    # null arguments
+    assert lib.ebc_get_stats(None, None, None) == ebc.EBC_ERR_INVALID_ARG

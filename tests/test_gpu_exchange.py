@@ -1,8 +1,10 @@
 """The exchange helper with NCCL on CUDA tensors, end to end through the codec:
 a one-rank group (every call on this machine gets one GPU) compresses its batch
 as a chunked buffer, trades it through error_bounded_lossy_gb300.exchange, and
-restores the received container into the columns of a wider output, bit for
-bit as the oracle does."""
+restores the received container into the columns of a wider output.  The
+buffer sent is compared with the oracle's chunked buffer byte for byte, the
+buffer received with what was sent, and the restored columns with the oracle's
+column decode bit for bit."""
 import os
 import socket
 
@@ -35,8 +37,15 @@ def test_nccl_exchange_one_rank():
         wl = workloads.make("fwd", batch=1000, tables=3)
         x = wl.x.cuda()
         buf, offs = codec.compress_chunked(x, 1, wl.eb.numpy())
+        torch.cuda.synchronize()
+        assert codec.last_error() == 0
+        # the sending buffer is the oracle's, byte for byte, before it is exchanged
+        rbuf, rofs = oracle.compress_chunked(wl.x.numpy(), wl.eb.numpy(), 1)
+        assert offs.cpu().tolist() == rofs.tolist()
+        assert np.array_equal(buf[: int(rofs[-1])].cpu().numpy(), rbuf)
         recv, roffs = exchange_containers(buf, offs)
         assert recv.is_cuda and roffs.tolist() == offs.tolist()
+        assert np.array_equal(recv.cpu().numpy(), rbuf)
         out = torch.full((1000, 5, 128), 3.0, dtype=torch.float32, device="cuda")
         codec.decompress_columns(recv, int(roffs[-1]), 3, out, 1)
         torch.cuda.synchronize()

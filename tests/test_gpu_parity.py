@@ -76,22 +76,36 @@ def test_workloads_bit_exact(codec, name, kw):
     assert info["total_bytes"] < wl.nbytes
 
 
-@pytest.mark.parametrize("it", [0, 1, 37, 98, 99])
-def test_sweep_iterations_with_schedule(codec, it):
-    wl = workloads.make("sweep", iteration=it)
-    s = wl.schedule
-    base = s["base"].numpy()
-    codec.set_error_bounds(base, s["iteration"], s["fn"], s["m0"], s["phase_len"], s["n_steps"])
-    want = oracle.scheduled_bounds(base, s["fn"], s["iteration"], s["m0"], s["phase_len"], s["n_steps"])
-    assert np.array_equal(codec.error_bounds(base.size), want)
-    # compress with the context's schedule (eb = None) and compare with the oracle
-    x = wl.x.to("cuda")
-    out, nb = codec.compress(x, None)
-    torch.cuda.synchronize()
-    assert codec.last_error() == 0
-    n = int(nb.item())
-    ref, _ = oracle.compress(wl.x.numpy(), want)
-    assert np.array_equal(out[:n].cpu().numpy(), ref)
+@pytest.mark.parametrize("first", [0, 20, 40, 60, 80])
+def test_sweep_all_iterations_with_schedule(codec, first):
+    """The iteration-wise sweep, all 100 iterations (20 per test): each batch is
+    generated on the device, compressed with the context's decayed bounds
+    (eb = None) and compared byte for byte with the oracle's container; every
+    reconstruction meets its bound, and every tenth is compared with the oracle
+    decoder bit for bit."""
+    for it in range(first, first + 20):
+        wl = workloads.make("sweep", iteration=it, device="cuda")
+        s = wl.schedule
+        base = s["base"].numpy()
+        codec.set_error_bounds(base, s["iteration"], s["fn"], s["m0"], s["phase_len"], s["n_steps"])
+        want = oracle.scheduled_bounds(base, s["fn"], s["iteration"], s["m0"], s["phase_len"], s["n_steps"])
+        assert np.array_equal(codec.error_bounds(base.size), want)
+        out, nb = codec.compress(wl.x, None)
+        torch.cuda.synchronize()
+        assert codec.last_error() == 0, it
+        n = int(nb.item())
+        x_np = wl.x.cpu().numpy()
+        ref, _ = oracle.compress(x_np, want)
+        got = out[:n].cpu().numpy()
+        assert n == len(ref) and np.array_equal(got, ref), f"iteration {it}: container differs"
+        xh = codec.decompress(out, n, *wl.shape)
+        torch.cuda.synchronize()
+        assert codec.last_error() == 0, it
+        err = (wl.x.double() - xh.double()).abs().amax(dim=(0, 2)).cpu().numpy()
+        assert (err <= want.astype(np.float64)).all(), f"iteration {it}: bound violated"
+        if it % 10 == 0:
+            xo, _ = oracle.decompress(ref, *wl.shape)
+            assert np.array_equal(xh.cpu().numpy().view(np.uint32), xo.view(np.uint32)), it
 
 
 @pytest.mark.parametrize("fn", ["none", "linear", "stepwise", "drop", "log"])
