@@ -175,9 +175,8 @@ def algorithmic_bytes(kernel: str, N: int, D: int, st: dict) -> int:
         "k_codebook": 0,
         "k_layout": 0,
         "k_emit": C,                                       # container written
-        "k_dec_prep": 0,
-        "k_dec_chunks": C + 4 * D * st["n_literal"],      # container read, literal rows written
-        "k_dec_matches": 4 * D * st["n_match"],           # matched rows written
+        "k_dec_lit": C + 4 * D * st["n_literal"],         # container read, literal rows written
+        "k_dec_match": 4 * D * st["n_match"],             # matched rows written
     }.get(kernel, 0)
 
 

@@ -46,6 +46,8 @@ struct ebc_ctx {
   // decompress scratch
   void* dbuf = nullptr;
   size_t dbuf_bytes = 0;
+  const void* dclean_buf = nullptr;    // dbuf whose decoder accumulators, dclean_bytes long, are zero
+  size_t dclean_bytes = 0;
   // host-buffer staging
   void* stage_in = nullptr;
   size_t stage_in_bytes = 0;
@@ -186,17 +188,15 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   return w;
 }
 
-static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total) {
+// The accumulators come first, so that their bytes (which must be zero before
+// a call) are the same for every shape with as many units and containers.
+static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total, size_t* acc_bytes = nullptr) {
   Carver c{reinterpret_cast<char*>(buf)};
   Work w{};
-  const size_t nsegT = (size_t)sh.U * sh.nseg;
-  const size_t max_chunks = nsegT * (size_t)(sh.SB / sh.KC);
-  w.lut = c.take<uint16_t>(2u * (1u << kLutBits) * (size_t)sh.U);
-  w.dtab = c.take<DecTab>(sizeof(DecTab) * (size_t)sh.U);
-  w.cdesc = c.take<uint4>(16 * max_chunks);
-  w.litrow = c.take<uint16_t>(2 * nsegT * (size_t)sh.SB);
-  w.mdesc = c.take<uint2>(8 * (size_t)sh.B * (size_t)sh.T);
-  w.runmap = c.take<uint4>(16 * (size_t)dec_run_slots(sh));
+  w.uacc = c.take<uint4>(16 * (size_t)(sh.U > 0 ? sh.U : 1));
+  w.cacc = c.take<uint2>(8 * (size_t)sh.R);
+  if (acc_bytes) *acc_bytes = c.off;
+  w.dtab = c.take<DTab>(sizeof(DTab) * (size_t)(sh.U > 0 ? sh.U : 1));
   w.srcrow = c.take<uint32_t>(4 * (size_t)sh.B * (size_t)sh.T);
   w.glob = g;
   *total = c.off;
@@ -277,7 +277,7 @@ int ebc_create(ebc_ctx** out, const ebc_config* cfg, int device) {
     ebc_destroy(c);
     return EBC_ERR_CUDA;
   }
-  if (set_kernel_attributes() != cudaSuccess) {
+  if (set_kernel_attributes() != cudaSuccess || set_decoder_attributes() != cudaSuccess) {
     ebc_destroy(c);
     return EBC_ERR_CUDA;
   }
@@ -489,16 +489,26 @@ static int decompress_any(ebc_ctx* c, const void* d_in, uint64_t in_bytes, const
     sh.t_off = t_off;
   }
   if (cudaSetDevice(c->device) != cudaSuccess) return EBC_ERR_CUDA;
-  size_t need = 0;
+  size_t need = 0, acc = 0;
   carve_decompress(nullptr, sh, c->glob, &need);
   int rc = grow(&c->dbuf, &c->dbuf_bytes, need);
   if (rc) return rc;
-  const Work w = carve_decompress(c->dbuf, sh, c->glob, &need);
+  const Work w = carve_decompress(c->dbuf, sh, c->glob, &need, &acc);
   cudaStream_t st = (cudaStream_t)stream;
   c->last_stream = st;
   c->depoch = (c->depoch + 1) & 0xFFFFFFu;
-  return cuda_err(launch_decompress((const uint8_t*)d_in, in_bytes, (const unsigned long long*)d_offsets, sh, w,
-                                    d_xhat, c->depoch, st, c->prof));
+  // The decoder's accumulators are left zero by every call.  A call whose
+  // accumulators span other bytes than the last call's (where a windowed call's
+  // row-source table may have been written since) clears them first.
+  if (c->dclean_buf != c->dbuf || c->dclean_bytes != acc) {
+    if (cudaMemsetAsync(c->dbuf, 0, acc, st) != cudaSuccess) return EBC_ERR_CUDA;
+    c->dclean_buf = c->dbuf;
+    c->dclean_bytes = acc;
+  }
+  const cudaError_t e = launch_decompress((const uint8_t*)d_in, in_bytes, (const unsigned long long*)d_offsets, sh,
+                                          w, d_xhat, c->depoch, st, c->prof);
+  if (e != cudaSuccess) c->dclean_buf = nullptr;   // the accumulators may be left dirty
+  return cuda_err(e);
 }
 
 int ebc_decompress(ebc_ctx* c, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B, int T, int D,
@@ -912,6 +922,7 @@ int noalloc_setup(int dev, NoAllocDevice** out) {
         cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return EBC_ERR_NO_DEVICE;
     if (!(major == 10 && minor == 3)) return EBC_ERR_NO_DEVICE;
+    if (set_decoder_attributes() != cudaSuccess) return EBC_ERR_CUDA;
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return EBC_ERR_CUDA;
     d.scratch = static_cast<unsigned char*>(p);
@@ -936,15 +947,16 @@ int ebc_decompress_noalloc(const void* d_in, uint64_t in_bytes, float* d_xhat, i
   int rc = noalloc_setup(dev, &nd);
   if (rc) return rc;
   const Shape sh = make_shape(B, T, D, nd->nsm);
-  size_t need = 0;
+  size_t need = 0, acc = 0;
   carve_decompress(nullptr, sh, nullptr, &need);
   if (need > kNoAllocScratchBytes - kNoAllocGlobBytes) return EBC_ERR_SCRATCH_LIMIT;
   Glob* g = reinterpret_cast<Glob*>(nd->scratch);
-  const Work w = carve_decompress(nd->scratch + kNoAllocGlobBytes, sh, g, &need);
+  const Work w = carve_decompress(nd->scratch + kNoAllocGlobBytes, sh, g, &need, &acc);
   cudaStream_t st = (cudaStream_t)stream;
-  // The array keeps whatever the previous call left; only the status block
-  // must start at zero (the tables are written before they are read).
-  if (cudaMemsetAsync(g, 0, sizeof(Glob), st) != cudaSuccess) return EBC_ERR_CUDA;
+  // The array keeps whatever the previous call left; the status block and the
+  // decoder's count accumulators must start at zero (everything else is
+  // written before it is read).
+  if (cudaMemsetAsync(g, 0, kNoAllocGlobBytes + acc, st) != cudaSuccess) return EBC_ERR_CUDA;
   if (launch_decompress((const uint8_t*)d_in, in_bytes, nullptr, sh, w, d_xhat, 1u, st, nullptr) != cudaSuccess)
     return EBC_ERR_CUDA;
   unsigned int code = 0;

@@ -5,20 +5,29 @@
 // §III-D (Huffman and vector-based LZ decoding, dequantization) and §III-E
 // ("parallel decompression" of chunks; one or several containers, one per
 // batch slice, decoded in the same pass).  The unit is a table of one
-// container.  Three launches:
-//   k_dec_prep     every CTA checks every header and layout; the first U CTAs
-//                  build each unit's canonical decode tables (2^11-entry
-//                  first-level table + long codes); the others, one warp per
-//                  segment, check the segment records against each other and
-//                  write one descriptor per chunk (start bit, length, rows)
-//   k_dec_chunks   one thread per chunk, one CTA per run of 64 chunks (listed
-//                  in a run map written by k_dec_prep): decodes its literal
-//                  rows (codes, inline outliers) from shared-memory copies of
-//                  the bitstream and writes them straight to the output
-//   k_dec_matches  copies each matched row from its (literal) reference
+// container.  Two launches, no pass over the container before them:
+//   k_dec_lit    one CTA per group of consecutive segments of one unit.  The
+//                sections it reads first sit at offsets that follow from the
+//                shape, so the header, the unit's code lengths, the group's
+//                segment records and match bitmap are all loaded at once (the
+//                header check confirms those offsets), then the chunk lengths
+//                and the group's bitstream (staged in shared memory when it
+//                fits).  The CTA builds the unit's canonical decode tables,
+//                the literal rows and chunk start bits of its segments, and
+//                its warps decode 32 chunks at a time (one per lane; codes,
+//                inline outliers), 32 values per lane into a shared-memory
+//                slot, stored by the warp with coalesced 16-byte stores.  The
+//                last CTA of a unit checks the unit's counts against its table
+//                record (and resolves the reference chains of a windowed
+//                container); the last unit of a container checks the
+//                container's outlier count.
+//   k_dec_match  persistent warps take the batch's 32-row bitmap words in turn
+//                and copy each matched row from its reference row (the literal
+//                it names, or the literal root of its chain).
 // Every read of the container is bounds-checked; a failed check records
 // EBC_ERR_CORRUPT and stops the remaining work without out-of-bounds access.
 #include <cstdint>
+#include <type_traits>
 
 #include "ebc_internal.cuh"
 
@@ -54,7 +63,6 @@ struct Layout {
   unsigned long long row0, n;       // the batch rows it restores: [row0, row0 + n)
   unsigned int window, ref_bytes;   // dedup window (0 = whole batch) and bytes per reference
   unsigned int nseg, nw;            // segments and bitmap words per table
-  unsigned int chunk0, match0;      // chunks and matches of the containers before it
 };
 
 // Header checks of a container of n rows and `bytes` bytes (h: its first
@@ -102,6 +110,50 @@ __device__ int parse_header(const uint8_t* h, unsigned long long bytes, unsigned
   return EBC_OK;
 }
 
+// Container r of the input: its bounds checked, then its header.
+__device__ int container_layout(const uint8_t* in, unsigned long long in_bytes, const unsigned long long* offs,
+                                const Shape& sh, int r, Layout* L) {
+  const unsigned long long lo = offs ? offs[r] : 0ull, hi = offs ? offs[r + 1] : in_bytes;
+  if ((lo & 15ull) != 0ull || lo > hi || hi > in_bytes) return EBC_ERR_CORRUPT;
+  uint4 hdr[kHeaderBytes / 16];   // the header, by independent 16-byte loads
+  if (hi - lo >= kHeaderBytes) {
+#pragma unroll
+    for (int k = 0; k < (int)(kHeaderBytes / 16); ++k) hdr[k] = reinterpret_cast<const uint4*>(in + lo)[k];
+  }
+  const int code = parse_header(reinterpret_cast<const uint8_t*>(hdr), hi - lo,
+                                (unsigned long long)slice_rows(sh, r), sh, L);
+  L->base = lo;
+  L->row0 = (unsigned long long)slice_row0(sh, r);
+  return code;
+}
+
+// Every container's header (also those without units), one window for all of
+// them; writes the call's totals to the status block.  Run once per call (by
+// one thread); kept out of line so that its header copies do not raise the
+// register count of the decoder's hot loop.  code: the caller's own check so
+// far.  first: if not null, receives container 0's layout.
+__device__ __noinline__ int check_all_headers(const uint8_t* in, unsigned long long in_bytes,
+                                              const unsigned long long* offs, const Shape& sh, Glob* g, int code,
+                                              Layout* first) {
+  unsigned long long tot[6] = {0, 0, 0, 0, 0, 0};
+  uint32_t win0 = 0;
+  for (int c = 0; c < sh.R && code == EBC_OK; ++c) {
+    Layout Lc{};
+    code = container_layout(in, in_bytes, offs, sh, c, &Lc);
+    if (c == 0) win0 = Lc.window;
+    else if (code == EBC_OK && Lc.window != win0) code = EBC_ERR_CORRUPT;
+    tot[0] += Lc.n_lit; tot[1] += Lc.n_match; tot[2] += Lc.n_out; tot[3] += Lc.n_chunks;
+    tot[4] += Lc.total; tot[5] += Lc.words;
+    if (c == 0 && first) *first = Lc;
+  }
+  if (code == EBC_OK) {
+    g->n_lit = tot[0]; g->n_match = tot[1]; g->n_out = tot[2]; g->n_chunks = tot[3]; g->total = tot[4];
+    g->words = tot[5];
+    g->window = win0;
+  }
+  return code;
+}
+
 // Exclusive scan of v across one warp.
 __device__ __forceinline__ uint32_t warp_excl(uint32_t v, uint32_t* total) {
   const int lane = threadIdx.x & 31;
@@ -115,615 +167,747 @@ __device__ __forceinline__ uint32_t warp_excl(uint32_t v, uint32_t* total) {
   return inc - v;
 }
 
-// ---------------------------------------------------------------------------
-// k_dec_prep: grid U + ceil(U * nseg / 8), 256 threads.  Every CTA checks all
-// R headers (thread r: container r) and takes the chunk and match bases of
-// each container from a scan of their counts; a failed check stops every CTA.
-// ---------------------------------------------------------------------------
-template <int D, int W>
-__global__ void __launch_bounds__(256) k_dec_prep(const uint8_t* __restrict__ in, unsigned long long in_bytes,
-                                                   const unsigned long long* __restrict__ offs, Shape sh, Work w,
-                                                   uint32_t epoch) {
-  pdl_enter();
-  using G = Geo<D>;
-  constexpr int kA = Alph<W>::kA, kPer = kA / 256;
-  __shared__ Layout s_L[8];   // the containers of this CTA's units: r_lo .. r_lo + 7
-  __shared__ uint32_t s_nc[kMaxSlices + 1], s_nm[kMaxSlices + 1], s_win[kMaxSlices];
-  __shared__ unsigned long long s_tot[4];   // literals, outliers, words, bytes of all containers
-  __shared__ int s_code;
-  __shared__ uint8_t s_len[kA];
-  __shared__ uint32_t s_wcnt[8 * (kLmax + 1)], s_run[kLmax + 1];   // canonical ranks
-  __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_offset[kLmax + 2];
-  __shared__ int s_bad;
-  __shared__ uint32_t s_c0, s_c1;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int T = sh.T;
-  const int U = sh.U;
-  const int nsegT = U * sh.nseg;
-  Glob* g = w.glob;
-  // the containers this CTA needs
-  int r_lo;
-  if ((int)blockIdx.x < U) {
-    r_lo = (int)blockIdx.x / T;
-  } else {
-    const int seg0 = ((int)blockIdx.x - U) * 8;
-    r_lo = seg0 < nsegT ? (seg0 / sh.nseg) / T : 0;
-  }
-  if (tid == 0) {
-    s_code = EBC_OK;
-    s_bad = 0;
-  }
-  if (tid < 4) s_tot[tid] = 0ull;
-  __syncthreads();
-  Layout L{};
-  int code = EBC_OK;
-  if (tid < sh.R) {
-    const unsigned long long lo = offs ? offs[tid] : 0ull, hi = offs ? offs[tid + 1] : in_bytes;
-    if ((lo & 15ull) != 0ull || lo > hi || hi > in_bytes) {
-      code = EBC_ERR_CORRUPT;
-    } else {
-      uint4 hdr[kHeaderBytes / 16];   // the header, by independent 16-byte loads
-      if (hi - lo >= kHeaderBytes) {
+// Canonical ranks over a CTA of kNT threads: thread tid holds the code lengths
+// of symbols k * kNT + tid (k < kPer); rank[k] is the number of symbols of the
+// same length with a smaller index (in its warp from a match mask, in the
+// warps and rounds before from counts).  s_wcnt: (kNT / 32) x (kLmax + 1)
+// words, s_run: kLmax + 1 words of shared scratch.
+template <int kPer, int kNT>
+__device__ void ranks_by_length(const uint32_t (&len)[kPer], uint32_t (&rank)[kPer], uint32_t* s_wcnt,
+                                uint32_t* s_run) {
+  constexpr int kL = kLmax + 1, kNW = kNT / 32;
+  const int tid = threadIdx.x, lane = tid & 31, wp = tid >> 5;
+  if (tid < kL) s_run[tid] = 0u;
 #pragma unroll
-        for (int k = 0; k < (int)(kHeaderBytes / 16); ++k) hdr[k] = reinterpret_cast<const uint4*>(in + lo)[k];
-      }
-      code = parse_header(reinterpret_cast<const uint8_t*>(hdr), hi - lo, (unsigned long long)slice_rows(sh, tid),
-                          sh, &L);
-      L.base = lo;
-      L.row0 = (unsigned long long)slice_row0(sh, tid);
-    }
-    // counts for the scan (zero for a container that failed: its check stops the decode)
-    s_nc[tid] = code == EBC_OK ? (uint32_t)L.n_chunks : 0u;
-    s_nm[tid] = code == EBC_OK ? (uint32_t)L.n_match : 0u;
-    s_win[tid] = code == EBC_OK ? L.window : 0u;
-    if (code != EBC_OK) {
-      atomicCAS(&s_code, EBC_OK, code);
-    } else if (blockIdx.x == 0) {
-      atomicAdd(&s_tot[0], L.n_lit);
-      atomicAdd(&s_tot[1], L.n_out);
-      atomicAdd(&s_tot[2], L.words);
-      atomicAdd(&s_tot[3], L.total);
-    }
-  }
-  __syncthreads();
-  if (tid == 0) {   // chunk and match bases of the containers; one window for all of them
-    uint32_t c = 0, m = 0;
-    for (int r = 0; r < sh.R; ++r) {
-      const uint32_t a = s_nc[r], b = s_nm[r];
-      s_nc[r] = c;
-      s_nm[r] = m;
-      c += a;
-      m += b;
-      if (s_win[r] != s_win[0] && s_code == EBC_OK) s_code = EBC_ERR_CORRUPT;
-    }
-    s_nc[sh.R] = c;
-    s_nm[sh.R] = m;
-  }
-  __syncthreads();
-  if (tid < sh.R && code == EBC_OK) {
-    L.chunk0 = s_nc[tid];
-    L.match0 = s_nm[tid];
-    if (tid >= r_lo && tid < r_lo + 8) s_L[tid - r_lo] = L;
-  }
-  __syncthreads();
-  if (blockIdx.x == 0 && tid == 0) {
-    if (s_code != EBC_OK) {
-      dec_fail(g, epoch, s_code);
-    } else {
-      g->n_match = s_nm[sh.R];
-      g->n_chunks = s_nc[sh.R];
-      g->window = s_win[0];
-      g->n_lit = s_tot[0];
-      g->n_out = s_tot[1];
-      g->words = s_tot[2];
-      g->total = s_tot[3];
-    }
-  }
-  if (s_code != EBC_OK) return;
-
-  if ((int)blockIdx.x < U) {
-    // ---- decode tables of unit u = (slice r, table t) ----
-    const int u = blockIdx.x;
-    const int t = u % T;
-    const Layout Lc = s_L[0];
-    const uint8_t* cin = in + Lc.base;
-    const uint8_t* rec = cin + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
-    uint32_t lens[kPer];
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      lens[k] = rec[16 + k * 256 + tid];
-      s_len[k * 256 + tid] = (uint8_t)lens[k];
-    }
-    if (tid < kLmax + 2) s_count[tid] = 0;
+  for (int k = 0; k < kPer; ++k) {
+    for (int i = tid; i < kNW * kL; i += kNT) s_wcnt[i] = 0u;
     __syncthreads();
-#pragma unroll
-    for (int k = 0; k < kPer; ++k) {
-      if (lens[k] > (uint32_t)kLmax) s_bad = 1;
-      else if (lens[k]) atomicAdd(&s_count[lens[k]], 1u);
-    }
+    const unsigned same = __match_any_sync(0xffffffffu, len[k]);
+    if (lane == __ffs(same) - 1) s_wcnt[wp * kL + len[k]] = (uint32_t)__popc(same);
     __syncthreads();
-    if (tid == 0) {
-      const float eb = __uint_as_float(ld32(rec));
-      unsigned long long kraft = 0;
-      for (int l = 1; l <= kLmax; ++l) kraft += (unsigned long long)s_count[l] << (kLmax - l);
-      if (kraft > (1ull << kLmax) || !eb_usable(eb)) s_bad = 1;
-      uint32_t c = 0, off = 0;
-      s_count[0] = 0;
-      for (int l = 1; l <= kLmax; ++l) {
-        c = (c + s_count[l - 1]) << 1;
-        s_next[l] = c;
-        s_offset[l] = off;
-        off += s_count[l];
-      }
-      DecTab* dt = w.dtab + u;
-      dt->ebx2 = __fmul_rn(2.0f, eb);
-      // the unit's chunk range (segment records are checked against each other by the segment warps)
-      const uint32_t* srec = reinterpret_cast<const uint32_t*>(cin + Lc.off_seg);
-      uint32_t c0 = 0, c1 = 0;
-      if (Lc.nseg > 0) {
-        c0 = srec[4ull * ((unsigned long long)t * Lc.nseg) + 1];
-        c1 = t + 1 < T ? srec[4ull * ((unsigned long long)(t + 1) * Lc.nseg) + 1] : (uint32_t)Lc.n_chunks;
-      }
-      if (c0 > c1 || c1 > Lc.n_chunks) s_bad = 1;
-      c0 += Lc.chunk0;   // over all containers
-      c1 += Lc.chunk0;
-      if (c1 > dec_max_chunks(sh)) s_bad = 1;
-      dt->chunk0 = c0;
-      dt->chunk1 = c1;
-      dt->t = (uint32_t)t;
-      dt->bits_off = Lc.base + Lc.off_bits;
-      dt->n_words = Lc.words;
-      dt->row0 = Lc.row0;
-      s_c0 = c0;
-      s_c1 = c1;
-      for (int l = 0; l <= kLmax; ++l) {
-        dt->first[l] = l ? s_next[l] : 0u;
-        dt->count[l] = l ? s_count[l] : 0u;
-        dt->offset[l] = l ? s_offset[l] : 0u;
-      }
-    }
+    uint32_t r = s_run[len[k]] + (uint32_t)__popc(same & ((1u << lane) - 1u));
+    for (int j = 0; j < wp; ++j) r += s_wcnt[j * kL + len[k]];
+    rank[k] = r;
     __syncthreads();
-    if (s_bad) {
-      if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
-      return;
+    if (tid < kL) {
+      uint32_t add = 0;
+      for (int j = 0; j < kNW; ++j) add += s_wcnt[j * kL + tid];
+      s_run[tid] += add;
     }
-    {   // this unit's run slots [c0 / kDecRun + u, c1 / kDecRun + u + 1): its runs, then one empty slot at most
-      const uint32_t c0 = s_c0, c1 = s_c1;
-      const uint32_t lo = c0 / kDecRun + (uint32_t)u, hi = c1 / kDecRun + (uint32_t)u + 1u;
-      const uint32_t nruns = (c1 - c0 + kDecRun - 1) / kDecRun;
-      for (uint32_t r = lo + tid; r < hi; r += 256) {
-        const uint32_t k = r - lo;
-        const uint32_t j0 = c0 + k * kDecRun;
-        w.runmap[r] = k < nruns ? make_uint4((uint32_t)u, j0, min(j0 + (uint32_t)kDecRun, c1), 0u)
-                                : make_uint4(~0u, 0u, 0u, 0u);
-      }
-    }
-    uint16_t* lut = w.lut + (size_t)u * (1u << kLutBits);
-    for (int i = tid; i < (1 << kLutBits); i += 256) lut[i] = 0;
-    __syncthreads();
-    {
-      // each symbol's rank among the symbols of its length below it: its index in sorted[] is
-      // offset[len] + rank, its code first[len] + rank
-      uint32_t rk[kPer];
-      canonical_ranks<kPer>(lens, rk, s_wcnt, s_run);
-#pragma unroll
-      for (int k = 0; k < kPer; ++k) {
-        const uint32_t len = lens[k], sy = (uint32_t)(k * 256 + tid);
-        if (!len) continue;
-        const uint32_t code = s_next[len] + rk[k];
-        w.dtab[u].sorted[s_offset[len] + rk[k]] = (uint16_t)sy;
-        if (len <= (uint32_t)kLutBits) {
-          const uint32_t lo = code << (kLutBits - len), n = 1u << (kLutBits - len);
-          for (uint32_t i = 0; i < n; ++i) lut[lo + i] = (uint16_t)(sy | (len << Alph<W>::kLenShift));
-        }
-      }
-    }
-    if (Lc.window && Lc.nseg > 0) {
-      // window references: every row's source (itself for a literal, b - distance for a match),
-      // from the unit's bitmap and one-byte distances, then the chains resolved to their
-      // literal roots (pointer jumping, CTA barriers between rounds)
-      const int64_t n = (int64_t)Lc.n, row0 = (int64_t)Lc.row0;
-      const int64_t nw = Lc.nw;
-      const uint32_t* bmt = reinterpret_cast<const uint32_t*>(cin + Lc.off_bitmap) + (size_t)t * nw;
-      const uint8_t* dist = cin + Lc.off_refs;
-      const uint32_t* srec = reinterpret_cast<const uint32_t*>(cin + Lc.off_seg);
-      const unsigned long long mbase = srec[4ull * ((unsigned long long)t * Lc.nseg) + 2];
-      uint32_t* src = w.srcrow + (size_t)t * sh.B + row0;
-      unsigned long long carry = 0;
-      for (int64_t base = 0; base < nw; base += 256) {
-        const int64_t wi = base + tid;
-        const uint32_t bm = wi < nw ? __ldcg(&bmt[wi]) : 0u;
-        // matches before this word: a CTA-wide exclusive scan of the words' counts
-        uint32_t wt;
-        const uint32_t in_warp = warp_excl((uint32_t)__popc(bm), &wt);
-        if (lane == 0) s_count[warp] = wt;
-        __syncthreads();
-        uint32_t before = 0, all = 0;
-        for (int k = 0; k < 8; ++k) {
-          if (k < warp) before += s_count[k];
-          all += s_count[k];
-        }
-        __syncthreads();
-        const unsigned long long rank0 = mbase + carry + before + in_warp;
-        if (wi < nw) {
-          for (int j = 0; j < 32; ++j) {
-            const int64_t b = wi * 32 + j;   // row of the slice
-            if (b >= n) break;
-            uint32_t from = (uint32_t)(row0 + b);
-            if ((bm >> j) & 1u) {
-              const unsigned long long k = rank0 + __popc(bm & ((1u << j) - 1u));
-              const uint32_t d = k < Lc.n_match ? dist[k] : 0u;
-              if (d == 0u || d > Lc.window || (int64_t)d > b) s_bad = 1;
-              else from = (uint32_t)(row0 + b - d);
-            }
-            src[b] = from;
-          }
-        }
-        carry += all;
-      }
-      __syncthreads();
-      if (s_bad) {
-        if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
-        return;
-      }
-      int rounds = 1;
-      while ((1ll << rounds) < n) ++rounds;
-      for (int rd = 0; rd <= rounds; ++rd) {
-        for (int64_t b = tid; b < n; b += 256) {
-          const uint32_t s = src[b];
-          if (s != (uint32_t)(row0 + b)) {
-            const uint32_t s2 = src[s - row0];   // one step further (a literal points at itself)
-            if (s2 != s) src[b] = s2;
-          }
-        }
-        __syncthreads();
-      }
-    }
-    return;
-  }
-
-  // ---- one warp per segment: literal rows and chunk descriptors ----
-  const int seg = ((int)blockIdx.x - U) * 8 + warp;
-  if (seg >= nsegT) return;
-  const int u = seg / sh.nseg;
-  const int s = seg - u * sh.nseg;
-  const int r = u / T;
-  const int t = u - r * T;
-  const Layout Lc = s_L[r - r_lo];
-  if (s >= (int)Lc.nseg) return;   // past the end of a shorter slice
-  const uint8_t* cin = in + Lc.base;
-  const int64_t B = (int64_t)Lc.n;                // rows of the slice
-  const int64_t row0 = (int64_t)s * G::kSB;      // within the slice
-  const int64_t nw = Lc.nw;
-  const unsigned long long ri = (unsigned long long)t * Lc.nseg + s;   // record of the segment
-  const uint32_t* rec = reinterpret_cast<const uint32_t*>(cin + Lc.off_seg) + 4ull * ri;
-  const uint32_t word_off = rec[0], chunk_base = rec[1], match_base = rec[2], nbits = rec[3];
-  unsigned long long nx_word, nx_chunk, nx_match;
-  if (ri + 1 < (unsigned long long)T * Lc.nseg) {
-    nx_word = rec[4];
-    nx_chunk = rec[5];
-    nx_match = rec[6];
-  } else {
-    nx_word = Lc.words;
-    nx_chunk = Lc.n_chunks;
-    nx_match = Lc.n_match;
-  }
-  const uint32_t* bmt = reinterpret_cast<const uint32_t*>(cin + Lc.off_bitmap) + (size_t)t * nw;
-  // literal rows, in row order: words 0..31 on the lanes, then words 32..63
-  uint32_t nlit = 0, nvalid_rows = 0;
-  uint16_t* litrow = w.litrow + (size_t)seg * G::kSB;
-#pragma unroll
-  for (int half = 0; half < 2; ++half) {
-    const int wi = half * 32 + lane;
-    uint32_t litw = 0, valid = 0;
-    if (wi < G::kBmWords) {
-      const int64_t gw = (int64_t)s * G::kBmWords + wi;
-      if (gw < nw) {
-        const int64_t nv = B - (row0 + (int64_t)wi * 32);
-        valid = nv >= 32 ? 0xffffffffu : ((1u << nv) - 1u);
-        const uint32_t bm = bmt[gw];
-        if (bm & ~valid) s_bad = 1;             // match bits past the slice
-        litw = ~bm & valid;
-      }
-    }
-    uint32_t tot;
-    uint32_t k = nlit + warp_excl(__popc(litw), &tot);
-    uint32_t vt;
-    warp_excl(__popc(valid), &vt);
-    nlit += tot;
-    nvalid_rows += vt;
-    for (uint32_t m = litw; m; m &= m - 1) litrow[k++] = (uint16_t)(wi * 32 + __ffs(m) - 1);
-  }
-  const uint32_t nmatch = nvalid_rows - nlit;
-  const uint32_t nchunks = (nlit + G::kKC - 1) / G::kKC;
-  const unsigned long long seg_words = ((nbits + 127ull) >> 7) * 4ull;
-  bool ok = (unsigned long long)chunk_base + nchunks == nx_chunk && nx_chunk <= Lc.n_chunks &&
-            (unsigned long long)match_base + nmatch == nx_match && nx_match <= Lc.n_match &&
-            (unsigned long long)word_off + seg_words == nx_word && nx_word <= Lc.words &&
-            (ri != 0 || (word_off == 0 && chunk_base == 0 && match_base == 0));
-  // chunk start bits
-  uint32_t cstart = 0;
-  if (ok) {
-    const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + Lc.off_chunks) + chunk_base;
-    uint32_t acc = 0;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const uint32_t c = half * 32 + lane;
-      const uint32_t len = c < nchunks ? (uint32_t)cl[c] : 0u;
-      uint32_t tot;
-      const uint32_t st = acc + warp_excl(len, &tot);
-      if (c < nchunks) {
-        const unsigned long long start = (unsigned long long)word_off * 32ull + st;
-        const uint32_t rows = min((uint32_t)G::kKC, nlit - c * G::kKC);
-        w.cdesc[Lc.chunk0 + chunk_base + c] = make_uint4((uint32_t)start, (uint32_t)(start >> 32) | (len << 16),
-                                                         (uint32_t)seg, (c * G::kKC) | (rows << 16));
-      }
-      acc += tot;
-    }
-    cstart = acc;
-    ok = cstart == nbits;
-  }
-  // matched rows: {destination, source} row pairs of the batch, in (unit, row) order
-  if (__all_sync(0xffffffffu, ok)) {
-    const uint8_t* refs = cin + Lc.off_refs;
-    const int64_t brow0 = (int64_t)Lc.row0;
-    uint32_t mbase = match_base;
-#pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      const int wi = half * 32 + lane;
-      uint32_t mw = 0;
-      if (wi < G::kBmWords) {
-        const int64_t gw = (int64_t)s * G::kBmWords + wi;
-        if (gw < nw) mw = bmt[gw];
-      }
-      uint32_t tot;
-      uint32_t k = mbase + warp_excl(__popc(mw), &tot);
-      for (uint32_t m = mw; m; m &= m - 1) {
-        const int64_t b = row0 + wi * 32 + __ffs(m) - 1;   // row of the slice
-        uint32_t ref;
-        if (Lc.window) {   // a distance back, within the window; the row there may itself be a match
-          const uint32_t dist = refs[k];
-          if (dist == 0u || dist > Lc.window || (int64_t)dist > b) {
-            ok = false;
-            break;
-          }
-          ref = (uint32_t)(b - dist);
-        } else {           // whole slice: the first occurrence, always a literal
-          ref = Lc.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[k]
-                                  : reinterpret_cast<const uint32_t*>(refs)[k];
-          if ((int64_t)ref >= b || ((bmt[ref >> 5] >> (ref & 31)) & 1u)) {
-            ok = false;
-            break;
-          }
-        }
-        w.mdesc[Lc.match0 + k] = make_uint2((uint32_t)((brow0 + b) * sh.T_out + sh.t_off + t),
-                                            (uint32_t)((brow0 + ref) * sh.T_out + sh.t_off + t));
-        ++k;
-      }
-      mbase += tot;
-    }
-  }
-  if (!__all_sync(0xffffffffu, ok) || s_bad) {
-    if (lane == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
+    __syncthreads();   // the counts are read before the next round clears them
   }
 }
 
-// ---------------------------------------------------------------------------
-// k_dec_chunks: one thread per chunk, one CTA per run of kDecRun consecutive
-// chunks of one table (the run map lists the runs first, so every CTA with
-// work precedes the empty ones).  The run's chunks are consecutive in the
-// bitstream: the CTA copies their words into shared memory with coalesced
-// loads (when they fit), together with the table's decode tables and the 256
-// reconstruction values.  Each thread then decodes its chunk with the
-// first-level table (long codes by the canonical first-code search), reads the
-// 32 raw bits after each outlier code, and writes each literal row with
-// 16-byte stores.
-// ---------------------------------------------------------------------------
+// Geometry of the literal decoder.  A CTA takes kSPC consecutive segments of
+// one unit (at least 320 rows) and decodes their chunks, a warp taking 32 of
+// them at a time (one per lane).  A lane decodes its chunk in pieces of kPiece
+// values (a row, or 32 values -- one 128-byte line -- of a longer row) into its
+// own shared-memory slot; the warp then stores the 32 pieces with coalesced
+// 16-byte stores.  Within a slot, float4 k of lane i sits at k ^ (i mod
+// kPieceQ), so that neither the decoding writes nor the storing reads conflict
+// on shared-memory banks.
 template <int D>
-struct DecStage {
-  static constexpr int kWords = D <= 128 ? 4096 : 8192;   // 16 / 32 KiB of bitstream per CTA
+struct DGeo {
+  static constexpr int kSB = Geo<D>::kSB;
+  static constexpr int kKC = Geo<D>::kKC;
+  static constexpr int kSPC = 320 / kSB < 1 ? 1 : 320 / kSB;         // segments per CTA
+  static constexpr int kRows = kSPC * kSB;                            // rows per CTA
+  static constexpr int kMaxChunks = kRows / kKC;                      // chunks per CTA at most
+  static constexpr int kThreads = 128;
+  static constexpr int kWarps = kThreads / 32;
+  static constexpr int kPiece = D < 32 ? D : 32;                      // values per piece
+  static constexpr int kPieceQ = kPiece / 4;                          // float4 per piece
+  static constexpr int kPiecesPerRow = D / kPiece;
+  static constexpr int kBmWords = kSB / 32;                           // bitmap words per segment
+  static constexpr int kSegChunks = kSB / kKC;                        // chunks per segment at most
+  static constexpr int kSlotQ = kWarps * 32 * kPieceQ;                // float4 of the warps' slots
+  static constexpr int kWarpWords = 768;                              // bitstream words staged per warp
 };
 
-// Decodes one chunk (rows literal rows of D codes) starting at bit `start`;
-// ldw(i) returns word i of the bitstream.  Returns the number of bits read.
-template <int D, int W, class LoadWord>
-__device__ __forceinline__ unsigned long long decode_chunk(LoadWord ldw, unsigned long long start,
-                                                           const uint16_t* s_lut, const float* s_val,
-                                                           const uint32_t* s_first, const uint32_t* s_count,
-                                                           const uint32_t* s_offset, const uint16_t* s_sorted,
-                                                           const uint16_t* lrow, uint32_t rows, int64_t row0, int T,
-                                                           int t, float* __restrict__ xhat, bool* bad) {
-  // bit window: the next stream bits are w0:w1 from bit `pos` of w0 (pos < 32); w0 is word wp - 2
-  unsigned long long wp = start >> 5;
-  uint32_t pos = (uint32_t)(start & 31ull);
-  uint32_t w0 = ldw(wp), w1 = ldw(wp + 1);
-  wp += 2;
-  for (uint32_t k = 0; k < rows; ++k) {
-    const int64_t b = row0 + lrow[k];
-    float4* dst = reinterpret_cast<float4*>(xhat + ((size_t)b * T + t) * D);
-#pragma unroll 2
-    for (int q4 = 0; q4 < D / 4; ++q4) {
-      float o[4];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint32_t peek = __funnelshift_l(w1, w0, pos);   // the next 32 bits
-        const uint32_t e = s_lut[peek >> (32 - kLutBits)];
-        uint32_t len = e >> Alph<W>::kLenShift, sym = e & ((1u << Alph<W>::kLenShift) - 1u);
-        if (len == 0u) {   // a code longer than the first-level table
-          for (int l = kLutBits + 1; l <= kLmax; ++l) {
-            const uint32_t code = peek >> (32 - l);
-            if (code - s_first[l] < s_count[l]) {
-              sym = s_sorted[s_offset[l] + code - s_first[l]];
-              len = (uint32_t)l;
-              break;
-            }
-          }
-          if (len == 0u) {
-            *bad = true;
-            len = 1;
-          }
-        }
-        pos += len;
-        if (pos >= 32u) {
-          pos -= 32u;
-          w0 = w1;
-          w1 = ldw(wp++);
-        }
-        o[q] = s_val[sym];
-        if (sym == 0u) {   // outlier: the next 32 bits are the raw value
-          o[q] = __uint_as_float(__funnelshift_l(w1, w0, pos));
-          w0 = w1;
-          w1 = ldw(wp++);
-        }
-      }
-      dst[q4] = make_float4(o[0], o[1], o[2], o[3]);
+// The code of the next symbol in the bit window w0:w1 from bit pos, through
+// the first-level table (entries sym | len << kLenShift; the symbol field is 0
+// for the outlier symbol and for codes longer than the table, the slow cases)
+// and, for a long code, the canonical first-code search.  Returns the symbol;
+// *len receives the code length (1 and *bad = true for a bit pattern that is
+// no code).
+template <int W>
+__device__ __noinline__ uint32_t long_code(uint32_t peek, const uint32_t* s_first, const uint32_t* s_count,
+                                              const uint32_t* s_offset, const uint16_t* s_sorted, uint32_t* len,
+                                              bool* bad) {
+#pragma unroll 1
+  for (int l = kLutBits + 1; l <= kLmax; ++l) {
+    const uint32_t code = peek >> (32 - l);
+    if (code - s_first[l] < s_count[l]) {
+      *len = (uint32_t)l;
+      return s_sorted[s_offset[l] + code - s_first[l]];
     }
   }
-  return (wp - 2ull) * 32ull + pos - start;
+  *bad = true;
+  *len = 1u;
+  return 1u;
 }
 
-template <int D, int W>
-__global__ void __launch_bounds__(kDecRun) k_dec_chunks(const uint8_t* __restrict__ in, Shape sh, Work w,
-                                                         float* __restrict__ xhat, uint32_t epoch) {
+// ---------------------------------------------------------------------------
+// k_dec_tables: grid U (at least 1), 128 threads.  Checks every container's
+// header (CTA 0: all of them, and one window for all; each CTA: its unit's),
+// and builds each unit's canonical decode tables once, from the code lengths of
+// its table record (lengths at most 24, a Kraft sum of at most 1, a usable
+// bound): the 2^11-entry first-level table (sym | len << shift; symbol field 0
+// for the outlier symbol and for the prefixes of longer codes), the first code,
+// count and sorted-table offset of each length, the symbols in canonical
+// order, and the reconstruction value of each symbol.  The decode CTAs copy
+// them into shared memory.
+// ---------------------------------------------------------------------------
+template <int W>
+__global__ void __launch_bounds__(128) k_dec_tables(const uint8_t* __restrict__ in, unsigned long long in_bytes,
+                                                    const unsigned long long* __restrict__ offs, Shape sh, Work w,
+                                                    uint32_t epoch) {
   pdl_enter();
-  using G = Geo<D>;
-  constexpr int kA = Alph<W>::kA;
-  constexpr int kStage = DecStage<D>::kWords;
+  constexpr int kA = Alph<W>::kA, kNT = 128, kPer = kA / kNT;
+  constexpr int kLenShift = Alph<W>::kLenShift;
   __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
-  __shared__ __align__(16) uint32_t s_words[kStage + 1];
-  __shared__ float s_val[kA];
+  __shared__ uint32_t s_len[kA / 4];
   __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
-  __shared__ uint16_t s_sorted[kA];
-  __shared__ unsigned long long s_lo, s_hi;
-  __shared__ int s_abort;
+  __shared__ uint32_t s_wcnt[(kNT / 32) * (kLmax + 1)], s_run[kLmax + 1];
+  __shared__ uint32_t s_rec[4];
+  __shared__ int s_code;
   Glob* g = w.glob;
-  const int tid = threadIdx.x;
-  const unsigned int slot = blockIdx.x;   // run slot of this CTA
-  // the run, and whether the decode was aborted (then the run map may be
-  // stale): one decision for the whole CTA, taken before the run is used
-  if (tid == 0) s_abort = dec_aborted(g, epoch);
-  const unsigned long long nslots = __ldcg(&g->n_chunks) / kDecRun + (unsigned long long)sh.U;
-  uint4 run = make_uint4(~0u, 0u, 0u, 0u);
-  if (slot < nslots) run = __ldcg(&w.runmap[slot]);
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int u = blockIdx.x;
+  const bool have_unit = u < sh.U;
+  const int T = sh.T;
+  const int r = have_unit ? u / T : 0, t = have_unit ? u - r * T : 0;
+  // one round of loads: the record (eb and code lengths) at the offset the shape gives (skipped outside
+  // the container; its header then fails the check), and the header
+  const unsigned long long lo = offs ? offs[r] : 0ull, hi = offs ? offs[r + 1] : in_bytes;
+  const unsigned long long size = (lo & 15ull) == 0ull && lo <= hi && hi <= in_bytes ? hi - lo : 0ull;
+  const uint8_t* rec = in + lo + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
+  const bool rec_in = have_unit && kHeaderBytes + (unsigned long long)(t + 1) * Alph<W>::kRecBytes <= size;
+  if (tid < 4) s_rec[tid] = rec_in ? ld32(rec + 4 * tid) : 0u;
+  for (int i = tid; i < kA / 4; i += kNT) s_len[i] = rec_in ? ld32(rec + 16 + 4 * i) : 0u;
+  for (int i = tid; i < (1 << kLutBits) / 8; i += kNT) reinterpret_cast<uint4*>(s_lut)[i] = make_uint4(0, 0, 0, 0);
+  if (tid <= kLmax) s_count[tid] = 0u;
+  if (tid == 0) {
+    // CTA 0 checks the containers in order and reports the first failure (the code the in-order
+    // decode of the containers meets first); a CTA whose own container fails stops silently
+    if (blockIdx.x == 0) {
+      const int all = check_all_headers(in, in_bytes, offs, sh, g, EBC_OK, nullptr);
+      if (all != EBC_OK) dec_fail(g, epoch, all);
+    }
+    Layout L{};
+    s_code = have_unit ? container_layout(in, in_bytes, offs, sh, r, &L) : EBC_OK;
+  }
   __syncthreads();
-  if (s_abort || run.x == ~0u) return;
-  if (run.x >= (uint32_t)sh.U || run.y >= run.z || run.z > dec_max_chunks(sh)) {
-    if (tid == 0) dec_fail(g, epoch, EBC_ERR_INTERNAL);
+  if (s_code != EBC_OK || !have_unit) return;
+  bool bad = false;
+  for (int i = tid; i < kA; i += kNT) {
+    const uint32_t len = (s_len[i >> 2] >> (8 * (i & 3))) & 0xffu;
+    if (len > (uint32_t)kLmax) bad = true;
+    else if (len) atomicAdd(&s_count[len], 1u);
+  }
+  if (bad) s_code = EBC_ERR_CORRUPT;
+  __syncthreads();
+  if (tid < 32) {
+    // lane l (1..24): the Kraft term of length l, the first canonical code of length l
+    // (sum over k < l of count[k] << (l - k)), and its offset in sorted[] (the counts below l)
+    const int l = lane;
+    const uint32_t cnt = l >= 1 && l <= kLmax ? s_count[l] : 0u;
+    unsigned long long kraft = l >= 1 && l <= kLmax ? (unsigned long long)cnt << (kLmax - l) : 0ull;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) kraft += __shfl_xor_sync(0xffffffffu, kraft, off);
+    unsigned long long first = 0;
+    uint32_t below = 0;
+    for (int k = 1; k < l && k <= kLmax; ++k) {
+      first += (unsigned long long)s_count[k] << (l - k);
+      below += s_count[k];
+    }
+    if (l <= kLmax) {
+      s_first[l] = l ? (uint32_t)first : 0u;
+      s_offset[l] = l ? below : 0u;
+    }
+    if (lane == 0 && (kraft > (1ull << kLmax) || !eb_usable(__uint_as_float(s_rec[0])))) s_code = EBC_ERR_CORRUPT;
+  }
+  __syncthreads();
+  if (s_code != EBC_OK) {
+    if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
     return;
   }
-  const int u = (int)run.x;   // unit: slice u / T, table u % T
-  const unsigned long long j = (unsigned long long)run.y + tid;
-  const bool mine = j < run.z;
-  const DecTab* dt = w.dtab + u;
-  uint4 dsc = make_uint4(0, 0, 0, 0);
-  if (mine) dsc = __ldcg(&w.cdesc[j]);
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(w.lut + (size_t)u * (1u << kLutBits));
-    uint4* dst = reinterpret_cast<uint4*>(s_lut);
+  DTab* dt = w.dtab + u;
+  const float ebx2 = __fmul_rn(2.0f, __uint_as_float(s_rec[0]));
+  for (int i = tid; i < kA; i += kNT) dt->val[i] = __fmul_rn((float)(i - Alph<W>::kR), ebx2);
+  if (tid <= kLmax) {
+    dt->first[tid] = s_first[tid];
+    dt->count[tid] = tid ? s_count[tid] : 0u;
+    dt->offset[tid] = s_offset[tid];
+  }
+  // each symbol's rank among the symbols of its length below it: its index in sorted[] is
+  // offset[len] + rank, its code first[len] + rank
+  uint32_t lens[kPer], rk[kPer];
 #pragma unroll
-    for (int i = tid; i < (1 << kLutBits) / 8; i += kDecRun) dst[i] = __ldcg(src + i);
+  for (int k = 0; k < kPer; ++k) {
+    const int i = k * kNT + tid;
+    lens[k] = (s_len[i >> 2] >> (8 * (i & 3))) & 0xffu;
+  }
+  ranks_by_length<kPer, kNT>(lens, rk, s_wcnt, s_run);
+#pragma unroll
+  for (int k = 0; k < kPer; ++k) {
+    const uint32_t len = lens[k], i = (uint32_t)(k * kNT + tid);
+    if (!len) continue;
+    dt->sorted[s_offset[len] + rk[k]] = (uint16_t)i;
+    if (len <= (uint32_t)kLutBits) {
+      const uint32_t code = s_first[len] + rk[k];
+      const uint32_t l0 = code << (kLutBits - len), n = 1u << (kLutBits - len);
+      const uint16_t e = (uint16_t)(i | (len << kLenShift));
+      for (uint32_t q = 0; q < n; ++q) s_lut[l0 + q] = e;
+    }
+  }
+  __syncthreads();
+  for (int i = tid; i < (1 << kLutBits) / 8; i += kNT)
+    reinterpret_cast<uint4*>(dt->lut)[i] = reinterpret_cast<const uint4*>(s_lut)[i];
+}
+
+// ---------------------------------------------------------------------------
+// k_dec_lit: grid U * G (G groups of kSPC segments per unit), 128 threads.
+// ---------------------------------------------------------------------------
+template <int D, int W>
+__global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ in, unsigned long long in_bytes,
+                                                    const unsigned long long* __restrict__ offs, Shape sh, Work w,
+                                                    float* __restrict__ xhat, uint32_t epoch) {
+  pdl_enter();
+  using G = DGeo<D>;
+  constexpr int kA = Alph<W>::kA, kNT = G::kThreads;
+  constexpr int kLenShift = Alph<W>::kLenShift;
+  constexpr uint32_t kSymMask = (1u << kLenShift) - 1u;
+  __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
+  __shared__ float s_val[kA];
+  __shared__ uint16_t s_sorted[kA];
+  __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
+  __shared__ uint32_t s_recs[(G::kSPC + 1) * 4];      // the group's segment records and the one after
+  __shared__ uint32_t s_bm[G::kSPC * G::kBmWords];    // the group's match bitmap words
+  __shared__ uint16_t s_clen[G::kMaxChunks];          // the group's chunk lengths
+  __shared__ uint32_t s_cbit[G::kMaxChunks];          // chunk start bit, from the group's first word
+  __shared__ uint32_t s_cinfo[G::kMaxChunks];         // segment in group << 24 | rows << 16 | first rank
+  __shared__ uint16_t s_litrow[G::kRows];             // by segment in group, literal rank: row of the segment
+  __shared__ __align__(16) float4 s_slot[G::kSlotQ];  // the warps' slots: [kWarps][32 * kPieceQ]
+  __shared__ __align__(16) uint32_t s_ws[G::kWarps][G::kWarpWords];   // each warp's batch of bitstream words
+  __shared__ uint32_t s_grp[4];                       // chunks, first chunk, first word, words of the group
+  __shared__ Layout s_L;
+  __shared__ int s_code, s_last;
+  __shared__ uint32_t s_cnt[3];                       // literals, matches, outliers of the CTA
+  __shared__ uint32_t s_next;                         // next batch of 32 chunks
+  __shared__ uint32_t s_rec[4];                       // the unit's table record head: eb, lit, match, out
+  Glob* g = w.glob;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int T = sh.T;
+  const int ngrp = div_up(sh.nseg, G::kSPC) > 0 ? div_up(sh.nseg, G::kSPC) : 1;
+  const int u = (int)blockIdx.x / ngrp;               // unit: slice u / T, table u % T
+  const int grp = (int)blockIdx.x - u * ngrp;
+  const bool have_unit = u < sh.U;
+  const int r = have_unit ? u / T : 0;
+  const int t = have_unit ? u - r * T : 0;
+
+  // ---- one round of loads: header, code lengths, segment records, bitmap words, at the offsets the
+  //      shape gives (loads outside the container are skipped; its header then fails the check) ----
+  const unsigned long long lo = offs ? offs[r] : 0ull, hi = offs ? offs[r + 1] : in_bytes;
+  const bool span = (lo & 15ull) == 0ull && lo <= hi && hi <= in_bytes;
+  const unsigned long long size = span ? hi - lo : 0ull;
+  const uint8_t* cin = in + lo;
+  const int64_t nr = slice_rows(sh, r);
+  const unsigned int nseg_r = (unsigned int)div_up(nr, G::kSB), nw_r = (unsigned int)div_up(nr, 32);
+  const unsigned long long off_seg = kHeaderBytes + (unsigned long long)T * table_rec_bytes(sh.A);
+  const unsigned long long off_bm = off_seg + (unsigned long long)T * nseg_r * kSegRecBytes;
+  const int s0 = grp * G::kSPC;                                             // first segment of the group
+  const int nsg = have_unit ? max(0, min(G::kSPC, (int)nseg_r - s0)) : 0;   // its segments in this slice
+  const unsigned long long rec0 = (unsigned long long)t * nseg_r + s0;       // record of its first segment
+  const bool rec_end = rec0 + nsg == (unsigned long long)T * nseg_r;         // its last is the container's last
+  if (have_unit) {
+    const uint8_t* rec = cin + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
+    const bool rec_in = kHeaderBytes + (unsigned long long)(t + 1) * Alph<W>::kRecBytes <= size;
+    if (tid < 4) s_rec[tid] = rec_in ? ld32(rec + 4 * tid) : 0u;
+    // the unit's decode tables (built by k_dec_tables; used only if its checks passed)
+    const DTab* dt = w.dtab + u;
+    for (int i = tid; i < (1 << kLutBits) / 8; i += kNT)
+      reinterpret_cast<uint4*>(s_lut)[i] = __ldcg(reinterpret_cast<const uint4*>(dt->lut) + i);
+    for (int i = tid; i < kA; i += kNT) {
+      s_val[i] = __ldcg(&dt->val[i]);
+      s_sorted[i] = dt->sorted[i];
+    }
     if (tid <= kLmax) {
       s_first[tid] = __ldcg(&dt->first[tid]);
       s_count[tid] = __ldcg(&dt->count[tid]);
       s_offset[tid] = __ldcg(&dt->offset[tid]);
     }
-    const float ebx2 = __ldcg(&dt->ebx2);
-#pragma unroll
-    for (int i = tid; i < kA; i += kDecRun) {
-      s_sorted[i] = dt->sorted[i];
-      s_val[i] = __fmul_rn((float)(i - Alph<W>::kR), ebx2);
+    const int nrw = 4 * (nsg + (rec_end ? 0 : 1));
+    for (int i = tid; i < nrw; i += kNT) {
+      const unsigned long long o = off_seg + rec0 * kSegRecBytes + 4ull * i;
+      s_recs[i] = o + 4 <= size ? ld32(cin + o) : 0u;
+    }
+    for (int i = tid; i < nsg * G::kBmWords; i += kNT) {
+      const unsigned long long wi = (unsigned long long)s0 * G::kBmWords + i;   // word of the unit's bitmap
+      const unsigned long long o = off_bm + 4ull * ((unsigned long long)t * nw_r + wi);
+      s_bm[i] = wi < nw_r && o + 4 <= size ? ld32(cin + o) : 0u;
     }
   }
-  // the bitstream of the unit's container
-  const unsigned long long n_words = __ldcg(&dt->n_words), off_bits = __ldcg(&dt->bits_off);
-  const int t = (int)__ldcg(&dt->t);
-  const int64_t slice0 = (int64_t)__ldcg(&dt->row0);
-  const uint32_t* words = reinterpret_cast<const uint32_t*>(in + off_bits);
-  const unsigned long long start = (unsigned long long)dsc.x | ((unsigned long long)(dsc.y & 0xffffu) << 32);
-  const uint32_t clen = dsc.y >> 16;
-  const unsigned long long wlim = (start + clen + 31ull) >> 5;   // words the chunk may read: [start/32, wlim)
-  if (tid == 0) s_lo = start >> 5;
-  if (j + 1 == run.z) s_hi = wlim;
-  __syncthreads();
-  // the run's words, if they fit (chunk ranges are consecutive by construction;
-  // a thread whose range lies outside the staged one reads global memory)
-  const unsigned long long lo = s_lo, hi = s_hi;
-  const bool staged = hi >= lo && hi - lo <= (unsigned long long)kStage && hi <= n_words;
-  if (staged) {
-    for (unsigned long long i = lo + tid; i < hi; i += kDecRun) s_words[i - lo] = __ldg(words + i);
-    if (tid == 0) s_words[hi - lo] = 0u;   // read past the run's end: a zero word
+  if (tid == 0) {
+    Layout L{};
+    // the headers and tables were checked by k_dec_tables: after a failure there (already recorded,
+    // code -1) the CTA only takes part in the unit's counters
+    int code = dec_aborted(g, epoch) ? -1 : EBC_OK;
+    if (have_unit && code == EBC_OK) code = container_layout(in, in_bytes, offs, sh, r, &L);
+    s_L = L;
+    s_code = code;
+    s_cnt[0] = s_cnt[1] = s_cnt[2] = 0u;
+    s_next = (uint32_t)G::kWarps * 32u;
+    if (tid == 0 && code == EBC_OK && have_unit) {
+      // the group's chunk and word ranges, from its first record and the one after its last
+      const uint32_t cb0 = nsg > 0 ? s_recs[1] : 0u, wb0 = nsg > 0 ? s_recs[0] : 0u;
+      const unsigned long long cb1 = nsg == 0 ? cb0 : (rec_end ? L.n_chunks : s_recs[4 * nsg + 1]);
+      const unsigned long long wb1 = nsg == 0 ? wb0 : (rec_end ? L.words : s_recs[4 * nsg]);
+      // (chunks hold literal rows, at least one bit per code: a group with chunks has words)
+      if (cb1 < cb0 || cb1 > L.n_chunks || cb1 - cb0 > (unsigned long long)G::kMaxChunks || wb1 < wb0 ||
+          wb1 > L.words || (wb0 & 3u) || (wb1 & 3ull) || (cb1 > cb0 && wb1 == wb0)) {
+        s_code = EBC_ERR_CORRUPT;
+      } else {
+        s_grp[0] = (uint32_t)(cb1 - cb0);
+        s_grp[1] = cb0;
+        s_grp[2] = wb0;
+        s_grp[3] = (uint32_t)(wb1 - wb0);
+      }
+    }
   }
   __syncthreads();
-  if (!mine) return;
-  const int seg = (int)dsc.z;
-  const uint32_t first = dsc.w & 0xffffu, rows = dsc.w >> 16;
-  if (seg / sh.nseg != u || rows == 0u || first + rows > (uint32_t)G::kSB || start + clen > n_words * 32ull) {
-    dec_fail(g, epoch, EBC_ERR_CORRUPT);
-    return;
+  const Layout& L = s_L;   // read from shared memory where used
+  bool ok = s_code == EBC_OK && have_unit;
+
+  // ---- second round: the chunk lengths ----
+  if (ok) {
+    const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + L.off_chunks) + s_grp[1];
+    for (uint32_t i = tid; i < s_grp[0]; i += kNT) s_clen[i] = cl[i];
+    __syncthreads();
   }
-  const int s = seg - u * sh.nseg;
-  const uint16_t* lrow = w.litrow + (size_t)seg * G::kSB + first;
-  const int64_t row0 = slice0 + (int64_t)s * G::kSB;   // batch row of the segment's first row
+
+  // ---- the group's segments: literal rows, chunk start bits, chain checks (a warp per segment) ----
+  uint32_t nchunks = 0;
+  if (ok) {
+    const uint32_t cb0 = s_grp[1], wb0 = s_grp[2], ngc = s_grp[0];
+    bool bad = false;
+    for (int j = warp; j < nsg; j += G::kWarps) {
+      const int s = s0 + j;
+      const unsigned long long ri = rec0 + j;   // record of the segment
+      const uint32_t* rc = s_recs + 4 * j;
+      const uint32_t word_off = rc[0], chunk_base = rc[1], match_base = rc[2], nbits = rc[3];
+      const bool last = j == nsg - 1 && rec_end;
+      const unsigned long long nx_word = last ? L.words : rc[4], nx_chunk = last ? L.n_chunks : rc[5],
+                               nx_match = last ? L.n_match : rc[6];
+      const int64_t row0 = (int64_t)s * G::kSB;   // within the slice
+      // literal rows in row order, two bitmap words per lane at most
+      uint32_t nlit = 0, nvalid = 0;
+#pragma unroll
+      for (int half = 0; half < (G::kBmWords + 31) / 32; ++half) {
+        const int wi = half * 32 + lane;
+        uint32_t litw = 0, valid = 0;
+        if (wi < G::kBmWords) {
+          const int64_t nv = nr - (row0 + (int64_t)wi * 32);
+          valid = nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+          if (nv > 0) {
+            const uint32_t bm = s_bm[j * G::kBmWords + wi];
+            if (bm & ~valid) bad = true;   // match bits past the slice
+            litw = ~bm & valid;
+          }
+        }
+        uint32_t tot, vt;
+        uint32_t k = nlit + warp_excl(__popc(litw), &tot);
+        warp_excl(__popc(valid), &vt);
+        nlit += tot;
+        nvalid += vt;
+        for (uint32_t m = litw; m; m &= m - 1) s_litrow[j * G::kSB + k++] = (uint16_t)(wi * 32 + __ffs(m) - 1);
+      }
+      const uint32_t nmatch = nvalid - nlit;
+      const uint32_t nch = (nlit + G::kKC - 1) / G::kKC;
+      const unsigned long long seg_words = ((nbits + 127ull) >> 7) * 4ull;
+      const uint32_t cl0 = chunk_base - cb0;
+      bool good = (unsigned long long)chunk_base + nch == nx_chunk && nx_chunk <= L.n_chunks &&
+                  (unsigned long long)match_base + nmatch == nx_match && nx_match <= L.n_match &&
+                  (unsigned long long)word_off + seg_words == nx_word && nx_word <= L.words &&
+                  (ri != 0 || (word_off == 0 && chunk_base == 0 && match_base == 0)) && chunk_base >= cb0 &&
+                  cl0 + nch <= ngc && word_off >= wb0;
+      if (__all_sync(0xffffffffu, good)) {   // chunk start bits: the segment's first bit + the lengths before
+        const uint32_t bit0 = (word_off - wb0) * 32u;   // the segment's first bit in the group's range
+        uint32_t acc = 0;
+#pragma unroll
+        for (int half = 0; half < (G::kSegChunks + 31) / 32; ++half) {
+          const uint32_t c = half * 32 + lane;
+          const uint32_t len = c < nch ? (uint32_t)s_clen[cl0 + c] : 0u;
+          uint32_t tot;
+          const uint32_t st = acc + warp_excl(len, &tot);
+          if (c < nch) {
+            s_cbit[cl0 + c] = bit0 + st;
+            s_cinfo[cl0 + c] = ((uint32_t)j << 24) | (min((uint32_t)G::kKC, nlit - c * G::kKC) << 16) |
+                               (c * G::kKC);
+          }
+          acc += tot;
+        }
+        good = acc == nbits;
+        if (lane == 0) {
+          atomicAdd(&s_cnt[0], nlit);
+          atomicAdd(&s_cnt[1], nmatch);
+        }
+      }
+      if (!__all_sync(0xffffffffu, good)) bad = true;
+    }
+    if (bad) s_code = EBC_ERR_CORRUPT;
+    __syncthreads();
+    ok = s_code == EBC_OK;
+    nchunks = ok ? s_grp[0] : 0u;
+  }
+
+  // ---- decode: a warp takes 32 chunks at a time, a piece per lane into its slot, then stores them ----
+  // Four symbols at a time on a branch-free path that assumes ordinary codes (first-level table,
+  // symbol field not 0); when one of the four was an outlier or a longer code, the four are decoded
+  // again from the same bit position by the general path.
+  uint32_t nout = 0;
   bool bad = false;
-  unsigned long long used;
-  if (staged && (start >> 5) >= lo && wlim <= hi) {
-    // reads past the chunk's end see the following chunks' words, then zeros:
-    // they never change a code that lies inside the chunk
-    const uint32_t* sw = s_words - lo;
-    used = decode_chunk<D, W>([&](unsigned long long i) -> uint32_t { return sw[i < hi ? i : hi]; }, start, s_lut,
-                           s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T_out, sh.t_off + t,
-                           xhat, &bad);
-  } else {
-    used = decode_chunk<D, W>([&](unsigned long long i) -> uint32_t { return i < wlim ? __ldg(words + i) : 0u; },
-                           start, s_lut, s_val, s_first, s_count, s_offset, s_sorted, lrow, rows, row0, sh.T_out,
-                           sh.t_off + t, xhat, &bad);
+  if (ok) {
+    const uint32_t gwords = s_grp[3];   // > 0 whenever there are chunks
+    const uint32_t* gw = reinterpret_cast<const uint32_t*>(cin + L.off_bits) + s_grp[2];   // the group's words
+    const int64_t brow0 = (int64_t)L.row0;
+    float4* slot = s_slot + warp * 32 * G::kPieceQ;
+    uint32_t* ws = s_ws[warp];
+    for (uint32_t b0 = (uint32_t)warp * 32u; b0 < nchunks;) {
+      // the batch's words (its chunks are consecutive, so their bits are too): staged in this warp's
+      // buffer with coalesced 16-byte loads when they fit, else read from global memory
+      const uint32_t clast = min(b0 + 31u, nchunks - 1u);
+      const uint32_t wlo = (s_cbit[b0] >> 5) & ~3u;
+      const uint32_t whi = min(((s_cbit[clast] + s_clen[clast]) >> 5) + 3u, gwords);   // exclusive; the window
+                                                                                         // reads 2 words ahead
+      const bool staged = whi - wlo <= (uint32_t)G::kWarpWords;
+      if (staged) {
+        const uint32_t n4 = (whi - wlo + 3u) >> 2;   // within the group's words (a multiple of 4)
+        const uint4* src = reinterpret_cast<const uint4*>(gw + wlo);
+        for (uint32_t i = lane; i < n4; i += 32) reinterpret_cast<uint4*>(ws)[i] = __ldg(src + i);
+        __syncwarp();
+      }
+      const uint32_t nst = whi - wlo;   // staged words (reads past them repeat the last)
+      auto run = [&](auto staged_tag) {
+        constexpr bool kStaged = decltype(staged_tag)::value;
+        auto word = [&](uint32_t i) -> uint32_t {
+          if constexpr (kStaged) return ws[min(i - wlo, nst - 1u)];
+          else return __ldg(gw + min(i, gwords - 1u));
+        };
+        const uint32_t c = b0 + lane;
+        const bool mine = c < nchunks;
+        const uint32_t info = mine ? s_cinfo[c] : 0u;
+        const uint32_t start = mine ? s_cbit[c] : s_cbit[b0];
+        const uint32_t clen = mine ? (uint32_t)s_clen[c] : 0u;
+        const int j = (int)(info >> 24);
+        const uint32_t rows = (info >> 16) & 0xffu, first = info & 0xffffu;
+        const uint32_t npieces = rows * G::kPiecesPerRow;
+        // bit buffer: the next nb bits, left-aligned in buf; wp is the next word to read (reads past the
+        // group's words repeat its last word; they never decide a code of a valid chunk)
+        const uint32_t wp0 = start >> 5, sbit = start & 31u;
+        uint32_t wp = wp0 + 2u, nb = 64u - sbit;
+        unsigned long long buf = (((unsigned long long)word(wp0) << 32) | word(wp0 + 1u)) << sbit;
+        auto refill = [&]() {   // nb <= 32 before: one more word
+          buf |= (unsigned long long)word(wp) << (32u - nb);
+          ++wp;
+          nb += 32u;
+        };
+        float* rowdst = nullptr;
+        const uint32_t allp = __reduce_max_sync(0xffffffffu, npieces);
+        for (uint32_t p = 0; p < allp; ++p) {
+          const bool act = p < npieces;
+          if (act) {
+            const uint32_t rk = p / G::kPiecesPerRow, pc = p % G::kPiecesPerRow;
+            if (pc == 0) {
+              const int64_t b = brow0 + (int64_t)(s0 + j) * G::kSB + s_litrow[j * G::kSB + first + rk];
+              rowdst = xhat + ((size_t)b * sh.T_out + sh.t_off + t) * D;
+            }
+#pragma unroll 1
+            for (int q4 = 0; q4 < G::kPieceQ; ++q4) {
+              const unsigned long long buf0 = buf;
+              const uint32_t nb0 = nb, wq = wp;
+              float o[4];
+              uint32_t plain = 1u;   // all four are first-table codes of ordinary symbols
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if ((q & 1) == 0 && nb < 22u) refill();   // two first-table codes take at most 22 bits
+                const uint32_t e = s_lut[(uint32_t)(buf >> (64 - kLutBits))];
+                const uint32_t sym = e & kSymMask;
+                plain = sym ? plain : 0u;
+                o[q] = s_val[sym];
+                buf <<= e >> kLenShift;
+                nb -= e >> kLenShift;
+              }
+              if (!plain) {   // an outlier or a longer code among the four: decode them again, in general
+                buf = buf0;
+                nb = nb0;
+                wp = wq;
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                  if (nb <= 32u) refill();   // at least 33 bits: any code fits
+                  const uint32_t peek = (uint32_t)(buf >> 32);
+                  const uint32_t e = s_lut[peek >> (32 - kLutBits)];
+                  uint32_t sym = e & kSymMask, len = e >> kLenShift;
+                  if (sym == 0u && len == 0u)
+                    sym = long_code<W>(peek, s_first, s_count, s_offset, s_sorted, &len, &bad);
+                  buf <<= len;
+                  nb -= len;
+                  float v = s_val[sym];
+                  if (sym == 0u) {   // outlier: the next 32 bits are the raw value
+                    if (nb <= 32u) refill();
+                    v = __uint_as_float((uint32_t)(buf >> 32));
+                    buf <<= 32;
+                    nb -= 32u;
+                    ++nout;
+                  }
+                  o[q] = v;
+                }
+              }
+              slot[lane * G::kPieceQ + (q4 ^ (lane & (G::kPieceQ - 1)))] = make_float4(o[0], o[1], o[2], o[3]);
+            }
+          }
+          __syncwarp();
+          // the warp's pieces: float4 i of the step goes to piece i / kPieceQ (lane), float4 i % kPieceQ
+          const unsigned long long pdst =
+              act ? (unsigned long long)(rowdst + (p % G::kPiecesPerRow) * G::kPiece) : 0ull;
+#pragma unroll
+          for (int k = 0; k < G::kPieceQ; ++k) {
+            const int i = k * 32 + lane;
+            const int owner = i / G::kPieceQ, q = i % G::kPieceQ;
+            const unsigned long long d = __shfl_sync(0xffffffffu, pdst, owner);
+            if (d) __stcs(reinterpret_cast<float4*>(d) + q, slot[owner * G::kPieceQ + (q ^ (owner & (G::kPieceQ - 1)))]);
+          }
+          __syncwarp();
+        }
+        if (mine && (wp - wp0) * 32u - nb - sbit != clen) bad = true;
+      };
+      if (staged) run(std::integral_constant<bool, true>{});
+      else run(std::integral_constant<bool, false>{});
+      __syncwarp();   // the staged words are read before the next batch overwrites them
+      // the next batch of 32 chunks of the group
+      uint32_t nb = 0;
+      if (lane == 0) nb = atomicAdd(&s_next, 32u);
+      b0 = __shfl_sync(0xffffffffu, nb, 0);
+    }
   }
-  if (bad || used != clen) dec_fail(g, epoch, EBC_ERR_CORRUPT);
+  if (bad) s_code = EBC_ERR_CORRUPT;   // (benign race: any writer stores the same value)
+  nout = __reduce_add_sync(0xffffffffu, nout);
+  if (lane == 0 && nout) atomicAdd(&s_cnt[2], nout);
+  __syncthreads();
+  if (have_unit && s_code > 0 && tid == 0) dec_fail(g, epoch, s_code);
+
+  // ---- the unit's last CTA: its counts against the table record ----
+  if (!have_unit) return;
+  if (tid == 0) {
+    uint4* acc = w.uacc + u;
+    if (s_cnt[0]) atomicAdd(&acc->x, s_cnt[0]);
+    if (s_cnt[1]) atomicAdd(&acc->y, s_cnt[1]);
+    if (s_cnt[2]) atomicAdd(&acc->z, s_cnt[2]);
+    __threadfence();
+    s_last = atomicAdd(&acc->w, 1u) == (unsigned)ngrp - 1u;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  const bool checked = !dec_aborted(g, epoch);   // the counts mean something only if nothing failed
+  __shared__ uint32_t s_unit[3];
+  if (tid == 0) {
+    uint4* acc = w.uacc + u;
+    s_unit[0] = atomicExch(&acc->x, 0u);
+    s_unit[1] = atomicExch(&acc->y, 0u);
+    s_unit[2] = atomicExch(&acc->z, 0u);
+    atomicExch(&acc->w, 0u);   // clean for the next call
+  }
+  __syncthreads();
+  int fail = EBC_OK;
+  if (checked && s_code == EBC_OK) {
+    const uint8_t* rec = cin + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
+    if (ld32(rec + 4) != s_unit[0] || ld32(rec + 8) != s_unit[1] || ld32(rec + 12) != s_unit[2])
+      fail = EBC_ERR_CORRUPT;
+  }
+  if (checked && s_code == EBC_OK && L.window && L.nseg > 0 && fail == EBC_OK) {
+    // window references: every row's source (itself for a literal, b - distance for a match),
+    // from the unit's bitmap and one-byte distances, then the chains resolved to their literal
+    // roots (pointer jumping, CTA barriers between rounds)
+    __shared__ uint32_t s_wc[kNT / 32];
+    __shared__ int s_wbad;
+    if (tid == 0) s_wbad = 0;
+    const int64_t n = (int64_t)L.n, row0 = (int64_t)L.row0;
+    const int64_t nw = L.nw;
+    const uint32_t* bmt = reinterpret_cast<const uint32_t*>(cin + L.off_bitmap) + (size_t)t * nw;
+    const uint8_t* dist = cin + L.off_refs;
+    const uint32_t* srec = reinterpret_cast<const uint32_t*>(cin + L.off_seg);
+    const unsigned long long mbase = srec[4ull * ((unsigned long long)t * L.nseg) + 2];
+    uint32_t* src = w.srcrow + (size_t)t * sh.B + row0;
+    unsigned long long carry = 0;
+    __syncthreads();
+    for (int64_t base = 0; base < nw; base += kNT) {
+      const int64_t wi = base + tid;
+      const uint32_t bm = wi < nw ? __ldcg(&bmt[wi]) : 0u;
+      uint32_t wt;
+      const uint32_t in_warp = warp_excl((uint32_t)__popc(bm), &wt);
+      if (lane == 0) s_wc[warp] = wt;
+      __syncthreads();
+      uint32_t before = 0, all = 0;
+      for (int k = 0; k < kNT / 32; ++k) {
+        if (k < warp) before += s_wc[k];
+        all += s_wc[k];
+      }
+      __syncthreads();
+      const unsigned long long rank0 = mbase + carry + before + in_warp;
+      if (wi < nw) {
+        for (int jj = 0; jj < 32; ++jj) {
+          const int64_t b = wi * 32 + jj;   // row of the slice
+          if (b >= n) break;
+          uint32_t from = (uint32_t)(row0 + b);
+          if ((bm >> jj) & 1u) {
+            const unsigned long long k = rank0 + __popc(bm & ((1u << jj) - 1u));
+            const uint32_t d = k < L.n_match ? dist[k] : 0u;
+            if (d == 0u || d > L.window || (int64_t)d > b) s_wbad = 1;
+            else from = (uint32_t)(row0 + b - d);
+          }
+          src[b] = from;
+        }
+      }
+      carry += all;
+    }
+    __syncthreads();
+    if (s_wbad) {
+      fail = EBC_ERR_CORRUPT;
+    } else {
+      int rounds = 1;
+      while ((1ll << rounds) < n) ++rounds;
+      for (int rd = 0; rd <= rounds; ++rd) {
+        for (int64_t b = tid; b < n; b += kNT) {
+          const uint32_t sv = src[b];
+          if (sv != (uint32_t)(row0 + b)) {
+            const uint32_t s2 = src[sv - row0];   // one step further (a literal points at itself)
+            if (s2 != sv) src[b] = s2;
+          }
+        }
+        __syncthreads();
+      }
+    }
+  }
+  if (tid == 0) {
+    if (fail != EBC_OK) dec_fail(g, epoch, fail);
+    // the container's outliers: the last of its T units compares their sum with the header
+    uint2* cacc = w.cacc + r;
+    atomicAdd(&cacc->x, s_unit[2]);
+    __threadfence();
+    if (atomicAdd(&cacc->y, 1u) == (unsigned)T - 1u) {
+      __threadfence();
+      const uint32_t total_out = atomicExch(&cacc->x, 0u);
+      atomicExch(&cacc->y, 0u);
+      if (checked && s_code == EBC_OK && fail == EBC_OK && !dec_aborted(g, epoch) &&
+          (unsigned long long)total_out != L.n_out)
+        dec_fail(g, epoch, EBC_ERR_CORRUPT);
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
-// k_dec_matches: each matched row copies its reference row: the literal the
-// reference names (whole batch), or the literal root of its chain (window;
-// resolved by k_dec_prep's table CTAs).  Grid-stride over (matched row,
-// 16-byte column) pairs, four copies in flight per thread.
+// k_dec_match: persistent warps over the bitmap words of all units (32 rows
+// each): every matched row of the word copies its reference row -- the literal
+// the reference names (whole batch; checked to precede the row and to be a
+// literal), or the literal root of its chain (window; resolved by k_dec_lit).
+// A lane copies 16 bytes of a row, kUnroll rows' worth in flight.
 // ---------------------------------------------------------------------------
+constexpr int kMatchThreads = 256;
+struct MLay {                    // what the match copy needs of a container
+  unsigned long long base, off_bm, off_refs, off_seg, row0;
+  unsigned int n, nseg, nw, ref_bytes, window;
+};
 template <int D>
-__global__ void __launch_bounds__(256) k_dec_matches(Shape sh, Work w, float* __restrict__ xhat, uint32_t epoch) {
+__global__ void __launch_bounds__(kMatchThreads, 4) k_dec_match(const uint8_t* __restrict__ in,
+                                                               unsigned long long in_bytes,
+                                                               const unsigned long long* __restrict__ offs, Shape sh,
+                                                               Work w, float* __restrict__ xhat, uint32_t epoch) {
   pdl_enter();
+  using G = DGeo<D>;
+  constexpr int kQ = D / 4;                         // float4 per row
+  constexpr int kUnroll = 4;                        // float4 per lane in flight
+  constexpr int kNW = kMatchThreads / 32;
+  __shared__ MLay s_lay[kMaxSlices];
+  __shared__ uint32_t s_dst[kNW][32], s_src[kNW][32];
+  __shared__ int s_abort;
   Glob* g = w.glob;
-  if (dec_aborted(g, epoch)) return;
-  constexpr int kQ = D / 4;
-  const unsigned long long n4 = __ldcg(&g->n_match) * (unsigned long long)kQ;
-  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
-  const unsigned long long i_start = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x;
-  if (__ldcg(&g->window) != 0u) {   // source = the chain's literal root
-    const uint32_t To = (uint32_t)sh.T_out;   // output rows hold T_out tables; ours start at column t_off
-    for (unsigned long long i = i_start; i < n4; i += stride) {
-      const uint2 m = __ldcg(&w.mdesc[i / kQ]);
-      const unsigned long long q = i % kQ;
-      const uint32_t b = m.x / To, col = m.x - b * To;
-      const uint32_t from = __ldcg(&w.srcrow[(size_t)(col - (uint32_t)sh.t_off) * sh.B + b]) * To + col;
-      __stcs(reinterpret_cast<float4*>(xhat + (size_t)m.x * D + 4 * q),
-             *reinterpret_cast<const float4*>(xhat + (size_t)from * D + 4 * q));
-    }
-    return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (tid == 0) s_abort = dec_aborted(g, epoch);
+  for (int c = tid; c < sh.R; c += kMatchThreads) {   // the containers' layouts (checked by k_dec_lit)
+    Layout Lc{};
+    if (container_layout(in, in_bytes, offs, sh, c, &Lc) != EBC_OK) s_abort = 1;
+    s_lay[c] = MLay{Lc.base, Lc.off_bitmap, Lc.off_refs, Lc.off_seg, Lc.row0, (unsigned int)Lc.n, Lc.nseg, Lc.nw,
+                    Lc.ref_bytes, Lc.window};
   }
-  for (unsigned long long i0 = i_start; i0 < n4; i0 += 4 * stride) {
-    float4 v[4];
-    unsigned long long dst[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const unsigned long long i = i0 + k * stride;
-      if (i < n4) {
-        const uint2 m = __ldcg(&w.mdesc[i / kQ]);
-        const unsigned long long q = i % kQ;
-        v[k] = *reinterpret_cast<const float4*>(xhat + (size_t)m.y * D + 4 * q);
-        dst[k] = (size_t)m.x * D + 4 * q;
+  __syncthreads();
+  if (s_abort) return;
+  const int T = sh.T;
+  const unsigned long long nbatch = (unsigned long long)sh.U * sh.nw;   // bitmap words of all units
+  const unsigned long long wstep = (unsigned long long)gridDim.x * kNW;
+  for (unsigned long long k = (unsigned long long)blockIdx.x * kNW + warp; k < nbatch; k += wstep) {
+    const int u = (int)(k / sh.nw);
+    const unsigned int wi = (unsigned int)(k - (unsigned long long)u * sh.nw);
+    const int r = u / T, t = u - r * T;
+    const MLay& Lc = s_lay[r];
+    if (wi >= Lc.nw) continue;
+    const uint8_t* cin = in + Lc.base;
+    const uint32_t* bmt = reinterpret_cast<const uint32_t*>(cin + Lc.off_bm) + (size_t)t * Lc.nw;
+    const uint32_t bm = bmt[wi];
+    if (bm == 0u) continue;
+    // the rank of the word's first match: the segment's match base + the matches of its earlier words
+    const unsigned int s = wi / G::kBmWords, wfirst = s * G::kBmWords;
+    uint32_t before = 0;
+    for (unsigned int i = wfirst + lane; i < wi; i += 32) before += __popc(bmt[i]);
+    before = __reduce_add_sync(0xffffffffu, before);
+    const uint32_t mbase =
+        reinterpret_cast<const uint32_t*>(cin + Lc.off_seg)[4ull * ((unsigned long long)t * Lc.nseg + s) + 2];
+    const int64_t b = (int64_t)wi * 32 + lane;   // row of the slice
+    const bool m = (bm >> lane) & 1u;
+    const uint32_t at = __popc(bm & ((1u << lane) - 1u));
+    bool good = true;
+    if (m) {
+      uint32_t ref;
+      if (Lc.window) {   // the chain's literal root, resolved by k_dec_lit
+        ref = __ldcg(&w.srcrow[(size_t)t * sh.B + Lc.row0 + b]) - (uint32_t)Lc.row0;
+        good = ref < (uint32_t)b;
+      } else {           // whole slice: the first occurrence, always a literal
+        const unsigned long long kk = (unsigned long long)mbase + before + at;
+        const uint8_t* refs = cin + Lc.off_refs;
+        ref = Lc.ref_bytes == 2 ? (uint32_t)reinterpret_cast<const uint16_t*>(refs)[kk]
+                                : reinterpret_cast<const uint32_t*>(refs)[kk];
+        good = (int64_t)ref < b && !((bmt[ref >> 5] >> (ref & 31)) & 1u);
       }
+      s_dst[warp][at] = (uint32_t)b;
+      s_src[warp][at] = good ? ref : (uint32_t)b;
     }
+    if (!__all_sync(0xffffffffu, good)) {
+      if (lane == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
+      return;
+    }
+    __syncwarp();
+    const uint32_t nm = __popc(bm);
+    const size_t rstride = (size_t)sh.T_out * D;   // floats between consecutive batch rows
+    float* base = xhat + ((size_t)Lc.row0 * sh.T_out + sh.t_off + t) * D;
+    // (row, float4) pairs of the word's matched rows, kUnroll per lane in flight
+    for (uint32_t p0 = 0; p0 < nm * kQ; p0 += 32u * kUnroll) {
+      float4 v[kUnroll];
+      float4* dp[kUnroll];
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (i0 + k * stride < n4) __stcs(reinterpret_cast<float4*>(xhat + dst[k]), v[k]);
+      for (int i = 0; i < kUnroll; ++i) {
+        const uint32_t pi = p0 + (uint32_t)i * 32u + lane;
+        dp[i] = nullptr;
+        if (pi < nm * kQ) {
+          const uint32_t row = pi / kQ, q = pi % kQ;
+          v[i] = __ldcg(reinterpret_cast<const float4*>(base + (size_t)s_src[warp][row] * rstride) + q);
+          dp[i] = reinterpret_cast<float4*>(base + (size_t)s_dst[warp][row] * rstride) + q;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < kUnroll; ++i)
+        if (dp[i]) __stcs(dp[i], v[i]);
+    }
+    __syncwarp();
   }
 }
 
@@ -734,22 +918,23 @@ template <int D, int W>
 static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, const unsigned long long* offs,
                                 const Shape& sh, const Work& w, float* xhat, uint32_t epoch, cudaStream_t st,
                                 Prof* prof) {
-  const unsigned nsegT = (unsigned)(sh.U * sh.nseg);
-  prof_begin(prof, "k_dec_prep", st);
-  launch_k(k_dec_prep<D, W>, (sh.U > 0 ? sh.U : 1) + (nsegT + 7) / 8, 256, 0, st, in, in_bytes, offs, sh, w,
-           epoch);
+  using G = DGeo<D>;
+  const unsigned ngrp = (unsigned)(div_up(sh.nseg, G::kSPC) > 0 ? div_up(sh.nseg, G::kSPC) : 1);
+  const unsigned grid = sh.U > 0 ? (unsigned)sh.U * ngrp : 1u;
+  prof_begin(prof, "k_dec_tables", st);
+  launch_k(k_dec_tables<W>, (unsigned)(sh.U > 0 ? sh.U : 1), 128, 0, st, in, in_bytes, offs, sh, w, epoch);
   prof_end(prof, st);
-  if (nsegT) {
-    // one CTA per run slot: enough for the largest possible chunk count
-    prof_begin(prof, "k_dec_chunks", st);
-    launch_k(k_dec_chunks<D, W>, (unsigned)(dec_run_slots(sh) - 1), kDecRun, 0, st, in, sh, w, xhat, epoch);
-    prof_end(prof, st);
-    prof_begin(prof, "k_dec_matches", st);
-    static int per_sm = -1;   // resident CTAs per SM: the grid-stride loop runs in one wave
-    if (per_sm < 0 &&
-        (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dec_matches<D>, 256, 0) != cudaSuccess || per_sm < 1))
-      per_sm = 4;
-    launch_k(k_dec_matches<D>, (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm), 256, 0, st, sh, w, xhat, epoch);
+  prof_begin(prof, "k_dec_lit", st);
+  launch_k(k_dec_lit<D, W>, grid, G::kThreads, 0, st, in, in_bytes, offs, sh, w, xhat, epoch);
+  prof_end(prof, st);
+  if (sh.U > 0 && sh.nseg > 0) {
+    // persistent: the resident CTAs, at most one warp per bitmap word
+    const unsigned long long words = (unsigned long long)sh.U * sh.nw;
+    unsigned mgrid = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * 4);
+    const unsigned long long need = (words + kMatchThreads / 32 - 1) / (kMatchThreads / 32);
+    if (need < mgrid) mgrid = (unsigned)need;
+    prof_begin(prof, "k_dec_match", st);
+    launch_k(k_dec_match<D>, mgrid, kMatchThreads, 0, st, in, in_bytes, offs, sh, w, xhat, epoch);
     prof_end(prof, st);
   }
 }
@@ -784,5 +969,7 @@ cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, co
   }
   return cudaGetLastError();
 }
+
+cudaError_t set_decoder_attributes() { return cudaSuccess; }   // every decoder kernel fits the default limits
 
 }  // namespace ebc

@@ -25,7 +25,6 @@ constexpr int kMaxB = 16777215;
 
 // ---- decoder ----
 constexpr int kLutBits = 11;               // first-level decode table: 2^11 entries
-constexpr int kDecRun = 64;                // chunks per decoder CTA (one thread each)
 
 constexpr unsigned long long kEmptySlot = ~0ull;
 
@@ -133,17 +132,6 @@ struct ContLay {
 constexpr uint32_t kModeNoDedup = 1;   // every vector of the table is a literal
 constexpr uint32_t kModeRawCodes = 2;  // every code 8 bits (lengths all 8: code of symbol s is s)
 
-// Decoder run slots: unit u's runs of kDecRun chunks start at slot
-// floor(chunk0_u / kDecRun) + u (chunk0_u counted over all containers), so the
-// slots of all units are disjoint and ordered, and every slot below
-// floor(n_chunks / kDecRun) + U is written.
-__host__ __device__ inline unsigned long long dec_max_chunks(const Shape& sh) {
-  return (unsigned long long)sh.U * (unsigned long long)sh.nseg * (unsigned long long)(sh.SB / sh.KC);
-}
-__host__ __device__ inline unsigned long long dec_run_slots(const Shape& sh) {
-  return dec_max_chunks(sh) / kDecRun + (unsigned long long)sh.U + 1ull;
-}
-
 // Per-table absolute bounds of one compress call, passed by value.
 struct EbParams {
   float eb[kMaxT];
@@ -162,18 +150,16 @@ struct Glob {
   unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
 };
 
-// Decoder side tables of one table (canonical code).
-struct DecTab {
-  uint32_t first[kLmax + 1];   // first code of each length
-  uint32_t count[kLmax + 1];   // codes of each length
-  uint32_t offset[kLmax + 1];  // index of that first code in sorted[]
-  float ebx2;                  // 2 * eb
-  uint32_t chunk0, chunk1;     // the unit's chunks: [chunk0, chunk1), over all containers
-  uint32_t t;                  // table of the unit
-  unsigned long long bits_off; // byte offset of the unit's container bitstream in the input
-  unsigned long long n_words;  // words of that bitstream
-  unsigned long long row0;     // first batch row of the unit's slice
-  uint16_t sorted[kMaxSyms];   // symbols by (length, symbol)
+// Decode tables of one unit, built once per call by the decoder's first kernel
+// (16-byte aligned: the first-level table is copied with 16-byte accesses).
+struct __align__(16) DTab {
+  uint16_t lut[1 << kLutBits];   // sym | len << kLenShift for codes of at most kLutBits bits (sym 0 and len 0:
+                                 // a longer code's prefix)
+  float val[kMaxSyms];           // reconstruction of each symbol
+  uint16_t sorted[kMaxSyms];     // symbols in canonical order (by length, then symbol)
+  uint32_t first[kLmax + 1];     // first code of each length
+  uint32_t count[kLmax + 1];     // codes of each length
+  uint32_t offset[kLmax + 1];    // index in sorted[] of each length's first code
 };
 
 // Device scratch of a context.  Sizes follow Shape.
@@ -201,14 +187,11 @@ struct Work {
   uint32_t* tabcode;           // [U][A] code << 8 | length
   ContLay* cont;               // [R] container layouts
   // decompress
-  uint16_t* lut;               // [U][1 << kLutBits] sym | len << kLenShift (len 0 = long code)
-  DecTab* dtab;                // [U]
-  uint4* cdesc;                // [U*nseg*chunks] {start bit lo, start bit hi | length << 16, segment, first literal | rows << 16}
-  uint16_t* litrow;            // [U*nseg][SB] literal rows of each segment, in row order
-  uint2* mdesc;                // [n_match] {destination row, source row} as b * T_out + t_off + t
+  uint4* uacc;                 // [U] per-unit accumulators {literals, matches, outliers, arrived CTAs}, zero
+                               //   between calls (the last CTA of each unit empties its own)
+  uint2* cacc;                 // [R] per-container accumulators {outliers, arrived units}, zero between calls
+  DTab* dtab;                  // [U] decode tables
   uint32_t* srcrow;            // [T][B] windowed containers: each row's source row (itself for a literal)
-  uint4* runmap;               // [dec_run_slots] {table, first chunk, end chunk, 0} of each run of chunks;
-                               //   table ~0u = no run
   Glob* glob;
 };
 
@@ -440,5 +423,6 @@ cudaError_t launch_decompress(const uint8_t* in, unsigned long long in_bytes, co
                               const Shape& sh, const Work& w, float* xhat, uint32_t epoch, cudaStream_t st,
                               Prof* prof);
 cudaError_t set_kernel_attributes();
+cudaError_t set_decoder_attributes();
 
 }  // namespace ebc

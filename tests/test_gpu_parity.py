@@ -271,33 +271,57 @@ def _decode_rc(codec, buf, shape):
     return codec.last_error(), xh
 
 
-def test_corrupt_containers(codec):
+def _corruption_cases(ref, rng, n_random):
+    """Single-bit flips: a few in every section of the container, then random ones."""
+    h = lambda o: int(np.frombuffer(ref[o:o + 8].tobytes(), np.uint64)[0])
+    off_seg, off_bitmap, off_chunks, off_refs, off_bits = h(88), h(96), h(104), h(112), h(120)
+    sections = [(0, 144), (144, off_seg), (off_seg, off_bitmap), (off_bitmap, off_chunks),
+                (off_chunks, off_refs), (off_refs, off_bits), (off_bits, len(ref))]
+    # the counts of each table record (literals, matches, outliers) and the header's counts
+    fields = [64, 48, 56, 72, 80] + [144 + k * 272 + f for k in range(2) for f in (4, 8, 12)]
+    cases = [(i, b) for i in fields for b in (0, 1, 5)]
+    for lo, hi in sections:
+        if hi > lo:
+            cases += [(int(rng.integers(lo, hi)), int(rng.integers(0, 8))) for _ in range(6)]
+    cases += [(int(rng.integers(0, len(ref))), int(rng.integers(0, 8))) for _ in range(n_random)]
+    return cases
+
+
+@pytest.mark.parametrize("window", [0, 16])
+def test_corrupt_containers(codec, window):
+    """The GPU decoder rejects exactly the containers the oracle's decoder rejects,
+    with the same code, and when both accept one, their reconstructions agree bit
+    for bit; the context keeps working."""
     wl = workloads.make("tiny", batch=256, tables=2)
-    x, eb = wl.x.numpy(), wl.eb.numpy()
-    ref, _ = oracle.compress(x, eb)
+    x, eb = wl.x.numpy().copy(), wl.eb.numpy()
+    x[3, 1, 5] = np.float32(7.5)          # outliers, so that the outlier counts are checked too
+    x[200, 0, 0] = np.float32(-3.25)
+    ref, info = oracle.compress(x, eb, window=window)
+    assert info["n_outlier"] >= 2 and info["n_match"] > 0
     shape = x.shape
-    assert _decode_rc(codec, ref, shape)[0] == 0
-    assert _decode_rc(codec, ref[:-1], shape)[0] == ebc.EBC_ERR_CORRUPT
-    bad = ref.copy(); bad[0] ^= 1
-    assert _decode_rc(codec, bad, shape)[0] == ebc.EBC_ERR_CORRUPT
-    off_chunks = int(np.frombuffer(ref[104:112].tobytes(), np.uint64)[0])
-    bad = ref.copy(); bad[off_chunks] ^= 1
-    assert _decode_rc(codec, bad, shape)[0] == ebc.EBC_ERR_CORRUPT
-    bad = ref.copy(); bad[160 + 128] = 30
-    assert _decode_rc(codec, bad, shape)[0] == ebc.EBC_ERR_CORRUPT
-    assert _decode_rc(codec, ref, (shape[0] + 1,) + shape[1:])[0] == ebc.EBC_ERR_INVALID_ARG
-    rng = np.random.default_rng(0)
-    for _ in range(40):
-        bad = ref.copy()
-        i = int(rng.integers(0, len(bad)))
-        bad[i] ^= np.uint8(1 << int(rng.integers(0, 8)))
-        rc_o = oracle.decompress_rc(bad, *shape)[0]
-        rc_g, _ = _decode_rc(codec, bad, shape)
-        assert rc_g in (0, ebc.EBC_ERR_CORRUPT, ebc.EBC_ERR_INVALID_ARG)
-        if rc_o == oracle.OK:
-            assert rc_g == 0
-    # still usable
-    assert _decode_rc(codec, ref, shape)[0] == 0
+    codec.set_window(window)
+    try:
+        assert _decode_rc(codec, ref, shape)[0] == 0
+        assert _decode_rc(codec, ref[:-1], shape)[0] == ebc.EBC_ERR_CORRUPT
+        assert _decode_rc(codec, ref, (shape[0] + 1,) + shape[1:])[0] == ebc.EBC_ERR_INVALID_ARG
+        rng = np.random.default_rng(window)
+        n_both_ok = 0
+        for i, bit in _corruption_cases(ref, rng, 120):
+            bad = ref.copy()
+            bad[i] ^= np.uint8(1 << bit)
+            rc_o, xo, _ = oracle.decompress_rc(bad, *shape)
+            rc_g, xg = _decode_rc(codec, bad, shape)
+            assert rc_g == rc_o, (i, bit, rc_g, rc_o)
+            if rc_o == oracle.OK:
+                n_both_ok += 1
+                assert np.array_equal(xg.cpu().numpy().view(np.uint32), xo.view(np.uint32)), (i, bit)
+        assert n_both_ok > 0
+        # still usable
+        rc, xg = _decode_rc(codec, ref, shape)
+        assert rc == 0
+        assert np.array_equal(xg.cpu().numpy().view(np.uint32), oracle.decompress(ref, *shape)[0].view(np.uint32))
+    finally:
+        codec.set_window(0)
 
 
 def test_full_size_large_batch(codec):

@@ -75,7 +75,7 @@ def test_recovers_after_a_corrupt_container(codec):
 
 
 def test_rejects_a_shape_beyond_the_static_scratch():
-    B, T, D = 1 << 20, 8, 4           # the match list alone needs 64 MiB
+    B, T, D = 1 << 20, 8, 4           # the reference-chain table alone needs 32 MiB
     src = torch.zeros(4096, dtype=torch.uint8, device="cuda")
     xhat = torch.full((B, T, D), 7.0, dtype=torch.float32, device="cuda")
     torch.cuda.synchronize()
