@@ -56,15 +56,6 @@ __device__ __forceinline__ bool eb_usable(float eb) {
   return __fdiv_rn(1.0f, ebx2) >= 1.17549435e-38f;
 }
 
-struct Layout {
-  unsigned long long n_lit, n_match, n_out, n_chunks, words;
-  unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;   // relative to base
-  unsigned long long base;          // the container's first byte in the input
-  unsigned long long row0, n;       // the batch rows it restores: [row0, row0 + n)
-  unsigned int window, ref_bytes;   // dedup window (0 = whole batch) and bytes per reference
-  unsigned int nseg, nw;            // segments and bitmap words per table
-};
-
 // Header checks of a container of n rows and `bytes` bytes (h: its first
 // byte).  Returns an EBC_* code; on success *L holds the section layout
 // recomputed from the counts.
@@ -296,6 +287,7 @@ __global__ void __launch_bounds__(128) k_dec_tables(const uint8_t* __restrict__ 
     }
     Layout L{};
     s_code = have_unit ? container_layout(in, in_bytes, offs, sh, r, &L) : EBC_OK;
+    if (have_unit && t == 0 && s_code == EBC_OK) w.lay[r] = L;   // for the decode CTAs: no second parse
   }
   __syncthreads();
   if (s_code != EBC_OK || !have_unit) return;
@@ -379,7 +371,6 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   constexpr int kLenShift = Alph<W>::kLenShift;
   constexpr uint32_t kSymMask = (1u << kLenShift) - 1u;
   __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
-  __shared__ float s_val[kA];
   __shared__ uint16_t s_sorted[kA];
   __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
   __shared__ uint32_t s_recs[(G::kSPC + 1) * 4];      // the group's segment records and the one after
@@ -428,10 +419,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     const DTab* dt = w.dtab + u;
     for (int i = tid; i < (1 << kLutBits) / 8; i += kNT)
       reinterpret_cast<uint4*>(s_lut)[i] = __ldcg(reinterpret_cast<const uint4*>(dt->lut) + i);
-    for (int i = tid; i < kA; i += kNT) {
-      s_val[i] = __ldcg(&dt->val[i]);
-      s_sorted[i] = dt->sorted[i];
-    }
+    for (int i = tid; i < kA; i += kNT) s_sorted[i] = dt->sorted[i];
     if (tid <= kLmax) {
       s_first[tid] = __ldcg(&dt->first[tid]);
       s_count[tid] = __ldcg(&dt->count[tid]);
@@ -449,11 +437,11 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     }
   }
   if (tid == 0) {
-    Layout L{};
-    // the headers and tables were checked by k_dec_tables: after a failure there (already recorded,
-    // code -1) the CTA only takes part in the unit's counters
-    int code = dec_aborted(g, epoch) ? -1 : EBC_OK;
-    if (have_unit && code == EBC_OK) code = container_layout(in, in_bytes, offs, sh, r, &L);
+    // the headers and tables were checked by k_dec_tables, which left each container's layout in the
+    // scratch: after a failure there (already recorded, code -1) the CTA only takes part in the unit's
+    // counters
+    const int code = dec_aborted(g, epoch) ? -1 : EBC_OK;
+    const Layout L = have_unit && code == EBC_OK ? w.lay[r] : Layout{};
     s_L = L;
     s_code = code;
     s_cnt[0] = s_cnt[1] = s_cnt[2] = 0u;
@@ -516,11 +504,18 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
           }
         }
         uint32_t tot, vt;
-        uint32_t k = nlit + warp_excl(__popc(litw), &tot);
+        const uint32_t k = nlit + warp_excl(__popc(litw), &tot);
         warp_excl(__popc(valid), &vt);
+        // the word's literal rows, by rank: lane b of the warp takes bit b of each word in turn
+        const uint32_t wbase = (uint32_t)(half * 32);
+        for (int wl = 0; wl < 32; ++wl) {
+          const uint32_t lw = __shfl_sync(0xffffffffu, litw, wl), kb = __shfl_sync(0xffffffffu, k, wl);
+          if ((lw >> lane) & 1u)
+            s_litrow[j * G::kSB + kb + __popc(lw & ((1u << lane) - 1u))] = (uint16_t)((wbase + wl) * 32 + lane);
+          if (wbase + wl + 1 >= (uint32_t)G::kBmWords) break;
+        }
         nlit += tot;
         nvalid += vt;
-        for (uint32_t m = litw; m; m &= m - 1) s_litrow[j * G::kSB + k++] = (uint16_t)(wi * 32 + __ffs(m) - 1);
       }
       const uint32_t nmatch = nvalid - nlit;
       const uint32_t nch = (nlit + G::kKC - 1) / G::kKC;
@@ -573,6 +568,12 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     const int64_t brow0 = (int64_t)L.row0;
     float4* slot = s_slot + warp * 32 * G::kPieceQ;
     uint32_t* ws = s_ws[warp];
+    // the reconstruction fl32((sym - R) * 2 eb): the integer sym - R (|.| < 2^22) becomes a float
+    // exactly by placing it in the mantissa of 1.5 * 2^23 and subtracting that
+    const float ebx2 = __fmul_rn(2.0f, __uint_as_float(s_rec[0]));
+    auto value = [&](uint32_t sym) -> float {
+      return __fmul_rn(__fsub_rn(__uint_as_float(0x4B400000u - (uint32_t)Alph<W>::kR + sym), 12582912.0f), ebx2);
+    };
     for (uint32_t b0 = (uint32_t)warp * 32u; b0 < nchunks;) {
       // the batch's words (its chunks are consecutive, so their bits are too): staged in this warp's
       // buffer with coalesced 16-byte loads when they fit, else read from global memory
@@ -634,7 +635,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
                 const uint32_t e = s_lut[(uint32_t)(buf >> (64 - kLutBits))];
                 const uint32_t sym = e & kSymMask;
                 plain = sym ? plain : 0u;
-                o[q] = s_val[sym];
+                o[q] = value(sym);
                 buf <<= e >> kLenShift;
                 nb -= e >> kLenShift;
               }
@@ -652,7 +653,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
                     sym = long_code<W>(peek, s_first, s_count, s_offset, s_sorted, &len, &bad);
                   buf <<= len;
                   nb -= len;
-                  float v = s_val[sym];
+                  float v = value(sym);
                   if (sym == 0u) {   // outlier: the next 32 bits are the raw value
                     if (nb <= 32u) refill();
                     v = __uint_as_float((uint32_t)(buf >> 32));
@@ -834,14 +835,14 @@ __global__ void __launch_bounds__(kMatchThreads, 4) k_dec_match(const uint8_t* _
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (tid == 0) s_abort = dec_aborted(g, epoch);
-  for (int c = tid; c < sh.R; c += kMatchThreads) {   // the containers' layouts (checked by k_dec_lit)
-    Layout Lc{};
-    if (container_layout(in, in_bytes, offs, sh, c, &Lc) != EBC_OK) s_abort = 1;
+  __syncthreads();
+  if (s_abort) return;
+  for (int c = tid; c < sh.R; c += kMatchThreads) {   // the containers' layouts, as k_dec_tables checked them
+    const Layout Lc = w.lay[c];
     s_lay[c] = MLay{Lc.base, Lc.off_bitmap, Lc.off_refs, Lc.off_seg, Lc.row0, (unsigned int)Lc.n, Lc.nseg, Lc.nw,
                     Lc.ref_bytes, Lc.window};
   }
   __syncthreads();
-  if (s_abort) return;
   const int T = sh.T;
   const unsigned long long nbatch = (unsigned long long)sh.U * sh.nw;   // bitmap words of all units
   const unsigned long long wstep = (unsigned long long)gridDim.x * kNW;

@@ -128,6 +128,16 @@ struct ContLay {
   uint32_t ref_bytes;
 };
 
+// Section layout of one container as the decoder checks it (offsets relative to base).
+struct Layout {
+  unsigned long long n_lit, n_match, n_out, n_chunks, words;
+  unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
+  unsigned long long base;          // the container's first byte in the input
+  unsigned long long row0, n;       // the batch rows it restores: [row0, row0 + n)
+  unsigned int window, ref_bytes;   // dedup window (0 = whole batch) and bytes per reference
+  unsigned int nseg, nw;            // segments and bitmap words per table
+};
+
 // Per-table coding modes (bit flags; 0 = vector dedup + Huffman codes).
 constexpr uint32_t kModeNoDedup = 1;   // every vector of the table is a literal
 constexpr uint32_t kModeRawCodes = 2;  // every code 8 bits (lengths all 8: code of symbol s is s)
@@ -191,6 +201,7 @@ struct Work {
                                //   between calls (the last CTA of each unit empties its own)
   uint2* cacc;                 // [R] per-container accumulators {outliers, arrived units}, zero between calls
   DTab* dtab;                  // [U] decode tables
+  Layout* lay;                 // [R] each container's section layout, as the decoder's header check found it
   uint32_t* srcrow;            // [T][B] windowed containers: each row's source row (itself for a literal)
   Glob* glob;
 };
