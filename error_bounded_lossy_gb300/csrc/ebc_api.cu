@@ -171,7 +171,6 @@ static Work carve_compress(void* buf, const Shape& sh, Glob* g, size_t* total) {
   w.seg_base = c.take<uint4>(16 * nsegT);
   w.sym = c.take<uint8_t>((size_t)sh.T * sh.symstride);
   w.vhash = c.take<uint32_t>(4 * nvec);
-  w.vnout = c.take<uint32_t>(4 * nvec);
   w.ref = c.take<uint32_t>(4 * nvec);
   w.bitmap = c.take<uint32_t>(4 * U * sh.nw);
   w.seg_hist = c.take<uint32_t>(4 * (size_t)sh.A * nsegT);

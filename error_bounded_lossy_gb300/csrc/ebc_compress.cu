@@ -81,6 +81,57 @@ __device__ __forceinline__ typename QuadOf<W>::T quantize_quad(float4 v, float e
   else return quantize_four_wide(v, eb, ebx2, inv, ok);
 }
 
+// The same arithmetic on pairs of values with the packed (two-lane) fp32
+// instructions: t = fl(x * inv), y = fl(t + 1.5*2^23), q = fl(y - 1.5*2^23),
+// h = fl(q * ebx2), each rounded to nearest as in the scalar form.  The error
+// x - h is taken with the scalar, explicitly rounded subtraction: a packed
+// subtraction after the packed product is contracted into one fused
+// multiply-add by the compiler (even written as an fma with a -0 addend),
+// which rounds x - q * ebx2 once and moves the error bound's edge.
+// inv2, ebx22, c2: the operands duplicated in both halves.
+__device__ __forceinline__ void quantize_pair(float x0, float x1, unsigned long long inv2, unsigned long long ebx22,
+                                              unsigned long long c2, float& t0, float& t1, float& y0, float& y1,
+                                              float& e0, float& e1) {
+  float h0, h1;
+  asm("{\n .reg .b64 X, T, Y, Q, H;\n"
+      " mov.b64 X, {%6, %7};\n"
+      " mul.rn.f32x2 T, X, %8;\n"
+      " add.rn.f32x2 Y, T, %10;\n"
+      " sub.rn.f32x2 Q, Y, %10;\n"
+      " mul.rn.f32x2 H, Q, %9;\n"
+      " mov.b64 {%0, %1}, T;\n mov.b64 {%2, %3}, Y;\n mov.b64 {%4, %5}, H;\n}"
+      : "=f"(t0), "=f"(t1), "=f"(y0), "=f"(y1), "=f"(h0), "=f"(h1)
+      : "f"(x0), "f"(x1), "l"(inv2), "l"(ebx22), "l"(c2));
+  e0 = __fsub_rn(x0, h0);
+  e1 = __fsub_rn(x1, h1);
+}
+__device__ __forceinline__ unsigned long long dup2(float v) {
+  return ((unsigned long long)__float_as_uint(v) << 32) | __float_as_uint(v);
+}
+
+// Four codes from the packed quantizer: ok[k] when |t| < R - 1/2 and |err| <= eb.
+template <int W>
+__device__ __forceinline__ typename QuadOf<W>::T quantize_quad2(float4 v, float eb, unsigned long long inv2,
+                                                                unsigned long long ebx22, bool ok[4]) {
+  constexpr float kLim = W == 1 ? 127.5f : 511.5f;
+  const unsigned long long c2 = 0x4B4000004B400000ull;   // 1.5 * 2^23 in both halves
+  float t[4], y[4], e[4];
+  quantize_pair(v.x, v.y, inv2, ebx22, c2, t[0], t[1], y[0], y[1], e[0], e[1]);
+  quantize_pair(v.z, v.w, inv2, ebx22, c2, t[2], t[3], y[2], y[3], e[2], e[3]);
+  uint32_t u[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ok[k] = (fabsf(t[k]) < kLim) & (fabsf(e[k]) <= eb);   // false for NaN and +-inf too
+    u[k] = ok[k] ? __float_as_uint(y[k]) : (W == 1 ? 0x80u : 0xFE00u);
+  }
+  if constexpr (W == 1) {
+    return __byte_perm(__byte_perm(u[0], u[1], 0x0040u), __byte_perm(u[2], u[3], 0x0040u), 0x5410u) ^ 0x80808080u;
+  } else {
+    return make_uint2(__vadd2(__byte_perm(u[0], u[1], 0x5410u), 0x02000200u),
+                      __vadd2(__byte_perm(u[2], u[3], 0x5410u), 0x02000200u));
+  }
+}
+
 // The dedup key's terms for four codes at element d of the row: one word of
 // four codes, or two words of two codes (word index k = d / 4 or d / 2).
 __device__ __forceinline__ uint32_t quad_key(uint32_t v, int d) {
@@ -268,8 +319,9 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
   using Q = QGeo<D, In>;
   using Quad = typename QuadOf<W>::T;
   constexpr int kA = Alph<W>::kA;
-  extern __shared__ __align__(128) unsigned char s_raw[];   // 2 stages of kStageFloats elements
+  extern __shared__ __align__(128) unsigned char s_raw[];   // 2 stages of kStageFloats elements, then T x {2 eb, 1/(2 eb)}
   In* s_x = reinterpret_cast<In*>(s_raw);
+  float2* s_tab = reinterpret_cast<float2*>(s_raw + 2 * Q::kStageBytes);
   __shared__ __align__(8) uint64_t s_bar[2];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nsegT = sh.T * sh.qseg;
@@ -283,6 +335,10 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     if ((int)(blockIdx.x + gridDim.x) < nsegT)
       issue_segment_tile<D, In>(s_x + Q::kStageFloats, &tmap, &s_bar[1], sh, blockIdx.x + gridDim.x);
   }
+  for (int t = tid; t < sh.T; t += 256) {   // each table's 2 eb and its reciprocal, once per CTA
+    const float ebx2 = __fmul_rn(2.0f, ep.eb[t]);
+    s_tab[t] = make_float2(ebx2, __fdiv_rn(1.0f, ebx2));
+  }
   __syncthreads();
   uint32_t parity = 0;   // bit i: phase of stage i
   int i = 0;
@@ -295,13 +351,16 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     if (s == 0) {   // per-call accumulators of the table's units, which k_resolve adds to
       for (int r = 0; r < sh.R; ++r) {
         const int u = r * sh.T + t;
-        for (int i = tid; i < kA; i += 256) w.tab_hist[(size_t)u * kA + i] = 0u;
+        for (int k = tid; k < kA; k += 256) w.tab_hist[(size_t)u * kA + k] = 0u;
         if (tid == 0) w.tab_cnt[u] = make_uint4(0, 0, 0, 0);
       }
     }
     const float eb = ep.eb[t];
-    const float ebx2 = __fmul_rn(2.0f, eb);
-    const float inv = __fdiv_rn(1.0f, ebx2);
+    const float2 tb = s_tab[t];
+    const unsigned long long ebx22 = dup2(tb.x), inv2 = dup2(tb.y);
+    const int nrows = (int)min((int64_t)G::kSB, B - row0);          // rows of the segment in the batch
+    uint8_t* symseg = w.sym + (size_t)t * sh.symstride + (size_t)row0 * D * W;
+    uint32_t* hseg = w.vhash + (size_t)t * B + row0;
     const bool arrived = mbar_wait(&s_bar[stg], (parity >> stg) & 1u, i == 0 ? sh.first_wait : kWaitLimit);
     if (__syncthreads_or(!arrived)) {   // the whole CTA stops together
       if (tid == 0) {
@@ -317,47 +376,34 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
       return;
     }
     parity ^= 1u << stg;
-    uint32_t acc = 0, nout = 0;
-#pragma unroll 4
+    uint32_t acc = 0;
+#pragma unroll
     for (int k = 0; k < G::kSlabsPerWarp; ++k) {
       const int slab = warp * G::kSlabsPerWarp + k;
-      const int e = slab * 128 + lane * 4;
-      const int r = e / D;
-      const int64_t b = row0 + r;
+      const int e = slab * 128 + lane * 4;   // element of the segment
+      const int r = e / D;                   // row of the segment
       const int d = e % D;
-      const bool valid = b < B;
+      const bool valid = r < nrows;
       const float4 v = load4(xs + Q::offset(r, d));
       bool ok[4];
-      const Quad word = quantize_quad<W>(v, eb, ebx2, inv, ok);
-      if (valid) st_keep_quad(w.sym + (size_t)t * sh.symstride, (size_t)b * D + d, word, pol);
+      const Quad word = quantize_quad2<W>(v, eb, inv2, ebx22, ok);
+      if (valid) st_keep_quad(symseg, (size_t)e, word, pol);
       acc += quad_key(word, d);
       if (!(ok[0] & ok[1] & ok[2] & ok[3])) {
-        if (!ok[0]) { acc += lowbias32(__float_as_uint(v.x) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu); ++nout; }
-        if (!ok[1]) { acc += lowbias32(__float_as_uint(v.y) ^ (uint32_t)(d + 2) * 0x85EBCA6Bu); ++nout; }
-        if (!ok[2]) { acc += lowbias32(__float_as_uint(v.z) ^ (uint32_t)(d + 3) * 0x85EBCA6Bu); ++nout; }
-        if (!ok[3]) { acc += lowbias32(__float_as_uint(v.w) ^ (uint32_t)(d + 4) * 0x85EBCA6Bu); ++nout; }
+        if (!ok[0]) acc += lowbias32(raw32(xs[Q::offset(r, d) + 0]) ^ (uint32_t)(d + 1) * 0x85EBCA6Bu);
+        if (!ok[1]) acc += lowbias32(raw32(xs[Q::offset(r, d) + 1]) ^ (uint32_t)(d + 2) * 0x85EBCA6Bu);
+        if (!ok[2]) acc += lowbias32(raw32(xs[Q::offset(r, d) + 2]) ^ (uint32_t)(d + 3) * 0x85EBCA6Bu);
+        if (!ok[3]) acc += lowbias32(raw32(xs[Q::offset(r, d) + 3]) ^ (uint32_t)(d + 4) * 0x85EBCA6Bu);
       }
-      if ((slab + 1) % G::kSPR == 0) {            // the row ends with this slab
-        // sums over the row's kLPR lanes; outliers are rare, so their count is
-        // reduced only when the warp has one
-        const bool any_out = __any_sync(0xffffffffu, nout != 0u);
+      if ((slab + 1) % G::kSPR == 0) {            // the row ends with this slab: its key, over its kLPR lanes
         if constexpr (G::kLPR == 32) {
           acc = __reduce_add_sync(0xffffffffu, acc);
-          if (any_out) nout = __reduce_add_sync(0xffffffffu, nout);
         } else {
 #pragma unroll
           for (int off = G::kLPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-          if (any_out) {
-#pragma unroll
-            for (int off = G::kLPR / 2; off > 0; off >>= 1) nout += __shfl_xor_sync(0xffffffffu, nout, off);
-          }
         }
-        if (valid && (lane % G::kLPR) == 0) {
-          w.vhash[(size_t)t * B + b] = acc;
-          w.vnout[(size_t)t * B + b] = nout;
-        }
+        if (valid && (lane % G::kLPR) == 0) hseg[r] = acc;
         acc = 0;
-        nout = 0;
       }
     }
     __syncthreads();   // the stage is consumed: refill it with the segment two steps ahead
@@ -414,7 +460,6 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   uint32_t* s_win = s_histwin;
   __shared__ __align__(16) uint32_t s_sym[G::kSegSyms * W / 4 + 4];   // the segment's own codes
   __shared__ uint32_t s_ref[G::kSB];
-  __shared__ uint32_t s_nout[G::kSB];
   __shared__ uint32_t s_bm[G::kBmWords];
   __shared__ uint32_t s_cnt[3];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -451,11 +496,6 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
     const int64_t lo = row0 - sh.window > b0 ? row0 - sh.window : b0;
     const int64_t hi = row0 + G::kSB < bend ? row0 + G::kSB : bend;
     for (int64_t i = tid; i < hi - lo; i += kNT) s_win[i] = __ldcg(&w.vhash[(size_t)t * B + lo + i]);
-#pragma unroll
-    for (int k = 0; k < kRPT; ++k) {
-      const int rr = k * kNT + tid;
-      if (rr < G::kSB && row0 + rr < bend) s_nout[rr] = __ldcg(&w.vnout[(size_t)t * B + row0 + rr]);
-    }
     __syncthreads();
 #pragma unroll 1
     for (int k = 0; k < kRPT; ++k) {
@@ -476,15 +516,12 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   } else
   // one thread per row: first occurrence of the row's key in the slice
   {
-    uint32_t h[kRPT], no[kRPT];
+    uint32_t h[kRPT];
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
       const int rr = k * kNT + tid;
       const int64_t b = row0 + rr;
-      if (rr < G::kSB && b < bend) {
-        h[k] = __ldcg(&w.vhash[(size_t)t * B + b]);
-        no[k] = __ldcg(&w.vnout[(size_t)t * B + b]);
-      }
+      if (rr < G::kSB && b < bend) h[k] = __ldcg(&w.vhash[(size_t)t * B + b]);
     }
 #pragma unroll
     for (int k = 0; k < kRPT; ++k) {
@@ -494,7 +531,6 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
         uint32_t ref = nodedup ? (uint32_t)b : dedup_lookup(slots, sh.S, h[k], w.glob);
         if (ref > (uint32_t)b || (int64_t)ref < b0) ref = (uint32_t)b;   // only on an internal error
         s_ref[rr] = ref;
-        s_nout[rr] = no[k];
       }
     }
   }
@@ -508,7 +544,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   const unsigned gshift = lane & ~(G::kLPR - 1);
   const unsigned gmask = (G::kLPR == 32 ? 0xffffffffu : ((1u << G::kLPR) - 1u)) << gshift;
   const bool leader = (lane % G::kLPR) == 0;
-  uint32_t n_lit = 0, n_match = 0, n_out = 0;
+  uint32_t n_lit = 0, n_match = 0;
   // the reference rows' codes of a group of steps (the next group's loads are in flight while
   // this one is compared)
   auto load_refs = [&](int g0, Quad (&wr)[kGroup][G::kSPR]) {
@@ -564,7 +600,6 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
           ++n_match;
         } else {
           ++n_lit;
-          n_out += s_nout[rr];
         }
       }
     }
@@ -582,11 +617,9 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   }
   n_lit = __reduce_add_sync(0xffffffffu, n_lit);
   n_match = __reduce_add_sync(0xffffffffu, n_match);
-  n_out = __reduce_add_sync(0xffffffffu, n_out);
   if (lane == 0) {
     atomicAdd(&s_cnt[0], n_lit);
     atomicAdd(&s_cnt[1], n_match);
-    atomicAdd(&s_cnt[2], n_out);
   }
   __syncthreads();
 #pragma unroll
@@ -595,6 +628,7 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
 #pragma unroll
     for (int k = 0; k < kNW; ++k) f = add4(f, reinterpret_cast<const uint4*>(s_histwin + k * kA)[i]);
     reinterpret_cast<uint4*>(w.seg_hist + (size_t)seg * kA)[i] = f;
+    if (i == 0) s_cnt[2] = f.x;   // the literal rows' outliers: their codes of symbol 0
     uint32_t* th = w.tab_hist + (size_t)u * kA + 4 * i;
     if (f.x) atomicAdd(th + 0, f.x);
     if (f.y) atomicAdd(th + 1, f.y);
@@ -1551,7 +1585,7 @@ static void launch_compress_d(const In* x, const Shape& sh, const EbParams& ep, 
   if (grid) {
     // persistent quantize: as many CTAs as fit at once (two input stages each), at most one per segment
     static int per_sm = -1;
-    const int smem = 2 * (int)QGeo<D, In>::kStageBytes;
+    const int smem = 2 * (int)QGeo<D, In>::kStageBytes + 8 * kMaxT;   // two input stages, the tables' bounds
     if (per_sm < 0) {
       cudaFuncSetAttribute(k_quantize<D, In, W>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_quantize<D, In, W>, 256, smem) != cudaSuccess ||

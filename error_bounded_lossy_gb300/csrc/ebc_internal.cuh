@@ -181,7 +181,6 @@ struct Work {
   uint8_t* sym;                // [T][B][D] quantization codes (W bytes each), table t at t * symstride
                                //   (16-byte aligned)
   uint32_t* vhash;             // [T][B] dedup key
-  uint32_t* vnout;             // [T][B] outliers per vector
   unsigned long long* slots;   // [U][S] (hash << 32 | first row); all ones = empty
   uint32_t* bitmap;            // [U][nw] match bits (rows of the unit's slice)
   uint32_t* ref;               // [T][B] reference row (batch row) of matched rows
