@@ -51,6 +51,8 @@ def parse():
     p.add_argument("--link-gbs", type=float, default=12.5,
                    help="network bandwidth (GB/s) for the Eq. (2) per-table mode choice (12.5 = 100 Gb/s)")
     p.add_argument("--no-hybrid", action="store_true", help="skip the per-table mode measurements")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the other workloads (backward gradients, large batch, iteration sweep)")
     p.add_argument("--radius", type=int, default=128, choices=[128, 512],
                    help="quantization radius of the timed steps (512: the wide alphabet)")
     p.add_argument("--chunks", type=int, default=1,
@@ -180,48 +182,87 @@ def algorithmic_bytes(kernel: str, N: int, D: int, st: dict) -> int:
     }.get(kernel, 0)
 
 
-def oracle_sample_rate(x_np, eb, seconds: float):
-    """Oracle compress+decompress GB/s on the host, looping over a bounded sample."""
+def host_cpu():
+    """The host's CPU model and logical core count."""
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    if not model:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        model = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return {"cpu_model": model or platform.machine(), "nproc": os.cpu_count()}
+
+
+def oracle_rate(x_np, eb, seconds: float, max_reps: int | None = None):
+    """Oracle compress+decompress GB/s on the host over whole passes of x_np
+    (at least one), until `seconds` have passed or max_reps were made."""
     import oracle
     oracle.build()
-    done, t_total, reps = 0, 0.0, 0
+    done, t_total, reps, info = 0, 0.0, 0, None
     B, T, D = x_np.shape
-    while t_total < seconds or reps == 0:
+    while (t_total < seconds or reps == 0) and (max_reps is None or reps < max_reps):
         t0 = time.perf_counter()
         buf, info = oracle.compress(x_np, eb)
         oracle.decompress(buf, B, T, D)
         t_total += time.perf_counter() - t0
         done += x_np.nbytes
         reps += 1
-    return done / t_total / 1e9, reps, info
+    return done / t_total / 1e9, reps, info, t_total
+
+
+def workload_config(B: int, T: int, D: int, world: int, args) -> dict:
+    return {"workload": "DLRM forward lookups [8192,26,128] fp32, 26 tables rows 1e3..1e6 log-uniform, "
+                        "Zipf(1.05), eb_t=1e-2*range", "global_batch": B * world, "tables": T, "dim": D,
+            "parallelism": f"replicas x{world}", "l2": "flushed before every step (2x L2 memset)",
+            "radius": args.radius, "chunks": args.chunks}
 
 
 def run_reference(args, world, rank):
+    """The oracle, as it stands, on the host cores: the full forward batch per step
+    (at most 20 timed steps and 3 warm-up passes, about 1 s each)."""
     if rank != 0:
         return
     import oracle
-    wl = workloads.make(WORKLOAD, batch=512)
+    oracle.build()
+    wl = workloads.make(WORKLOAD)
     x_np, eb = wl.x.numpy(), wl.eb.numpy()
-    for _ in range(args.warmup):
-        _, _, info = oracle_sample_rate(x_np, eb, 0.0)
-    steps = max(1, args.steps)
+    B, T, D = x_np.shape
+    warm = min(args.warmup, 3)
+    for _ in range(warm):
+        buf, info = oracle.compress(x_np, eb)
+        oracle.decompress(buf, B, T, D)
+    steps = max(1, min(args.steps, 20))
     times = []
     for _ in range(steps):
         s = time.perf_counter()
-        buf, _ = oracle.compress(x_np, eb)
-        oracle.decompress(buf, *x_np.shape)
+        buf, info = oracle.compress(x_np, eb)
+        oracle.decompress(buf, B, T, D)
         times.append(time.perf_counter() - s)
     total = sum(times)
     value = steps * x_np.nbytes / total / 1e9
-    sample = f"first 512 of 8192 batch rows, all 26 tables, D=128 ({x_np.nbytes} B) per step"
+    sample = f"the whole batch [{B},{T},{D}] ({x_np.nbytes} B) per step, compress + decompress"
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 0,
-        "steps": steps, "warmup": args.warmup, "ms_per_step": round(1e3 * total / steps, 3),
+        "steps": steps, "warmup": warm, "steps_requested": args.steps, "warmup_requested": args.warmup,
+        "ms_per_step": round(1e3 * total / steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": "DLRM forward lookups [8192,26,128] fp32, Zipf(1.05), eb=1e-2*range (oracle sample)",
-                   "global_batch": 512, "tables": 26, "dim": 128, "l2": "n/a (host)"},
+        "config": workload_config(B, T, D, 1, args),
         "compression_ratio": round(x_np.nbytes / info["total_bytes"], 3),
-        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                         **host_cpu()},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -560,13 +601,120 @@ def main():
             codec.set_radius(args.radius)
             wide[wname] = row
 
+    # ---- the other workloads (outside the timed region): backward gradients [8192,26,128], the large
+    #      batch [65536,26,256] (fp32 and bf16-cast; it does not fit in L2), and the iteration sweep ----
+    configs = None
+    if not args.no_configs:
+        def run_case(xin, ebv, nrep, prof_steps):
+            """Mean compress / decompress time over nrep steps (L2 flushed before each), the stats, the
+            per-kernel profile over prof_steps more steps, and whether every bound held."""
+            Bc, Tc, Dc = xin.shape
+            capc = codec.compress_bound(Bc, Tc, Dc)
+            oc = torch.empty(capc, dtype=torch.uint8, device=dev)
+            nbc = torch.zeros(1, dtype=torch.int64, device=dev)
+            xh = torch.empty(xin.shape, dtype=torch.float32, device=dev)
+
+            def c_():
+                codec.compress_into(xin, ebv, oc, nbc, stream)
+
+            def d_():
+                codec.decompress_into(oc, capc, xh, stream)
+
+            c_()
+            d_()
+            torch.cuda.synchronize()
+            codec.check()
+            stc = codec.stats()
+            bnd = codec.error_bounds(Tc) if ebv is None else np.asarray(ebv, np.float32)
+            ok = True
+            for t0 in range(0, Tc, 4):   # |x - x^| <= eb_t, a few tables at a time in fp64
+                xs = xin[:, t0:t0 + 4].to(torch.float64)
+                e = (xs - xh[:, t0:t0 + 4].to(torch.float64)).abs().amax(dim=(0, 2)).cpu().numpy()
+                ok = ok and bool((e <= bnd[t0:t0 + 4].astype(np.float64)).all())
+                del xs
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+                   torch.cuda.Event(enable_timing=True)) for _ in range(nrep)]
+            for a, b_, c2 in ev:
+                flush.zero_()
+                a.record(stream)
+                c_()
+                b_.record(stream)
+                d_()
+                c2.record(stream)
+            torch.cuda.synchronize()
+            codec.check()
+            tc = sum(a.elapsed_time(b_) for a, b_, _ in ev) / 1e3 / nrep
+            td = sum(b_.elapsed_time(c2) for _, b_, c2 in ev) / 1e3 / nrep
+            kern = None
+            if prof_steps:
+                codec.set_profiling(True)
+                codec.profile()
+                for _ in range(prof_steps):
+                    flush.zero_()
+                    c_()
+                    d_()
+                pr = codec.profile()
+                codec.set_profiling(False)
+                tot = sum(v[1] for v in pr.values())
+                kern = {k: {"launches": v[0], "avg_us": round(1e3 * v[1] / v[0], 2), "share": round(v[1] / tot, 4)}
+                        for k, v in pr.items()}
+            del oc, xh
+            return tc, td, stc, kern, ok
+
+        def case_line(nbytes_in, tc, td, stc, kern, ok):
+            C2 = stc["out_bytes"]
+            return {"compress_gbs": round(nbytes_in / tc / 1e9, 1), "decompress_gbs": round(nbytes_in / td / 1e9, 1),
+                    "compression_ratio": round(nbytes_in / C2, 3), "out_bytes": C2,
+                    "n_literal": stc["n_literal"], "n_match": stc["n_match"], "n_outlier": stc["n_outlier"],
+                    "hbm_frac_compress": round((nbytes_in + C2) / tc / 1e9 / peak, 4),
+                    "hbm_frac_decompress": round((nbytes_in + C2) / td / 1e9 / peak, 4),
+                    "bound_held": ok, "kernels": kern}
+
+        configs = {}
+        wlb = workloads.make("bwd", device=dev, seed=rank)
+        r = run_case(wlb.x, wlb.eb.numpy(), max(3, min(K, 50)), max(3, min(K, 50)))
+        configs["bwd_gradients"] = {"shape": list(wlb.x.shape),
+                                    "workload": "per-row N(0,1e-4) x lookup count, Zipf(1.2); eb_t 1e-3..3e-2 "
+                                                "log-spaced", **case_line(4 * wlb.x.numel(), *r)}
+        del wlb
+        for variant in (None, "bf16"):
+            wll = workloads.make("large", device=dev, seed=rank, variant=variant)
+            r = run_case(wll.x, wll.eb.numpy(), 5, 5)
+            row = {"shape": list(wll.x.shape), "input_bytes": 4 * wll.x.numel(), **case_line(4 * wll.x.numel(), *r)}
+            if variant == "bf16":   # the same values read as bf16 (the cast is exact)
+                xb = wll.x.to(torch.bfloat16)
+                r2 = run_case(xb, wll.eb.numpy(), 5, 5)
+                row["native_bf16_input"] = {"input_bytes": 2 * xb.numel(), **case_line(4 * wll.x.numel(), *r2)}
+                del xb
+            configs["large_fp32" if variant is None else "large_bf16_cast"] = row
+            del wll
+        sweep = {"compress_gbs": [], "decompress_gbs": [], "compression_ratio": [], "eb_mean": [],
+                 "bound_held": True}
+        for it in range(100):
+            wls = workloads.make("sweep", iteration=it, device=dev, seed=rank)
+            sch = wls.schedule
+            codec.set_error_bounds(sch["base"].numpy(), sch["iteration"], sch["fn"], sch["m0"], sch["phase_len"],
+                                   sch["n_steps"])
+            tc, td, stc, _, ok = run_case(wls.x, None, 3, 0)
+            sweep["compress_gbs"].append(round(4 * wls.x.numel() / tc / 1e9, 1))
+            sweep["decompress_gbs"].append(round(4 * wls.x.numel() / td / 1e9, 1))
+            sweep["compression_ratio"].append(round(4 * wls.x.numel() / stc["out_bytes"], 3))
+            sweep["eb_mean"].append(float(np.format_float_scientific(codec.error_bounds(T).mean(), 4)))
+            sweep["bound_held"] = sweep["bound_held"] and ok
+            del wls
+        for k in ("compress_gbs", "decompress_gbs", "compression_ratio"):
+            sweep[k + "_median"] = float(np.median(sweep[k]))
+        sweep["workload"] = ("config-2 batch regenerated per iteration (seed = iteration, rows drifting N(0,1e-3) "
+                             "per step), eb decayed linearly 3e-2 -> 3e-3 by the context's schedule; 3 steps each")
+        configs["iteration_sweep"] = sweep
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
-        sample = workloads.make(WORKLOAD, batch=512)
-        rate, reps, _ = oracle_sample_rate(sample.x.numpy(), sample.eb.numpy(), args.cpu_seconds)
+        x_np = wl.x.cpu().numpy()
+        rate, reps, _, secs = oracle_rate(x_np, eb, args.cpu_seconds)
         cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-               "sample": f"first 512 of 8192 batch rows x 26 tables x 128 ({sample.nbytes} B), "
-                         f"compress+decompress repeated {reps}x"}
+               "sample": f"the whole batch [{B},{T},{D}] ({x_np.nbytes} B), compress+decompress repeated {reps}x "
+                         f"({secs:.1f} s)", **host_cpu()}
 
     if rank == 0:
         clocks = clk.summary()
@@ -574,10 +722,7 @@ def main():
             "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(1e3 * t_step / K, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "DLRM forward lookups [8192,26,128] fp32, 26 tables rows 1e3..1e6 log-uniform, "
-                                   "Zipf(1.05), eb_t=1e-2*range", "global_batch": B * world, "tables": T, "dim": D,
-                       "parallelism": f"replicas x{world}", "l2": "flushed before every step (2x L2 memset)",
-                       "radius": args.radius, "chunks": args.chunks},
+            "config": workload_config(B, T, D, world, args),
             "compress_gbs": round(job_throughput_gbs(world, K, N, t_c), 2),
             "decompress_gbs": round(job_throughput_gbs(world, K, N, t_d), 2),
             "compression_ratio": round(4 * N / C, 3),
@@ -596,6 +741,7 @@ def main():
             "bf16_input": bf16,
             "chunked": chunked,
             "wide_alphabet": wide,
+            "configs": configs,
             "clocks": clocks,
             "wall_s": round(wall, 3),
         }

@@ -15,7 +15,7 @@ using namespace ebc;
 // Per-kernel timing: a pool of CUDA event pairs recorded around each launch
 // while profiling is on; read back (and cleared) by ebc_get_profile.
 struct ebc::Prof {
-  static constexpr int kPairs = 2048;
+  static constexpr int kPairs = 8192;
   cudaEvent_t ev[2 * kPairs] = {};
   const char* name[kPairs] = {};
   int used = 0;
