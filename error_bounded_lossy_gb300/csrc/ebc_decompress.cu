@@ -215,27 +215,35 @@ struct DGeo {
   static constexpr int kWarpWords = 768;                              // bitstream words staged per warp
 };
 
-// The code of the next symbol in the bit window w0:w1 from bit pos, through
-// the first-level table (entries sym | len << kLenShift; the symbol field is 0
-// for the outlier symbol and for codes longer than the table, the slow cases)
-// and, for a long code, the canonical first-code search.  Returns the symbol;
-// *len receives the code length (1 and *bad = true for a bit pattern that is
-// no code).
+// A code longer than the first-level table, from the next 32 bits of the
+// stream (peek, MSB first).  With canonical codes the codes of each length are
+// consecutive and every shorter code sorts before every longer one, so with
+// the limits lim[l] = (first[l] + count[l]) << (24 - l) (codes left-aligned to
+// 24 bits, non-decreasing in l) the code's length is 12 plus the number of
+// lengths l = 12..24 with lim[l] <= the stream's first 24 bits; 25 means no code
+// (*bad, and *len = 1).  Returns the symbol.
 template <int W>
-__device__ __noinline__ uint32_t long_code(uint32_t peek, const uint32_t* s_first, const uint32_t* s_count,
+__device__ __forceinline__ uint32_t long_code(uint32_t peek, const uint32_t* s_lim, const uint32_t* s_first,
                                               const uint32_t* s_offset, const uint16_t* s_sorted, uint32_t* len,
                                               bool* bad) {
-#pragma unroll 1
-  for (int l = kLutBits + 1; l <= kLmax; ++l) {
-    const uint32_t code = peek >> (32 - l);
-    if (code - s_first[l] < s_count[l]) {
-      *len = (uint32_t)l;
-      return s_sorted[s_offset[l] + code - s_first[l]];
-    }
+  const uint32_t p24 = peek >> (32 - kLmax);
+  uint32_t l = kLutBits + 1;
+#pragma unroll
+  for (int k = kLutBits + 1; k <= kLmax; ++k) l += p24 >= s_lim[k] ? 1u : 0u;
+  if (l > (uint32_t)kLmax) {
+    *bad = true;
+    *len = 1u;
+    return 1u;
   }
-  *bad = true;
-  *len = 1u;
-  return 1u;
+  *len = l;
+  return s_sorted[s_offset[l] + (p24 >> (kLmax - l)) - s_first[l]];
+}
+
+// Chunks a warp of the decoder takes at a time: 32, or an even share of a
+// group's chunks over its warps when that is fewer.
+__device__ __forceinline__ uint32_t batch_chunks(uint32_t nchunks, int warps) {
+  const uint32_t share = (nchunks + (uint32_t)warps - 1u) / (uint32_t)warps;
+  return share < 1u ? 1u : (share > 32u ? 32u : share);
 }
 
 // ---------------------------------------------------------------------------
@@ -350,7 +358,13 @@ __global__ void __launch_bounds__(128) k_dec_tables(const uint8_t* __restrict__ 
       const uint32_t code = s_first[len] + rk[k];
       const uint32_t l0 = code << (kLutBits - len), n = 1u << (kLutBits - len);
       const uint16_t e = (uint16_t)(i | (len << kLenShift));
-      for (uint32_t q = 0; q < n; ++q) s_lut[l0 + q] = e;
+      if (n >= 8u) {   // 16-byte aligned runs of 8 entries (l0 is a multiple of n)
+        const uint32_t e2 = (uint32_t)e | ((uint32_t)e << 16);
+        uint4* p = reinterpret_cast<uint4*>(s_lut + l0);
+        for (uint32_t q = 0; q < n / 8u; ++q) p[q] = make_uint4(e2, e2, e2, e2);
+      } else {
+        for (uint32_t q = 0; q < n; ++q) s_lut[l0 + q] = e;
+      }
     }
   }
   __syncthreads();
@@ -372,7 +386,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   constexpr uint32_t kSymMask = (1u << kLenShift) - 1u;
   __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
   __shared__ uint16_t s_sorted[kA];
-  __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
+  __shared__ uint32_t s_first[kLmax + 1], s_offset[kLmax + 1], s_lim[kLmax + 1];
   __shared__ uint32_t s_recs[(G::kSPC + 1) * 4];      // the group's segment records and the one after
   __shared__ uint32_t s_bm[G::kSPC * G::kBmWords];    // the group's match bitmap words
   __shared__ uint16_t s_clen[G::kMaxChunks];          // the group's chunk lengths
@@ -421,9 +435,11 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
       reinterpret_cast<uint4*>(s_lut)[i] = __ldcg(reinterpret_cast<const uint4*>(dt->lut) + i);
     for (int i = tid; i < kA; i += kNT) s_sorted[i] = dt->sorted[i];
     if (tid <= kLmax) {
-      s_first[tid] = __ldcg(&dt->first[tid]);
-      s_count[tid] = __ldcg(&dt->count[tid]);
+      const uint32_t f = __ldcg(&dt->first[tid]), c = __ldcg(&dt->count[tid]);
+      s_first[tid] = f;
       s_offset[tid] = __ldcg(&dt->offset[tid]);
+      // (a Kraft sum of at most 1 keeps first + count <= 2^l: the limit fits 25 bits)
+      s_lim[tid] = tid ? (f + c) << (kLmax - tid) : 0u;
     }
     const int nrw = 4 * (nsg + (rec_end ? 0 : 1));
     for (int i = tid; i < nrw; i += kNT) {
@@ -445,7 +461,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     s_L = L;
     s_code = code;
     s_cnt[0] = s_cnt[1] = s_cnt[2] = 0u;
-    s_next = (uint32_t)G::kWarps * 32u;
+    s_grp[0] = 0u;
     if (tid == 0 && code == EBC_OK && have_unit) {
       // the group's chunk and word ranges, from its first record and the one after its last
       const uint32_t cb0 = nsg > 0 ? s_recs[1] : 0u, wb0 = nsg > 0 ? s_recs[0] : 0u;
@@ -462,6 +478,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
         s_grp[3] = (uint32_t)(wb1 - wb0);
       }
     }
+    s_next = (uint32_t)G::kWarps * batch_chunks(s_grp[0], G::kWarps);
   }
   __syncthreads();
   const Layout& L = s_L;   // read from shared memory where used
@@ -574,10 +591,12 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     auto value = [&](uint32_t sym) -> float {
       return __fmul_rn(__fsub_rn(__uint_as_float(0x4B400000u - (uint32_t)Alph<W>::kR + sym), 12582912.0f), ebx2);
     };
-    for (uint32_t b0 = (uint32_t)warp * 32u; b0 < nchunks;) {
+    // batches of up to 32 chunks, smaller when the group has few, so that every warp takes a share
+    const uint32_t bsz = batch_chunks(nchunks, G::kWarps);
+    for (uint32_t b0 = (uint32_t)warp * bsz; b0 < nchunks;) {
       // the batch's words (its chunks are consecutive, so their bits are too): staged in this warp's
       // buffer with coalesced 16-byte loads when they fit, else read from global memory
-      const uint32_t clast = min(b0 + 31u, nchunks - 1u);
+      const uint32_t clast = min(b0 + bsz - 1u, nchunks - 1u);
       const uint32_t wlo = (s_cbit[b0] >> 5) & ~3u;
       const uint32_t whi = min(((s_cbit[clast] + s_clen[clast]) >> 5) + 3u, gwords);   // exclusive; the window
                                                                                          // reads 2 words ahead
@@ -596,7 +615,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
           else return __ldg(gw + min(i, gwords - 1u));
         };
         const uint32_t c = b0 + lane;
-        const bool mine = c < nchunks;
+        const bool mine = (uint32_t)lane < bsz && c < nchunks;
         const uint32_t info = mine ? s_cinfo[c] : 0u;
         const uint32_t start = mine ? s_cbit[c] : s_cbit[b0];
         const uint32_t clen = mine ? (uint32_t)s_clen[c] : 0u;
@@ -650,7 +669,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
                   const uint32_t e = s_lut[peek >> (32 - kLutBits)];
                   uint32_t sym = e & kSymMask, len = e >> kLenShift;
                   if (sym == 0u && len == 0u)
-                    sym = long_code<W>(peek, s_first, s_count, s_offset, s_sorted, &len, &bad);
+                    sym = long_code<W>(peek, s_lim, s_first, s_offset, s_sorted, &len, &bad);
                   buf <<= len;
                   nb -= len;
                   float v = value(sym);
@@ -687,7 +706,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
       __syncwarp();   // the staged words are read before the next batch overwrites them
       // the next batch of 32 chunks of the group
       uint32_t nb = 0;
-      if (lane == 0) nb = atomicAdd(&s_next, 32u);
+      if (lane == 0) nb = atomicAdd(&s_next, bsz);
       b0 = __shfl_sync(0xffffffffu, nb, 0);
     }
   }
@@ -728,10 +747,19 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   }
   if (checked && s_code == EBC_OK && L.window && L.nseg > 0 && fail == EBC_OK) {
     // window references: every row's source (itself for a literal, b - distance for a match),
-    // from the unit's bitmap and one-byte distances, then the chains resolved to their literal
-    // roots (pointer jumping, CTA barriers between rounds)
-    __shared__ uint32_t s_wc[kNT / 32];
+    // from the unit's bitmap and one-byte distances, resolved to the literal roots of the chains.
+    // Rows go in blocks of kBlk: a block's sources are built in shared memory (the staging words
+    // are free now), a source in an earlier block is replaced by its final root (the last 256
+    // roots of the previous block are kept: a distance is at most 255), then the block's chains
+    // are resolved by pointer jumping in shared memory and its roots written out.
+    constexpr int kBlk = 2048, kBW = kBlk / 32;
+    static_assert(G::kWarps * G::kWarpWords >= kBlk + 256, "block and tail fit the staging words");
+    static_assert(kNT >= kBW && kBlk % kNT == 0 && 32 % (kBlk / kNT) == 0,
+                  "a thread per bitmap word of the block; each thread's run of rows inside one word");
+    __shared__ uint32_t s_wc[kNT / 32], s_bmw[kBW], s_pre[kBW];
     __shared__ int s_wbad;
+    uint32_t* s_blk = &s_ws[0][0];        // [kBlk] sources (absolute rows), then roots
+    uint32_t* s_tail = s_blk + kBlk;      // roots of the previous block's last 256 rows
     if (tid == 0) s_wbad = 0;
     const int64_t n = (int64_t)L.n, row0 = (int64_t)L.row0;
     const int64_t nw = L.nw;
@@ -740,55 +768,67 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     const uint32_t* srec = reinterpret_cast<const uint32_t*>(cin + L.off_seg);
     const unsigned long long mbase = srec[4ull * ((unsigned long long)t * L.nseg) + 2];
     uint32_t* src = w.srcrow + (size_t)t * sh.B + row0;
-    unsigned long long carry = 0;
+    unsigned long long carry = 0;   // matches of the unit before the block
     __syncthreads();
-    for (int64_t base = 0; base < nw; base += kNT) {
-      const int64_t wi = base + tid;
-      const uint32_t bm = wi < nw ? __ldcg(&bmt[wi]) : 0u;
+    for (int64_t bs = 0; bs < n; bs += kBlk) {
+      const int nb = (int)min((int64_t)kBlk, n - bs);
+      // the block's bitmap words and the matches before each
+      const int64_t wi = bs / 32 + tid;
+      const uint32_t bm = (tid < kBW && wi < nw) ? __ldcg(&bmt[wi]) : 0u;
       uint32_t wt;
-      const uint32_t in_warp = warp_excl((uint32_t)__popc(bm), &wt);
+      const uint32_t ex = warp_excl((uint32_t)__popc(bm), &wt);
       if (lane == 0) s_wc[warp] = wt;
       __syncthreads();
-      uint32_t before = 0, all = 0;
-      for (int k = 0; k < kNT / 32; ++k) {
-        if (k < warp) before += s_wc[k];
-        all += s_wc[k];
+      if (tid < kBW) {
+        uint32_t before = 0;
+        for (int k = 0; k < warp; ++k) before += s_wc[k];
+        s_bmw[tid] = bm;
+        s_pre[tid] = before + ex;
       }
+      uint32_t blk_matches = 0;
+      for (int k = 0; k < kNT / 32; ++k) blk_matches += s_wc[k];
       __syncthreads();
-      const unsigned long long rank0 = mbase + carry + before + in_warp;
-      if (wi < nw) {
-        for (int jj = 0; jj < 32; ++jj) {
-          const int64_t b = wi * 32 + jj;   // row of the slice
-          if (b >= n) break;
+      {   // sources: each thread a run of the block's rows
+        constexpr int kRun = kBlk / kNT;
+        const int i0 = tid * kRun;
+        const int wd = i0 >> 5;
+        const uint32_t bmv = s_bmw[wd];
+        const unsigned long long rk0 = mbase + carry + s_pre[wd];
+#pragma unroll 4
+        for (int jj = 0; jj < kRun; ++jj) {
+          const int i = i0 + jj;
+          if (i >= nb) break;
+          const int bit = i & 31;
+          const int64_t b = bs + i;   // row of the slice
           uint32_t from = (uint32_t)(row0 + b);
-          if ((bm >> jj) & 1u) {
-            const unsigned long long k = rank0 + __popc(bm & ((1u << jj) - 1u));
+          if ((bmv >> bit) & 1u) {
+            const unsigned long long k = rk0 + __popc(bmv & ((1u << bit) - 1u));
             const uint32_t d = k < L.n_match ? dist[k] : 0u;
-            if (d == 0u || d > L.window || (int64_t)d > b) s_wbad = 1;
-            else from = (uint32_t)(row0 + b - d);
+            if (d == 0u || d > L.window || (int64_t)d > b) {
+              s_wbad = 1;
+            } else {
+              const int64_t sb = b - d;
+              from = sb >= bs ? (uint32_t)(row0 + sb) : s_tail[sb - (bs - 256)];   // earlier block: its root
+            }
           }
-          src[b] = from;
+          s_blk[i] = from;
         }
       }
-      carry += all;
-    }
-    __syncthreads();
-    if (s_wbad) {
-      fail = EBC_ERR_CORRUPT;
-    } else {
-      int rounds = 1;
-      while ((1ll << rounds) < n) ++rounds;
-      for (int rd = 0; rd <= rounds; ++rd) {
-        for (int64_t b = tid; b < n; b += kNT) {
-          const uint32_t sv = src[b];
-          if (sv != (uint32_t)(row0 + b)) {
-            const uint32_t s2 = src[sv - row0];   // one step further (a literal points at itself)
-            if (s2 != sv) src[b] = s2;
-          }
+      carry += blk_matches;
+      __syncthreads();
+      for (int rd = 0; rd < 12; ++rd) {   // chains inside the block are shorter than 2^11
+        for (int i = tid; i < nb; i += kNT) {
+          const int64_t rel = (int64_t)s_blk[i] - row0 - bs;
+          if (rel >= 0 && rel < i) s_blk[i] = s_blk[rel];
         }
         __syncthreads();
       }
+      for (int i = tid; i < nb; i += kNT) src[bs + i] = s_blk[i];
+      if (nb == kBlk)
+        for (int j = tid; j < 256; j += kNT) s_tail[j] = s_blk[kBlk - 256 + j];
+      __syncthreads();
     }
+    if (s_wbad) fail = EBC_ERR_CORRUPT;
   }
   if (tid == 0) {
     if (fail != EBC_OK) dec_fail(g, epoch, fail);
