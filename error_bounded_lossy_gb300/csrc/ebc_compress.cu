@@ -286,8 +286,8 @@ template <int D, typename In>
 __device__ __forceinline__ void issue_segment_tile(In* stage, const CUtensorMap* map, uint64_t* bar, const Shape& sh,
                                                    int seg) {
   using Q = QGeo<D, In>;
-  const int t = seg / sh.qseg;
-  const int s = seg - t * sh.qseg;
+  const int s = seg / sh.T;   // segments go table-fastest: tiles in flight cover whole rows
+  const int t = seg - s * sh.T;
   unsigned long long first;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(first));
   mbar_expect_tx(bar, Q::kStageBytes);
@@ -345,8 +345,8 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
   for (int seg = blockIdx.x; seg < nsegT; seg += gridDim.x, ++i) {
     const int stg = i & 1;
     const In* xs = s_x + stg * Q::kStageFloats;
-    const int t = seg / sh.qseg;
-    const int s = seg - t * sh.qseg;
+    const int s = seg / sh.T;
+    const int t = seg - s * sh.T;
     const int64_t row0 = (int64_t)s * G::kSB;
     if (s == 0) {   // per-call accumulators of the table's units, which k_resolve adds to
       for (int r = 0; r < sh.R; ++r) {
@@ -417,8 +417,9 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
     const int total = nmine * G::kSB;   // a multiple of 32: a warp's rows lie in one segment
     for (int i = tid; i < total; i += 256) {
       const int seg = (int)blockIdx.x + (i / G::kSB) * (int)gridDim.x;
-      const int t = seg / sh.qseg;
-      const int64_t b = (int64_t)(seg - t * sh.qseg) * G::kSB + i % G::kSB;
+      const int st = seg / sh.T;
+      const int t = seg - st * sh.T;
+      const int64_t b = (int64_t)st * G::kSB + i % G::kSB;
       const bool valid = b < B && !(table_mode(w, t) & kModeNoDedup);
       // each slice keeps its own table: a row never refers into another slice
       const int u = valid ? slice_of_row(sh, b) * sh.T + t : 0;

@@ -405,8 +405,10 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = sh.T;
   const int ngrp = div_up(sh.nseg, G::kSPC) > 0 ? div_up(sh.nseg, G::kSPC) : 1;
-  const int u = (int)blockIdx.x / ngrp;               // unit: slice u / T, table u % T
-  const int grp = (int)blockIdx.x - u * ngrp;
+  // CTAs go unit-fastest, so the CTAs running at a time write whole rows of the output
+  const int nu = sh.U > 0 ? sh.U : 1;
+  const int grp = (int)blockIdx.x / nu;
+  const int u = (int)blockIdx.x - grp * nu;           // unit: slice u / T, table u % T
   const bool have_unit = u < sh.U;
   const int r = have_unit ? u / T : 0;
   const int t = have_unit ? u - r * T : 0;
@@ -887,8 +889,9 @@ __global__ void __launch_bounds__(kMatchThreads, 4) k_dec_match(const uint8_t* _
   const unsigned long long nbatch = (unsigned long long)sh.U * sh.nw;   // bitmap words of all units
   const unsigned long long wstep = (unsigned long long)gridDim.x * kNW;
   for (unsigned long long k = (unsigned long long)blockIdx.x * kNW + warp; k < nbatch; k += wstep) {
-    const int u = (int)(k / sh.nw);
-    const unsigned int wi = (unsigned int)(k - (unsigned long long)u * sh.nw);
+    // words go unit-fastest: the rows written at a time are whole rows of the output
+    const unsigned int wi = (unsigned int)(k / (unsigned long long)sh.U);
+    const int u = (int)(k - (unsigned long long)wi * sh.U);
     const int r = u / T, t = u - r * T;
     const MLay& Lc = s_lay[r];
     if (wi >= Lc.nw) continue;
