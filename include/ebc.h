@@ -142,7 +142,9 @@ typedef struct {
 } ebc_config;
 #define EBC_CONFIG_DEFAULT {128, 0, 24, 1, 0}
 
-/* Create a context on CUDA device `device` (must be sm_103) with options cfg
+/* A codec context ([EBLC] §III-E "Compressor Fine-tuning": the compressor's
+ * settings are fixed per context, §III-C: so is the bound schedule).
+ * Create a context on CUDA device `device` (must be sm_103) with options cfg
  * (host struct, read during the call; NULL = EBC_CONFIG_DEFAULT).  *out
  * receives the context; it is released with ebc_destroy.  Returns
  * EBC_ERR_INVALID_ARG for a bad cfg (checked first, without touching a
@@ -163,7 +165,9 @@ int ebc_set_error_bounds(ebc_ctx* ctx, const float* eb_base, int T, int64_t iter
 /* Copy the current scheduled bounds (T of them) into eb_out (host). */
 int ebc_get_error_bounds(const ebc_ctx* ctx, float* eb_out, int T);
 
-/* Worst-case container bytes for a [B,T,D] input coded with options cfg
+/* [EBLC] §III-A "Training Pipeline with Compression" (the sending buffer is
+ * sized before the variable-size output is known).
+ * Worst-case container bytes for a [B,T,D] input coded with options cfg
  * (NULL = EBC_CONFIG_DEFAULT; only its radius changes the bound); 0 for an
  * unsupported shape or a bad cfg.  Host-only. */
 uint64_t ebc_compress_bound(int64_t B, int T, int D, const ebc_config* cfg);
@@ -189,7 +193,10 @@ int ebc_set_radius(ebc_ctx* ctx, int radius);
 /* ebc_compress_bound for either radius (0 for another value). */
 uint64_t ebc_compress_bound_radius(int64_t B, int T, int D, int radius);
 
-/* Compress d_x[B][T][D] (device, fp32) with bounds eb[T] (host array; NULL =
+/* The compressor of [EBLC] §III-A "Training Pipeline with Compression" (before
+ * the all-to-all) with the hybrid design of §III-D: quantization encoder
+ * (no predictor, §III-B observation 1), vector-based LZ, Huffman encoder.
+ * Compress d_x[B][T][D] (device, fp32) with bounds eb[T] (host array; NULL =
  * the context's schedule) into d_out (device, out_capacity bytes).  The
  * container size is written to *d_out_bytes (device u64) by the kernels, also
  * when it exceeds out_capacity (then nothing beyond the fixed-size head of the
@@ -209,7 +216,10 @@ int ebc_compress(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D, const 
 int ebc_compress_bf16(ebc_ctx* ctx, const uint16_t* d_x, int64_t B, int T, int D, const float* eb,
                       void* d_out, uint64_t out_capacity, uint64_t* d_out_bytes, void* stream);
 
-/* Decompress a container (device, in_bytes bytes) made for the same B, T, D
+/* The decompressor of [EBLC] §III-A (after the all-to-all): the inverse of
+ * §III-D's encoders, chunk-parallel as in §III-E "Buffer Optimization" /
+ * Fig. 7 (bottom).
+ * Decompress a container (device, in_bytes bytes) made for the same B, T, D
  * into d_xhat[B][T][D] (device, fp32).  Asynchronous.  A container that fails
  * validation makes the kernels stop without writing out of bounds and records
  * EBC_ERR_CORRUPT (EBC_ERR_INVALID_ARG if its B, T, D differ from the
@@ -217,7 +227,7 @@ int ebc_compress_bf16(ebc_ctx* ctx, const uint16_t* d_x, int64_t B, int T, int D
 int ebc_decompress(ebc_ctx* ctx, const void* d_in, uint64_t in_bytes, float* d_xhat, int64_t B,
                    int T, int D, void* stream);
 
-/* Chunked sending buffer (§III-E "Buffer Optimization", Fig. 7; §IV-E,
+/* Chunked sending buffer (§III-E "Buffer Optimization", Fig. 7; §IV-D,
  * Fig. 15): the batch is split into n_chunks slices, one per destination rank
  * of the all-to-all, and every slice is coded as a container of its own, all
  * of them in one pass of the kernels and back to back in one buffer.  Slice r

@@ -268,7 +268,7 @@ def select_modes(cr, tc, td, bw: float):
 def chunk_rows(B: int, n_chunks: int):
     """Row ranges [b0, b1) of the n_chunks slices of a batch of B rows.
 
-    §III-E "Buffer Optimization" and §IV-E: the batch is split equally into
+    §III-E "Buffer Optimization" and §IV-D: the batch is split equally into
     one slice per destination rank of the all-to-all.  Where B is not a
     multiple of n_chunks, the first B % n_chunks slices take one row more
     (slices past B are empty)."""

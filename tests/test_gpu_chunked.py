@@ -1,6 +1,6 @@
 """Chunked sending buffer on the GPU against the oracle ("Accelerating
 Communication in Deep Learning Recommendation Model Training with Dual-Level
-Adaptive Lossy Compression", §III-E "Buffer Optimization", Fig. 7; §IV-E,
+Adaptive Lossy Compression", §III-E "Buffer Optimization", Fig. 7; §IV-D,
 Fig. 15): one self-contained container per batch slice, all written by one
 pass of the kernels, and all decoded by one pass.
 

@@ -1,6 +1,6 @@
 """Pins of the oracle's chunked sending buffer ("Accelerating Communication in
 Deep Learning Recommendation Model Training with Dual-Level Adaptive Lossy
-Compression", §III-E "Buffer Optimization", Fig. 7; §IV-E, Fig. 15): the
+Compression", §III-E "Buffer Optimization", Fig. 7; §IV-D, Fig. 15): the
 batch is split equally into one slice per destination rank, each slice is
 compressed as a container of its own, and the containers lie back to back in
 one buffer.  Pinned against numpy's array_split (the slice boundaries), hand
