@@ -195,7 +195,6 @@ static Work carve_decompress(void* buf, const Shape& sh, Glob* g, size_t* total,
   w.uacc = c.take<uint4>(16 * (size_t)(sh.U > 0 ? sh.U : 1));
   w.cacc = c.take<uint2>(8 * (size_t)sh.R);
   if (acc_bytes) *acc_bytes = c.off;
-  w.dtab = c.take<DTab>(sizeof(DTab) * (size_t)(sh.U > 0 ? sh.U : 1));
   w.lay = c.take<Layout>(sizeof(Layout) * (size_t)sh.R);
   w.srcrow = c.take<uint32_t>(4 * (size_t)sh.B * (size_t)sh.T);
   w.glob = g;

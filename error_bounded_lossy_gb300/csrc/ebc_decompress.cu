@@ -10,7 +10,9 @@
 //                sections it reads first sit at offsets that follow from the
 //                shape, so the header, the unit's code lengths, the group's
 //                segment records and match bitmap are all loaded at once (the
-//                header check confirms those offsets), then the chunk lengths
+//                header check confirms those offsets; CTA 0 also checks every
+//                container's header in order and reports the first failure,
+//                as the in-order decode does), then the chunk lengths
 //                and the group's bitstream (staged in shared memory when it
 //                fits).  The CTA builds the unit's canonical decode tables,
 //                the literal rows and chunk start bits of its segments, and
@@ -247,132 +249,6 @@ __device__ __forceinline__ uint32_t batch_chunks(uint32_t nchunks, int warps) {
 }
 
 // ---------------------------------------------------------------------------
-// k_dec_tables: grid U (at least 1), 128 threads.  Checks every container's
-// header (CTA 0: all of them, and one window for all; each CTA: its unit's),
-// and builds each unit's canonical decode tables once, from the code lengths of
-// its table record (lengths at most 24, a Kraft sum of at most 1, a usable
-// bound): the 2^11-entry first-level table (sym | len << shift; symbol field 0
-// for the outlier symbol and for the prefixes of longer codes), the first code,
-// count and sorted-table offset of each length, the symbols in canonical
-// order, and the reconstruction value of each symbol.  The decode CTAs copy
-// them into shared memory.
-// ---------------------------------------------------------------------------
-template <int W>
-__global__ void __launch_bounds__(128) k_dec_tables(const uint8_t* __restrict__ in, unsigned long long in_bytes,
-                                                    const unsigned long long* __restrict__ offs, Shape sh, Work w,
-                                                    uint32_t epoch) {
-  pdl_enter();
-  constexpr int kA = Alph<W>::kA, kNT = 128, kPer = kA / kNT;
-  constexpr int kLenShift = Alph<W>::kLenShift;
-  __shared__ __align__(16) uint16_t s_lut[1 << kLutBits];
-  __shared__ uint32_t s_len[kA / 4];
-  __shared__ uint32_t s_first[kLmax + 1], s_count[kLmax + 1], s_offset[kLmax + 1];
-  __shared__ uint32_t s_wcnt[(kNT / 32) * (kLmax + 1)], s_run[kLmax + 1];
-  __shared__ uint32_t s_rec[4];
-  __shared__ int s_code;
-  Glob* g = w.glob;
-  const int tid = threadIdx.x, lane = tid & 31;
-  const int u = blockIdx.x;
-  const bool have_unit = u < sh.U;
-  const int T = sh.T;
-  const int r = have_unit ? u / T : 0, t = have_unit ? u - r * T : 0;
-  // one round of loads: the record (eb and code lengths) at the offset the shape gives (skipped outside
-  // the container; its header then fails the check), and the header
-  const unsigned long long lo = offs ? offs[r] : 0ull, hi = offs ? offs[r + 1] : in_bytes;
-  const unsigned long long size = (lo & 15ull) == 0ull && lo <= hi && hi <= in_bytes ? hi - lo : 0ull;
-  const uint8_t* rec = in + lo + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
-  const bool rec_in = have_unit && kHeaderBytes + (unsigned long long)(t + 1) * Alph<W>::kRecBytes <= size;
-  if (tid < 4) s_rec[tid] = rec_in ? ld32(rec + 4 * tid) : 0u;
-  for (int i = tid; i < kA / 4; i += kNT) s_len[i] = rec_in ? ld32(rec + 16 + 4 * i) : 0u;
-  for (int i = tid; i < (1 << kLutBits) / 8; i += kNT) reinterpret_cast<uint4*>(s_lut)[i] = make_uint4(0, 0, 0, 0);
-  if (tid <= kLmax) s_count[tid] = 0u;
-  if (tid == 0) {
-    // CTA 0 checks the containers in order and reports the first failure (the code the in-order
-    // decode of the containers meets first); a CTA whose own container fails stops silently
-    if (blockIdx.x == 0) {
-      const int all = check_all_headers(in, in_bytes, offs, sh, g, EBC_OK, nullptr);
-      if (all != EBC_OK) dec_fail(g, epoch, all);
-    }
-    Layout L{};
-    s_code = have_unit ? container_layout(in, in_bytes, offs, sh, r, &L) : EBC_OK;
-    if (have_unit && t == 0 && s_code == EBC_OK) w.lay[r] = L;   // for the decode CTAs: no second parse
-  }
-  __syncthreads();
-  if (s_code != EBC_OK || !have_unit) return;
-  bool bad = false;
-  for (int i = tid; i < kA; i += kNT) {
-    const uint32_t len = (s_len[i >> 2] >> (8 * (i & 3))) & 0xffu;
-    if (len > (uint32_t)kLmax) bad = true;
-    else if (len) atomicAdd(&s_count[len], 1u);
-  }
-  if (bad) s_code = EBC_ERR_CORRUPT;
-  __syncthreads();
-  if (tid < 32) {
-    // lane l (1..24): the Kraft term of length l, the first canonical code of length l
-    // (sum over k < l of count[k] << (l - k)), and its offset in sorted[] (the counts below l)
-    const int l = lane;
-    const uint32_t cnt = l >= 1 && l <= kLmax ? s_count[l] : 0u;
-    unsigned long long kraft = l >= 1 && l <= kLmax ? (unsigned long long)cnt << (kLmax - l) : 0ull;
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) kraft += __shfl_xor_sync(0xffffffffu, kraft, off);
-    unsigned long long first = 0;
-    uint32_t below = 0;
-    for (int k = 1; k < l && k <= kLmax; ++k) {
-      first += (unsigned long long)s_count[k] << (l - k);
-      below += s_count[k];
-    }
-    if (l <= kLmax) {
-      s_first[l] = l ? (uint32_t)first : 0u;
-      s_offset[l] = l ? below : 0u;
-    }
-    if (lane == 0 && (kraft > (1ull << kLmax) || !eb_usable(__uint_as_float(s_rec[0])))) s_code = EBC_ERR_CORRUPT;
-  }
-  __syncthreads();
-  if (s_code != EBC_OK) {
-    if (tid == 0) dec_fail(g, epoch, EBC_ERR_CORRUPT);
-    return;
-  }
-  DTab* dt = w.dtab + u;
-  const float ebx2 = __fmul_rn(2.0f, __uint_as_float(s_rec[0]));
-  for (int i = tid; i < kA; i += kNT) dt->val[i] = __fmul_rn((float)(i - Alph<W>::kR), ebx2);
-  if (tid <= kLmax) {
-    dt->first[tid] = s_first[tid];
-    dt->count[tid] = tid ? s_count[tid] : 0u;
-    dt->offset[tid] = s_offset[tid];
-  }
-  // each symbol's rank among the symbols of its length below it: its index in sorted[] is
-  // offset[len] + rank, its code first[len] + rank
-  uint32_t lens[kPer], rk[kPer];
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const int i = k * kNT + tid;
-    lens[k] = (s_len[i >> 2] >> (8 * (i & 3))) & 0xffu;
-  }
-  ranks_by_length<kPer, kNT>(lens, rk, s_wcnt, s_run);
-#pragma unroll
-  for (int k = 0; k < kPer; ++k) {
-    const uint32_t len = lens[k], i = (uint32_t)(k * kNT + tid);
-    if (!len) continue;
-    dt->sorted[s_offset[len] + rk[k]] = (uint16_t)i;
-    if (len <= (uint32_t)kLutBits) {
-      const uint32_t code = s_first[len] + rk[k];
-      const uint32_t l0 = code << (kLutBits - len), n = 1u << (kLutBits - len);
-      const uint16_t e = (uint16_t)(i | (len << kLenShift));
-      if (n >= 8u) {   // 16-byte aligned runs of 8 entries (l0 is a multiple of n)
-        const uint32_t e2 = (uint32_t)e | ((uint32_t)e << 16);
-        uint4* p = reinterpret_cast<uint4*>(s_lut + l0);
-        for (uint32_t q = 0; q < n / 8u; ++q) p[q] = make_uint4(e2, e2, e2, e2);
-      } else {
-        for (uint32_t q = 0; q < n; ++q) s_lut[l0 + q] = e;
-      }
-    }
-  }
-  __syncthreads();
-  for (int i = tid; i < (1 << kLutBits) / 8; i += kNT)
-    reinterpret_cast<uint4*>(dt->lut)[i] = reinterpret_cast<const uint4*>(s_lut)[i];
-}
-
-// ---------------------------------------------------------------------------
 // k_dec_lit: grid U * G (G groups of kSPC segments per unit), 128 threads.
 // ---------------------------------------------------------------------------
 template <int D, int W>
@@ -401,6 +277,8 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   __shared__ uint32_t s_cnt[3];                       // literals, matches, outliers of the CTA
   __shared__ uint32_t s_next;                         // next batch of 32 chunks
   __shared__ uint32_t s_rec[4];                       // the unit's table record head: eb, lit, match, out
+  __shared__ uint32_t s_len[kA / 4];                  // the unit's code lengths (a byte each)
+  __shared__ uint32_t s_count[kLmax + 1], s_wcnt[(kNT / 32) * (kLmax + 1)], s_run[kLmax + 1];
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = sh.T;
@@ -431,18 +309,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     const uint8_t* rec = cin + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
     const bool rec_in = kHeaderBytes + (unsigned long long)(t + 1) * Alph<W>::kRecBytes <= size;
     if (tid < 4) s_rec[tid] = rec_in ? ld32(rec + 4 * tid) : 0u;
-    // the unit's decode tables (built by k_dec_tables; used only if its checks passed)
-    const DTab* dt = w.dtab + u;
-    for (int i = tid; i < (1 << kLutBits) / 8; i += kNT)
-      reinterpret_cast<uint4*>(s_lut)[i] = __ldcg(reinterpret_cast<const uint4*>(dt->lut) + i);
-    for (int i = tid; i < kA; i += kNT) s_sorted[i] = dt->sorted[i];
-    if (tid <= kLmax) {
-      const uint32_t f = __ldcg(&dt->first[tid]), c = __ldcg(&dt->count[tid]);
-      s_first[tid] = f;
-      s_offset[tid] = __ldcg(&dt->offset[tid]);
-      // (a Kraft sum of at most 1 keeps first + count <= 2^l: the limit fits 25 bits)
-      s_lim[tid] = tid ? (f + c) << (kLmax - tid) : 0u;
-    }
+    for (int i = tid; i < kA / 4; i += kNT) s_len[i] = rec_in ? ld32(rec + 16 + 4 * i) : 0u;
     const int nrw = 4 * (nsg + (rec_end ? 0 : 1));
     for (int i = tid; i < nrw; i += kNT) {
       const unsigned long long o = off_seg + rec0 * kSegRecBytes + 4ull * i;
@@ -454,12 +321,19 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
       s_bm[i] = wi < nw_r && o + 4 <= size ? ld32(cin + o) : 0u;
     }
   }
+  for (int i = tid; i < (1 << kLutBits) / 8; i += kNT) reinterpret_cast<uint4*>(s_lut)[i] = make_uint4(0, 0, 0, 0);
+  if (tid <= kLmax) s_count[tid] = 0u;
   if (tid == 0) {
-    // the headers and tables were checked by k_dec_tables, which left each container's layout in the
-    // scratch: after a failure there (already recorded, code -1) the CTA only takes part in the unit's
-    // counters
-    const int code = dec_aborted(g, epoch) ? -1 : EBC_OK;
-    const Layout L = have_unit && code == EBC_OK ? w.lay[r] : Layout{};
+    // CTA 0 checks the containers in order and reports the first failure (the code the in-order
+    // decode of the containers meets first); a CTA whose own container fails stops silently (code -1)
+    // and only takes part in the unit's counters
+    if (blockIdx.x == 0) {
+      const int all = check_all_headers(in, in_bytes, offs, sh, g, EBC_OK, nullptr);
+      if (all != EBC_OK) dec_fail(g, epoch, all);
+    }
+    Layout L{};
+    const int code = have_unit ? (container_layout(in, in_bytes, offs, sh, r, &L) == EBC_OK ? EBC_OK : -1) : EBC_OK;
+    if (have_unit && t == 0 && grp == 0 && code == EBC_OK) w.lay[r] = L;   // for the match copy
     s_L = L;
     s_code = code;
     s_cnt[0] = s_cnt[1] = s_cnt[2] = 0u;
@@ -484,6 +358,75 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   }
   __syncthreads();
   const Layout& L = s_L;   // read from shared memory where used
+
+  // ---- the unit's canonical decode tables, from its code lengths: lengths at most 24, a Kraft sum of
+  //      at most 1 and a usable bound, else the container is corrupt ----
+  if (s_code == EBC_OK && have_unit) {
+    bool bad = false;
+    for (int i = tid; i < kA; i += kNT) {
+      const uint32_t len = (s_len[i >> 2] >> (8 * (i & 3))) & 0xffu;
+      if (len > (uint32_t)kLmax) bad = true;
+      else if (len) atomicAdd(&s_count[len], 1u);
+    }
+    if (bad) s_code = EBC_ERR_CORRUPT;   // (benign race: any writer stores the same value)
+    __syncthreads();
+    if (tid < 32) {
+      // lane l (1..24): the Kraft term of length l, the first canonical code of length l (sum over
+      // k < l of count[k] << (l - k)), its offset in sorted[] (the counts below l), and the limit
+      // (first + count) << (24 - l) of the long-code search
+      const int l = lane;
+      const uint32_t cnt = l >= 1 && l <= kLmax ? s_count[l] : 0u;
+      unsigned long long kraft = l >= 1 && l <= kLmax ? (unsigned long long)cnt << (kLmax - l) : 0ull;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) kraft += __shfl_xor_sync(0xffffffffu, kraft, off);
+      unsigned long long first = 0;
+      uint32_t below = 0;
+      for (int k = 1; k < l && k <= kLmax; ++k) {
+        first += (unsigned long long)s_count[k] << (l - k);
+        below += s_count[k];
+      }
+      if (l <= kLmax) {
+        s_first[l] = l ? (uint32_t)first : 0u;
+        s_offset[l] = l ? below : 0u;
+        // (a Kraft sum of at most 1 keeps first + count <= 2^l: the limit fits 25 bits)
+        s_lim[l] = l ? (uint32_t)((first + cnt) << (kLmax - l)) : 0u;
+      }
+      if (lane == 0 && (kraft > (1ull << kLmax) || !eb_usable(__uint_as_float(s_rec[0])))) s_code = EBC_ERR_CORRUPT;
+    }
+    __syncthreads();
+    if (s_code == EBC_OK) {
+      // each symbol's rank among the symbols of its length below it: its index in sorted[] is
+      // offset[len] + rank, its code first[len] + rank
+      constexpr int kPer = kA / kNT;
+      constexpr int kLenShiftT = Alph<W>::kLenShift;
+      uint32_t lens[kPer], rk[kPer];
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const int i = k * kNT + tid;
+        lens[k] = (s_len[i >> 2] >> (8 * (i & 3))) & 0xffu;
+      }
+      ranks_by_length<kPer, kNT>(lens, rk, s_wcnt, s_run);
+#pragma unroll
+      for (int k = 0; k < kPer; ++k) {
+        const uint32_t len = lens[k], i = (uint32_t)(k * kNT + tid);
+        if (!len) continue;
+        s_sorted[s_offset[len] + rk[k]] = (uint16_t)i;
+        if (len <= (uint32_t)kLutBits) {
+          const uint32_t code = s_first[len] + rk[k];
+          const uint32_t l0 = code << (kLutBits - len), n = 1u << (kLutBits - len);
+          const uint16_t e = (uint16_t)(i | (len << kLenShiftT));
+          if (n >= 8u) {   // 16-byte aligned runs of 8 entries (l0 is a multiple of n)
+            const uint32_t e2 = (uint32_t)e | ((uint32_t)e << 16);
+            uint4* p = reinterpret_cast<uint4*>(s_lut + l0);
+            for (uint32_t q = 0; q < n / 8u; ++q) p[q] = make_uint4(e2, e2, e2, e2);
+          } else {
+            for (uint32_t q = 0; q < n; ++q) s_lut[l0 + q] = e;
+          }
+        }
+      }
+    }
+    __syncthreads();
+  }
   bool ok = s_code == EBC_OK && have_unit;
 
   // ---- second round: the chunk lengths ----
@@ -879,7 +822,7 @@ __global__ void __launch_bounds__(kMatchThreads, 4) k_dec_match(const uint8_t* _
   if (tid == 0) s_abort = dec_aborted(g, epoch);
   __syncthreads();
   if (s_abort) return;
-  for (int c = tid; c < sh.R; c += kMatchThreads) {   // the containers' layouts, as k_dec_tables checked them
+  for (int c = tid; c < sh.R; c += kMatchThreads) {   // the containers' layouts, as k_dec_lit checked them
     const Layout Lc = w.lay[c];
     s_lay[c] = MLay{Lc.base, Lc.off_bitmap, Lc.off_refs, Lc.off_seg, Lc.row0, (unsigned int)Lc.n, Lc.nseg, Lc.nw,
                     Lc.ref_bytes, Lc.window};
@@ -965,9 +908,6 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
   using G = DGeo<D>;
   const unsigned ngrp = (unsigned)(div_up(sh.nseg, G::kSPC) > 0 ? div_up(sh.nseg, G::kSPC) : 1);
   const unsigned grid = sh.U > 0 ? (unsigned)sh.U * ngrp : 1u;
-  prof_begin(prof, "k_dec_tables", st);
-  launch_k(k_dec_tables<W>, (unsigned)(sh.U > 0 ? sh.U : 1), 128, 0, st, in, in_bytes, offs, sh, w, epoch);
-  prof_end(prof, st);
   prof_begin(prof, "k_dec_lit", st);
   launch_k(k_dec_lit<D, W>, grid, G::kThreads, 0, st, in, in_bytes, offs, sh, w, xhat, epoch);
   prof_end(prof, st);

@@ -160,18 +160,6 @@ struct Glob {
   unsigned long long off_seg, off_bitmap, off_chunks, off_refs, off_bits, total;
 };
 
-// Decode tables of one unit, built once per call by the decoder's first kernel
-// (16-byte aligned: the first-level table is copied with 16-byte accesses).
-struct __align__(16) DTab {
-  uint16_t lut[1 << kLutBits];   // sym | len << kLenShift for codes of at most kLutBits bits (sym 0 and len 0:
-                                 // a longer code's prefix)
-  float val[kMaxSyms];           // reconstruction of each symbol
-  uint16_t sorted[kMaxSyms];     // symbols in canonical order (by length, then symbol)
-  uint32_t first[kLmax + 1];     // first code of each length
-  uint32_t count[kLmax + 1];     // codes of each length
-  uint32_t offset[kLmax + 1];    // index in sorted[] of each length's first code
-};
-
 // Device scratch of a context.  Sizes follow Shape.
 struct Work {
   const uint8_t* modes;        // [T] per-table modes, or null (all 0)
@@ -199,7 +187,6 @@ struct Work {
   uint4* uacc;                 // [U] per-unit accumulators {literals, matches, outliers, arrived CTAs}, zero
                                //   between calls (the last CTA of each unit empties its own)
   uint2* cacc;                 // [R] per-container accumulators {outliers, arrived units}, zero between calls
-  DTab* dtab;                  // [U] decode tables
   Layout* lay;                 // [R] each container's section layout, as the decoder's header check found it
   uint32_t* srcrow;            // [T][B] windowed containers: each row's source row (itself for a literal)
   Glob* glob;

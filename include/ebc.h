@@ -392,10 +392,11 @@ int ebc_table_homo_index(ebc_ctx* ctx, const float* d_x, int64_t B, int T, int D
  * Host-side errors: EBC_ERR_INVALID_ARG (bad shape or pointer),
  * EBC_ERR_NO_DEVICE (the current device is not sm_103), EBC_ERR_CUDA, and
  * EBC_ERR_SCRATCH_LIMIT when the shape's scratch does not fit the 16 MiB,
- * in which case nothing is launched.  The scratch is about 4*B*T + 10.3 KB*T
- * bytes (the row-source table of windowed containers, per-table decode tables
- * and counters, after a 256-byte status block); [8192, 26, 128] needs about
- * 1.1 MB, and shapes of up to about 4 M rows B*T fit.
+ * in which case nothing is launched.  The scratch is about 4*B*T + 16*T bytes
+ * (the row-source table of windowed containers and per-table counters, with
+ * the containers' checked layouts, after a 256-byte status block);
+ * [8192, 26, 128] needs about 0.85 MB, and shapes of up to about 4 M rows B*T
+ * fit.
  * Every call shares the one array per device, and each call clears its status
  * block and counters first: calls whose work overlaps on the GPU (from several host
  * threads, or on several streams) race and must be serialised by the caller. */
