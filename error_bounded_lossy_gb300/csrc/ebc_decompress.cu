@@ -278,6 +278,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   __shared__ uint32_t s_next;                         // next batch of 32 chunks
   __shared__ uint32_t s_rec[4];                       // the unit's table record head: eb, lit, match, out
   __shared__ uint32_t s_len[kA / 4];                  // the unit's code lengths (a byte each)
+  __shared__ int s_tbad;                              // the code lengths or the bound are unusable
   __shared__ uint32_t s_count[kLmax + 1], s_wcnt[(kNT / 32) * (kLmax + 1)], s_run[kLmax + 1];
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -324,6 +325,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   for (int i = tid; i < (1 << kLutBits) / 8; i += kNT) reinterpret_cast<uint4*>(s_lut)[i] = make_uint4(0, 0, 0, 0);
   if (tid <= kLmax) s_count[tid] = 0u;
   if (tid == 0) {
+    s_tbad = 0;
     // CTA 0 checks the containers in order and reports the first failure (the code the in-order
     // decode of the containers meets first); a CTA whose own container fails stops silently (code -1)
     // and only takes part in the unit's counters
@@ -359,16 +361,24 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   __syncthreads();
   const Layout& L = s_L;   // read from shared memory where used
 
+  // whether the tables are built: read once here (s_code changes only after the barriers below)
+  const bool build = s_code == EBC_OK && have_unit;
+  // ---- second round: the chunk lengths (in flight while the tables are built) ----
+  if (build) {
+    const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + L.off_chunks) + s_grp[1];
+    for (uint32_t i = tid; i < s_grp[0]; i += kNT) s_clen[i] = cl[i];
+  }
+
   // ---- the unit's canonical decode tables, from its code lengths: lengths at most 24, a Kraft sum of
   //      at most 1 and a usable bound, else the container is corrupt ----
-  if (s_code == EBC_OK && have_unit) {
+  if (build) {
     bool bad = false;
     for (int i = tid; i < kA; i += kNT) {
       const uint32_t len = (s_len[i >> 2] >> (8 * (i & 3))) & 0xffu;
       if (len > (uint32_t)kLmax) bad = true;
       else if (len) atomicAdd(&s_count[len], 1u);
     }
-    if (bad) s_code = EBC_ERR_CORRUPT;   // (benign race: any writer stores the same value)
+    if (bad) s_tbad = 1;   // (benign race: any writer stores the same value)
     __syncthreads();
     if (tid < 32) {
       // lane l (1..24): the Kraft term of length l, the first canonical code of length l (sum over
@@ -391,10 +401,10 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
         // (a Kraft sum of at most 1 keeps first + count <= 2^l: the limit fits 25 bits)
         s_lim[l] = l ? (uint32_t)((first + cnt) << (kLmax - l)) : 0u;
       }
-      if (lane == 0 && (kraft > (1ull << kLmax) || !eb_usable(__uint_as_float(s_rec[0])))) s_code = EBC_ERR_CORRUPT;
+      if (lane == 0 && (kraft > (1ull << kLmax) || !eb_usable(__uint_as_float(s_rec[0])))) s_tbad = 1;
     }
     __syncthreads();
-    if (s_code == EBC_OK) {
+    if (!s_tbad) {
       // each symbol's rank among the symbols of its length below it: its index in sorted[] is
       // offset[len] + rank, its code first[len] + rank
       constexpr int kPer = kA / kNT;
@@ -425,16 +435,10 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
         }
       }
     }
+    if (tid == 0 && s_tbad) s_code = EBC_ERR_CORRUPT;
     __syncthreads();
   }
   bool ok = s_code == EBC_OK && have_unit;
-
-  // ---- second round: the chunk lengths ----
-  if (ok) {
-    const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + L.off_chunks) + s_grp[1];
-    for (uint32_t i = tid; i < s_grp[0]; i += kNT) s_clen[i] = cl[i];
-    __syncthreads();
-  }
 
   // ---- the group's segments: literal rows, chunk start bits, chain checks (a warp per segment) ----
   uint32_t nchunks = 0;
