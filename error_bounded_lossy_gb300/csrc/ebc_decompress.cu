@@ -10,9 +10,9 @@
 //                sections it reads first sit at offsets that follow from the
 //                shape, so the header, the unit's code lengths, the group's
 //                segment records and match bitmap are all loaded at once (the
-//                header check confirms those offsets; CTA 0 also checks every
-//                container's header in order and reports the first failure,
-//                as the in-order decode does), then the chunk lengths
+//                header check confirms those offsets; the last CTA also checks
+//                every container's header in order and reports the first
+//                failure, as the in-order decode does), then the chunk lengths
 //                and the group's bitstream (staged in shared memory when it
 //                fits).  The CTA builds the unit's canonical decode tables,
 //                the literal rows and chunk start bits of its segments, and
@@ -326,10 +326,11 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   if (tid <= kLmax) s_count[tid] = 0u;
   if (tid == 0) {
     s_tbad = 0;
-    // CTA 0 checks the containers in order and reports the first failure (the code the in-order
-    // decode of the containers meets first); a CTA whose own container fails stops silently (code -1)
-    // and only takes part in the unit's counters
-    if (blockIdx.x == 0) {
+    // the grid's last CTA (the batch's last rows: mostly matches, little to decode) checks the
+    // containers in order and reports the first failure (the code the in-order decode of the
+    // containers meets first); a CTA whose own container fails stops silently (code -1) and only takes
+    // part in the unit's counters
+    if (blockIdx.x == gridDim.x - 1) {
       const int all = check_all_headers(in, in_bytes, offs, sh, g, EBC_OK, nullptr);
       if (all != EBC_OK) dec_fail(g, epoch, all);
     }
