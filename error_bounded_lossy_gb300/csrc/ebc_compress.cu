@@ -153,6 +153,24 @@ __device__ __forceinline__ uint32_t sm_quad(const uint32_t* s, int i, uint32_t*)
 __device__ __forceinline__ uint2 sm_quad(const uint32_t* s, int i, uint2*) {
   return *reinterpret_cast<const uint2*>(s + i);
 }
+// Code c of 16 bytes of codes (W bytes each), and whether one of them is 0.
+template <int W>
+__device__ __forceinline__ uint32_t v4_code(const uint4& v, int c) {
+  constexpr int kPerWord = 4 / W;
+  const int k = c / kPerWord;
+  const uint32_t x = k == 0 ? v.x : (k == 1 ? v.y : (k == 2 ? v.z : v.w));
+  return (x >> (8 * W * (c % kPerWord))) & (W == 1 ? 0xffu : 0xffffu);
+}
+template <int W>
+__device__ __forceinline__ bool v4_has_zero(const uint4& v) {
+  if constexpr (W == 1)
+    return quad_has_zero(v.x) || quad_has_zero(v.y) || quad_has_zero(v.z) || quad_has_zero(v.w);
+  else
+    return quad_has_zero(make_uint2(v.x, v.y)) || quad_has_zero(make_uint2(v.z, v.w));
+}
+__device__ __forceinline__ bool v4_eq(const uint4& a, const uint4& b) {
+  return ((a.x ^ b.x) | (a.y ^ b.y) | (a.z ^ b.z) | (a.w ^ b.w)) == 0u;
+}
 
 // Input element types: fp32, or bf16 carried as its 16 raw bits (its fp32
 // value is exact: the bf16 bits followed by 16 zero bits).
@@ -440,7 +458,11 @@ __global__ void __launch_bounds__(256) k_quantize(const __grid_constant__ CUtens
 // occurrence as reference (§III-D, §III-E "fixed pattern length"): row b is a
 // match when the first row with its key precedes it and carries the same codes
 // and the same raw bits at outliers; otherwise a literal (a key collision is a
-// literal too).  Literal codes feed the segment and table histograms.
+// literal too).  Literal codes feed the segment and table histograms.  Rows
+// of 16 bytes or more are compared 16 bytes per lane (a warp step covers
+// 32 * 16 bytes of rows), and the literal rows are listed; their codes then go
+// into the warp's histogram in a second pass.  Shorter rows are compared and
+// counted in one pass, four codes per lane.
 // ---------------------------------------------------------------------------
 constexpr int kResolveThreads = 64;   // two warps per segment: many segments in flight per SM
 
@@ -463,6 +485,15 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   __shared__ uint32_t s_ref[G::kSB];
   __shared__ uint32_t s_bm[G::kBmWords];
   __shared__ uint32_t s_cnt[3];
+  // rows of 16 bytes or more: the match test takes 16 bytes of codes per lane
+  constexpr bool kWide = D * W >= 16;
+  constexpr int kRU = kWide ? D * W / 16 : 1;          // 16-byte pieces of a row
+  constexpr int kLPV = kRU < 32 ? kRU : 32;            // lanes per row
+  constexpr int kUPL = kRU / kLPV;                     // pieces per lane
+  constexpr int kRPV = 32 / kLPV;                      // rows per warp step
+  constexpr int kStepsV = G::kSB / kNW / kRPV;         // warp steps per warp
+  constexpr int kGV = kStepsV < 4 ? kStepsV : 4;       // steps whose loads are issued together
+  __shared__ uint16_t s_lit[kWide ? G::kSB : 1];       // each warp's literal rows, in its half
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   for (int i = tid; i < G::kBmWords; i += kNT) s_bm[i] = 0u;
   if (tid < 3) s_cnt[tid] = 0u;
@@ -542,78 +573,161 @@ __global__ void __launch_bounds__(kResolveThreads) k_resolve(const In* __restric
   __syncthreads();
 
   uint32_t* hist = s_histwin + warp * kA;
-  const unsigned gshift = lane & ~(G::kLPR - 1);
-  const unsigned gmask = (G::kLPR == 32 ? 0xffffffffu : ((1u << G::kLPR) - 1u)) << gshift;
-  const bool leader = (lane % G::kLPR) == 0;
   uint32_t n_lit = 0, n_match = 0;
-  // the reference rows' codes of a group of steps (the next group's loads are in flight while
-  // this one is compared)
-  auto load_refs = [&](int g0, Quad (&wr)[kGroup][G::kSPR]) {
+  if constexpr (kWide) {
+    // ---- rows of at least 16 bytes: first the match test, 16 bytes of codes per lane (kLPV lanes
+    //      per row, kRPV rows per warp step), with the reference rows of kGV steps in flight ----
+    const int sub = lane % kLPV;   // the lane's 16 bytes of its row: sub + k * kLPV, k < kUPL
+    const unsigned gmask = (kLPV == 32 ? 0xffffffffu : ((1u << kLPV) - 1u)) << (lane & ~(kLPV - 1));
+    const bool leader = sub == 0;
+    const unsigned below = (1u << lane) - 1u;
+    uint16_t* lits = s_lit + warp * (G::kSB / kNW);   // this warp's literal rows (row of the segment)
+    int nlw = 0;                                      // ... and their number (the same in every lane)
+    auto load_refs = [&](int g0, uint4 (&rv)[kGV][kUPL]) {
 #pragma unroll
-    for (int it = 0; it < kGroup; ++it) {
-      const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
-      const int64_t b = row0 + rr;
-      const uint32_t ref = b < bend ? s_ref[rr] : (uint32_t)b;
+      for (int it = 0; it < kGV; ++it) {
+        const int rr = (warp * kStepsV + g0 + it) * kRPV + lane / kLPV;
+        const int64_t b = row0 + rr;
+        const uint32_t ref = b < bend ? s_ref[rr] : (uint32_t)b;
+        const uint4* rp = reinterpret_cast<const uint4*>(symt + (size_t)ref * (D * W)) + sub;
 #pragma unroll
-      for (int j = 0; j < G::kSPR; ++j) {
-        const int d = (lane % G::kLPR) * 4 + j * 128;
-        wr[it][j] = ref != (uint32_t)b ? ld_quad(symt, (size_t)ref * D + d, (Quad*)nullptr) : Quad{};
+        for (int k = 0; k < kUPL; ++k) rv[it][k] = ref != (uint32_t)b ? __ldcg(rp + k * kLPV) : make_uint4(0, 0, 0, 0);
       }
-    }
-  };
-  auto process = [&](int g0, const Quad (&wr)[kGroup][G::kSPR]) {
+    };
+    auto test = [&](int g0, const uint4 (&rv)[kGV][kUPL]) {
 #pragma unroll
-    for (int it = 0; it < kGroup; ++it) {
-      const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
-      const int64_t b = row0 + rr;
-      const bool valid = b < bend;
-      const uint32_t ref = valid ? s_ref[rr] : 0u;
-      const bool cand = valid && ref != (uint32_t)b;
-      Quad wb[G::kSPR];
-      bool eq = true;
+      for (int it = 0; it < kGV; ++it) {
+        const int rr = (warp * kStepsV + g0 + it) * kRPV + lane / kLPV;
+        const int64_t b = row0 + rr;
+        const bool valid = b < bend;
+        const uint32_t ref = valid ? s_ref[rr] : 0u;
+        const bool cand = valid && ref != (uint32_t)b;
+        bool eq = true;
 #pragma unroll
-      for (int j = 0; j < G::kSPR; ++j) {
-        wb[j] = sm_quad(s_sym, so + (rr * (D / 4) + (lane % G::kLPR) + j * 32) * W, (Quad*)nullptr);
-        bool e = quad_eq(wr[it][j], wb[j]);
-        if (cand && e && quad_has_zero(wb[j])) {
-          const int d = (lane % G::kLPR) * 4 + j * 128;
-          const In* xb = x + ((size_t)b * T + t) * D + d;
-          const In* xr = x + ((size_t)ref * T + t) * D + d;
-#pragma unroll
-          for (int q = 0; q < 4; ++q)
-            if (quad_code(wb[j], q) == 0u && raw32(xb[q]) != raw32(xr[q])) e = false;
+        for (int k = 0; k < kUPL; ++k) {
+          const uint4 ov = reinterpret_cast<const uint4*>(s_sym)[rr * (D * W / 16) + sub + k * kLPV];
+          bool e = v4_eq(ov, rv[it][k]);
+          if (cand && e && v4_has_zero<W>(ov)) {   // outliers: their raw bits must agree too
+            const int d0 = (sub + k * kLPV) * (16 / W);
+            const In* xb = x + ((size_t)b * T + t) * D + d0;
+            const In* xr = x + ((size_t)ref * T + t) * D + d0;
+            for (int c = 0; c < 16 / W; ++c)
+              if (v4_code<W>(ov, c) == 0u && raw32(xb[c]) != raw32(xr[c])) e = false;
+          }
+          eq = eq && e;
         }
-        eq = eq && e;
-      }
-      const unsigned bad = __ballot_sync(0xffffffffu, !eq);
-      const bool match = cand && (bad & gmask) == 0u;
-      if (valid && !match) {
-#pragma unroll
-        for (int j = 0; j < G::kSPR; ++j) {
-#pragma unroll
-          for (int q = 0; q < 4; ++q) atomicAdd(&hist[quad_code(wb[j], q)], 1u);
-        }
-      }
-      if (valid && leader) {
-        if (match) {
+        const unsigned bad = __ballot_sync(0xffffffffu, !eq);
+        const bool match = cand && (bad & gmask) == 0u;
+        if (valid && leader && match) {
           w.ref[(size_t)t * B + b] = ref;
           atomicOr(&s_bm[rr >> 5], 1u << (rr & 31));
           ++n_match;
-        } else {
-          ++n_lit;
+        }
+        const bool lit = valid && leader && !match;
+        const unsigned litm = __ballot_sync(0xffffffffu, lit);
+        if (lit) lits[nlw + __popc(litm & below)] = (uint16_t)rr;
+        nlw += __popc(litm);
+      }
+    };
+    uint4 rv0[kGV][kUPL], rv1[kGV][kUPL];
+    load_refs(0, rv0);
+#pragma unroll 1
+    for (int g0 = 0; g0 < kStepsV; g0 += 2 * kGV) {
+      if (g0 + kGV < kStepsV) load_refs(g0 + kGV, rv1);
+      test(g0, rv0);
+      if (g0 + kGV < kStepsV) {
+        if (g0 + 2 * kGV < kStepsV) load_refs(g0 + 2 * kGV, rv0);
+        test(g0 + kGV, rv1);
+      }
+    }
+    __syncwarp();
+    // ---- then the literal rows' codes into the warp's histogram, kLPR lanes per row, 4 codes each ----
+    for (int i0 = 0; i0 < nlw; i0 += G::kRPS) {
+      const int li = i0 + lane / G::kLPR;
+      if (li < nlw) {
+        const int rr = lits[li];
+#pragma unroll
+        for (int j = 0; j < G::kSPR; ++j) {
+          const Quad wb = sm_quad(s_sym, (rr * (D / 4) + (lane % G::kLPR) + j * 32) * W, (Quad*)nullptr);
+#pragma unroll
+          for (int q = 0; q < 4; ++q) atomicAdd(&hist[quad_code(wb, q)], 1u);
         }
       }
     }
-  };
-  Quad wr0[kGroup][G::kSPR], wr1[kGroup][G::kSPR];
-  load_refs(0, wr0);
+    n_lit = lane == 0 ? (uint32_t)nlw : 0u;
+  } else {
+    const unsigned gshift = lane & ~(G::kLPR - 1);
+    const unsigned gmask = (G::kLPR == 32 ? 0xffffffffu : ((1u << G::kLPR) - 1u)) << gshift;
+    const bool leader = (lane % G::kLPR) == 0;
+      // the reference rows' codes of a group of steps (the next group's loads are in flight while
+    // this one is compared)
+    auto load_refs = [&](int g0, Quad (&wr)[kGroup][G::kSPR]) {
+#pragma unroll
+      for (int it = 0; it < kGroup; ++it) {
+        const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
+        const int64_t b = row0 + rr;
+        const uint32_t ref = b < bend ? s_ref[rr] : (uint32_t)b;
+#pragma unroll
+        for (int j = 0; j < G::kSPR; ++j) {
+          const int d = (lane % G::kLPR) * 4 + j * 128;
+          wr[it][j] = ref != (uint32_t)b ? ld_quad(symt, (size_t)ref * D + d, (Quad*)nullptr) : Quad{};
+        }
+      }
+    };
+    auto process = [&](int g0, const Quad (&wr)[kGroup][G::kSPR]) {
+#pragma unroll
+      for (int it = 0; it < kGroup; ++it) {
+        const int rr = (warp * kSteps + g0 + it) * G::kRPS + lane / G::kLPR;
+        const int64_t b = row0 + rr;
+        const bool valid = b < bend;
+        const uint32_t ref = valid ? s_ref[rr] : 0u;
+        const bool cand = valid && ref != (uint32_t)b;
+        Quad wb[G::kSPR];
+        bool eq = true;
+#pragma unroll
+        for (int j = 0; j < G::kSPR; ++j) {
+          wb[j] = sm_quad(s_sym, so + (rr * (D / 4) + (lane % G::kLPR) + j * 32) * W, (Quad*)nullptr);
+          bool e = quad_eq(wr[it][j], wb[j]);
+          if (cand && e && quad_has_zero(wb[j])) {
+            const int d = (lane % G::kLPR) * 4 + j * 128;
+            const In* xb = x + ((size_t)b * T + t) * D + d;
+            const In* xr = x + ((size_t)ref * T + t) * D + d;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (quad_code(wb[j], q) == 0u && raw32(xb[q]) != raw32(xr[q])) e = false;
+          }
+          eq = eq && e;
+        }
+        const unsigned bad = __ballot_sync(0xffffffffu, !eq);
+        const bool match = cand && (bad & gmask) == 0u;
+        if (valid && !match) {
+#pragma unroll
+          for (int j = 0; j < G::kSPR; ++j) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) atomicAdd(&hist[quad_code(wb[j], q)], 1u);
+          }
+        }
+        if (valid && leader) {
+          if (match) {
+            w.ref[(size_t)t * B + b] = ref;
+            atomicOr(&s_bm[rr >> 5], 1u << (rr & 31));
+            ++n_match;
+          } else {
+            ++n_lit;
+          }
+        }
+      }
+    };
+    Quad wr0[kGroup][G::kSPR], wr1[kGroup][G::kSPR];
+    load_refs(0, wr0);
 #pragma unroll 1
-  for (int g0 = 0; g0 < kSteps; g0 += 2 * kGroup) {
-    if (g0 + kGroup < kSteps) load_refs(g0 + kGroup, wr1);
-    process(g0, wr0);
-    if (g0 + kGroup < kSteps) {
-      if (g0 + 2 * kGroup < kSteps) load_refs(g0 + 2 * kGroup, wr0);
-      process(g0 + kGroup, wr1);
+    for (int g0 = 0; g0 < kSteps; g0 += 2 * kGroup) {
+      if (g0 + kGroup < kSteps) load_refs(g0 + kGroup, wr1);
+      process(g0, wr0);
+      if (g0 + kGroup < kSteps) {
+        if (g0 + 2 * kGroup < kSteps) load_refs(g0 + 2 * kGroup, wr0);
+        process(g0 + kGroup, wr1);
+      }
     }
   }
   n_lit = __reduce_add_sync(0xffffffffu, n_lit);
