@@ -794,7 +794,7 @@ __device__ __forceinline__ unsigned long long pad16(unsigned long long n) { retu
 // table records (k_emit writes them otherwise), and sets the status.
 __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Work& w, ContLay c, uint8_t* out,
                                   unsigned long long cap, unsigned long long* out_bytes,
-                                  unsigned long long* chunk_off, uint32_t epoch) {
+                                  unsigned long long* chunk_off, uint32_t epoch, uint32_t cabort) {
   __shared__ unsigned long long s_size[kMaxSlices];
   __shared__ unsigned long long s_sum[5];   // literals, matches, outliers, chunks, words
   __shared__ unsigned long long s_total;
@@ -834,7 +834,7 @@ __device__ void finish_containers(const Shape& sh, const EbParams& ep, const Wor
   __syncthreads();
   const unsigned long long total = s_total;
   int status = total > cap ? EBC_ERR_CAPACITY : EBC_OK;
-  if (__ldcg(&g->cabort) == status_word(epoch, EBC_ERR_DEVICE_TIMEOUT)) status = EBC_ERR_DEVICE_TIMEOUT;
+  if (cabort == status_word(epoch, EBC_ERR_DEVICE_TIMEOUT)) status = EBC_ERR_DEVICE_TIMEOUT;
   if (tid < sh.R) {
     c.base = s_size[tid];
     w.cont[tid] = c;
@@ -1045,9 +1045,10 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   __shared__ unsigned long long s_bits64[8];
   __shared__ uint16_t s_order[kA];
   __shared__ Par s_leafpar[kA], s_nodepar[kA], s_depth[kA];
-  __shared__ uint8_t s_len[kA];
+  __shared__ __align__(16) uint8_t s_len[kA];
   __shared__ uint32_t s_count[kLmax + 2], s_next[kLmax + 2], s_run[kLmax + 2];
   __shared__ int s_maxlen, s_last;
+  __shared__ uint32_t s_wn[8];                // used symbols per warp
   __shared__ uint32_t s_wcnt[8][kLmax + 1];   // symbols of each length per warp
   __shared__ uint4 s_warp[8];
   __shared__ uint4 s_cpre[kMaxSlices + 1], s_wpre[kMaxSlices + 1];   // unit prefixes at container starts
@@ -1057,6 +1058,13 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   const int U = sh.U;
   Glob* g = w.glob;
 
+  if (u < U && sh.fold && sh.nseg > 0) {
+    // the segments' chunk and match counts (nseg <= 256), requested before the code is built
+    if (tid < sh.nseg) {
+      const uint4 cnt = __ldcg(&w.seg_cnt[u * sh.nseg + tid]);
+      s_seg[tid] = make_uint4(0u, cnt.w, cnt.y, 0u);
+    }
+  }
   if (u < U) {
     const int t = u % T;
     const bool raw = (table_mode(w, t) & kModeRawCodes) != 0;   // every code log2(A) bits: no Huffman
@@ -1066,19 +1074,33 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     } else {
     // (with no segments, k_quantize did not run and the accumulators are stale)
     const uint32_t f0 = sh.nseg > 0 ? __ldcg(&w.tab_hist[(size_t)u * 256 + tid]) : 0u;
+    const uint4 tc = tid == 0 && sh.nseg > 0 ? __ldcg(&w.tab_cnt[u]) : make_uint4(0, 0, 0, 0);
     s_f[tid] = f0;
     if (raw) s_len[tid] = 8;
     __syncthreads();
     for (int round = 0; round < 40 && !raw; ++round) {
       const uint32_t fi = s_f[tid];
-      // leaves in (count, symbol) order: a bitonic sort of the keys count << 8 | symbol over the
-      // 256 threads (absent symbols sort last); thread i ends with the key of rank i
-      const unsigned long long key = fi > 0u ? ((unsigned long long)fi << 8) | (unsigned)tid : ~0ull;
-      const unsigned long long sk = bitonic_sort256(key, s_key);
-      const int n = __syncthreads_count(fi > 0u);
+      // leaves in (count, symbol) order: the keys count << 8 | symbol of the used symbols are
+      // compacted, and each is placed at its rank among them (the keys are distinct)
+      const int lane = tid & 31, wp = tid >> 5;
+      const unsigned used = __ballot_sync(0xffffffffu, fi > 0u);
+      if (lane == 0) s_wn[wp] = __popc(used);
+      __syncthreads();
+      int n = 0, pos = __popc(used & ((1u << lane) - 1u));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        pos += k < wp ? (int)s_wn[k] : 0;
+        n += (int)s_wn[k];
+      }
+      if (fi > 0u) s_key[pos] = ((unsigned long long)fi << 8) | (unsigned)tid;
+      __syncthreads();
       if (tid < n) {
-        s_order[tid] = (uint16_t)(sk & 0xffu);
-        s_lw[tid] = (uint32_t)(sk >> 8);
+        const unsigned long long mk = s_key[tid];
+        int rank = 0;
+#pragma unroll 4
+        for (int j = 0; j < n; ++j) rank += s_key[j] < mk ? 1 : 0;
+        s_order[rank] = (uint16_t)(mk & 0xffu);
+        s_lw[rank] = (uint32_t)(mk >> 8);
       }
       s_len[tid] = 0;
       if (tid == 0) s_maxlen = 0;
@@ -1173,33 +1195,30 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
         unsigned long long tot = 0;
         for (int k = 0; k < 8; ++k) tot += s_bits64[k];
         w.tab_bits[u] = tot;
-        const uint4 tc = sh.nseg > 0 ? __ldcg(&w.tab_cnt[u]) : make_uint4(0, 0, 0, 0);
         w.tab_rec[u] = make_uint4(__float_as_uint(ep.eb[t]), tc.x, tc.y, tc.z);   // head of the table record
       }
     }
     }   // W == 1
     if (sh.fold && sh.nseg > 0) {
       // this unit's segments: bits = sum over codes of count * length (+32 raw bits per outlier),
-      // one warp per segment; then offsets relative to the unit (a scan) and the unit's totals
+      // one warp per segment, the histograms of all segments loaded in one round (lengths from
+      // shared memory); then offsets relative to the unit (a scan) and the unit's totals
       const int warp = tid >> 5, lane = tid & 31;
-      constexpr int kV = kA / 128;                  // uint4 of histogram and codes per lane
-      constexpr int kBatch = W == 1 ? 8 : 2;        // segments whose histograms are loaded together
-      const uint4* cp = reinterpret_cast<const uint4*>(w.tabcode + (size_t)u * kA) + lane * kV;
-      __syncthreads();   // tabcode of this unit is written
-      uint4 c[kV];
+      constexpr int kV = kA / 128;                  // uint4 of histogram (and words of 4 lengths) per lane
+      constexpr int kBatch = W == 1 ? 16 : 2;       // segments per warp whose histograms are loaded together
+      __syncthreads();   // the unit's code lengths are final
+      uint32_t c[kV];
 #pragma unroll
-      for (int v = 0; v < kV; ++v) c[v] = __ldcg(cp + v);
+      for (int v = 0; v < kV; ++v) c[v] = reinterpret_cast<const uint32_t*>(s_len)[lane * kV + v];
       for (int i0 = warp; i0 < sh.nseg; i0 += 8 * kBatch) {
-        uint4 h[kBatch][kV], cnt[kBatch];
+        uint4 h[kBatch][kV];
 #pragma unroll
         for (int q = 0; q < kBatch; ++q) {
           const int i = i0 + 8 * q;
           if (i < sh.nseg) {
-            const int seg = u * sh.nseg + i;
-            const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)seg * kA) + lane * kV;
+            const uint4* hp = reinterpret_cast<const uint4*>(w.seg_hist + (size_t)(u * sh.nseg + i) * kA) + lane * kV;
 #pragma unroll
             for (int v = 0; v < kV; ++v) h[q][v] = __ldcg(hp + v);
-            cnt[q] = lane == 0 ? __ldcg(&w.seg_cnt[seg]) : make_uint4(0, 0, 0, 0);
           }
         }
 #pragma unroll
@@ -1209,11 +1228,14 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
             uint32_t bits = 0;
 #pragma unroll
             for (int v = 0; v < kV; ++v)
-              bits += h[q][v].x * (c[v].x & 0xffu) + h[q][v].y * (c[v].y & 0xffu) + h[q][v].z * (c[v].z & 0xffu) +
-                      h[q][v].w * (c[v].w & 0xffu);
+              bits += h[q][v].x * (c[v] & 0xffu) + h[q][v].y * ((c[v] >> 8) & 0xffu) +
+                      h[q][v].z * ((c[v] >> 16) & 0xffu) + h[q][v].w * (c[v] >> 24);
             if (lane == 0) bits += 32u * h[q][0].x;   // symbol 0: the outliers' raw bits
             bits = __reduce_add_sync(0xffffffffu, bits);
-            if (lane == 0) s_seg[i] = make_uint4(((bits + 127u) >> 7) * 4u, cnt[q].w, cnt[q].y, bits);
+            if (lane == 0) {
+              s_seg[i].x = ((bits + 127u) >> 7) * 4u;
+              s_seg[i].w = bits;
+            }
           }
         }
       }
@@ -1235,6 +1257,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   __syncthreads();
   if (!s_last) return;
   __threadfence();
+  const uint32_t cab = __ldcg(&g->cabort);   // (read now: the status needs it at the end)
   // exclusive scans over the units of their counts (and, folded, of their bitstream sizes); the
   // values at each container's first unit, and the totals, are kept
   const bool have = sh.nseg > 0;
@@ -1244,12 +1267,12 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
   for (int base = 0; base < U; base += 256) {
     const int i = base + tid;
     const uint4 v = i < U && have ? __ldcg(&w.tab_cnt[i]) : make_uint4(0, 0, 0, 0);
+    const uint4 d = i < U && have && sh.fold ? __ldcg(&w.seg_desc[i]) : make_uint4(0, 0, 0, 0);
     uint4 tot;
     const uint4 ex = add4(carry, block_excl_scan4(v, &tot, s_warp));
     if (i < U && i % T == 0) s_cpre[i / T] = ex;
     carry = add4(carry, tot);
     if (sh.fold && have) {
-      const uint4 d = i < U ? __ldcg(&w.seg_desc[i]) : make_uint4(0, 0, 0, 0);
       const uint4 wex = add4(wcarry, block_excl_scan4(d, &tot, s_warp));
       if (i < U) w.tile_base[i] = wex;
       if (i < U && i % T == 0) s_wpre[i / T] = wex;
@@ -1275,7 +1298,7 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     c.match0 = wa.z;
   }
   if (sh.fold || !have) {
-    finish_containers(sh, ep, w, c, out, cap, out_bytes, chunk_off, epoch);
+    finish_containers(sh, ep, w, c, out, cap, out_bytes, chunk_off, epoch, cab);
   } else {
     if (tid < sh.R) w.cont[tid] = c;   // the counts; k_layout adds the bitstream sizes
     if (tid == 0) {
@@ -1404,7 +1427,7 @@ __global__ void __launch_bounds__(256) k_layout(Shape sh, EbParams ep, Work w, u
     c.chunk0 = at[0].y;
     c.match0 = at[0].z;
   }
-  finish_containers(sh, ep, w, c, out, cap, out_bytes, chunk_off, epoch);
+  finish_containers(sh, ep, w, c, out, cap, out_bytes, chunk_off, epoch, __ldcg(&w.glob->cabort));
 }
 
 // ---------------------------------------------------------------------------
