@@ -1201,11 +1201,12 @@ __global__ void __launch_bounds__(256) k_codebook(Shape sh, EbParams ep, Work w,
     }   // W == 1
     if (sh.fold && sh.nseg > 0) {
       // this unit's segments: bits = sum over codes of count * length (+32 raw bits per outlier),
-      // one warp per segment, the histograms of all segments loaded in one round (lengths from
-      // shared memory); then offsets relative to the unit (a scan) and the unit's totals
+      // one warp per segment, eight histograms in flight per warp (lengths from shared memory);
+      // then offsets relative to the unit (a scan) and the unit's totals
       const int warp = tid >> 5, lane = tid & 31;
       constexpr int kV = kA / 128;                  // uint4 of histogram (and words of 4 lengths) per lane
-      constexpr int kBatch = W == 1 ? 16 : 2;       // segments per warp whose histograms are loaded together
+      constexpr int kBatch = W == 1 ? 8 : 2;        // segments per warp whose histograms are loaded together
+                                                    // (more would keep two CTAs of 256 threads off an SM)
       __syncthreads();   // the unit's code lengths are final
       uint32_t c[kV];
 #pragma unroll
