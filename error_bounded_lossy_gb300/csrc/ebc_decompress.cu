@@ -6,7 +6,8 @@
 // ("parallel decompression" of chunks; one or several containers, one per
 // batch slice, decoded in the same pass).  The unit is a table of one
 // container.  Two launches, no pass over the container before them:
-//   k_dec_lit    one CTA per group of consecutive segments of one unit.  The
+//   k_dec_lit    CTAs per unit: one per group of consecutive segments (more when
+//                the unit is decoded in shares, see below).  The
 //                sections it reads first sit at offsets that follow from the
 //                shape, so the header, the unit's code lengths, the group's
 //                segment records and match bitmap are all loaded at once (the
@@ -23,6 +24,14 @@
 //                record (and resolves the reference chains of a windowed
 //                container); the last unit of a container checks the
 //                container's outlier count.
+//                When a chunk is one row and a unit has at most kDecShareMaxSeg
+//                segments, the unit gets as many CTAs as are resident at once
+//                divided among the units, and CTA k decodes the k-th of that many
+//                equal shares of the unit's chunks (its literal rows and chunk
+//                start bits from the segments the share spans), not its group's:
+//                the batch's first rows hold most first occurrences, so groups
+//                of segments hold very uneven numbers of chunks.  The group
+//                checks stay with the groups.
 //   k_dec_match  persistent warps take the batch's 32-row bitmap words in turn
 //                and copy each matched row from its reference row (the literal
 //                it names, or the literal root of its chain).
@@ -248,13 +257,18 @@ __device__ __forceinline__ uint32_t batch_chunks(uint32_t nchunks, int warps) {
   return share < 1u ? 1u : (share > 32u ? 32u : share);
 }
 
+// Units of at most this many segments (of one-row chunks) are decoded in equal
+// shares of their chunks.
+constexpr int kDecShareMaxSeg = 512;
+
 // ---------------------------------------------------------------------------
-// k_dec_lit: grid U * G (G groups of kSPC segments per unit), 128 threads.
+// k_dec_lit: grid U * nshare (nshare >= the groups of kSPC segments per unit),
+// 128 threads.
 // ---------------------------------------------------------------------------
 template <int D, int W>
 __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ in, unsigned long long in_bytes,
                                                     const unsigned long long* __restrict__ offs, Shape sh, Work w,
-                                                    float* __restrict__ xhat, uint32_t epoch) {
+                                                    float* __restrict__ xhat, uint32_t epoch, int nshare) {
   pdl_enter();
   using G = DGeo<D>;
   constexpr int kA = Alph<W>::kA, kNT = G::kThreads;
@@ -280,10 +294,20 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   __shared__ uint32_t s_len[kA / 4];                  // the unit's code lengths (a byte each)
   __shared__ int s_tbad;                              // the code lengths or the bound are unusable
   __shared__ uint32_t s_count[kLmax + 1], s_wcnt[(kNT / 32) * (kLmax + 1)], s_run[kLmax + 1];
+  // decode shares (a chunk is one row, at most kMaxSegU segments per unit): the unit's segment chunk
+  // bases and its end, the share's chunk lengths from its first segment's first chunk, and
+  // {c0, c1, first segment, last segment, first segment's word, unusable}
+  constexpr bool kShareD = G::kKC == 1;
+  constexpr int kMaxSegU = kDecShareMaxSeg;
+  __shared__ uint32_t s_ucb[kShareD ? kMaxSegU + 1 : 1];
+  __shared__ uint16_t s_sclen[kShareD ? G::kMaxChunks + G::kSegChunks : 1];
+  __shared__ uint32_t s_sh[6];
   Glob* g = w.glob;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int T = sh.T;
-  const int ngrp = div_up(sh.nseg, G::kSPC) > 0 ? div_up(sh.nseg, G::kSPC) : 1;
+  // nshare CTAs per unit (at least one per group of kSPC segments; more when the unit's chunks are
+  // decoded in shares, CTAs past the groups then only decode)
+  const int ngrp = nshare;
   // CTAs go unit-fastest, so the CTAs running at a time write whole rows of the output
   const int nu = sh.U > 0 ? sh.U : 1;
   const int grp = (int)blockIdx.x / nu;
@@ -306,6 +330,14 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   const int nsg = have_unit ? max(0, min(G::kSPC, (int)nseg_r - s0)) : 0;   // its segments in this slice
   const unsigned long long rec0 = (unsigned long long)t * nseg_r + s0;       // record of its first segment
   const bool rec_end = rec0 + nsg == (unsigned long long)T * nseg_r;         // its last is the container's last
+  const bool use_share = kShareD && have_unit && nseg_r <= (unsigned)kMaxSegU;
+  if (use_share) {   // the unit's segment chunk bases (record word 1), and the next table's first
+    const unsigned int nb = nseg_r + (t + 1 < T ? 1u : 0u);
+    for (unsigned int i = tid; i < nb; i += kNT) {
+      const unsigned long long o = off_seg + ((unsigned long long)t * nseg_r + i) * kSegRecBytes + 4ull;
+      s_ucb[i] = o + 4 <= size ? ld32(cin + o) : 0u;
+    }
+  }
   if (have_unit) {
     const uint8_t* rec = cin + kHeaderBytes + (size_t)t * Alph<W>::kRecBytes;
     const bool rec_in = kHeaderBytes + (unsigned long long)(t + 1) * Alph<W>::kRecBytes <= size;
@@ -337,6 +369,7 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     Layout L{};
     const int code = have_unit ? (container_layout(in, in_bytes, offs, sh, r, &L) == EBC_OK ? EBC_OK : -1) : EBC_OK;
     if (have_unit && t == 0 && grp == 0 && code == EBC_OK) w.lay[r] = L;   // for the match copy
+    if (use_share && t + 1 == T) s_ucb[nseg_r] = code == EBC_OK && L.n_chunks < 0xFFFFFFFFull ? (uint32_t)L.n_chunks : 0u;
     s_L = L;
     s_code = code;
     s_cnt[0] = s_cnt[1] = s_cnt[2] = 0u;
@@ -523,6 +556,115 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     nchunks = ok ? s_grp[0] : 0u;
   }
 
+  // ---- decode share: with a chunk per row and a unit of at most kMaxSegU segments, this CTA decodes
+  //      the grp-th of ngrp equal shares of its unit's chunks instead of its group's (the batch's first
+  //      rows hold most first occurrences, so the groups' chunks are uneven); a warp per segment of the
+  //      share: its literal rows by rank and the chunk start bits ----
+  const bool share = ok && use_share;
+  if (share) {
+    if (tid == 0) {
+      const uint32_t u0 = s_ucb[0], u1 = s_ucb[nseg_r];
+      uint32_t c0 = u0, c1 = u0, unusable = u1 < u0 || u1 > L.n_chunks;
+      if (!unusable) {
+        const unsigned long long n_u = u1 - u0;
+        c0 = u0 + (uint32_t)(n_u * (unsigned)grp / (unsigned)ngrp);
+        c1 = u0 + (uint32_t)(n_u * (unsigned)(grp + 1) / (unsigned)ngrp);
+        unusable = c1 - c0 > (uint32_t)G::kMaxChunks;
+      }
+      s_sh[0] = c0;
+      s_sh[1] = c1;
+      s_sh[2] = s_sh[3] = 0xFFFFFFFFu;
+      s_sh[4] = 0u;
+      s_sh[5] = unusable;
+    }
+    __syncthreads();
+    const uint32_t c0 = s_sh[0], c1 = s_sh[1];
+    if (c1 > c0 && !s_sh[5]) {   // the segments holding chunks c0 and c1 - 1
+      for (unsigned int sg = tid; sg < nseg_r; sg += kNT) {
+        const uint32_t a = s_ucb[sg], e = s_ucb[sg + 1];
+        if (a <= c0 && c0 < e) s_sh[2] = sg;
+        if (a <= c1 - 1u && c1 - 1u < e) s_sh[3] = sg;
+      }
+    }
+    __syncthreads();
+    const uint32_t sa = s_sh[2], sb = s_sh[3];
+    // (an inconsistent share exists only in a corrupt container, whose group checks fail elsewhere)
+    bool sbad = c1 > c0 && (s_sh[5] != 0u || sa >= nseg_r || sb >= nseg_r || sb < sa);
+    const uint32_t cbS = c1 > c0 && !sbad ? s_ucb[sa] : c0;   // the first chunk of the first segment
+    if (c1 - cbS > (uint32_t)(G::kMaxChunks + G::kSegChunks)) sbad = true;
+    if (c1 > c0 && !sbad) {   // the chunk lengths from cbS to c1, and the first segment's first word
+      const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + L.off_chunks);
+      for (uint32_t i = tid; i < c1 - cbS; i += kNT) s_sclen[i] = cl[cbS + i];
+      if (tid == 0) s_sh[4] = ld32(cin + off_seg + ((unsigned long long)t * nseg_r + sa) * kSegRecBytes);
+    }
+    __syncthreads();
+    const uint32_t wbS = s_sh[4];
+    if (c1 > c0 && !sbad && ((wbS & 3u) || wbS > L.words)) sbad = true;
+    if (c1 > c0 && !sbad) {
+      const uint32_t below = (1u << lane) - 1u;
+      for (uint32_t sg = sa + (uint32_t)warp; sg <= sb; sg += (uint32_t)G::kWarps) {
+        const uint32_t a = s_ucb[sg], e = s_ucb[sg + 1];
+        if (e <= a) continue;   // no literal rows
+        const uint32_t word_off =
+            __shfl_sync(0xffffffffu, lane == 0 ? ld32(cin + off_seg + ((unsigned long long)t * nseg_r + sg) * kSegRecBytes) : 0u, 0);
+        const int64_t row0 = (int64_t)sg * G::kSB;   // within the slice
+        // literal rows in row order: rank j is chunk a + j (its row into s_cinfo when in the share)
+        uint32_t nlit = 0;
+#pragma unroll
+        for (int half = 0; half < (G::kBmWords + 31) / 32; ++half) {
+          const int wi = half * 32 + lane;
+          uint32_t litw = 0;
+          if (wi < G::kBmWords) {
+            const int64_t nv = nr - (row0 + (int64_t)wi * 32);
+            const uint32_t valid = nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
+            const unsigned long long bwi = (unsigned long long)sg * G::kBmWords + wi;
+            const unsigned long long o = off_bm + 4ull * ((unsigned long long)t * nw_r + bwi);
+            const uint32_t bm = nv > 0 && bwi < nw_r && o + 4 <= size ? ld32(cin + o) : 0u;
+            litw = ~bm & valid;
+          }
+          uint32_t tot;
+          const uint32_t k = nlit + warp_excl(__popc(litw), &tot);
+          const uint32_t wbase = (uint32_t)(half * 32);
+          for (int wl = 0; wl < 32; ++wl) {
+            const uint32_t lw = __shfl_sync(0xffffffffu, litw, wl), kb = __shfl_sync(0xffffffffu, k, wl);
+            if ((lw >> lane) & 1u) {
+              const uint32_t c = a + kb + __popc(lw & below);
+              if (c >= c0 && c < c1) s_cinfo[c - c0] = (uint32_t)(row0 + (int64_t)((wbase + wl) * 32 + lane));
+            }
+            if (wbase + wl + 1 >= (uint32_t)G::kBmWords) break;
+          }
+          nlit += tot;
+        }
+        if (nlit != e - a) sbad = true;
+        // chunk start bits: the segment's first bit (relative to the share's first segment) + the lengths
+        // of its chunks before
+        uint32_t acc = 0;
+#pragma unroll
+        for (int half = 0; half < (G::kSegChunks + 31) / 32; ++half) {
+          const uint32_t j = (uint32_t)(half * 32 + lane);
+          const uint32_t c = a + j;
+          const uint32_t len = j < e - a && c < c1 ? (uint32_t)s_sclen[c - cbS] : 0u;
+          uint32_t tot;
+          const uint32_t st = acc + warp_excl(len, &tot);
+          if (j < e - a && c >= c0 && c < c1) {
+            s_cbit[c - c0] = (word_off - wbS) * 32u + st;
+            s_clen[c - c0] = (uint16_t)len;
+          }
+          acc += tot;
+        }
+      }
+    }
+    if (sbad) s_code = EBC_ERR_CORRUPT;   // (benign race: any writer stores the same value)
+    if (tid == 0) {
+      s_grp[2] = wbS;
+      s_grp[3] = wbS <= L.words ? (uint32_t)(L.words - wbS) : 0u;
+      s_next = (uint32_t)G::kWarps * batch_chunks(c1 - c0, G::kWarps);
+    }
+    __syncthreads();
+    ok = s_code == EBC_OK;
+    nchunks = ok ? c1 - c0 : 0u;
+  }
+
   // ---- decode: a warp takes 32 chunks at a time, a piece per lane into its slot, then stores them ----
   // Four symbols at a time on a branch-free path that assumes ordinary codes (first-level table,
   // symbol field not 0); when one of the four was an outlier or a longer code, the four are decoded
@@ -570,7 +712,8 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
         const uint32_t start = mine ? s_cbit[c] : s_cbit[b0];
         const uint32_t clen = mine ? (uint32_t)s_clen[c] : 0u;
         const int j = (int)(info >> 24);
-        const uint32_t rows = (info >> 16) & 0xffu, first = info & 0xffffu;
+        // (a share's chunk is one row, which s_cinfo holds; a group's chunk: segment, rows, first rank)
+        const uint32_t rows = share ? (mine ? 1u : 0u) : (info >> 16) & 0xffu, first = info & 0xffffu;
         const uint32_t npieces = rows * G::kPiecesPerRow;
         // bit buffer: the next nb bits, left-aligned in buf; wp is the next word to read (reads past the
         // group's words repeat its last word; they never decide a code of a valid chunk)
@@ -589,7 +732,8 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
           if (act) {
             const uint32_t rk = p / G::kPiecesPerRow, pc = p % G::kPiecesPerRow;
             if (pc == 0) {
-              const int64_t b = brow0 + (int64_t)(s0 + j) * G::kSB + s_litrow[j * G::kSB + first + rk];
+              const int64_t b = share ? brow0 + (int64_t)info
+                                      : brow0 + (int64_t)(s0 + j) * G::kSB + s_litrow[j * G::kSB + first + rk];
               rowdst = xhat + ((size_t)b * sh.T_out + sh.t_off + t) * D;
             }
 #pragma unroll 1
@@ -912,9 +1056,20 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
                                 Prof* prof) {
   using G = DGeo<D>;
   const unsigned ngrp = (unsigned)(div_up(sh.nseg, G::kSPC) > 0 ? div_up(sh.nseg, G::kSPC) : 1);
-  const unsigned grid = sh.U > 0 ? (unsigned)sh.U * ngrp : 1u;
+  unsigned nshare = ngrp;
+  if (G::kKC == 1 && sh.nseg <= kDecShareMaxSeg && sh.U > 0) {
+    // decode shares: as many CTAs per unit as are resident at once (at least one per group)
+    static int per_sm = -1;
+    if (per_sm < 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dec_lit<D, W>, G::kThreads, 0) !=
+                           cudaSuccess ||
+                       per_sm < 1))
+      per_sm = 1;
+    const unsigned fit = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm) / (unsigned)sh.U;
+    if (fit > nshare) nshare = fit;
+  }
+  const unsigned grid = sh.U > 0 ? (unsigned)sh.U * nshare : 1u;
   prof_begin(prof, "k_dec_lit", st);
-  launch_k(k_dec_lit<D, W>, grid, G::kThreads, 0, st, in, in_bytes, offs, sh, w, xhat, epoch);
+  launch_k(k_dec_lit<D, W>, grid, G::kThreads, 0, st, in, in_bytes, offs, sh, w, xhat, epoch, (int)nshare);
   prof_end(prof, st);
   if (sh.U > 0 && sh.nseg > 0) {
     // persistent: the resident CTAs, at most one warp per bitmap word
