@@ -397,6 +397,72 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
 
   // whether the tables are built: read once here (s_code changes only after the barriers below)
   const bool build = s_code == EBC_OK && have_unit;
+
+  // ---- decode share (with a chunk per row and a unit of at most kMaxSegU segments): this CTA decodes
+  //      the grp-th of ngrp equal shares of its unit's chunks instead of its group's chunks (the batch's
+  //      first rows hold most first occurrences, so groups hold very uneven numbers of chunks).  Its
+  //      range and first segments are found now and their loads issued into registers, so that they
+  //      are in flight while the tables are built and the group is checked ----
+  const bool share = build && use_share;   // (uniform: s_code was read after the barrier)
+  constexpr int kLenPer = (G::kMaxChunks + G::kSegChunks + kNT - 1) / kNT;   // chunk lengths per thread
+  uint32_t c0 = 0, c1 = 0, sa = 0, sb = 0, cbS = 0;
+  bool sbad = false;
+  uint32_t pre_len[kLenPer], pre_wbS = 0, pre_word = 0, pre_bm = 0;
+  if (share) {
+    if (tid == 0) {
+      const uint32_t u0 = s_ucb[0], u1 = s_ucb[nseg_r];
+      uint32_t a0 = u0, a1 = u0, unusable = u1 < u0 || u1 > L.n_chunks;
+      if (!unusable) {
+        const unsigned long long n_u = u1 - u0;
+        a0 = u0 + (uint32_t)(n_u * (unsigned)grp / (unsigned)ngrp);
+        a1 = u0 + (uint32_t)(n_u * (unsigned)(grp + 1) / (unsigned)ngrp);
+        unusable = a1 - a0 > (uint32_t)G::kMaxChunks;
+      }
+      s_sh[0] = a0;
+      s_sh[1] = a1;
+      s_sh[2] = s_sh[3] = 0xFFFFFFFFu;
+      s_sh[5] = unusable;
+    }
+    __syncthreads();
+    c0 = s_sh[0];
+    c1 = s_sh[1];
+    if (c1 > c0 && !s_sh[5]) {   // the segments holding chunks c0 and c1 - 1
+      for (unsigned int sg = tid; sg < nseg_r; sg += kNT) {
+        const uint32_t a = s_ucb[sg], e = s_ucb[sg + 1];
+        if (a <= c0 && c0 < e) s_sh[2] = sg;
+        if (a <= c1 - 1u && c1 - 1u < e) s_sh[3] = sg;
+      }
+    }
+    __syncthreads();
+    sa = s_sh[2];
+    sb = s_sh[3];
+    // (an inconsistent share exists only in a corrupt container, whose group checks fail elsewhere)
+    sbad = c1 > c0 && (s_sh[5] != 0u || sa >= nseg_r || sb >= nseg_r || sb < sa);
+    cbS = c1 > c0 && !sbad ? s_ucb[sa] : c0;   // the first chunk of the first segment
+    if (c1 - cbS > (uint32_t)(G::kMaxChunks + G::kSegChunks)) sbad = true;
+    if (c1 > c0 && !sbad) {
+      // the chunk lengths from cbS to c1, the first segment's first word, and each warp's first
+      // segment's first word and bitmap words
+      const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + L.off_chunks);
+#pragma unroll
+      for (int k = 0; k < kLenPer; ++k) {
+        const uint32_t i = (uint32_t)(k * kNT + tid);
+        pre_len[k] = i < c1 - cbS ? (uint32_t)cl[cbS + i] : 0u;
+      }
+      if (tid == 0) pre_wbS = ld32(cin + off_seg + ((unsigned long long)t * nseg_r + sa) * kSegRecBytes);
+      const uint32_t sg = sa + (uint32_t)warp;
+      if (sg <= sb) {
+        if (lane == 0) pre_word = ld32(cin + off_seg + ((unsigned long long)t * nseg_r + sg) * kSegRecBytes);
+        const int64_t nv = nr - ((int64_t)sg * G::kSB + (int64_t)lane * 32);
+        const unsigned long long bwi = (unsigned long long)sg * G::kBmWords + lane;
+        const unsigned long long o = off_bm + 4ull * ((unsigned long long)t * nw_r + bwi);
+        if (lane < G::kBmWords && nv > 0 && bwi < nw_r && o + 4 <= size) pre_bm = ld32(cin + o);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < kLenPer; ++k) pre_len[k] = 0u;
+    }
+  }
   // ---- second round: the chunk lengths (in flight while the tables are built) ----
   if (build) {
     const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + L.off_chunks) + s_grp[1];
@@ -556,47 +622,15 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
     nchunks = ok ? s_grp[0] : 0u;
   }
 
-  // ---- decode share: with a chunk per row and a unit of at most kMaxSegU segments, this CTA decodes
-  //      the grp-th of ngrp equal shares of its unit's chunks instead of its group's (the batch's first
-  //      rows hold most first occurrences, so the groups' chunks are uneven); a warp per segment of the
-  //      share: its literal rows by rank and the chunk start bits ----
-  const bool share = ok && use_share;
-  if (share) {
-    if (tid == 0) {
-      const uint32_t u0 = s_ucb[0], u1 = s_ucb[nseg_r];
-      uint32_t c0 = u0, c1 = u0, unusable = u1 < u0 || u1 > L.n_chunks;
-      if (!unusable) {
-        const unsigned long long n_u = u1 - u0;
-        c0 = u0 + (uint32_t)(n_u * (unsigned)grp / (unsigned)ngrp);
-        c1 = u0 + (uint32_t)(n_u * (unsigned)(grp + 1) / (unsigned)ngrp);
-        unusable = c1 - c0 > (uint32_t)G::kMaxChunks;
-      }
-      s_sh[0] = c0;
-      s_sh[1] = c1;
-      s_sh[2] = s_sh[3] = 0xFFFFFFFFu;
-      s_sh[4] = 0u;
-      s_sh[5] = unusable;
+  // ---- decode share, its metadata: a warp per segment of the share, its literal rows by rank and the
+  //      chunk start bits ----
+  if (share && ok) {
+#pragma unroll
+    for (int k = 0; k < kLenPer; ++k) {
+      const uint32_t i = (uint32_t)(k * kNT + tid);
+      if (i < (uint32_t)(G::kMaxChunks + G::kSegChunks)) s_sclen[i] = (uint16_t)pre_len[k];
     }
-    __syncthreads();
-    const uint32_t c0 = s_sh[0], c1 = s_sh[1];
-    if (c1 > c0 && !s_sh[5]) {   // the segments holding chunks c0 and c1 - 1
-      for (unsigned int sg = tid; sg < nseg_r; sg += kNT) {
-        const uint32_t a = s_ucb[sg], e = s_ucb[sg + 1];
-        if (a <= c0 && c0 < e) s_sh[2] = sg;
-        if (a <= c1 - 1u && c1 - 1u < e) s_sh[3] = sg;
-      }
-    }
-    __syncthreads();
-    const uint32_t sa = s_sh[2], sb = s_sh[3];
-    // (an inconsistent share exists only in a corrupt container, whose group checks fail elsewhere)
-    bool sbad = c1 > c0 && (s_sh[5] != 0u || sa >= nseg_r || sb >= nseg_r || sb < sa);
-    const uint32_t cbS = c1 > c0 && !sbad ? s_ucb[sa] : c0;   // the first chunk of the first segment
-    if (c1 - cbS > (uint32_t)(G::kMaxChunks + G::kSegChunks)) sbad = true;
-    if (c1 > c0 && !sbad) {   // the chunk lengths from cbS to c1, and the first segment's first word
-      const uint16_t* cl = reinterpret_cast<const uint16_t*>(cin + L.off_chunks);
-      for (uint32_t i = tid; i < c1 - cbS; i += kNT) s_sclen[i] = cl[cbS + i];
-      if (tid == 0) s_sh[4] = ld32(cin + off_seg + ((unsigned long long)t * nseg_r + sa) * kSegRecBytes);
-    }
+    if (tid == 0) s_sh[4] = pre_wbS;
     __syncthreads();
     const uint32_t wbS = s_sh[4];
     if (c1 > c0 && !sbad && ((wbS & 3u) || wbS > L.words)) sbad = true;
@@ -605,8 +639,12 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
       for (uint32_t sg = sa + (uint32_t)warp; sg <= sb; sg += (uint32_t)G::kWarps) {
         const uint32_t a = s_ucb[sg], e = s_ucb[sg + 1];
         if (e <= a) continue;   // no literal rows
-        const uint32_t word_off =
-            __shfl_sync(0xffffffffu, lane == 0 ? ld32(cin + off_seg + ((unsigned long long)t * nseg_r + sg) * kSegRecBytes) : 0u, 0);
+        const bool first_seg = sg == sa + (uint32_t)warp;   // its word and bitmap words were loaded early
+        const uint32_t word_off = __shfl_sync(
+            0xffffffffu,
+            first_seg ? pre_word
+                      : (lane == 0 ? ld32(cin + off_seg + ((unsigned long long)t * nseg_r + sg) * kSegRecBytes) : 0u),
+            0);
         const int64_t row0 = (int64_t)sg * G::kSB;   // within the slice
         // literal rows in row order: rank j is chunk a + j (its row into s_cinfo when in the share)
         uint32_t nlit = 0;
@@ -619,7 +657,8 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
             const uint32_t valid = nv >= 32 ? 0xffffffffu : (nv <= 0 ? 0u : ((1u << nv) - 1u));
             const unsigned long long bwi = (unsigned long long)sg * G::kBmWords + wi;
             const unsigned long long o = off_bm + 4ull * ((unsigned long long)t * nw_r + bwi);
-            const uint32_t bm = nv > 0 && bwi < nw_r && o + 4 <= size ? ld32(cin + o) : 0u;
+            const uint32_t bm =
+                first_seg && half == 0 ? pre_bm : (nv > 0 && bwi < nw_r && o + 4 <= size ? ld32(cin + o) : 0u);
             litw = ~bm & valid;
           }
           uint32_t tot;
