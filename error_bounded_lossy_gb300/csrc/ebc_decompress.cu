@@ -24,9 +24,10 @@
 //                record (and resolves the reference chains of a windowed
 //                container); the last unit of a container checks the
 //                container's outlier count.
-//                When a chunk is one row and a unit has at most kDecShareMaxSeg
-//                segments, the unit gets as many CTAs as are resident at once
-//                divided among the units, and CTA k decodes the k-th of that many
+//                When a chunk is one row, a unit has at most kDecShareMaxSeg
+//                segments and more CTAs are resident at once than there are
+//                groups, each unit gets the resident CTAs divided among the
+//                units, and CTA k decodes the k-th of that many
 //                equal shares of the unit's chunks (its literal rows and chunk
 //                start bits from the segments the share spans), not its group's:
 //                the batch's first rows hold most first occurrences, so groups
@@ -330,7 +331,8 @@ __global__ void __launch_bounds__(128, 5) k_dec_lit(const uint8_t* __restrict__ 
   const int nsg = have_unit ? max(0, min(G::kSPC, (int)nseg_r - s0)) : 0;   // its segments in this slice
   const unsigned long long rec0 = (unsigned long long)t * nseg_r + s0;       // record of its first segment
   const bool rec_end = rec0 + nsg == (unsigned long long)T * nseg_r;         // its last is the container's last
-  const bool use_share = kShareD && have_unit && nseg_r <= (unsigned)kMaxSegU;
+  // (shares only when they add CTAs: with as many CTAs as groups, the groups' own chunks decode sooner)
+  const bool use_share = kShareD && have_unit && nseg_r <= (unsigned)kMaxSegU && ngrp > div_up(sh.nseg, G::kSPC);
   if (use_share) {   // the unit's segment chunk bases (record word 1), and the next table's first
     const unsigned int nb = nseg_r + (t + 1 < T ? 1u : 0u);
     for (unsigned int i = tid; i < nb; i += kNT) {
@@ -1096,7 +1098,7 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
   using G = DGeo<D>;
   const unsigned ngrp = (unsigned)(div_up(sh.nseg, G::kSPC) > 0 ? div_up(sh.nseg, G::kSPC) : 1);
   unsigned nshare = ngrp;
-  if (G::kKC == 1 && sh.nseg <= kDecShareMaxSeg && sh.U > 0) {
+  if (G::kKC == 1 && sh.nseg > 0 && sh.nseg <= kDecShareMaxSeg && sh.U > 0) {
     // decode shares: as many CTAs per unit as are resident at once (at least one per group)
     static int per_sm = -1;
     if (per_sm < 0 && (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_dec_lit<D, W>, G::kThreads, 0) !=
@@ -1104,7 +1106,7 @@ static void launch_decompress_d(const uint8_t* in, unsigned long long in_bytes, 
                        per_sm < 1))
       per_sm = 1;
     const unsigned fit = (unsigned)((sh.nsm > 0 ? sh.nsm : 152) * per_sm) / (unsigned)sh.U;
-    if (fit > nshare) nshare = fit;
+    if (fit > nshare) nshare = fit;   // (else the groups decode their own chunks)
   }
   const unsigned grid = sh.U > 0 ? (unsigned)sh.U * nshare : 1u;
   prof_begin(prof, "k_dec_lit", st);
