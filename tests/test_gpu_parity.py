@@ -271,14 +271,14 @@ def _decode_rc(codec, buf, shape):
     return codec.last_error(), xh
 
 
-def _corruption_cases(ref, rng, n_random):
+def _corruption_cases(ref, rng, n_random, tables=2):
     """Single-bit flips: a few in every section of the container, then random ones."""
     h = lambda o: int(np.frombuffer(ref[o:o + 8].tobytes(), np.uint64)[0])
     off_seg, off_bitmap, off_chunks, off_refs, off_bits = h(88), h(96), h(104), h(112), h(120)
     sections = [(0, 144), (144, off_seg), (off_seg, off_bitmap), (off_bitmap, off_chunks),
                 (off_chunks, off_refs), (off_refs, off_bits), (off_bits, len(ref))]
     # the counts of each table record (literals, matches, outliers) and the header's counts
-    fields = [64, 48, 56, 72, 80] + [144 + k * 272 + f for k in range(2) for f in (4, 8, 12)]
+    fields = [64, 48, 56, 72, 80] + [144 + k * 272 + f for k in range(tables) for f in (4, 8, 12)]
     cases = [(i, b) for i in fields for b in (0, 1, 5)]
     for lo, hi in sections:
         if hi > lo:
@@ -317,6 +317,46 @@ def test_corrupt_containers(codec, window):
                 assert np.array_equal(xg.cpu().numpy().view(np.uint32), xo.view(np.uint32)), (i, bit)
         assert n_both_ok > 0
         # still usable
+        rc, xg = _decode_rc(codec, ref, shape)
+        assert rc == 0
+        assert np.array_equal(xg.cpu().numpy().view(np.uint32), oracle.decompress(ref, *shape)[0].view(np.uint32))
+    finally:
+        codec.set_window(0)
+
+
+@pytest.mark.parametrize("window", [0, 16])
+def test_corrupt_containers_shares(codec, window):
+    """As test_corrupt_containers, with rows of 128 codes (a chunk per row), where every decode CTA
+    takes an equal share of its table's chunks (far more CTAs than segment groups): the GPU rejects
+    exactly what the oracle rejects, with the same code, and agrees bit for bit when both accept.
+    Flips in the segment records and chunk table reach the shares' range search and start bits."""
+    wl = workloads.make("fwd", batch=512, tables=3)
+    x, eb = wl.x.numpy().copy(), wl.eb.numpy()
+    x[3, 1, 5] = np.float32(1e3)           # outliers
+    x[200, 0, 0] = np.float32(-1e3)
+    ref, info = oracle.compress(x, eb, window=window)
+    assert info["n_outlier"] >= 2 and info["n_match"] > 0 and info["n_literal"] > 0
+    shape = x.shape
+    codec.set_window(window)
+    try:
+        assert _decode_rc(codec, ref, shape)[0] == 0
+        h = lambda o: int(np.frombuffer(ref[o:o + 8].tobytes(), np.uint64)[0])
+        rng = np.random.default_rng(100 + window)
+        cases = _corruption_cases(ref, rng, 60, tables=3)
+        # more flips in the segment records (chunk bases, word offsets) and the chunk table
+        cases += [(int(rng.integers(h(88), h(96))), int(rng.integers(0, 8))) for _ in range(40)]
+        cases += [(int(rng.integers(h(104), h(112))), int(rng.integers(0, 8))) for _ in range(20)]
+        n_both_ok = 0
+        for i, bit in cases:
+            bad = ref.copy()
+            bad[i] ^= np.uint8(1 << bit)
+            rc_o, xo, _ = oracle.decompress_rc(bad, *shape)
+            rc_g, xg = _decode_rc(codec, bad, shape)
+            assert rc_g == rc_o, (i, bit, rc_g, rc_o)
+            if rc_o == oracle.OK:
+                n_both_ok += 1
+                assert np.array_equal(xg.cpu().numpy().view(np.uint32), xo.view(np.uint32)), (i, bit)
+        assert n_both_ok > 0
         rc, xg = _decode_rc(codec, ref, shape)
         assert rc == 0
         assert np.array_equal(xg.cpu().numpy().view(np.uint32), oracle.decompress(ref, *shape)[0].view(np.uint32))
